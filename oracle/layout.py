@@ -1,0 +1,111 @@
+"""The kernel-side ("repacked") weight layout, written from its specification.
+
+The Humming preprocessing step "checks parameters, pads dimensions and repacks
+tensors for the target kernel" (kinachrichten.com, "Wie die Architektur
+funktioniert"); the retrivium.ai retrospective ("Representation answers a
+different question") adds that repacking may rearrange tensors for a device
+without changing what the stored values mean.  The pages leave the target
+layout to the implementation.  This module restates the layout that the CUDA
+repack must produce, from the specification alone, so that the repack can be
+checked bit for bit.
+
+W4A16 tiled layout (N and K multiples of 128; KT = K / 128 k-tiles):
+
+  weights: one 8192-byte block per (n-tile nt, k-tile kt), blocks ordered
+    nt-major: block index nt * KT + kt.  A block is 512 little-endian 16-byte
+    vectors; vector v = (qd * 4 + j) * 32 + t holds row n = 128 nt + 32 qd + t
+    and the 32 values k = 128 kt + 32 j + [0, 32).  Its 32-bit word w
+    (w = 0..3) holds k-offsets 8w + [0, 8) within the vector, nibble position
+    p (bits [4p, 4p+4)) holding k-offset 8w + PERM[p] with
+    PERM = [0, 2, 4, 6, 1, 3, 5, 7], so that nibbles p and p + 4 are the two
+    consecutive k-offsets 8w + 2p and 8w + 2p + 1.
+    Nibble value: offset binary q + 8 for signed INT4, the raw code for UINT4.
+
+  scales: one block of 128 * ST 16-bit words per (nt, kt), same block order,
+    with ST = max(1, 128 / g) groups touched by a k-tile; word sg * 128 + r is
+    the scale of row n = 128 nt + r for the group holding
+    k = 128 kt + sg * min(g, 128).
+
+  zeros (UINT4 only): one block of 128 * ST bytes per (nt, kt), byte
+    sg * 128 + r is the zero point (0..15) of the same (group, row).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+TILE_N = 128
+TILE_K = 128
+PERM = np.array([0, 2, 4, 6, 1, 3, 5, 7])
+
+
+def scale_groups_per_tile(g: int) -> int:
+    return max(1, TILE_K // g)
+
+
+def tiled_weights(q, signed: bool) -> np.ndarray:
+    """Codes q[K, N] -> the tiled byte stream (uint8, N*K/2 bytes)."""
+    q = np.asarray(q, dtype=np.int64)
+    k, n = q.shape
+    nib = (q + 8) if signed else q.copy()
+    if nib.min() < 0 or nib.max() > 15:
+        raise ValueError("code out of range")
+    kt_n, nt_n = k // TILE_K, n // TILE_N
+    # nib4[kt, k_local, nt, n_local]
+    nib4 = nib.astype(np.uint64).reshape(kt_n, TILE_K, nt_n, TILE_N)
+    out = np.zeros((nt_n, kt_n, 4, 4, 32, 4), dtype=np.uint64)   # words
+    for qd in range(4):
+        for j in range(4):
+            for w in range(4):
+                for p in range(8):
+                    kl = 32 * j + 8 * w + PERM[p]
+                    vals = nib4[:, kl, :, 32 * qd: 32 * qd + 32]         # [KT, NT, 32]
+                    out[:, :, qd, j, :, w] |= vals.transpose(1, 0, 2) << np.uint64(4 * p)
+    return out.astype(np.uint32).reshape(-1).view(np.uint8)
+
+
+def tiled_scales(s_bits, g: int, k: int) -> np.ndarray:
+    """Scale bit patterns [K/g, N] (uint16) -> tiled uint16 stream."""
+    s_bits = np.asarray(s_bits, dtype=np.uint16)
+    n = s_bits.shape[1]
+    st = scale_groups_per_tile(g)
+    kt_n, nt_n = k // TILE_K, n // TILE_N
+    out = np.zeros((nt_n, kt_n, st, TILE_N), dtype=np.uint16)
+    for nt in range(nt_n):
+        for kt in range(kt_n):
+            for sg in range(st):
+                kk = TILE_K * kt + sg * min(g, TILE_K)
+                out[nt, kt, sg, :] = s_bits[kk // g, TILE_N * nt: TILE_N * (nt + 1)]
+    return out.reshape(-1)
+
+
+def tiled_zeros(z, g: int, k: int) -> np.ndarray:
+    """Zero points [K/g, N] (0..15) -> tiled uint8 stream."""
+    z = np.asarray(z, dtype=np.int64)
+    n = z.shape[1]
+    st = scale_groups_per_tile(g)
+    kt_n, nt_n = k // TILE_K, n // TILE_N
+    out = np.zeros((nt_n, kt_n, st, TILE_N), dtype=np.uint8)
+    for nt in range(nt_n):
+        for kt in range(kt_n):
+            for sg in range(st):
+                kk = TILE_K * kt + sg * min(g, TILE_K)
+                out[nt, kt, sg, :] = z[kk // g, TILE_N * nt: TILE_N * (nt + 1)]
+    return out.reshape(-1)
+
+
+def tiled_weights_inverse(stream, k: int, n: int, signed: bool) -> np.ndarray:
+    """Read the codes back out of a tiled stream (for round-trip checks)."""
+    words = np.asarray(stream, dtype=np.uint8).view(np.uint32).astype(np.uint64)
+    kt_n, nt_n = k // TILE_K, n // TILE_N
+    words = words.reshape(nt_n, kt_n, 4, 4, 32, 4)
+    q4 = np.full((kt_n, TILE_K, nt_n, TILE_N), -99, dtype=np.int64)
+    for qd in range(4):
+        for j in range(4):
+            for w in range(4):
+                for p in range(8):
+                    kl = 32 * j + 8 * w + PERM[p]
+                    vals = (words[:, :, qd, j, :, w] >> np.uint64(4 * p)) & np.uint64(0xF)
+                    q4[:, kl, :, 32 * qd: 32 * qd + 32] = vals.transpose(1, 0, 2).astype(np.int64)
+    q = q4.reshape(k, n)
+    return q - 8 if signed else q

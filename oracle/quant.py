@@ -1,0 +1,213 @@
+"""Quantizers, the standard-format encoding and dequantization.
+
+The Humming pages describe a "standard format" into which every exported
+checkpoint is converted, holding weights, scales, zero points and further
+tensors uniformly (jetabc.cn post, "Humming 的做法", item 1; kinachrichten.com,
+"Wie die Architektur funktioniert"), and a representation that fixes "what
+stored values and associated scales mean" (retrivium.ai retrospective "vLLM
+Humming: why shared quantization still needs specialized kernels", section
+"Representation answers a different question").  They give no formulas and no
+byte layout, so the following readings are taken (each also listed in the
+design notes):
+
+Weights are a logical matrix W[k, n] (K rows, N columns; C = A @ W).
+
+Symmetric INT4 (group g along K, one scale per (group, column)):
+    amax = max |W| over the group
+    s    = sdt(amax / 7)          (sdt = scale dtype, round to nearest even;
+                                   amax == 0 gives s = 1)
+    q    = clip(rint(W / s), -8, 7)   using the stored, rounded s
+    w^   = adt(q * s)             one rounding to the activation dtype
+
+Asymmetric UINT4 (min/max):
+    lo, hi = min W, max W over the group
+    s    = sdt((hi - lo) / 15)    (hi == lo gives s = 1)
+    z    = clip(rint(-lo / s), 0, 15)
+    q    = clip(rint(W / s) + z, 0, 15)
+    w^   = adt((q - z) * s)       one rounding
+
+MXFP4 (one e8m0 exponent per 32 consecutive k of one column; OCP MX v1.0):
+    E    = floor(log2(amax)) - 2 (2 = the e2m1 maximum exponent), clamped to
+           [-127, 127]; b = E + 127;  amax == 0 gives b = 0 and all codes 0
+    c    = e2m1_rne_saturating(W / 2^E)
+    w^   = e2m1(c) * 2^E          exact in float64
+
+``rint`` rounds half to even.  The product (q - z) * s is exact in float64
+(a 5-bit integer times an 8- or 11-bit significand), so w^ is rounded once.
+
+Standard-format encoding (the tensors the library's pack entry point takes):
+    qweight int32 [K/8, N]: word (j, n) holds k = 8j + i in bits [4i, 4i+4),
+            least significant nibble first; INT4 as 4-bit two's complement,
+            UINT4 raw.
+    scales  [K/g, N] row-major (group-major), in the scale dtype.
+    qzeros  int32 [K/g, N/8]: nibble i of word (G, j) is the zero of column
+            8j + i (the stored zero is the true zero, no "-1" offset).
+    MXFP4:  codes uint8 [N, K/2]: byte (n, j) holds k = 2j in the low nibble
+            and k = 2j + 1 in the high nibble; e2m1 bits are s|e1 e0|m.
+            scales uint8 e8m0 [N, K/32].
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from . import codecs
+
+
+def _grouped(w: np.ndarray, g: int) -> np.ndarray:
+    """View W[K, N] as [K/g, g, N] (groups along K)."""
+    k, n = w.shape
+    if k % g:
+        raise ValueError("K must be a multiple of the group size")
+    return w.reshape(k // g, g, n)
+
+
+# ------------------------------------------------------------ quantizers
+
+def quantize_int4_sym(w, g: int, sdt: str):
+    """Symmetric INT4 quantization.  Returns (q int64 [K,N] in [-8,7],
+    s float64 [K/g, N] representable in ``sdt``)."""
+    w = np.asarray(w, dtype=np.float64)
+    wg = _grouped(w, g)
+    amax = np.max(np.abs(wg), axis=1)
+    s = codecs.round_dtype(sdt)(amax / 7.0)
+    s = np.where(amax == 0, 1.0, s)
+    q = np.clip(np.rint(wg / s[:, None, :]), -8, 7)
+    return q.reshape(w.shape).astype(np.int64), s
+
+
+def quantize_uint4_asym(w, g: int, sdt: str):
+    """Asymmetric UINT4 quantization with min/max range.  Returns
+    (q int64 [K,N] in [0,15], s float64 [K/g,N], z int64 [K/g,N] in [0,15])."""
+    w = np.asarray(w, dtype=np.float64)
+    wg = _grouped(w, g)
+    lo = np.min(wg, axis=1)
+    hi = np.max(wg, axis=1)
+    s = codecs.round_dtype(sdt)((hi - lo) / 15.0)
+    s = np.where(hi == lo, 1.0, s)
+    z = np.clip(np.rint(-lo / s), 0, 15)
+    q = np.clip(np.rint(wg / s[:, None, :]) + z[:, None, :], 0, 15)
+    return q.reshape(w.shape).astype(np.int64), s, z.astype(np.int64)
+
+
+def quantize_mxfp4(w):
+    """MXFP4 quantization along K in blocks of 32.  Returns
+    (codes uint8 [K, N] e2m1 nibbles, b uint8 [K/32, N] e8m0 exponents)."""
+    w = np.asarray(w, dtype=np.float64)
+    wg = _grouped(w, 32)
+    amax = np.max(np.abs(wg), axis=1)
+    _, e = np.frexp(np.where(amax == 0, 1.0, amax))
+    big_e = np.clip(e - 1 - 2, -127, 127)        # floor(log2 amax) - emax(e2m1)
+    b = np.where(amax == 0, 0, big_e + 127)
+    scale = np.ldexp(1.0, b - 127)
+    scaled = wg / scale[:, None, :]                # exact: power-of-two divide
+    codes = codecs.encode_e2m1(scaled)
+    codes = np.where(amax[:, None, :] == 0, 0, codes)
+    return codes.reshape(w.shape).astype(np.uint8), b.astype(np.uint8)
+
+
+# ------------------------------------------------------------ dequantization
+
+def dequant_int(q, s, z, g: int, adt: str) -> np.ndarray:
+    """w^[k, n] = adt((q[k,n] - z[k/g, n]) * s[k/g, n]), one rounding.
+
+    ``z`` is None for symmetric INT4 (q already signed)."""
+    q = np.asarray(q, dtype=np.float64)
+    k, n = q.shape
+    s_full = np.repeat(np.asarray(s, dtype=np.float64), g, axis=0)
+    zz = 0.0 if z is None else np.repeat(np.asarray(z, dtype=np.float64), g, axis=0)
+    exact = (q - zz) * s_full
+    return codecs.round_dtype(adt)(exact)
+
+
+def dequant_int_unrounded(q, s, z, g: int) -> np.ndarray:
+    """(q - z) * s in float64 without the activation-dtype rounding (for
+    reporting the alternative reading's error only)."""
+    q = np.asarray(q, dtype=np.float64)
+    s_full = np.repeat(np.asarray(s, dtype=np.float64), g, axis=0)
+    zz = 0.0 if z is None else np.repeat(np.asarray(z, dtype=np.float64), g, axis=0)
+    return (q - zz) * s_full
+
+
+def dequant_mxfp4(codes, b) -> np.ndarray:
+    """w^[k, n] = e2m1(codes[k, n]) * 2^(b[k/32, n] - 127), exact."""
+    vals = codecs.decode_e2m1(codes)
+    scale = np.repeat(codecs.decode_e8m0(b), 32, axis=0)
+    return vals * scale
+
+
+# ------------------------------------------------------------ standard format
+
+def pack_int4_kn(q, signed: bool) -> np.ndarray:
+    """Codes [K, N] -> qweight int32 [K/8, N], k = 8j + i in bits [4i, 4i+4)."""
+    q = np.asarray(q, dtype=np.int64)
+    k, n = q.shape
+    if k % 8:
+        raise ValueError("K must be a multiple of 8")
+    lo, hi = (-8, 7) if signed else (0, 15)
+    if q.min(initial=lo) < lo or q.max(initial=hi) > hi:
+        raise ValueError("code out of range")
+    nib = (q & 0xF).astype(np.uint64).reshape(k // 8, 8, n)
+    word = np.zeros((k // 8, n), dtype=np.uint64)
+    for i in range(8):
+        word |= nib[:, i, :] << np.uint64(4 * i)
+    return word.astype(np.uint32).view(np.int32)
+
+
+def unpack_int4_kn(qweight, signed: bool) -> np.ndarray:
+    """Inverse of ``pack_int4_kn``."""
+    w = np.asarray(qweight).view(np.uint32).astype(np.uint64)
+    kw, n = w.shape
+    out = np.empty((kw, 8, n), dtype=np.int64)
+    for i in range(8):
+        out[:, i, :] = (w >> np.uint64(4 * i)) & np.uint64(0xF)
+    out = out.reshape(kw * 8, n)
+    if signed:
+        out = np.where(out >= 8, out - 16, out)
+    return out
+
+
+def pack_zeros(z) -> np.ndarray:
+    """Zeros [K/g, N] in [0,15] -> qzeros int32 [K/g, N/8], column 8j + i in
+    nibble i of word (G, j)."""
+    z = np.asarray(z, dtype=np.int64)
+    gk, n = z.shape
+    if n % 8:
+        raise ValueError("N must be a multiple of 8")
+    nib = (z & 0xF).astype(np.uint64).reshape(gk, n // 8, 8)
+    word = np.zeros((gk, n // 8), dtype=np.uint64)
+    for i in range(8):
+        word |= nib[:, :, i] << np.uint64(4 * i)
+    return word.astype(np.uint32).view(np.int32)
+
+
+def unpack_zeros(qzeros) -> np.ndarray:
+    w = np.asarray(qzeros).view(np.uint32).astype(np.uint64)
+    gk, nw = w.shape
+    out = np.empty((gk, nw, 8), dtype=np.int64)
+    for i in range(8):
+        out[:, :, i] = (w >> np.uint64(4 * i)) & np.uint64(0xF)
+    return out.reshape(gk, nw * 8)
+
+
+def pack_mxfp4(codes_kn, b_kn):
+    """MXFP4 codes [K, N] and exponents [K/32, N] -> (uint8 [N, K/2] with the
+    even k in the low nibble, uint8 [N, K/32])."""
+    c = np.asarray(codes_kn, dtype=np.uint8).T          # [N, K]
+    packed = (c[:, 0::2] & 0xF) | ((c[:, 1::2] & 0xF) << 4)
+    return packed.astype(np.uint8), np.ascontiguousarray(np.asarray(b_kn, dtype=np.uint8).T)
+
+
+def unpack_mxfp4(packed_nk, b_nk):
+    """Inverse of ``pack_mxfp4``: -> (codes [K, N], b [K/32, N])."""
+    p = np.asarray(packed_nk, dtype=np.uint8)
+    n, kh = p.shape
+    c = np.empty((n, 2 * kh), dtype=np.uint8)
+    c[:, 0::2] = p & 0xF
+    c[:, 1::2] = p >> 4
+    return np.ascontiguousarray(c.T), np.ascontiguousarray(np.asarray(b_nk, dtype=np.uint8).T)
+
+
+def scales_bits(s, sdt: str) -> np.ndarray:
+    """Scale values -> uint16 bit patterns of the scale dtype."""
+    return codecs.dtype_bits(sdt, s)

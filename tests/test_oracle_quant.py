@@ -1,0 +1,179 @@
+"""Pins for the quantizers, the standard-format encoding, dequantization and
+the kernel-side tiled layout."""
+
+import numpy as np
+import pytest
+
+import synth
+from conftest import read_golden
+from oracle import codecs, layout, quant
+
+
+def test_dequant_golden_cases():
+    for row in read_golden("dequant_cases.txt"):
+        if row[0] == "int":
+            _, q, z, s, adt, want = row
+            got = quant.dequant_int(np.array([[int(q)]]), np.array([[float(s)]]),
+                                    np.array([[int(z)]]), 1, adt)
+            assert float(got[0, 0]) == float(want), row
+        else:
+            _, code, b, want = row
+            got = quant.dequant_mxfp4(np.full((32, 1), int(code)), np.array([[int(b)]]))
+            assert float(got[0, 0]) == float(want), row
+
+
+@pytest.mark.parametrize("sdt", ["fp16", "bf16"])
+def test_int4_sym_invariants(sdt):
+    g = synth.rng(5)
+    w = synth.weights_fp32(g, 512, 64)
+    q, s = quant.quantize_int4_sym(w, 128, sdt)
+    assert q.min() >= -8 and q.max() <= 7
+    assert np.array_equal(codecs.round_dtype(sdt)(s), s)          # s is representable
+    full_s = np.repeat(s, 128, axis=0)
+    err = np.abs(w.astype(np.float64) - q * full_s)
+    inside = (q > -8) & (q < 7)
+    assert np.all(err[inside] <= full_s[inside] / 2 * (1 + 1e-12))
+    # the group's absmax element lands on +-7 (or -8 after scale rounding)
+    wg = np.abs(w.astype(np.float64)).reshape(4, 128, 64)
+    arg = wg.argmax(axis=1)
+    qg = q.reshape(4, 128, 64)
+    top = np.take_along_axis(qg, arg[:, None, :], axis=1)[:, 0, :]
+    assert np.all(np.abs(top) >= 7)
+
+
+def test_int4_sym_brute_force_small():
+    g = synth.rng(6)
+    w = synth.weights_fp32(g, 64, 8)
+    q, s = quant.quantize_int4_sym(w, 32, "fp16")
+    for gi in range(2):
+        for n in range(8):
+            col = [float(w[k, n]) for k in range(32 * gi, 32 * gi + 32)]
+            amax = max(abs(v) for v in col)
+            sv = float(np.float16(amax / 7.0))
+            assert s[gi, n] == sv
+            for i, v in enumerate(col):
+                qq = max(-8, min(7, int(np.rint(v / sv))))
+                assert q[32 * gi + i, n] == qq
+
+
+def test_int4_zero_group_scale_is_one():
+    w = np.zeros((128, 8), dtype=np.float32)
+    q, s = quant.quantize_int4_sym(w, 128, "bf16")
+    assert np.all(s == 1.0) and np.all(q == 0)
+
+
+def test_uint4_asym_invariants():
+    g = synth.rng(7)
+    w = synth.weights_fp32(g, 512, 64)
+    q, s, z = quant.quantize_uint4_asym(w, 128, "bf16")
+    assert q.min() >= 0 and q.max() <= 15 and z.min() >= 0 and z.max() <= 15
+    full_s = np.repeat(s, 128, axis=0)
+    full_z = np.repeat(z, 128, axis=0)
+    err = np.abs(w.astype(np.float64) - (q - full_z) * full_s)
+    inside = (q > 0) & (q < 15)
+    assert np.all(err[inside] <= full_s[inside] / 2 * (1 + 1e-12))
+    # the range spans all 16 codes up to rounding: min near 0, max near 15
+    qg = q.reshape(4, 128, 64)
+    assert np.all(qg.min(axis=1) <= 1) and np.all(qg.max(axis=1) >= 14)
+
+
+def test_mxfp4_exponent_rule_and_codes():
+    w = np.zeros((64, 3))
+    w[:32, 0] = np.linspace(-6, 6, 32)                 # amax 6 -> E = 0, b = 127
+    w[:32, 1] = 0.05 * np.linspace(-1, 1, 32)         # amax .05 -> floor(log2) = -5 -> E = -7
+    w[32:, 2] = 0.0                                    # zero block -> b = 0, codes 0
+    w[:32, 2] = 7.9                                    # saturates: E = 0, codes 6
+    codes, b = quant.quantize_mxfp4(w)
+    assert b[0, 0] == 127 and b[0, 1] == 120 and b[0, 2] == 127 and b[1, 2] == 0
+    assert np.all(codecs.decode_e2m1(codes[:32, 2]) == 6.0)
+    assert np.all(codes[32:, 2] == 0)
+    deq = quant.dequant_mxfp4(codes, b)
+    assert np.array_equal(deq[:32, 0], codecs.e2m1(w[:32, 0]))
+    # relative error bound of e2m1 within the non-saturated range: half a step
+    step = np.where(np.abs(w[:32, 1] / 2.0 ** -7) < 2, 0.5, np.where(np.abs(w[:32, 1] / 2.0 ** -7) < 4, 1.0, 2.0))
+    assert np.all(np.abs(deq[:32, 1] - w[:32, 1]) <= step * 2.0 ** -7 / 2 + 1e-15)
+
+
+def test_pack_unpack_roundtrip_and_handbuilt_words():
+    g = np.random.default_rng(8)
+    q = g.integers(-8, 8, (64, 40))
+    assert np.array_equal(quant.unpack_int4_kn(quant.pack_int4_kn(q, True), True), q)
+    u = g.integers(0, 16, (64, 40))
+    assert np.array_equal(quant.unpack_int4_kn(quant.pack_int4_kn(u, False), False), u)
+    # word 0x76543210 at (0, 0): k = 0..7 hold 0..7, least significant nibble first
+    word = np.array([[0x76543210]], dtype=np.uint32).view(np.int32)
+    assert list(quant.unpack_int4_kn(word, False)[:, 0]) == list(range(8))
+    # signed: 0x89ABCDEF -> -1, -2, ..., -8
+    word = np.array([[0x89ABCDEF]], dtype=np.uint32).view(np.int32)
+    assert list(quant.unpack_int4_kn(word, True)[:, 0]) == [-1, -2, -3, -4, -5, -6, -7, -8]
+    packed = quant.pack_int4_kn(np.arange(8).reshape(8, 1), False)
+    assert packed.view(np.uint32)[0, 0] == 0x76543210
+
+
+def test_zero_points_pack_handbuilt():
+    z = np.arange(16).reshape(1, 16) % 16
+    qz = quant.pack_zeros(z)
+    assert qz.shape == (1, 2)
+    assert qz.view(np.uint32)[0, 0] == 0x76543210 and qz.view(np.uint32)[0, 1] == 0xFEDCBA98
+    assert np.array_equal(quant.unpack_zeros(qz), z)
+
+
+def test_mxfp4_pack_handbuilt():
+    codes = np.zeros((64, 2), dtype=np.uint8)
+    codes[0, 0], codes[1, 0] = 1, 2           # k=0 low nibble, k=1 high nibble
+    codes[63, 1] = 15
+    b = np.full((2, 2), 127, dtype=np.uint8)
+    b[1, 1] = 3
+    p, bs = quant.pack_mxfp4(codes, b)
+    assert p.shape == (2, 32) and p[0, 0] == 0x21 and p[1, 31] == 0xF0
+    assert bs.shape == (2, 2) and bs[1, 1] == 3
+    c2, b2 = quant.unpack_mxfp4(p, bs)
+    assert np.array_equal(c2, codes) and np.array_equal(b2, b)
+
+
+def _nibble_at(stream, n, k, kt_count):
+    """Scalar statement of the tiled layout: location of (n, k)."""
+    nt, nl = divmod(n, 128)
+    kt, kl = divmod(k, 128)
+    qd, t = divmod(nl, 32)
+    j, r = divmod(kl, 32)
+    w, o = divmod(r, 8)
+    p = [0, 4, 1, 5, 2, 6, 3, 7][o]           # inverse of PERM: k-offset -> nibble position
+    vec = (nt * kt_count + kt) * 512 + (qd * 4 + j) * 32 + t
+    byte = vec * 16 + w * 4 + p // 2
+    v = int(stream[byte])
+    return (v >> 4) if p % 2 else (v & 0xF)
+
+
+@pytest.mark.parametrize("signed", [True, False])
+def test_tiled_layout_scalar_spec(signed):
+    g = np.random.default_rng(9)
+    k, n = 384, 256
+    q = g.integers(-8, 8, (k, n)) if signed else g.integers(0, 16, (k, n))
+    stream = layout.tiled_weights(q, signed)
+    assert stream.size == k * n // 2
+    for _ in range(3000):
+        kk, nn = int(g.integers(0, k)), int(g.integers(0, n))
+        want = q[kk, nn] + 8 if signed else q[kk, nn]
+        assert _nibble_at(stream, nn, kk, k // 128) == want
+    assert np.array_equal(layout.tiled_weights_inverse(stream, k, n, signed), q)
+
+
+@pytest.mark.parametrize("gsize", [32, 64, 128, 256])
+def test_tiled_scales_and_zeros_scalar_spec(gsize):
+    g = np.random.default_rng(10)
+    k, n = 512, 256
+    sb = g.integers(0, 65535, (k // gsize, n)).astype(np.uint16)
+    z = g.integers(0, 16, (k // gsize, n))
+    ts = layout.tiled_scales(sb, gsize, k)
+    tz = layout.tiled_zeros(z, gsize, k)
+    st = max(1, 128 // gsize)
+    assert ts.size == (k // 128) * (n // 128) * st * 128
+    for kk in range(0, k, 32):
+        for nn in range(0, n, 7):
+            nt, r = divmod(nn, 128)
+            kt, kl = divmod(kk, 128)
+            sg = kl // gsize if gsize < 128 else 0
+            idx = ((nt * (k // 128) + kt) * st + sg) * 128 + r
+            assert ts[idx] == sb[kk // gsize, nn]
+            assert tz[idx] == z[kk // gsize, nn]
