@@ -1,0 +1,309 @@
+/*
+ * qgemm.h -- C ABI of the B300 (sm_103a) quantized-weight GEMM library.
+ *
+ * The library runs the hot path of a mixed-precision GEMM over 4-bit quantized
+ * weights: W4A16 (INT4 / UINT4 codes with per-group fp16 or bf16 scales and
+ * optional zero points, dequantized in registers and fed to 16-bit tensor-core
+ * MMA with fp32 accumulation), W4A8-MXFP4 (e2m1 codes with e8m0 per-32 scales
+ * against per-token FP8 e4m3 activations) and the grouped-MoE variant that
+ * runs one such GEMM per expert over router-permuted tokens.
+ *
+ * Where the operations come from (the Humming pages; titles and sections):
+ *   - kinachrichten.com, "Ant Group und vLLM stellen Humming als Open Source
+ *     vor: Kernel-Bibliothek fuer quantisierte Inferenz", section "Wie die
+ *     Architektur funktioniert": a standard format for weights, scales, zero
+ *     points; a preprocessing step that checks parameters, pads and repacks
+ *     for the target kernel; three configurations per kernel (Layer, Compute,
+ *     Tuning); device heuristics choosing the tuning, with different kernels
+ *     for different input-size ranges.  Section "Kompilierzeiten und
+ *     geraetespezifisches Tuning": kernels built from scheduling, data
+ *     movement, dequantization/scaling, tensor-core compute and output
+ *     processing components; the W4A8-MXFP4 path.
+ *   - jetabc.cn, "一个库吃下所有量化格式：蚂蚁和 vLLM 开源推理内核库 Humming",
+ *     section "Humming 的做法" (standard format, three configs) and
+ *     "跑得有多快" (W4A16, grouped MoE and W4A8-MXFP4 kernel families).
+ *   - retrivium.ai retrospective "vLLM Humming: why shared quantization still
+ *     needs specialized kernels", section "The architectural gain is a smaller
+ *     maintenance surface": unsupported combinations are rejected clearly.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are caller-owned.  Pointers marked "device" are CUDA device
+ *     pointers on the current device; the library allocates no device memory
+ *     and never frees caller memory.  Pointers must be 16-byte aligned; every
+ *     tensor is dense row-major with the strides implied by its shape.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous on it and never synchronize, except qgemm_check_status.
+ *   - Arguments are validated synchronously on the host; on any error nothing
+ *     is launched and a status != QGEMM_OK is returned.  qgemm_last_error()
+ *     returns a human-readable reason for the last failing call of the thread.
+ *   - Unsupported combinations (e.g. zero points with MXFP4, N or K not a
+ *     multiple of 128, K not a multiple of the group size) return
+ *     QGEMM_ERR_UNSUPPORTED.  There is no fallback path.
+ *   - A CUDA launch error returns QGEMM_ERR_CUDA.
+ */
+#ifndef QGEMM_H_
+#define QGEMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QGEMM_OK = 0,
+  QGEMM_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment        */
+  QGEMM_ERR_UNSUPPORTED = 2, /* valid but not implemented combination       */
+  QGEMM_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required  */
+  QGEMM_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed           */
+  QGEMM_ERR_TIMEOUT = 5,     /* a kernel gave up a bounded wait             */
+  QGEMM_ERR_DEVICE = 6       /* a kernel reported an internal error         */
+} qgemm_status;
+
+/* weight formats */
+enum { QGEMM_W_INT4_SYM = 0, QGEMM_W_UINT4_ZP = 1, QGEMM_W_MXFP4 = 2 };
+/* scale formats */
+enum { QGEMM_S_FP16 = 0, QGEMM_S_BF16 = 1, QGEMM_S_E8M0 = 2 };
+/* zero-point formats */
+enum { QGEMM_Z_NONE = 0, QGEMM_Z_UINT4 = 1 };
+/* activation / output data types */
+enum { QGEMM_FP16 = 0, QGEMM_BF16 = 1, QGEMM_FP8E4M3 = 2 };
+/* GEMM types (compute config) */
+enum { QGEMM_GEMM_DENSE = 0, QGEMM_GEMM_GROUPED = 1 };
+
+/*
+ * Layer config: what the layer is.  Shapes are those of one expert; a dense
+ * layer has num_experts = 1.
+ *   n, k          output features, input features (C[M,N] = A[M,K] W[K,N])
+ *   group_size    K-extent of one scale (W4A16: 32, 64 or a multiple of 128
+ *                 dividing K; MXFP4: must be 32)
+ *   weight_format QGEMM_W_*;  scale_format QGEMM_S_*;  zero_format QGEMM_Z_*
+ *   act_dtype     activation dtype: QGEMM_FP16 / QGEMM_BF16 (W4A16) or
+ *                 QGEMM_FP8E4M3 (W4A8; the caller passes e4m3 codes and
+ *                 per-row fp32 scales from qgemm_quantize_act_fp8)
+ *   out_dtype     output dtype: equal to act_dtype for W4A16, QGEMM_BF16 for W4A8
+ *   has_bias      1: add bias[N] (out_dtype) in fp32 before the final rounding
+ *   num_experts   1 for a dense layer, E for a grouped (MoE) layer
+ */
+typedef struct {
+  int64_t n;
+  int64_t k;
+  int32_t group_size;
+  int32_t weight_format;
+  int32_t scale_format;
+  int32_t zero_format;
+  int32_t act_dtype;
+  int32_t out_dtype;
+  int32_t has_bias;
+  int32_t num_experts;
+} qgemm_layer_config;
+
+/* Compute config: what computation.  batch_invariant is reserved and must be 0. */
+typedef struct {
+  int32_t gemm_type;
+  int32_t batch_invariant;
+} qgemm_compute_config;
+
+/*
+ * Tuning config: how to run it on this device.  Pass NULL for the built-in
+ * B300 heuristic (token tile chosen by the M range).  Fields left 0 are chosen
+ * by the heuristic.
+ *   block_tok  tokens per tile (the MMA N extent): 16, 32, 64 or 128
+ *   stages     shared-memory pipeline depth (2 .. 16)
+ *   max_ctas   upper bound on the persistent grid (<= number of SMs)
+ *   split_k    1 = never split a tile's K range across CTAs; 0 = allowed
+ *   cta_pair   reserved, must be 0
+ */
+typedef struct {
+  int32_t block_tok;
+  int32_t stages;
+  int32_t max_ctas;
+  int32_t split_k;
+  int32_t cta_pair;
+} qgemm_tuning_config;
+
+/*
+ * Standard-format input tensors (what qgemm_pack_weights consumes).  Weights
+ * are the logical matrix W[k, n].  Per expert (stacked on a leading E axis):
+ *   INT4 / UINT4:
+ *     qweight  int32 [K/8, N]: word (j, n) holds k = 8j + i in bits [4i, 4i+4),
+ *              least significant nibble first; INT4 as 4-bit two's complement,
+ *              UINT4 as raw 0..15
+ *     scales   fp16 or bf16 [K/g, N], row-major (group-major)
+ *     qzeros   int32 [K/g, N/8] (UINT4_ZP only): nibble i of word (G, j) is the
+ *              zero point (0..15) of column 8j + i; the stored value is the
+ *              true zero point
+ *     meaning  w[k, n] = (q - z) * s, rounded once to the activation dtype
+ *              (z = 0 for INT4)
+ *   MXFP4:
+ *     codes    uint8 [N, K/2]: byte (n, j) holds k = 2j (low nibble) and
+ *              k = 2j + 1 (high nibble) as e2m1 (sign | 2 exponent | 1 mantissa)
+ *     scales   uint8 e8m0 [N, K/32]: the block scale 2^(b - 127); 255 is invalid
+ *     meaning  w[k, n] = e2m1(code) * 2^(b - 127)
+ */
+
+/*
+ * Bytes of the packed (kernel-layout) tensors for one layer (all experts).
+ * Any output pointer may be NULL.  Returns INVALID_ARG / UNSUPPORTED on a bad
+ * config.
+ */
+qgemm_status qgemm_packed_sizes(const qgemm_layer_config* layer, size_t* w_bytes,
+                                size_t* s_bytes, size_t* z_bytes);
+
+/*
+ * Preprocessing (the "repack for the target kernel" step): validates the
+ * config and rearranges the standard-format tensors (device, layout above)
+ * into the kernel layout (device outputs, sizes from qgemm_packed_sizes).
+ * INT4 codes are re-encoded as offset binary (q + 8); nothing else changes
+ * value, so the packed tensors mean exactly what the standard ones mean.
+ * qzeros / z_out must be NULL unless zero_format = QGEMM_Z_UINT4.  Runs once
+ * per layer; the outputs are read-only afterwards.
+ */
+qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qweight,
+                                const void* scales, const void* qzeros, void* w_out,
+                                void* s_out, void* z_out, void* stream);
+
+/*
+ * Workspace bytes qgemm_run / qgemm_grouped_run need for `m` rows (for the
+ * grouped call: the total number of permuted rows).  The workspace holds a
+ * status word, split-K tile counters and fp32 partial tiles.  It must be
+ * zero-filled once before first use (qgemm_workspace_init); every successful
+ * call leaves the counters at zero again.  One workspace must not be used by
+ * two calls that can run at the same time.
+ */
+qgemm_status qgemm_workspace_size(const qgemm_layer_config* layer,
+                                  const qgemm_compute_config* compute,
+                                  const qgemm_tuning_config* tuning, int64_t m, size_t* bytes);
+
+/* Zero-fill a workspace on `stream` (asynchronous). */
+qgemm_status qgemm_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/*
+ * Dense quantized GEMM: C[m, n] = out_dtype(A[m, :] . W[:, n] (+ bias[n])).
+ *   m         rows of A and C (0 is allowed and launches nothing)
+ *   a         device, [m, K] in act_dtype (e4m3 codes for W4A8)
+ *   a_scale   device fp32 [m] per-row activation scales (W4A8), else NULL
+ *   w, s, z   device packed tensors from qgemm_pack_weights (z NULL if none)
+ *   bias      device [N] in out_dtype, or NULL when has_bias = 0
+ *   c         device, [m, N] in out_dtype
+ *   workspace device, >= qgemm_workspace_size bytes, zero-initialised once
+ * Fixed-order split-K reduction: results are bitwise reproducible for a given
+ * (config, m, tuning, device).
+ */
+qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_config* compute,
+                       const qgemm_tuning_config* tuning, int64_t m, const void* a,
+                       const float* a_scale, const void* w, const void* s, const void* z,
+                       const void* bias, void* c, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/*
+ * Grouped (MoE) quantized GEMM over router-permuted rows: for each expert e,
+ * rows [offsets[e], offsets[e+1]) of A are multiplied by expert e's weights.
+ *   expert_offsets device int32 [E+1], non-decreasing, offsets[0] = 0,
+ *                  offsets[E] = total_rows (e.g. from qgemm_moe_permute)
+ *   total_rows     number of rows of A and C (host value)
+ *   w, s, z        packed tensors of all E experts (stacked)
+ *   bias           device [E, N] or NULL
+ * The tile schedule is built on the device from expert_offsets: no host
+ * synchronization is needed between the permute and the GEMM.
+ */
+qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
+                               const qgemm_compute_config* compute,
+                               const qgemm_tuning_config* tuning, const int32_t* expert_offsets,
+                               int64_t total_rows, const void* a, const float* a_scale,
+                               const void* w, const void* s, const void* z, const void* bias,
+                               void* c, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Per-token FP8 activation quantization (W4A8 path):
+ *   a_scale[r] = max_k |x[r, k]| / 448 (fp32; 1 for an all-zero row)
+ *   a8[r, k]   = e4m3(x[r, k] / a_scale[r]), IEEE fp32 divide, round to
+ *                nearest even, saturating at +-448
+ *   x device bf16 [m, k]; a8 device uint8 [m, k]; a_scale device fp32 [m].
+ */
+qgemm_status qgemm_quantize_act_fp8(const void* x, int64_t m, int64_t k, void* a8,
+                                    float* a_scale, void* stream);
+
+/*
+ * MoE permutation: stable counting sort of the t*topk (token, slot) pairs by
+ * expert id, then the row gather.
+ *   topk_ids    device int32 [t, topk], values in [0, e); e <= 256.  Ids
+ *               outside [0, e) are placed after the last expert (rows
+ *               offsets[e] .. t*topk - 1) and join no expert GEMM
+ *   offsets     device int32 [e+1] (output): rows of expert x are
+ *               [offsets[x], offsets[x+1])
+ *   perm        device int32 [t*topk] (output): perm[r] = token*topk + j, the
+ *               (token, slot) pair placed at row r; pairs of one expert keep
+ *               their (token, slot) order
+ *   inv_perm    device int32 [t*topk] (output): inv_perm[token*topk + j] = r
+ *   a           device [t, hidden] activations (2-byte elements)
+ *   a_perm      device [t*topk, hidden] (output): a_perm[r] = a[perm[r] / topk]
+ */
+qgemm_status qgemm_moe_permute(const int32_t* topk_ids, int64_t t, int32_t topk, int32_t e,
+                               int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                               const void* a, void* a_perm, int64_t hidden, void* stream);
+
+/*
+ * SiLU gate: h[r, i] = bf16(silu(gu[r, i]) * gu[r, inter + i]) in fp32,
+ * gu device bf16 [rows, 2*inter], h device bf16 [rows, inter].
+ */
+qgemm_status qgemm_moe_silu_mul(const void* gu, int64_t rows, int64_t inter, void* h,
+                                void* stream);
+
+/*
+ * Combine: y[t, :] = bf16(sum_{j < topk} w[t, j] * y2[inv_perm[t*topk + j], :])
+ * in fp32, summed in slot order j = 0..topk-1.
+ *   y2 device bf16 [t*topk, hidden]; inv_perm device int32 [t*topk] (from
+ *   qgemm_moe_permute); topk_weights device fp32 [t, topk]; y device bf16
+ *   [t, hidden].
+ */
+qgemm_status qgemm_moe_combine(const void* y2, const int32_t* inv_perm,
+                               const float* topk_weights, int64_t t, int32_t topk,
+                               int64_t hidden, void* y, void* stream);
+
+/*
+ * Debug: write the dequantized weights of a packed W4A16 layer (expert 0 or
+ * the dense layer) as out[k, n] in act_dtype (device, [K, N]), using exactly
+ * the kernels' dequantization arithmetic.
+ */
+qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* w, const void* s,
+                                 const void* z, void* out_kn, void* stream);
+
+/*
+ * Synchronizes `stream`, reads the workspace status word written by the GEMM
+ * kernels, clears it and returns QGEMM_OK, QGEMM_ERR_TIMEOUT (a bounded wait
+ * gave up) or QGEMM_ERR_DEVICE.  After a timeout the caller must zero the
+ * workspace again (qgemm_workspace_init) before reuse.
+ */
+qgemm_status qgemm_check_status(void* workspace, void* stream);
+
+/*
+ * Wait limit, in nanoseconds, that kernels launched afterwards by this process
+ * give each internal wait before they abandon the launch and report
+ * QGEMM_ERR_TIMEOUT (default 1e9).  Exists to test the timeout path.
+ */
+void qgemm_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * The compatibility record of a call: writes into buf (NUL-terminated, at most
+ * len bytes) which kernel variant and tuning the heuristic picks for this
+ * (layer, compute, m) on the current device, or why the combination is
+ * rejected.  Returns the status the corresponding run call would return for
+ * the configuration checks.
+ */
+qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
+                                 const qgemm_compute_config* compute, int64_t m, char* buf,
+                                 size_t len);
+
+/* Static string naming a status code. */
+const char* qgemm_status_string(qgemm_status status);
+
+/* Reason for the last non-OK status returned on this thread ("" if none). */
+const char* qgemm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_H_ */

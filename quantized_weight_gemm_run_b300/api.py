@@ -1,0 +1,137 @@
+"""Torch-facing convenience layer over the C ABI.
+
+PyTorch only provides device memory and streams here: each class allocates
+the packed weights and the workspace as torch tensors once and then calls the
+library's entry points (``qgemm.py``) on the current torch stream.  No
+arithmetic of the method runs in Python.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import qgemm as Q
+
+_DT = {torch.float16: Q.QGEMM_FP16, torch.bfloat16: Q.QGEMM_BF16}
+
+
+class Workspace:
+    """A zero-initialised device workspace that grows on demand."""
+
+    def __init__(self, device="cuda"):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+class W4A16Linear:
+    """A packed W4A16 layer (dense, or the stacked experts of a grouped layer).
+
+    qweight int32 [E*K/8, N], scales [E*K/g, N] (act dtype), qzeros int32
+    [E*K/g, N/8] or None: the standard format of ``include/qgemm.h``."""
+
+    def __init__(self, qweight, scales, qzeros, n, k, group, act_dtype, num_experts=1,
+                 bias=None, tuning=None):
+        self.n, self.k, self.group, self.num_experts = n, k, group, num_experts
+        self.act_dtype = act_dtype
+        asym = qzeros is not None
+        adt = _DT[act_dtype]
+        self.layer = Q.layer_config(
+            n, k, group, Q.QGEMM_W_UINT4_ZP if asym else Q.QGEMM_W_INT4_SYM,
+            Q.QGEMM_S_FP16 if adt == Q.QGEMM_FP16 else Q.QGEMM_S_BF16,
+            Q.QGEMM_Z_UINT4 if asym else Q.QGEMM_Z_NONE, adt, adt,
+            1 if bias is not None else 0, num_experts)
+        st, wb, sb, zb = Q.qgemm_packed_sizes(self.layer)
+        Q.check(st)
+        dev = qweight.device
+        self.w = torch.empty(wb, dtype=torch.uint8, device=dev)
+        self.s = torch.empty(sb // 2, dtype=torch.int16, device=dev)
+        self.z = torch.empty(zb, dtype=torch.uint8, device=dev) if asym else None
+        Q.check(Q.qgemm_pack_weights(self.layer, qweight, scales, qzeros, self.w, self.s,
+                                     self.z))
+        self.bias = bias
+        self.tuning = tuning
+        self.ws = Workspace(dev)
+        self.dense = Q.compute_config(Q.QGEMM_GEMM_DENSE)
+        self.grouped = Q.compute_config(Q.QGEMM_GEMM_GROUPED)
+
+    def __call__(self, a: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+        m = a.shape[0]
+        if out is None:
+            out = torch.empty(m, self.n, dtype=self.act_dtype, device=a.device)
+        st, nbytes = Q.qgemm_workspace_size(self.layer, self.dense, self.tuning, max(m, 1))
+        Q.check(st)
+        ws = self.ws.get(nbytes)
+        Q.check(Q.qgemm_run(self.layer, self.dense, self.tuning, m, a, None, self.w, self.s,
+                            self.z, self.bias, out, ws, ws.numel()))
+        return out
+
+    def run_grouped(self, a_perm: torch.Tensor, offsets: torch.Tensor,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+        rows = a_perm.shape[0]
+        if out is None:
+            out = torch.empty(rows, self.n, dtype=self.act_dtype, device=a_perm.device)
+        st, nbytes = Q.qgemm_workspace_size(self.layer, self.grouped, self.tuning, max(rows, 1))
+        Q.check(st)
+        ws = self.ws.get(nbytes)
+        Q.check(Q.qgemm_grouped_run(self.layer, self.grouped, self.tuning, offsets, rows, a_perm,
+                                    None, self.w, self.s, self.z, self.bias, out, ws,
+                                    ws.numel()))
+        return out
+
+    def dequantized(self) -> torch.Tensor:
+        """W^[K, N] as the kernels feed it to the tensor core (expert 0)."""
+        out = torch.empty(self.k, self.n, dtype=self.act_dtype, device=self.w.device)
+        Q.check(Q.qgemm_debug_dequant(self.layer, self.w, self.s, self.z, out))
+        return out
+
+    def status(self) -> int:
+        return Q.qgemm_check_status(self.ws.get(256))
+
+
+class MoELayer:
+    """Grouped-MoE W4A16 layer: permute -> GEMM1 (gate|up) -> SiLU gate ->
+    GEMM2 (down) -> combine, all on the current stream, no host sync."""
+
+    def __init__(self, w1: W4A16Linear, w2: W4A16Linear, num_experts: int, topk: int):
+        self.w1, self.w2 = w1, w2
+        self.e, self.topk = num_experts, topk
+        self.hidden = w1.k
+        self.inter = w2.k
+        self._bufs = {}
+
+    def buffers(self, t: int, device):
+        if t not in self._bufs:
+            r = t * self.topk
+            bf = torch.bfloat16
+            self._bufs[t] = dict(
+                offsets=torch.empty(self.e + 1, dtype=torch.int32, device=device),
+                perm=torch.empty(max(r, 1), dtype=torch.int32, device=device),
+                inv=torch.empty(max(r, 1), dtype=torch.int32, device=device),
+                a_perm=torch.empty(max(r, 1), self.hidden, dtype=bf, device=device),
+                gu=torch.empty(max(r, 1), 2 * self.inter, dtype=bf, device=device),
+                h=torch.empty(max(r, 1), self.inter, dtype=bf, device=device),
+                y2=torch.empty(max(r, 1), self.hidden, dtype=bf, device=device),
+            )
+        return self._bufs[t]
+
+    def __call__(self, a, topk_ids, topk_weights, out=None, keep=False):
+        t = a.shape[0]
+        b = self.buffers(t, a.device)
+        r = t * self.topk
+        if out is None:
+            out = torch.empty(t, self.hidden, dtype=torch.bfloat16, device=a.device)
+        Q.check(Q.qgemm_moe_permute(topk_ids, t, self.topk, self.e, b["offsets"], b["perm"],
+                                    b["inv"], a, b["a_perm"], self.hidden))
+        self.w1.run_grouped(b["a_perm"][:r], b["offsets"], out=b["gu"][:r])
+        Q.check(Q.qgemm_moe_silu_mul(b["gu"], r, self.inter, b["h"]))
+        self.w2.run_grouped(b["h"][:r], b["offsets"], out=b["y2"][:r])
+        Q.check(Q.qgemm_moe_combine(b["y2"], b["inv"], topk_weights, t, self.topk, self.hidden,
+                                    out))
+        if keep:
+            return out, b
+        return out

@@ -1,0 +1,226 @@
+// Memory-bound support kernels of the hot path: per-token FP8 activation
+// quantization (W4A8 path), and the MoE permutation, SiLU gate and combine
+// around the grouped GEMMs.
+//
+// The pages name the W4A8-MXFP4 path with FP8 activations (kinachrichten.com,
+// "Kompilierzeiten und geraetespezifisches Tuning", MXFP4 paragraph) and MoE
+// layers in which each token activates a subset of the experts (same article,
+// "Warum quantisierte Kernel wichtig sind"); the arithmetic of each kernel is
+// stated at the kernel.
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "internal.h"
+
+namespace qg {
+
+// ----------------------------------------------------------- FP8 act quant
+// One CTA per row: s = max|x| / 448 (fp32, IEEE divide; 1 for an all-zero
+// row), code = e4m3_rn_satfinite(x / s) with an IEEE fp32 divide.
+__global__ void act_quant_fp8_kernel(const uint16_t* __restrict__ x, int k,
+                                     uint8_t* __restrict__ a8, float* __restrict__ scale) {
+  const long long row = blockIdx.x;
+  const uint16_t* xr = x + row * k;
+  float amax = 0.f;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    uint16_t b = xr[i];
+    amax = fmaxf(amax, fabsf(__bfloat162float(*reinterpret_cast<__nv_bfloat16*>(&b))));
+  }
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  amax = red[0];
+  const float s = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
+  if (threadIdx.x == 0) scale[row] = s;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    uint16_t b = xr[i];
+    const float v = __fdiv_rn(__bfloat162float(*reinterpret_cast<__nv_bfloat16*>(&b)), s);
+    a8[row * k + i] = (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+  }
+}
+
+cudaError_t launch_act_quant_fp8(const uint16_t* x, int64_t m, int64_t k, uint8_t* a8,
+                                 float* scale, cudaStream_t stream) {
+  if (m == 0) return cudaSuccess;
+  act_quant_fp8_kernel<<<(unsigned)m, 256, 0, stream>>>(x, (int)k, a8, scale);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------- MoE permute
+// Stable counting sort of the slots s = token*topk + j by expert id in one
+// CTA of 1024 threads: a histogram, an exclusive scan (the expert offsets),
+// then the slots in chunks of 1024 in slot order, each placed at
+// base[e] + (number of earlier slots of expert e), found with a warp match
+// and a scan of per-warp counts.  Ids outside [0, E) go to an extra bucket
+// after the last expert, so perm is always a full permutation of the slots.
+__global__ void __launch_bounds__(1024) moe_sort_kernel(const int32_t* __restrict__ ids,
+                                                        int n_slots, int E,
+                                                        int32_t* __restrict__ offsets,
+                                                        int32_t* __restrict__ perm,
+                                                        int32_t* __restrict__ inv_perm) {
+  constexpr int NB = kMaxPermuteExperts + 1;
+  __shared__ int base[NB];
+  __shared__ int chunk_total[NB];
+  __shared__ int warp_cnt[32][NB];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = E + 1;   // buckets: the experts and the invalid-id bucket
+  for (int e = tid; e < B; e += blockDim.x) {
+    base[e] = 0;
+    for (int w = 0; w < 32; ++w) warp_cnt[w][e] = 0;
+  }
+  __syncthreads();
+  auto bucket = [&](int i) {
+    const int v = ids[i];
+    return (v >= 0 && v < E) ? v : E;
+  };
+  for (int i = tid; i < n_slots; i += blockDim.x) atomicAdd(&base[bucket(i)], 1);
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int e = 0; e < B; ++e) {
+      const int c = base[e];
+      if (e <= E) offsets[e] = run;
+      base[e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
+    const int i = c0 + tid;
+    const int e = i < n_slots ? bucket(i) : -1;
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & lt_mask);
+    if (e >= 0 && rank == 0) warp_cnt[warp][e] = __popc(same);
+    __syncthreads();
+    for (int x = tid; x < B; x += blockDim.x) {
+      int run = 0;
+      for (int w = 0; w < 32; ++w) {
+        const int t = warp_cnt[w][x];
+        warp_cnt[w][x] = run;
+        run += t;
+      }
+      chunk_total[x] = run;
+    }
+    __syncthreads();
+    if (e >= 0) {
+      const int pos = base[e] + warp_cnt[warp][e] + rank;
+      perm[pos] = i;
+      inv_perm[i] = pos;
+    }
+    __syncthreads();
+    for (int x = tid; x < B; x += blockDim.x) {
+      base[x] += chunk_total[x];
+      for (int w = 0; w < 32; ++w) warp_cnt[w][x] = 0;
+    }
+    __syncthreads();
+  }
+}
+
+// a_perm[r] = a[perm[r] / topk]: one warp per row, 16-byte vectors.
+__global__ void gather_rows_kernel(const uint4* __restrict__ a, const int32_t* __restrict__ perm,
+                                   uint4* __restrict__ a_perm, int rows, int topk, int vecs) {
+  const int warps = blockDim.x >> 5;
+  const int r = blockIdx.x * warps + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const int src = perm[r] / topk;
+  const uint4* s = a + (long long)src * vecs;
+  uint4* d = a_perm + (long long)r * vecs;
+  for (int v = threadIdx.x & 31; v < vecs; v += 32) d[v] = s[v];
+}
+
+cudaError_t launch_moe_permute(const int32_t* ids, int64_t t, int topk, int e, int32_t* offsets,
+                               int32_t* perm, int32_t* inv_perm, const uint16_t* a,
+                               uint16_t* a_perm, int64_t hidden, cudaStream_t stream) {
+  const int n_slots = (int)(t * topk);
+  moe_sort_kernel<<<1, 1024, 0, stream>>>(ids, n_slots, e, offsets, perm, inv_perm);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || n_slots == 0) return err;
+  const int vecs = (int)(hidden * 2 / 16);
+  gather_rows_kernel<<<(n_slots + 7) / 8, 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(a), perm, reinterpret_cast<uint4*>(a_perm), n_slots, topk,
+      vecs);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------- SiLU gate
+// h[r, i] = bf16(silu(g) * u), g = gu[r, i], u = gu[r, inter + i], fp32 math,
+// silu(g) = g / (1 + exp(-g)).  Eight elements per thread.
+__global__ void silu_mul_kernel(const uint16_t* __restrict__ gu, uint16_t* __restrict__ h,
+                                long long rows, int inter) {
+  const int per_row = inter / 8;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * per_row) return;
+  const long long r = idx / per_row;
+  const int c = (int)(idx % per_row) * 8;
+  const uint4 gv = *reinterpret_cast<const uint4*>(gu + r * 2 * inter + c);
+  const uint4 uv = *reinterpret_cast<const uint4*>(gu + r * 2 * inter + inter + c);
+  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+  const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uv);
+  uint4 ov;
+  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&ov);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 g = __bfloat1622float2(g2[i]);
+    const float2 u = __bfloat1622float2(u2[i]);
+    const float s0 = g.x / (1.f + expf(-g.x));
+    const float s1 = g.y / (1.f + expf(-g.y));
+    o2[i] = __floats2bfloat162_rn(s0 * u.x, s1 * u.y);
+  }
+  *reinterpret_cast<uint4*>(h + r * inter + c) = ov;
+}
+
+cudaError_t launch_silu_mul(const uint16_t* gu, int64_t rows, int64_t inter, uint16_t* h,
+                            cudaStream_t stream) {
+  const long long total = rows * (inter / 8);
+  if (total == 0) return cudaSuccess;
+  silu_mul_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(gu, h, rows, (int)inter);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------- combine
+// y[t, :] = bf16(sum_j w[t, j] * y2[inv_perm[t*topk + j], :]), fp32, j in order.
+__global__ void combine_kernel(const uint16_t* __restrict__ y2, const int32_t* __restrict__ inv_perm,
+                               const float* __restrict__ w, uint16_t* __restrict__ y, int topk,
+                               int hidden) {
+  const int t = blockIdx.x;
+  const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
+  if (c >= hidden) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < topk; ++j) {
+    const float wj = w[(long long)t * topk + j];
+    const int r = inv_perm[(long long)t * topk + j];
+    const uint4 v = *reinterpret_cast<const uint4*>(y2 + (long long)r * hidden + c);
+    const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(v2[i]);
+      acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
+    }
+  }
+  uint4 ov;
+  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&ov);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o2[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+  *reinterpret_cast<uint4*>(y + (long long)t * hidden + c) = ov;
+}
+
+cudaError_t launch_combine(const uint16_t* y2, const int32_t* inv_perm, const float* w, int64_t t,
+                           int topk, int64_t hidden, uint16_t* y, cudaStream_t stream) {
+  if (t == 0) return cudaSuccess;
+  const int threads = 128;
+  dim3 grid((unsigned)t, (unsigned)((hidden / 8 + threads - 1) / threads));
+  combine_kernel<<<grid, threads, 0, stream>>>(y2, inv_perm, w, y, topk, (int)hidden);
+  return cudaGetLastError();
+}
+
+}  // namespace qg

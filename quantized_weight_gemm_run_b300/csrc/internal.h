@@ -1,0 +1,99 @@
+// Library-internal declarations shared by the C ABI layer and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace qg {
+
+constexpr int kTileN = 128;       // output features per tile (MMA M extent)
+constexpr int kTileK = 128;       // K per pipeline stage
+constexpr int kTileBytes = kTileN * kTileK / 2;   // packed 4-bit weights per tile
+constexpr int kNumThreads = 512;  // 16 warps: producer, MMA, TMEM, spare, 8 dequant, 4 epilogue
+constexpr int kASlots = 4;        // TMEM slots for dequantized weight tiles
+constexpr int kASlotCols = 64;    // TMEM columns per slot (128 K x 16 bit)
+constexpr int kStatusTimeout = 1;
+constexpr int kStatusDevice = 2;
+constexpr int kMaxExperts = 1024;      // grouped GEMM
+constexpr int kMaxPermuteExperts = 256; // MoE permutation
+
+// Workspace layout (bytes): [0, 256) status word and padding; then `counters`
+// int32 per 32-column quarter of every output tile; then fp32 partial tiles, two per CTA.
+struct WorkspaceLayout {
+  size_t counters_off, counters_bytes, partials_off, partials_bytes, total;
+};
+
+WorkspaceLayout workspace_layout(int64_t max_tiles, int grid, int block_tok);
+
+struct W4A16Params {
+  const uint8_t* w;          // tiled weights (all experts)
+  const uint16_t* s;         // tiled scales
+  const uint8_t* z;          // tiled zero points or null
+  const uint16_t* bias;      // [E, N] or null
+  uint16_t* c;               // [rows, N]
+  int rows;                  // M (dense) or total permuted rows (grouped)
+  int n, k;
+  int kt, nt;                // k-tiles, n-tiles
+  int st;                    // scale groups per k-tile
+  int group;                 // group size
+  int has_zp;
+  const int* expert_offsets; // device [E+1] or null (dense)
+  int num_experts;
+  long long w_expert_stride; // bytes
+  long long s_expert_stride; // uint16 elements
+  long long z_expert_stride; // bytes
+  float* partials;
+  int* counters;
+  int* status;
+  long long max_tiles;
+  int stages;
+  int stage_bytes;
+  int off_w, off_s, off_z;   // within a stage
+  int smem_bytes;            // total dynamic shared memory
+  unsigned long long wait_limit_ns;
+};
+
+// Host-side plan for one W4A16 launch.
+struct W4A16Plan {
+  int block_tok;
+  int stages;
+  int grid;
+  int st;
+  int stage_bytes, off_w, off_s, off_z, smem_bytes;
+};
+
+int device_sm_count();
+W4A16Plan plan_w4a16(int block_tok, int stages, int max_ctas, int64_t units, int group,
+                     int has_zp);
+cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const W4A16Params& p, int block_tok,
+                         bool fp16, bool grouped, int grid, cudaStream_t stream);
+
+cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
+                             const int32_t* qzeros, uint8_t* w_out, uint16_t* s_out,
+                             uint8_t* z_out, int64_t n, int64_t k, int group, int signed_q,
+                             int experts, cudaStream_t stream);
+
+cudaError_t launch_debug_dequant(const uint8_t* w, const uint16_t* s, const uint8_t* z,
+                                 uint16_t* out, int64_t n, int64_t k, int group, int has_zp,
+                                 bool fp16, cudaStream_t stream);
+
+cudaError_t launch_act_quant_fp8(const uint16_t* x, int64_t m, int64_t k, uint8_t* a8,
+                                 float* scale, cudaStream_t stream);
+
+cudaError_t launch_moe_permute(const int32_t* ids, int64_t t, int topk, int e, int32_t* offsets,
+                               int32_t* perm, int32_t* inv_perm, const uint16_t* a,
+                               uint16_t* a_perm, int64_t hidden, cudaStream_t stream);
+
+cudaError_t launch_silu_mul(const uint16_t* gu, int64_t rows, int64_t inter, uint16_t* h,
+                            cudaStream_t stream);
+
+cudaError_t launch_combine(const uint16_t* y2, const int32_t* inv_perm, const float* w, int64_t t,
+                           int topk, int64_t hidden, uint16_t* y, cudaStream_t stream);
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                    uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+}  // namespace qg

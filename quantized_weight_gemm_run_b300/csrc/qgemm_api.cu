@@ -1,0 +1,589 @@
+// The C ABI (include/qgemm.h): validation, the B300 tuning heuristic, plans,
+// tensor maps and launches.  Host code only; the kernels live in the other
+// translation units.
+//
+// The three-config split (layer / compute / tuning), the device heuristic
+// that picks a tuning per input-size range, and the explicit rejection of
+// unsupported combinations follow the Humming pages (kinachrichten.com,
+// "Wie die Architektur funktioniert"; retrivium.ai, "vLLM Humming: why
+// shared quantization still needs specialized kernels", section "The
+// architectural gain is a smaller maintenance surface").  The plan record
+// written by qgemm_describe_plan follows the compatibility record of the
+// retrivium.ai retrospective on the format-kernel contract (section "A
+// compatibility example"): representation, activation type, device and shape,
+// and which implementation serves them.
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/qgemm.h"
+#include "internal.h"
+
+namespace qg {
+
+static thread_local std::string g_last_error;
+static unsigned long long g_wait_limit_ns = 1000000000ull;
+
+static qgemm_status fail(qgemm_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+static qgemm_status ok() {
+  g_last_error.clear();
+  return QGEMM_OK;
+}
+
+static qgemm_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(QGEMM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Per-device properties, queried once per device (up to 64 devices).
+struct DeviceProps {
+  int sms = 0, max_smem = 0, major = 0, minor = 0;
+};
+
+static const DeviceProps* device_props() {
+  static DeviceProps props[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::call_once(once[dev], [dev] {
+    DeviceProps& d = props[dev];
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+  });
+  return props[dev].sms > 0 ? &props[dev] : nullptr;
+}
+
+int device_sm_count() {
+  const DeviceProps* d = device_props();
+  return d ? d->sms : 0;
+}
+
+static int device_max_smem() {
+  const DeviceProps* d = device_props();
+  return d ? d->max_smem : 0;
+}
+
+static bool device_is_sm103() {
+  const DeviceProps* d = device_props();
+  return d && d->major == 10 && d->minor == 3;
+}
+
+// ------------------------------------------------------------ validation
+
+static qgemm_status check_layer(const qgemm_layer_config* L) {
+  if (!L) return fail(QGEMM_ERR_INVALID_ARG, "layer config is NULL");
+  if (L->n <= 0 || L->k <= 0) return fail(QGEMM_ERR_INVALID_ARG, "n and k must be positive");
+  if (L->num_experts < 1) return fail(QGEMM_ERR_INVALID_ARG, "num_experts must be >= 1");
+  if (L->num_experts > kMaxExperts)
+    return fail(QGEMM_ERR_UNSUPPORTED, "num_experts %d exceeds %d", L->num_experts, kMaxExperts);
+  if (L->n % kTileN || L->k % kTileK)
+    return fail(QGEMM_ERR_UNSUPPORTED, "n and k must be multiples of 128 (got n=%lld k=%lld)",
+                (long long)L->n, (long long)L->k);
+  if (L->n > (1 << 20) || L->k > (1 << 20))
+    return fail(QGEMM_ERR_UNSUPPORTED, "n or k above 2^20");
+  if (L->has_bias != 0 && L->has_bias != 1)
+    return fail(QGEMM_ERR_INVALID_ARG, "has_bias must be 0 or 1");
+  switch (L->weight_format) {
+    case QGEMM_W_INT4_SYM:
+    case QGEMM_W_UINT4_ZP: {
+      if (L->act_dtype != QGEMM_FP16 && L->act_dtype != QGEMM_BF16)
+        return fail(QGEMM_ERR_UNSUPPORTED, "W4A16 needs fp16 or bf16 activations");
+      if (L->out_dtype != L->act_dtype)
+        return fail(QGEMM_ERR_UNSUPPORTED, "W4A16 output dtype must equal the activation dtype");
+      if (L->scale_format != QGEMM_S_FP16 && L->scale_format != QGEMM_S_BF16)
+        return fail(QGEMM_ERR_UNSUPPORTED, "W4A16 scales must be fp16 or bf16");
+      if ((L->scale_format == QGEMM_S_FP16) != (L->act_dtype == QGEMM_FP16))
+        return fail(QGEMM_ERR_UNSUPPORTED,
+                    "W4A16 scale dtype must equal the activation dtype (dequant runs in it)");
+      const int g = L->group_size;
+      const bool g_ok = g == 32 || g == 64 || (g >= 128 && g % 128 == 0);
+      if (!g_ok) return fail(QGEMM_ERR_UNSUPPORTED, "group size %d not in {32, 64, 128j}", g);
+      if (L->k % g) return fail(QGEMM_ERR_UNSUPPORTED, "k must be a multiple of the group size");
+      if (L->weight_format == QGEMM_W_INT4_SYM && L->zero_format != QGEMM_Z_NONE)
+        return fail(QGEMM_ERR_UNSUPPORTED, "symmetric INT4 takes no zero points");
+      if (L->weight_format == QGEMM_W_UINT4_ZP && L->zero_format != QGEMM_Z_UINT4)
+        return fail(QGEMM_ERR_UNSUPPORTED, "UINT4 needs uint4 zero points");
+      return ok();
+    }
+    case QGEMM_W_MXFP4:
+      if (L->zero_format != QGEMM_Z_NONE)
+        return fail(QGEMM_ERR_UNSUPPORTED, "MXFP4 takes no zero points");
+      if (L->scale_format != QGEMM_S_E8M0 || L->group_size != 32)
+        return fail(QGEMM_ERR_UNSUPPORTED, "MXFP4 needs e8m0 scales per 32 k");
+      if (L->act_dtype != QGEMM_FP8E4M3 || L->out_dtype != QGEMM_BF16)
+        return fail(QGEMM_ERR_UNSUPPORTED, "MXFP4 runs against e4m3 activations, bf16 output");
+      return fail(QGEMM_ERR_UNSUPPORTED, "the W4A8-MXFP4 GEMM is not available in this build");
+    default:
+      return fail(QGEMM_ERR_UNSUPPORTED, "unknown weight format %d", L->weight_format);
+  }
+}
+
+static qgemm_status check_compute(const qgemm_compute_config* C, const qgemm_layer_config* L,
+                                  bool grouped_call) {
+  if (!C) return fail(QGEMM_ERR_INVALID_ARG, "compute config is NULL");
+  if (C->batch_invariant != 0)
+    return fail(QGEMM_ERR_UNSUPPORTED, "batch-invariant mode is not available");
+  if (C->gemm_type != (grouped_call ? QGEMM_GEMM_GROUPED : QGEMM_GEMM_DENSE))
+    return fail(QGEMM_ERR_INVALID_ARG, "gemm_type does not match the entry point");
+  if (!grouped_call && L->num_experts != 1)
+    return fail(QGEMM_ERR_INVALID_ARG, "a dense GEMM needs num_experts = 1");
+  return ok();
+}
+
+static int st_of(int group) { return group < kTileK ? kTileK / group : 1; }
+
+// ------------------------------------------------------------ plans
+
+WorkspaceLayout workspace_layout(int64_t max_tiles, int grid, int block_tok) {
+  WorkspaceLayout w;
+  w.counters_off = 256;
+  w.counters_bytes = ((size_t)max_tiles * 4 * sizeof(int) + 255) & ~size_t(255);
+  w.partials_off = w.counters_off + w.counters_bytes;
+  w.partials_bytes = (size_t)2 * grid * block_tok * kTileN * sizeof(float);
+  w.total = w.partials_off + w.partials_bytes;
+  return w;
+}
+
+static int heuristic_block_tok(int64_t rows_per_group) {
+  if (rows_per_group <= 16) return 16;
+  if (rows_per_group <= 32) return 32;
+  if (rows_per_group <= 64) return 64;
+  return 128;
+}
+
+// Pipeline stage geometry: [activation tile][weights][scales][zeros], 1 KB aligned.
+static void stage_geometry(int bt, int st, int has_zp, int* stage_bytes, int* off_w,
+                           int* off_s, int* off_z) {
+  const int act = bt * kTileK * 2;
+  *off_w = act;
+  *off_s = act + kTileBytes;
+  *off_z = *off_s + st * kTileN * 2;
+  const int end = *off_z + (has_zp ? st * kTileN : 0);
+  *stage_bytes = (end + 1023) & ~1023;
+}
+
+static int fixed_smem(int stages, int experts) {
+  // alignment slack + barriers + shared state + grouped prefix arrays
+  return 1024 + (2 * stages + 2 * kASlots + 4 + 1) * 8 + 32 + 2 * (experts + 1) * 4 + 64;
+}
+
+struct Plan {
+  int bt, stages, grid, st, stage_bytes, off_w, off_s, off_z, smem;
+  int64_t max_tiles;
+  WorkspaceLayout ws;
+};
+
+static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_config* T,
+                              int64_t rows, bool grouped, Plan* P) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return fail(QGEMM_ERR_CUDA, "no CUDA device");
+  const int E = L->num_experts;
+  int bt = (T && T->block_tok) ? T->block_tok
+                               : heuristic_block_tok(grouped ? (rows + E - 1) / E : rows);
+  if (bt != 16 && bt != 32 && bt != 64 && bt != 128)
+    return fail(QGEMM_ERR_UNSUPPORTED, "block_tok %d not in {16, 32, 64, 128}", bt);
+  if (T && (T->cta_pair != 0)) return fail(QGEMM_ERR_UNSUPPORTED, "cta_pair is reserved");
+  if (T && T->split_k != 0 && T->split_k != 1)
+    return fail(QGEMM_ERR_INVALID_ARG, "split_k must be 0 or 1");
+  const int st = st_of(L->group_size);
+  const int has_zp = L->zero_format == QGEMM_Z_UINT4;
+  int stage_bytes, off_w, off_s, off_z;
+  stage_geometry(bt, st, has_zp, &stage_bytes, &off_w, &off_s, &off_z);
+  const int smem_cap = device_max_smem();
+  int stages = (T && T->stages) ? T->stages : 16;
+  if (stages < 2 || stages > 16) return fail(QGEMM_ERR_INVALID_ARG, "stages must be in [2, 16]");
+  while (stages > 2 && stages * stage_bytes + fixed_smem(stages, E) > smem_cap) --stages;
+  const int smem = stages * stage_bytes + fixed_smem(stages, E);
+  if (smem > smem_cap) return fail(QGEMM_ERR_UNSUPPORTED, "tile does not fit shared memory");
+  const int64_t kt = L->k / kTileK, nt = L->n / kTileN;
+  int64_t tiles_bound;
+  if (grouped)
+    tiles_bound = ((rows + bt - 1) / bt + E) * nt;
+  else
+    tiles_bound = ((rows + bt - 1) / bt) * nt;
+  if (tiles_bound >= (int64_t(1) << 31))
+    return fail(QGEMM_ERR_UNSUPPORTED, "problem has more than 2^31 output tiles");
+  int grid = sms;
+  if (T && T->max_ctas > 0 && T->max_ctas < grid) grid = T->max_ctas;
+  if (!grouped) {
+    const int64_t units = tiles_bound * kt;
+    if (units < grid) grid = (int)(units > 0 ? units : 1);
+    if (T && T->split_k == 1 && tiles_bound < grid) grid = (int)(tiles_bound > 0 ? tiles_bound : 1);
+  }
+  P->bt = bt;
+  P->stages = stages;
+  P->grid = grid;
+  P->st = st;
+  P->stage_bytes = stage_bytes;
+  P->off_w = off_w;
+  P->off_s = off_s;
+  P->off_z = off_z;
+  P->smem = smem;
+  P->max_tiles = tiles_bound;
+  P->ws = workspace_layout(tiles_bound, grid, bt);
+  return ok();
+}
+
+// ------------------------------------------------------------ tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                    uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ the W4A16 run
+
+static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_config* T,
+                              bool grouped, const int32_t* offsets, int64_t rows, const void* a,
+                              const void* w, const void* s, const void* z, const void* bias,
+                              void* c, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (rows < 0) return fail(QGEMM_ERR_INVALID_ARG, "row count is negative");
+  if (rows > (1 << 30)) return fail(QGEMM_ERR_UNSUPPORTED, "row count above 2^30");
+  if (rows == 0) return ok();
+  if (!device_is_sm103()) return fail(QGEMM_ERR_UNSUPPORTED, "this library runs on sm_103 only");
+  const bool has_zp = L->zero_format == QGEMM_Z_UINT4;
+  if (!a || !w || !s || !c || (has_zp && !z) || (L->has_bias && !bias) || (grouped && !offsets))
+    return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!has_zp && z) return fail(QGEMM_ERR_INVALID_ARG, "zero points given for a format without");
+  if (!L->has_bias && bias) return fail(QGEMM_ERR_INVALID_ARG, "bias given with has_bias = 0");
+  if (!aligned16(a) || !aligned16(w) || !aligned16(s) || !aligned16(c) || (z && !aligned16(z)) ||
+      (bias && !aligned16(bias)) || !aligned16(workspace))
+    return fail(QGEMM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  Plan P;
+  qgemm_status st = make_plan(L, T, rows, grouped, &P);
+  if (st != QGEMM_OK) return st;
+  if (!workspace || ws_bytes < P.ws.total)
+    return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", P.ws.total,
+                ws_bytes);
+  const bool fp16 = L->act_dtype == QGEMM_FP16;
+  CUtensorMap tmap;
+  if (!encode_tmap_2d(&tmap, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      a, (uint64_t)L->k, (uint64_t)rows, (uint64_t)L->k * 2, 64, (uint32_t)P.bt,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+    return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the activation tensor");
+  size_t wb, sb, zb;
+  qgemm_packed_sizes(L, &wb, &sb, &zb);
+  const int E = L->num_experts;
+  W4A16Params p;
+  memset(&p, 0, sizeof(p));
+  p.w = static_cast<const uint8_t*>(w);
+  p.s = static_cast<const uint16_t*>(s);
+  p.z = static_cast<const uint8_t*>(z);
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.c = static_cast<uint16_t*>(c);
+  p.rows = (int)rows;
+  p.n = (int)L->n;
+  p.k = (int)L->k;
+  p.kt = (int)(L->k / kTileK);
+  p.nt = (int)(L->n / kTileN);
+  p.st = P.st;
+  p.group = L->group_size;
+  p.has_zp = has_zp ? 1 : 0;
+  p.expert_offsets = offsets;
+  p.num_experts = E;
+  p.w_expert_stride = (long long)(wb / E);
+  p.s_expert_stride = (long long)(sb / E / 2);
+  p.z_expert_stride = (long long)(has_zp ? zb / E : 0);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.status = reinterpret_cast<int*>(ws);
+  p.counters = reinterpret_cast<int*>(ws + P.ws.counters_off);
+  p.partials = reinterpret_cast<float*>(ws + P.ws.partials_off);
+  p.max_tiles = P.max_tiles;
+  p.stages = P.stages;
+  p.stage_bytes = P.stage_bytes;
+  p.off_w = P.off_w;
+  p.off_s = P.off_s;
+  p.off_z = P.off_z;
+  p.smem_bytes = P.smem;
+  p.wait_limit_ns = g_wait_limit_ns;
+  cudaError_t e = launch_w4a16(tmap, p, P.bt, fp16, grouped, P.grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "W4A16 GEMM launch");
+  return ok();
+}
+
+}  // namespace qg
+
+using namespace qg;
+
+extern "C" {
+
+qgemm_status qgemm_packed_sizes(const qgemm_layer_config* layer, size_t* w_bytes,
+                                size_t* s_bytes, size_t* z_bytes) {
+  qgemm_status st = check_layer(layer);
+  if (st != QGEMM_OK) return st;
+  const size_t E = (size_t)layer->num_experts;
+  const size_t tiles = (size_t)(layer->n / kTileN) * (size_t)(layer->k / kTileK);
+  const size_t stv = (size_t)st_of(layer->group_size);
+  if (w_bytes) *w_bytes = E * tiles * kTileBytes;
+  if (s_bytes) *s_bytes = E * tiles * stv * kTileN * 2;
+  if (z_bytes) *z_bytes = layer->zero_format == QGEMM_Z_UINT4 ? E * tiles * stv * kTileN : 0;
+  return ok();
+}
+
+qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qweight,
+                                const void* scales, const void* qzeros, void* w_out,
+                                void* s_out, void* z_out, void* stream) {
+  qgemm_status st = check_layer(layer);
+  if (st != QGEMM_OK) return st;
+  const bool has_zp = layer->zero_format == QGEMM_Z_UINT4;
+  if (!qweight || !scales || !w_out || !s_out || (has_zp && (!qzeros || !z_out)))
+    return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!has_zp && (qzeros || z_out))
+    return fail(QGEMM_ERR_INVALID_ARG, "zero-point tensors given for a format without");
+  if (!aligned16(w_out) || !aligned16(s_out) || !aligned16(qweight) || (z_out && !aligned16(z_out)))
+    return fail(QGEMM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  cudaError_t e = launch_repack_w4(
+      static_cast<const int32_t*>(qweight), static_cast<const uint16_t*>(scales),
+      static_cast<const int32_t*>(qzeros), static_cast<uint8_t*>(w_out),
+      static_cast<uint16_t*>(s_out), static_cast<uint8_t*>(z_out), layer->n, layer->k,
+      layer->group_size, layer->weight_format == QGEMM_W_INT4_SYM ? 1 : 0, layer->num_experts,
+      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "repack launch");
+  return ok();
+}
+
+qgemm_status qgemm_workspace_size(const qgemm_layer_config* layer,
+                                  const qgemm_compute_config* compute,
+                                  const qgemm_tuning_config* tuning, int64_t m, size_t* bytes) {
+  if (!bytes) return fail(QGEMM_ERR_INVALID_ARG, "bytes is NULL");
+  qgemm_status st = check_layer(layer);
+  if (st != QGEMM_OK) return st;
+  const bool grouped = compute && compute->gemm_type == QGEMM_GEMM_GROUPED;
+  st = check_compute(compute, layer, grouped);
+  if (st != QGEMM_OK) return st;
+  if (m < 0) return fail(QGEMM_ERR_INVALID_ARG, "m is negative");
+  Plan P;
+  st = make_plan(layer, tuning, m > 0 ? m : 1, grouped, &P);
+  if (st != QGEMM_OK) return st;
+  *bytes = P.ws.total;
+  return ok();
+}
+
+qgemm_status qgemm_workspace_init(void* workspace, size_t bytes, void* stream) {
+  if (!workspace || bytes == 0) return fail(QGEMM_ERR_INVALID_ARG, "empty workspace");
+  cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "workspace memset");
+  return ok();
+}
+
+qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_config* compute,
+                       const qgemm_tuning_config* tuning, int64_t m, const void* a,
+                       const float* a_scale, const void* w, const void* s, const void* z,
+                       const void* bias, void* c, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  qgemm_status st = check_layer(layer);
+  if (st != QGEMM_OK) return st;
+  st = check_compute(compute, layer, false);
+  if (st != QGEMM_OK) return st;
+  if (a_scale) return fail(QGEMM_ERR_INVALID_ARG, "a_scale is only used by the W4A8 path");
+  return run_w4a16(layer, tuning, false, nullptr, m, a, w, s, z, bias, c, workspace,
+                   workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
+                               const qgemm_compute_config* compute,
+                               const qgemm_tuning_config* tuning, const int32_t* expert_offsets,
+                               int64_t total_rows, const void* a, const float* a_scale,
+                               const void* w, const void* s, const void* z, const void* bias,
+                               void* c, void* workspace, size_t workspace_bytes, void* stream) {
+  qgemm_status st = check_layer(layer);
+  if (st != QGEMM_OK) return st;
+  st = check_compute(compute, layer, true);
+  if (st != QGEMM_OK) return st;
+  if (a_scale) return fail(QGEMM_ERR_INVALID_ARG, "a_scale is only used by the W4A8 path");
+  return run_w4a16(layer, tuning, true, expert_offsets, total_rows, a, w, s, z, bias, c,
+                   workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+qgemm_status qgemm_quantize_act_fp8(const void* x, int64_t m, int64_t k, void* a8,
+                                    float* a_scale, void* stream) {
+  if (m < 0 || k <= 0) return fail(QGEMM_ERR_INVALID_ARG, "bad shape");
+  if (m == 0) return ok();
+  if (!x || !a8 || !a_scale) return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
+  cudaError_t e = launch_act_quant_fp8(static_cast<const uint16_t*>(x), m, k,
+                                       static_cast<uint8_t*>(a8), a_scale,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "activation quantization launch");
+  return ok();
+}
+
+qgemm_status qgemm_moe_permute(const int32_t* topk_ids, int64_t t, int32_t topk, int32_t e,
+                               int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                               const void* a, void* a_perm, int64_t hidden, void* stream) {
+  if (t < 0 || topk <= 0 || e <= 0 || hidden <= 0)
+    return fail(QGEMM_ERR_INVALID_ARG, "bad shape");
+  if (e > kMaxPermuteExperts)
+    return fail(QGEMM_ERR_UNSUPPORTED, "at most %d experts", kMaxPermuteExperts);
+  if (hidden % 8) return fail(QGEMM_ERR_UNSUPPORTED, "hidden must be a multiple of 8");
+  if (t * topk > (1 << 28)) return fail(QGEMM_ERR_UNSUPPORTED, "too many slots");
+  if (!offsets || (t > 0 && (!topk_ids || !perm || !inv_perm || !a || !a_perm)))
+    return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if ((a && !aligned16(a)) || (a_perm && !aligned16(a_perm)))
+    return fail(QGEMM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  cudaError_t err = launch_moe_permute(topk_ids, t, topk, e, offsets, perm, inv_perm,
+                                       static_cast<const uint16_t*>(a),
+                                       static_cast<uint16_t*>(a_perm), hidden,
+                                       static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "MoE permute launch");
+  return ok();
+}
+
+qgemm_status qgemm_moe_silu_mul(const void* gu, int64_t rows, int64_t inter, void* h,
+                                void* stream) {
+  if (rows < 0 || inter <= 0 || inter % 8) return fail(QGEMM_ERR_INVALID_ARG, "bad shape");
+  if (rows == 0) return ok();
+  if (!gu || !h || !aligned16(gu) || !aligned16(h))
+    return fail(QGEMM_ERR_INVALID_ARG, "pointers must be non-NULL and 16-byte aligned");
+  cudaError_t err = launch_silu_mul(static_cast<const uint16_t*>(gu), rows, inter,
+                                    static_cast<uint16_t*>(h), static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "SiLU launch");
+  return ok();
+}
+
+qgemm_status qgemm_moe_combine(const void* y2, const int32_t* inv_perm,
+                               const float* topk_weights, int64_t t, int32_t topk,
+                               int64_t hidden, void* y, void* stream) {
+  if (t < 0 || topk <= 0 || hidden <= 0 || hidden % 8)
+    return fail(QGEMM_ERR_INVALID_ARG, "bad shape");
+  if (t == 0) return ok();
+  if (!y2 || !inv_perm || !topk_weights || !y || !aligned16(y2) || !aligned16(y))
+    return fail(QGEMM_ERR_INVALID_ARG, "pointers must be non-NULL and 16-byte aligned");
+  cudaError_t err = launch_combine(static_cast<const uint16_t*>(y2), inv_perm, topk_weights, t,
+                                   topk, hidden, static_cast<uint16_t*>(y),
+                                   static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "combine launch");
+  return ok();
+}
+
+qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* w, const void* s,
+                                 const void* z, void* out_kn, void* stream) {
+  qgemm_status st = check_layer(layer);
+  if (st != QGEMM_OK) return st;
+  const bool has_zp = layer->zero_format == QGEMM_Z_UINT4;
+  if (!w || !s || !out_kn || (has_zp && !z))
+    return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
+  cudaError_t e = launch_debug_dequant(
+      static_cast<const uint8_t*>(w), static_cast<const uint16_t*>(s),
+      static_cast<const uint8_t*>(z), static_cast<uint16_t*>(out_kn), layer->n, layer->k,
+      layer->group_size, has_zp ? 1 : 0, layer->act_dtype == QGEMM_FP16,
+      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
+  return ok();
+}
+
+qgemm_status qgemm_check_status(void* workspace, void* stream) {
+  if (!workspace) return fail(QGEMM_ERR_INVALID_ARG, "workspace is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (word != 0) {
+    const int zero = 0;
+    e = cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    if (word & kStatusTimeout) return fail(QGEMM_ERR_TIMEOUT, "a kernel gave up a bounded wait");
+    return fail(QGEMM_ERR_DEVICE, "a kernel reported inconsistent inputs (status %d)", word);
+  }
+  return ok();
+}
+
+void qgemm_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
+
+qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
+                                 const qgemm_compute_config* compute, int64_t m, char* buf,
+                                 size_t len) {
+  std::string rec;
+  qgemm_status st = check_layer(layer);
+  const bool grouped = compute && compute->gemm_type == QGEMM_GEMM_GROUPED;
+  if (st == QGEMM_OK) st = check_compute(compute, layer, grouped);
+  if (st != QGEMM_OK) {
+    rec = std::string("rejected: ") + g_last_error;
+  } else {
+    Plan P;
+    st = make_plan(layer, nullptr, m > 0 ? m : 1, grouped, &P);
+    if (st != QGEMM_OK) {
+      rec = std::string("rejected: ") + g_last_error;
+    } else {
+      static const char* wf[] = {"int4_sym", "uint4_zp", "mxfp4"};
+      static const char* dt[] = {"fp16", "bf16", "fp8e4m3"};
+      char tmp[512];
+      snprintf(tmp, sizeof(tmp),
+               "kernel=w4a16_tcgen05_swapab%s weights=%s group=%d act=%s out=%s n=%lld k=%lld "
+               "m=%lld experts=%d block_tok=%d stages=%d grid=%d smem=%d workspace=%zu "
+               "device=sm_103",
+               grouped ? "_grouped" : "", wf[layer->weight_format], layer->group_size,
+               dt[layer->act_dtype], dt[layer->out_dtype], (long long)layer->n,
+               (long long)layer->k, (long long)m, layer->num_experts, P.bt, P.stages, P.grid,
+               P.smem, P.ws.total);
+      rec = tmp;
+    }
+  }
+  if (buf && len) {
+    strncpy(buf, rec.c_str(), len - 1);
+    buf[len - 1] = 0;
+  }
+  return st;
+}
+
+const char* qgemm_status_string(qgemm_status s) {
+  switch (s) {
+    case QGEMM_OK: return "QGEMM_OK";
+    case QGEMM_ERR_INVALID_ARG: return "QGEMM_ERR_INVALID_ARG";
+    case QGEMM_ERR_UNSUPPORTED: return "QGEMM_ERR_UNSUPPORTED";
+    case QGEMM_ERR_WORKSPACE: return "QGEMM_ERR_WORKSPACE";
+    case QGEMM_ERR_CUDA: return "QGEMM_ERR_CUDA";
+    case QGEMM_ERR_TIMEOUT: return "QGEMM_ERR_TIMEOUT";
+    case QGEMM_ERR_DEVICE: return "QGEMM_ERR_DEVICE";
+    default: return "QGEMM_UNKNOWN_STATUS";
+  }
+}
+
+const char* qgemm_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+// Weight preprocessing: standard format -> the GEMM kernel's tiled layout.
+//
+// The Humming preprocessing step checks parameters, pads dimensions and
+// repacks tensors for the target kernel (kinachrichten.com, "Wie die
+// Architektur funktioniert"); repacking rearranges without changing what the
+// stored values mean (retrivium.ai, "vLLM Humming: why shared quantization
+// still needs specialized kernels", section "Representation answers a
+// different question").  Target layout (per expert; KT = K/128 k-tiles):
+//
+//   weights  8192-byte block per (n-tile, k-tile), n-tile major.  Block =
+//            512 16-byte vectors, vector (qd*4 + j)*32 + t = row 32qd + t of
+//            the tile, k = 32j .. 32j+31; word w of the vector holds 8 k, the
+//            nibble at position p holding k-offset {0,2,4,6,1,3,5,7}[p], so a
+//            single 0x000F000F mask extracts two consecutive k.  INT4 codes
+//            are stored offset binary (q + 8).
+//   scales   128 * ST 16-bit words per block (ST = max(1, 128/g)): word
+//            sg*128 + r is the scale of row r for the sg-th group of the tile.
+//   zeros    128 * ST bytes per block, same order, zero point 0..15.
+//
+// Every thread writes one output vector / element; reads of the standard
+// tensors are coalesced along N.
+
+#include "internal.h"
+
+namespace qg {
+
+__global__ void repack_weights_kernel(const int32_t* __restrict__ qweight, uint4* __restrict__ out,
+                                      int n, int k, int signed_q, long long total) {
+  const long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (vec >= total) return;
+  const int KT = k / kTileK, NT = n / kTileN;
+  const long long per_expert = (long long)NT * KT * 512;
+  const long long ex = vec / per_expert;
+  const long long rem = vec - ex * per_expert;
+  const long long blk = rem / 512;
+  const int v = (int)(rem % 512);
+  const int nt = (int)(blk / KT), kt = (int)(blk % KT);
+  const int t = v & 31, j = (v >> 5) & 3, qd = v >> 7;
+  const int col = nt * kTileN + qd * 32 + t;
+  const long long word_row0 = (long long)(kt * kTileK + j * 32) / 8;   // first K/8 row
+  const int32_t* src = qweight + ex * (long long)(k / 8) * n;
+  uint32_t o[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t in = (uint32_t)src[(word_row0 + w) * n + col];
+    uint32_t r = 0;
+    // nibble position p takes input nibble {0,2,4,6,1,3,5,7}[p]
+    r |= ((in >> 0) & 0xFu) << 0;
+    r |= ((in >> 8) & 0xFu) << 4;
+    r |= ((in >> 16) & 0xFu) << 8;
+    r |= ((in >> 24) & 0xFu) << 12;
+    r |= ((in >> 4) & 0xFu) << 16;
+    r |= ((in >> 12) & 0xFu) << 20;
+    r |= ((in >> 20) & 0xFu) << 24;
+    r |= ((in >> 28) & 0xFu) << 28;
+    if (signed_q) r ^= 0x88888888u;   // two's complement nibble -> q + 8
+    o[w] = r;
+  }
+  out[vec] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void repack_scales_kernel(const uint16_t* __restrict__ scales,
+                                     const int32_t* __restrict__ qzeros, uint16_t* __restrict__ s_out,
+                                     uint8_t* __restrict__ z_out, int n, int k, int group,
+                                     long long total) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= total) return;
+  const int KT = k / kTileK, NT = n / kTileN;
+  const int st = group < kTileK ? kTileK / group : 1;
+  const long long per_expert = (long long)NT * KT * st * kTileN;
+  const long long ex = idx / per_expert;
+  const long long rem = idx - ex * per_expert;
+  const int r = (int)(rem % kTileN);
+  const long long rest = rem / kTileN;
+  const int sg = (int)(rest % st);
+  const long long blk = rest / st;
+  const int nt = (int)(blk / KT), kt = (int)(blk % KT);
+  const int kk = kt * kTileK + sg * (group < kTileK ? group : kTileK);
+  const int grp = kk / group;
+  const int col = nt * kTileN + r;
+  const long long groups = k / group;
+  s_out[idx] = scales[ex * groups * n + (long long)grp * n + col];
+  if (z_out) {
+    const uint32_t word = (uint32_t)qzeros[ex * groups * (n / 8) + (long long)grp * (n / 8) + col / 8];
+    z_out[idx] = (uint8_t)((word >> (4 * (col % 8))) & 0xFu);
+  }
+}
+
+cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
+                             const int32_t* qzeros, uint8_t* w_out, uint16_t* s_out,
+                             uint8_t* z_out, int64_t n, int64_t k, int group, int signed_q,
+                             int experts, cudaStream_t stream) {
+  const int threads = 256;
+  const long long vecs = (long long)experts * (n / kTileN) * (k / kTileK) * 512;
+  repack_weights_kernel<<<(unsigned)((vecs + threads - 1) / threads), threads, 0, stream>>>(
+      qweight, reinterpret_cast<uint4*>(w_out), (int)n, (int)k, signed_q, vecs);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int st = group < kTileK ? kTileK / group : 1;
+  const long long elems = (long long)experts * (n / kTileN) * (k / kTileK) * st * kTileN;
+  repack_scales_kernel<<<(unsigned)((elems + threads - 1) / threads), threads, 0, stream>>>(
+      scales, qzeros, s_out, z_out, (int)n, (int)k, group, elems);
+  return cudaGetLastError();
+}
+
+}  // namespace qg

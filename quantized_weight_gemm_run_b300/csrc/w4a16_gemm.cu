@@ -1,0 +1,653 @@
+// W4A16 GEMM for sm_103a: C[M, N] = A[M, K] . W^[K, N], W^ = adt((q - z) * s).
+//
+// The Humming pages assemble their kernels from scheduling, data movement,
+// dequantization/scaling, tensor-core compute and output processing
+// (kinachrichten.com, "Kompilierzeiten und geraetespezifisches Tuning"), with
+// a TMA + UMMA pipeline for larger batches and a multi-stage cp.async + MMA
+// pipeline for small ones (same article, section "Kompilierzeiten...",
+// paragraph on small vs larger batch sizes).  This kernel is the B300 design
+// of those five components, one kernel for every M:
+//
+//   swap-AB:  the MMA computes D[n, m] = W^[n, :] . A[m, :], so the 128 output
+//             features of a tile are the MMA M extent and the tokens are the
+//             MMA N extent (16 .. 128), which keeps the tensor core busy at
+//             tiny M.
+//   data movement (warp 0): plain bulk copies of the pre-tiled 4-bit weight,
+//             scale and zero blocks, and a TMA tensor load (128-byte swizzle)
+//             of the activation tile, into a ring of shared-memory stages.
+//   dequant (warps 4..11): each thread owns one output feature (one TMEM
+//             lane), unpacks 32 nibbles per 16-byte vector with LOP3 against a
+//             magic exponent, subtracts (magic + z) exactly and multiplies by
+//             the scale once (the single rounding of the dequant definition),
+//             and stores the 16-bit pairs straight into tensor memory, where
+//             tcgen05.mma reads them as its A operand.  No shared-memory
+//             round trip for the dequantized weights.
+//   tensor core (warp 1): one thread issues tcgen05.mma kind::f16 with A in
+//             TMEM and the activation tile as the shared-memory B operand,
+//             accumulating in fp32 in TMEM (two accumulator buffers).
+//   output (warps 12..15): tcgen05.ld of the accumulator, bias, rounding,
+//             stores; or an fp32 partial tile plus a fixed-order reduction by
+//             the last-arriving CTA when a tile's K range was split.
+//   scheduling: a persistent grid of at most one CTA per SM walks whole tiles
+//             round-robin, then splits the remaining tiles' K ranges evenly
+//             across all CTAs (stream-K), so every SM streams the same number
+//             of weight bytes at any M.  The grouped (MoE) variant derives its
+//             tiles from the expert offsets on the device.
+//
+// Every wait is bounded (see mbar_wait); a CTA that gives up records a
+// timeout in the workspace status word and drains its own copies before it
+// frees tensor memory and exits.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qg {
+
+namespace {
+
+struct WorkItem {
+  int tile;
+  int k0, k1;
+};
+
+// Whole tiles round-robin (waves), then an even split of the remaining tiles'
+// K-tiles ("units") across the first Gs = min(G, U) CTAs, so that every CTA
+// taking part in the split owns at least one unit; the CTAs that share a tile
+// are then exactly cta_of_unit(first unit) .. cta_of_unit(last unit).
+struct Schedule {
+  long long T;     // tiles
+  int KT;          // k-tiles per tile
+  int G, c;        // grid size, this CTA
+  long long W;     // full waves of whole tiles
+  long long U;     // stream-K units
+  long long Gs;    // CTAs sharing the stream-K units
+  long long it, u, u_end;
+
+  __device__ void init(long long T_, int KT_, int G_, int c_) {
+    T = T_;
+    KT = KT_;
+    G = G_;
+    c = c_;
+    W = T / G;
+    U = (T - W * G) * KT;
+    Gs = U < G ? U : G;
+    it = 0;
+    if (c < Gs) {
+      u = sk_begin(c);
+      u_end = sk_begin(c + 1);
+    } else {
+      u = u_end = 0;
+    }
+  }
+  __device__ long long sk_begin(long long cta) const { return (cta * U) / Gs; }
+  // CTA whose unit range holds unit uu.
+  __device__ long long cta_of_unit(long long uu) const { return ((uu + 1) * Gs - 1) / U; }
+
+  __device__ bool next(WorkItem& wi) {
+    if (it < W) {
+      wi.tile = (int)(c + it * G);
+      wi.k0 = 0;
+      wi.k1 = KT;
+      ++it;
+      return true;
+    }
+    if (u >= u_end) return false;
+    long long tl = u / KT;
+    int k0 = (int)(u % KT);
+    long long seg_end = min((tl + 1) * KT, u_end);
+    wi.tile = (int)(W * G + tl);
+    wi.k0 = k0;
+    wi.k1 = k0 + (int)(seg_end - u);
+    u = seg_end;
+    return true;
+  }
+};
+
+struct SharedState {
+  uint32_t tmem_base;
+  int abort_flag;
+  int pad0;
+  int pad1;
+  long long tiles;     // total tiles (grouped: from offsets)
+};
+
+template <int BT>
+struct TileCoord {
+  int e, row0, rows, nt;
+};
+
+}  // namespace
+
+template <bool FP16>
+__device__ __forceinline__ uint32_t dq_pair(uint32_t bits, uint32_t zero2, uint32_t scale2) {
+  if constexpr (FP16) {
+    __half2 x = *reinterpret_cast<__half2*>(&bits);
+    __half2 zz = *reinterpret_cast<__half2*>(&zero2);
+    __half2 ss = *reinterpret_cast<__half2*>(&scale2);
+    __half2 r = __hmul2(__hsub2(x, zz), ss);
+    return *reinterpret_cast<uint32_t*>(&r);
+  } else {
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&bits);
+    __nv_bfloat162 zz = *reinterpret_cast<__nv_bfloat162*>(&zero2);
+    __nv_bfloat162 ss = *reinterpret_cast<__nv_bfloat162*>(&scale2);
+    __nv_bfloat162 r = __hmul2(__hsub2(x, zz), ss);
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));   // (a & b) | c
+  return d;
+}
+
+// 32 nibbles (one 16-byte vector of the tiled layout) -> 16 packed 16-bit pairs.
+// Nibble positions p and p+4 of a word hold consecutive k, so one mask
+// extracts a (k, k+1) pair straight into the low mantissa bits of two
+// 16-bit floats whose exponent encodes `magic` (128 for bf16, 1024 for fp16,
+// where the unit in the last place is 1): the pair reads magic + u exactly.
+template <bool FP16>
+__device__ __forceinline__ void dequant_vec(const uint4 v, uint32_t zero2, uint32_t scale2,
+                                            uint32_t (&out)[16]) {
+  constexpr uint32_t magic = FP16 ? 0x64006400u : 0x43004300u;
+  const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t x = lop3_and_or(wds[w] >> (4 * i), 0x000F000Fu, magic);
+      out[w * 4 + i] = dq_pair<FP16>(x, zero2, scale2);
+    }
+  }
+}
+
+template <bool FP16>
+__device__ __forceinline__ uint16_t to_out(float v) {
+  if constexpr (FP16) {
+    __half h = __float2half_rn(v);
+    return *reinterpret_cast<uint16_t*>(&h);
+  } else {
+    __nv_bfloat16 h = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t*>(&h);
+  }
+}
+
+template <bool FP16>
+__device__ __forceinline__ float from_out(uint16_t b) {
+  if constexpr (FP16) {
+    return __half2float(*reinterpret_cast<__half*>(&b));
+  } else {
+    return __bfloat162float(*reinterpret_cast<__nv_bfloat16*>(&b));
+  }
+}
+
+template <int BT, bool FP16, bool GROUPED>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    w4a16_kernel(const __grid_constant__ CUtensorMap tmap_a, const W4A16Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled operand tiles
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int S = p.stages;
+  uint8_t* stage_base = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * p.stage_bytes);
+  uint64_t* full = bars;
+  uint64_t* empty = full + S;
+  uint64_t* a_full = empty + S;
+  uint64_t* a_empty = a_full + kASlots;
+  uint64_t* acc_full = a_empty + kASlots;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  SharedState* sh = reinterpret_cast<SharedState*>(drain + 1);
+  int* mt_prefix = reinterpret_cast<int*>(sh + 1);     // grouped: m-tile prefix [E+1]
+  int* offs = mt_prefix + (GROUPED ? (p.num_experts + 1) : 0);   // grouped: offsets [E+1]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &sh->abort_flag;
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < kASlots; ++i) {
+      mbar_init(&a_full[i], 8);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    mbar_init(drain, 1);
+    sh->abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmap_a);
+  }
+  if (warp == 2) {
+    tmem_alloc(&sh->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == 3) {
+    if constexpr (GROUPED) {
+      // m-tile prefix over experts, from the device-side offsets
+      const int E = p.num_experts;
+      for (int i = lane; i <= E; i += 32) offs[i] = min(max(p.expert_offsets[i], 0), p.rows);
+      __syncwarp();
+      if (lane == 0) {
+        // offsets are caller data: clamp to [0, rows] and make them monotone so
+        // that no tile reaches outside the row range
+        offs[0] = 0;
+        for (int e = 1; e <= E; ++e) offs[e] = max(offs[e], offs[e - 1]);
+        int acc = 0;
+        mt_prefix[0] = 0;
+        for (int e = 0; e < E; ++e) {
+          int r = offs[e + 1] - offs[e];
+          if (r < 0) r = 0;
+          acc += (r + BT - 1) / BT;
+          mt_prefix[e + 1] = acc;
+        }
+        long long T = (long long)acc * p.nt;
+        if (T > p.max_tiles) {   // offsets inconsistent with the workspace bound
+          atomicOr(p.status, kStatusDevice);
+          T = 0;
+        }
+        sh->tiles = T;
+      }
+    } else {
+      if (lane == 0) sh->tiles = (long long)((p.rows + BT - 1) / BT) * p.nt;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+  const long long T = sh->tiles;
+
+  Schedule sched;
+  sched.init(T, p.kt, gridDim.x, blockIdx.x);
+
+  auto coords = [&](int tile) {
+    TileCoord<BT> tc;
+    const int mtg = tile / p.nt;
+    tc.nt = tile - mtg * p.nt;
+    if constexpr (GROUPED) {
+      int lo = 0, hi = p.num_experts;   // find e: mt_prefix[e] <= mtg < mt_prefix[e+1]
+      while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (mt_prefix[mid] <= mtg) lo = mid; else hi = mid;
+      }
+      tc.e = lo;
+      tc.row0 = offs[lo] + (mtg - mt_prefix[lo]) * BT;
+      tc.rows = min(BT, offs[lo + 1] - tc.row0);
+    } else {
+      tc.e = 0;
+      tc.row0 = mtg * BT;
+      tc.rows = min(BT, p.rows - tc.row0);
+    }
+    return tc;
+  };
+
+  const uint32_t act_bytes = BT * kTileK * 2;
+  const uint32_t w_bytes = kTileBytes;
+  const uint32_t s_bytes = p.st * kTileN * 2;
+  const uint32_t z_bytes = p.has_zp ? p.st * kTileN : 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------ producer
+    if (elect_one()) {
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      WorkItem wi;
+      bool ok = true;
+      while (ok && sched.next(wi)) {
+        const TileCoord<BT> tc = coords(wi.tile);
+        const uint8_t* wbase = p.w + tc.e * p.w_expert_stride;
+        const uint16_t* sbase = p.s + tc.e * p.s_expert_stride;
+        const uint8_t* zbase = p.has_zp ? p.z + tc.e * p.z_expert_stride : nullptr;
+        for (int kt = wi.k0; kt < wi.k1; ++kt) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status, lim, kStatusTimeout)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sp = stage_base + stage * p.stage_bytes;
+          mbar_arrive_expect_tx(&full[stage], act_bytes + w_bytes + s_bytes + z_bytes);
+          tma_load_2d_hint(sp, &tmap_a, &full[stage], kt * kTileK, tc.row0, pol_keep);
+          tma_load_2d_hint(sp + BT * 128, &tmap_a, &full[stage], kt * kTileK + 64, tc.row0,
+                           pol_keep);
+          const long long blk = (long long)tc.nt * p.kt + kt;
+          bulk_load(sp + p.off_w, wbase + blk * kTileBytes, w_bytes, &full[stage], pol_stream);
+          bulk_load(sp + p.off_s, sbase + blk * p.st * kTileN, s_bytes, &full[stage], pol_stream);
+          if (p.has_zp)
+            bulk_load(sp + p.off_z, zbase + blk * p.st * kTileN, z_bytes, &full[stage],
+                      pol_stream);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // drain: never leave a copy in flight into shared memory we are leaving
+      for (int s = 0; s < S && s < issued; ++s) {
+        long long last = s + ((issued - 1 - s) / S) * S;
+        uint32_t par = (uint32_t)((last / S) & 1);
+        volatile int no_abort = 0;
+        mbar_wait(&full[s], par, &no_abort, nullptr, 100000000ull, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      const uint32_t idesc = idesc_f16(FP16 ? 0u : 1u, BT);
+      int stage = 0, slot = 0, acc = 0;
+      uint32_t phase = 0, aphase = 0, accphase = 0;
+      WorkItem wi;
+      bool ok = true;
+      while (ok && sched.next(wi)) {
+        if (!mbar_wait(&acc_empty[acc], accphase ^ 1, abort_flag, p.status, lim,
+                       kStatusTimeout))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + kASlots * kASlotCols + acc * BT;
+        for (int kt = wi.k0; kt < wi.k1; ++kt) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim, kStatusTimeout) ||
+              !mbar_wait(&a_full[slot], aphase, abort_flag, p.status, lim, kStatusTimeout)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b0 = smem_u32(stage_base + stage * p.stage_bytes);
+#pragma unroll
+          for (int ks = 0; ks < kTileK / 16; ++ks) {
+            const uint32_t boff = (ks >> 2) * (BT * 128) + (ks & 3) * 32;
+            mma_ts_f16(d_tmem, tmem_base + slot * kASlotCols + ks * 8,
+                       smem_desc_sw128(b0 + boff), idesc, (kt > wi.k0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          mma_commit(&a_empty[slot]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (++slot == kASlots) {
+            slot = 0;
+            aphase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          accphase ^= 1;
+        }
+      }
+      // every MMA this thread issued completes before TMEM is released
+      mma_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, &no_abort, nullptr, 100000000ull, 0);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------ dequant
+    const int q = warp & 3;             // TMEM lane quadrant
+    const int h = (warp - 4) >> 2;      // which half of the k-tile
+    const int row = q * 32 + lane;      // output feature within the tile
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    constexpr uint32_t magic16 = FP16 ? 0x6400u : 0x4300u;
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, aphase = 0;
+    WorkItem wi;
+    bool ok = true;
+    while (ok && sched.next(wi)) {
+      for (int kt = wi.k0; kt < wi.k1; ++kt) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim, kStatusTimeout) ||
+            !mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim, kStatusTimeout)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sp = stage_base + stage * p.stage_bytes;
+        const uint4* wv = reinterpret_cast<const uint4*>(sp + p.off_w);
+        const uint16_t* sv = reinterpret_cast<const uint16_t*>(sp + p.off_s);
+        const uint8_t* zv = sp + p.off_z;
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * h + jj;     // 32-wide k chunk
+          const int sg = p.group < kTileK ? (32 * j) / p.group : 0;
+          const uint4 v = wv[(q * 4 + j) * 32 + lane];
+          const uint32_t sbits = sv[sg * kTileN + row];
+          const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
+          const uint32_t zero2 = (magic16 + zq) * 0x00010001u;
+          const uint32_t scale2 = sbits * 0x00010001u;
+          uint32_t out[16];
+          dequant_vec<FP16>(v, zero2, scale2, out);
+          tmem_st16(tmem_base + lane_addr + slot * kASlotCols + j * 16, out);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[slot]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++slot == kASlots) {
+          slot = 0;
+          aphase ^= 1;
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int col = q * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    int acc = 0;
+    uint32_t accphase = 0;
+    WorkItem wi;
+    while (sched.next(wi)) {
+      const TileCoord<BT> tc = coords(wi.tile);
+      const bool whole = (wi.k0 == 0 && wi.k1 == p.kt);
+      if (!mbar_wait(&acc_full[acc], accphase, abort_flag, p.status, lim, kStatusTimeout)) break;
+      tc_fence_after();
+      const int n = tc.nt * kTileN + col;
+      float bias = 0.f;
+      if (p.bias) bias = from_out<FP16>(p.bias[(long long)tc.e * p.n + n]);
+      const uint32_t tbase = tmem_base + lane_addr + kASlots * kASlotCols + acc * BT;
+      // partial slot of this CTA for this segment (split tiles only)
+      const long long tl = wi.tile - sched.W * sched.G;
+      const long long u_start = tl * p.kt;
+      float* my_part = nullptr;
+      if (!whole) {
+        const int which = (sched.sk_begin(blockIdx.x) >= u_start) ? 0 : 1;
+        my_part = p.partials + ((long long)(2 * blockIdx.x + which)) * (BT * kTileN);
+      }
+#pragma unroll 1
+      for (int mc = 0; mc < BT / 16; ++mc) {
+        uint32_t v[16];
+        tmem_ld16(tbase + mc * 16, v);
+        tmem_wait_ld();
+        if (whole) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int m = mc * 16 + i;
+            if (m < tc.rows)
+              p.c[(long long)(tc.row0 + m) * p.n + n] =
+                  to_out<FP16>(__uint_as_float(v[i]) + bias);
+          }
+        } else {
+          // partial tile, column-major [col][BT]: this thread's column is contiguous
+          float4* dst = reinterpret_cast<float4*>(my_part + col * BT + mc * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        accphase ^= 1;
+      }
+      if (!whole) {
+        // Fixed-order split-K reduction, per 32-column quadrant: the warp of
+        // the last CTA to arrive for this quadrant of the tile sums every
+        // contributor's partial in CTA order (independent of arrival order).
+        const long long c_first = sched.cta_of_unit(u_start);
+        const long long c_last = sched.cta_of_unit(u_start + p.kt - 1);
+        const int contributors = (int)(c_last - c_first + 1);
+        int* counter = &p.counters[(long long)wi.tile * 4 + q];
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) old = atomicAdd(counter, 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == contributors - 1) {
+          __threadfence();
+          // 16 rows per pass; the partials of up to 3 contributors are loaded
+          // before any is added, then summed in CTA order (fixed rounding order)
+          for (int m0 = 0; m0 < tc.rows; m0 += 16) {
+            float4 acc4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (long long cc0 = c_first; cc0 <= c_last; cc0 += 3) {
+              float4 v4[3][4];
+#pragma unroll
+              for (int i = 0; i < 3; ++i) {
+                const long long cc = cc0 + i;
+                if (cc <= c_last) {
+                  const int which = (sched.sk_begin(cc) >= u_start) ? 0 : 1;
+                  const float4* src4 = reinterpret_cast<const float4*>(
+                      p.partials + ((long long)(2 * cc + which)) * (BT * kTileN) + col * BT + m0);
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) v4[i][j] = __ldcg(src4 + j);
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < 3; ++i) {
+                if (cc0 + i <= c_last) {
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    acc4[j].x += v4[i][j].x;
+                    acc4[j].y += v4[i][j].y;
+                    acc4[j].z += v4[i][j].z;
+                    acc4[j].w += v4[i][j].w;
+                  }
+                }
+              }
+            }
+            const float* accf = reinterpret_cast<const float*>(acc4);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              if (m0 + i < tc.rows)
+                p.c[(long long)(tc.row0 + m0 + i) * p.n + n] = to_out<FP16>(accf[i] + bias);
+            }
+          }
+          if (lane == 0) *counter = 0;   // ready for the next launch
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem_base, 512);
+}
+
+// ---------------------------------------------------------------- host side
+
+template <int BT, bool FP16, bool GROUPED>
+static cudaError_t launch_t(const CUtensorMap& tmap, const W4A16Params& p, int grid,
+                            cudaStream_t stream) {
+  auto kern = w4a16_kernel<BT, FP16, GROUPED>;
+  static int attr_set = 0;   // largest dynamic shared memory size enabled so far
+  if (p.smem_bytes > attr_set) {
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+    if (err != cudaSuccess) return err;
+    attr_set = p.smem_bytes;
+  }
+  kern<<<grid, kNumThreads, p.smem_bytes, stream>>>(tmap, p);
+  return cudaGetLastError();
+}
+
+template <bool FP16, bool GROUPED>
+static cudaError_t launch_bt(const CUtensorMap& tmap, const W4A16Params& p, int bt, int grid,
+                             cudaStream_t stream) {
+  switch (bt) {
+    case 16: return launch_t<16, FP16, GROUPED>(tmap, p, grid, stream);
+    case 32: return launch_t<32, FP16, GROUPED>(tmap, p, grid, stream);
+    case 64: return launch_t<64, FP16, GROUPED>(tmap, p, grid, stream);
+    case 128: return launch_t<128, FP16, GROUPED>(tmap, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const W4A16Params& p, int block_tok,
+                         bool fp16, bool grouped, int grid, cudaStream_t stream) {
+  if (fp16)
+    return grouped ? launch_bt<true, true>(tmap_a, p, block_tok, grid, stream)
+                   : launch_bt<true, false>(tmap_a, p, block_tok, grid, stream);
+  return grouped ? launch_bt<false, true>(tmap_a, p, block_tok, grid, stream)
+                 : launch_bt<false, false>(tmap_a, p, block_tok, grid, stream);
+}
+
+// ------------------------------------------------------------ debug dequant
+
+// out[k, n] = the value the GEMM kernel feeds the tensor core for W^[k, n].
+template <bool FP16>
+__global__ void debug_dequant_kernel(const uint8_t* w, const uint16_t* s, const uint8_t* z,
+                                     uint16_t* out, int n, int k, int group, int has_zp) {
+  const int KT = k / kTileK;
+  const long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // one 16-byte vector
+  const long long total = (long long)(n / kTileN) * KT * 512;
+  if (vec >= total) return;
+  const long long blk = vec / 512;
+  const int v = (int)(vec % 512);
+  const int nt = (int)(blk / KT), kt = (int)(blk % KT);
+  const int t = v & 31, j = (v >> 5) & 3, q = v >> 7;
+  const int row = q * 32 + t;
+  const int st = group < kTileK ? kTileK / group : 1;
+  const int sg = group < kTileK ? (32 * j) / group : 0;
+  const uint4 wv = reinterpret_cast<const uint4*>(w)[vec];
+  const uint32_t sbits = s[(blk * st + sg) * kTileN + row];
+  const uint32_t zq = has_zp ? (uint32_t)z[(blk * st + sg) * kTileN + row] : 8u;
+  constexpr uint32_t magic16 = FP16 ? 0x6400u : 0x4300u;
+  uint32_t o[16];
+  dequant_vec<FP16>(wv, (magic16 + zq) * 0x00010001u, sbits * 0x00010001u, o);
+  const int nn = nt * kTileN + row;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const int kk = kt * kTileK + j * 32 + 2 * c;
+    out[(long long)kk * n + nn] = (uint16_t)(o[c] & 0xFFFF);
+    out[(long long)(kk + 1) * n + nn] = (uint16_t)(o[c] >> 16);
+  }
+}
+
+cudaError_t launch_debug_dequant(const uint8_t* w, const uint16_t* s, const uint8_t* z,
+                                 uint16_t* out, int64_t n, int64_t k, int group, int has_zp,
+                                 bool fp16, cudaStream_t stream) {
+  const long long total = (n / kTileN) * (k / kTileK) * 512;
+  const int threads = 256;
+  const long long blocks = (total + threads - 1) / threads;
+  if (fp16)
+    debug_dequant_kernel<true><<<blocks, threads, 0, stream>>>(w, s, z, out, (int)n, (int)k,
+                                                                group, has_zp);
+  else
+    debug_dequant_kernel<false><<<blocks, threads, 0, stream>>>(w, s, z, out, (int)n, (int)k,
+                                                                 group, has_zp);
+  return cudaGetLastError();
+}
+
+}  // namespace qg

@@ -1,0 +1,93 @@
+"""CPU-side checks of the library boundary: the shared library loads, exports
+every entry point the header declares, and its host-side validation rejects
+bad configurations without needing a GPU."""
+
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "qgemm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qgemm_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def Q():
+    from quantized_weight_gemm_run_b300 import qgemm
+    return qgemm
+
+
+def test_header_declares_the_boundary():
+    names = _header_functions()
+    for required in ("qgemm_pack_weights", "qgemm_run", "qgemm_grouped_run"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(Q):
+    missing = [n for n in _header_functions() if not hasattr(Q.lib, n)]
+    assert not missing, missing
+
+
+def test_binding_has_every_entry_point(Q):
+    missing = [n for n in _header_functions() if not callable(getattr(Q, n, None))]
+    assert not missing, missing
+
+
+def _layer(Q, **kw):
+    d = dict(n=4096, k=4096, group_size=128, weight_format=Q.QGEMM_W_INT4_SYM,
+             scale_format=Q.QGEMM_S_FP16, zero_format=Q.QGEMM_Z_NONE, act_dtype=Q.QGEMM_FP16,
+             out_dtype=Q.QGEMM_FP16, has_bias=0, num_experts=1)
+    d.update(kw)
+    return Q.layer_config(**d)
+
+
+def test_packed_sizes_host_only(Q):
+    st, w, s, z = Q.qgemm_packed_sizes(_layer(Q))
+    assert st == Q.QGEMM_OK
+    assert w == 4096 * 4096 // 2 and s == 4096 * 32 * 2 and z == 0
+    st, w, s, z = Q.qgemm_packed_sizes(_layer(Q, weight_format=Q.QGEMM_W_UINT4_ZP,
+                                              zero_format=Q.QGEMM_Z_UINT4, group_size=32,
+                                              num_experts=3))
+    assert st == Q.QGEMM_OK and w == 3 * 4096 * 2048 and s == 3 * 4096 * 128 * 2
+    assert z == 3 * 4096 * 128
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(n=100), "UNSUPPORTED"),
+    (dict(k=1000), "UNSUPPORTED"),
+    (dict(group_size=48), "UNSUPPORTED"),
+    (dict(group_size=384), "UNSUPPORTED"),          # does not divide K = 4096
+    (dict(zero_format=1), "UNSUPPORTED"),           # zeros with symmetric INT4
+    (dict(out_dtype=1), "UNSUPPORTED"),             # W4A16 output dtype differs
+    (dict(scale_format=1), "UNSUPPORTED"),          # scale dtype differs from act dtype
+    (dict(weight_format=2, scale_format=2, group_size=32, act_dtype=2, out_dtype=1,
+          zero_format=1), "UNSUPPORTED"),          # zero points with MXFP4
+    (dict(weight_format=9), "UNSUPPORTED"),
+    (dict(n=0), "INVALID_ARG"),
+    (dict(num_experts=0), "INVALID_ARG"),
+    (dict(has_bias=2), "INVALID_ARG"),
+])
+def test_rejections_are_clear(Q, bad, code):
+    st, *_ = Q.qgemm_packed_sizes(_layer(Q, **bad))
+    assert Q.status_string(st) == f"QGEMM_ERR_{code}"
+    assert Q.last_error()
+
+
+def test_status_strings(Q):
+    assert Q.status_string(Q.QGEMM_OK) == "QGEMM_OK"
+    assert Q.status_string(Q.QGEMM_ERR_TIMEOUT) == "QGEMM_ERR_TIMEOUT"
+    assert Q.status_string(99) == "QGEMM_UNKNOWN_STATUS"
+
+
+def test_pack_rejects_missing_pointers_before_launch(Q):
+    assert Q.qgemm_pack_weights(_layer(Q), None, None, None, None, None, None, 0) == \
+        Q.QGEMM_ERR_INVALID_ARG
+    asym = _layer(Q, weight_format=Q.QGEMM_W_UINT4_ZP, zero_format=Q.QGEMM_Z_UINT4,
+                  act_dtype=Q.QGEMM_BF16, out_dtype=Q.QGEMM_BF16, scale_format=Q.QGEMM_S_BF16)
+    # zero-point tensors are required for UINT4
+    assert Q.qgemm_pack_weights(asym, 16, 16, None, 16, 16, None, 0) == Q.QGEMM_ERR_INVALID_ARG

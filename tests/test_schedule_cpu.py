@@ -1,0 +1,57 @@
+"""The persistent GEMM kernel's work split, restated on the host: whole tiles
+round-robin over the grid, then the remaining tiles' K-tiles split evenly
+over min(grid, units) CTAs.  Checks that every (tile, k-tile) unit is owned by
+exactly one CTA, that the CTAs sharing a split tile are exactly the
+contiguous range the kernel's reducer sums over, and that the partial-tile
+slots (two per CTA) never collide."""
+
+import itertools
+
+import pytest
+
+
+def schedule(T, KT, G):
+    W = T // G
+    U = (T - W * G) * KT
+    Gs = U if U < G else G
+
+    def sk_begin(c):
+        return (c * U) // Gs
+
+    def cta_of_unit(u):
+        return ((u + 1) * Gs - 1) // U
+
+    owner, slots, items_of = {}, set(), {}
+    for c in range(G):
+        items = [(c + it * G, 0, KT) for it in range(W)]
+        if c < Gs and U > 0:
+            u, ue = sk_begin(c), sk_begin(c + 1)
+            assert ue > u, "a CTA of the split owns no unit"
+            while u < ue:
+                tl, k0 = divmod(u, KT)
+                se = min((tl + 1) * KT, ue)
+                items.append((W * G + tl, k0, k0 + se - u))
+                u = se
+        items_of[c] = items
+        for t, k0, k1 in items:
+            for k in range(k0, k1):
+                assert (t, k) not in owner
+                owner[(t, k)] = c
+            if not (k0 == 0 and k1 == KT):
+                us = (t - W * G) * KT
+                which = 0 if sk_begin(c) >= us else 1
+                assert (c, which) not in slots
+                slots.add((c, which))
+    return W, cta_of_unit, owner
+
+
+@pytest.mark.parametrize("T,KT,G", list(itertools.product(
+    [1, 2, 3, 8, 32, 149, 150, 256, 300, 4096], [1, 2, 3, 32, 64], [1, 7, 37, 148])))
+def test_schedule_partition(T, KT, G):
+    W, cta_of_unit, owner = schedule(T, KT, G)
+    assert len(owner) == T * KT
+    for t in range(W * G, T):
+        us = (t - W * G) * KT
+        owners = {owner[(t, k)] for k in range(KT)}
+        if len(owners) > 1:
+            assert owners == set(range(cta_of_unit(us), cta_of_unit(us + KT - 1) + 1))
