@@ -198,6 +198,31 @@ qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_conf
                        void* stream);
 
 /*
+ * qgemm_run without a workspace argument, for callers that cannot allocate
+ * device memory when they run a GEMM (code running under an allocator or
+ * memory-pool lock it does not own, plugins inside a host program that owns
+ * every device byte, start-up or recovery paths that must not touch the
+ * allocator).  The Humming pages have no counterpart to this entry point.
+ * It allocates nothing: the split-K scratch is a fixed 32 MiB array inside
+ * the library that every GPU loading the library holds until the process
+ * exits.  Arguments and results are those of qgemm_run (dense GEMMs only).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents: calls
+ *     that can overlap on the GPU race and must be serialised by the caller.
+ *     Each call zeroes the status word and the tile counters it uses
+ *     (cudaMemsetAsync on `stream`) before it launches.
+ *   - A problem needing more than 32 MiB of scratch is rejected with
+ *     QGEMM_ERR_UNSUPPORTED before anything is launched (qgemm_last_error
+ *     names the size); kernel-side timeouts are not reported by this call.
+ */
+qgemm_status qgemm_run_noalloc(const qgemm_layer_config* layer,
+                               const qgemm_compute_config* compute,
+                               const qgemm_tuning_config* tuning, int64_t m, const void* a,
+                               const float* a_scale, const void* w, const void* s, const void* z,
+                               const void* bias, void* c, void* stream);
+
+/*
  * Grouped (MoE) quantized GEMM over router-permuted rows: for each expert e,
  * rows [offsets[e], offsets[e+1]) of A are multiplied by expert e's weights.
  *   expert_offsets device int32 [E+1], non-decreasing, offsets[0] = 0,

@@ -92,6 +92,13 @@ cudaError_t launch_silu_mul(const uint16_t* gu, int64_t rows, int64_t inter, uin
 cudaError_t launch_combine(const uint16_t* y2, const int32_t* inv_perm, const float* w, int64_t t,
                            int topk, int64_t hidden, uint16_t* y, cudaStream_t stream);
 
+// Host helpers shared with the allocation-free entry point: set the calling
+// thread's error message, and the bytes of a dense GEMM's workspace that must
+// be zero before a launch (status word and split-K counters) and in total.
+int set_last_error(int status, const char* message);
+int dense_workspace_bytes(const void* layer, const void* tuning, int64_t m, size_t* must_clear,
+                          size_t* total);
+
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                     uint32_t box_outer, CUtensorMapSwizzle swizzle);

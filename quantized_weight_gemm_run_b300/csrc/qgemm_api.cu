@@ -345,6 +345,24 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   return ok();
 }
 
+int set_last_error(int status, const char* message) {
+  g_last_error = message;
+  return status;
+}
+
+int dense_workspace_bytes(const void* layer, const void* tuning, int64_t m, size_t* must_clear,
+                          size_t* total) {
+  const qgemm_layer_config* L = static_cast<const qgemm_layer_config*>(layer);
+  qgemm_status st = check_layer(L);
+  if (st != QGEMM_OK) return st;
+  Plan P;
+  st = make_plan(L, static_cast<const qgemm_tuning_config*>(tuning), m > 0 ? m : 1, false, &P);
+  if (st != QGEMM_OK) return st;
+  *must_clear = P.ws.partials_off;
+  *total = P.ws.total;
+  return QGEMM_OK;
+}
+
 }  // namespace qg
 
 using namespace qg;

@@ -77,6 +77,7 @@ _SIGS = {
     "qgemm_workspace_size": [_L, _C, _T, _I64, ctypes.POINTER(_SZ)],
     "qgemm_workspace_init": [_P, _SZ, _P],
     "qgemm_run": [_L, _C, _T, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
+    "qgemm_run_noalloc": [_L, _C, _T, _I64, _P, _P, _P, _P, _P, _P, _P, _P],
     "qgemm_grouped_run": [_L, _C, _T, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "qgemm_quantize_act_fp8": [_P, _I64, _I64, _P, _P, _P],
     "qgemm_moe_permute": [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _I64, _P],
@@ -177,6 +178,12 @@ def qgemm_run(layer, compute, tuning, m, a, a_scale, w, s, z, bias, c, workspace
     return lib.qgemm_run(ctypes.byref(layer), ctypes.byref(compute), _ref(tuning), m, _ptr(a),
                          _ptr(a_scale), _ptr(w), _ptr(s), _ptr(z), _ptr(bias), _ptr(c),
                          _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def qgemm_run_noalloc(layer, compute, tuning, m, a, a_scale, w, s, z, bias, c, stream=None):
+    return lib.qgemm_run_noalloc(ctypes.byref(layer), ctypes.byref(compute), _ref(tuning), m,
+                                 _ptr(a), _ptr(a_scale), _ptr(w), _ptr(s), _ptr(z), _ptr(bias),
+                                 _ptr(c), _stream(stream))
 
 
 def qgemm_grouped_run(layer, compute, tuning, expert_offsets, total_rows, a, a_scale, w, s, z,
