@@ -99,10 +99,22 @@ typedef struct {
   int32_t num_experts;
 } qgemm_layer_config;
 
-/* Compute config: what computation.  batch_invariant is reserved and must be 0. */
+/*
+ * Compute config: what computation.
+ *   gemm_type       QGEMM_GEMM_DENSE or QGEMM_GEMM_GROUPED
+ *   batch_invariant reserved, must be 0
+ *   deterministic   0: when a tile's K range is split across CTAs, the fp32
+ *                   partial sums are added into an L2-resident accumulator by
+ *                   atomic reductions (fastest; the order of those fp32
+ *                   additions, and so the last bit of a result, can differ
+ *                   between runs).  1: the partial sums are added in a fixed
+ *                   CTA order (bitwise reproducible for a given problem,
+ *                   tuning and device).
+ */
 typedef struct {
   int32_t gemm_type;
   int32_t batch_invariant;
+  int32_t deterministic;
 } qgemm_compute_config;
 
 /*
@@ -188,8 +200,8 @@ qgemm_status qgemm_workspace_init(void* workspace, size_t bytes, void* stream);
  *   bias      device [N] in out_dtype, or NULL when has_bias = 0
  *   c         device, [m, N] in out_dtype
  *   workspace device, >= qgemm_workspace_size bytes, zero-initialised once
- * Fixed-order split-K reduction: results are bitwise reproducible for a given
- * (config, m, tuning, device).
+ * With compute->deterministic = 1 the split-K reduction runs in a fixed order
+ * and results are bitwise reproducible for a given (config, m, tuning, device).
  */
 qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_config* compute,
                        const qgemm_tuning_config* tuning, int64_t m, const void* a,
@@ -210,8 +222,8 @@ qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_conf
  *     that device current; make that first call before any stream capture.
  *   - All calls share the array and it keeps the last call's contents: calls
  *     that can overlap on the GPU race and must be serialised by the caller.
- *     Each call zeroes the status word and the tile counters it uses
- *     (cudaMemsetAsync on `stream`) before it launches.
+ *     Each call zeroes the scratch its launch uses (status word, split-K
+ *     counters and accumulators; cudaMemsetAsync on `stream`) first.
  *   - A problem needing more than 32 MiB of scratch is rejected with
  *     QGEMM_ERR_UNSUPPORTED before anything is launched (qgemm_last_error
  *     names the size); kernel-side timeouts are not reported by this call.

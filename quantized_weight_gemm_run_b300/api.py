@@ -35,7 +35,7 @@ class W4A16Linear:
     [E*K/g, N/8] or None: the standard format of ``include/qgemm.h``."""
 
     def __init__(self, qweight, scales, qzeros, n, k, group, act_dtype, num_experts=1,
-                 bias=None, tuning=None):
+                 bias=None, tuning=None, deterministic=False):
         self.n, self.k, self.group, self.num_experts = n, k, group, num_experts
         self.act_dtype = act_dtype
         asym = qzeros is not None
@@ -56,8 +56,9 @@ class W4A16Linear:
         self.bias = bias
         self.tuning = tuning
         self.ws = Workspace(dev)
-        self.dense = Q.compute_config(Q.QGEMM_GEMM_DENSE)
-        self.grouped = Q.compute_config(Q.QGEMM_GEMM_GROUPED)
+        det = 1 if deterministic else 0
+        self.dense = Q.compute_config(Q.QGEMM_GEMM_DENSE, deterministic=det)
+        self.grouped = Q.compute_config(Q.QGEMM_GEMM_GROUPED, deterministic=det)
 
     def __call__(self, a: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
         m = a.shape[0]

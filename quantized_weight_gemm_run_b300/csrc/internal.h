@@ -38,13 +38,15 @@ struct W4A16Params {
   int kt, nt;                // k-tiles, n-tiles
   int st;                    // scale groups per k-tile
   int group;                 // group size
+  int sg_shift;              // scale group of 32-wide k chunk j is j >> sg_shift
   int has_zp;
   const int* expert_offsets; // device [E+1] or null (dense)
   int num_experts;
   long long w_expert_stride; // bytes
   long long s_expert_stride; // uint16 elements
   long long z_expert_stride; // bytes
-  float* partials;
+  float* partials;           // fixed-order: two slots per CTA; atomic: one per split tile
+  int deterministic;         // 1: fixed-order split-K reduction
   int* counters;
   int* status;
   long long max_tiles;

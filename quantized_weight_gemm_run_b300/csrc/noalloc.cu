@@ -15,12 +15,11 @@
 // first call should therefore come before any CUDA stream capture.  All calls
 // share the one array and it keeps what the last call left in it: calls that
 // can overlap on the GPU (different streams, or different host threads) race
-// on it and must be serialised by the caller.  Each call zeroes the status
-// word and the split-K tile counters it needs (cudaMemsetAsync on its stream,
-// which allocates nothing) before the launch; the partial tiles are always
-// written before they are read and need no clearing.  A problem whose scratch
-// exceeds the array is rejected with QGEMM_ERR_UNSUPPORTED before anything is
-// launched.
+// on it and must be serialised by the caller.  Each call zeroes the part of
+// the array its launch needs (status word, split-K tile counters and split-K
+// accumulators; cudaMemsetAsync on its stream, which allocates nothing)
+// before the launch.  A problem whose scratch exceeds the array is rejected
+// with QGEMM_ERR_UNSUPPORTED before anything is launched.
 
 #include <cstdio>
 #include <mutex>

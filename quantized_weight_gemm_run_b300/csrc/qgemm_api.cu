@@ -138,6 +138,8 @@ static qgemm_status check_compute(const qgemm_compute_config* C, const qgemm_lay
   if (!C) return fail(QGEMM_ERR_INVALID_ARG, "compute config is NULL");
   if (C->batch_invariant != 0)
     return fail(QGEMM_ERR_UNSUPPORTED, "batch-invariant mode is not available");
+  if (C->deterministic != 0 && C->deterministic != 1)
+    return fail(QGEMM_ERR_INVALID_ARG, "deterministic must be 0 or 1");
   if (C->gemm_type != (grouped_call ? QGEMM_GEMM_GROUPED : QGEMM_GEMM_DENSE))
     return fail(QGEMM_ERR_INVALID_ARG, "gemm_type does not match the entry point");
   if (!grouped_call && L->num_experts != 1)
@@ -278,7 +280,7 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 // ------------------------------------------------------------ the W4A16 run
 
 static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_config* T,
-                              bool grouped, const int32_t* offsets, int64_t rows, const void* a,
+                              bool deterministic, bool grouped, const int32_t* offsets, int64_t rows, const void* a,
                               const void* w, const void* s, const void* z, const void* bias,
                               void* c, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   if (rows < 0) return fail(QGEMM_ERR_INVALID_ARG, "row count is negative");
@@ -322,6 +324,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.nt = (int)(L->n / kTileN);
   p.st = P.st;
   p.group = L->group_size;
+  p.sg_shift = L->group_size == 32 ? 0 : L->group_size == 64 ? 1 : 2;
   p.has_zp = has_zp ? 1 : 0;
   p.expert_offsets = offsets;
   p.num_experts = E;
@@ -332,6 +335,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.status = reinterpret_cast<int*>(ws);
   p.counters = reinterpret_cast<int*>(ws + P.ws.counters_off);
   p.partials = reinterpret_cast<float*>(ws + P.ws.partials_off);
+  p.deterministic = deterministic ? 1 : 0;
   p.max_tiles = P.max_tiles;
   p.stages = P.stages;
   p.stage_bytes = P.stage_bytes;
@@ -358,7 +362,9 @@ int dense_workspace_bytes(const void* layer, const void* tuning, int64_t m, size
   Plan P;
   st = make_plan(L, static_cast<const qgemm_tuning_config*>(tuning), m > 0 ? m : 1, false, &P);
   if (st != QGEMM_OK) return st;
-  *must_clear = P.ws.partials_off;
+  // the status word and tile counters start at zero, and so do the split-K
+  // accumulators of the atomic reduction
+  *must_clear = P.ws.total;
   *total = P.ws.total;
   return QGEMM_OK;
 }
@@ -438,7 +444,8 @@ qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_conf
   st = check_compute(compute, layer, false);
   if (st != QGEMM_OK) return st;
   if (a_scale) return fail(QGEMM_ERR_INVALID_ARG, "a_scale is only used by the W4A8 path");
-  return run_w4a16(layer, tuning, false, nullptr, m, a, w, s, z, bias, c, workspace,
+  return run_w4a16(layer, tuning, compute->deterministic != 0, false, nullptr, m, a, w, s, z,
+                   bias, c, workspace,
                    workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
@@ -453,7 +460,8 @@ qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
   st = check_compute(compute, layer, true);
   if (st != QGEMM_OK) return st;
   if (a_scale) return fail(QGEMM_ERR_INVALID_ARG, "a_scale is only used by the W4A8 path");
-  return run_w4a16(layer, tuning, true, expert_offsets, total_rows, a, w, s, z, bias, c,
+  return run_w4a16(layer, tuning, compute->deterministic != 0, true, expert_offsets,
+                   total_rows, a, w, s, z, bias, c,
                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 

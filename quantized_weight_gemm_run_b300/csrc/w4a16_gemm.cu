@@ -138,6 +138,30 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t bits, uint32_t zero2, uint3
   }
 }
 
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Fire-and-forget fp32 vector reduction into global memory (performed at L2).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));   // (a & b) | c
@@ -211,67 +235,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   volatile int* abort_flag = &sh->abort_flag;
   const uint64_t lim = p.wait_limit_ns;
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
-    for (int i = 0; i < kASlots; ++i) {
-      mbar_init(&a_full[i], 8);
-      mbar_init(&a_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
-    }
-    mbar_init(drain, 1);
-    sh->abort_flag = 0;
-    fence_barrier_init();
-    prefetch_tmap(&tmap_a);
-  }
-  if (warp == 2) {
-    tmem_alloc(&sh->tmem_base, 512);
-    tmem_relinquish();
-  }
-  if (warp == 3) {
-    if constexpr (GROUPED) {
-      // m-tile prefix over experts, from the device-side offsets
-      const int E = p.num_experts;
-      for (int i = lane; i <= E; i += 32) offs[i] = min(max(p.expert_offsets[i], 0), p.rows);
-      __syncwarp();
-      if (lane == 0) {
-        // offsets are caller data: clamp to [0, rows] and make them monotone so
-        // that no tile reaches outside the row range
-        offs[0] = 0;
-        for (int e = 1; e <= E; ++e) offs[e] = max(offs[e], offs[e - 1]);
-        int acc = 0;
-        mt_prefix[0] = 0;
-        for (int e = 0; e < E; ++e) {
-          int r = offs[e + 1] - offs[e];
-          if (r < 0) r = 0;
-          acc += (r + BT - 1) / BT;
-          mt_prefix[e + 1] = acc;
-        }
-        long long T = (long long)acc * p.nt;
-        if (T > p.max_tiles) {   // offsets inconsistent with the workspace bound
-          atomicOr(p.status, kStatusDevice);
-          T = 0;
-        }
-        sh->tiles = T;
-      }
-    } else {
-      if (lane == 0) sh->tiles = (long long)((p.rows + BT - 1) / BT) * p.nt;
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = sh->tmem_base;
-  const long long T = sh->tiles;
-
-  Schedule sched;
-  sched.init(T, p.kt, gridDim.x, blockIdx.x);
-
   auto coords = [&](int tile) {
     TileCoord<BT> tc;
     const int mtg = tile / p.nt;
@@ -298,43 +261,167 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const uint32_t s_bytes = p.st * kTileN * 2;
   const uint32_t z_bytes = p.has_zp ? p.st * kTileN : 0;
 
+  // ---- producer state (thread 0): one (tile, k-tile) unit per pipeline stage
+  Schedule psched;
+  WorkItem pwi{0, 0, 0};
+  int pkt = 0;
+  bool phave = false;
+  int pstage = 0;
+  uint32_t pphase = 0;
+  long long issued = 0;
+  uint64_t pol_stream = 0, pol_keep = 0;
+  auto pnext = [&]() -> bool {   // advance to the next unit; false when none is left
+    if (phave && ++pkt < pwi.k1) return true;
+    if (!psched.next(pwi)) return false;
+    phave = true;
+    pkt = pwi.k0;
+    return true;
+  };
+  auto issue = [&]() {
+    const TileCoord<BT> tc = coords(pwi.tile);
+    uint8_t* sp = stage_base + pstage * p.stage_bytes;
+    const long long blk = (long long)tc.nt * p.kt + pkt;
+    mbar_arrive_expect_tx(&full[pstage], act_bytes + w_bytes + s_bytes + z_bytes);
+    // weights first: they do not depend on the activations' producer
+    bulk_load(sp + p.off_w, p.w + tc.e * p.w_expert_stride + blk * kTileBytes, w_bytes,
+              &full[pstage], pol_stream);
+    bulk_load(sp + p.off_s, p.s + tc.e * p.s_expert_stride + blk * p.st * kTileN, s_bytes,
+              &full[pstage], pol_stream);
+    if (p.has_zp)
+      bulk_load(sp + p.off_z, p.z + tc.e * p.z_expert_stride + blk * p.st * kTileN, z_bytes,
+                &full[pstage], pol_stream);
+    tma_load_2d_hint(sp, &tmap_a, &full[pstage], pkt * kTileK, tc.row0, pol_keep);
+    tma_load_2d_hint(sp + BT * 128, &tmap_a, &full[pstage], pkt * kTileK + 64, tc.row0,
+                     pol_keep);
+    ++issued;
+    if (++pstage == S) {
+      pstage = 0;
+      pphase ^= 1;
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < kASlots; ++i) {
+      mbar_init(&a_full[i], 4);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    mbar_init(drain, 1);
+    sh->abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmap_a);
+    pol_stream = policy_evict_first();
+    pol_keep = policy_evict_last();
+  }
+  if (warp == 2) {
+    tmem_alloc(&sh->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == 3) {
+    if constexpr (GROUPED) {
+      // m-tile prefix over experts, from the device-side offsets (written by
+      // the previous grid on the stream, so wait for it first)
+      grid_dependency_wait();
+      const int E = p.num_experts;
+      for (int i = lane; i <= E; i += 32) offs[i] = min(max(p.expert_offsets[i], 0), p.rows);
+      __syncwarp();
+      if (lane == 0) {
+        // offsets are caller data: clamp to [0, rows] and make them monotone so
+        // that no tile reaches outside the row range
+        offs[0] = 0;
+        for (int e = 1; e <= E; ++e) offs[e] = max(offs[e], offs[e - 1]);
+        int acc = 0;
+        mt_prefix[0] = 0;
+        for (int e = 0; e < E; ++e) {
+          acc += (offs[e + 1] - offs[e] + BT - 1) / BT;
+          mt_prefix[e + 1] = acc;
+        }
+        long long T = (long long)acc * p.nt;
+        if (T > p.max_tiles) {   // offsets inconsistent with the workspace bound
+          atomicOr(p.status, kStatusDevice);
+          T = 0;
+        }
+        sh->tiles = T;
+      }
+    } else {
+      if (lane == 0) sh->tiles = (long long)((p.rows + BT - 1) / BT) * p.nt;
+    }
+  }
+  // Start-up barrier.  For a dense GEMM the producer warp only arrives (it
+  // needs neither tensor memory nor the grouped tile table), so the weight
+  // stream starts while the other warps wait for the allocation.
+  tc_fence_before();
+  if (!GROUPED && warp == 0) {
+    __syncwarp();
+    asm volatile("bar.arrive 1, %0;" ::"n"(kNumThreads) : "memory");
+  } else {
+    asm volatile("bar.sync 1, %0;" ::"n"(kNumThreads) : "memory");
+  }
+  tc_fence_after();
+  const uint32_t tmem_base = (!GROUPED && warp == 0) ? 0u : sh->tmem_base;
+  const long long T = (!GROUPED && warp == 0)
+                          ? (long long)((p.rows + BT - 1) / BT) * p.nt
+                          : sh->tiles;
+
+  Schedule sched;
+  sched.init(T, p.kt, gridDim.x, blockIdx.x);
+
+  // Programmatic dependent launch: the next grid on the stream may start its
+  // CTAs as soon as SMs free up; everything it reads from this grid is read
+  // after its own grid_dependency_wait.
+  grid_launch_dependents();
+
   if (warp == 0) {
     // ------------------------------------------------ producer
-    if (elect_one()) {
-      const uint64_t pol_stream = policy_evict_first();
-      const uint64_t pol_keep = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      long long issued = 0;
-      WorkItem wi;
-      bool ok = true;
-      while (ok && sched.next(wi)) {
-        const TileCoord<BT> tc = coords(wi.tile);
-        const uint8_t* wbase = p.w + tc.e * p.w_expert_stride;
-        const uint16_t* sbase = p.s + tc.e * p.s_expert_stride;
-        const uint8_t* zbase = p.has_zp ? p.z + tc.e * p.z_expert_stride : nullptr;
-        for (int kt = wi.k0; kt < wi.k1; ++kt) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status, lim, kStatusTimeout)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sp = stage_base + stage * p.stage_bytes;
-          mbar_arrive_expect_tx(&full[stage], act_bytes + w_bytes + s_bytes + z_bytes);
-          tma_load_2d_hint(sp, &tmap_a, &full[stage], kt * kTileK, tc.row0, pol_keep);
-          tma_load_2d_hint(sp + BT * 128, &tmap_a, &full[stage], kt * kTileK + 64, tc.row0,
-                           pol_keep);
-          const long long blk = (long long)tc.nt * p.kt + kt;
-          bulk_load(sp + p.off_w, wbase + blk * kTileBytes, w_bytes, &full[stage], pol_stream);
-          bulk_load(sp + p.off_s, sbase + blk * p.st * kTileN, s_bytes, &full[stage], pol_stream);
-          if (p.has_zp)
-            bulk_load(sp + p.off_z, zbase + blk * p.st * kTileN, z_bytes, &full[stage],
-                      pol_stream);
-          ++issued;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1;
-          }
+    if (lane == 0) {
+      psched.init(T, p.kt, gridDim.x, blockIdx.x);
+      // The packed weights are read-only layer data: the first S stages of
+      // them are requested before waiting for the previous grid on the stream
+      // (which may still be writing this GEMM's activations or workspace);
+      // the activation tiles of those stages follow the wait.
+      int pre = 0;
+      WorkItem pre_wi[16];
+      int pre_kt[16];
+      while (pre < S && pnext()) {
+        const TileCoord<BT> tc = coords(pwi.tile);
+        uint8_t* sp = stage_base + pstage * p.stage_bytes;
+        const long long blk = (long long)tc.nt * p.kt + pkt;
+        mbar_arrive_expect_tx(&full[pstage], act_bytes + w_bytes + s_bytes + z_bytes);
+        bulk_load(sp + p.off_w, p.w + tc.e * p.w_expert_stride + blk * kTileBytes, w_bytes,
+                  &full[pstage], pol_stream);
+        bulk_load(sp + p.off_s, p.s + tc.e * p.s_expert_stride + blk * p.st * kTileN, s_bytes,
+                  &full[pstage], pol_stream);
+        if (p.has_zp)
+          bulk_load(sp + p.off_z, p.z + tc.e * p.z_expert_stride + blk * p.st * kTileN,
+                    z_bytes, &full[pstage], pol_stream);
+        pre_wi[pre] = pwi;
+        pre_kt[pre] = pkt;
+        ++pre;
+        ++issued;
+        if (++pstage == S) {
+          pstage = 0;
+          pphase ^= 1;
         }
+      }
+      grid_dependency_wait();
+      for (int i = 0; i < pre; ++i) {   // stages 0 .. pre-1 of the first ring pass
+        const TileCoord<BT> tc = coords(pre_wi[i].tile);
+        uint8_t* sp = stage_base + i * p.stage_bytes;
+        tma_load_2d_hint(sp, &tmap_a, &full[i], pre_kt[i] * kTileK, tc.row0, pol_keep);
+        tma_load_2d_hint(sp + BT * 128, &tmap_a, &full[i], pre_kt[i] * kTileK + 64, tc.row0,
+                         pol_keep);
+      }
+      while (pnext()) {
+        if (!mbar_wait(&empty[pstage], pphase ^ 1, abort_flag, p.status, lim, kStatusTimeout))
+          break;
+        issue();
       }
       // drain: never leave a copy in flight into shared memory we are leaving
       for (int s = 0; s < S && s < issued; ++s) {
@@ -397,43 +484,55 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------ dequant
+    // Two warps per TMEM lane quadrant; warp group h takes every other k-tile
+    // unit (h = unit index & 1) and dequantizes all 128 k of its 32 rows.
     const int q = warp & 3;             // TMEM lane quadrant
-    const int h = (warp - 4) >> 2;      // which half of the k-tile
+    const int h = (warp - 4) >> 2;      // which units: even (0) or odd (1)
     const int row = q * 32 + lane;      // output feature within the tile
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     constexpr uint32_t magic16 = FP16 ? 0x6400u : 0x4300u;
     int stage = 0, slot = 0;
     uint32_t phase = 0, aphase = 0;
+    long long unit = 0;
     WorkItem wi;
     bool ok = true;
     while (ok && sched.next(wi)) {
-      for (int kt = wi.k0; kt < wi.k1; ++kt) {
-        if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim, kStatusTimeout) ||
-            !mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim, kStatusTimeout)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* sp = stage_base + stage * p.stage_bytes;
-        const uint4* wv = reinterpret_cast<const uint4*>(sp + p.off_w);
-        const uint16_t* sv = reinterpret_cast<const uint16_t*>(sp + p.off_s);
-        const uint8_t* zv = sp + p.off_z;
+      for (int kt = wi.k0; kt < wi.k1; ++kt, ++unit) {
+        if ((unit & 1) == h) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim, kStatusTimeout) ||
+              !mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
+                         kStatusTimeout)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* sp = stage_base + stage * p.stage_bytes;
+          const uint4* wv = reinterpret_cast<const uint4*>(sp + p.off_w);
+          const uint16_t* sv = reinterpret_cast<const uint16_t*>(sp + p.off_s);
+          const uint8_t* zv = sp + p.off_z;
+          // every shared-memory read of the unit first, then the arithmetic
+          uint4 v[4];
+          uint32_t scale2[4], zero2[4];
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * h + jj;     // 32-wide k chunk
-          const int sg = p.group < kTileK ? (32 * j) / p.group : 0;
-          const uint4 v = wv[(q * 4 + j) * 32 + lane];
-          const uint32_t sbits = sv[sg * kTileN + row];
-          const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
-          const uint32_t zero2 = (magic16 + zq) * 0x00010001u;
-          const uint32_t scale2 = sbits * 0x00010001u;
-          uint32_t out[16];
-          dequant_vec<FP16>(v, zero2, scale2, out);
-          tmem_st16(tmem_base + lane_addr + slot * kASlotCols + j * 16, out);
+          for (int j = 0; j < 4; ++j) v[j] = wv[(q * 4 + j) * 32 + lane];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int sg = j >> p.sg_shift;
+            scale2[j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
+            const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
+            zero2[j] = (magic16 + zq) * 0x00010001u;
+          }
+          const uint32_t tbase = tmem_base + lane_addr + slot * kASlotCols;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t out[16];
+            dequant_vec<FP16>(v[j], zero2[j], scale2[j], out);
+            tmem_st16(tbase + j * 16, out);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[slot]);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[slot]);
         if (++stage == S) {
           stage = 0;
           phase ^= 1;
@@ -446,6 +545,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
   } else if (warp >= 12) {
     // ------------------------------------------------ epilogue
+    grid_dependency_wait();   // workspace and output may still be in use upstream
     const int q = warp & 3;
     const int col = q * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
@@ -464,16 +564,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // partial slot of this CTA for this segment (split tiles only)
       const long long tl = wi.tile - sched.W * sched.G;
       const long long u_start = tl * p.kt;
+      // split tiles: fixed-order mode writes this CTA's partial to its own
+      // slot; atomic mode adds it into the tile's accumulator
       float* my_part = nullptr;
       if (!whole) {
-        const int which = (sched.sk_begin(blockIdx.x) >= u_start) ? 0 : 1;
-        my_part = p.partials + ((long long)(2 * blockIdx.x + which)) * (BT * kTileN);
+        if (p.deterministic) {
+          const int which = (sched.sk_begin(blockIdx.x) >= u_start) ? 0 : 1;
+          my_part = p.partials + ((long long)(2 * blockIdx.x + which)) * (BT * kTileN);
+        } else {
+          my_part = p.partials + tl * (BT * kTileN);
+        }
       }
 #pragma unroll 1
       for (int mc = 0; mc < BT / 16; ++mc) {
         uint32_t v[16];
-        tmem_ld16(tbase + mc * 16, v);
-        tmem_wait_ld();
+        tmem_ld16_wait(tbase + mc * 16, v);
         if (whole) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -482,13 +587,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               p.c[(long long)(tc.row0 + m) * p.n + n] =
                   to_out<FP16>(__uint_as_float(v[i]) + bias);
           }
-        } else {
+        } else if (p.deterministic) {
           // partial tile, column-major [col][BT]: this thread's column is contiguous
           float4* dst = reinterpret_cast<float4*>(my_part + col * BT + mc * 16);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+        } else {
+          float* dst = my_part + col * BT + mc * 16;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            red_add_v4(dst + 4 * i, __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                       __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
         }
       }
       tc_fence_before();
@@ -502,41 +613,70 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // Fixed-order split-K reduction, per 32-column quadrant: the warp of
         // the last CTA to arrive for this quadrant of the tile sums every
         // contributor's partial in CTA order (independent of arrival order).
+        // The warp's partial stores are ordered before lane 0's release add;
+        // the acquiring add of the last arrival orders the reads after it.
         const long long c_first = sched.cta_of_unit(u_start);
         const long long c_last = sched.cta_of_unit(u_start + p.kt - 1);
         const int contributors = (int)(c_last - c_first + 1);
         int* counter = &p.counters[(long long)wi.tile * 4 + q];
-        __threadfence();
         __syncwarp();
         int old = 0;
-        if (lane == 0) old = atomicAdd(counter, 1);
+        if (lane == 0) old = atomic_add_acq_rel_gpu(counter, 1);
         old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == contributors - 1) {
-          __threadfence();
-          // 16 rows per pass; the partials of up to 3 contributors are loaded
-          // before any is added, then summed in CTA order (fixed rounding order)
-          for (int m0 = 0; m0 < tc.rows; m0 += 16) {
-            float4 acc4[4];
+        __syncwarp();   // orders every lane's reads after lane 0's acquire
+        if (old == contributors - 1 && !p.deterministic) {
+          // atomic mode: the accumulator holds the sum; read it (32 rows per
+          // pass, all loads issued before use), write the output, and leave
+          // the accumulator zeroed for the next launch
+          const float4* src4 = reinterpret_cast<const float4*>(my_part + col * BT);
+          float4* z4 = reinterpret_cast<float4*>(my_part + col * BT);
+          for (int m0 = 0; m0 < tc.rows; m0 += 32) {
+            float4 a4[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (long long cc0 = c_first; cc0 <= c_last; cc0 += 3) {
-              float4 v4[3][4];
+            for (int j = 0; j < 8; ++j)
+              if (m0 + 4 * j < BT) a4[j] = __ldcg(src4 + m0 / 4 + j);
 #pragma unroll
-              for (int i = 0; i < 3; ++i) {
+            for (int j = 0; j < 8; ++j) {
+              if (m0 + 4 * j < BT) {
+                z4[m0 / 4 + j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float* af = reinterpret_cast<const float*>(&a4[j]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int m = m0 + 4 * j + i;
+                  if (m < tc.rows)
+                    p.c[(long long)(tc.row0 + m) * p.n + n] = to_out<FP16>(af[i] + bias);
+                }
+              }
+            }
+          }
+          // rows past tc.rows hold what the MMA computed for the tile's padding
+          // rows (zero fill or the next expert's tokens): clear them as well
+          for (int m0 = ((tc.rows + 31) / 32) * 32; m0 < BT; m0 += 4)
+            z4[m0 / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (lane == 0) *counter = 0;   // ready for the next launch
+        } else if (old == contributors - 1) {
+          // 8 rows per pass; up to 4 contributors' partials are loaded before
+          // any is added, then summed in CTA order (fixed rounding order)
+          for (int m0 = 0; m0 < tc.rows; m0 += 8) {
+            float4 acc4[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+            for (long long cc0 = c_first; cc0 <= c_last; cc0 += 4) {
+              float4 v4[4][2];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
                 const long long cc = cc0 + i;
                 if (cc <= c_last) {
                   const int which = (sched.sk_begin(cc) >= u_start) ? 0 : 1;
                   const float4* src4 = reinterpret_cast<const float4*>(
                       p.partials + ((long long)(2 * cc + which)) * (BT * kTileN) + col * BT + m0);
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) v4[i][j] = __ldcg(src4 + j);
+                  v4[i][0] = __ldcg(src4);
+                  v4[i][1] = __ldcg(src4 + 1);
                 }
               }
 #pragma unroll
-              for (int i = 0; i < 3; ++i) {
+              for (int i = 0; i < 4; ++i) {
                 if (cc0 + i <= c_last) {
 #pragma unroll
-                  for (int j = 0; j < 4; ++j) {
+                  for (int j = 0; j < 2; ++j) {
                     acc4[j].x += v4[i][j].x;
                     acc4[j].y += v4[i][j].y;
                     acc4[j].z += v4[i][j].z;
@@ -547,7 +687,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
             const float* accf = reinterpret_cast<const float*>(acc4);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 8; ++i) {
               if (m0 + i < tc.rows)
                 p.c[(long long)(tc.row0 + m0 + i) * p.n + n] = to_out<FP16>(accf[i] + bias);
             }
@@ -578,8 +718,17 @@ static cudaError_t launch_t(const CUtensorMap& tmap, const W4A16Params& p, int g
     if (err != cudaSuccess) return err;
     attr_set = p.smem_bytes;
   }
-  kern<<<grid, kNumThreads, p.smem_bytes, stream>>>(tmap, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kNumThreads);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmap, p);
 }
 
 template <bool FP16, bool GROUPED>

@@ -39,7 +39,8 @@ class qgemm_layer_config(ctypes.Structure):
 
 
 class qgemm_compute_config(ctypes.Structure):
-    _fields_ = [("gemm_type", ctypes.c_int32), ("batch_invariant", ctypes.c_int32)]
+    _fields_ = [("gemm_type", ctypes.c_int32), ("batch_invariant", ctypes.c_int32),
+                ("deterministic", ctypes.c_int32)]
 
 
 class qgemm_tuning_config(ctypes.Structure):
@@ -140,8 +141,9 @@ def layer_config(n, k, group_size, weight_format, scale_format, zero_format, act
                               act_dtype, out_dtype, has_bias, num_experts)
 
 
-def compute_config(gemm_type=QGEMM_GEMM_DENSE, batch_invariant=0) -> qgemm_compute_config:
-    return qgemm_compute_config(gemm_type, batch_invariant)
+def compute_config(gemm_type=QGEMM_GEMM_DENSE, batch_invariant=0,
+                   deterministic=0) -> qgemm_compute_config:
+    return qgemm_compute_config(gemm_type, batch_invariant, deterministic)
 
 
 def tuning_config(block_tok=0, stages=0, max_ctas=0, split_k=0, cta_pair=0):

@@ -51,11 +51,11 @@ class Case:
         return gemm.w4a16_reference(a, self.w_hat, self.bias)
 
 
-def linear(case: Case, tuning=None):
+def linear(case: Case, tuning=None, deterministic=False):
     from quantized_weight_gemm_run_b300.api import W4A16Linear
     qw, sc, qz = case.dev_weights()
     return W4A16Linear(qw, sc, qz, case.n, case.k, case.g, TD[case.adt], bias=case.dev_bias(),
-                       tuning=tuning)
+                       tuning=tuning, deterministic=deterministic)
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:

@@ -67,23 +67,35 @@ def test_gemm_bias(Q):
     assert_close(to_np(out), c.reference(), what="bias")
 
 
+@pytest.mark.parametrize("det", [False, True])
 @pytest.mark.parametrize("bt", [16, 32, 64, 128])
 @pytest.mark.parametrize("split_k,max_ctas", [(0, 0), (1, 0), (0, 7)])
-def test_tuning_overrides_same_result(Q, bt, split_k, max_ctas):
+def test_tuning_overrides_same_result(Q, bt, split_k, max_ctas, det):
     c = Case(70, 384, 768, 128, "bf16", False, seed=9)
-    lin = linear(c, tuning=Q.tuning_config(block_tok=bt, split_k=split_k, max_ctas=max_ctas))
+    lin = linear(c, tuning=Q.tuning_config(block_tok=bt, split_k=split_k, max_ctas=max_ctas),
+                 deterministic=det)
     out = lin(c.dev_act())
     assert lin.status() == Q.QGEMM_OK
     assert_close(to_np(out), c.reference(), what=f"bt={bt} split_k={split_k} ctas={max_ctas}")
 
 
-def test_deterministic_bits(Q):
+def test_deterministic_mode_bits_repeat(Q):
     c = Case(48, 512, 2048, 128, "bf16", True, seed=12)
-    lin = linear(c, tuning=Q.tuning_config(max_ctas=37))    # many split tiles
+    lin = linear(c, tuning=Q.tuning_config(max_ctas=37), deterministic=True)   # many split tiles
     x = c.dev_act()
     o1 = lin(x).clone()
     o2 = lin(x).clone()
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert_close(to_np(o1), c.reference(), what="deterministic mode")
+
+
+def test_atomic_mode_repeats_within_tolerance(Q):
+    c = Case(48, 512, 2048, 128, "bf16", True, seed=12)
+    lin = linear(c, tuning=Q.tuning_config(max_ctas=37))
+    x = c.dev_act()
+    outs = [to_np(lin(x)) for _ in range(3)]   # accumulators must come back zeroed each time
+    for o in outs:
+        assert_close(o, c.reference(), what="atomic split-K")
 
 
 def test_m_zero_launches_nothing(Q):
