@@ -72,11 +72,39 @@ def workload_points(name):
         return [dict(m=s["m"], n=s["n"], k=s["k"], g=128, asym=False, adt="bf16")], dict(
             workload="w4a16_sym_8192x8192x8192", m=8192, n=8192, k=8192, group=128,
             weights="int4", act="bf16")
+    if name == "w4a8":
+        s = synth.W4A8_SHAPE
+        return ([dict(kind="w4a8", m=m, n=s["n"], k=s["k"], g=32, asym=False, adt="bf16")
+                 for m in synth.W4A8_MS],
+                dict(workload="w4a8_mxfp4_7168x2048", n=s["n"], k=s["k"], ms=synth.W4A8_MS,
+                     weights="mxfp4 (e2m1 + e8m0/32)", act="bf16 -> e4m3 per token"))
+    if name.startswith("moe"):
+        t = int(name[3:])
+        s = synth.MOE_SHAPE
+        return ([dict(kind="moe", m=t, n=s["hidden"], k=s["hidden"], g=128, asym=False,
+                      adt="bf16")],
+                dict(workload=f"grouped_moe_w4a16_T{t}", tokens=t, experts=s["experts"],
+                     topk=s["topk"], hidden=s["hidden"], inter=s["inter"], group=128,
+                     weights="int4 per expert"))
     raise ValueError(name)
 
 
 def point_bytes(p):
     m, n, k, g = p["m"], p["n"], p["k"], p["g"]
+    kind = p.get("kind", "w4a16")
+    if kind == "w4a8":
+        # act quant: read bf16 x, write e4m3 + scale; GEMM: codes, e8m0, a8, scale, bf16 out
+        return (2 * m * k + m * k + 4 * m) + (n * k // 2 + n * k // 32 + m * k + 4 * m + 2 * m * n)
+    if kind == "moe":
+        s = synth.MOE_SHAPE
+        e, h, i, topk = s["experts"], s["hidden"], s["inter"], s["topk"]
+        r = m * topk
+        active = min(e, r)   # upper bound on the experts that receive a row
+        w_e = (h * 2 * i + i * h) // 2 + (h // 128) * 2 * i * 2 + (i // 128) * h * 2
+        act = (2 * m * h + 2 * r * h * 2            # permute: read tokens, write a_perm (+read)
+               + 2 * r * 2 * i * 2 + 2 * r * i      # GEMM1 out, SiLU in/out
+               + 2 * r * i + 2 * r * h * 2 + 2 * m * h)   # GEMM2 in/out, combine
+        return active * w_e + act
     b = n * k // 2 + (k // g) * n * 2 + m * k * 2 + m * n * 2
     if p["asym"]:
         b += (k // g) * n // 2
@@ -84,6 +112,9 @@ def point_bytes(p):
 
 
 def point_flops(p):
+    if p.get("kind") == "moe":
+        s = synth.MOE_SHAPE
+        return 2 * p["m"] * s["topk"] * (s["hidden"] * 2 * s["inter"] + s["inter"] * s["hidden"])
     return 2 * p["m"] * p["n"] * p["k"]
 
 
@@ -106,22 +137,31 @@ class ClockSampler:
 
     def start(self):
         import threading
+        self._stop = threading.Event()
         try:
             import pynvml
             pynvml.nvmlInit()
             h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:       # no NVML: report it instead of clocks
-            self.error = f"nvml unavailable: {e}"
-            return
-        self._stop = threading.Event()
+
+            def sample():
+                return (pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM),
+                        pynvml.nvmlDeviceGetCurrentClocksEventReasons(h))
+        except Exception:            # no NVML binding: poll nvidia-smi instead
+            import subprocess
+            q = ["nvidia-smi", "-i", str(self.index), "--format=csv,noheader,nounits",
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active"]
+
+            def sample():
+                out = subprocess.run(q, capture_output=True, text=True, timeout=5).stdout
+                sm, smax, active = [x.strip() for x in out.strip().split(",")[:3]]
+                self.max_mhz = float(smax)
+                return float(sm), int(active, 16)
 
         def run():
             while not self._stop.is_set():
                 try:
-                    mhz = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
-                    rs = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
-                    self.samples.append((mhz, rs))
+                    self.samples.append(sample())
                 except Exception as e:
                     self.error = str(e)
                 self._stop.wait(0.05)
@@ -148,23 +188,32 @@ class GemmPoint:
     """Buffers of one GEMM of the workload (own weights, activations, output).
 
     ``clone()`` duplicates every device buffer, so that a rotation of clones
-    reads its operands cold from HBM."""
+    reads its operands cold from HBM.  A W4A8 point's launch is the per-token
+    FP8 quantization of its bf16 activations followed by the GEMM."""
 
     def __init__(self, p, seed, device, host=False, src=None):
         import torch
         from quantized_weight_gemm_run_b300 import qgemm as Q
-        from quantized_weight_gemm_run_b300.api import W4A16Linear
+        from quantized_weight_gemm_run_b300.api import W4A16Linear, W4A8Linear
         self.p, self.Q = p, Q
+        self.mx = p.get("kind") == "w4a8"
         m, n, k, gs = p["m"], p["n"], p["k"], p["g"]
-        dt = torch.bfloat16 if p["adt"] == "bf16" else torch.float16
+        dt = torch.float16 if p["adt"] == "fp16" else torch.bfloat16
         if src is None:
             g = synth.rng(seed)
-            qweight = torch.from_numpy(synth.random_words(g, (k // 8, n))).to(device)
-            scales = torch.from_numpy(synth.random_scales_fp32(g, (k // gs, n))).to(dt).to(device)
-            qzeros = (torch.from_numpy(synth.random_words(g, (k // gs, n // 8))).to(device)
-                      if p["asym"] else None)
-            self.lin = W4A16Linear(qweight, scales, qzeros, n, k, gs, dt)
-            del qweight, scales, qzeros
+            if self.mx:
+                codes = torch.from_numpy(synth.random_bytes(g, (n, k // 2))).to(device)
+                b = torch.from_numpy(synth.random_bytes(g, (n, k // 32), 116, 124)).to(device)
+                self.lin = W4A8Linear(codes, b, n, k)
+                del codes, b
+            else:
+                qweight = torch.from_numpy(synth.random_words(g, (k // 8, n))).to(device)
+                scales = torch.from_numpy(
+                    synth.random_scales_fp32(g, (k // gs, n))).to(dt).to(device)
+                qzeros = (torch.from_numpy(synth.random_words(g, (k // gs, n // 8))).to(device)
+                          if p["asym"] else None)
+                self.lin = W4A16Linear(qweight, scales, qzeros, n, k, gs, dt)
+                del qweight, scales, qzeros
             self.a = torch.from_numpy(synth.activations_fp32(g, m, k)).to(dt).to(device)
         else:
             import copy
@@ -173,6 +222,9 @@ class GemmPoint:
             self.lin.s = src.lin.s.clone()
             self.lin.z = None if src.lin.z is None else src.lin.z.clone()
             self.a = src.a.clone()
+        if self.mx:
+            self.a8 = torch.empty(m, k, dtype=torch.uint8, device=device)
+            self.a_scale = torch.empty(max(m, 1), dtype=torch.float32, device=device)
         self.c = torch.empty(m, n, dtype=dt, device=device)
         st, nbytes = Q.qgemm_workspace_size(self.lin.layer, self.lin.dense, None, m)
         Q.check(st)
@@ -180,20 +232,92 @@ class GemmPoint:
         if host:
             self.a_host = self.a.cpu().pin_memory()
             self.c_host = torch.empty(m, n, dtype=dt).pin_memory()
+        self.launches = 2 if self.mx else 1
 
     def clone(self):
         return GemmPoint(self.p, 0, self.c.device, src=self)
 
     def launch(self):
         Q = self.Q
-        Q.check(Q.qgemm_run(self.lin.layer, self.lin.dense, None, self.p["m"], self.a, None,
-                            self.lin.w, self.lin.s, self.lin.z, None, self.c, self.ws,
-                            self.ws.numel()))
+        m = self.p["m"]
+        if self.mx:
+            Q.check(Q.qgemm_quantize_act_fp8(self.a, m, self.p["k"], self.a8, self.a_scale))
+            Q.check(Q.qgemm_run(self.lin.layer, self.lin.dense, None, m, self.a8, self.a_scale,
+                                self.lin.w, self.lin.s, None, None, self.c, self.ws,
+                                self.ws.numel()))
+        else:
+            Q.check(Q.qgemm_run(self.lin.layer, self.lin.dense, None, m, self.a, None,
+                                self.lin.w, self.lin.s, self.lin.z, None, self.c, self.ws,
+                                self.ws.numel()))
 
     def launch_e2e(self):
         self.a.copy_(self.a_host, non_blocking=True)
         self.launch()
         self.c_host.copy_(self.c, non_blocking=True)
+
+
+class MoEPoint:
+    """One grouped-MoE W4A16 layer (E=64, top-8, hidden 2048, intermediate
+    1408) over T tokens: permute, gate|up GEMM, SiLU gate, down GEMM, combine.
+    Router logits are drawn seeded and routed once at set-up (softmax top-k on
+    the device, outside the timed region)."""
+
+    def __init__(self, p, seed, device, host=False):
+        import torch
+        from quantized_weight_gemm_run_b300 import qgemm as Q
+        from quantized_weight_gemm_run_b300.api import MoELayer, W4A16Linear
+        self.p, self.Q = p, Q
+        s = synth.MOE_SHAPE
+        e, h, i, topk, t = s["experts"], s["hidden"], s["inter"], s["topk"], p["m"]
+        g = synth.rng(seed)
+        bf = torch.bfloat16
+
+        def expert_stack(k, n):
+            qw = torch.from_numpy(synth.random_words(g, (e * k // 8, n))).to(device)
+            sc = torch.from_numpy(synth.random_scales_fp32(g, (e * k // 128, n))).to(bf).to(device)
+            return W4A16Linear(qw, sc, None, n, k, 128, bf, num_experts=e)
+
+        self.l1 = expert_stack(h, 2 * i)
+        self.l2 = expert_stack(i, h)
+        self.layer = MoELayer(self.l1, self.l2, e, topk)
+        self.x = torch.from_numpy(synth.activations_fp32(g, t, h)).to(bf).to(device)
+        logits = torch.from_numpy(synth.router_logits_fp32(g, t, e)).to(device)
+        probs = torch.softmax(logits.double(), dim=-1)
+        w, ids = torch.topk(probs, topk, dim=-1)
+        self.ids = ids.to(torch.int32).contiguous()
+        self.wts = w.to(torch.float32).contiguous()
+        self.y = torch.empty(t, h, dtype=bf, device=device)
+        self.layer(self.x, self.ids, self.wts, out=self.y)   # sizes the workspaces once
+        torch.cuda.synchronize()
+        if host:
+            self.x_host = self.x.cpu().pin_memory()
+            self.y_host = torch.empty(t, h, dtype=bf).pin_memory()
+        self.launches = 8   # sort, gather, GEMM1, SiLU, GEMM2, combine (+2 per GEMM none)
+
+    def clone(self):
+        return self   # 285 MB of expert weights already exceed twice the L2
+
+    def launch(self):
+        self.layer(self.x, self.ids, self.wts, out=self.y)
+
+    def launch_e2e(self):
+        self.x.copy_(self.x_host, non_blocking=True)
+        self.launch()
+        self.y_host.copy_(self.y, non_blocking=True)
+
+    @property
+    def a(self):
+        return self.x
+
+    @property
+    def c(self):
+        return self.y
+
+
+def make_point(p, seed, device, host=False):
+    if p.get("kind") == "moe":
+        return MoEPoint(p, seed, device, host)
+    return GemmPoint(p, seed, device, host)
 
 
 def cold_copies(p):
@@ -202,8 +326,13 @@ def cold_copies(p):
 
 
 def kernel_name(p):
-    bt = 16 if p["m"] <= 16 else 32 if p["m"] <= 32 else 64 if p["m"] <= 64 else 128
-    return f"w4a16_kernel<{bt},{'fp16' if p['adt'] == 'fp16' else 'bf16'},dense>"
+    kind = p.get("kind", "w4a16")
+    if kind == "moe":
+        return "moe_layer (sort, gather, grouped GEMM x2, SiLU, combine)"
+    m = p["m"]
+    bt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
+    fmt = "w4a8_mxf8f6f4" if kind == "w4a8" else ("fp16" if p["adt"] == "fp16" else "bf16")
+    return f"w4a16_kernel<{bt},{fmt},dense>"
 
 
 def run_ours(args, rank, world, device):
@@ -212,7 +341,7 @@ def run_ours(args, rank, world, device):
     peaks, peak_src = load_peaks()
     torch.cuda.set_device(device)
     # one buffer set per GEMM of the step
-    base = [GemmPoint(p, 1000 + i, device, host=True) for i, p in enumerate(pts)]
+    base = [make_point(p, 1000 + i, device, host=True) for i, p in enumerate(pts)]
     gemms = list(base)
     step_bytes = sum(point_bytes(p) for p in pts)
     if step_bytes < 2 * L2_BYTES:     # single-GEMM workloads: rotate clones to stay cold
@@ -263,13 +392,21 @@ def run_ours(args, rank, world, device):
     flops_step = sum(point_flops(gm.p) for gm in gemms)
     bytes_step = sum(point_bytes(gm.p) for gm in gemms)
     ms_step = ms_total / args.steps
-    value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
+    is_moe = pts[0].get("kind") == "moe"
+    if is_moe:
+        tokens_step = sum(gm.p["m"] for gm in gemms)
+        value = world * tokens_step * args.steps / (ms_total * 1e-3)
+        unit = "tokens/s"
+    else:
+        value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
+        unit = "TFLOP/s"
 
     # per-GEMM device times (dominant kernel and the per-M table): each GEMM
     # launched back to back over a rotation of cold clones, inside a graph
     per_point = []
     for i, p in enumerate(pts):
-        copies = [base[i]] + [base[i].clone() for _ in range(cold_copies(p) - 1)]
+        copies = [base[i]] + ([] if is_moe else
+                              [base[i].clone() for _ in range(cold_copies(p) - 1)])
         r = max(20, len(copies))
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g2, stream=stream):
@@ -340,12 +477,15 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     e2e_ms = reduce_max(b0.elapsed_time(b1), world)
     flops_pts = sum(point_flops(p) for p in pts)
-    e2e_val = world * flops_pts * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    if is_moe:
+        e2e_val = world * sum(p["m"] for p in pts) * e2e_steps / (e2e_ms * 1e-3)
+    else:
+        e2e_val = world * flops_pts * e2e_steps / (e2e_ms * 1e-3) / 1e12
 
     line = {
         "metric": "W4A16 GEMM TFLOP/s and HBM GB/s vs M (frac of B300 roofline); MoE tokens/s",
         "value": round(value, 3),
-        "unit": "TFLOP/s",
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -353,7 +493,8 @@ def run_ours(args, rank, world, device):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if pts[0]["adt"] == "bf16" else "fp16",
+        "dtype": ("bf16 x e4m3 (fp32 acc)" if pts[0].get("kind") == "w4a8"
+                  else "bf16" if pts[0]["adt"] == "bf16" else "fp16"),
         "data": "synthetic (seeded random 4-bit codes, scales, zero points, N(0,1) activations)",
         "config": dict(cfg, gemms_per_step=len(gemms), bytes_per_step=bytes_step,
                        l2="operands of every GEMM are distinct buffers; a step touches "
@@ -362,9 +503,9 @@ def run_ours(args, rank, world, device):
         "hbm_gbs": round(world * bytes_step * args.steps / (ms_total * 1e-3) / 1e9, 1),
         "roofline": roof,
         "points": per_point,
-        "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(e2e_val, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": len(gemms) * args.steps,
+        "gpu_launches": sum(gm.launches for gm in gemms) * args.steps,
         "clocks": clk,
     }
     if rank == 0:
@@ -385,38 +526,76 @@ def reduce_max(x, world):
 # ------------------------------------------------------------------ CPU oracle
 
 def _oracle_point(p, seed):
-    """The oracle on one GEMM of the workload (dequant + float64 matmul)."""
-    from oracle import codecs, quant, gemm
+    """The oracle on one unit of the workload: a GEMM (dequant + float64
+    matmul; W4A8 with its per-token FP8 quantization), or for MoE the whole
+    layer for two tokens.  Returns the units done (flops, or tokens)."""
+    from oracle import codecs, gemm, moe, quant
     g = synth.rng(seed)
     m, n, k, gs = p["m"], p["n"], p["k"], p["g"]
+    kind = p.get("kind", "w4a16")
+    if kind == "w4a8":
+        codes = synth.random_bytes(g, (n, k // 2))
+        b = synth.random_bytes(g, (n, k // 32), 116, 124)
+        ckn, bkn = quant.unpack_mxfp4(codes, b)
+        x = codecs.bf16(synth.activations_fp32(g, m, k))
+        a8, sc = gemm.act_quant_fp8(x)
+        gemm.w4a8_output(a8, sc, ckn, bkn)
+        return point_flops(p)
+    if kind == "moe":
+        s = synth.MOE_SHAPE
+        e, h, i, topk, t = s["experts"], s["hidden"], s["inter"], s["topk"], 2
+        x = codecs.bf16(synth.activations_fp32(g, t, h))
+        ids, wts = moe.route(synth.router_logits_fp32(g, t, e), topk)
+
+        def w_hat(k_, n_):
+            def f(_):
+                q = quant.unpack_int4_kn(synth.random_words(g, (k_ // 8, n_)), True)
+                sc = codecs.bf16(synth.random_scales_fp32(g, (k_ // 128, n_)).astype(np.float64))
+                return quant.dequant_int(q, sc, None, 128, "bf16")
+            return f
+        moe.moe_layer(x, ids, wts, w_hat(h, 2 * i), w_hat(i, h), e, i)
+        return t
     qw = synth.random_words(g, (k // 8, n))
     s = codecs.bf16(synth.random_scales_fp32(g, (k // gs, n)).astype(np.float64))
     q = quant.unpack_int4_kn(qw, signed=not p["asym"])
     z = quant.unpack_zeros(synth.random_words(g, (k // gs, n // 8))) if p["asym"] else None
     a = codecs.bf16(synth.activations_fp32(g, m, k))
     w_hat = quant.dequant_int(q, s, z, gs, p["adt"])
-    return gemm.w4a16_output(a, w_hat, p["adt"])
+    gemm.w4a16_output(a, w_hat, p["adt"])
+    return point_flops(p)
+
+
+def _unit_of(pts):
+    return "tokens/s" if pts[0].get("kind") == "moe" else "TFLOP/s"
+
+
+def _scale(units, seconds, pts):
+    return units / seconds if pts[0].get("kind") == "moe" else units / seconds / 1e12
+
+
+def _label(p):
+    return f"T={p['m']}" if p.get("kind") == "moe" else f"{p['m']}x{p['n']}x{p['k']}"
 
 
 def cpu_baseline(pts, budget_s=15.0):
-    """Time the oracle on a bounded sample of the workload's GEMMs."""
+    """Time the oracle on a bounded sample of the workload (its smallest
+    units first, until about budget_s of CPU work)."""
     cores = len(os.sched_getaffinity(0))
-    done, flops, t_used = [], 0, 0.0
+    done, units, t_used = [], 0, 0.0
     order = sorted(range(len(pts)), key=lambda i: (pts[i]["n"] * pts[i]["k"], pts[i]["m"]))
     t0 = time.perf_counter()
     for i in order:
         if t_used > budget_s:
             break
-        p = pts[i]
-        t1 = time.perf_counter()
-        _oracle_point(p, 77 + i)
+        units += _oracle_point(pts[i], 77 + i)
         t_used = time.perf_counter() - t0
-        flops += point_flops(p)
-        done.append(f"{p['m']}x{p['n']}x{p['k']}")
-    return {"value": round(flops / t_used / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+        done.append(_label(pts[i]))
+    what = ("2 tokens through the whole layer" if pts[0].get("kind") == "moe"
+            else "numpy float64 dequant + matmul")
+    return {"value": round(_scale(units, t_used, pts), 6), "unit": _unit_of(pts), "cores": cores,
             "kind": "oracle",
-            "sample": f"{len(done)} of {len(pts)} GEMMs ({', '.join(done)}), numpy float64 "
-                      f"dequant + matmul, {t_used:.1f} s"}
+            "sample": f"{len(done)} of {len(pts)} units ({', '.join(done)}), {what}, "
+                      f"{t_used:.1f} s"}
 
 
 def run_reference(args):
@@ -425,26 +604,26 @@ def run_reference(args):
     order = sorted(range(len(pts)), key=lambda i: (pts[i]["n"] * pts[i]["k"], pts[i]["m"]))
     for w in range(args.warmup):
         _oracle_point(pts[order[w % len(order)]], 300 + w)
-    flops, names = 0, []
+    units, names = 0, []
     t0 = time.perf_counter()
-    for s in range(args.steps):
-        p = pts[order[s % len(order)]]
-        _oracle_point(p, 400 + s)
-        flops += point_flops(p)
-        names.append(f"{p['m']}x{p['n']}x{p['k']}")
+    for st in range(args.steps):
+        p = pts[order[st % len(order)]]
+        units += _oracle_point(p, 400 + st)
+        names.append(_label(p))
     dt = time.perf_counter() - t0
-    v = flops / dt / 1e12
-    sample = (f"one GEMM of the workload per step, cycling smallest first "
-              f"({', '.join(sorted(set(names)))}); numpy float64 dequant + matmul")
+    v = _scale(units, dt, pts)
+    unit = _unit_of(pts)
+    sample = (f"one unit of the workload per step, cycling smallest first "
+              f"({', '.join(sorted(set(names)))}); the CPU oracle in numpy float64")
     return {"impl": "reference", "metric": "W4A16 GEMM TFLOP/s and HBM GB/s vs M (frac of B300 "
-            "roofline); MoE tokens/s", "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": 1,
+            "roofline); MoE tokens/s", "value": round(v, 6), "unit": unit, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3 / max(args.steps, 1), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": cfg,
-            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores,
+            "cpu_baseline": {"value": round(v, 6), "unit": unit, "cores": cores,
                              "kind": "oracle", "sample": sample},
-            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+            "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
 
@@ -456,7 +635,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="sweep", choices=["sweep", "w4a16_m16", "large"])
+    ap.add_argument("--workload", default="sweep",
+                    choices=["sweep", "w4a16_m16", "large", "w4a8", "moe16", "moe256", "moe4096"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()
     if args.warmup < 3:

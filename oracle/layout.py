@@ -28,6 +28,16 @@ W4A16 tiled layout (N and K multiples of 128; KT = K / 128 k-tiles):
 
   zeros (UINT4 only): one block of 128 * ST bytes per (nt, kt), byte
     sg * 128 + r is the zero point (0..15) of the same (group, row).
+
+MXFP4 tiled layout (same tiling):
+
+  weights: one 8192-byte block per (nt, kt), vector v = (qd * 4 + j) * 32 + t
+    holds row n = 128 nt + 32 qd + t and k = 128 kt + 32 j + [0, 32) as 16
+    bytes in the standard order (byte b: k = 2b in the low nibble, 2b + 1 in
+    the high nibble), i.e. 32 consecutive codes of the row.
+  scales: one 512-byte block per (nt, kt); bytes 4 r .. 4 r + 3 are the e8m0
+    exponents of row n = 128 nt + r for k = 128 kt + [0, 32), [32, 64),
+    [64, 96), [96, 128) in that order.
 """
 
 from __future__ import annotations
@@ -109,3 +119,24 @@ def tiled_weights_inverse(stream, k: int, n: int, signed: bool) -> np.ndarray:
                     q4[:, kl, :, 32 * qd: 32 * qd + 32] = vals.transpose(1, 0, 2).astype(np.int64)
     q = q4.reshape(k, n)
     return q - 8 if signed else q
+
+
+def tiled_mxfp4_weights(codes_nk) -> np.ndarray:
+    """Standard MXFP4 codes uint8 [N, K/2] -> tiled byte stream."""
+    c = np.asarray(codes_nk, dtype=np.uint8)
+    n, kh = c.shape
+    k = 2 * kh
+    kt_n, nt_n = k // TILE_K, n // TILE_N
+    # c4[nt, qd, t, kt, j, 16 bytes]
+    c4 = c.reshape(nt_n, 4, 32, kt_n, 4, 16)
+    out = c4.transpose(0, 3, 1, 4, 2, 5)          # nt, kt, qd, j, t, bytes
+    return np.ascontiguousarray(out).reshape(-1)
+
+
+def tiled_mxfp4_scales(b_nk) -> np.ndarray:
+    """Standard e8m0 exponents uint8 [N, K/32] -> tiled byte stream."""
+    b = np.asarray(b_nk, dtype=np.uint8)
+    n, kb = b.shape
+    kt_n, nt_n = kb // 4, n // TILE_N
+    b4 = b.reshape(nt_n, TILE_N, kt_n, 4)
+    return np.ascontiguousarray(b4.transpose(0, 2, 1, 3)).reshape(-1)

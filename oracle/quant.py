@@ -195,7 +195,8 @@ def pack_mxfp4(codes_kn, b_kn):
     even k in the low nibble, uint8 [N, K/32])."""
     c = np.asarray(codes_kn, dtype=np.uint8).T          # [N, K]
     packed = (c[:, 0::2] & 0xF) | ((c[:, 1::2] & 0xF) << 4)
-    return packed.astype(np.uint8), np.ascontiguousarray(np.asarray(b_kn, dtype=np.uint8).T)
+    return (np.ascontiguousarray(packed, dtype=np.uint8),
+            np.ascontiguousarray(np.asarray(b_kn, dtype=np.uint8).T))
 
 
 def unpack_mxfp4(packed_nk, b_nk):

@@ -48,6 +48,8 @@ class W4A16Linear:
         st, wb, sb, zb = Q.qgemm_packed_sizes(self.layer)
         Q.check(st)
         dev = qweight.device
+        qweight, scales = qweight.contiguous(), scales.contiguous()
+        qzeros = None if qzeros is None else qzeros.contiguous()
         self.w = torch.empty(wb, dtype=torch.uint8, device=dev)
         self.s = torch.empty(sb // 2, dtype=torch.int16, device=dev)
         self.z = torch.empty(zb, dtype=torch.uint8, device=dev) if asym else None
@@ -61,6 +63,7 @@ class W4A16Linear:
         self.grouped = Q.compute_config(Q.QGEMM_GEMM_GROUPED, deterministic=det)
 
     def __call__(self, a: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+        a = a.contiguous()
         m = a.shape[0]
         if out is None:
             out = torch.empty(m, self.n, dtype=self.act_dtype, device=a.device)
@@ -88,6 +91,65 @@ class W4A16Linear:
         """W^[K, N] as the kernels feed it to the tensor core (expert 0)."""
         out = torch.empty(self.k, self.n, dtype=self.act_dtype, device=self.w.device)
         Q.check(Q.qgemm_debug_dequant(self.layer, self.w, self.s, self.z, out))
+        return out
+
+    def status(self) -> int:
+        return Q.qgemm_check_status(self.ws.get(256))
+
+
+class W4A8Linear:
+    """A packed W4A8-MXFP4 layer: e2m1 codes uint8 [E*N, K/2] and e8m0 scales
+    uint8 [E*N, K/32] in the standard format; activations are quantized per
+    row to e4m3 by the library and the output is bf16."""
+
+    def __init__(self, codes, scales, n, k, num_experts=1, bias=None, tuning=None,
+                 deterministic=False):
+        self.n, self.k, self.num_experts = n, k, num_experts
+        self.layer = Q.layer_config(n, k, 32, Q.QGEMM_W_MXFP4, Q.QGEMM_S_E8M0, Q.QGEMM_Z_NONE,
+                                    Q.QGEMM_FP8E4M3, Q.QGEMM_BF16,
+                                    1 if bias is not None else 0, num_experts)
+        st, wb, sb, _ = Q.qgemm_packed_sizes(self.layer)
+        Q.check(st)
+        dev = codes.device
+        codes, scales = codes.contiguous(), scales.contiguous()
+        self.w = torch.empty(wb, dtype=torch.uint8, device=dev)
+        self.s = torch.empty(sb, dtype=torch.uint8, device=dev)
+        self.z = None
+        Q.check(Q.qgemm_pack_weights(self.layer, codes, scales, None, self.w, self.s, None))
+        self.bias, self.tuning = bias, tuning
+        self.ws = Workspace(dev)
+        det = 1 if deterministic else 0
+        self.dense = Q.compute_config(Q.QGEMM_GEMM_DENSE, deterministic=det)
+        self.grouped = Q.compute_config(Q.QGEMM_GEMM_GROUPED, deterministic=det)
+        self._act = {}
+
+    def quantize(self, x: torch.Tensor):
+        """x bf16 [M, K] -> (e4m3 codes uint8 [M, K], fp32 scales [M])."""
+        m = x.shape[0]
+        a8 = torch.empty(m, self.k, dtype=torch.uint8, device=x.device)
+        sc = torch.empty(max(m, 1), dtype=torch.float32, device=x.device)
+        Q.check(Q.qgemm_quantize_act_fp8(x, m, self.k, a8, sc))
+        return a8, sc
+
+    def run_quantized(self, a8, a_scale, out=None):
+        m = a8.shape[0]
+        if out is None:
+            out = torch.empty(m, self.n, dtype=torch.bfloat16, device=a8.device)
+        st, nbytes = Q.qgemm_workspace_size(self.layer, self.dense, self.tuning, max(m, 1))
+        Q.check(st)
+        ws = self.ws.get(nbytes)
+        Q.check(Q.qgemm_run(self.layer, self.dense, self.tuning, m, a8, a_scale, self.w, self.s,
+                            None, self.bias, out, ws, ws.numel()))
+        return out
+
+    def __call__(self, x: torch.Tensor, out=None) -> torch.Tensor:
+        a8, sc = self.quantize(x.contiguous())
+        return self.run_quantized(a8, sc, out)
+
+    def codes_e4m3(self) -> torch.Tensor:
+        """The e4m3 bytes the kernel feeds the tensor core, uint8 [K, N]."""
+        out = torch.empty(self.k, self.n, dtype=torch.uint8, device=self.w.device)
+        Q.check(Q.qgemm_debug_dequant(self.layer, self.w, self.s, None, out))
         return out
 
     def status(self) -> int:

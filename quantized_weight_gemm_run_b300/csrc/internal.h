@@ -33,6 +33,7 @@ struct W4A16Params {
   const uint8_t* z;          // tiled zero points or null
   const uint16_t* bias;      // [E, N] or null
   uint16_t* c;               // [rows, N]
+  const float* a_scale;      // W4A8: per-row activation scales [rows], else null
   int rows;                  // M (dense) or total permuted rows (grouped)
   int n, k;
   int kt, nt;                // k-tiles, n-tiles
@@ -69,8 +70,16 @@ struct W4A16Plan {
 int device_sm_count();
 W4A16Plan plan_w4a16(int block_tok, int stages, int max_ctas, int64_t units, int group,
                      int has_zp);
+// fmt: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 x e4m3, bf16 out)
 cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const W4A16Params& p, int block_tok,
-                         bool fp16, bool grouped, int grid, cudaStream_t stream);
+                         int fmt, bool grouped, int grid, cudaStream_t stream);
+
+cudaError_t launch_repack_mxfp4(const uint8_t* codes, const uint8_t* scales, uint8_t* w_out,
+                                uint8_t* s_out, int64_t n, int64_t k, int experts,
+                                cudaStream_t stream);
+
+cudaError_t launch_debug_mx_codes(const uint8_t* w, uint8_t* out_kn, int64_t n, int64_t k,
+                                  cudaStream_t stream);
 
 cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
                              const int32_t* qzeros, uint8_t* w_out, uint16_t* s_out,

@@ -127,7 +127,7 @@ static qgemm_status check_layer(const qgemm_layer_config* L) {
         return fail(QGEMM_ERR_UNSUPPORTED, "MXFP4 needs e8m0 scales per 32 k");
       if (L->act_dtype != QGEMM_FP8E4M3 || L->out_dtype != QGEMM_BF16)
         return fail(QGEMM_ERR_UNSUPPORTED, "MXFP4 runs against e4m3 activations, bf16 output");
-      return fail(QGEMM_ERR_UNSUPPORTED, "the W4A8-MXFP4 GEMM is not available in this build");
+      return ok();
     default:
       return fail(QGEMM_ERR_UNSUPPORTED, "unknown weight format %d", L->weight_format);
   }
@@ -149,6 +149,8 @@ static qgemm_status check_compute(const qgemm_compute_config* C, const qgemm_lay
 
 static int st_of(int group) { return group < kTileK ? kTileK / group : 1; }
 
+static bool is_mx(const qgemm_layer_config* L) { return L->weight_format == QGEMM_W_MXFP4; }
+
 // ------------------------------------------------------------ plans
 
 WorkspaceLayout workspace_layout(int64_t max_tiles, int grid, int block_tok) {
@@ -169,19 +171,20 @@ static int heuristic_block_tok(int64_t rows_per_group) {
 }
 
 // Pipeline stage geometry: [activation tile][weights][scales][zeros], 1 KB aligned.
-static void stage_geometry(int bt, int st, int has_zp, int* stage_bytes, int* off_w,
+// W4A8 stages hold an 8-bit activation tile and 4 e8m0 bytes per weight row.
+static void stage_geometry(int bt, int st, int has_zp, bool mx, int* stage_bytes, int* off_w,
                            int* off_s, int* off_z) {
-  const int act = bt * kTileK * 2;
+  const int act = bt * kTileK * (mx ? 1 : 2);
   *off_w = act;
   *off_s = act + kTileBytes;
-  *off_z = *off_s + st * kTileN * 2;
+  *off_z = *off_s + (mx ? kTileN * 4 : st * kTileN * 2);
   const int end = *off_z + (has_zp ? st * kTileN : 0);
   *stage_bytes = (end + 1023) & ~1023;
 }
 
 static int fixed_smem(int stages, int experts) {
   // alignment slack + barriers + shared state + grouped prefix arrays
-  return 1024 + (2 * stages + 2 * kASlots + 4 + 1) * 8 + 32 + 2 * (experts + 1) * 4 + 64;
+  return 1024 + (2 * stages + 2 * kASlots + 4 + 2) * 8 + 32 + 2 * (experts + 1) * 4 + 64;
 }
 
 struct Plan {
@@ -205,7 +208,7 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   const int st = st_of(L->group_size);
   const int has_zp = L->zero_format == QGEMM_Z_UINT4;
   int stage_bytes, off_w, off_s, off_z;
-  stage_geometry(bt, st, has_zp, &stage_bytes, &off_w, &off_s, &off_z);
+  stage_geometry(bt, st, has_zp, is_mx(L), &stage_bytes, &off_w, &off_s, &off_z);
   const int smem_cap = device_max_smem();
   int stages = (T && T->stages) ? T->stages : 16;
   if (stages < 2 || stages > 16) return fail(QGEMM_ERR_INVALID_ARG, "stages must be in [2, 16]");
@@ -280,9 +283,10 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 // ------------------------------------------------------------ the W4A16 run
 
 static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_config* T,
-                              bool deterministic, bool grouped, const int32_t* offsets, int64_t rows, const void* a,
-                              const void* w, const void* s, const void* z, const void* bias,
-                              void* c, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+                              bool deterministic, bool grouped, const int32_t* offsets,
+                              int64_t rows, const void* a, const float* a_scale, const void* w,
+                              const void* s, const void* z, const void* bias, void* c,
+                              void* workspace, size_t ws_bytes, cudaStream_t stream) {
   if (rows < 0) return fail(QGEMM_ERR_INVALID_ARG, "row count is negative");
   if (rows > (1 << 30)) return fail(QGEMM_ERR_UNSUPPORTED, "row count above 2^30");
   if (rows == 0) return ok();
@@ -292,6 +296,10 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
     return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
   if (!has_zp && z) return fail(QGEMM_ERR_INVALID_ARG, "zero points given for a format without");
   if (!L->has_bias && bias) return fail(QGEMM_ERR_INVALID_ARG, "bias given with has_bias = 0");
+  const bool mx = is_mx(L);
+  if (mx && !a_scale)
+    return fail(QGEMM_ERR_INVALID_ARG, "the W4A8 path needs the per-row activation scales");
+  if (!mx && a_scale) return fail(QGEMM_ERR_INVALID_ARG, "a_scale is only used by the W4A8 path");
   if (!aligned16(a) || !aligned16(w) || !aligned16(s) || !aligned16(c) || (z && !aligned16(z)) ||
       (bias && !aligned16(bias)) || !aligned16(workspace))
     return fail(QGEMM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
@@ -303,9 +311,15 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
                 ws_bytes);
   const bool fp16 = L->act_dtype == QGEMM_FP16;
   CUtensorMap tmap;
-  if (!encode_tmap_2d(&tmap, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      a, (uint64_t)L->k, (uint64_t)rows, (uint64_t)L->k * 2, 64, (uint32_t)P.bt,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
+  // activation tiles: 128-byte rows, 128-byte swizzle (64 16-bit or 128 e4m3 values)
+  const bool tmap_ok =
+      mx ? encode_tmap_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, (uint64_t)L->k, (uint64_t)rows,
+                          (uint64_t)L->k, 128, (uint32_t)P.bt, CU_TENSOR_MAP_SWIZZLE_128B)
+         : encode_tmap_2d(&tmap,
+                          fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          a, (uint64_t)L->k, (uint64_t)rows, (uint64_t)L->k * 2, 64,
+                          (uint32_t)P.bt, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!tmap_ok)
     return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the activation tensor");
   size_t wb, sb, zb;
   qgemm_packed_sizes(L, &wb, &sb, &zb);
@@ -317,6 +331,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.z = static_cast<const uint8_t*>(z);
   p.bias = static_cast<const uint16_t*>(bias);
   p.c = static_cast<uint16_t*>(c);
+  p.a_scale = a_scale;
   p.rows = (int)rows;
   p.n = (int)L->n;
   p.k = (int)L->k;
@@ -344,7 +359,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.off_z = P.off_z;
   p.smem_bytes = P.smem;
   p.wait_limit_ns = g_wait_limit_ns;
-  cudaError_t e = launch_w4a16(tmap, p, P.bt, fp16, grouped, P.grid, stream);
+  cudaError_t e = launch_w4a16(tmap, p, P.bt, mx ? 2 : fp16 ? 1 : 0, grouped, P.grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "W4A16 GEMM launch");
   return ok();
 }
@@ -383,7 +398,7 @@ qgemm_status qgemm_packed_sizes(const qgemm_layer_config* layer, size_t* w_bytes
   const size_t tiles = (size_t)(layer->n / kTileN) * (size_t)(layer->k / kTileK);
   const size_t stv = (size_t)st_of(layer->group_size);
   if (w_bytes) *w_bytes = E * tiles * kTileBytes;
-  if (s_bytes) *s_bytes = E * tiles * stv * kTileN * 2;
+  if (s_bytes) *s_bytes = is_mx(layer) ? E * tiles * kTileN * 4 : E * tiles * stv * kTileN * 2;
   if (z_bytes) *z_bytes = layer->zero_format == QGEMM_Z_UINT4 ? E * tiles * stv * kTileN : 0;
   return ok();
 }
@@ -400,6 +415,16 @@ qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qwe
     return fail(QGEMM_ERR_INVALID_ARG, "zero-point tensors given for a format without");
   if (!aligned16(w_out) || !aligned16(s_out) || !aligned16(qweight) || (z_out && !aligned16(z_out)))
     return fail(QGEMM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  if (is_mx(layer)) {
+    if ((reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
+      return fail(QGEMM_ERR_INVALID_ARG, "MXFP4 scales must be 4-byte aligned");
+    cudaError_t e = launch_repack_mxfp4(
+        static_cast<const uint8_t*>(qweight), static_cast<const uint8_t*>(scales),
+        static_cast<uint8_t*>(w_out), static_cast<uint8_t*>(s_out), layer->n, layer->k,
+        layer->num_experts, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "repack launch");
+    return ok();
+  }
   cudaError_t e = launch_repack_w4(
       static_cast<const int32_t*>(qweight), static_cast<const uint16_t*>(scales),
       static_cast<const int32_t*>(qzeros), static_cast<uint8_t*>(w_out),
@@ -443,9 +468,8 @@ qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_conf
   if (st != QGEMM_OK) return st;
   st = check_compute(compute, layer, false);
   if (st != QGEMM_OK) return st;
-  if (a_scale) return fail(QGEMM_ERR_INVALID_ARG, "a_scale is only used by the W4A8 path");
-  return run_w4a16(layer, tuning, compute->deterministic != 0, false, nullptr, m, a, w, s, z,
-                   bias, c, workspace,
+  return run_w4a16(layer, tuning, compute->deterministic != 0, false, nullptr, m, a, a_scale, w,
+                   s, z, bias, c, workspace,
                    workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
@@ -459,9 +483,8 @@ qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
   if (st != QGEMM_OK) return st;
   st = check_compute(compute, layer, true);
   if (st != QGEMM_OK) return st;
-  if (a_scale) return fail(QGEMM_ERR_INVALID_ARG, "a_scale is only used by the W4A8 path");
   return run_w4a16(layer, tuning, compute->deterministic != 0, true, expert_offsets,
-                   total_rows, a, w, s, z, bias, c,
+                   total_rows, a, a_scale, w, s, z, bias, c,
                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
@@ -532,6 +555,13 @@ qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* w,
   const bool has_zp = layer->zero_format == QGEMM_Z_UINT4;
   if (!w || !s || !out_kn || (has_zp && !z))
     return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (is_mx(layer)) {
+    cudaError_t e = launch_debug_mx_codes(static_cast<const uint8_t*>(w),
+                                          static_cast<uint8_t*>(out_kn), layer->n, layer->k,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
+    return ok();
+  }
   cudaError_t e = launch_debug_dequant(
       static_cast<const uint8_t*>(w), static_cast<const uint16_t*>(s),
       static_cast<const uint8_t*>(z), static_cast<uint16_t*>(out_kn), layer->n, layer->k,
@@ -580,9 +610,10 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
       static const char* dt[] = {"fp16", "bf16", "fp8e4m3"};
       char tmp[512];
       snprintf(tmp, sizeof(tmp),
-               "kernel=w4a16_tcgen05_swapab%s weights=%s group=%d act=%s out=%s n=%lld k=%lld "
+               "kernel=%s%s weights=%s group=%d act=%s out=%s n=%lld k=%lld "
                "m=%lld experts=%d block_tok=%d stages=%d grid=%d smem=%d workspace=%zu "
                "device=sm_103",
+               is_mx(layer) ? "w4a8_tcgen05_mxf8f6f4_swapab" : "w4a16_tcgen05_swapab",
                grouped ? "_grouped" : "", wf[layer->weight_format], layer->group_size,
                dt[layer->act_dtype], dt[layer->out_dtype], (long long)layer->n,
                (long long)layer->k, (long long)m, layer->num_experts, P.bt, P.stages, P.grid,

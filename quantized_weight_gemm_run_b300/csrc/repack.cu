@@ -103,4 +103,53 @@ cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
   return cudaGetLastError();
 }
 
+// MXFP4: standard codes [N, K/2] (k = 2j low nibble, 2j+1 high nibble) and
+// e8m0 scales [N, K/32] -> per (n-tile, k-tile) an 8192-byte block of 512
+// 16-byte vectors, vector (qd*4 + j)*32 + t = row 32qd + t, k = 32j .. 32j+31
+// with the nibbles left in their standard order (the kernel's table lookup
+// wants consecutive k in consecutive nibbles), and a 512-byte scale block of
+// one 32-bit word per row whose byte j is the scale of the row's j-th 32-k block.
+__global__ void repack_mxfp4_kernel(const uint8_t* __restrict__ codes,
+                                    const uint8_t* __restrict__ scales, uint4* __restrict__ w_out,
+                                    uint32_t* __restrict__ s_out, int n, int k, long long vecs,
+                                    long long words) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int KT = k / kTileK, NT = n / kTileN;
+  if (idx < vecs) {
+    const long long per_expert = (long long)NT * KT * 512;
+    const long long ex = idx / per_expert;
+    const long long rem = idx - ex * per_expert;
+    const long long blk = rem / 512;
+    const int v = (int)(rem % 512);
+    const int nt = (int)(blk / KT), kt = (int)(blk % KT);
+    const int t = v & 31, j = (v >> 5) & 3, qd = v >> 7;
+    const long long row = (long long)nt * kTileN + qd * 32 + t;
+    const uint8_t* src = codes + (ex * n + row) * (k / 2) + (kt * kTileK + j * 32) / 2;
+    w_out[idx] = *reinterpret_cast<const uint4*>(src);
+  }
+  if (idx < words) {
+    const long long per_expert = (long long)NT * KT * kTileN;
+    const long long ex = idx / per_expert;
+    const long long rem = idx - ex * per_expert;
+    const int r = (int)(rem % kTileN);
+    const long long blk = rem / kTileN;
+    const int nt = (int)(blk / KT), kt = (int)(blk % KT);
+    const long long row = (long long)nt * kTileN + r;
+    s_out[idx] = *reinterpret_cast<const uint32_t*>(scales + (ex * n + row) * (k / 32) + kt * 4);
+  }
+}
+
+cudaError_t launch_repack_mxfp4(const uint8_t* codes, const uint8_t* scales, uint8_t* w_out,
+                                uint8_t* s_out, int64_t n, int64_t k, int experts,
+                                cudaStream_t stream) {
+  const long long tiles = (long long)experts * (n / kTileN) * (k / kTileK);
+  const long long vecs = tiles * 512, words = tiles * kTileN;
+  const long long total = vecs > words ? vecs : words;
+  const int threads = 256;
+  repack_mxfp4_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, stream>>>(
+      codes, scales, reinterpret_cast<uint4*>(w_out), reinterpret_cast<uint32_t*>(s_out), (int)n,
+      (int)k, vecs, words);
+  return cudaGetLastError();
+}
+
 }  // namespace qg

@@ -188,6 +188,30 @@ __device__ __forceinline__ void dequant_vec(const uint4 v, uint32_t zero2, uint3
   }
 }
 
+// 32 e2m1 codes (one 16-byte vector, k in nibble order, low nibble first) ->
+// 32 e4m3 bytes, exactly (every e2m1 value is an e4m3 value).  prmt looks up
+// the e4m3 byte of the 3-bit magnitude in an 8-entry byte table; a second
+// prmt against 0x80 bytes turns each nibble's sign bit into bit 6 of its byte
+// (sign-replicate mode), which the final lop3 moves into bit 7.
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t c16) {
+  constexpr uint32_t kLo = 0x3C383000u;   // e4m3 of 0, 0.5, 1, 1.5
+  constexpr uint32_t kHi = 0x4C484440u;   // e4m3 of 2, 3, 4, 6
+  uint32_t mag, sgn, out;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(mag) : "r"(kLo), "r"(kHi), "r"(c16 & 0x7777u));
+  asm("prmt.b32 %0, %1, %1, %2;" : "=r"(sgn) : "r"(0x80808080u), "r"(c16));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(out) : "r"(sgn << 1), "r"(0x80808080u), "r"(mag));
+  return out;   // ((sgn << 1) & 0x80808080) | mag
+}
+
+__device__ __forceinline__ void dequant_vec_mx(const uint4 v, uint32_t (&out)[8]) {
+  const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    out[2 * w] = e2m1x4_to_e4m3x4(wds[w]);
+    out[2 * w + 1] = e2m1x4_to_e4m3x4(wds[w] >> 16);
+  }
+}
+
 template <bool FP16>
 __device__ __forceinline__ uint16_t to_out(float v) {
   if constexpr (FP16) {
@@ -208,9 +232,17 @@ __device__ __forceinline__ float from_out(uint16_t b) {
   }
 }
 
-template <int BT, bool FP16, bool GROUPED>
+// FMT: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 weights, e4m3
+// activations with per-row fp32 scales, block-scaled MMA, bf16 output).
+template <int BT, int FMT, bool GROUPED>
 __global__ void __launch_bounds__(kNumThreads, 1)
     w4a16_kernel(const __grid_constant__ CUtensorMap tmap_a, const W4A16Params p) {
+  constexpr bool FP16 = FMT == 1;
+  constexpr bool MX = FMT == 2;
+  // tensor-memory columns: dequantized weight slots, then (MX) the A and B
+  // scale factors, accumulators from column 256
+  constexpr int kSlotCols = MX ? 32 : kASlotCols;
+  constexpr uint32_t kSfaCol = 128, kSfbCol = 160, kAccCol = 256;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -226,7 +258,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint64_t* acc_full = a_empty + kASlots;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  SharedState* sh = reinterpret_cast<SharedState*>(drain + 1);
+  uint64_t* sfb_ready = drain + 1;
+  SharedState* sh = reinterpret_cast<SharedState*>(sfb_ready + 1);
   int* mt_prefix = reinterpret_cast<int*>(sh + 1);     // grouped: m-tile prefix [E+1]
   int* offs = mt_prefix + (GROUPED ? (p.num_experts + 1) : 0);   // grouped: offsets [E+1]
 
@@ -256,10 +289,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     return tc;
   };
 
-  const uint32_t act_bytes = BT * kTileK * 2;
+  uint64_t pol_stream = 0, pol_keep = 0;   // L2 policies (set by thread 0)
+  const uint32_t act_bytes = BT * kTileK * (MX ? 1 : 2);
   const uint32_t w_bytes = kTileBytes;
-  const uint32_t s_bytes = p.st * kTileN * 2;
+  const uint32_t s_bytes = MX ? kTileN * 4 : p.st * kTileN * 2;
   const uint32_t z_bytes = p.has_zp ? p.st * kTileN : 0;
+  auto scale_src = [&](int e, long long blk) {
+    return reinterpret_cast<const uint8_t*>(p.s) + e * p.s_expert_stride * 2 + blk * s_bytes;
+  };
+  auto load_act = [&](uint8_t* sp, uint64_t* bar, int kt, int row0) {
+    if constexpr (MX) {
+      tma_load_2d_hint(sp, &tmap_a, bar, kt * kTileK, row0, pol_keep);
+    } else {
+      tma_load_2d_hint(sp, &tmap_a, bar, kt * kTileK, row0, pol_keep);
+      tma_load_2d_hint(sp + BT * 128, &tmap_a, bar, kt * kTileK + 64, row0, pol_keep);
+    }
+  };
 
   // ---- producer state (thread 0): one (tile, k-tile) unit per pipeline stage
   Schedule psched;
@@ -269,7 +314,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   int pstage = 0;
   uint32_t pphase = 0;
   long long issued = 0;
-  uint64_t pol_stream = 0, pol_keep = 0;
   auto pnext = [&]() -> bool {   // advance to the next unit; false when none is left
     if (phave && ++pkt < pwi.k1) return true;
     if (!psched.next(pwi)) return false;
@@ -285,14 +329,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // weights first: they do not depend on the activations' producer
     bulk_load(sp + p.off_w, p.w + tc.e * p.w_expert_stride + blk * kTileBytes, w_bytes,
               &full[pstage], pol_stream);
-    bulk_load(sp + p.off_s, p.s + tc.e * p.s_expert_stride + blk * p.st * kTileN, s_bytes,
-              &full[pstage], pol_stream);
+    bulk_load(sp + p.off_s, scale_src(tc.e, blk), s_bytes, &full[pstage], pol_stream);
     if (p.has_zp)
       bulk_load(sp + p.off_z, p.z + tc.e * p.z_expert_stride + blk * p.st * kTileN, z_bytes,
                 &full[pstage], pol_stream);
-    tma_load_2d_hint(sp, &tmap_a, &full[pstage], pkt * kTileK, tc.row0, pol_keep);
-    tma_load_2d_hint(sp + BT * 128, &tmap_a, &full[pstage], pkt * kTileK + 64, tc.row0,
-                     pol_keep);
+    load_act(sp, &full[pstage], pkt, tc.row0);
     ++issued;
     if (++pstage == S) {
       pstage = 0;
@@ -314,6 +355,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(&acc_empty[i], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(sfb_ready, 4);
     sh->abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmap_a);
@@ -396,8 +438,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         mbar_arrive_expect_tx(&full[pstage], act_bytes + w_bytes + s_bytes + z_bytes);
         bulk_load(sp + p.off_w, p.w + tc.e * p.w_expert_stride + blk * kTileBytes, w_bytes,
                   &full[pstage], pol_stream);
-        bulk_load(sp + p.off_s, p.s + tc.e * p.s_expert_stride + blk * p.st * kTileN, s_bytes,
-                  &full[pstage], pol_stream);
+        bulk_load(sp + p.off_s, scale_src(tc.e, blk), s_bytes, &full[pstage], pol_stream);
         if (p.has_zp)
           bulk_load(sp + p.off_z, p.z + tc.e * p.z_expert_stride + blk * p.st * kTileN,
                     z_bytes, &full[pstage], pol_stream);
@@ -414,9 +455,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       for (int i = 0; i < pre; ++i) {   // stages 0 .. pre-1 of the first ring pass
         const TileCoord<BT> tc = coords(pre_wi[i].tile);
         uint8_t* sp = stage_base + i * p.stage_bytes;
-        tma_load_2d_hint(sp, &tmap_a, &full[i], pre_kt[i] * kTileK, tc.row0, pol_keep);
-        tma_load_2d_hint(sp + BT * 128, &tmap_a, &full[i], pre_kt[i] * kTileK + 64, tc.row0,
-                         pol_keep);
+        load_act(sp, &full[i], pre_kt[i], tc.row0);
       }
       while (pnext()) {
         if (!mbar_wait(&empty[pstage], pphase ^ 1, abort_flag, p.status, lim, kStatusTimeout))
@@ -434,17 +473,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (elect_one()) {
-      const uint32_t idesc = idesc_f16(FP16 ? 0u : 1u, BT);
+      const uint32_t idesc = MX ? idesc_mxf8f6f4_e4m3(BT) : idesc_f16(FP16 ? 0u : 1u, BT);
       int stage = 0, slot = 0, acc = 0;
       uint32_t phase = 0, aphase = 0, accphase = 0;
       WorkItem wi;
       bool ok = true;
+      if constexpr (MX)   // the B scale factors (all 1.0) are written by the epilogue warps
+        ok = mbar_wait(sfb_ready, 0, abort_flag, p.status, lim, kStatusTimeout);
       while (ok && sched.next(wi)) {
         if (!mbar_wait(&acc_empty[acc], accphase ^ 1, abort_flag, p.status, lim,
                        kStatusTimeout))
           break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + kASlots * kASlotCols + acc * BT;
+        const uint32_t d_tmem = tmem_base + kAccCol + acc * BT;
         for (int kt = wi.k0; kt < wi.k1; ++kt) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim, kStatusTimeout) ||
               !mbar_wait(&a_full[slot], aphase, abort_flag, p.status, lim, kStatusTimeout)) {
@@ -453,11 +494,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           tc_fence_after();
           const uint32_t b0 = smem_u32(stage_base + stage * p.stage_bytes);
+          if constexpr (MX) {
+            // four K=32 steps over one 128-byte activation row; the scale
+            // factor id selects the step's byte of the scale columns
 #pragma unroll
-          for (int ks = 0; ks < kTileK / 16; ++ks) {
-            const uint32_t boff = (ks >> 2) * (BT * 128) + (ks & 3) * 32;
-            mma_ts_f16(d_tmem, tmem_base + slot * kASlotCols + ks * 8,
-                       smem_desc_sw128(b0 + boff), idesc, (kt > wi.k0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks)
+              mma_ts_mxf8f6f4(d_tmem, tmem_base + slot * kSlotCols + ks * 8,
+                              smem_desc_sw128(b0 + ks * 32), idesc_with_sf_ids(idesc, ks, ks),
+                              tmem_base + kSfaCol + slot * 4, tmem_base + kSfbCol,
+                              (kt > wi.k0 || ks > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < kTileK / 16; ++ks) {
+              const uint32_t boff = (ks >> 2) * (BT * 128) + (ks & 3) * 32;
+              mma_ts_f16(d_tmem, tmem_base + slot * kSlotCols + ks * 8,
+                         smem_desc_sw128(b0 + boff), idesc, (kt > wi.k0 || ks > 0) ? 1u : 0u);
+            }
           }
           mma_commit(&empty[stage]);
           mma_commit(&a_empty[slot]);
@@ -507,6 +559,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           const uint8_t* sp = stage_base + stage * p.stage_bytes;
           const uint4* wv = reinterpret_cast<const uint4*>(sp + p.off_w);
+          if constexpr (MX) {
+            // 128 e2m1 codes of this row -> 128 e4m3 bytes (32 columns), and
+            // its four e8m0 block scales -> the slot's four scale columns
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = wv[(q * 4 + j) * 32 + lane];
+            const uint32_t sf = reinterpret_cast<const uint32_t*>(sp + p.off_s)[row];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t o8[8];
+              dequant_vec_mx(v[j], o8);
+              tmem_st8(tmem_base + lane_addr + slot * kSlotCols + j * 8, o8);
+            }
+            const uint32_t sf4[4] = {sf, sf, sf, sf};
+            tmem_st4(tmem_base + lane_addr + kSfaCol + slot * 4, sf4);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[slot]);
+          } else {
           const uint16_t* sv = reinterpret_cast<const uint16_t*>(sp + p.off_s);
           const uint8_t* zv = sp + p.off_z;
           // every shared-memory read of the unit first, then the arithmetic
@@ -521,7 +593,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
             zero2[j] = (magic16 + zq) * 0x00010001u;
           }
-          const uint32_t tbase = tmem_base + lane_addr + slot * kASlotCols;
+          const uint32_t tbase = tmem_base + lane_addr + slot * kSlotCols;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint32_t out[16];
@@ -532,6 +604,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&a_full[slot]);
+          }
         }
         if (++stage == S) {
           stage = 0;
@@ -549,6 +622,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int q = warp & 3;
     const int col = q * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    if constexpr (MX) {   // B scale factors: every byte 2^0 (e8m0 127)
+      uint32_t ones[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ones[i] = 0x7F7F7F7Fu;
+      tmem_st32(tmem_base + lane_addr + kSfbCol, ones);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfb_ready);
+    }
     int acc = 0;
     uint32_t accphase = 0;
     WorkItem wi;
@@ -560,7 +643,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int n = tc.nt * kTileN + col;
       float bias = 0.f;
       if (p.bias) bias = from_out<FP16>(p.bias[(long long)tc.e * p.n + n]);
-      const uint32_t tbase = tmem_base + lane_addr + kASlots * kASlotCols + acc * BT;
+      const uint32_t tbase = tmem_base + lane_addr + kAccCol + acc * BT;
+      // W4A8: the per-row activation scale multiplies the fp32 accumulator
+      auto row_scale = [&](int m) -> float {
+        if constexpr (MX) return p.a_scale[tc.row0 + m];
+        else return 1.f;
+      };
       // partial slot of this CTA for this segment (split tiles only)
       const long long tl = wi.tile - sched.W * sched.G;
       const long long u_start = tl * p.kt;
@@ -585,7 +673,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int m = mc * 16 + i;
             if (m < tc.rows)
               p.c[(long long)(tc.row0 + m) * p.n + n] =
-                  to_out<FP16>(__uint_as_float(v[i]) + bias);
+                  to_out<FP16>(__uint_as_float(v[i]) * row_scale(m) + bias);
           }
         } else if (p.deterministic) {
           // partial tile, column-major [col][BT]: this thread's column is contiguous
@@ -644,7 +732,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 for (int i = 0; i < 4; ++i) {
                   const int m = m0 + 4 * j + i;
                   if (m < tc.rows)
-                    p.c[(long long)(tc.row0 + m) * p.n + n] = to_out<FP16>(af[i] + bias);
+                    p.c[(long long)(tc.row0 + m) * p.n + n] =
+                        to_out<FP16>(af[i] * row_scale(m) + bias);
                 }
               }
             }
@@ -689,7 +778,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               if (m0 + i < tc.rows)
-                p.c[(long long)(tc.row0 + m0 + i) * p.n + n] = to_out<FP16>(accf[i] + bias);
+                p.c[(long long)(tc.row0 + m0 + i) * p.n + n] =
+                    to_out<FP16>(accf[i] * row_scale(m0 + i) + bias);
             }
           }
           if (lane == 0) *counter = 0;   // ready for the next launch
@@ -707,10 +797,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int BT, bool FP16, bool GROUPED>
+template <int BT, int FMT, bool GROUPED>
 static cudaError_t launch_t(const CUtensorMap& tmap, const W4A16Params& p, int grid,
                             cudaStream_t stream) {
-  auto kern = w4a16_kernel<BT, FP16, GROUPED>;
+  auto kern = w4a16_kernel<BT, FMT, GROUPED>;
   static int attr_set = 0;   // largest dynamic shared memory size enabled so far
   if (p.smem_bytes > attr_set) {
     cudaError_t err =
@@ -731,25 +821,29 @@ static cudaError_t launch_t(const CUtensorMap& tmap, const W4A16Params& p, int g
   return cudaLaunchKernelEx(&cfg, kern, tmap, p);
 }
 
-template <bool FP16, bool GROUPED>
+template <int FMT, bool GROUPED>
 static cudaError_t launch_bt(const CUtensorMap& tmap, const W4A16Params& p, int bt, int grid,
                              cudaStream_t stream) {
   switch (bt) {
-    case 16: return launch_t<16, FP16, GROUPED>(tmap, p, grid, stream);
-    case 32: return launch_t<32, FP16, GROUPED>(tmap, p, grid, stream);
-    case 64: return launch_t<64, FP16, GROUPED>(tmap, p, grid, stream);
-    case 128: return launch_t<128, FP16, GROUPED>(tmap, p, grid, stream);
+    case 16: return launch_t<16, FMT, GROUPED>(tmap, p, grid, stream);
+    case 32: return launch_t<32, FMT, GROUPED>(tmap, p, grid, stream);
+    case 64: return launch_t<64, FMT, GROUPED>(tmap, p, grid, stream);
+    case 128: return launch_t<128, FMT, GROUPED>(tmap, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const W4A16Params& p, int block_tok,
-                         bool fp16, bool grouped, int grid, cudaStream_t stream) {
-  if (fp16)
-    return grouped ? launch_bt<true, true>(tmap_a, p, block_tok, grid, stream)
-                   : launch_bt<true, false>(tmap_a, p, block_tok, grid, stream);
-  return grouped ? launch_bt<false, true>(tmap_a, p, block_tok, grid, stream)
-                 : launch_bt<false, false>(tmap_a, p, block_tok, grid, stream);
+                         int fmt, bool grouped, int grid, cudaStream_t stream) {
+  switch (fmt) {
+    case 0: return grouped ? launch_bt<0, true>(tmap_a, p, block_tok, grid, stream)
+                           : launch_bt<0, false>(tmap_a, p, block_tok, grid, stream);
+    case 1: return grouped ? launch_bt<1, true>(tmap_a, p, block_tok, grid, stream)
+                           : launch_bt<1, false>(tmap_a, p, block_tok, grid, stream);
+    case 2: return grouped ? launch_bt<2, true>(tmap_a, p, block_tok, grid, stream)
+                           : launch_bt<2, false>(tmap_a, p, block_tok, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // ------------------------------------------------------------ debug dequant
@@ -796,6 +890,35 @@ cudaError_t launch_debug_dequant(const uint8_t* w, const uint16_t* s, const uint
   else
     debug_dequant_kernel<false><<<blocks, threads, 0, stream>>>(w, s, z, out, (int)n, (int)k,
                                                                  group, has_zp);
+  return cudaGetLastError();
+}
+
+// out[k, n] = the e4m3 byte the W4A8 kernel writes to tensor memory for the
+// code of W[k, n] (the e8m0 block scale is applied by the MMA, not here).
+__global__ void debug_mx_codes_kernel(const uint8_t* w, uint8_t* out, int n, int k) {
+  const int KT = k / kTileK;
+  const long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long total = (long long)(n / kTileN) * KT * 512;
+  if (vec >= total) return;
+  const long long blk = vec / 512;
+  const int v = (int)(vec % 512);
+  const int nt = (int)(blk / KT), kt = (int)(blk % KT);
+  const int t = v & 31, j = (v >> 5) & 3, q = v >> 7;
+  uint32_t o[8];
+  dequant_vec_mx(reinterpret_cast<const uint4*>(w)[vec], o);
+  const int nn = nt * kTileN + q * 32 + t;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const int kk = kt * kTileK + j * 32 + c;
+    out[(long long)kk * n + nn] = (uint8_t)((o[c >> 2] >> (8 * (c & 3))) & 0xFF);
+  }
+}
+
+cudaError_t launch_debug_mx_codes(const uint8_t* w, uint8_t* out_kn, int64_t n, int64_t k,
+                                  cudaStream_t stream) {
+  const long long total = (n / kTileN) * (k / kTileK) * 512;
+  debug_mx_codes_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(w, out_kn, (int)n,
+                                                                           (int)k);
   return cudaGetLastError();
 }
 

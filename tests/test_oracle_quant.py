@@ -125,6 +125,7 @@ def test_mxfp4_pack_handbuilt():
     b = np.full((2, 2), 127, dtype=np.uint8)
     b[1, 1] = 3
     p, bs = quant.pack_mxfp4(codes, b)
+    assert p.flags.c_contiguous and bs.flags.c_contiguous
     assert p.shape == (2, 32) and p[0, 0] == 0x21 and p[1, 31] == 0xF0
     assert bs.shape == (2, 2) and bs[1, 1] == 3
     c2, b2 = quant.unpack_mxfp4(p, bs)
@@ -177,3 +178,26 @@ def test_tiled_scales_and_zeros_scalar_spec(gsize):
             idx = ((nt * (k // 128) + kt) * st + sg) * 128 + r
             assert ts[idx] == sb[kk // gsize, nn]
             assert tz[idx] == z[kk // gsize, nn]
+
+
+def test_mxfp4_tiled_layout_scalar_spec():
+    g = np.random.default_rng(14)
+    n, k = 256, 384
+    codes = g.integers(0, 256, (n, k // 2)).astype(np.uint8)
+    b = g.integers(100, 140, (n, k // 32)).astype(np.uint8)
+    ws = layout.tiled_mxfp4_weights(codes)
+    ss = layout.tiled_mxfp4_scales(b)
+    assert ws.size == n * k // 2 and ss.size == n * k // 32
+    kt_count = k // 128
+    for _ in range(2000):
+        nn, kk = int(g.integers(0, n)), int(g.integers(0, k))
+        nt, nl = divmod(nn, 128)
+        kt, kl = divmod(kk, 128)
+        qd, t = divmod(nl, 32)
+        j, r = divmod(kl, 32)
+        vec = (nt * kt_count + kt) * 512 + (qd * 4 + j) * 32 + t
+        byte = int(ws[vec * 16 + r // 2])
+        nib = (byte >> 4) if r % 2 else (byte & 0xF)
+        sb = int(codes[nn, kk // 2])
+        assert nib == ((sb >> 4) if kk % 2 else (sb & 0xF))
+        assert ss[(nt * kt_count + kt) * 512 + nl * 4 + kl // 32] == b[nn, kk // 32]
