@@ -218,9 +218,7 @@ class GemmPoint:
         else:
             import copy
             self.lin = copy.copy(src.lin)
-            self.lin.w = src.lin.w.clone()
-            self.lin.s = src.lin.s.clone()
-            self.lin.z = None if src.lin.z is None else src.lin.z.clone()
+            self.lin.packed = src.lin.packed.clone()
             self.a = src.a.clone()
         if self.mx:
             self.a8 = torch.empty(m, k, dtype=torch.uint8, device=device)
@@ -243,12 +241,10 @@ class GemmPoint:
         if self.mx:
             Q.check(Q.qgemm_quantize_act_fp8(self.a, m, self.p["k"], self.a8, self.a_scale))
             Q.check(Q.qgemm_run(self.lin.layer, self.lin.dense, None, m, self.a8, self.a_scale,
-                                self.lin.w, self.lin.s, None, None, self.c, self.ws,
-                                self.ws.numel()))
+                                self.lin.packed, None, self.c, self.ws, self.ws.numel()))
         else:
             Q.check(Q.qgemm_run(self.lin.layer, self.lin.dense, None, m, self.a, None,
-                                self.lin.w, self.lin.s, self.lin.z, None, self.c, self.ws,
-                                self.ws.numel()))
+                                self.lin.packed, None, self.c, self.ws, self.ws.numel()))
 
     def launch_e2e(self):
         self.a.copy_(self.a_host, non_blocking=True)

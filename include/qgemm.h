@@ -156,25 +156,26 @@ typedef struct {
  */
 
 /*
- * Bytes of the packed (kernel-layout) tensors for one layer (all experts).
- * Any output pointer may be NULL.  Returns INVALID_ARG / UNSUPPORTED on a bad
- * config.
+ * Bytes of the packed (kernel-layout) buffer of one layer (all experts).
+ * Returns INVALID_ARG / UNSUPPORTED on a bad config.
  */
-qgemm_status qgemm_packed_sizes(const qgemm_layer_config* layer, size_t* w_bytes,
-                                size_t* s_bytes, size_t* z_bytes);
+qgemm_status qgemm_packed_size(const qgemm_layer_config* layer, size_t* bytes);
 
 /*
  * Preprocessing (the "repack for the target kernel" step): validates the
  * config and rearranges the standard-format tensors (device, layout above)
- * into the kernel layout (device outputs, sizes from qgemm_packed_sizes).
- * INT4 codes are re-encoded as offset binary (q + 8); nothing else changes
- * value, so the packed tensors mean exactly what the standard ones mean.
- * qzeros / z_out must be NULL unless zero_format = QGEMM_Z_UINT4.  Runs once
- * per layer; the outputs are read-only afterwards.
+ * into one packed device buffer (`packed`, qgemm_packed_size bytes, 16-byte
+ * aligned).  Per expert, the buffer holds one block per (128-row n-tile,
+ * 128-deep k-tile), n-tile major: the tile's codes, then its scales, then its
+ * zero points, so that consecutive k-tiles of a tile are contiguous.  INT4
+ * codes are re-encoded as offset binary (q + 8); nothing else changes value,
+ * so the packed buffer means exactly what the standard tensors mean.  qzeros
+ * must be NULL unless zero_format = QGEMM_Z_UINT4.  Runs once per layer; the
+ * buffer is read-only afterwards.
  */
 qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qweight,
-                                const void* scales, const void* qzeros, void* w_out,
-                                void* s_out, void* z_out, void* stream);
+                                const void* scales, const void* qzeros, void* packed,
+                                void* stream);
 
 /*
  * Workspace bytes qgemm_run / qgemm_grouped_run need for `m` rows (for the
@@ -196,7 +197,7 @@ qgemm_status qgemm_workspace_init(void* workspace, size_t bytes, void* stream);
  *   m         rows of A and C (0 is allowed and launches nothing)
  *   a         device, [m, K] in act_dtype (e4m3 codes for W4A8)
  *   a_scale   device fp32 [m] per-row activation scales (W4A8), else NULL
- *   w, s, z   device packed tensors from qgemm_pack_weights (z NULL if none)
+ *   packed    device packed buffer from qgemm_pack_weights
  *   bias      device [N] in out_dtype, or NULL when has_bias = 0
  *   c         device, [m, N] in out_dtype
  *   workspace device, >= qgemm_workspace_size bytes, zero-initialised once
@@ -205,9 +206,8 @@ qgemm_status qgemm_workspace_init(void* workspace, size_t bytes, void* stream);
  */
 qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_config* compute,
                        const qgemm_tuning_config* tuning, int64_t m, const void* a,
-                       const float* a_scale, const void* w, const void* s, const void* z,
-                       const void* bias, void* c, void* workspace, size_t workspace_bytes,
-                       void* stream);
+                       const float* a_scale, const void* packed, const void* bias, void* c,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * qgemm_run without a workspace argument, for callers that cannot allocate
@@ -231,8 +231,8 @@ qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_conf
 qgemm_status qgemm_run_noalloc(const qgemm_layer_config* layer,
                                const qgemm_compute_config* compute,
                                const qgemm_tuning_config* tuning, int64_t m, const void* a,
-                               const float* a_scale, const void* w, const void* s, const void* z,
-                               const void* bias, void* c, void* stream);
+                               const float* a_scale, const void* packed, const void* bias,
+                               void* c, void* stream);
 
 /*
  * Grouped (MoE) quantized GEMM over router-permuted rows: for each expert e,
@@ -240,7 +240,7 @@ qgemm_status qgemm_run_noalloc(const qgemm_layer_config* layer,
  *   expert_offsets device int32 [E+1], non-decreasing, offsets[0] = 0,
  *                  offsets[E] = total_rows (e.g. from qgemm_moe_permute)
  *   total_rows     number of rows of A and C (host value)
- *   w, s, z        packed tensors of all E experts (stacked)
+ *   packed         packed buffer of all E experts
  *   bias           device [E, N] or NULL
  * The tile schedule is built on the device from expert_offsets: no host
  * synchronization is needed between the permute and the GEMM.
@@ -249,8 +249,8 @@ qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
                                const qgemm_compute_config* compute,
                                const qgemm_tuning_config* tuning, const int32_t* expert_offsets,
                                int64_t total_rows, const void* a, const float* a_scale,
-                               const void* w, const void* s, const void* z, const void* bias,
-                               void* c, void* workspace, size_t workspace_bytes, void* stream);
+                               const void* packed, const void* bias, void* c, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /*
  * Per-token FP8 activation quantization (W4A8 path):
@@ -300,12 +300,14 @@ qgemm_status qgemm_moe_combine(const void* y2, const int32_t* inv_perm,
                                int64_t hidden, void* y, void* stream);
 
 /*
- * Debug: write the dequantized weights of a packed W4A16 layer (expert 0 or
- * the dense layer) as out[k, n] in act_dtype (device, [K, N]), using exactly
- * the kernels' dequantization arithmetic.
+ * Debug: the weights of a packed layer (expert 0 or the dense layer) as the
+ * kernels feed them to the tensor core, written as out[k, n] (device, [K, N]):
+ * W4A16 the dequantized values in act_dtype, computed with exactly the
+ * kernels' arithmetic; MXFP4 the e4m3 byte of each e2m1 code (the e8m0 block
+ * scale is applied inside the MMA).
  */
-qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* w, const void* s,
-                                 const void* z, void* out_kn, void* stream);
+qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* packed,
+                                 void* out_kn, void* stream);
 
 /*
  * Synchronizes `stream`, reads the workspace status word written by the GEMM

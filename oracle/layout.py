@@ -38,6 +38,13 @@ MXFP4 tiled layout (same tiling):
   scales: one 512-byte block per (nt, kt); bytes 4 r .. 4 r + 3 are the e8m0
     exponents of row n = 128 nt + r for k = 128 kt + [0, 32), [32, 64),
     [64, 96), [96, 128) in that order.
+
+Packed buffer (what the pack entry point writes): the three streams above
+interleaved block by block, so that block (nt, kt) is one contiguous run of
+bytes [weights block][scales block][zeros block] and the blocks follow in the
+same nt-major order; experts follow one another, each expert's blocks
+contiguous.  Block sizes: 8192 + 256 ST (+ 128 ST with zeros) bytes for
+INT4/UINT4, 8192 + 512 for MXFP4.
 """
 
 from __future__ import annotations
@@ -140,3 +147,39 @@ def tiled_mxfp4_scales(b_nk) -> np.ndarray:
     kt_n, nt_n = kb // 4, n // TILE_N
     b4 = b.reshape(nt_n, TILE_N, kt_n, 4)
     return np.ascontiguousarray(b4.transpose(0, 2, 1, 3)).reshape(-1)
+
+
+def interleave_blocks(*streams_and_sizes) -> np.ndarray:
+    """Interleave per-block streams: arguments are (byte stream, block bytes)
+    pairs with the same number of blocks; block i of the result is block i of
+    each stream in argument order."""
+    parts = []
+    count = None
+    for stream, size in streams_and_sizes:
+        b = np.ascontiguousarray(stream).view(np.uint8).reshape(-1)
+        if b.size % size:
+            raise ValueError("stream is not a whole number of blocks")
+        if count is None:
+            count = b.size // size
+        elif b.size // size != count:
+            raise ValueError("streams hold different block counts")
+        parts.append(b.reshape(count, size))
+    return np.concatenate(parts, axis=1).reshape(-1)
+
+
+def packed_w4(q, s_bits, z, g: int, signed: bool) -> np.ndarray:
+    """Codes q[K, N], scale bits [K/g, N] and zero points [K/g, N] (None for
+    signed INT4) -> the packed buffer of one matrix."""
+    k = np.asarray(q).shape[0]
+    st = scale_groups_per_tile(g)
+    pieces = [(tiled_weights(q, signed), 8192), (tiled_scales(s_bits, g, k), 256 * st)]
+    if z is not None:
+        pieces.append((tiled_zeros(z, g, k), 128 * st))
+    return interleave_blocks(*pieces)
+
+
+def packed_mxfp4(codes_nk, b_nk) -> np.ndarray:
+    """Standard MXFP4 codes [N, K/2] and exponents [N, K/32] -> the packed
+    buffer of one matrix."""
+    return interleave_blocks((tiled_mxfp4_weights(codes_nk), 8192),
+                             (tiled_mxfp4_scales(b_nk), 512))

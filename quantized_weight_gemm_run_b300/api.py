@@ -45,16 +45,13 @@ class W4A16Linear:
             Q.QGEMM_S_FP16 if adt == Q.QGEMM_FP16 else Q.QGEMM_S_BF16,
             Q.QGEMM_Z_UINT4 if asym else Q.QGEMM_Z_NONE, adt, adt,
             1 if bias is not None else 0, num_experts)
-        st, wb, sb, zb = Q.qgemm_packed_sizes(self.layer)
+        st, nbytes = Q.qgemm_packed_size(self.layer)
         Q.check(st)
         dev = qweight.device
         qweight, scales = qweight.contiguous(), scales.contiguous()
         qzeros = None if qzeros is None else qzeros.contiguous()
-        self.w = torch.empty(wb, dtype=torch.uint8, device=dev)
-        self.s = torch.empty(sb // 2, dtype=torch.int16, device=dev)
-        self.z = torch.empty(zb, dtype=torch.uint8, device=dev) if asym else None
-        Q.check(Q.qgemm_pack_weights(self.layer, qweight, scales, qzeros, self.w, self.s,
-                                     self.z))
+        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        Q.check(Q.qgemm_pack_weights(self.layer, qweight, scales, qzeros, self.packed))
         self.bias = bias
         self.tuning = tuning
         self.ws = Workspace(dev)
@@ -70,8 +67,8 @@ class W4A16Linear:
         st, nbytes = Q.qgemm_workspace_size(self.layer, self.dense, self.tuning, max(m, 1))
         Q.check(st)
         ws = self.ws.get(nbytes)
-        Q.check(Q.qgemm_run(self.layer, self.dense, self.tuning, m, a, None, self.w, self.s,
-                            self.z, self.bias, out, ws, ws.numel()))
+        Q.check(Q.qgemm_run(self.layer, self.dense, self.tuning, m, a, None, self.packed,
+                            self.bias, out, ws, ws.numel()))
         return out
 
     def run_grouped(self, a_perm: torch.Tensor, offsets: torch.Tensor,
@@ -83,14 +80,13 @@ class W4A16Linear:
         Q.check(st)
         ws = self.ws.get(nbytes)
         Q.check(Q.qgemm_grouped_run(self.layer, self.grouped, self.tuning, offsets, rows, a_perm,
-                                    None, self.w, self.s, self.z, self.bias, out, ws,
-                                    ws.numel()))
+                                    None, self.packed, self.bias, out, ws, ws.numel()))
         return out
 
     def dequantized(self) -> torch.Tensor:
         """W^[K, N] as the kernels feed it to the tensor core (expert 0)."""
-        out = torch.empty(self.k, self.n, dtype=self.act_dtype, device=self.w.device)
-        Q.check(Q.qgemm_debug_dequant(self.layer, self.w, self.s, self.z, out))
+        out = torch.empty(self.k, self.n, dtype=self.act_dtype, device=self.packed.device)
+        Q.check(Q.qgemm_debug_dequant(self.layer, self.packed, out))
         return out
 
     def status(self) -> int:
@@ -108,14 +104,12 @@ class W4A8Linear:
         self.layer = Q.layer_config(n, k, 32, Q.QGEMM_W_MXFP4, Q.QGEMM_S_E8M0, Q.QGEMM_Z_NONE,
                                     Q.QGEMM_FP8E4M3, Q.QGEMM_BF16,
                                     1 if bias is not None else 0, num_experts)
-        st, wb, sb, _ = Q.qgemm_packed_sizes(self.layer)
+        st, nbytes = Q.qgemm_packed_size(self.layer)
         Q.check(st)
         dev = codes.device
         codes, scales = codes.contiguous(), scales.contiguous()
-        self.w = torch.empty(wb, dtype=torch.uint8, device=dev)
-        self.s = torch.empty(sb, dtype=torch.uint8, device=dev)
-        self.z = None
-        Q.check(Q.qgemm_pack_weights(self.layer, codes, scales, None, self.w, self.s, None))
+        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        Q.check(Q.qgemm_pack_weights(self.layer, codes, scales, None, self.packed))
         self.bias, self.tuning = bias, tuning
         self.ws = Workspace(dev)
         det = 1 if deterministic else 0
@@ -138,8 +132,8 @@ class W4A8Linear:
         st, nbytes = Q.qgemm_workspace_size(self.layer, self.dense, self.tuning, max(m, 1))
         Q.check(st)
         ws = self.ws.get(nbytes)
-        Q.check(Q.qgemm_run(self.layer, self.dense, self.tuning, m, a8, a_scale, self.w, self.s,
-                            None, self.bias, out, ws, ws.numel()))
+        Q.check(Q.qgemm_run(self.layer, self.dense, self.tuning, m, a8, a_scale, self.packed,
+                            self.bias, out, ws, ws.numel()))
         return out
 
     def __call__(self, x: torch.Tensor, out=None) -> torch.Tensor:
@@ -148,8 +142,8 @@ class W4A8Linear:
 
     def codes_e4m3(self) -> torch.Tensor:
         """The e4m3 bytes the kernel feeds the tensor core, uint8 [K, N]."""
-        out = torch.empty(self.k, self.n, dtype=torch.uint8, device=self.w.device)
-        Q.check(Q.qgemm_debug_dequant(self.layer, self.w, self.s, None, out))
+        out = torch.empty(self.k, self.n, dtype=torch.uint8, device=self.packed.device)
+        Q.check(Q.qgemm_debug_dequant(self.layer, self.packed, out))
         return out
 
     def status(self) -> int:

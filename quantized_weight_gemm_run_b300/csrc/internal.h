@@ -14,6 +14,10 @@ constexpr int kTileBytes = kTileN * kTileK / 2;   // packed 4-bit weights per ti
 constexpr int kNumThreads = 512;  // 16 warps: producer, MMA, TMEM, spare, 8 dequant, 4 epilogue
 constexpr int kASlots = 4;        // TMEM slots for dequantized weight tiles
 constexpr int kASlotCols = 64;    // TMEM columns per slot (128 K x 16 bit)
+// k-tiles ("units") per pipeline stage for a token tile of bt rows: a stage is
+// filled by one bulk copy of its weights and one TMA box of its activations,
+// so small token tiles group several k-tiles to keep every copy large.
+__host__ __device__ constexpr int units_per_stage(int bt) { return bt <= 32 ? 4 : bt == 64 ? 2 : 1; }
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusDevice = 2;
 constexpr int kMaxExperts = 1024;      // grouped GEMM
@@ -28,9 +32,7 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(int64_t max_tiles, int grid, int block_tok);
 
 struct W4A16Params {
-  const uint8_t* w;          // tiled weights (all experts)
-  const uint16_t* s;         // tiled scales
-  const uint8_t* z;          // tiled zero points or null
+  const uint8_t* w;          // packed blocks of all experts: [weights][scales][zeros]
   const uint16_t* bias;      // [E, N] or null
   uint16_t* c;               // [rows, N]
   const float* a_scale;      // W4A8: per-row activation scales [rows], else null
@@ -43,9 +45,9 @@ struct W4A16Params {
   int has_zp;
   const int* expert_offsets; // device [E+1] or null (dense)
   int num_experts;
-  long long w_expert_stride; // bytes
-  long long s_expert_stride; // uint16 elements
-  long long z_expert_stride; // bytes
+  long long w_expert_stride; // bytes between experts' packed blocks
+  int block_bytes;           // one (n-tile, k-tile) block: 8192 + scale + zero bytes
+  int s_off, z_off;          // scales and zero points inside a block
   float* partials;           // fixed-order: two slots per CTA; atomic: one per split tile
   int deterministic;         // 1: fixed-order split-K reduction
   int* counters;
@@ -53,42 +55,39 @@ struct W4A16Params {
   long long max_tiles;
   int stages;
   int stage_bytes;
-  int off_w, off_s, off_z;   // within a stage
+  int off_w;                 // first packed block inside a stage
   int smem_bytes;            // total dynamic shared memory
   unsigned long long wait_limit_ns;
 };
 
 // Host-side plan for one W4A16 launch.
-struct W4A16Plan {
-  int block_tok;
-  int stages;
-  int grid;
-  int st;
-  int stage_bytes, off_w, off_s, off_z, smem_bytes;
-};
-
 int device_sm_count();
-W4A16Plan plan_w4a16(int block_tok, int stages, int max_ctas, int64_t units, int group,
-                     int has_zp);
 // fmt: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 x e4m3, bf16 out)
 cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const W4A16Params& p, int block_tok,
                          int fmt, bool grouped, int grid, cudaStream_t stream);
 
-cudaError_t launch_repack_mxfp4(const uint8_t* codes, const uint8_t* scales, uint8_t* w_out,
-                                uint8_t* s_out, int64_t n, int64_t k, int experts,
-                                cudaStream_t stream);
+cudaError_t launch_repack_mxfp4(const uint8_t* codes, const uint8_t* scales, uint8_t* packed,
+                                int64_t n, int64_t k, int experts, cudaStream_t stream);
 
 cudaError_t launch_debug_mx_codes(const uint8_t* w, uint8_t* out_kn, int64_t n, int64_t k,
                                   cudaStream_t stream);
 
-cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
-                             const int32_t* qzeros, uint8_t* w_out, uint16_t* s_out,
-                             uint8_t* z_out, int64_t n, int64_t k, int group, int signed_q,
-                             int experts, cudaStream_t stream);
+// Packed block of one (n-tile, k-tile): 8192 bytes of codes, then the scales
+// (W4A16: 128 * st 16-bit words; MXFP4: 128 32-bit words), then the zero
+// points (128 * st bytes) when the format has them.
+__host__ __device__ constexpr int packed_scale_bytes(bool mx, int st) {
+  return mx ? kTileN * 4 : st * kTileN * 2;
+}
+__host__ __device__ constexpr int packed_block_bytes(bool mx, int st, bool zp) {
+  return kTileBytes + packed_scale_bytes(mx, st) + (zp ? st * kTileN : 0);
+}
 
-cudaError_t launch_debug_dequant(const uint8_t* w, const uint16_t* s, const uint8_t* z,
-                                 uint16_t* out, int64_t n, int64_t k, int group, int has_zp,
-                                 bool fp16, cudaStream_t stream);
+cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
+                             const int32_t* qzeros, uint8_t* packed, int64_t n, int64_t k,
+                             int group, int signed_q, int experts, cudaStream_t stream);
+
+cudaError_t launch_debug_dequant(const uint8_t* packed, uint16_t* out, int64_t n, int64_t k,
+                                 int group, int has_zp, bool fp16, cudaStream_t stream);
 
 cudaError_t launch_act_quant_fp8(const uint16_t* x, int64_t m, int64_t k, uint8_t* a8,
                                  float* scale, cudaStream_t stream);
@@ -109,6 +108,10 @@ cudaError_t launch_combine(const uint16_t* y2, const int32_t* inv_perm, const fl
 int set_last_error(int status, const char* message);
 int dense_workspace_bytes(const void* layer, const void* tuning, int64_t m, size_t* must_clear,
                           size_t* total);
+
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    const uint64_t dims[3], const uint64_t strides_bytes[2],
+                    const uint32_t box[3], CUtensorMapSwizzle swizzle);
 
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,

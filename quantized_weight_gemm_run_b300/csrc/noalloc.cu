@@ -65,16 +65,16 @@ cudaError_t scratch_for_current_device(void** out) {
 extern "C" qgemm_status qgemm_run_noalloc(const qgemm_layer_config* layer,
                                           const qgemm_compute_config* compute,
                                           const qgemm_tuning_config* tuning, int64_t m,
-                                          const void* a, const float* a_scale, const void* w,
-                                          const void* s, const void* z, const void* bias,
-                                          void* c, void* stream) {
+                                          const void* a, const float* a_scale,
+                                          const void* packed, const void* bias, void* c,
+                                          void* stream) {
   using namespace qg;
   if (!compute || compute->gemm_type != QGEMM_GEMM_DENSE)
     return qgemm_status(set_last_error(QGEMM_ERR_INVALID_ARG,
                                        "qgemm_run_noalloc runs dense GEMMs only"));
   if (m < 0) return qgemm_status(set_last_error(QGEMM_ERR_INVALID_ARG, "m is negative"));
   if (m == 0)
-    return qgemm_run(layer, compute, tuning, 0, a, a_scale, w, s, z, bias, c, nullptr, 0, stream);
+    return qgemm_run(layer, compute, tuning, 0, a, a_scale, packed, bias, c, nullptr, 0, stream);
   size_t must_clear = 0, need = 0;
   const int st = dense_workspace_bytes(layer, tuning, m, &must_clear, &need);
   if (st != QGEMM_OK) return qgemm_status(st);
@@ -93,6 +93,6 @@ extern "C" qgemm_status qgemm_run_noalloc(const qgemm_layer_config* layer,
   e = cudaMemsetAsync(scratch, 0, must_clear, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return qgemm_status(set_last_error(QGEMM_ERR_CUDA, cudaGetErrorString(e)));
-  return qgemm_run(layer, compute, tuning, m, a, a_scale, w, s, z, bias, c, scratch,
+  return qgemm_run(layer, compute, tuning, m, a, a_scale, packed, bias, c, scratch,
                    kNoAllocScratchBytes, stream);
 }

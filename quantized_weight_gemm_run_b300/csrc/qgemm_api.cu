@@ -174,11 +174,12 @@ static int heuristic_block_tok(int64_t rows_per_group) {
 // W4A8 stages hold an 8-bit activation tile and 4 e8m0 bytes per weight row.
 static void stage_geometry(int bt, int st, int has_zp, bool mx, int* stage_bytes, int* off_w,
                            int* off_s, int* off_z) {
-  const int act = bt * kTileK * (mx ? 1 : 2);
+  const int r = units_per_stage(bt);
+  const int act = r * bt * kTileK * (mx ? 1 : 2);
   *off_w = act;
-  *off_s = act + kTileBytes;
-  *off_z = *off_s + (mx ? kTileN * 4 : st * kTileN * 2);
-  const int end = *off_z + (has_zp ? st * kTileN : 0);
+  *off_s = kTileBytes;                                   // inside a packed block
+  *off_z = kTileBytes + packed_scale_bytes(mx, st);
+  const int end = act + r * packed_block_bytes(mx, st, has_zp != 0);
   *stage_bytes = (end + 1023) & ~1023;
 }
 
@@ -265,6 +266,21 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    const uint64_t dims[3], const uint64_t strides_bytes[2],
+                    const uint32_t box[3], CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult res = fn(map, dtype, 3, const_cast<void*>(base), d, st, bx, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return res == CUDA_SUCCESS;
+}
+
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                     uint32_t box_outer, CUtensorMapSwizzle swizzle) {
@@ -285,23 +301,22 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_config* T,
                               bool deterministic, bool grouped, const int32_t* offsets,
                               int64_t rows, const void* a, const float* a_scale, const void* w,
-                              const void* s, const void* z, const void* bias, void* c,
-                              void* workspace, size_t ws_bytes, cudaStream_t stream) {
+                              const void* bias, void* c, void* workspace, size_t ws_bytes,
+                              cudaStream_t stream) {
   if (rows < 0) return fail(QGEMM_ERR_INVALID_ARG, "row count is negative");
   if (rows > (1 << 30)) return fail(QGEMM_ERR_UNSUPPORTED, "row count above 2^30");
   if (rows == 0) return ok();
   if (!device_is_sm103()) return fail(QGEMM_ERR_UNSUPPORTED, "this library runs on sm_103 only");
   const bool has_zp = L->zero_format == QGEMM_Z_UINT4;
-  if (!a || !w || !s || !c || (has_zp && !z) || (L->has_bias && !bias) || (grouped && !offsets))
+  if (!a || !w || !c || (L->has_bias && !bias) || (grouped && !offsets))
     return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (!has_zp && z) return fail(QGEMM_ERR_INVALID_ARG, "zero points given for a format without");
   if (!L->has_bias && bias) return fail(QGEMM_ERR_INVALID_ARG, "bias given with has_bias = 0");
   const bool mx = is_mx(L);
   if (mx && !a_scale)
     return fail(QGEMM_ERR_INVALID_ARG, "the W4A8 path needs the per-row activation scales");
   if (!mx && a_scale) return fail(QGEMM_ERR_INVALID_ARG, "a_scale is only used by the W4A8 path");
-  if (!aligned16(a) || !aligned16(w) || !aligned16(s) || !aligned16(c) || (z && !aligned16(z)) ||
-      (bias && !aligned16(bias)) || !aligned16(workspace))
+  if (!aligned16(a) || !aligned16(w) || !aligned16(c) || (bias && !aligned16(bias)) ||
+      !aligned16(workspace))
     return fail(QGEMM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
   Plan P;
   qgemm_status st = make_plan(L, T, rows, grouped, &P);
@@ -311,24 +326,28 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
                 ws_bytes);
   const bool fp16 = L->act_dtype == QGEMM_FP16;
   CUtensorMap tmap;
-  // activation tiles: 128-byte rows, 128-byte swizzle (64 16-bit or 128 e4m3 values)
-  const bool tmap_ok =
-      mx ? encode_tmap_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, (uint64_t)L->k, (uint64_t)rows,
-                          (uint64_t)L->k, 128, (uint32_t)P.bt, CU_TENSOR_MAP_SWIZZLE_128B)
-         : encode_tmap_2d(&tmap,
-                          fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                          a, (uint64_t)L->k, (uint64_t)rows, (uint64_t)L->k * 2, 64,
-                          (uint32_t)P.bt, CU_TENSOR_MAP_SWIZZLE_128B);
+  // activation boxes [chunk][row][128 bytes]: the K axis split into 128-byte
+  // chunks (64 16-bit or 128 e4m3 values) as the outermost box dimension, so
+  // one box holds a stage's k-tiles in the 128-byte-swizzled operand layout
+  const int r = units_per_stage(P.bt);
+  const uint64_t row_bytes = (uint64_t)L->k * (mx ? 1 : 2);
+  const uint64_t dims[3] = {(uint64_t)(mx ? 128 : 64), (uint64_t)rows, row_bytes / 128};
+  const uint64_t strides[2] = {row_bytes, 128};
+  const uint32_t box[3] = {(uint32_t)(mx ? 128 : 64), (uint32_t)P.bt,
+                           (uint32_t)(mx ? r : 2 * r)};
+  const bool tmap_ok = encode_tmap_3d(
+      &tmap,
+      mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+         : fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+      a, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!tmap_ok)
     return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the activation tensor");
-  size_t wb, sb, zb;
-  qgemm_packed_sizes(L, &wb, &sb, &zb);
+  size_t wb = 0;
+  qgemm_packed_size(L, &wb);
   const int E = L->num_experts;
   W4A16Params p;
   memset(&p, 0, sizeof(p));
   p.w = static_cast<const uint8_t*>(w);
-  p.s = static_cast<const uint16_t*>(s);
-  p.z = static_cast<const uint8_t*>(z);
   p.bias = static_cast<const uint16_t*>(bias);
   p.c = static_cast<uint16_t*>(c);
   p.a_scale = a_scale;
@@ -344,8 +363,9 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.expert_offsets = offsets;
   p.num_experts = E;
   p.w_expert_stride = (long long)(wb / E);
-  p.s_expert_stride = (long long)(sb / E / 2);
-  p.z_expert_stride = (long long)(has_zp ? zb / E : 0);
+  p.block_bytes = packed_block_bytes(mx, P.st, has_zp);
+  p.s_off = P.off_s;
+  p.z_off = P.off_z;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.status = reinterpret_cast<int*>(ws);
   p.counters = reinterpret_cast<int*>(ws + P.ws.counters_off);
@@ -355,8 +375,6 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.stages = P.stages;
   p.stage_bytes = P.stage_bytes;
   p.off_w = P.off_w;
-  p.off_s = P.off_s;
-  p.off_z = P.off_z;
   p.smem_bytes = P.smem;
   p.wait_limit_ns = g_wait_limit_ns;
   cudaError_t e = launch_w4a16(tmap, p, P.bt, mx ? 2 : fp16 ? 1 : 0, grouped, P.grid, stream);
@@ -390,47 +408,44 @@ using namespace qg;
 
 extern "C" {
 
-qgemm_status qgemm_packed_sizes(const qgemm_layer_config* layer, size_t* w_bytes,
-                                size_t* s_bytes, size_t* z_bytes) {
+qgemm_status qgemm_packed_size(const qgemm_layer_config* layer, size_t* bytes) {
   qgemm_status st = check_layer(layer);
   if (st != QGEMM_OK) return st;
-  const size_t E = (size_t)layer->num_experts;
+  if (!bytes) return fail(QGEMM_ERR_INVALID_ARG, "bytes is NULL");
   const size_t tiles = (size_t)(layer->n / kTileN) * (size_t)(layer->k / kTileK);
-  const size_t stv = (size_t)st_of(layer->group_size);
-  if (w_bytes) *w_bytes = E * tiles * kTileBytes;
-  if (s_bytes) *s_bytes = is_mx(layer) ? E * tiles * kTileN * 4 : E * tiles * stv * kTileN * 2;
-  if (z_bytes) *z_bytes = layer->zero_format == QGEMM_Z_UINT4 ? E * tiles * stv * kTileN : 0;
+  *bytes = (size_t)layer->num_experts * tiles *
+           (size_t)packed_block_bytes(is_mx(layer), st_of(layer->group_size),
+                                      layer->zero_format == QGEMM_Z_UINT4);
   return ok();
 }
 
 qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qweight,
-                                const void* scales, const void* qzeros, void* w_out,
-                                void* s_out, void* z_out, void* stream) {
+                                const void* scales, const void* qzeros, void* packed,
+                                void* stream) {
   qgemm_status st = check_layer(layer);
   if (st != QGEMM_OK) return st;
   const bool has_zp = layer->zero_format == QGEMM_Z_UINT4;
-  if (!qweight || !scales || !w_out || !s_out || (has_zp && (!qzeros || !z_out)))
+  if (!qweight || !scales || !packed || (has_zp && !qzeros))
     return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (!has_zp && (qzeros || z_out))
-    return fail(QGEMM_ERR_INVALID_ARG, "zero-point tensors given for a format without");
-  if (!aligned16(w_out) || !aligned16(s_out) || !aligned16(qweight) || (z_out && !aligned16(z_out)))
+  if (!has_zp && qzeros)
+    return fail(QGEMM_ERR_INVALID_ARG, "zero points given for a format without");
+  if (!aligned16(packed) || !aligned16(qweight))
     return fail(QGEMM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  cudaError_t e;
   if (is_mx(layer)) {
     if ((reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
       return fail(QGEMM_ERR_INVALID_ARG, "MXFP4 scales must be 4-byte aligned");
-    cudaError_t e = launch_repack_mxfp4(
-        static_cast<const uint8_t*>(qweight), static_cast<const uint8_t*>(scales),
-        static_cast<uint8_t*>(w_out), static_cast<uint8_t*>(s_out), layer->n, layer->k,
-        layer->num_experts, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "repack launch");
-    return ok();
+    e = launch_repack_mxfp4(static_cast<const uint8_t*>(qweight),
+                            static_cast<const uint8_t*>(scales), static_cast<uint8_t*>(packed),
+                            layer->n, layer->k, layer->num_experts,
+                            static_cast<cudaStream_t>(stream));
+  } else {
+    e = launch_repack_w4(static_cast<const int32_t*>(qweight),
+                         static_cast<const uint16_t*>(scales), static_cast<const int32_t*>(qzeros),
+                         static_cast<uint8_t*>(packed), layer->n, layer->k, layer->group_size,
+                         layer->weight_format == QGEMM_W_INT4_SYM ? 1 : 0, layer->num_experts,
+                         static_cast<cudaStream_t>(stream));
   }
-  cudaError_t e = launch_repack_w4(
-      static_cast<const int32_t*>(qweight), static_cast<const uint16_t*>(scales),
-      static_cast<const int32_t*>(qzeros), static_cast<uint8_t*>(w_out),
-      static_cast<uint16_t*>(s_out), static_cast<uint8_t*>(z_out), layer->n, layer->k,
-      layer->group_size, layer->weight_format == QGEMM_W_INT4_SYM ? 1 : 0, layer->num_experts,
-      static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "repack launch");
   return ok();
 }
@@ -461,15 +476,14 @@ qgemm_status qgemm_workspace_init(void* workspace, size_t bytes, void* stream) {
 
 qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_config* compute,
                        const qgemm_tuning_config* tuning, int64_t m, const void* a,
-                       const float* a_scale, const void* w, const void* s, const void* z,
-                       const void* bias, void* c, void* workspace, size_t workspace_bytes,
-                       void* stream) {
+                       const float* a_scale, const void* packed, const void* bias, void* c,
+                       void* workspace, size_t workspace_bytes, void* stream) {
   qgemm_status st = check_layer(layer);
   if (st != QGEMM_OK) return st;
   st = check_compute(compute, layer, false);
   if (st != QGEMM_OK) return st;
-  return run_w4a16(layer, tuning, compute->deterministic != 0, false, nullptr, m, a, a_scale, w,
-                   s, z, bias, c, workspace,
+  return run_w4a16(layer, tuning, compute->deterministic != 0, false, nullptr, m, a, a_scale,
+                   packed, bias, c, workspace,
                    workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
@@ -477,14 +491,14 @@ qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
                                const qgemm_compute_config* compute,
                                const qgemm_tuning_config* tuning, const int32_t* expert_offsets,
                                int64_t total_rows, const void* a, const float* a_scale,
-                               const void* w, const void* s, const void* z, const void* bias,
-                               void* c, void* workspace, size_t workspace_bytes, void* stream) {
+                               const void* packed, const void* bias, void* c, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   qgemm_status st = check_layer(layer);
   if (st != QGEMM_OK) return st;
   st = check_compute(compute, layer, true);
   if (st != QGEMM_OK) return st;
   return run_w4a16(layer, tuning, compute->deterministic != 0, true, expert_offsets,
-                   total_rows, a, a_scale, w, s, z, bias, c,
+                   total_rows, a, a_scale, packed, bias, c,
                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
@@ -548,25 +562,20 @@ qgemm_status qgemm_moe_combine(const void* y2, const int32_t* inv_perm,
   return ok();
 }
 
-qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* w, const void* s,
-                                 const void* z, void* out_kn, void* stream) {
+qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* packed,
+                                 void* out_kn, void* stream) {
   qgemm_status st = check_layer(layer);
   if (st != QGEMM_OK) return st;
-  const bool has_zp = layer->zero_format == QGEMM_Z_UINT4;
-  if (!w || !s || !out_kn || (has_zp && !z))
-    return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (is_mx(layer)) {
-    cudaError_t e = launch_debug_mx_codes(static_cast<const uint8_t*>(w),
-                                          static_cast<uint8_t*>(out_kn), layer->n, layer->k,
-                                          static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
-    return ok();
-  }
-  cudaError_t e = launch_debug_dequant(
-      static_cast<const uint8_t*>(w), static_cast<const uint16_t*>(s),
-      static_cast<const uint8_t*>(z), static_cast<uint16_t*>(out_kn), layer->n, layer->k,
-      layer->group_size, has_zp ? 1 : 0, layer->act_dtype == QGEMM_FP16,
-      static_cast<cudaStream_t>(stream));
+  if (!packed || !out_kn) return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
+  cudaError_t e;
+  if (is_mx(layer))
+    e = launch_debug_mx_codes(static_cast<const uint8_t*>(packed), static_cast<uint8_t*>(out_kn),
+                              layer->n, layer->k, static_cast<cudaStream_t>(stream));
+  else
+    e = launch_debug_dequant(static_cast<const uint8_t*>(packed), static_cast<uint16_t*>(out_kn),
+                             layer->n, layer->k, layer->group_size,
+                             layer->zero_format == QGEMM_Z_UINT4 ? 1 : 0,
+                             layer->act_dtype == QGEMM_FP16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
   return ok();
 }

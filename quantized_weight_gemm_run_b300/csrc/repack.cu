@@ -1,21 +1,26 @@
-// Weight preprocessing: standard format -> the GEMM kernel's tiled layout.
+// Weight preprocessing: standard format -> the GEMM kernel's packed layout.
 //
 // The Humming preprocessing step checks parameters, pads dimensions and
 // repacks tensors for the target kernel (kinachrichten.com, "Wie die
 // Architektur funktioniert"); repacking rearranges without changing what the
 // stored values mean (retrivium.ai, "vLLM Humming: why shared quantization
 // still needs specialized kernels", section "Representation answers a
-// different question").  Target layout (per expert; KT = K/128 k-tiles):
+// different question").  Target layout (per expert; KT = K/128 k-tiles): one
+// packed block per (n-tile, k-tile), n-tile major, so that the blocks of one
+// n-tile's consecutive k-tiles are contiguous and a pipeline stage is filled
+// by a single bulk copy.  A block is
 //
-//   weights  8192-byte block per (n-tile, k-tile), n-tile major.  Block =
-//            512 16-byte vectors, vector (qd*4 + j)*32 + t = row 32qd + t of
-//            the tile, k = 32j .. 32j+31; word w of the vector holds 8 k, the
-//            nibble at position p holding k-offset {0,2,4,6,1,3,5,7}[p], so a
-//            single 0x000F000F mask extracts two consecutive k.  INT4 codes
-//            are stored offset binary (q + 8).
-//   scales   128 * ST 16-bit words per block (ST = max(1, 128/g)): word
-//            sg*128 + r is the scale of row r for the sg-th group of the tile.
-//   zeros    128 * ST bytes per block, same order, zero point 0..15.
+//   codes    8192 bytes: 512 16-byte vectors, vector (qd*4 + j)*32 + t = row
+//            32qd + t of the tile, k = 32j .. 32j+31.  INT4/UINT4: word w of
+//            the vector holds 8 k, the nibble at position p holding k-offset
+//            {0,2,4,6,1,3,5,7}[p], so a single 0x000F000F mask extracts two
+//            consecutive k; INT4 codes are stored offset binary (q + 8).
+//            MXFP4: the 16 bytes of the row's 32 codes in standard order.
+//   scales   INT4/UINT4: 128 * ST 16-bit words (ST = max(1, 128/g)), word
+//            sg*128 + r the scale of row r for the sg-th group of the tile.
+//            MXFP4: 128 32-bit words, byte j of word r the e8m0 exponent of
+//            row r for k = 32j .. 32j+31 of the tile.
+//   zeros    UINT4 only: 128 * ST bytes, same order, zero point 0..15.
 //
 // Every thread writes one output vector / element; reads of the standard
 // tensors are coalesced along N.
@@ -24,8 +29,9 @@
 
 namespace qg {
 
-__global__ void repack_weights_kernel(const int32_t* __restrict__ qweight, uint4* __restrict__ out,
-                                      int n, int k, int signed_q, long long total) {
+__global__ void repack_weights_kernel(const int32_t* __restrict__ qweight, uint8_t* __restrict__ out,
+                                      int n, int k, int signed_q, int block_bytes,
+                                      long long total) {
   const long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (vec >= total) return;
   const int KT = k / kTileK, NT = n / kTileN;
@@ -56,13 +62,13 @@ __global__ void repack_weights_kernel(const int32_t* __restrict__ qweight, uint4
     if (signed_q) r ^= 0x88888888u;   // two's complement nibble -> q + 8
     o[w] = r;
   }
-  out[vec] = make_uint4(o[0], o[1], o[2], o[3]);
+  const long long gblk = ex * ((long long)NT * KT) + blk;
+  *reinterpret_cast<uint4*>(out + gblk * block_bytes + v * 16) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __global__ void repack_scales_kernel(const uint16_t* __restrict__ scales,
-                                     const int32_t* __restrict__ qzeros, uint16_t* __restrict__ s_out,
-                                     uint8_t* __restrict__ z_out, int n, int k, int group,
-                                     long long total) {
+                                     const int32_t* __restrict__ qzeros, uint8_t* __restrict__ out,
+                                     int n, int k, int group, int block_bytes, long long total) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= total) return;
   const int KT = k / kTileK, NT = n / kTileN;
@@ -79,40 +85,41 @@ __global__ void repack_scales_kernel(const uint16_t* __restrict__ scales,
   const int grp = kk / group;
   const int col = nt * kTileN + r;
   const long long groups = k / group;
-  s_out[idx] = scales[ex * groups * n + (long long)grp * n + col];
-  if (z_out) {
+  uint8_t* bp = out + (ex * ((long long)NT * KT) + blk) * block_bytes;
+  reinterpret_cast<uint16_t*>(bp + kTileBytes)[sg * kTileN + r] =
+      scales[ex * groups * n + (long long)grp * n + col];
+  if (qzeros) {
     const uint32_t word = (uint32_t)qzeros[ex * groups * (n / 8) + (long long)grp * (n / 8) + col / 8];
-    z_out[idx] = (uint8_t)((word >> (4 * (col % 8))) & 0xFu);
+    bp[kTileBytes + packed_scale_bytes(false, st) + sg * kTileN + r] =
+        (uint8_t)((word >> (4 * (col % 8))) & 0xFu);
   }
 }
 
 cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
-                             const int32_t* qzeros, uint8_t* w_out, uint16_t* s_out,
-                             uint8_t* z_out, int64_t n, int64_t k, int group, int signed_q,
-                             int experts, cudaStream_t stream) {
+                             const int32_t* qzeros, uint8_t* packed, int64_t n, int64_t k,
+                             int group, int signed_q, int experts, cudaStream_t stream) {
   const int threads = 256;
+  const int st = group < kTileK ? kTileK / group : 1;
+  const int block_bytes = packed_block_bytes(false, st, qzeros != nullptr);
   const long long vecs = (long long)experts * (n / kTileN) * (k / kTileK) * 512;
   repack_weights_kernel<<<(unsigned)((vecs + threads - 1) / threads), threads, 0, stream>>>(
-      qweight, reinterpret_cast<uint4*>(w_out), (int)n, (int)k, signed_q, vecs);
+      qweight, packed, (int)n, (int)k, signed_q, block_bytes, vecs);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const int st = group < kTileK ? kTileK / group : 1;
   const long long elems = (long long)experts * (n / kTileN) * (k / kTileK) * st * kTileN;
   repack_scales_kernel<<<(unsigned)((elems + threads - 1) / threads), threads, 0, stream>>>(
-      scales, qzeros, s_out, z_out, (int)n, (int)k, group, elems);
+      scales, qzeros, packed, (int)n, (int)k, group, block_bytes, elems);
   return cudaGetLastError();
 }
 
 // MXFP4: standard codes [N, K/2] (k = 2j low nibble, 2j+1 high nibble) and
-// e8m0 scales [N, K/32] -> per (n-tile, k-tile) an 8192-byte block of 512
-// 16-byte vectors, vector (qd*4 + j)*32 + t = row 32qd + t, k = 32j .. 32j+31
-// with the nibbles left in their standard order (the kernel's table lookup
-// wants consecutive k in consecutive nibbles), and a 512-byte scale block of
-// one 32-bit word per row whose byte j is the scale of the row's j-th 32-k block.
+// e8m0 scales [N, K/32] -> packed blocks (layout above); the nibbles stay in
+// their standard order because the kernel's table lookup wants consecutive k
+// in consecutive nibbles.
 __global__ void repack_mxfp4_kernel(const uint8_t* __restrict__ codes,
-                                    const uint8_t* __restrict__ scales, uint4* __restrict__ w_out,
-                                    uint32_t* __restrict__ s_out, int n, int k, long long vecs,
-                                    long long words) {
+                                    const uint8_t* __restrict__ scales, uint8_t* __restrict__ out,
+                                    int n, int k, long long vecs, long long words) {
+  constexpr int kBlock = packed_block_bytes(true, 1, false);
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int KT = k / kTileK, NT = n / kTileN;
   if (idx < vecs) {
@@ -125,7 +132,8 @@ __global__ void repack_mxfp4_kernel(const uint8_t* __restrict__ codes,
     const int t = v & 31, j = (v >> 5) & 3, qd = v >> 7;
     const long long row = (long long)nt * kTileN + qd * 32 + t;
     const uint8_t* src = codes + (ex * n + row) * (k / 2) + (kt * kTileK + j * 32) / 2;
-    w_out[idx] = *reinterpret_cast<const uint4*>(src);
+    *reinterpret_cast<uint4*>(out + (ex * ((long long)NT * KT) + blk) * kBlock + v * 16) =
+        *reinterpret_cast<const uint4*>(src);
   }
   if (idx < words) {
     const long long per_expert = (long long)NT * KT * kTileN;
@@ -135,20 +143,19 @@ __global__ void repack_mxfp4_kernel(const uint8_t* __restrict__ codes,
     const long long blk = rem / kTileN;
     const int nt = (int)(blk / KT), kt = (int)(blk % KT);
     const long long row = (long long)nt * kTileN + r;
-    s_out[idx] = *reinterpret_cast<const uint32_t*>(scales + (ex * n + row) * (k / 32) + kt * 4);
+    reinterpret_cast<uint32_t*>(out + (ex * ((long long)NT * KT) + blk) * kBlock + kTileBytes)[r] =
+        *reinterpret_cast<const uint32_t*>(scales + (ex * n + row) * (k / 32) + kt * 4);
   }
 }
 
-cudaError_t launch_repack_mxfp4(const uint8_t* codes, const uint8_t* scales, uint8_t* w_out,
-                                uint8_t* s_out, int64_t n, int64_t k, int experts,
-                                cudaStream_t stream) {
+cudaError_t launch_repack_mxfp4(const uint8_t* codes, const uint8_t* scales, uint8_t* packed,
+                                int64_t n, int64_t k, int experts, cudaStream_t stream) {
   const long long tiles = (long long)experts * (n / kTileN) * (k / kTileK);
   const long long vecs = tiles * 512, words = tiles * kTileN;
   const long long total = vecs > words ? vecs : words;
   const int threads = 256;
   repack_mxfp4_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, stream>>>(
-      codes, scales, reinterpret_cast<uint4*>(w_out), reinterpret_cast<uint32_t*>(s_out), (int)n,
-      (int)k, vecs, words);
+      codes, scales, packed, (int)n, (int)k, vecs, words);
   return cudaGetLastError();
 }
 

@@ -234,15 +234,23 @@ __device__ __forceinline__ float from_out(uint16_t b) {
 
 // FMT: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 weights, e4m3
 // activations with per-row fp32 scales, block-scaled MMA, bf16 output).
+//
+// A pipeline stage holds up to R = units_per_stage(BT) consecutive k-tiles
+// ("units") of one output tile, so that each stage is filled by few, large
+// copies: one bulk copy of R weight blocks, one of their scales (and zero
+// points), and one three-dimensional TMA box holding the R activation tiles.
 template <int BT, int FMT, bool GROUPED>
 __global__ void __launch_bounds__(kNumThreads, 1)
     w4a16_kernel(const __grid_constant__ CUtensorMap tmap_a, const W4A16Params p) {
   constexpr bool FP16 = FMT == 1;
   constexpr bool MX = FMT == 2;
+  constexpr int R = units_per_stage(BT);
   // tensor-memory columns: dequantized weight slots, then (MX) the A and B
   // scale factors, accumulators from column 256
   constexpr int kSlotCols = MX ? 32 : kASlotCols;
   constexpr uint32_t kSfaCol = 128, kSfbCol = 160, kAccCol = 256;
+  constexpr uint32_t kActUnit = BT * kTileK * (MX ? 1 : 2);   // bytes of one unit's activations
+
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -290,50 +298,45 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   };
 
   uint64_t pol_stream = 0, pol_keep = 0;   // L2 policies (set by thread 0)
-  const uint32_t act_bytes = BT * kTileK * (MX ? 1 : 2);
-  const uint32_t w_bytes = kTileBytes;
-  const uint32_t s_bytes = MX ? kTileN * 4 : p.st * kTileN * 2;
-  const uint32_t z_bytes = p.has_zp ? p.st * kTileN : 0;
-  auto scale_src = [&](int e, long long blk) {
-    return reinterpret_cast<const uint8_t*>(p.s) + e * p.s_expert_stride * 2 + blk * s_bytes;
-  };
-  auto load_act = [&](uint8_t* sp, uint64_t* bar, int kt, int row0) {
-    if constexpr (MX) {
-      tma_load_2d_hint(sp, &tmap_a, bar, kt * kTileK, row0, pol_keep);
-    } else {
-      tma_load_2d_hint(sp, &tmap_a, bar, kt * kTileK, row0, pol_keep);
-      tma_load_2d_hint(sp + BT * 128, &tmap_a, bar, kt * kTileK + 64, row0, pol_keep);
-    }
-  };
+  const uint32_t blk_bytes = p.block_bytes;   // packed block: codes, scales, zero points
 
-  // ---- producer state (thread 0): one (tile, k-tile) unit per pipeline stage
+  // ---- producer state (thread 0): one stage = up to R units of one work item
   Schedule psched;
   WorkItem pwi{0, 0, 0};
-  int pkt = 0;
+  int pkt = 0, pr = 0;             // first k-tile and unit count of the current stage
   bool phave = false;
   int pstage = 0;
   uint32_t pphase = 0;
-  long long issued = 0;
-  auto pnext = [&]() -> bool {   // advance to the next unit; false when none is left
-    if (phave && ++pkt < pwi.k1) return true;
-    if (!psched.next(pwi)) return false;
-    phave = true;
-    pkt = pwi.k0;
+  long long issued = 0;            // stages issued
+  auto pnext = [&]() -> bool {     // advance to the next stage; false when none is left
+    if (phave && pkt + pr < pwi.k1) {
+      pkt += pr;
+    } else {
+      if (!psched.next(pwi)) return false;
+      phave = true;
+      pkt = pwi.k0;
+    }
+    pr = min(R, pwi.k1 - pkt);
     return true;
   };
-  auto issue = [&]() {
+  // weights, scales and zero points of the current stage: read-only layer
+  // data, so they may be requested before the previous grid has finished
+  auto issue_weights = [&]() {
     const TileCoord<BT> tc = coords(pwi.tile);
     uint8_t* sp = stage_base + pstage * p.stage_bytes;
     const long long blk = (long long)tc.nt * p.kt + pkt;
-    mbar_arrive_expect_tx(&full[pstage], act_bytes + w_bytes + s_bytes + z_bytes);
-    // weights first: they do not depend on the activations' producer
-    bulk_load(sp + p.off_w, p.w + tc.e * p.w_expert_stride + blk * kTileBytes, w_bytes,
+    // the pr packed blocks of one n-tile's consecutive k-tiles are contiguous
+    mbar_arrive_expect_tx(&full[pstage], R * kActUnit + pr * blk_bytes);
+    bulk_load(sp + p.off_w, p.w + tc.e * p.w_expert_stride + blk * blk_bytes, pr * blk_bytes,
               &full[pstage], pol_stream);
-    bulk_load(sp + p.off_s, scale_src(tc.e, blk), s_bytes, &full[pstage], pol_stream);
-    if (p.has_zp)
-      bulk_load(sp + p.off_z, p.z + tc.e * p.z_expert_stride + blk * p.st * kTileN, z_bytes,
-                &full[pstage], pol_stream);
-    load_act(sp, &full[pstage], pkt, tc.row0);
+  };
+  // the R activation tiles of a stage in one box: [chunk][BT rows][128 bytes]
+  auto issue_act = [&](int stage, int tile, int kt) {
+    const TileCoord<BT> tc = coords(tile);
+    tma_load_3d_hint(stage_base + stage * p.stage_bytes, &tmap_a, &full[stage], 0, tc.row0,
+                     kt * (MX ? 1 : 2), pol_keep);
+  };
+  auto advance_pstage = [&]() {
     ++issued;
     if (++pstage == S) {
       pstage = 0;
@@ -424,50 +427,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // ------------------------------------------------ producer
     if (lane == 0) {
       psched.init(T, p.kt, gridDim.x, blockIdx.x);
-      // The packed weights are read-only layer data: the first S stages of
-      // them are requested before waiting for the previous grid on the stream
-      // (which may still be writing this GEMM's activations or workspace);
-      // the activation tiles of those stages follow the wait.
+      // the first S stages' weights go out before waiting for the previous
+      // grid on the stream (which may still write this GEMM's activations or
+      // workspace); their activation boxes follow the wait
       int pre = 0;
-      WorkItem pre_wi[16];
-      int pre_kt[16];
+      int pre_tile[16], pre_kt[16];
       while (pre < S && pnext()) {
-        const TileCoord<BT> tc = coords(pwi.tile);
-        uint8_t* sp = stage_base + pstage * p.stage_bytes;
-        const long long blk = (long long)tc.nt * p.kt + pkt;
-        mbar_arrive_expect_tx(&full[pstage], act_bytes + w_bytes + s_bytes + z_bytes);
-        bulk_load(sp + p.off_w, p.w + tc.e * p.w_expert_stride + blk * kTileBytes, w_bytes,
-                  &full[pstage], pol_stream);
-        bulk_load(sp + p.off_s, scale_src(tc.e, blk), s_bytes, &full[pstage], pol_stream);
-        if (p.has_zp)
-          bulk_load(sp + p.off_z, p.z + tc.e * p.z_expert_stride + blk * p.st * kTileN,
-                    z_bytes, &full[pstage], pol_stream);
-        pre_wi[pre] = pwi;
+        issue_weights();
+        pre_tile[pre] = pwi.tile;
         pre_kt[pre] = pkt;
         ++pre;
-        ++issued;
-        if (++pstage == S) {
-          pstage = 0;
-          pphase ^= 1;
-        }
+        advance_pstage();
       }
       grid_dependency_wait();
-      for (int i = 0; i < pre; ++i) {   // stages 0 .. pre-1 of the first ring pass
-        const TileCoord<BT> tc = coords(pre_wi[i].tile);
-        uint8_t* sp = stage_base + i * p.stage_bytes;
-        load_act(sp, &full[i], pre_kt[i], tc.row0);
-      }
+      for (int i = 0; i < pre; ++i) issue_act(i, pre_tile[i], pre_kt[i]);
       while (pnext()) {
         if (!mbar_wait(&empty[pstage], pphase ^ 1, abort_flag, p.status, lim, kStatusTimeout))
           break;
-        issue();
+        issue_weights();
+        issue_act(pstage, pwi.tile, pkt);
+        advance_pstage();
       }
       // drain: never leave a copy in flight into shared memory we are leaving
-      for (int s = 0; s < S && s < issued; ++s) {
-        long long last = s + ((issued - 1 - s) / S) * S;
+      for (int st = 0; st < S && st < issued; ++st) {
+        long long last = st + ((issued - 1 - st) / S) * S;
         uint32_t par = (uint32_t)((last / S) & 1);
         volatile int no_abort = 0;
-        mbar_wait(&full[s], par, &no_abort, nullptr, 100000000ull, 0);
+        mbar_wait(&full[st], par, &no_abort, nullptr, 100000000ull, 0);
       }
     }
   } else if (warp == 1) {
@@ -486,40 +472,49 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + kAccCol + acc * BT;
-        for (int kt = wi.k0; kt < wi.k1; ++kt) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim, kStatusTimeout) ||
-              !mbar_wait(&a_full[slot], aphase, abort_flag, p.status, lim, kStatusTimeout)) {
+        for (int kt0 = wi.k0; ok && kt0 < wi.k1; kt0 += R) {
+          const int r = min(R, wi.k1 - kt0);
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim, kStatusTimeout)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t b0 = smem_u32(stage_base + stage * p.stage_bytes);
-          if constexpr (MX) {
-            // four K=32 steps over one 128-byte activation row; the scale
-            // factor id selects the step's byte of the scale columns
+          const uint32_t sbase = smem_u32(stage_base + stage * p.stage_bytes);
+          for (int i = 0; i < r; ++i) {
+            if (!mbar_wait(&a_full[slot], aphase, abort_flag, p.status, lim, kStatusTimeout)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t b0 = sbase + i * kActUnit;
+            const bool first = (kt0 + i == wi.k0);
+            if constexpr (MX) {
+              // four K=32 steps over one 128-byte activation row; the scale
+              // factor id selects the step's byte of the scale columns
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_ts_mxf8f6f4(d_tmem, tmem_base + slot * kSlotCols + ks * 8,
-                              smem_desc_sw128(b0 + ks * 32), idesc_with_sf_ids(idesc, ks, ks),
-                              tmem_base + kSfaCol + slot * 4, tmem_base + kSfbCol,
-                              (kt > wi.k0 || ks > 0) ? 1u : 0u);
-          } else {
+              for (int ks = 0; ks < 4; ++ks)
+                mma_ts_mxf8f6f4(d_tmem, tmem_base + slot * kSlotCols + ks * 8,
+                                smem_desc_sw128(b0 + ks * 32), idesc_with_sf_ids(idesc, ks, ks),
+                                tmem_base + kSfaCol + slot * 4, tmem_base + kSfbCol,
+                                (!first || ks > 0) ? 1u : 0u);
+            } else {
 #pragma unroll
-            for (int ks = 0; ks < kTileK / 16; ++ks) {
-              const uint32_t boff = (ks >> 2) * (BT * 128) + (ks & 3) * 32;
-              mma_ts_f16(d_tmem, tmem_base + slot * kSlotCols + ks * 8,
-                         smem_desc_sw128(b0 + boff), idesc, (kt > wi.k0 || ks > 0) ? 1u : 0u);
+              for (int ks = 0; ks < kTileK / 16; ++ks) {
+                const uint32_t boff = (ks >> 2) * (BT * 128) + (ks & 3) * 32;
+                mma_ts_f16(d_tmem, tmem_base + slot * kSlotCols + ks * 8,
+                           smem_desc_sw128(b0 + boff), idesc, (!first || ks > 0) ? 1u : 0u);
+              }
+            }
+            mma_commit(&a_empty[slot]);
+            if (++slot == kASlots) {
+              slot = 0;
+              aphase ^= 1;
             }
           }
+          if (!ok) break;
           mma_commit(&empty[stage]);
-          mma_commit(&a_empty[slot]);
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
-          }
-          if (++slot == kASlots) {
-            slot = 0;
-            aphase ^= 1;
           }
         }
         if (!ok) break;
@@ -536,8 +531,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------ dequant
-    // Two warps per TMEM lane quadrant; warp group h takes every other k-tile
-    // unit (h = unit index & 1) and dequantizes all 128 k of its 32 rows.
+    // Two warps per TMEM lane quadrant; warp group h takes every other unit
+    // (h = unit index & 1) and dequantizes all 128 k of its 32 rows.
     const int q = warp & 3;             // TMEM lane quadrant
     const int h = (warp - 4) >> 2;      // which units: even (0) or odd (1)
     const int row = q * 32 + lane;      // output feature within the tile
@@ -549,70 +544,71 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     WorkItem wi;
     bool ok = true;
     while (ok && sched.next(wi)) {
-      for (int kt = wi.k0; kt < wi.k1; ++kt, ++unit) {
-        if ((unit & 1) == h) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim, kStatusTimeout) ||
-              !mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
-                         kStatusTimeout)) {
-            ok = false;
-            break;
-          }
-          const uint8_t* sp = stage_base + stage * p.stage_bytes;
-          const uint4* wv = reinterpret_cast<const uint4*>(sp + p.off_w);
-          if constexpr (MX) {
-            // 128 e2m1 codes of this row -> 128 e4m3 bytes (32 columns), and
-            // its four e8m0 block scales -> the slot's four scale columns
-            uint4 v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = wv[(q * 4 + j) * 32 + lane];
-            const uint32_t sf = reinterpret_cast<const uint32_t*>(sp + p.off_s)[row];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t o8[8];
-              dequant_vec_mx(v[j], o8);
-              tmem_st8(tmem_base + lane_addr + slot * kSlotCols + j * 8, o8);
+      for (int kt0 = wi.k0; ok && kt0 < wi.k1; kt0 += R) {
+        const int r = min(R, wi.k1 - kt0);
+        const uint8_t* sp = stage_base + stage * p.stage_bytes;
+        for (int i = 0; i < r; ++i, ++unit) {
+          if ((unit & 1) == h) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim, kStatusTimeout) ||
+                !mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
+                           kStatusTimeout)) {
+              ok = false;
+              break;
             }
-            const uint32_t sf4[4] = {sf, sf, sf, sf};
-            tmem_st4(tmem_base + lane_addr + kSfaCol + slot * 4, sf4);
+            const uint8_t* bp = sp + p.off_w + i * blk_bytes;   // this unit's packed block
+            const uint4* wv = reinterpret_cast<const uint4*>(bp);
+            if constexpr (MX) {
+              // 128 e2m1 codes of this row -> 128 e4m3 bytes (32 columns), and
+              // its four e8m0 block scales -> the slot's four scale columns
+              uint4 v[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) v[j] = wv[(q * 4 + j) * 32 + lane];
+              const uint32_t sf =
+                  reinterpret_cast<const uint32_t*>(bp + p.s_off)[row];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t o8[8];
+                dequant_vec_mx(v[j], o8);
+                tmem_st8(tmem_base + lane_addr + slot * kSlotCols + j * 8, o8);
+              }
+              const uint32_t sf4[4] = {sf, sf, sf, sf};
+              tmem_st4(tmem_base + lane_addr + kSfaCol + slot * 4, sf4);
+            } else {
+              const uint16_t* sv = reinterpret_cast<const uint16_t*>(bp + p.s_off);
+              const uint8_t* zv = bp + p.z_off;
+              // every shared-memory read of the unit first, then the arithmetic
+              uint4 v[4];
+              uint32_t scale2[4], zero2[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) v[j] = wv[(q * 4 + j) * 32 + lane];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int sg = j >> p.sg_shift;
+                scale2[j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
+                const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
+                zero2[j] = (magic16 + zq) * 0x00010001u;
+              }
+              const uint32_t tbase = tmem_base + lane_addr + slot * kSlotCols;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t out[16];
+                dequant_vec<FP16>(v[j], zero2[j], scale2[j], out);
+                tmem_st16(tbase + j * 16, out);
+              }
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[slot]);
-          } else {
-          const uint16_t* sv = reinterpret_cast<const uint16_t*>(sp + p.off_s);
-          const uint8_t* zv = sp + p.off_z;
-          // every shared-memory read of the unit first, then the arithmetic
-          uint4 v[4];
-          uint32_t scale2[4], zero2[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = wv[(q * 4 + j) * 32 + lane];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int sg = j >> p.sg_shift;
-            scale2[j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
-            const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
-            zero2[j] = (magic16 + zq) * 0x00010001u;
           }
-          const uint32_t tbase = tmem_base + lane_addr + slot * kSlotCols;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t out[16];
-            dequant_vec<FP16>(v[j], zero2[j], scale2[j], out);
-            tmem_st16(tbase + j * 16, out);
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[slot]);
+          if (++slot == kASlots) {
+            slot = 0;
+            aphase ^= 1;
           }
         }
         if (++stage == S) {
           stage = 0;
           phase ^= 1;
-        }
-        if (++slot == kASlots) {
-          slot = 0;
-          aphase ^= 1;
         }
       }
     }
@@ -698,11 +694,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         accphase ^= 1;
       }
       if (!whole) {
-        // Fixed-order split-K reduction, per 32-column quadrant: the warp of
-        // the last CTA to arrive for this quadrant of the tile sums every
-        // contributor's partial in CTA order (independent of arrival order).
-        // The warp's partial stores are ordered before lane 0's release add;
-        // the acquiring add of the last arrival orders the reads after it.
+        // Split-K fixup, per 32-column quadrant, by the warp of the last CTA
+        // to arrive for this quadrant of the tile.  The warp's partial stores
+        // (or reductions) are ordered before lane 0's release add; the
+        // acquiring add of the last arrival orders the reads after it.
         const long long c_first = sched.cta_of_unit(u_start);
         const long long c_last = sched.cta_of_unit(u_start + p.kt - 1);
         const int contributors = (int)(c_last - c_first + 1);
@@ -744,8 +739,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             z4[m0 / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (lane == 0) *counter = 0;   // ready for the next launch
         } else if (old == contributors - 1) {
-          // 8 rows per pass; up to 4 contributors' partials are loaded before
-          // any is added, then summed in CTA order (fixed rounding order)
+          // fixed-order mode, 8 rows per pass; up to 4 contributors' partials
+          // are loaded before any is added, then summed in CTA order
           for (int m0 = 0; m0 < tc.rows; m0 += 8) {
             float4 acc4[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
             for (long long cc0 = c_first; cc0 <= c_last; cc0 += 4) {
@@ -850,8 +845,8 @@ cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const W4A16Params& p, int bl
 
 // out[k, n] = the value the GEMM kernel feeds the tensor core for W^[k, n].
 template <bool FP16>
-__global__ void debug_dequant_kernel(const uint8_t* w, const uint16_t* s, const uint8_t* z,
-                                     uint16_t* out, int n, int k, int group, int has_zp) {
+__global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n, int k,
+                                     int group, int has_zp) {
   const int KT = k / kTileK;
   const long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // one 16-byte vector
   const long long total = (long long)(n / kTileN) * KT * 512;
@@ -863,9 +858,11 @@ __global__ void debug_dequant_kernel(const uint8_t* w, const uint16_t* s, const 
   const int row = q * 32 + t;
   const int st = group < kTileK ? kTileK / group : 1;
   const int sg = group < kTileK ? (32 * j) / group : 0;
-  const uint4 wv = reinterpret_cast<const uint4*>(w)[vec];
-  const uint32_t sbits = s[(blk * st + sg) * kTileN + row];
-  const uint32_t zq = has_zp ? (uint32_t)z[(blk * st + sg) * kTileN + row] : 8u;
+  const uint8_t* bp = packed + blk * packed_block_bytes(false, st, has_zp != 0);
+  const uint4 wv = reinterpret_cast<const uint4*>(bp)[v];
+  const uint32_t sbits = reinterpret_cast<const uint16_t*>(bp + kTileBytes)[sg * kTileN + row];
+  const uint32_t zq =
+      has_zp ? (uint32_t)(bp + kTileBytes + packed_scale_bytes(false, st))[sg * kTileN + row] : 8u;
   constexpr uint32_t magic16 = FP16 ? 0x6400u : 0x4300u;
   uint32_t o[16];
   dequant_vec<FP16>(wv, (magic16 + zq) * 0x00010001u, sbits * 0x00010001u, o);
@@ -878,17 +875,16 @@ __global__ void debug_dequant_kernel(const uint8_t* w, const uint16_t* s, const 
   }
 }
 
-cudaError_t launch_debug_dequant(const uint8_t* w, const uint16_t* s, const uint8_t* z,
-                                 uint16_t* out, int64_t n, int64_t k, int group, int has_zp,
-                                 bool fp16, cudaStream_t stream) {
+cudaError_t launch_debug_dequant(const uint8_t* packed, uint16_t* out, int64_t n, int64_t k,
+                                 int group, int has_zp, bool fp16, cudaStream_t stream) {
   const long long total = (n / kTileN) * (k / kTileK) * 512;
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   if (fp16)
-    debug_dequant_kernel<true><<<blocks, threads, 0, stream>>>(w, s, z, out, (int)n, (int)k,
+    debug_dequant_kernel<true><<<blocks, threads, 0, stream>>>(packed, out, (int)n, (int)k,
                                                                 group, has_zp);
   else
-    debug_dequant_kernel<false><<<blocks, threads, 0, stream>>>(w, s, z, out, (int)n, (int)k,
+    debug_dequant_kernel<false><<<blocks, threads, 0, stream>>>(packed, out, (int)n, (int)k,
                                                                  group, has_zp);
   return cudaGetLastError();
 }
@@ -905,7 +901,8 @@ __global__ void debug_mx_codes_kernel(const uint8_t* w, uint8_t* out, int n, int
   const int nt = (int)(blk / KT), kt = (int)(blk % KT);
   const int t = v & 31, j = (v >> 5) & 3, q = v >> 7;
   uint32_t o[8];
-  dequant_vec_mx(reinterpret_cast<const uint4*>(w)[vec], o);
+  dequant_vec_mx(reinterpret_cast<const uint4*>(w + blk * packed_block_bytes(true, 1, false))[v],
+                 o);
   const int nn = nt * kTileN + q * 32 + t;
 #pragma unroll
   for (int c = 0; c < 32; ++c) {

@@ -73,18 +73,18 @@ _C = ctypes.POINTER(qgemm_compute_config)
 _T = ctypes.POINTER(qgemm_tuning_config)
 
 _SIGS = {
-    "qgemm_packed_sizes": [_L, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)],
-    "qgemm_pack_weights": [_L, _P, _P, _P, _P, _P, _P, _P],
+    "qgemm_packed_size": [_L, ctypes.POINTER(_SZ)],
+    "qgemm_pack_weights": [_L, _P, _P, _P, _P, _P],
     "qgemm_workspace_size": [_L, _C, _T, _I64, ctypes.POINTER(_SZ)],
     "qgemm_workspace_init": [_P, _SZ, _P],
-    "qgemm_run": [_L, _C, _T, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
-    "qgemm_run_noalloc": [_L, _C, _T, _I64, _P, _P, _P, _P, _P, _P, _P, _P],
-    "qgemm_grouped_run": [_L, _C, _T, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
+    "qgemm_run": [_L, _C, _T, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
+    "qgemm_run_noalloc": [_L, _C, _T, _I64, _P, _P, _P, _P, _P, _P],
+    "qgemm_grouped_run": [_L, _C, _T, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "qgemm_quantize_act_fp8": [_P, _I64, _I64, _P, _P, _P],
     "qgemm_moe_permute": [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _I64, _P],
     "qgemm_moe_silu_mul": [_P, _I64, _I64, _P, _P],
     "qgemm_moe_combine": [_P, _P, _P, _I64, _I32, _I64, _P, _P],
-    "qgemm_debug_dequant": [_L, _P, _P, _P, _P, _P],
+    "qgemm_debug_dequant": [_L, _P, _P, _P],
     "qgemm_check_status": [_P, _P],
     "qgemm_describe_plan": [_L, _C, _I64, ctypes.c_char_p, _SZ],
 }
@@ -152,16 +152,15 @@ def tuning_config(block_tok=0, stages=0, max_ctas=0, split_k=0, cta_pair=0):
 
 # ------------------------------------------------------------- entry points
 
-def qgemm_packed_sizes(layer):
-    w, s, z = _SZ(), _SZ(), _SZ()
-    st = lib.qgemm_packed_sizes(ctypes.byref(layer), ctypes.byref(w), ctypes.byref(s),
-                                ctypes.byref(z))
-    return st, w.value, s.value, z.value
+def qgemm_packed_size(layer):
+    b = _SZ()
+    st = lib.qgemm_packed_size(ctypes.byref(layer), ctypes.byref(b))
+    return st, b.value
 
 
-def qgemm_pack_weights(layer, qweight, scales, qzeros, w_out, s_out, z_out, stream=None):
+def qgemm_pack_weights(layer, qweight, scales, qzeros, packed, stream=None):
     return lib.qgemm_pack_weights(ctypes.byref(layer), _ptr(qweight), _ptr(scales), _ptr(qzeros),
-                                  _ptr(w_out), _ptr(s_out), _ptr(z_out), _stream(stream))
+                                  _ptr(packed), _stream(stream))
 
 
 def qgemm_workspace_size(layer, compute, tuning, m):
@@ -175,25 +174,25 @@ def qgemm_workspace_init(workspace, nbytes, stream=None):
     return lib.qgemm_workspace_init(_ptr(workspace), nbytes, _stream(stream))
 
 
-def qgemm_run(layer, compute, tuning, m, a, a_scale, w, s, z, bias, c, workspace,
+def qgemm_run(layer, compute, tuning, m, a, a_scale, packed, bias, c, workspace,
               workspace_bytes, stream=None):
     return lib.qgemm_run(ctypes.byref(layer), ctypes.byref(compute), _ref(tuning), m, _ptr(a),
-                         _ptr(a_scale), _ptr(w), _ptr(s), _ptr(z), _ptr(bias), _ptr(c),
-                         _ptr(workspace), workspace_bytes, _stream(stream))
+                         _ptr(a_scale), _ptr(packed), _ptr(bias), _ptr(c), _ptr(workspace),
+                         workspace_bytes, _stream(stream))
 
 
-def qgemm_run_noalloc(layer, compute, tuning, m, a, a_scale, w, s, z, bias, c, stream=None):
+def qgemm_run_noalloc(layer, compute, tuning, m, a, a_scale, packed, bias, c, stream=None):
     return lib.qgemm_run_noalloc(ctypes.byref(layer), ctypes.byref(compute), _ref(tuning), m,
-                                 _ptr(a), _ptr(a_scale), _ptr(w), _ptr(s), _ptr(z), _ptr(bias),
-                                 _ptr(c), _stream(stream))
+                                 _ptr(a), _ptr(a_scale), _ptr(packed), _ptr(bias), _ptr(c),
+                                 _stream(stream))
 
 
-def qgemm_grouped_run(layer, compute, tuning, expert_offsets, total_rows, a, a_scale, w, s, z,
+def qgemm_grouped_run(layer, compute, tuning, expert_offsets, total_rows, a, a_scale, packed,
                       bias, c, workspace, workspace_bytes, stream=None):
     return lib.qgemm_grouped_run(ctypes.byref(layer), ctypes.byref(compute), _ref(tuning),
                                  _ptr(expert_offsets), total_rows, _ptr(a), _ptr(a_scale),
-                                 _ptr(w), _ptr(s), _ptr(z), _ptr(bias), _ptr(c),
-                                 _ptr(workspace), workspace_bytes, _stream(stream))
+                                 _ptr(packed), _ptr(bias), _ptr(c), _ptr(workspace),
+                                 workspace_bytes, _stream(stream))
 
 
 def qgemm_quantize_act_fp8(x, m, k, a8, a_scale, stream=None):
@@ -215,8 +214,8 @@ def qgemm_moe_combine(y2, inv_perm, topk_weights, t, topk, hidden, y, stream=Non
                                  _ptr(y), _stream(stream))
 
 
-def qgemm_debug_dequant(layer, w, s, z, out_kn, stream=None):
-    return lib.qgemm_debug_dequant(ctypes.byref(layer), _ptr(w), _ptr(s), _ptr(z), _ptr(out_kn),
+def qgemm_debug_dequant(layer, packed, out_kn, stream=None):
+    return lib.qgemm_debug_dequant(ctypes.byref(layer), _ptr(packed), _ptr(out_kn),
                                    _stream(stream))
 
 

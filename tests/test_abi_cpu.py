@@ -46,15 +46,19 @@ def _layer(Q, **kw):
     return Q.layer_config(**d)
 
 
-def test_packed_sizes_host_only(Q):
-    st, w, s, z = Q.qgemm_packed_sizes(_layer(Q))
+def test_packed_size_host_only(Q):
+    blocks = (4096 // 128) ** 2
+    st, b = Q.qgemm_packed_size(_layer(Q))
     assert st == Q.QGEMM_OK
-    assert w == 4096 * 4096 // 2 and s == 4096 * 32 * 2 and z == 0
-    st, w, s, z = Q.qgemm_packed_sizes(_layer(Q, weight_format=Q.QGEMM_W_UINT4_ZP,
-                                              zero_format=Q.QGEMM_Z_UINT4, group_size=32,
-                                              num_experts=3))
-    assert st == Q.QGEMM_OK and w == 3 * 4096 * 2048 and s == 3 * 4096 * 128 * 2
-    assert z == 3 * 4096 * 128
+    assert b == blocks * (8192 + 256)                    # codes + one scale per row
+    st, b = Q.qgemm_packed_size(_layer(Q, weight_format=Q.QGEMM_W_UINT4_ZP,
+                                       zero_format=Q.QGEMM_Z_UINT4, group_size=32,
+                                       num_experts=3))
+    assert st == Q.QGEMM_OK and b == 3 * blocks * (8192 + 4 * 256 + 4 * 128)
+    st, b = Q.qgemm_packed_size(_layer(Q, weight_format=Q.QGEMM_W_MXFP4,
+                                       scale_format=Q.QGEMM_S_E8M0, group_size=32,
+                                       act_dtype=Q.QGEMM_FP8E4M3, out_dtype=Q.QGEMM_BF16))
+    assert st == Q.QGEMM_OK and b == blocks * (8192 + 512)
 
 
 @pytest.mark.parametrize("bad,code", [
@@ -73,7 +77,7 @@ def test_packed_sizes_host_only(Q):
     (dict(has_bias=2), "INVALID_ARG"),
 ])
 def test_rejections_are_clear(Q, bad, code):
-    st, *_ = Q.qgemm_packed_sizes(_layer(Q, **bad))
+    st, _ = Q.qgemm_packed_size(_layer(Q, **bad))
     assert Q.status_string(st) == f"QGEMM_ERR_{code}"
     assert Q.last_error()
 
@@ -85,9 +89,9 @@ def test_status_strings(Q):
 
 
 def test_pack_rejects_missing_pointers_before_launch(Q):
-    assert Q.qgemm_pack_weights(_layer(Q), None, None, None, None, None, None, 0) == \
+    assert Q.qgemm_pack_weights(_layer(Q), None, None, None, None, 0) == \
         Q.QGEMM_ERR_INVALID_ARG
     asym = _layer(Q, weight_format=Q.QGEMM_W_UINT4_ZP, zero_format=Q.QGEMM_Z_UINT4,
                   act_dtype=Q.QGEMM_BF16, out_dtype=Q.QGEMM_BF16, scale_format=Q.QGEMM_S_BF16)
     # zero-point tensors are required for UINT4
-    assert Q.qgemm_pack_weights(asym, 16, 16, None, 16, 16, None, 0) == Q.QGEMM_ERR_INVALID_ARG
+    assert Q.qgemm_pack_weights(asym, 16, 16, None, 16, 0) == Q.QGEMM_ERR_INVALID_ARG

@@ -29,10 +29,8 @@ def test_repack_and_dequant_bit_exact(Q, adt, sym, g):
     c = Case(8, 384, 512, g, adt, sym, seed=31)
     lin = linear(c)
     torch.cuda.synchronize()
-    assert np.array_equal(lin.w.cpu().numpy(), layout.tiled_weights(c.q, sym))
-    assert np.array_equal(lin.s.cpu().numpy().view(np.uint16), layout.tiled_scales(c.s_bits, g, c.k))
-    if not sym:
-        assert np.array_equal(lin.z.cpu().numpy(), layout.tiled_zeros(c.z, g, c.k))
+    want = layout.packed_w4(c.q, c.s_bits, c.z, g, signed=sym)
+    assert np.array_equal(lin.packed.cpu().numpy(), want)
     deq = lin.dequantized().cpu().view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(deq, codecs.dtype_bits(adt, c.w_hat))
 
@@ -105,7 +103,7 @@ def test_m_zero_launches_nothing(Q):
     out = torch.empty(0, 128, dtype=torch.bfloat16, device=DEV)
     st, ws_bytes = Q.qgemm_workspace_size(lin.layer, lin.dense, None, 1)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV)
-    assert Q.qgemm_run(lin.layer, lin.dense, None, 0, x, None, lin.w, lin.s, lin.z, None, out,
+    assert Q.qgemm_run(lin.layer, lin.dense, None, 0, x, None, lin.packed, None, out,
                        ws, ws_bytes) == Q.QGEMM_OK
 
 
@@ -169,7 +167,7 @@ def test_error_paths_launch_nothing(Q):
     st, need = Q.qgemm_workspace_size(lin.layer, lin.dense, None, 8)
     ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
     run = lambda **kw: Q.qgemm_run(kw.get("layer", lin.layer), kw.get("compute", lin.dense), None,
-                                   kw.get("m", 8), kw.get("a", x), None, lin.w, lin.s, None, None,
+                                   kw.get("m", 8), kw.get("a", x), None, lin.packed, None,
                                    kw.get("c", out), kw.get("ws", ws), kw.get("wsb", need))
     assert run(wsb=need - 1) == Q.QGEMM_ERR_WORKSPACE
     assert run(a=x.data_ptr() + 2) == Q.QGEMM_ERR_INVALID_ARG

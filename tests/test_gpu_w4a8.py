@@ -50,8 +50,7 @@ def test_mxfp4_repack_and_e4m3_conversion_bit_exact(Q):
     c = MxCase(4, 384, 512, seed=51)
     lin = c.layer()
     torch.cuda.synchronize()
-    assert np.array_equal(lin.w.cpu().numpy(), layout.tiled_mxfp4_weights(c.codes_nk))
-    assert np.array_equal(lin.s.cpu().numpy(), layout.tiled_mxfp4_scales(c.b_nk))
+    assert np.array_equal(lin.packed.cpu().numpy(), layout.packed_mxfp4(c.codes_nk, c.b_nk))
     e4 = lin.codes_e4m3().cpu().numpy()
     want = codecs.encode_e4m3(codecs.decode_e2m1(c.codes_kn))
     # e2m1 -0 (code 8) maps to e4m3 -0 (0x80); both sides keep the sign
@@ -110,5 +109,5 @@ def test_w4a8_rejects_missing_scales(Q):
     out = torch.empty(8, 128, dtype=torch.bfloat16, device=DEV)
     st, need = Q.qgemm_workspace_size(lin.layer, lin.dense, None, 8)
     ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
-    assert Q.qgemm_run(lin.layer, lin.dense, None, 8, a8, None, lin.w, lin.s, None, None, out,
+    assert Q.qgemm_run(lin.layer, lin.dense, None, 8, a8, None, lin.packed, None, out,
                        ws, need) == Q.QGEMM_ERR_INVALID_ARG

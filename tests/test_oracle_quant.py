@@ -201,3 +201,54 @@ def test_mxfp4_tiled_layout_scalar_spec():
         sb = int(codes[nn, kk // 2])
         assert nib == ((sb >> 4) if kk % 2 else (sb & 0xF))
         assert ss[(nt * kt_count + kt) * 512 + nl * 4 + kl // 32] == b[nn, kk // 32]
+
+
+@pytest.mark.parametrize("gsize,zp", [(32, True), (128, False), (256, True)])
+def test_packed_buffer_scalar_spec(gsize, zp):
+    """Each packed block is [codes 8192][scales 256 ST][zeros 128 ST], blocks
+    in n-tile-major order: read single entries back by their byte address."""
+    g = np.random.default_rng(17)
+    k, n = 512, 256
+    q = g.integers(0, 16, (k, n)) if zp else g.integers(-8, 8, (k, n))
+    sb = g.integers(0, 65535, (k // gsize, n)).astype(np.uint16)
+    z = g.integers(0, 16, (k // gsize, n)) if zp else None
+    buf = layout.packed_w4(q, sb, z, gsize, signed=not zp)
+    st = max(1, 128 // gsize)
+    blk = 8192 + 256 * st + (128 * st if zp else 0)
+    kt_count = k // 128
+    assert buf.size == (k // 128) * (n // 128) * blk
+    for _ in range(1500):
+        kk, nn = int(g.integers(0, k)), int(g.integers(0, n))
+        nt, r = divmod(nn, 128)
+        kt, kl = divmod(kk, 128)
+        base = (nt * kt_count + kt) * blk
+        codes = buf[base: base + 8192]
+        want = q[kk, nn] if zp else q[kk, nn] + 8
+        # the block's codes sit at the start, so a one-block stream reader applies
+        assert _nibble_at(codes, r, kl, 1) == want
+        sg = kl // gsize if gsize < 128 else 0
+        sbyte = base + 8192 + 2 * (sg * 128 + r)
+        assert int(buf[sbyte]) | (int(buf[sbyte + 1]) << 8) == sb[kk // gsize, nn]
+        if zp:
+            assert buf[base + 8192 + 256 * st + sg * 128 + r] == z[kk // gsize, nn]
+
+
+def test_packed_mxfp4_scalar_spec():
+    g = np.random.default_rng(18)
+    n, k = 256, 384
+    codes = g.integers(0, 256, (n, k // 2)).astype(np.uint8)
+    b = g.integers(100, 140, (n, k // 32)).astype(np.uint8)
+    buf = layout.packed_mxfp4(codes, b)
+    kt_count = k // 128
+    assert buf.size == (n // 128) * kt_count * (8192 + 512)
+    for _ in range(1500):
+        nn, kk = int(g.integers(0, n)), int(g.integers(0, k))
+        nt, nl = divmod(nn, 128)
+        kt, kl = divmod(kk, 128)
+        qd, t = divmod(nl, 32)
+        j, rr = divmod(kl, 32)
+        base = (nt * kt_count + kt) * (8192 + 512)
+        byte = int(buf[base + ((qd * 4 + j) * 32 + t) * 16 + rr // 2])
+        nib = (byte >> 4) if rr % 2 else (byte & 0xF)
+        assert nib == (codes[nn, kk // 2] >> (4 * (kk % 2))) & 0xF
+        assert buf[base + 8192 + 4 * nl + j] == b[nn, kk // 32]

@@ -37,8 +37,8 @@ def test_noalloc_matches_workspace_entry_point(Q, m, n, k, g, adt, sym):
     assert lin.status() == Q.QGEMM_OK
     for _ in range(2):                                     # two calls in a row
         out = torch.full_like(ref_out, float("nan"))
-        st = Q.qgemm_run_noalloc(lin.layer, lin.dense, None, m, x, None, lin.w, lin.s, lin.z,
-                                 None, out)
+        st = Q.qgemm_run_noalloc(lin.layer, lin.dense, None, m, x, None, lin.packed, None,
+                                 out)
         assert st == Q.QGEMM_OK, Q.last_error()
         torch.cuda.synchronize()
         assert_close(to_np(out), to_np(ref_out), what="noalloc vs qgemm_run")
@@ -51,8 +51,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch(Q):
                            Q.QGEMM_BF16, Q.QGEMM_BF16)
     dense = Q.compute_config(Q.QGEMM_GEMM_DENSE)
     dummy = torch.zeros(16, dtype=torch.uint8, device=DEV)
-    st = Q.qgemm_run_noalloc(layer, dense, None, 1 << 20, dummy, None, dummy, dummy, None, None,
-                             dummy)
+    st = Q.qgemm_run_noalloc(layer, dense, None, 1 << 20, dummy, None, dummy, None, dummy)
     assert st == Q.QGEMM_ERR_UNSUPPORTED
     assert "scratch" in Q.last_error()
 
@@ -61,5 +60,5 @@ def test_noalloc_refuses_grouped(Q):
     layer = Q.layer_config(256, 256, 128, Q.QGEMM_W_INT4_SYM, Q.QGEMM_S_BF16, Q.QGEMM_Z_NONE,
                            Q.QGEMM_BF16, Q.QGEMM_BF16, num_experts=4)
     st = Q.qgemm_run_noalloc(layer, Q.compute_config(Q.QGEMM_GEMM_GROUPED), None, 8, 16, None,
-                             16, 16, None, None, 16)
+                             16, None, 16)
     assert st == Q.QGEMM_ERR_INVALID_ARG
