@@ -11,13 +11,16 @@ namespace qg {
 constexpr int kTileN = 128;       // output features per tile (MMA M extent)
 constexpr int kTileK = 128;       // K per pipeline stage
 constexpr int kTileBytes = kTileN * kTileK / 2;   // packed 4-bit weights per tile
-constexpr int kNumThreads = 512;  // 16 warps: producer, MMA, TMEM, spare, 8 dequant, 4 epilogue
+constexpr int kNumThreads = 512;  // 16 warps: weights, MMA, TMEM, activations, 8 dequant, 4 epilogue
 constexpr int kASlots = 4;        // TMEM slots for dequantized weight tiles
 constexpr int kASlotCols = 64;    // TMEM columns per slot (128 K x 16 bit)
-// k-tiles ("units") per pipeline stage for a token tile of bt rows: a stage is
-// filled by one bulk copy of its weights and one TMA box of its activations,
-// so small token tiles group several k-tiles to keep every copy large.
+// k-tiles ("units") per activation slot for a token tile of bt rows: a slot
+// is filled by one TMA box, so small token tiles group several k-tiles to
+// keep every copy large.
 __host__ __device__ constexpr int units_per_stage(int bt) { return bt <= 32 ? 4 : bt == 64 ? 2 : 1; }
+// k-tiles per weight slot (one bulk copy of their packed blocks).
+__host__ __device__ constexpr int weight_units_per_slot(int bt) { return bt <= 32 ? 4 : 2; }
+constexpr int kEpiStageBytes = 4 * 2 * 16 * 32 * 2;   // output staging: 4 warps x 2 x 16 x 32
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusDevice = 2;
 constexpr int kMaxExperts = 1024;      // grouped GEMM
@@ -53,9 +56,10 @@ struct W4A16Params {
   int* counters;
   int* status;
   long long max_tiles;
-  int stages;
-  int stage_bytes;
-  int off_w;                 // first packed block inside a stage
+  int x_stages, x_bytes;     // activation ring: slots, bytes per slot (1 KB multiple)
+  int w_stages, w_bytes, rw; // weight ring: slots, bytes per slot, k-tiles per slot
+  int off_w, off_epi, off_bar;   // shared-memory offsets of the weight ring, staging, barriers
+  int w_reuse;               // 1: several token tiles read each weight block (keep it in L2)
   int smem_bytes;            // total dynamic shared memory
   unsigned long long wait_limit_ns;
 };
@@ -63,8 +67,9 @@ struct W4A16Params {
 // Host-side plan for one W4A16 launch.
 int device_sm_count();
 // fmt: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 x e4m3, bf16 out)
-cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const W4A16Params& p, int block_tok,
-                         int fmt, bool grouped, int grid, cudaStream_t stream);
+cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
+                         const W4A16Params& p, int block_tok, int fmt, bool grouped, int grid,
+                         cudaStream_t stream);
 
 cudaError_t launch_repack_mxfp4(const uint8_t* codes, const uint8_t* scales, uint8_t* packed,
                                 int64_t n, int64_t k, int experts, cudaStream_t stream);

@@ -170,26 +170,47 @@ static int heuristic_block_tok(int64_t rows_per_group) {
   return 128;
 }
 
-// Pipeline stage geometry: [activation tile][weights][scales][zeros], 1 KB aligned.
-// W4A8 stages hold an 8-bit activation tile and 4 e8m0 bytes per weight row.
-static void stage_geometry(int bt, int st, int has_zp, bool mx, int* stage_bytes, int* off_w,
-                           int* off_s, int* off_z) {
-  const int r = units_per_stage(bt);
-  const int act = r * bt * kTileK * (mx ? 1 : 2);
-  *off_w = act;
-  *off_s = kTileBytes;                                   // inside a packed block
-  *off_z = kTileBytes + packed_scale_bytes(mx, st);
-  const int end = act + r * packed_block_bytes(mx, st, has_zp != 0);
-  *stage_bytes = (end + 1023) & ~1023;
+// Shared-memory geometry: the activation ring (1 KB aligned slots of
+// units_per_stage(bt) token tiles), the weight ring (slots of
+// weight_units_per_slot(bt) packed blocks), the per-warp output staging
+// buffers, then barriers, shared state and the grouped prefix arrays.  The
+// activation ring gets enough slots to cover a copy's latency at the tensor
+// rate; the weight ring gets the rest of shared memory (at most w_cap slots),
+// since it is what streams from HBM at small M.
+struct Geometry {
+  int x_bytes, x_stages, w_bytes, w_stages, rw, off_w, off_epi, off_bar, smem;
+};
+
+static int tail_smem(int sx, int sw, int experts) {
+  return (2 * sx + 2 * sw + 2 * kASlots + 4 + 2) * 8 + 32 + 2 * (experts + 1) * 4 + 64;
 }
 
-static int fixed_smem(int stages, int experts) {
-  // alignment slack + barriers + shared state + grouped prefix arrays
-  return 1024 + (2 * stages + 2 * kASlots + 4 + 2) * 8 + 32 + 2 * (experts + 1) * 4 + 64;
+static bool make_geometry(int bt, int st, int has_zp, bool mx, int experts, int w_cap,
+                          int smem_cap, Geometry* g) {
+  const int rx = units_per_stage(bt);
+  g->rw = weight_units_per_slot(bt);
+  g->x_bytes = (rx * bt * kTileK * (mx ? 1 : 2) + 1023) & ~1023;
+  g->w_bytes = g->rw * packed_block_bytes(mx, st, has_zp != 0);
+  for (int sx = bt <= 32 ? 3 : 4; sx >= 2; --sx) {
+    const int fixed = 1024 /* alignment slack */ + sx * g->x_bytes + 1023 + kEpiStageBytes +
+                      tail_smem(sx, 16, experts);
+    int sw = (smem_cap - fixed) / g->w_bytes;
+    if (sw > w_cap) sw = w_cap;
+    if (sw < 2) continue;
+    g->x_stages = sx;
+    g->w_stages = sw;
+    g->off_w = sx * g->x_bytes;
+    g->off_epi = (g->off_w + sw * g->w_bytes + 1023) & ~1023;
+    g->off_bar = g->off_epi + kEpiStageBytes;
+    g->smem = 1024 + g->off_bar + tail_smem(sx, sw, experts);
+    if (g->smem <= smem_cap) return true;
+  }
+  return false;
 }
 
 struct Plan {
-  int bt, stages, grid, st, stage_bytes, off_w, off_s, off_z, smem;
+  int bt, grid, st, off_s, off_z;
+  Geometry g;
   int64_t max_tiles;
   WorkspaceLayout ws;
 };
@@ -208,14 +229,11 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
     return fail(QGEMM_ERR_INVALID_ARG, "split_k must be 0 or 1");
   const int st = st_of(L->group_size);
   const int has_zp = L->zero_format == QGEMM_Z_UINT4;
-  int stage_bytes, off_w, off_s, off_z;
-  stage_geometry(bt, st, has_zp, is_mx(L), &stage_bytes, &off_w, &off_s, &off_z);
-  const int smem_cap = device_max_smem();
-  int stages = (T && T->stages) ? T->stages : 16;
-  if (stages < 2 || stages > 16) return fail(QGEMM_ERR_INVALID_ARG, "stages must be in [2, 16]");
-  while (stages > 2 && stages * stage_bytes + fixed_smem(stages, E) > smem_cap) --stages;
-  const int smem = stages * stage_bytes + fixed_smem(stages, E);
-  if (smem > smem_cap) return fail(QGEMM_ERR_UNSUPPORTED, "tile does not fit shared memory");
+  const int w_cap = (T && T->stages) ? T->stages : 16;
+  if (w_cap < 2 || w_cap > 16) return fail(QGEMM_ERR_INVALID_ARG, "stages must be in [2, 16]");
+  Geometry g;
+  if (!make_geometry(bt, st, has_zp, is_mx(L), E, w_cap, device_max_smem(), &g))
+    return fail(QGEMM_ERR_UNSUPPORTED, "tile does not fit shared memory");
   const int64_t kt = L->k / kTileK, nt = L->n / kTileN;
   int64_t tiles_bound;
   if (grouped)
@@ -232,14 +250,11 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
     if (T && T->split_k == 1 && tiles_bound < grid) grid = (int)(tiles_bound > 0 ? tiles_bound : 1);
   }
   P->bt = bt;
-  P->stages = stages;
   P->grid = grid;
   P->st = st;
-  P->stage_bytes = stage_bytes;
-  P->off_w = off_w;
-  P->off_s = off_s;
-  P->off_z = off_z;
-  P->smem = smem;
+  P->off_s = kTileBytes;                                   // inside a packed block
+  P->off_z = kTileBytes + packed_scale_bytes(is_mx(L), st);
+  P->g = g;
   P->max_tiles = tiles_bound;
   P->ws = workspace_layout(tiles_bound, grid, bt);
   return ok();
@@ -372,12 +387,26 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.partials = reinterpret_cast<float*>(ws + P.ws.partials_off);
   p.deterministic = deterministic ? 1 : 0;
   p.max_tiles = P.max_tiles;
-  p.stages = P.stages;
-  p.stage_bytes = P.stage_bytes;
-  p.off_w = P.off_w;
-  p.smem_bytes = P.smem;
+  p.x_stages = P.g.x_stages;
+  p.x_bytes = P.g.x_bytes;
+  p.w_stages = P.g.w_stages;
+  p.w_bytes = P.g.w_bytes;
+  p.rw = P.g.rw;
+  p.off_w = P.g.off_w;
+  p.off_epi = P.g.off_epi;
+  p.off_bar = P.g.off_bar;
+  p.smem_bytes = P.g.smem;
+  // several token tiles per weight block: keep weights in L2 rather than
+  // marking them first to evict
+  p.w_reuse = grouped ? (rows > (int64_t)E * P.bt) : (rows > P.bt);
   p.wait_limit_ns = g_wait_limit_ns;
-  cudaError_t e = launch_w4a16(tmap, p, P.bt, mx ? 2 : fp16 ? 1 : 0, grouped, P.grid, stream);
+  // output [rows, n] of 16-bit values, written by 16-row x 32-column tensor stores
+  CUtensorMap tmap_c;
+  if (!encode_tmap_2d(&tmap_c, CU_TENSOR_MAP_DATA_TYPE_UINT16, c, (uint64_t)L->n, (uint64_t)rows,
+                      (uint64_t)L->n * 2, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the output tensor");
+  cudaError_t e =
+      launch_w4a16(tmap, tmap_c, p, P.bt, mx ? 2 : fp16 ? 1 : 0, grouped, P.grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "W4A16 GEMM launch");
   return ok();
 }
@@ -620,13 +649,14 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
       char tmp[512];
       snprintf(tmp, sizeof(tmp),
                "kernel=%s%s weights=%s group=%d act=%s out=%s n=%lld k=%lld "
-               "m=%lld experts=%d block_tok=%d stages=%d grid=%d smem=%d workspace=%zu "
+               "m=%lld experts=%d block_tok=%d act_slots=%d weight_slots=%dx%d grid=%d smem=%d "
+               "workspace=%zu "
                "device=sm_103",
                is_mx(layer) ? "w4a8_tcgen05_mxf8f6f4_swapab" : "w4a16_tcgen05_swapab",
                grouped ? "_grouped" : "", wf[layer->weight_format], layer->group_size,
                dt[layer->act_dtype], dt[layer->out_dtype], (long long)layer->n,
-               (long long)layer->k, (long long)m, layer->num_experts, P.bt, P.stages, P.grid,
-               P.smem, P.ws.total);
+               (long long)layer->k, (long long)m, layer->num_experts, P.bt, P.g.x_stages,
+               P.g.w_stages, P.g.rw, P.grid, P.g.smem, P.ws.total);
       rec = tmp;
     }
   }

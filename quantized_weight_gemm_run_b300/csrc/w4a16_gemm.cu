@@ -235,16 +235,22 @@ __device__ __forceinline__ float from_out(uint16_t b) {
 // FMT: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 weights, e4m3
 // activations with per-row fp32 scales, block-scaled MMA, bf16 output).
 //
-// A pipeline stage holds up to R = units_per_stage(BT) consecutive k-tiles
-// ("units") of one output tile, so that each stage is filled by few, large
-// copies: one bulk copy of R weight blocks, one of their scales (and zero
-// points), and one three-dimensional TMA box holding the R activation tiles.
+// Shared memory holds two rings that turn over independently:
+//   activation slots: RX = units_per_stage(BT) consecutive k-tiles ("units")
+//     of one work item, one three-dimensional TMA box each; a slot goes back
+//     to its producer when the MMAs that read it have completed;
+//   weight slots: up to p.rw units' packed blocks (codes, scales, zero
+//     points), one bulk copy each; a slot goes back as soon as the dequant
+//     warps have read it into registers,
+// so the weight stream runs ahead of the activations and of the tensor core,
+// limited only by the weight ring's depth.
 template <int BT, int FMT, bool GROUPED>
 __global__ void __launch_bounds__(kNumThreads, 1)
-    w4a16_kernel(const __grid_constant__ CUtensorMap tmap_a, const W4A16Params p) {
+    w4a16_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                 const __grid_constant__ CUtensorMap tmap_c, const W4A16Params p) {
   constexpr bool FP16 = FMT == 1;
   constexpr bool MX = FMT == 2;
-  constexpr int R = units_per_stage(BT);
+  constexpr int RX = units_per_stage(BT);
   // tensor-memory columns: dequantized weight slots, then (MX) the A and B
   // scale factors, accumulators from column 256
   constexpr int kSlotCols = MX ? 32 : kASlotCols;
@@ -256,12 +262,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  const int S = p.stages;
-  uint8_t* stage_base = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * p.stage_bytes);
-  uint64_t* full = bars;
-  uint64_t* empty = full + S;
-  uint64_t* a_full = empty + S;
+  const int SX = p.x_stages, SW = p.w_stages, RW = p.rw;
+  uint8_t* x_base = smem;                    // SX slots of p.x_bytes (1 KB multiples)
+  uint8_t* w_base = smem + p.off_w;          // SW slots of p.w_bytes
+  uint16_t* epi_stage = reinterpret_cast<uint16_t*>(smem + p.off_epi);   // 4 warps x 2 x 16 x 32
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+  uint64_t* x_full = bars;
+  uint64_t* x_empty = x_full + SX;
+  uint64_t* w_full = x_empty + SX;
+  uint64_t* w_empty = w_full + SW;
+  uint64_t* a_full = w_empty + SW;
   uint64_t* a_empty = a_full + kASlots;
   uint64_t* acc_full = a_empty + kASlots;
   uint64_t* acc_empty = acc_full + 2;
@@ -275,6 +285,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = &sh->abort_flag;
   const uint64_t lim = p.wait_limit_ns;
+  const int blk_bytes = p.block_bytes;   // packed block: codes, scales, zero points
 
   auto coords = [&](int tile) {
     TileCoord<BT> tc;
@@ -296,58 +307,24 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     return tc;
   };
-
-  uint64_t pol_stream = 0, pol_keep = 0;   // L2 policies (set by thread 0)
-  const uint32_t blk_bytes = p.block_bytes;   // packed block: codes, scales, zero points
-
-  // ---- producer state (thread 0): one stage = up to R units of one work item
-  Schedule psched;
-  WorkItem pwi{0, 0, 0};
-  int pkt = 0, pr = 0;             // first k-tile and unit count of the current stage
-  bool phave = false;
-  int pstage = 0;
-  uint32_t pphase = 0;
-  long long issued = 0;            // stages issued
-  auto pnext = [&]() -> bool {     // advance to the next stage; false when none is left
-    if (phave && pkt + pr < pwi.k1) {
-      pkt += pr;
-    } else {
-      if (!psched.next(pwi)) return false;
-      phave = true;
-      pkt = pwi.k0;
-    }
-    pr = min(R, pwi.k1 - pkt);
-    return true;
-  };
-  // weights, scales and zero points of the current stage: read-only layer
-  // data, so they may be requested before the previous grid has finished
-  auto issue_weights = [&]() {
-    const TileCoord<BT> tc = coords(pwi.tile);
-    uint8_t* sp = stage_base + pstage * p.stage_bytes;
-    const long long blk = (long long)tc.nt * p.kt + pkt;
-    // the pr packed blocks of one n-tile's consecutive k-tiles are contiguous
-    mbar_arrive_expect_tx(&full[pstage], R * kActUnit + pr * blk_bytes);
-    bulk_load(sp + p.off_w, p.w + tc.e * p.w_expert_stride + blk * blk_bytes, pr * blk_bytes,
-              &full[pstage], pol_stream);
-  };
-  // the R activation tiles of a stage in one box: [chunk][BT rows][128 bytes]
-  auto issue_act = [&](int stage, int tile, int kt) {
-    const TileCoord<BT> tc = coords(tile);
-    tma_load_3d_hint(stage_base + stage * p.stage_bytes, &tmap_a, &full[stage], 0, tc.row0,
-                     kt * (MX ? 1 : 2), pol_keep);
-  };
-  auto advance_pstage = [&]() {
-    ++issued;
-    if (++pstage == S) {
-      pstage = 0;
-      pphase ^= 1;
+  // waits for every copy a producer issued into its ring to land, so that no
+  // copy is still writing shared memory when the CTA exits
+  auto drain_ring = [&](uint64_t* full, int S, long long issued) {
+    for (int st = 0; st < S && st < issued; ++st) {
+      const long long last = st + ((issued - 1 - st) / S) * S;
+      volatile int no_abort = 0;
+      mbar_wait(&full[st], (uint32_t)((last / S) & 1), &no_abort, nullptr, 100000000ull, 0);
     }
   };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+    for (int i = 0; i < SX; ++i) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&x_empty[i], 1);
+    }
+    for (int i = 0; i < SW; ++i) {
+      mbar_init(&w_full[i], 1);
+      mbar_init(&w_empty[i], 8);   // every dequant warp hands the slot back once
     }
     for (int i = 0; i < kASlots; ++i) {
       mbar_init(&a_full[i], 4);
@@ -361,9 +338,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     mbar_init(sfb_ready, 4);
     sh->abort_flag = 0;
     fence_barrier_init();
-    prefetch_tmap(&tmap_a);
-    pol_stream = policy_evict_first();
-    pol_keep = policy_evict_last();
   }
   if (warp == 2) {
     tmem_alloc(&sh->tmem_base, 512);
@@ -399,7 +373,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (lane == 0) sh->tiles = (long long)((p.rows + BT - 1) / BT) * p.nt;
     }
   }
-  // Start-up barrier.  For a dense GEMM the producer warp only arrives (it
+  // Start-up barrier.  For a dense GEMM the weight producer only arrives (it
   // needs neither tensor memory nor the grouped tile table), so the weight
   // stream starts while the other warps wait for the allocation.
   tc_fence_before();
@@ -417,51 +391,82 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   Schedule sched;
   sched.init(T, p.kt, gridDim.x, blockIdx.x);
-
   // Programmatic dependent launch: the next grid on the stream may start its
   // CTAs as soon as SMs free up; everything it reads from this grid is read
   // after its own grid_dependency_wait.
   grid_launch_dependents();
 
   if (warp == 0) {
-    // ------------------------------------------------ producer
+    // ------------------------------------------------ weight producer
+    // Packed weights are read-only layer data, so they stream before (and
+    // regardless of) the wait for the previous grid on the stream.
     if (lane == 0) {
-      psched.init(T, p.kt, gridDim.x, blockIdx.x);
-      // the first S stages' weights go out before waiting for the previous
-      // grid on the stream (which may still write this GEMM's activations or
-      // workspace); their activation boxes follow the wait
-      int pre = 0;
-      int pre_tile[16], pre_kt[16];
-      while (pre < S && pnext()) {
-        issue_weights();
-        pre_tile[pre] = pwi.tile;
-        pre_kt[pre] = pkt;
-        ++pre;
-        advance_pstage();
+      const uint64_t pol = p.w_reuse ? policy_evict_normal() : policy_evict_first();
+      long long issued = 0;
+      int ws = 0;
+      uint32_t wph = 0;
+      WorkItem wi;
+      bool ok = true;
+      while (ok && sched.next(wi)) {
+        const TileCoord<BT> tc = coords(wi.tile);
+        // the blocks of one n-tile's consecutive k-tiles are contiguous
+        const uint8_t* src = p.w + tc.e * p.w_expert_stride +
+                             ((long long)tc.nt * p.kt + wi.k0) * blk_bytes;
+        for (int kt = wi.k0; kt < wi.k1; kt += RW) {
+          const int r = min(RW, wi.k1 - kt);
+          if (!mbar_wait(&w_empty[ws], wph ^ 1, abort_flag, p.status, lim, kStatusTimeout)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&w_full[ws], r * blk_bytes);
+          bulk_load(w_base + ws * p.w_bytes, src + (long long)(kt - wi.k0) * blk_bytes,
+                    r * blk_bytes, &w_full[ws], pol);
+          ++issued;
+          if (++ws == SW) {
+            ws = 0;
+            wph ^= 1;
+          }
+        }
       }
-      grid_dependency_wait();
-      for (int i = 0; i < pre; ++i) issue_act(i, pre_tile[i], pre_kt[i]);
-      while (pnext()) {
-        if (!mbar_wait(&empty[pstage], pphase ^ 1, abort_flag, p.status, lim, kStatusTimeout))
-          break;
-        issue_weights();
-        issue_act(pstage, pwi.tile, pkt);
-        advance_pstage();
+      drain_ring(w_full, SW, issued);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------ activation producer
+    if (lane == 0) {
+      prefetch_tmap(&tmap_a);
+      const uint64_t pol = policy_evict_last();
+      grid_dependency_wait();   // the previous grid may still write the activations
+      long long issued = 0;
+      int xs = 0;
+      uint32_t xph = 0;
+      WorkItem wi;
+      bool ok = true;
+      while (ok && sched.next(wi)) {
+        const TileCoord<BT> tc = coords(wi.tile);
+        for (int kt = wi.k0; kt < wi.k1; kt += RX) {
+          if (!mbar_wait(&x_empty[xs], xph ^ 1, abort_flag, p.status, lim, kStatusTimeout)) {
+            ok = false;
+            break;
+          }
+          // the RX activation tiles of a slot in one box: [chunk][BT rows][128 bytes]
+          mbar_arrive_expect_tx(&x_full[xs], RX * kActUnit);
+          tma_load_3d_hint(x_base + xs * p.x_bytes, &tmap_a, &x_full[xs], 0, tc.row0,
+                           kt * (MX ? 1 : 2), pol);
+          ++issued;
+          if (++xs == SX) {
+            xs = 0;
+            xph ^= 1;
+          }
+        }
       }
-      // drain: never leave a copy in flight into shared memory we are leaving
-      for (int st = 0; st < S && st < issued; ++st) {
-        long long last = st + ((issued - 1 - st) / S) * S;
-        uint32_t par = (uint32_t)((last / S) & 1);
-        volatile int no_abort = 0;
-        mbar_wait(&full[st], par, &no_abort, nullptr, 100000000ull, 0);
-      }
+      drain_ring(x_full, SX, issued);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (elect_one()) {
       const uint32_t idesc = MX ? idesc_mxf8f6f4_e4m3(BT) : idesc_f16(FP16 ? 0u : 1u, BT);
-      int stage = 0, slot = 0, acc = 0;
-      uint32_t phase = 0, aphase = 0, accphase = 0;
+      int xs = 0, slot = 0, acc = 0;
+      uint32_t xph = 0, aphase = 0, accphase = 0;
       WorkItem wi;
       bool ok = true;
       if constexpr (MX)   // the B scale factors (all 1.0) are written by the epilogue warps
@@ -472,13 +477,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + kAccCol + acc * BT;
-        for (int kt0 = wi.k0; ok && kt0 < wi.k1; kt0 += R) {
-          const int r = min(R, wi.k1 - kt0);
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim, kStatusTimeout)) {
+        for (int kt0 = wi.k0; ok && kt0 < wi.k1; kt0 += RX) {
+          const int r = min(RX, wi.k1 - kt0);
+          if (!mbar_wait(&x_full[xs], xph, abort_flag, p.status, lim, kStatusTimeout)) {
             ok = false;
             break;
           }
-          const uint32_t sbase = smem_u32(stage_base + stage * p.stage_bytes);
+          const uint32_t sbase = smem_u32(x_base + xs * p.x_bytes);
           for (int i = 0; i < r; ++i) {
             if (!mbar_wait(&a_full[slot], aphase, abort_flag, p.status, lim, kStatusTimeout)) {
               ok = false;
@@ -511,10 +516,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
           }
           if (!ok) break;
-          mma_commit(&empty[stage]);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1;
+          mma_commit(&x_empty[xs]);
+          if (++xs == SX) {
+            xs = 0;
+            xph ^= 1;
           }
         }
         if (!ok) break;
@@ -532,39 +537,66 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------ dequant
     // Two warps per TMEM lane quadrant; warp group h takes every other unit
-    // (h = unit index & 1) and dequantizes all 128 k of its 32 rows.
+    // (h = unit index & 1) and dequantizes all 128 k of its 32 rows.  Each
+    // warp hands a weight slot back once per use, right after its last read
+    // of it (at once when the slot holds none of its group's units).
     const int q = warp & 3;             // TMEM lane quadrant
     const int h = (warp - 4) >> 2;      // which units: even (0) or odd (1)
     const int row = q * 32 + lane;      // output feature within the tile
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     constexpr uint32_t magic16 = FP16 ? 0x6400u : 0x4300u;
-    int stage = 0, slot = 0;
-    uint32_t phase = 0, aphase = 0;
+    int ws = 0, slot = 0;
+    uint32_t wph = 0, aphase = 0;
     long long unit = 0;
     WorkItem wi;
     bool ok = true;
     while (ok && sched.next(wi)) {
-      for (int kt0 = wi.k0; ok && kt0 < wi.k1; kt0 += R) {
-        const int r = min(R, wi.k1 - kt0);
-        const uint8_t* sp = stage_base + stage * p.stage_bytes;
-        for (int i = 0; i < r; ++i, ++unit) {
-          if ((unit & 1) == h) {
-            if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim, kStatusTimeout) ||
-                !mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
+      for (int kt0 = wi.k0; ok && kt0 < wi.k1; kt0 += RW) {
+        const int r = min(RW, wi.k1 - kt0);
+        if (!mbar_wait(&w_full[ws], wph, abort_flag, p.status, lim, kStatusTimeout)) {
+          ok = false;
+          break;
+        }
+        int i_last = r - 1;                       // this group's last unit in the slot
+        if ((int)((unit + i_last) & 1) != h) --i_last;
+        if (i_last < 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&w_empty[ws]);
+        }
+        const uint8_t* sp = w_base + ws * p.w_bytes;
+        for (int i = 0; i < r; ++i) {
+          if ((int)((unit + i) & 1) == h) {
+            const uint8_t* bp = sp + i * blk_bytes;   // this unit's packed block
+            const uint4* wv = reinterpret_cast<const uint4*>(bp);
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = wv[(q * 4 + j) * 32 + lane];
+            uint32_t scale2[4], zero2[4], sf = 0;
+            if constexpr (MX) {
+              sf = reinterpret_cast<const uint32_t*>(bp + p.s_off)[row];
+            } else {
+              const uint16_t* sv = reinterpret_cast<const uint16_t*>(bp + p.s_off);
+              const uint8_t* zv = bp + p.z_off;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int sg = j >> p.sg_shift;
+                scale2[j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
+                const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
+                zero2[j] = (magic16 + zq) * 0x00010001u;
+              }
+            }
+            if (i == i_last) {   // every read of the slot by this warp is done
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&w_empty[ws]);
+            }
+            if (!mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
                            kStatusTimeout)) {
               ok = false;
               break;
             }
-            const uint8_t* bp = sp + p.off_w + i * blk_bytes;   // this unit's packed block
-            const uint4* wv = reinterpret_cast<const uint4*>(bp);
             if constexpr (MX) {
               // 128 e2m1 codes of this row -> 128 e4m3 bytes (32 columns), and
               // its four e8m0 block scales -> the slot's four scale columns
-              uint4 v[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) v[j] = wv[(q * 4 + j) * 32 + lane];
-              const uint32_t sf =
-                  reinterpret_cast<const uint32_t*>(bp + p.s_off)[row];
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 uint32_t o8[8];
@@ -574,20 +606,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               const uint32_t sf4[4] = {sf, sf, sf, sf};
               tmem_st4(tmem_base + lane_addr + kSfaCol + slot * 4, sf4);
             } else {
-              const uint16_t* sv = reinterpret_cast<const uint16_t*>(bp + p.s_off);
-              const uint8_t* zv = bp + p.z_off;
-              // every shared-memory read of the unit first, then the arithmetic
-              uint4 v[4];
-              uint32_t scale2[4], zero2[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) v[j] = wv[(q * 4 + j) * 32 + lane];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int sg = j >> p.sg_shift;
-                scale2[j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
-                const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
-                zero2[j] = (magic16 + zq) * 0x00010001u;
-              }
               const uint32_t tbase = tmem_base + lane_addr + slot * kSlotCols;
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
@@ -606,9 +624,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             aphase ^= 1;
           }
         }
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1;
+        unit += r;
+        if (++ws == SW) {
+          ws = 0;
+          wph ^= 1;
         }
       }
     }
@@ -618,6 +637,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int q = warp & 3;
     const int col = q * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    if (lane == 0) prefetch_tmap(&tmap_c);
     if constexpr (MX) {   // B scale factors: every byte 2^0 (e8m0 127)
       uint32_t ones[32];
 #pragma unroll
@@ -628,6 +648,41 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(sfb_ready);
     }
+    // Output of 16 rows x this warp's 32 columns: rounded into a per-warp
+    // staging buffer (two, used in turn) and written by one tensor store,
+    // which drops rows past the end of the output.  A grouped tile's last
+    // chunk may end inside the tile (the next rows belong to the next
+    // expert); its rows are stored one by one instead.
+    uint16_t* stg = epi_stage + q * (2 * 16 * 32);
+    int sbuf = 0;
+    auto emit = [&](const TileCoord<BT>& tc, int m0, const float (&f)[16], float bias) {
+      uint16_t o[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float v = f[i];
+        if constexpr (MX)   // W4A8: the per-row activation scale multiplies the fp32 sum
+          v *= (m0 + i < tc.rows) ? p.a_scale[tc.row0 + m0 + i] : 0.f;
+        o[i] = to_out<FP16>(v + bias);
+      }
+      const int valid = tc.rows - m0;
+      if (!GROUPED || valid >= 16) {
+        uint16_t* sb = stg + sbuf * (16 * 32);
+        if (lane == 0) bulk_wait_group_read<1>();   // this buffer's previous store has read it
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sb[i * 32 + lane] = o[i];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmap_c, sb, tc.nt * kTileN + q * 32, tc.row0 + m0);
+          bulk_commit_group();
+        }
+        sbuf ^= 1;
+      } else {
+        uint16_t* dst = p.c + (long long)(tc.row0 + m0) * p.n + tc.nt * kTileN + col;
+        for (int i = 0; i < valid; ++i) dst[(long long)i * p.n] = o[i];
+      }
+    };
     int acc = 0;
     uint32_t accphase = 0;
     WorkItem wi;
@@ -637,19 +692,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (!mbar_wait(&acc_full[acc], accphase, abort_flag, p.status, lim, kStatusTimeout)) break;
       tc_fence_after();
       const int n = tc.nt * kTileN + col;
-      float bias = 0.f;
-      if (p.bias) bias = from_out<FP16>(p.bias[(long long)tc.e * p.n + n]);
+      const float bias = p.bias ? from_out<FP16>(p.bias[(long long)tc.e * p.n + n]) : 0.f;
       const uint32_t tbase = tmem_base + lane_addr + kAccCol + acc * BT;
-      // W4A8: the per-row activation scale multiplies the fp32 accumulator
-      auto row_scale = [&](int m) -> float {
-        if constexpr (MX) return p.a_scale[tc.row0 + m];
-        else return 1.f;
-      };
-      // partial slot of this CTA for this segment (split tiles only)
+      // partial tile of this CTA for this segment (split tiles only),
+      // column-major [col][BT]: this thread's column is contiguous
       const long long tl = wi.tile - sched.W * sched.G;
       const long long u_start = tl * p.kt;
-      // split tiles: fixed-order mode writes this CTA's partial to its own
-      // slot; atomic mode adds it into the tile's accumulator
       float* my_part = nullptr;
       if (!whole) {
         if (p.deterministic) {
@@ -659,20 +707,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           my_part = p.partials + tl * (BT * kTileN);
         }
       }
+      // only 16-row chunks holding output rows are read: rows past the end
+      // stay untouched (zero) in the split accumulators
 #pragma unroll 1
-      for (int mc = 0; mc < BT / 16; ++mc) {
+      for (int mc = 0; mc < BT / 16 && mc * 16 < tc.rows; ++mc) {
         uint32_t v[16];
         tmem_ld16_wait(tbase + mc * 16, v);
         if (whole) {
+          float f[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int m = mc * 16 + i;
-            if (m < tc.rows)
-              p.c[(long long)(tc.row0 + m) * p.n + n] =
-                  to_out<FP16>(__uint_as_float(v[i]) * row_scale(m) + bias);
-          }
+          for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+          emit(tc, mc * 16, f, bias);
         } else if (p.deterministic) {
-          // partial tile, column-major [col][BT]: this thread's column is contiguous
           float4* dst = reinterpret_cast<float4*>(my_part + col * BT + mc * 16);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -708,79 +754,66 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         old = __shfl_sync(0xffffffffu, old, 0);
         __syncwarp();   // orders every lane's reads after lane 0's acquire
         if (old == contributors - 1 && !p.deterministic) {
-          // atomic mode: the accumulator holds the sum; read it (32 rows per
-          // pass, all loads issued before use), write the output, and leave
-          // the accumulator zeroed for the next launch
-          const float4* src4 = reinterpret_cast<const float4*>(my_part + col * BT);
-          float4* z4 = reinterpret_cast<float4*>(my_part + col * BT);
-          for (int m0 = 0; m0 < tc.rows; m0 += 32) {
-            float4 a4[8];
+          // atomic mode: the accumulator holds the sum; read it 16 rows at a
+          // time, write the output, and leave the accumulator zeroed for the
+          // next launch
+          float4* acc4 = reinterpret_cast<float4*>(my_part + col * BT);
+          for (int m0 = 0; m0 < tc.rows; m0 += 16) {
+            float f[16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (m0 + 4 * j < BT) a4[j] = __ldcg(src4 + m0 / 4 + j);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (m0 + 4 * j < BT) {
-                z4[m0 / 4 + j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                const float* af = reinterpret_cast<const float*>(&a4[j]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const int m = m0 + 4 * j + i;
-                  if (m < tc.rows)
-                    p.c[(long long)(tc.row0 + m) * p.n + n] =
-                        to_out<FP16>(af[i] * row_scale(m) + bias);
-                }
-              }
+            for (int j = 0; j < 4; ++j) {
+              const float4 a4 = __ldcg(acc4 + m0 / 4 + j);
+              f[4 * j] = a4.x;
+              f[4 * j + 1] = a4.y;
+              f[4 * j + 2] = a4.z;
+              f[4 * j + 3] = a4.w;
             }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc4[m0 / 4 + j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            emit(tc, m0, f, bias);
           }
-          // rows past tc.rows hold what the MMA computed for the tile's padding
-          // rows (zero fill or the next expert's tokens): clear them as well
-          for (int m0 = ((tc.rows + 31) / 32) * 32; m0 < BT; m0 += 4)
-            z4[m0 / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (lane == 0) *counter = 0;   // ready for the next launch
         } else if (old == contributors - 1) {
-          // fixed-order mode, 8 rows per pass; up to 4 contributors' partials
-          // are loaded before any is added, then summed in CTA order
-          for (int m0 = 0; m0 < tc.rows; m0 += 8) {
-            float4 acc4[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-            for (long long cc0 = c_first; cc0 <= c_last; cc0 += 4) {
-              float4 v4[4][2];
+          // fixed-order mode: the contributors' partials summed in CTA order,
+          // two contributors' loads in flight at a time
+          for (int m0 = 0; m0 < tc.rows; m0 += 16) {
+            float f[16];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 16; ++i) f[i] = 0.f;
+            for (long long cc0 = c_first; cc0 <= c_last; cc0 += 2) {
+              float4 v4[2][4];
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
                 const long long cc = cc0 + i;
                 if (cc <= c_last) {
                   const int which = (sched.sk_begin(cc) >= u_start) ? 0 : 1;
                   const float4* src4 = reinterpret_cast<const float4*>(
                       p.partials + ((long long)(2 * cc + which)) * (BT * kTileN) + col * BT + m0);
-                  v4[i][0] = __ldcg(src4);
-                  v4[i][1] = __ldcg(src4 + 1);
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) v4[i][j] = __ldcg(src4 + j);
                 }
               }
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
+              for (int i = 0; i < 2; ++i) {
                 if (cc0 + i <= c_last) {
 #pragma unroll
-                  for (int j = 0; j < 2; ++j) {
-                    acc4[j].x += v4[i][j].x;
-                    acc4[j].y += v4[i][j].y;
-                    acc4[j].z += v4[i][j].z;
-                    acc4[j].w += v4[i][j].w;
+                  for (int j = 0; j < 4; ++j) {
+                    f[4 * j] += v4[i][j].x;
+                    f[4 * j + 1] += v4[i][j].y;
+                    f[4 * j + 2] += v4[i][j].z;
+                    f[4 * j + 3] += v4[i][j].w;
                   }
                 }
               }
             }
-            const float* accf = reinterpret_cast<const float*>(acc4);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              if (m0 + i < tc.rows)
-                p.c[(long long)(tc.row0 + m0 + i) * p.n + n] =
-                    to_out<FP16>(accf[i] * row_scale(m0 + i) + bias);
-            }
+            emit(tc, m0, f, bias);
           }
           if (lane == 0) *counter = 0;   // ready for the next launch
         }
       }
     }
+    if (lane == 0) bulk_wait_group_all();   // tensor stores done before the CTA exits
+    __syncwarp();
   }
 
   __syncwarp();
@@ -793,8 +826,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 // ---------------------------------------------------------------- host side
 
 template <int BT, int FMT, bool GROUPED>
-static cudaError_t launch_t(const CUtensorMap& tmap, const W4A16Params& p, int grid,
-                            cudaStream_t stream) {
+static cudaError_t launch_t(const CUtensorMap& tmap, const CUtensorMap& tmap_c,
+                            const W4A16Params& p, int grid, cudaStream_t stream) {
   auto kern = w4a16_kernel<BT, FMT, GROUPED>;
   static int attr_set = 0;   // largest dynamic shared memory size enabled so far
   if (p.smem_bytes > attr_set) {
@@ -813,30 +846,31 @@ static cudaError_t launch_t(const CUtensorMap& tmap, const W4A16Params& p, int g
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmap, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_c, p);
 }
 
 template <int FMT, bool GROUPED>
-static cudaError_t launch_bt(const CUtensorMap& tmap, const W4A16Params& p, int bt, int grid,
-                             cudaStream_t stream) {
+static cudaError_t launch_bt(const CUtensorMap& tmap, const CUtensorMap& tmap_c,
+                             const W4A16Params& p, int bt, int grid, cudaStream_t stream) {
   switch (bt) {
-    case 16: return launch_t<16, FMT, GROUPED>(tmap, p, grid, stream);
-    case 32: return launch_t<32, FMT, GROUPED>(tmap, p, grid, stream);
-    case 64: return launch_t<64, FMT, GROUPED>(tmap, p, grid, stream);
-    case 128: return launch_t<128, FMT, GROUPED>(tmap, p, grid, stream);
+    case 16: return launch_t<16, FMT, GROUPED>(tmap, tmap_c, p, grid, stream);
+    case 32: return launch_t<32, FMT, GROUPED>(tmap, tmap_c, p, grid, stream);
+    case 64: return launch_t<64, FMT, GROUPED>(tmap, tmap_c, p, grid, stream);
+    case 128: return launch_t<128, FMT, GROUPED>(tmap, tmap_c, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const W4A16Params& p, int block_tok,
-                         int fmt, bool grouped, int grid, cudaStream_t stream) {
+cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
+                         const W4A16Params& p, int block_tok, int fmt, bool grouped, int grid,
+                         cudaStream_t stream) {
   switch (fmt) {
-    case 0: return grouped ? launch_bt<0, true>(tmap_a, p, block_tok, grid, stream)
-                           : launch_bt<0, false>(tmap_a, p, block_tok, grid, stream);
-    case 1: return grouped ? launch_bt<1, true>(tmap_a, p, block_tok, grid, stream)
-                           : launch_bt<1, false>(tmap_a, p, block_tok, grid, stream);
-    case 2: return grouped ? launch_bt<2, true>(tmap_a, p, block_tok, grid, stream)
-                           : launch_bt<2, false>(tmap_a, p, block_tok, grid, stream);
+    case 0: return grouped ? launch_bt<0, true>(tmap_a, tmap_c, p, block_tok, grid, stream)
+                           : launch_bt<0, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
+    case 1: return grouped ? launch_bt<1, true>(tmap_a, tmap_c, p, block_tok, grid, stream)
+                           : launch_bt<1, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
+    case 2: return grouped ? launch_bt<2, true>(tmap_a, tmap_c, p, block_tok, grid, stream)
+                           : launch_bt<2, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
