@@ -10,7 +10,8 @@ step touches ~330 MB and each GEMM reads its operands cold from HBM (the
 CUDA graph and replayed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload sweep|w4a16_m16|large|moe]
+                  [--workload sweep|w4a16_m16|large|w4a8|moe16|moe256|moe4096|
+                              shape:M,N,K[,sym|asym][,bf16|fp16]]
 
 Other workloads (--workload) are for kernel studies and print the same line
 format for their own configuration.  --impl reference times the CPU oracle
@@ -58,6 +59,15 @@ def sweep_points():
 
 
 def workload_points(name):
+    if name.startswith("shape:"):
+        # one W4A16 GEMM of the given shape (kernel studies, profiling)
+        f = name[len("shape:"):].split(",")
+        m, n, k = (int(v) for v in f[:3])
+        asym = "asym" in f[3:]
+        adt = "fp16" if "fp16" in f[3:] else "bf16"
+        return [dict(m=m, n=n, k=k, g=128, asym=asym, adt=adt)], dict(
+            workload=f"w4a16_{'asym' if asym else 'sym'}_{m}x{n}x{k}", m=m, n=n, k=k, group=128,
+            weights="uint4+zp" if asym else "int4", act=adt)
     if name == "sweep":
         return sweep_points(), dict(workload="w4a16_asym_sweep", shapes=synth.W4A16_ASYM_SHAPES,
                                     ms=synth.W4A16_ASYM_MS, group=128, weights="uint4+zp",
@@ -316,6 +326,43 @@ def make_point(p, seed, device, host=False):
     return GemmPoint(p, seed, device, host)
 
 
+def kernel_source_digest():
+    """Digest of the GEMM kernel's sources; a committed ncu traffic figure is
+    used only while it matches."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("w4a16_gemm.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "quantized_weight_gemm_run_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per launch from the committed ncu summaries under profiles/:
+    lines 'traffic shape=MxNxK(,asym|,sym)(,bf16|,fp16) dram_bytes=B source=D'."""
+    out = {}
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return out
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, fn)) as fh:
+            for line in fh:
+                line = line.strip().strip("`")
+                if not line.startswith("traffic "):
+                    continue
+                kv = dict(t.split("=", 1) for t in line.split()[1:] if "=" in t)
+                if {"shape", "dram_bytes", "source"} <= kv.keys():
+                    out[kv["shape"]] = (int(kv["dram_bytes"]), kv["source"])
+    return out
+
+
+def shape_key(p):
+    return (f"{p['m']}x{p['n']}x{p['k']},{'asym' if p.get('asym') else 'sym'},{p['adt']}"
+            if p.get("kind", "w4a16") == "w4a16" else None)
+
+
 def cold_copies(p):
     """Distinct buffer sets needed so that a rotation exceeds twice the L2."""
     return int(np.ceil(2 * L2_BYTES / point_bytes(p))) + 1
@@ -448,6 +495,14 @@ def run_ours(args, rank, world, device):
         achieved = dom_bytes / dom_us / 1e3
         roof = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
                     unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None)
+    # DRAM traffic per launch of the dominant kernel from the committed ncu
+    # captures of its shapes, while they match the current kernel source
+    traffic = committed_traffic()
+    digest = kernel_source_digest()
+    dom_pts = [p for pp, p in zip(per_point, pts) if pp["kernel"] == dom[0]]
+    keys = [shape_key(p) for p in dom_pts]
+    if keys and all(k in traffic and traffic[k][1] == digest for k in keys):
+        roof["traffic"] = int(sum(traffic[k][0] for k in keys) / len(keys))
     roof.update(kernel=dom[0], launches_per_step=dom_launches,
                 per_launch="algorithmic bytes/flops of its GEMMs / mean CUDA-event time per launch",
                 peak_source=f"{peak_src} ({'bf16 burst' if tensor_bound else 'copy bandwidth'})")
@@ -632,11 +687,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sweep",
-                    choices=["sweep", "w4a16_m16", "large", "w4a8", "moe16", "moe256", "moe4096"])
+                    help="sweep | w4a16_m16 | large | w4a8 | moe16 | moe256 | moe4096 | "
+                         "shape:M,N,K[,sym|asym][,bf16|fp16]")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    try:
+        workload_points(args.workload)
+    except (ValueError, IndexError):
+        ap.error(f"unknown workload {args.workload!r}")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
