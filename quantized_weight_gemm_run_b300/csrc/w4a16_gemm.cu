@@ -755,22 +755,32 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         __syncwarp();   // orders every lane's reads after lane 0's acquire
         if (old == contributors - 1 && !p.deterministic) {
           // atomic mode: the accumulator holds the sum; read it 16 rows at a
-          // time, write the output, and leave the accumulator zeroed for the
-          // next launch
+          // time with two chunks' loads in flight (each L2 round trip
+          // is long while other CTAs' reductions drain), write the output,
+          // and leave the accumulator zeroed for the next launch
           float4* acc4 = reinterpret_cast<float4*>(my_part + col * BT);
-          for (int m0 = 0; m0 < tc.rows; m0 += 16) {
+          const int nch = (tc.rows + 15) / 16;
+          float4 cur[4], nxt[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) cur[j] = __ldcg(acc4 + j);
+#pragma unroll 1
+          for (int c = 0; c < nch; ++c) {
+            if (c + 1 < nch)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) nxt[j] = __ldcg(acc4 + (c + 1) * 4 + j);
             float f[16];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const float4 a4 = __ldcg(acc4 + m0 / 4 + j);
-              f[4 * j] = a4.x;
-              f[4 * j + 1] = a4.y;
-              f[4 * j + 2] = a4.z;
-              f[4 * j + 3] = a4.w;
+              f[4 * j] = cur[j].x;
+              f[4 * j + 1] = cur[j].y;
+              f[4 * j + 2] = cur[j].z;
+              f[4 * j + 3] = cur[j].w;
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc4[m0 / 4 + j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            emit(tc, m0, f, bias);
+            for (int j = 0; j < 4; ++j) acc4[c * 4 + j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            emit(tc, c * 16, f, bias);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
           }
           if (lane == 0) *counter = 0;   // ready for the next launch
         } else if (old == contributors - 1) {
