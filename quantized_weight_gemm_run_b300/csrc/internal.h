@@ -60,6 +60,7 @@ struct W4A16Params {
   int w_stages, w_bytes, rw; // weight ring: slots, bytes per slot, k-tiles per slot
   int off_w, off_epi, off_bar;   // shared-memory offsets of the weight ring, staging, barriers
   int w_reuse;               // 1: several token tiles read each weight block (keep it in L2)
+  int fix_smem;              // 1: the activation ring can hold a split tile's fp32 sum
   int smem_bytes;            // total dynamic shared memory
   unsigned long long wait_limit_ns;
 };

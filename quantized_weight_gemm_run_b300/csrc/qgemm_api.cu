@@ -182,7 +182,7 @@ struct Geometry {
 };
 
 static int tail_smem(int sx, int sw, int experts) {
-  return (2 * sx + 2 * sw + 2 * kASlots + 4 + 2) * 8 + 32 + 2 * (experts + 1) * 4 + 64;
+  return (2 * sx + 2 * sw + 2 * kASlots + 4 + 2 + 4) * 8 + 32 + 2 * (experts + 1) * 4 + 64;
 }
 
 static bool make_geometry(int bt, int st, int has_zp, bool mx, int experts, int w_cap,
@@ -399,6 +399,9 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   // several token tiles per weight block: keep weights in L2 rather than
   // marking them first to evict
   p.w_reuse = grouped ? (rows > (int64_t)E * P.bt) : (rows > P.bt);
+  // a split tile's finisher copies the other contributors' fp32 sum (BT x 128)
+  // into the activation ring when it is large enough
+  p.fix_smem = (int64_t)P.g.x_stages * P.g.x_bytes >= (int64_t)P.bt * kTileN * 4;
   p.wait_limit_ns = g_wait_limit_ns;
   // output [rows, n] of 16-bit values, written by 16-row x 32-column tensor stores
   CUtensorMap tmap_c;

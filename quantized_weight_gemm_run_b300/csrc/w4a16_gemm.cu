@@ -26,8 +26,11 @@
 //             TMEM and the activation tile as the shared-memory B operand,
 //             accumulating in fp32 in TMEM (two accumulator buffers).
 //   output (warps 12..15): tcgen05.ld of the accumulator, bias, rounding,
-//             stores; or an fp32 partial tile plus a fixed-order reduction by
-//             the last-arriving CTA when a tile's K range was split.
+//             stores.  A tile whose K range was split is finished by the CTA
+//             holding its first k-tiles (its last work item): the others add
+//             their fp32 partials into an accumulator in L2 and count in; the
+//             finisher adds the copied-in sum to its own partial in tensor
+//             memory.  A fixed-order variant sums per-CTA partial slots.
 //   scheduling: a persistent grid of at most one CTA per SM walks whole tiles
 //             round-robin, then splits the remaining tiles' K ranges evenly
 //             across all CTAs (stream-K), so every SM streams the same number
@@ -151,6 +154,22 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
   asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a),
                "f"(b), "f"(c), "f"(d)
                : "memory");
+}
+
+__device__ __forceinline__ void red_release_add_gpu(int* addr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* addr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+// Orders this thread's generic-proxy view of global memory before its later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* addr, int v) {
@@ -277,7 +296,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint64_t* sfb_ready = drain + 1;
-  SharedState* sh = reinterpret_cast<SharedState*>(sfb_ready + 1);
+  uint64_t* fix_bar = sfb_ready + 1;   // one per epilogue warp: split-K sum copied in
+  SharedState* sh = reinterpret_cast<SharedState*>(fix_bar + 4);
   int* mt_prefix = reinterpret_cast<int*>(sh + 1);     // grouped: m-tile prefix [E+1]
   int* offs = mt_prefix + (GROUPED ? (p.num_experts + 1) : 0);   // grouped: offsets [E+1]
 
@@ -336,6 +356,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     mbar_init(drain, 1);
     mbar_init(sfb_ready, 4);
+    for (int i = 0; i < 4; ++i) mbar_init(&fix_bar[i], 1);
     sh->abort_flag = 0;
     fence_barrier_init();
   }
@@ -694,96 +715,141 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int n = tc.nt * kTileN + col;
       const float bias = p.bias ? from_out<FP16>(p.bias[(long long)tc.e * p.n + n]) : 0.f;
       const uint32_t tbase = tmem_base + lane_addr + kAccCol + acc * BT;
-      // partial tile of this CTA for this segment (split tiles only),
-      // column-major [col][BT]: this thread's column is contiguous
+      // Split tiles.  Partial tiles are column-major [col][BT] (this thread's
+      // column contiguous), so a 32-column quadrant is one contiguous block.
       const long long tl = wi.tile - sched.W * sched.G;
       const long long u_start = tl * p.kt;
-      float* my_part = nullptr;
-      if (!whole) {
-        if (p.deterministic) {
-          const int which = (sched.sk_begin(blockIdx.x) >= u_start) ? 0 : 1;
-          my_part = p.partials + ((long long)(2 * blockIdx.x + which)) * (BT * kTileN);
-        } else {
-          my_part = p.partials + tl * (BT * kTileN);
-        }
-      }
-      // only 16-row chunks holding output rows are read: rows past the end
-      // stay untouched (zero) in the split accumulators
+      const long long c_first = whole ? 0 : sched.cta_of_unit(u_start);
+      const long long c_last = whole ? 0 : sched.cta_of_unit(u_start + p.kt - 1);
+      const int contributors = (int)(c_last - c_first + 1);
+      int* counter = &p.counters[(long long)wi.tile * 4 + q];
+      const bool finisher = !whole && !p.deterministic && c_first == (long long)blockIdx.x;
+      if (whole || (!p.deterministic && !finisher)) {
+        // whole tile: output; atomic-mode contributor: add into the tile's
+        // accumulator.  Only 16-row chunks holding output rows are read, so
+        // rows past the end stay untouched (zero) in the accumulator.
+        float* acc_col = whole ? nullptr : p.partials + tl * (BT * kTileN) + col * BT;
 #pragma unroll 1
-      for (int mc = 0; mc < BT / 16 && mc * 16 < tc.rows; ++mc) {
-        uint32_t v[16];
-        tmem_ld16_wait(tbase + mc * 16, v);
-        if (whole) {
-          float f[16];
+        for (int mc = 0; mc < BT / 16 && mc * 16 < tc.rows; ++mc) {
+          uint32_t v[16];
+          tmem_ld16_wait(tbase + mc * 16, v);
+          if (whole) {
+            float f[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
-          emit(tc, mc * 16, f, bias);
-        } else if (p.deterministic) {
+            for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+            emit(tc, mc * 16, f, bias);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              red_add_v4(acc_col + mc * 16 + 4 * i, __uint_as_float(v[4 * i]),
+                         __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                         __uint_as_float(v[4 * i + 3]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[acc]);
+          // the warp's reductions (ordered before this by the warp barrier)
+          // become visible before the count: release
+          if (!whole) red_release_add_gpu(counter, 1);
+        }
+      } else if (finisher) {
+        // Atomic-mode finisher: the CTA holding the tile's first k-tiles,
+        // which (stream-K order) is this CTA's last work item.  Its own
+        // partial stays in tensor memory; once the other contributors'
+        // counts arrive, their sum is copied in with one bulk copy per
+        // quadrant (into the activation ring, idle after the last item's
+        // MMAs) or read directly, added, written out, and the accumulator
+        // and counter are left at zero for the next launch.
+        Schedule peek = sched;
+        WorkItem nx;
+        const bool via_smem = p.fix_smem && !peek.next(nx);
+        float* quad = p.partials + tl * (BT * kTileN) + q * 32 * BT;
+        bool ok = true;
+        if (lane == 0) {
+          const uint64_t t0 = globaltimer();
+          while (ld_acquire_gpu(counter) < contributors - 1) {
+            if (*abort_flag || globaltimer() - t0 >= lim) {
+              if (!*abort_flag) {
+                *abort_flag = 1;
+                atomicOr(p.status, kStatusTimeout);
+              }
+              ok = false;
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+        __syncwarp();   // orders every lane's reads after lane 0's acquire
+        const float* sum_col = quad + lane * BT;
+        if (ok && via_smem) {
+          float* fsm = reinterpret_cast<float*>(x_base) + q * 32 * BT;
+          if (lane == 0) {
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(&fix_bar[q], BT * 128);
+            bulk_load(fsm, quad, BT * 128, &fix_bar[q], policy_evict_first());
+          }
+          __syncwarp();
+          ok = mbar_wait(&fix_bar[q], 0, abort_flag, p.status, lim, kStatusTimeout);
+          if (!ok) {   // never leave the copy writing shared memory the CTA is leaving
+            volatile int no_abort = 0;
+            mbar_wait(&fix_bar[q], 0, &no_abort, nullptr, 100000000ull, 0);
+          }
+          sum_col = fsm + lane * BT;
+        }
+        if (ok) {
+#pragma unroll 1
+          for (int mc = 0; mc < BT / 16 && mc * 16 < tc.rows; ++mc) {
+            uint32_t v[16];
+            tmem_ld16_wait(tbase + mc * 16, v);
+            const float4* s4 = reinterpret_cast<const float4*>(sum_col + mc * 16);
+            float f[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float4 a4 = via_smem ? s4[j] : __ldcg(s4 + j);
+              f[4 * j] = __uint_as_float(v[4 * j]) + a4.x;
+              f[4 * j + 1] = __uint_as_float(v[4 * j + 1]) + a4.y;
+              f[4 * j + 2] = __uint_as_float(v[4 * j + 2]) + a4.z;
+              f[4 * j + 3] = __uint_as_float(v[4 * j + 3]) + a4.w;
+            }
+            emit(tc, mc * 16, f, bias);
+          }
+          // leave the quadrant's accumulator zeroed (coalesced) and the count reset
+          float4* q4 = reinterpret_cast<float4*>(quad);
+          for (int i = lane; i < 8 * BT; i += 32) q4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (lane == 0) *counter = 0;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      } else {
+        // fixed-order mode: this CTA's partial to its own slot; the last
+        // CTA to arrive for a quadrant sums the slots in CTA order
+        const int which = (sched.sk_begin(blockIdx.x) >= u_start) ? 0 : 1;
+        float* my_part = p.partials + ((long long)(2 * blockIdx.x + which)) * (BT * kTileN);
+#pragma unroll 1
+        for (int mc = 0; mc < BT / 16 && mc * 16 < tc.rows; ++mc) {
+          uint32_t v[16];
+          tmem_ld16_wait(tbase + mc * 16, v);
           float4* dst = reinterpret_cast<float4*>(my_part + col * BT + mc * 16);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-        } else {
-          float* dst = my_part + col * BT + mc * 16;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            red_add_v4(dst + 4 * i, __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                       __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      if (++acc == 2) {
-        acc = 0;
-        accphase ^= 1;
-      }
-      if (!whole) {
-        // Split-K fixup, per 32-column quadrant, by the warp of the last CTA
-        // to arrive for this quadrant of the tile.  The warp's partial stores
-        // (or reductions) are ordered before lane 0's release add; the
-        // acquiring add of the last arrival orders the reads after it.
-        const long long c_first = sched.cta_of_unit(u_start);
-        const long long c_last = sched.cta_of_unit(u_start + p.kt - 1);
-        const int contributors = (int)(c_last - c_first + 1);
-        int* counter = &p.counters[(long long)wi.tile * 4 + q];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        // the warp's partial stores are ordered before lane 0's release add;
+        // the acquiring add of the last arrival orders the reads after it
         __syncwarp();
         int old = 0;
         if (lane == 0) old = atomic_add_acq_rel_gpu(counter, 1);
         old = __shfl_sync(0xffffffffu, old, 0);
-        __syncwarp();   // orders every lane's reads after lane 0's acquire
-        if (old == contributors - 1 && !p.deterministic) {
-          // atomic mode: the accumulator holds the sum; read it 16 rows at a
-          // time with two chunks' loads in flight (each L2 round trip
-          // is long while other CTAs' reductions drain), write the output,
-          // and leave the accumulator zeroed for the next launch
-          float4* acc4 = reinterpret_cast<float4*>(my_part + col * BT);
-          const int nch = (tc.rows + 15) / 16;
-          float4 cur[4], nxt[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) cur[j] = __ldcg(acc4 + j);
-#pragma unroll 1
-          for (int c = 0; c < nch; ++c) {
-            if (c + 1 < nch)
-#pragma unroll
-              for (int j = 0; j < 4; ++j) nxt[j] = __ldcg(acc4 + (c + 1) * 4 + j);
-            float f[16];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              f[4 * j] = cur[j].x;
-              f[4 * j + 1] = cur[j].y;
-              f[4 * j + 2] = cur[j].z;
-              f[4 * j + 3] = cur[j].w;
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc4[c * 4 + j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            emit(tc, c * 16, f, bias);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
-          }
-          if (lane == 0) *counter = 0;   // ready for the next launch
-        } else if (old == contributors - 1) {
+        __syncwarp();
+        if (old == contributors - 1) {
           // fixed-order mode: the contributors' partials summed in CTA order,
           // two contributors' loads in flight at a time
           for (int m0 = 0; m0 < tc.rows; m0 += 16) {
@@ -820,6 +886,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           if (lane == 0) *counter = 0;   // ready for the next launch
         }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        accphase ^= 1;
       }
     }
     if (lane == 0) bulk_wait_group_all();   // tensor stores done before the CTA exits
