@@ -34,6 +34,25 @@ struct WorkspaceLayout {
 
 WorkspaceLayout workspace_layout(int64_t max_tiles, int grid, int block_tok);
 
+// Division by a run-time invariant divisor d >= 1 with one multiply-high, an
+// add and a shift (Granlund and Montgomery, "Division by invariant integers
+// using multiplication", PLDI 1994): with s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1, n / d = (umulhi(n, m) + n) >> s for
+// every 0 <= n < 2^31 (the sum then stays below 2^32).
+struct FastDiv {
+  uint32_t d, mul, shift;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  uint32_t s = 0;
+  while (s < 32 && (uint64_t(1) << s) < d) ++s;
+  f.shift = s;
+  f.mul = (uint32_t)(((uint64_t(1) << 32) * ((uint64_t(1) << s) - d)) / d + 1);
+  return f;
+}
+
 struct W4A16Params {
   const uint8_t* w;          // packed blocks of all experts: [weights][scales][zeros]
   const uint16_t* bias;      // [E, N] or null
@@ -61,6 +80,10 @@ struct W4A16Params {
   int off_w, off_epi, off_bar;   // shared-memory offsets of the weight ring, staging, barriers
   int w_reuse;               // 1: several token tiles read each weight block (keep it in L2)
   int fix_smem;              // 1: the activation ring can hold a split tile's fp32 sum
+  // dense schedule, computed on the host: tiles, whole waves, stream-K units,
+  // CTAs sharing them, and dividers for the schedule's invariant divisors
+  int sk_t, sk_w, sk_u, sk_gs;
+  FastDiv div_kt, div_nt, div_gs, div_u;
   int smem_bytes;            // total dynamic shared memory
   unsigned long long wait_limit_ns;
 };

@@ -242,6 +242,9 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
     tiles_bound = ((rows + bt - 1) / bt) * nt;
   if (tiles_bound >= (int64_t(1) << 31))
     return fail(QGEMM_ERR_UNSUPPORTED, "problem has more than 2^31 output tiles");
+  // the device schedule works in 32-bit: stream-K units times CTAs < 2^31
+  if (kt * (int64_t)sms * sms >= (int64_t(1) << 31))
+    return fail(QGEMM_ERR_UNSUPPORTED, "k = %lld is too large for one GEMM", (long long)L->k);
   int grid = sms;
   if (T && T->max_ctas > 0 && T->max_ctas < grid) grid = T->max_ctas;
   if (!grouped) {
@@ -399,6 +402,22 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   // several token tiles per weight block: keep weights in L2 rather than
   // marking them first to evict
   p.w_reuse = grouped ? (rows > (int64_t)E * P.bt) : (rows > P.bt);
+  // the dense schedule's constants and divisors (the device re-derives the
+  // grouped one from the expert offsets)
+  {
+    const int64_t T = grouped ? 0 : ((rows + P.bt - 1) / P.bt) * (L->n / kTileN);
+    const int64_t G = P.grid;
+    const int64_t W = T / G;
+    const int64_t U = (T - W * G) * p.kt;
+    p.sk_t = (int)T;
+    p.sk_w = (int)W;
+    p.sk_u = (int)U;
+    p.sk_gs = (int)(U < G ? U : G);
+    p.div_kt = make_fastdiv((uint32_t)p.kt);
+    p.div_nt = make_fastdiv((uint32_t)p.nt);
+    p.div_gs = make_fastdiv(p.sk_gs > 0 ? (uint32_t)p.sk_gs : 1u);
+    p.div_u = make_fastdiv(p.sk_u > 0 ? (uint32_t)p.sk_u : 1u);
+  }
   // a split tile's finisher copies the other contributors' fp32 sum (BT x 128)
   // into the activation ring when it is large enough
   p.fix_smem = (int64_t)P.g.x_stages * P.g.x_bytes >= (int64_t)P.bt * kTileN * 4;

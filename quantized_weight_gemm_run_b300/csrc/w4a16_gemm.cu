@@ -56,27 +56,57 @@ struct WorkItem {
   int k0, k1;
 };
 
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+  return (int)((__umulhi((unsigned)n, f.mul) + (unsigned)n) >> f.shift);
+}
+
 // Whole tiles round-robin (waves), then an even split of the remaining tiles'
 // K-tiles ("units") across the first Gs = min(G, U) CTAs, so that every CTA
 // taking part in the split owns at least one unit; the CTAs that share a tile
-// are then exactly cta_of_unit(first unit) .. cta_of_unit(last unit).
+// are then exactly cta_of_unit(first unit) .. cta_of_unit(last unit).  All
+// arithmetic is 32-bit (the host bounds U * G below 2^31), and a dense GEMM's
+// schedule constants and divisors come from the host: integer division is a
+// long instruction sequence on the critical path of a kernel's start.
 struct Schedule {
-  long long T;     // tiles
+  int T;           // tiles
   int KT;          // k-tiles per tile
   int G, c;        // grid size, this CTA
-  long long W;     // full waves of whole tiles
-  long long U;     // stream-K units
-  long long Gs;    // CTAs sharing the stream-K units
-  long long it, u, u_end;
+  int W;           // full waves of whole tiles
+  int U;           // stream-K units
+  int Gs;          // CTAs sharing the stream-K units
+  int it, u, u_end;
+  bool fast;       // host-made dividers for Gs and U
+  FastDiv dkt, dgs, du;
 
-  __device__ void init(long long T_, int KT_, int G_, int c_) {
-    T = T_;
-    KT = KT_;
-    G = G_;
+  // dense: everything from the host
+  __device__ void init_dense(const W4A16Params& p, int c_) {
+    T = p.sk_t;
+    KT = p.kt;
+    G = gridDim.x;
+    c = c_;
+    W = p.sk_w;
+    U = p.sk_u;
+    Gs = p.sk_gs;
+    fast = true;
+    dkt = p.div_kt;
+    dgs = p.div_gs;
+    du = p.div_u;
+    start();
+  }
+  // grouped: the tile count is known only on the device
+  __device__ void init(long long T_, const W4A16Params& p, int c_) {
+    T = (int)T_;
+    KT = p.kt;
+    G = gridDim.x;
     c = c_;
     W = T / G;
     U = (T - W * G) * KT;
     Gs = U < G ? U : G;
+    fast = false;
+    dkt = p.div_kt;
+    start();
+  }
+  __device__ void start() {
     it = 0;
     if (c < Gs) {
       u = sk_begin(c);
@@ -85,25 +115,30 @@ struct Schedule {
       u = u_end = 0;
     }
   }
-  __device__ long long sk_begin(long long cta) const { return (cta * U) / Gs; }
+  __device__ int sk_begin(int cta) const {
+    return fast ? fdiv(cta * U, dgs) : (int)((unsigned)(cta * U) / (unsigned)Gs);
+  }
   // CTA whose unit range holds unit uu.
-  __device__ long long cta_of_unit(long long uu) const { return ((uu + 1) * Gs - 1) / U; }
+  __device__ int cta_of_unit(int uu) const {
+    const int x = (uu + 1) * Gs - 1;
+    return fast ? fdiv(x, du) : (int)((unsigned)x / (unsigned)U);
+  }
 
   __device__ bool next(WorkItem& wi) {
     if (it < W) {
-      wi.tile = (int)(c + it * G);
+      wi.tile = c + it * G;
       wi.k0 = 0;
       wi.k1 = KT;
       ++it;
       return true;
     }
     if (u >= u_end) return false;
-    long long tl = u / KT;
-    int k0 = (int)(u % KT);
-    long long seg_end = min((tl + 1) * KT, u_end);
-    wi.tile = (int)(W * G + tl);
+    const int tl = fdiv(u, dkt);
+    const int k0 = u - tl * KT;
+    const int seg_end = min((tl + 1) * KT, u_end);
+    wi.tile = W * G + tl;
     wi.k0 = k0;
-    wi.k1 = k0 + (int)(seg_end - u);
+    wi.k1 = k0 + (seg_end - u);
     u = seg_end;
     return true;
   }
@@ -309,7 +344,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   auto coords = [&](int tile) {
     TileCoord<BT> tc;
-    const int mtg = tile / p.nt;
+    const int mtg = fdiv(tile, p.div_nt);
     tc.nt = tile - mtg * p.nt;
     if constexpr (GROUPED) {
       int lo = 0, hi = p.num_experts;   // find e: mt_prefix[e] <= mtg < mt_prefix[e+1]
@@ -329,35 +364,30 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   };
   // waits for every copy a producer issued into its ring to land, so that no
   // copy is still writing shared memory when the CTA exits
-  auto drain_ring = [&](uint64_t* full, int S, long long issued) {
+  auto drain_ring = [&](uint64_t* full, int S, int issued) {
     for (int st = 0; st < S && st < issued; ++st) {
-      const long long last = st + ((issued - 1 - st) / S) * S;
+      const int last = st + ((issued - 1 - st) / S) * S;
       volatile int no_abort = 0;
       mbar_wait(&full[st], (uint32_t)((last / S) & 1), &no_abort, nullptr, 100000000ull, 0);
     }
   };
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < SX; ++i) {
-      mbar_init(&x_full[i], 1);
-      mbar_init(&x_empty[i], 1);
+  if (warp == 0) {
+    // barrier initialization spread over the warp's lanes: lane i sets up
+    // barrier i of the contiguous array (arrival counts by the array it is in)
+    const int nb = 2 * SX + 2 * SW + 2 * kASlots + 4 + 2 + 4;
+    for (int i = lane; i < nb; i += 32) {
+      uint32_t count = 1;
+      int j = i - 2 * SX;
+      if (j >= SW && j < 2 * SW) count = 8;                 // w_empty: every dequant warp
+      j -= 2 * SW;
+      if (j >= 0 && j < kASlots) count = 4;                 // a_full: one per lane quadrant
+      j -= 2 * kASlots;
+      if (j == 2 || j == 3) count = 4;                      // acc_empty
+      if (j == 5) count = 4;                                // sfb_ready
+      mbar_init(&bars[i], count);
     }
-    for (int i = 0; i < SW; ++i) {
-      mbar_init(&w_full[i], 1);
-      mbar_init(&w_empty[i], 8);   // every dequant warp hands the slot back once
-    }
-    for (int i = 0; i < kASlots; ++i) {
-      mbar_init(&a_full[i], 4);
-      mbar_init(&a_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
-    }
-    mbar_init(drain, 1);
-    mbar_init(sfb_ready, 4);
-    for (int i = 0; i < 4; ++i) mbar_init(&fix_bar[i], 1);
-    sh->abort_flag = 0;
+    if (lane == 0) sh->abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 2) {
@@ -411,7 +441,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                           : sh->tiles;
 
   Schedule sched;
-  sched.init(T, p.kt, gridDim.x, blockIdx.x);
+  if constexpr (GROUPED)
+    sched.init(T, p, blockIdx.x);
+  else
+    sched.init_dense(p, blockIdx.x);
   // Programmatic dependent launch: the next grid on the stream may start its
   // CTAs as soon as SMs free up; everything it reads from this grid is read
   // after its own grid_dependency_wait.
@@ -423,7 +456,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // regardless of) the wait for the previous grid on the stream.
     if (lane == 0) {
       const uint64_t pol = p.w_reuse ? policy_evict_normal() : policy_evict_first();
-      long long issued = 0;
+      int issued = 0;
       int ws = 0;
       uint32_t wph = 0;
       WorkItem wi;
@@ -457,7 +490,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       prefetch_tmap(&tmap_a);
       const uint64_t pol = policy_evict_last();
       grid_dependency_wait();   // the previous grid may still write the activations
-      long long issued = 0;
+      int issued = 0;
       int xs = 0;
       uint32_t xph = 0;
       WorkItem wi;
@@ -717,18 +750,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const uint32_t tbase = tmem_base + lane_addr + kAccCol + acc * BT;
       // Split tiles.  Partial tiles are column-major [col][BT] (this thread's
       // column contiguous), so a 32-column quadrant is one contiguous block.
-      const long long tl = wi.tile - sched.W * sched.G;
-      const long long u_start = tl * p.kt;
-      const long long c_first = whole ? 0 : sched.cta_of_unit(u_start);
-      const long long c_last = whole ? 0 : sched.cta_of_unit(u_start + p.kt - 1);
+      const int tl = wi.tile - sched.W * sched.G;
+      const int u_start = tl * p.kt;
+      const int c_first = whole ? 0 : sched.cta_of_unit(u_start);
+      const int c_last = whole ? 0 : sched.cta_of_unit(u_start + p.kt - 1);
       const int contributors = (int)(c_last - c_first + 1);
       int* counter = &p.counters[(long long)wi.tile * 4 + q];
-      const bool finisher = !whole && !p.deterministic && c_first == (long long)blockIdx.x;
+      const bool finisher = !whole && !p.deterministic && c_first == (int)blockIdx.x;
       if (whole || (!p.deterministic && !finisher)) {
         // whole tile: output; atomic-mode contributor: add into the tile's
         // accumulator.  Only 16-row chunks holding output rows are read, so
         // rows past the end stay untouched (zero) in the accumulator.
-        float* acc_col = whole ? nullptr : p.partials + tl * (BT * kTileN) + col * BT;
+        float* acc_col = whole ? nullptr : p.partials + (long long)tl * (BT * kTileN) + col * BT;
 #pragma unroll 1
         for (int mc = 0; mc < BT / 16 && mc * 16 < tc.rows; ++mc) {
           uint32_t v[16];
@@ -765,7 +798,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         Schedule peek = sched;
         WorkItem nx;
         const bool via_smem = p.fix_smem && !peek.next(nx);
-        float* quad = p.partials + tl * (BT * kTileN) + q * 32 * BT;
+        float* quad = p.partials + (long long)tl * (BT * kTileN) + q * 32 * BT;
         bool ok = true;
         if (lane == 0) {
           const uint64_t t0 = globaltimer();
@@ -856,11 +889,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             float f[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) f[i] = 0.f;
-            for (long long cc0 = c_first; cc0 <= c_last; cc0 += 2) {
+            for (int cc0 = c_first; cc0 <= c_last; cc0 += 2) {
               float4 v4[2][4];
 #pragma unroll
               for (int i = 0; i < 2; ++i) {
-                const long long cc = cc0 + i;
+                const int cc = cc0 + i;
                 if (cc <= c_last) {
                   const int which = (sched.sk_begin(cc) >= u_start) ? 0 : 1;
                   const float4* src4 = reinterpret_cast<const float4*>(

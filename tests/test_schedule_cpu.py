@@ -55,3 +55,34 @@ def test_schedule_partition(T, KT, G):
         owners = {owner[(t, k)] for k in range(KT)}
         if len(owners) > 1:
             assert owners == set(range(cta_of_unit(us), cta_of_unit(us + KT - 1) + 1))
+
+
+def _fastdiv(d):
+    """Divider constants for division by an invariant d (Granlund and
+    Montgomery 1994): s = ceil(log2 d), m = floor(2^32 (2^s - d) / d) + 1."""
+    s = 0
+    while (1 << s) < d:
+        s += 1
+    return ((1 << 32) * ((1 << s) - d)) // d + 1, s
+
+
+def test_fastdiv_constants_fit_and_divide_exactly():
+    """The multiply-high division the kernel's schedule uses equals integer
+    division for every dividend below 2^31 (checked at the edges, at
+    multiples of the divisor and on random dividends)."""
+    import random
+    rnd = random.Random(5)
+    divisors = list(range(1, 300)) + [2 ** k for k in range(1, 31)] + \
+        [2 ** k + 1 for k in range(1, 30)] + [2 ** k - 1 for k in range(2, 31)] + \
+        [rnd.randrange(1, 2 ** 31) for _ in range(200)]
+    for d in divisors:
+        m, s = _fastdiv(d)
+        assert 0 <= m < 2 ** 32
+        ns = {0, 1, d - 1, d, d + 1, 2 ** 31 - 1, 2 ** 31 - 2}
+        ns |= {q * d + r for q in (1, 2, 7, (2 ** 31 - 1) // d) for r in (0, d - 1) if q * d + r < 2 ** 31}
+        ns |= {rnd.randrange(0, 2 ** 31) for _ in range(50)}
+        for n in ns:
+            if 0 <= n < 2 ** 31:
+                hi = (n * m) >> 32
+                assert hi + n < 2 ** 32
+                assert (hi + n) >> s == n // d, (d, n)
