@@ -591,17 +591,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------ dequant
     // Two warps per TMEM lane quadrant; warp group h takes every other unit
-    // (h = unit index & 1) and dequantizes all 128 k of its 32 rows.  Each
-    // warp hands a weight slot back once per use, right after its last read
-    // of it (at once when the slot holds none of its group's units).
+    // (h = unit index & 1) and dequantizes all 128 k of its 32 rows.  A warp
+    // reads all of its group's units in a weight slot (at most two) into
+    // registers as soon as the slot is full and hands the slot back at once;
+    // the second unit's shared-memory reads are then off its critical path.
     const int q = warp & 3;             // TMEM lane quadrant
     const int h = (warp - 4) >> 2;      // which units: even (0) or odd (1)
     const int row = q * 32 + lane;      // output feature within the tile
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     constexpr uint32_t magic16 = FP16 ? 0x6400u : 0x4300u;
-    int ws = 0, slot = 0;
-    uint32_t wph = 0, aphase = 0;
-    long long unit = 0;
+    int ws = 0;
+    uint32_t wph = 0;
+    int unit = 0;                       // units of this CTA before the current slot
     WorkItem wi;
     bool ok = true;
     while (ok && sched.next(wi)) {
@@ -611,72 +612,73 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           ok = false;
           break;
         }
-        int i_last = r - 1;                       // this group's last unit in the slot
-        if ((int)((unit + i_last) & 1) != h) --i_last;
-        if (i_last < 0) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&w_empty[ws]);
-        }
         const uint8_t* sp = w_base + ws * p.w_bytes;
-        for (int i = 0; i < r; ++i) {
-          if ((int)((unit + i) & 1) == h) {
+        const int i0 = ((unit & 1) == h) ? 0 : 1;   // this group's units: i0, i0 + 2
+        uint4 v[2][4];
+        uint32_t scale2[2][4], zero2[2][4], sf[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int i = i0 + 2 * t;
+          if (i < r) {
             const uint8_t* bp = sp + i * blk_bytes;   // this unit's packed block
             const uint4* wv = reinterpret_cast<const uint4*>(bp);
-            uint4 v[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = wv[(q * 4 + j) * 32 + lane];
-            uint32_t scale2[4], zero2[4], sf = 0;
+            for (int j = 0; j < 4; ++j) v[t][j] = wv[(q * 4 + j) * 32 + lane];
             if constexpr (MX) {
-              sf = reinterpret_cast<const uint32_t*>(bp + p.s_off)[row];
+              sf[t] = reinterpret_cast<const uint32_t*>(bp + p.s_off)[row];
             } else {
               const uint16_t* sv = reinterpret_cast<const uint16_t*>(bp + p.s_off);
               const uint8_t* zv = bp + p.z_off;
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 const int sg = j >> p.sg_shift;
-                scale2[j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
+                scale2[t][j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
                 const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
-                zero2[j] = (magic16 + zq) * 0x00010001u;
+                zero2[t][j] = (magic16 + zq) * 0x00010001u;
               }
             }
-            if (i == i_last) {   // every read of the slot by this warp is done
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&w_empty[ws]);
-            }
-            if (!mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
-                           kStatusTimeout)) {
-              ok = false;
-              break;
-            }
-            if constexpr (MX) {
-              // 128 e2m1 codes of this row -> 128 e4m3 bytes (32 columns), and
-              // its four e8m0 block scales -> the slot's four scale columns
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t o8[8];
-                dequant_vec_mx(v[j], o8);
-                tmem_st8(tmem_base + lane_addr + slot * kSlotCols + j * 8, o8);
-              }
-              const uint32_t sf4[4] = {sf, sf, sf, sf};
-              tmem_st4(tmem_base + lane_addr + kSfaCol + slot * 4, sf4);
-            } else {
-              const uint32_t tbase = tmem_base + lane_addr + slot * kSlotCols;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t out[16];
-                dequant_vec<FP16>(v[j], zero2[j], scale2[j], out);
-                tmem_st16(tbase + j * 16, out);
-              }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[slot]);
           }
-          if (++slot == kASlots) {
-            slot = 0;
-            aphase ^= 1;
+        }
+        // every read of the slot by this warp is done (or it holds none of
+        // the group's units)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&w_empty[ws]);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int i = i0 + 2 * t;
+          if (i >= r) break;
+          const int g = unit + i;                    // unit index within the CTA
+          const int slot = g & (kASlots - 1);
+          const uint32_t aphase = (uint32_t)(g / kASlots) & 1u;
+          if (!mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
+                         kStatusTimeout)) {
+            ok = false;
+            break;
           }
+          if constexpr (MX) {
+            // 128 e2m1 codes of this row -> 128 e4m3 bytes (32 columns), and
+            // its four e8m0 block scales -> the slot's four scale columns
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t o8[8];
+              dequant_vec_mx(v[t][j], o8);
+              tmem_st8(tmem_base + lane_addr + slot * kSlotCols + j * 8, o8);
+            }
+            const uint32_t sf4[4] = {sf[t], sf[t], sf[t], sf[t]};
+            tmem_st4(tmem_base + lane_addr + kSfaCol + slot * 4, sf4);
+          } else {
+            const uint32_t tbase = tmem_base + lane_addr + slot * kSlotCols;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t out[16];
+              dequant_vec<FP16>(v[t][j], zero2[t][j], scale2[t][j], out);
+              tmem_st16(tbase + j * 16, out);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[slot]);
         }
         unit += r;
         if (++ws == SW) {
