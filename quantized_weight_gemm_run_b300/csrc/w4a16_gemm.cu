@@ -372,11 +372,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
   };
 
+  // Dense GEMMs: the first weight slot goes out before anything else, from
+  // the host-made schedule, so that the weight stream starts within a few
+  // hundred instructions of the launch.
+  bool first_issued = false;
+  if (!GROUPED && threadIdx.x == 0) {
+    mbar_init(&w_full[0], 1);
+    mbar_init(&w_empty[0], 8);
+    fence_barrier_init();
+    Schedule s0;
+    s0.init_dense(p, blockIdx.x);
+    WorkItem w0;
+    if (s0.next(w0)) {
+      const int nt0 = w0.tile - fdiv(w0.tile, p.div_nt) * p.nt;
+      const int r = min(RW, w0.k1 - w0.k0);
+      mbar_arrive_expect_tx(&w_full[0], r * blk_bytes);
+      bulk_load(w_base, p.w + ((long long)nt0 * p.kt + w0.k0) * blk_bytes, r * blk_bytes,
+                &w_full[0], p.w_reuse ? policy_evict_normal() : policy_evict_first());
+      first_issued = true;
+    }
+  }
   if (warp == 0) {
     // barrier initialization spread over the warp's lanes: lane i sets up
-    // barrier i of the contiguous array (arrival counts by the array it is in)
+    // barrier i of the contiguous array (arrival counts by the array it is in);
+    // a dense GEMM's first weight slot barriers are set up already
     const int nb = 2 * SX + 2 * SW + 2 * kASlots + 4 + 2 + 4;
     for (int i = lane; i < nb; i += 32) {
+      if (!GROUPED && (i == 2 * SX || i == 2 * SX + SW)) continue;
       uint32_t count = 1;
       int j = i - 2 * SX;
       if (j >= SW && j < 2 * SW) count = 8;                 // w_empty: every dequant warp
@@ -457,6 +479,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (lane == 0) {
       const uint64_t pol = p.w_reuse ? policy_evict_normal() : policy_evict_first();
       int issued = 0;
+      bool skip_first = first_issued;
       int ws = 0;
       uint32_t wph = 0;
       WorkItem wi;
@@ -472,9 +495,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&w_full[ws], r * blk_bytes);
-          bulk_load(w_base + ws * p.w_bytes, src + (long long)(kt - wi.k0) * blk_bytes,
-                    r * blk_bytes, &w_full[ws], pol);
+          if (skip_first) {
+            skip_first = false;   // went out at the start of the kernel
+          } else {
+            mbar_arrive_expect_tx(&w_full[ws], r * blk_bytes);
+            bulk_load(w_base + ws * p.w_bytes, src + (long long)(kt - wi.k0) * blk_bytes,
+                      r * blk_bytes, &w_full[ws], pol);
+          }
           ++issued;
           if (++ws == SW) {
             ws = 0;
