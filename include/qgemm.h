@@ -275,7 +275,9 @@ qgemm_status qgemm_quantize_act_fp8(const void* x, int64_t m, int64_t k, void* a
  *               their (token, slot) order
  *   inv_perm    device int32 [t*topk] (output): inv_perm[token*topk + j] = r
  *   a           device [t, hidden] activations (2-byte elements)
- *   a_perm      device [t*topk, hidden] (output): a_perm[r] = a[perm[r] / topk]
+ *   a_perm      device [t*topk, hidden] (output): a_perm[r] = a[perm[r] / topk];
+ *               it also holds the sort's per-block histograms until the
+ *               gather overwrites it, so it must not overlap a or the ids
  */
 qgemm_status qgemm_moe_permute(const int32_t* topk_ids, int64_t t, int32_t topk, int32_t e,
                                int32_t* offsets, int32_t* perm, int32_t* inv_perm,

@@ -55,73 +55,115 @@ cudaError_t launch_act_quant_fp8(const uint16_t* x, int64_t m, int64_t k, uint8_
 }
 
 // ----------------------------------------------------------- MoE permute
-// Stable counting sort of the slots s = token*topk + j by expert id in one
-// CTA of 1024 threads: a histogram, an exclusive scan (the expert offsets),
-// then the slots in chunks of 1024 in slot order, each placed at
-// base[e] + (number of earlier slots of expert e), found with a warp match
-// and a scan of per-warp counts.  Ids outside [0, E) go to an extra bucket
-// after the last expert, so perm is always a full permutation of the slots.
-__global__ void __launch_bounds__(1024) moe_sort_kernel(const int32_t* __restrict__ ids,
-                                                        int n_slots, int E,
-                                                        int32_t* __restrict__ offsets,
-                                                        int32_t* __restrict__ perm,
-                                                        int32_t* __restrict__ inv_perm) {
+// Stable counting sort of the slots s = token*topk + j by expert id.  Ids
+// outside [0, E) go to an extra bucket after the last expert, so perm is
+// always a full permutation of the slots.
+//
+// The slots are cut into blocks of kSortBlock, one CTA (32 warps) each, and
+// each block into 32 contiguous warp segments.  A slot's place is
+//   (slots of lower experts) + (slots of its expert in earlier blocks)
+//   + (... in earlier segments of its block) + (... earlier in its segment),
+// the first three from per-block and per-warp histograms (order-free shared
+// memory atomics), the last from a warp match over 32 consecutive slots.
+// One block: a single kernel; more: a histogram kernel per block, then the
+// placement kernel, which sums the blocks' histograms itself.
+constexpr int kSortBlock = 2048;
+
+__device__ __forceinline__ int sort_bucket(const int32_t* ids, int i, int E) {
+  const int v = ids[i];
+  return (v >= 0 && v < E) ? v : E;
+}
+
+// Per-block histograms: hist[blockIdx.x][e], e in [0, E].
+__global__ void __launch_bounds__(1024) moe_count_kernel(const int32_t* __restrict__ ids,
+                                                         int n_slots, int E,
+                                                         int32_t* __restrict__ hist) {
   constexpr int NB = kMaxPermuteExperts + 1;
-  __shared__ int base[NB];
-  __shared__ int chunk_total[NB];
-  __shared__ int warp_cnt[32][NB];
+  __shared__ int h[NB];
+  const int B = E + 1;
+  for (int x = threadIdx.x; x < B; x += blockDim.x) h[x] = 0;
+  __syncthreads();
+  const int lo = blockIdx.x * kSortBlock, hi = min(lo + kSortBlock, n_slots);
+  for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) atomicAdd(&h[sort_bucket(ids, i, E)], 1);
+  __syncthreads();
+  for (int x = threadIdx.x; x < B; x += blockDim.x) hist[blockIdx.x * B + x] = h[x];
+}
+
+// Places the slots of block blockIdx.x.  hist: the per-block histograms of
+// all nblocks blocks, or NULL when there is one block (counted here).
+__global__ void __launch_bounds__(1024) moe_place_kernel(const int32_t* __restrict__ ids,
+                                                         int n_slots, int E, int nblocks,
+                                                         const int32_t* __restrict__ hist,
+                                                         int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ perm,
+                                                         int32_t* __restrict__ inv_perm) {
+  constexpr int NB = kMaxPermuteExperts + 1;
+  __shared__ int cnt[32][NB];   // per-warp counts, then per-warp running bases
+  __shared__ int start[NB];     // this block's first place per bucket
+  __shared__ int tot[NB];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int B = E + 1;   // buckets: the experts and the invalid-id bucket
-  for (int e = tid; e < B; e += blockDim.x) {
-    base[e] = 0;
-    for (int w = 0; w < 32; ++w) warp_cnt[w][e] = 0;
+  const int B = E + 1;
+  const int blo = blockIdx.x * kSortBlock, bhi = min(blo + kSortBlock, n_slots);
+  for (int x = tid; x < 32 * NB; x += blockDim.x) (&cnt[0][0])[x] = 0;
+  __syncthreads();
+  const int seg = (bhi - blo + 31) / 32;
+  const int lo = min(blo + warp * seg, bhi), hi = min(lo + seg, bhi);
+  for (int i = lo + lane; i < hi; i += 32) atomicAdd(&cnt[warp][sort_bucket(ids, i, E)], 1);
+  __syncthreads();
+  // per bucket: exclusive scan over this block's warps; the block's own
+  // total, and the slots of the bucket in earlier blocks
+  for (int x = tid; x < B; x += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int c = cnt[w][x];
+      cnt[w][x] = run;
+      run += c;
+    }
+    int before = 0, all = run;
+    if (hist) {
+      all = 0;
+      for (int b = 0; b < nblocks; ++b) {
+        const int c = hist[b * B + x];
+        if (b < (int)blockIdx.x) before += c;
+        all += c;
+      }
+    }
+    tot[x] = all;
+    start[x] = before;
   }
   __syncthreads();
-  auto bucket = [&](int i) {
-    const int v = ids[i];
-    return (v >= 0 && v < E) ? v : E;
-  };
-  for (int i = tid; i < n_slots; i += blockDim.x) atomicAdd(&base[bucket(i)], 1);
-  __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int e = 0; e < B; ++e) {
-      const int c = base[e];
-      if (e <= E) offsets[e] = run;
-      base[e] = run;
-      run += c;
+  if (warp == 0) {   // exclusive scan of the bucket totals: the expert offsets
+    int carry = 0;
+    for (int x0 = 0; x0 < B; x0 += 32) {
+      const int x = x0 + lane;
+      const int v = x < B ? tot[x] : 0;
+      int incl = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += t;
+      }
+      if (x < B) {
+        start[x] += carry + incl - v;
+        if (blockIdx.x == 0 && x <= E) offsets[x] = carry + incl - v;
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
   __syncthreads();
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
-    const int i = c0 + tid;
-    const int e = i < n_slots ? bucket(i) : -1;
+  for (int i0 = lo; i0 < hi; i0 += 32) {
+    const int i = i0 + lane;
+    const int e = i < hi ? sort_bucket(ids, i, E) : -1;
     const unsigned same = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(same & lt_mask);
-    if (e >= 0 && rank == 0) warp_cnt[warp][e] = __popc(same);
-    __syncthreads();
-    for (int x = tid; x < B; x += blockDim.x) {
-      int run = 0;
-      for (int w = 0; w < 32; ++w) {
-        const int t = warp_cnt[w][x];
-        warp_cnt[w][x] = run;
-        run += t;
-      }
-      chunk_total[x] = run;
-    }
-    __syncthreads();
     if (e >= 0) {
-      const int pos = base[e] + warp_cnt[warp][e] + rank;
+      const int pos = start[e] + cnt[warp][e] + __popc(same & lt_mask);
       perm[pos] = i;
       inv_perm[i] = pos;
     }
-    __syncthreads();
-    for (int x = tid; x < B; x += blockDim.x) {
-      base[x] += chunk_total[x];
-      for (int w = 0; w < 32; ++w) warp_cnt[w][x] = 0;
-    }
-    __syncthreads();
+    __syncwarp();
+    if (e >= 0 && (same & lt_mask) == 0) cnt[warp][e] += __popc(same);
+    __syncwarp();
   }
 }
 
@@ -141,8 +183,22 @@ cudaError_t launch_moe_permute(const int32_t* ids, int64_t t, int topk, int e, i
                                int32_t* perm, int32_t* inv_perm, const uint16_t* a,
                                uint16_t* a_perm, int64_t hidden, cudaStream_t stream) {
   const int n_slots = (int)(t * topk);
-  moe_sort_kernel<<<1, 1024, 0, stream>>>(ids, n_slots, e, offsets, perm, inv_perm);
-  cudaError_t err = cudaGetLastError();
+  const int nblocks = (n_slots + kSortBlock - 1) / kSortBlock;
+  cudaError_t err;
+  if (nblocks <= 1) {
+    moe_place_kernel<<<1, 1024, 0, stream>>>(ids, n_slots, e, 1, nullptr, offsets, perm,
+                                             inv_perm);
+  } else {
+    // the per-block histograms (nblocks x (E + 1) ints, far smaller than the
+    // gathered rows) live in a_perm, which the gather overwrites afterwards
+    int32_t* hist = reinterpret_cast<int32_t*>(a_perm);
+    moe_count_kernel<<<nblocks, 1024, 0, stream>>>(ids, n_slots, e, hist);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    moe_place_kernel<<<nblocks, 1024, 0, stream>>>(ids, n_slots, e, nblocks, hist, offsets, perm,
+                                                   inv_perm);
+  }
+  err = cudaGetLastError();
   if (err != cudaSuccess || n_slots == 0) return err;
   const int vecs = (int)(hidden * 2 / 16);
   gather_rows_kernel<<<(n_slots + 7) / 8, 256, 0, stream>>>(
@@ -195,16 +251,33 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y2, const int32_t* _
   const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
   if (c >= hidden) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < topk; ++j) {
-    const float wj = w[(long long)t * topk + j];
-    const int r = inv_perm[(long long)t * topk + j];
-    const uint4 v = *reinterpret_cast<const uint4*>(y2 + (long long)r * hidden + c);
-    const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+  // eight slots at a time: every load of a batch is issued before the first
+  // use, and the products are added in slot order
+  for (int j0 = 0; j0 < topk; j0 += 8) {
+    float wj[8];
+    int r[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(v2[i]);
-      acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
-      acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
+    for (int j = 0; j < 8; ++j) {
+      if (j0 + j < topk) {
+        wj[j] = w[(long long)t * topk + j0 + j];
+        r[j] = inv_perm[(long long)t * topk + j0 + j];
+      }
+    }
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j0 + j < topk) v[j] = *reinterpret_cast<const uint4*>(y2 + (long long)r[j] * hidden + c);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j0 + j < topk) {
+        const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(v2[i]);
+          acc[2 * i] = fmaf(wj[j], f.x, acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wj[j], f.y, acc[2 * i + 1]);
+        }
+      }
     }
   }
   uint4 ov;

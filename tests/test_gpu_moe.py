@@ -49,7 +49,8 @@ def _permute(Q, ids, e, a):
     return offs.cpu().numpy(), perm.cpu().numpy(), inv.cpu().numpy(), a_perm
 
 
-@pytest.mark.parametrize("t,topk,e", [(37, 3, 6), (1, 8, 64), (4096, 8, 64), (3000, 2, 256)])
+@pytest.mark.parametrize("t,topk,e", [(37, 3, 6), (1, 8, 64), (4096, 8, 64), (3000, 2, 256),
+                                      (2048, 8, 4)])
 def test_permute_bit_exact(Q, t, topk, e):
     g = np.random.default_rng(t + e)
     ids = g.integers(0, max(1, e - 1), (t, topk)).astype(np.int32)   # the last expert gets none
