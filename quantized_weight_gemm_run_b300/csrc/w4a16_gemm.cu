@@ -419,22 +419,42 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   if (warp == 3) {
     if constexpr (GROUPED) {
       // m-tile prefix over experts, from the device-side offsets (written by
-      // the previous grid on the stream, so wait for it first)
+      // the previous grid on the stream, so wait for it first).  Offsets are
+      // caller data: clamped to [0, rows] and made monotone (a running max)
+      // so that no tile reaches outside the row range; both passes are warp
+      // scans, 32 experts at a time.
       grid_dependency_wait();
       const int E = p.num_experts;
-      for (int i = lane; i <= E; i += 32) offs[i] = min(max(p.expert_offsets[i], 0), p.rows);
-      __syncwarp();
-      if (lane == 0) {
-        // offsets are caller data: clamp to [0, rows] and make them monotone so
-        // that no tile reaches outside the row range
-        offs[0] = 0;
-        for (int e = 1; e <= E; ++e) offs[e] = max(offs[e], offs[e - 1]);
-        int acc = 0;
-        mt_prefix[0] = 0;
-        for (int e = 0; e < E; ++e) {
-          acc += (offs[e + 1] - offs[e] + BT - 1) / BT;
-          mt_prefix[e + 1] = acc;
+      int carry = 0;
+      for (int x0 = 0; x0 <= E; x0 += 32) {
+        const int x = x0 + lane;
+        int v = x <= E ? min(max(p.expert_offsets[x], 0), p.rows) : p.rows;
+        if (x == 0) v = 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, v, d);
+          if (lane >= d) v = max(v, t);
         }
+        v = max(v, carry);
+        if (x <= E) offs[x] = v;
+        carry = __shfl_sync(0xffffffffu, v, 31);
+      }
+      __syncwarp();
+      int acc = 0;
+      for (int x0 = 0; x0 < E; x0 += 32) {
+        const int x = x0 + lane;
+        const int c = x < E ? (offs[x + 1] - offs[x] + BT - 1) / BT : 0;
+        int incl = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += t;
+        }
+        if (x < E) mt_prefix[x + 1] = acc + incl;
+        acc += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) {
+        mt_prefix[0] = 0;
         long long T = (long long)acc * p.nt;
         if (T > p.max_tiles) {   // offsets inconsistent with the workspace bound
           atomicOr(p.status, kStatusDevice);
