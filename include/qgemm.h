@@ -71,6 +71,8 @@ enum { QGEMM_Z_NONE = 0, QGEMM_Z_UINT4 = 1 };
 enum { QGEMM_FP16 = 0, QGEMM_BF16 = 1, QGEMM_FP8E4M3 = 2 };
 /* GEMM types (compute config) */
 enum { QGEMM_GEMM_DENSE = 0, QGEMM_GEMM_GROUPED = 1 };
+/* gated activation fused into the output (layer config) */
+enum { QGEMM_ACT_NONE = 0, QGEMM_ACT_SILU_GLU = 1 };
 
 /*
  * Layer config: what the layer is.  Shapes are those of one expert; a dense
@@ -85,6 +87,18 @@ enum { QGEMM_GEMM_DENSE = 0, QGEMM_GEMM_GROUPED = 1 };
  *   out_dtype     output dtype: equal to act_dtype for W4A16, QGEMM_BF16 for W4A8
  *   has_bias      1: add bias[N] (out_dtype) in fp32 before the final rounding
  *   num_experts   1 for a dense layer, E for a grouped (MoE) layer
+ *   gated_act     QGEMM_ACT_NONE: C[M, N] = A W (+ bias).
+ *                 QGEMM_ACT_SILU_GLU: the N columns of W are a gate half G
+ *                 (columns [0, N/2)) and an up half U (columns [N/2, N)) of
+ *                 an expert's first MoE projection; the output is
+ *                 H[M, N/2] = silu(G') * U', where G' and U' are the two
+ *                 halves of A W (+ bias) rounded to out_dtype, silu in fp32,
+ *                 the product rounded to out_dtype (bit-identical to running
+ *                 the layer with QGEMM_ACT_NONE and then qgemm_moe_silu_mul).
+ *                 The weights are passed in the standard format and order;
+ *                 the pack entry point interleaves the two halves so that a
+ *                 gate column and its up column land in one output tile.
+ *                 Needs out_dtype QGEMM_BF16.
  */
 typedef struct {
   int64_t n;
@@ -97,6 +111,7 @@ typedef struct {
   int32_t out_dtype;
   int32_t has_bias;
   int32_t num_experts;
+  int32_t gated_act;
 } qgemm_layer_config;
 
 /*
@@ -171,7 +186,9 @@ qgemm_status qgemm_packed_size(const qgemm_layer_config* layer, size_t* bytes);
  * codes are re-encoded as offset binary (q + 8); nothing else changes value,
  * so the packed buffer means exactly what the standard tensors mean.  qzeros
  * must be NULL unless zero_format = QGEMM_Z_UINT4.  Runs once per layer; the
- * buffer is read-only afterwards.
+ * buffer is read-only afterwards.  For a gated layer (gated_act != 0) row
+ * 2i + s of n-tile nt holds the standard column s * N/2 + 64 nt + i (gate
+ * columns on even rows, the matching up columns on odd rows).
  */
 qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qweight,
                                 const void* scales, const void* qzeros, void* packed,
@@ -199,7 +216,7 @@ qgemm_status qgemm_workspace_init(void* workspace, size_t bytes, void* stream);
  *   a_scale   device fp32 [m] per-row activation scales (W4A8), else NULL
  *   packed    device packed buffer from qgemm_pack_weights
  *   bias      device [N] in out_dtype, or NULL when has_bias = 0
- *   c         device, [m, N] in out_dtype
+ *   c         device, [m, N] in out_dtype ([m, N/2] for a gated layer)
  *   workspace device, >= qgemm_workspace_size bytes, zero-initialised once
  * With compute->deterministic = 1 the split-K reduction runs in a fixed order
  * and results are bitwise reproducible for a given (config, m, tuning, device).
@@ -242,6 +259,7 @@ qgemm_status qgemm_run_noalloc(const qgemm_layer_config* layer,
  *   total_rows     number of rows of A and C (host value)
  *   packed         packed buffer of all E experts
  *   bias           device [E, N] or NULL
+ *   c              device [total_rows, N] ([total_rows, N/2] when gated)
  * The tile schedule is built on the device from expert_offsets: no host
  * synchronization is needed between the permute and the GEMM.
  */
@@ -306,7 +324,8 @@ qgemm_status qgemm_moe_combine(const void* y2, const int32_t* inv_perm,
  * kernels feed them to the tensor core, written as out[k, n] (device, [K, N]):
  * W4A16 the dequantized values in act_dtype, computed with exactly the
  * kernels' arithmetic; MXFP4 the e4m3 byte of each e2m1 code (the e8m0 block
- * scale is applied inside the MMA).
+ * scale is applied inside the MMA).  Columns are in the standard order for
+ * gated layers too (the pack's gate/up interleave is undone).
  */
 qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* packed,
                                  void* out_kn, void* stream);

@@ -39,6 +39,13 @@ MXFP4 tiled layout (same tiling):
     exponents of row n = 128 nt + r for k = 128 kt + [0, 32), [32, 64),
     [64, 96), [96, 128) in that order.
 
+Gated layers (an MoE expert's gate|up projection, N = 2I: gate columns
+[0, I), up columns [I, 2I)): the SiLU gate multiplies gate column i by up
+column I + i, so the pack places the pair in one tile, on neighbouring rows:
+row 2i + s of n-tile nt is standard column s * I + 64 nt + i (s = 0 gate,
+s = 1 up).  The layout above then applies to the matrix with its columns in
+that order.  The pages fix no pack order; this one is the implementation's.
+
 Packed buffer (what the pack entry point writes): the three streams above
 interleaved block by block, so that block (nt, kt) is one contiguous run of
 bytes [weights block][scales block][zeros block] and the blocks follow in the
@@ -147,6 +154,25 @@ def tiled_mxfp4_scales(b_nk) -> np.ndarray:
     kt_n, nt_n = kb // 4, n // TILE_N
     b4 = b.reshape(nt_n, TILE_N, kt_n, 4)
     return np.ascontiguousarray(b4.transpose(0, 2, 1, 3)).reshape(-1)
+
+
+def glu_column_order(n: int) -> np.ndarray:
+    """Standard column index held by each packed column of a gated layer of
+    width n (gate half first): entry 128 nt + 2 i + s is s * n/2 + 64 nt + i."""
+    if n % TILE_N:
+        raise ValueError("n must be a multiple of 128")
+    order = np.empty(n, dtype=np.int64)
+    for nt in range(n // TILE_N):
+        for i in range(TILE_N // 2):
+            for s in range(2):
+                order[TILE_N * nt + 2 * i + s] = s * (n // 2) + (TILE_N // 2) * nt + i
+    return order
+
+
+def glu_interleave_columns(x, axis: int = -1) -> np.ndarray:
+    """x with its gate|up columns (along axis) in the gated pack order."""
+    x = np.asarray(x)
+    return np.take(x, glu_column_order(x.shape[axis]), axis=axis)
 
 
 def interleave_blocks(*streams_and_sizes) -> np.ndarray:

@@ -32,11 +32,15 @@ class W4A16Linear:
     """A packed W4A16 layer (dense, or the stacked experts of a grouped layer).
 
     qweight int32 [E*K/8, N], scales [E*K/g, N] (act dtype), qzeros int32
-    [E*K/g, N/8] or None: the standard format of ``include/qgemm.h``."""
+    [E*K/g, N/8] or None: the standard format of ``include/qgemm.h``.
+    gated=True: the N columns are an MoE gate half and up half and the layer
+    writes silu(gate) * up, [rows, N/2] (bf16 only)."""
 
     def __init__(self, qweight, scales, qzeros, n, k, group, act_dtype, num_experts=1,
-                 bias=None, tuning=None, deterministic=False):
+                 bias=None, tuning=None, deterministic=False, gated=False):
         self.n, self.k, self.group, self.num_experts = n, k, group, num_experts
+        self.gated = gated
+        self.n_out = n // 2 if gated else n
         self.act_dtype = act_dtype
         asym = qzeros is not None
         adt = _DT[act_dtype]
@@ -44,7 +48,8 @@ class W4A16Linear:
             n, k, group, Q.QGEMM_W_UINT4_ZP if asym else Q.QGEMM_W_INT4_SYM,
             Q.QGEMM_S_FP16 if adt == Q.QGEMM_FP16 else Q.QGEMM_S_BF16,
             Q.QGEMM_Z_UINT4 if asym else Q.QGEMM_Z_NONE, adt, adt,
-            1 if bias is not None else 0, num_experts)
+            1 if bias is not None else 0, num_experts,
+            Q.QGEMM_ACT_SILU_GLU if gated else Q.QGEMM_ACT_NONE)
         st, nbytes = Q.qgemm_packed_size(self.layer)
         Q.check(st)
         dev = qweight.device
@@ -63,7 +68,7 @@ class W4A16Linear:
         a = a.contiguous()
         m = a.shape[0]
         if out is None:
-            out = torch.empty(m, self.n, dtype=self.act_dtype, device=a.device)
+            out = torch.empty(m, self.n_out, dtype=self.act_dtype, device=a.device)
         st, nbytes = Q.qgemm_workspace_size(self.layer, self.dense, self.tuning, max(m, 1))
         Q.check(st)
         ws = self.ws.get(nbytes)
@@ -75,7 +80,7 @@ class W4A16Linear:
                     out: torch.Tensor | None = None) -> torch.Tensor:
         rows = a_perm.shape[0]
         if out is None:
-            out = torch.empty(rows, self.n, dtype=self.act_dtype, device=a_perm.device)
+            out = torch.empty(rows, self.n_out, dtype=self.act_dtype, device=a_perm.device)
         st, nbytes = Q.qgemm_workspace_size(self.layer, self.grouped, self.tuning, max(rows, 1))
         Q.check(st)
         ws = self.ws.get(nbytes)
@@ -96,14 +101,18 @@ class W4A16Linear:
 class W4A8Linear:
     """A packed W4A8-MXFP4 layer: e2m1 codes uint8 [E*N, K/2] and e8m0 scales
     uint8 [E*N, K/32] in the standard format; activations are quantized per
-    row to e4m3 by the library and the output is bf16."""
+    row to e4m3 by the library and the output is bf16 (gated=True: as for
+    W4A16Linear, silu(gate) * up of the two column halves, [rows, N/2])."""
 
     def __init__(self, codes, scales, n, k, num_experts=1, bias=None, tuning=None,
-                 deterministic=False):
+                 deterministic=False, gated=False):
         self.n, self.k, self.num_experts = n, k, num_experts
+        self.gated = gated
+        self.n_out = n // 2 if gated else n
         self.layer = Q.layer_config(n, k, 32, Q.QGEMM_W_MXFP4, Q.QGEMM_S_E8M0, Q.QGEMM_Z_NONE,
                                     Q.QGEMM_FP8E4M3, Q.QGEMM_BF16,
-                                    1 if bias is not None else 0, num_experts)
+                                    1 if bias is not None else 0, num_experts,
+                                    Q.QGEMM_ACT_SILU_GLU if gated else Q.QGEMM_ACT_NONE)
         st, nbytes = Q.qgemm_packed_size(self.layer)
         Q.check(st)
         dev = codes.device
@@ -128,7 +137,7 @@ class W4A8Linear:
     def run_quantized(self, a8, a_scale, out=None):
         m = a8.shape[0]
         if out is None:
-            out = torch.empty(m, self.n, dtype=torch.bfloat16, device=a8.device)
+            out = torch.empty(m, self.n_out, dtype=torch.bfloat16, device=a8.device)
         st, nbytes = Q.qgemm_workspace_size(self.layer, self.dense, self.tuning, max(m, 1))
         Q.check(st)
         ws = self.ws.get(nbytes)
@@ -152,7 +161,9 @@ class W4A8Linear:
 
 class MoELayer:
     """Grouped-MoE W4A16 layer: permute -> GEMM1 (gate|up) -> SiLU gate ->
-    GEMM2 (down) -> combine, all on the current stream, no host sync."""
+    GEMM2 (down) -> combine, all on the current stream, no host sync.  When
+    w1 is gated the SiLU gate runs in GEMM1's epilogue (one launch fewer,
+    no [rows, 2I] intermediate)."""
 
     def __init__(self, w1: W4A16Linear, w2: W4A16Linear, num_experts: int, topk: int):
         self.w1, self.w2 = w1, w2
@@ -170,7 +181,8 @@ class MoELayer:
                 perm=torch.empty(max(r, 1), dtype=torch.int32, device=device),
                 inv=torch.empty(max(r, 1), dtype=torch.int32, device=device),
                 a_perm=torch.empty(max(r, 1), self.hidden, dtype=bf, device=device),
-                gu=torch.empty(max(r, 1), 2 * self.inter, dtype=bf, device=device),
+                gu=(None if self.w1.gated else
+                    torch.empty(max(r, 1), 2 * self.inter, dtype=bf, device=device)),
                 h=torch.empty(max(r, 1), self.inter, dtype=bf, device=device),
                 y2=torch.empty(max(r, 1), self.hidden, dtype=bf, device=device),
             )
@@ -184,8 +196,11 @@ class MoELayer:
             out = torch.empty(t, self.hidden, dtype=torch.bfloat16, device=a.device)
         Q.check(Q.qgemm_moe_permute(topk_ids, t, self.topk, self.e, b["offsets"], b["perm"],
                                     b["inv"], a, b["a_perm"], self.hidden))
-        self.w1.run_grouped(b["a_perm"][:r], b["offsets"], out=b["gu"][:r])
-        Q.check(Q.qgemm_moe_silu_mul(b["gu"], r, self.inter, b["h"]))
+        if self.w1.gated:
+            self.w1.run_grouped(b["a_perm"][:r], b["offsets"], out=b["h"][:r])
+        else:
+            self.w1.run_grouped(b["a_perm"][:r], b["offsets"], out=b["gu"][:r])
+            Q.check(Q.qgemm_moe_silu_mul(b["gu"], r, self.inter, b["h"]))
         self.w2.run_grouped(b["h"][:r], b["offsets"], out=b["y2"][:r])
         Q.check(Q.qgemm_moe_combine(b["y2"], b["inv"], topk_weights, t, self.topk, self.hidden,
                                     out))

@@ -227,9 +227,7 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ gu, uint16_t* __res
   for (int i = 0; i < 4; ++i) {
     const float2 g = __bfloat1622float2(g2[i]);
     const float2 u = __bfloat1622float2(u2[i]);
-    const float s0 = g.x / (1.f + expf(-g.x));
-    const float s1 = g.y / (1.f + expf(-g.y));
-    o2[i] = __floats2bfloat162_rn(s0 * u.x, s1 * u.y);
+    o2[i] = __floats2bfloat162_rn(silu_mul_f32(g.x, u.x), silu_mul_f32(g.y, u.y));
   }
   *reinterpret_cast<uint4*>(h + r * inter + c) = ov;
 }

@@ -56,7 +56,7 @@ inline FastDiv make_fastdiv(uint32_t d) {
 struct W4A16Params {
   const uint8_t* w;          // packed blocks of all experts: [weights][scales][zeros]
   const uint16_t* bias;      // [E, N] or null
-  uint16_t* c;               // [rows, N]
+  uint16_t* c;               // [rows, N], or [rows, N/2] when gated
   const float* a_scale;      // W4A8: per-row activation scales [rows], else null
   int rows;                  // M (dense) or total permuted rows (grouped)
   int n, k;
@@ -65,6 +65,8 @@ struct W4A16Params {
   int group;                 // group size
   int sg_shift;              // scale group of 32-wide k chunk j is j >> sg_shift
   int has_zp;
+  int gated;                 // 1: SiLU-gated output from interleaved gate/up rows
+  int whole_tiles;           // 1: never split a tile's K range across CTAs
   const int* expert_offsets; // device [E+1] or null (dense)
   int num_experts;
   long long w_expert_stride; // bytes between experts' packed blocks
@@ -96,10 +98,10 @@ cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
                          cudaStream_t stream);
 
 cudaError_t launch_repack_mxfp4(const uint8_t* codes, const uint8_t* scales, uint8_t* packed,
-                                int64_t n, int64_t k, int experts, cudaStream_t stream);
+                                int64_t n, int64_t k, int experts, int gated, cudaStream_t stream);
 
 cudaError_t launch_debug_mx_codes(const uint8_t* w, uint8_t* out_kn, int64_t n, int64_t k,
-                                  cudaStream_t stream);
+                                  int gated, cudaStream_t stream);
 
 // Packed block of one (n-tile, k-tile): 8192 bytes of codes, then the scales
 // (W4A16: 128 * st 16-bit words; MXFP4: 128 32-bit words), then the zero
@@ -111,12 +113,36 @@ __host__ __device__ constexpr int packed_block_bytes(bool mx, int st, bool zp) {
   return kTileBytes + packed_scale_bytes(mx, st) + (zp ? st * kTileN : 0);
 }
 
+// Gated layers: packed row r of n-tile nt holds standard column
+// (r & 1) * N/2 + 64 nt + r/2, so gate column i and up column N/2 + i sit on
+// neighbouring rows (neighbouring lanes of the epilogue) of one tile.
+__host__ __device__ inline int glu_source_col(int nt, int r, int n) {
+  return (r & 1) * (n >> 1) + nt * (kTileN / 2) + (r >> 1);
+}
+__host__ __device__ inline int packed_source_col(int nt, int r, int n, int gated) {
+  return gated ? glu_source_col(nt, r, n) : nt * kTileN + r;
+}
+
+#ifdef __CUDACC__
+// SiLU gate of one (gate, up) pair in fp32: g / (1 + e^-g) * u with the
+// hardware exponential and the approximate divide (relative error ~1e-6,
+// far below the bf16 rounding that follows; e^-g = inf gives the limit 0).
+// The GEMM epilogue runs it beside the dequant warps, where an IEEE exp and
+// divide would cost several times the issue slots.  Each operation is
+// rounded on its own (no contraction), so the fused GEMM epilogue and the
+// standalone kernel produce the same bits from the same rounded inputs.
+__device__ __forceinline__ float silu_mul_f32(float g, float u) {
+  return __fmul_rn(__fdividef(g, __fadd_rn(1.f, __expf(-g))), u);
+}
+#endif
+
 cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
                              const int32_t* qzeros, uint8_t* packed, int64_t n, int64_t k,
-                             int group, int signed_q, int experts, cudaStream_t stream);
+                             int group, int signed_q, int experts, int gated,
+                             cudaStream_t stream);
 
 cudaError_t launch_debug_dequant(const uint8_t* packed, uint16_t* out, int64_t n, int64_t k,
-                                 int group, int has_zp, bool fp16, cudaStream_t stream);
+                                 int group, int has_zp, bool fp16, int gated, cudaStream_t stream);
 
 cudaError_t launch_act_quant_fp8(const uint16_t* x, int64_t m, int64_t k, uint8_t* a8,
                                  float* scale, cudaStream_t stream);

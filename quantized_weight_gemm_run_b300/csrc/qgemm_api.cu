@@ -98,6 +98,10 @@ static qgemm_status check_layer(const qgemm_layer_config* L) {
     return fail(QGEMM_ERR_UNSUPPORTED, "n or k above 2^20");
   if (L->has_bias != 0 && L->has_bias != 1)
     return fail(QGEMM_ERR_INVALID_ARG, "has_bias must be 0 or 1");
+  if (L->gated_act != QGEMM_ACT_NONE && L->gated_act != QGEMM_ACT_SILU_GLU)
+    return fail(QGEMM_ERR_INVALID_ARG, "unknown gated_act %d", L->gated_act);
+  if (L->gated_act != QGEMM_ACT_NONE && L->out_dtype != QGEMM_BF16)
+    return fail(QGEMM_ERR_UNSUPPORTED, "a gated output must be bf16");
   switch (L->weight_format) {
     case QGEMM_W_INT4_SYM:
     case QGEMM_W_UINT4_ZP: {
@@ -210,6 +214,7 @@ static bool make_geometry(int bt, int st, int has_zp, bool mx, int experts, int 
 
 struct Plan {
   int bt, grid, st, off_s, off_z;
+  int whole_tiles;   // 1: no tile's K range is split across CTAs
   Geometry g;
   int64_t max_tiles;
   WorkspaceLayout ws;
@@ -254,6 +259,7 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   }
   P->bt = bt;
   P->grid = grid;
+  P->whole_tiles = (T && T->split_k == 1) ? 1 : 0;
   P->st = st;
   P->off_s = kTileBytes;                                   // inside a packed block
   P->off_z = kTileBytes + packed_scale_bytes(is_mx(L), st);
@@ -378,6 +384,8 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.group = L->group_size;
   p.sg_shift = L->group_size == 32 ? 0 : L->group_size == 64 ? 1 : 2;
   p.has_zp = has_zp ? 1 : 0;
+  p.gated = L->gated_act != 0;
+  p.whole_tiles = P.whole_tiles;
   p.expert_offsets = offsets;
   p.num_experts = E;
   p.w_expert_stride = (long long)(wb / E);
@@ -412,7 +420,8 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
     p.sk_t = (int)T;
     p.sk_w = (int)W;
     p.sk_u = (int)U;
-    p.sk_gs = (int)(U < G ? U : G);
+    // whole tiles only: the r remaining tiles go to r CTAs, one each
+    p.sk_gs = (int)(P.whole_tiles ? U / p.kt : (U < G ? U : G));
     p.div_kt = make_fastdiv((uint32_t)p.kt);
     p.div_nt = make_fastdiv((uint32_t)p.nt);
     p.div_gs = make_fastdiv(p.sk_gs > 0 ? (uint32_t)p.sk_gs : 1u);
@@ -422,10 +431,12 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   // into the activation ring when it is large enough
   p.fix_smem = (int64_t)P.g.x_stages * P.g.x_bytes >= (int64_t)P.bt * kTileN * 4;
   p.wait_limit_ns = g_wait_limit_ns;
-  // output [rows, n] of 16-bit values, written by 16-row x 32-column tensor stores
+  // output [rows, n] of 16-bit values, written by 16-row x 32-column tensor
+  // stores; a gated output [rows, n/2] by 16-row x 16-column ones
   CUtensorMap tmap_c;
-  if (!encode_tmap_2d(&tmap_c, CU_TENSOR_MAP_DATA_TYPE_UINT16, c, (uint64_t)L->n, (uint64_t)rows,
-                      (uint64_t)L->n * 2, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+  const uint64_t n_out = p.gated ? (uint64_t)L->n / 2 : (uint64_t)L->n;
+  if (!encode_tmap_2d(&tmap_c, CU_TENSOR_MAP_DATA_TYPE_UINT16, c, n_out, (uint64_t)rows,
+                      n_out * 2, p.gated ? 16 : 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
     return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the output tensor");
   cudaError_t e =
       launch_w4a16(tmap, tmap_c, p, P.bt, mx ? 2 : fp16 ? 1 : 0, grouped, P.grid, stream);
@@ -488,14 +499,14 @@ qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qwe
       return fail(QGEMM_ERR_INVALID_ARG, "MXFP4 scales must be 4-byte aligned");
     e = launch_repack_mxfp4(static_cast<const uint8_t*>(qweight),
                             static_cast<const uint8_t*>(scales), static_cast<uint8_t*>(packed),
-                            layer->n, layer->k, layer->num_experts,
+                            layer->n, layer->k, layer->num_experts, layer->gated_act != 0,
                             static_cast<cudaStream_t>(stream));
   } else {
     e = launch_repack_w4(static_cast<const int32_t*>(qweight),
                          static_cast<const uint16_t*>(scales), static_cast<const int32_t*>(qzeros),
                          static_cast<uint8_t*>(packed), layer->n, layer->k, layer->group_size,
                          layer->weight_format == QGEMM_W_INT4_SYM ? 1 : 0, layer->num_experts,
-                         static_cast<cudaStream_t>(stream));
+                         layer->gated_act != 0, static_cast<cudaStream_t>(stream));
   }
   if (e != cudaSuccess) return cuda_fail(e, "repack launch");
   return ok();
@@ -621,12 +632,14 @@ qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* pa
   cudaError_t e;
   if (is_mx(layer))
     e = launch_debug_mx_codes(static_cast<const uint8_t*>(packed), static_cast<uint8_t*>(out_kn),
-                              layer->n, layer->k, static_cast<cudaStream_t>(stream));
+                              layer->n, layer->k, layer->gated_act != 0,
+                              static_cast<cudaStream_t>(stream));
   else
     e = launch_debug_dequant(static_cast<const uint8_t*>(packed), static_cast<uint16_t*>(out_kn),
                              layer->n, layer->k, layer->group_size,
                              layer->zero_format == QGEMM_Z_UINT4 ? 1 : 0,
-                             layer->act_dtype == QGEMM_FP16, static_cast<cudaStream_t>(stream));
+                             layer->act_dtype == QGEMM_FP16, layer->gated_act != 0,
+                             static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
   return ok();
 }
@@ -672,13 +685,14 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
       snprintf(tmp, sizeof(tmp),
                "kernel=%s%s weights=%s group=%d act=%s out=%s n=%lld k=%lld "
                "m=%lld experts=%d block_tok=%d act_slots=%d weight_slots=%dx%d grid=%d smem=%d "
-               "workspace=%zu "
+               "workspace=%zu epilogue=%s "
                "device=sm_103",
                is_mx(layer) ? "w4a8_tcgen05_mxf8f6f4_swapab" : "w4a16_tcgen05_swapab",
                grouped ? "_grouped" : "", wf[layer->weight_format], layer->group_size,
                dt[layer->act_dtype], dt[layer->out_dtype], (long long)layer->n,
                (long long)layer->k, (long long)m, layer->num_experts, P.bt, P.g.x_stages,
-               P.g.w_stages, P.g.rw, P.grid, P.g.smem, P.ws.total);
+               P.g.w_stages, P.g.rw, P.grid, P.g.smem, P.ws.total,
+               layer->gated_act ? "silu_glu" : "plain");
       rec = tmp;
     }
   }

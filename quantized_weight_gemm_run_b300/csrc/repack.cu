@@ -22,15 +22,17 @@
 //            row r for k = 32j .. 32j+31 of the tile.
 //   zeros    UINT4 only: 128 * ST bytes, same order, zero point 0..15.
 //
-// Every thread writes one output vector / element; reads of the standard
-// tensors are coalesced along N.
+// A gated layer's rows are taken in the gate/up interleaved order
+// (glu_source_col).  Every thread writes one output vector / element; reads
+// of the standard tensors are coalesced along N (in two runs per warp when
+// gated).
 
 #include "internal.h"
 
 namespace qg {
 
 __global__ void repack_weights_kernel(const int32_t* __restrict__ qweight, uint8_t* __restrict__ out,
-                                      int n, int k, int signed_q, int block_bytes,
+                                      int n, int k, int signed_q, int block_bytes, int gated,
                                       long long total) {
   const long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (vec >= total) return;
@@ -42,7 +44,7 @@ __global__ void repack_weights_kernel(const int32_t* __restrict__ qweight, uint8
   const int v = (int)(rem % 512);
   const int nt = (int)(blk / KT), kt = (int)(blk % KT);
   const int t = v & 31, j = (v >> 5) & 3, qd = v >> 7;
-  const int col = nt * kTileN + qd * 32 + t;
+  const int col = packed_source_col(nt, qd * 32 + t, n, gated);
   const long long word_row0 = (long long)(kt * kTileK + j * 32) / 8;   // first K/8 row
   const int32_t* src = qweight + ex * (long long)(k / 8) * n;
   uint32_t o[4];
@@ -68,7 +70,8 @@ __global__ void repack_weights_kernel(const int32_t* __restrict__ qweight, uint8
 
 __global__ void repack_scales_kernel(const uint16_t* __restrict__ scales,
                                      const int32_t* __restrict__ qzeros, uint8_t* __restrict__ out,
-                                     int n, int k, int group, int block_bytes, long long total) {
+                                     int n, int k, int group, int block_bytes, int gated,
+                                     long long total) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= total) return;
   const int KT = k / kTileK, NT = n / kTileN;
@@ -83,7 +86,7 @@ __global__ void repack_scales_kernel(const uint16_t* __restrict__ scales,
   const int nt = (int)(blk / KT), kt = (int)(blk % KT);
   const int kk = kt * kTileK + sg * (group < kTileK ? group : kTileK);
   const int grp = kk / group;
-  const int col = nt * kTileN + r;
+  const int col = packed_source_col(nt, r, n, gated);
   const long long groups = k / group;
   uint8_t* bp = out + (ex * ((long long)NT * KT) + blk) * block_bytes;
   reinterpret_cast<uint16_t*>(bp + kTileBytes)[sg * kTileN + r] =
@@ -97,18 +100,19 @@ __global__ void repack_scales_kernel(const uint16_t* __restrict__ scales,
 
 cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
                              const int32_t* qzeros, uint8_t* packed, int64_t n, int64_t k,
-                             int group, int signed_q, int experts, cudaStream_t stream) {
+                             int group, int signed_q, int experts, int gated,
+                             cudaStream_t stream) {
   const int threads = 256;
   const int st = group < kTileK ? kTileK / group : 1;
   const int block_bytes = packed_block_bytes(false, st, qzeros != nullptr);
   const long long vecs = (long long)experts * (n / kTileN) * (k / kTileK) * 512;
   repack_weights_kernel<<<(unsigned)((vecs + threads - 1) / threads), threads, 0, stream>>>(
-      qweight, packed, (int)n, (int)k, signed_q, block_bytes, vecs);
+      qweight, packed, (int)n, (int)k, signed_q, block_bytes, gated, vecs);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const long long elems = (long long)experts * (n / kTileN) * (k / kTileK) * st * kTileN;
   repack_scales_kernel<<<(unsigned)((elems + threads - 1) / threads), threads, 0, stream>>>(
-      scales, qzeros, packed, (int)n, (int)k, group, block_bytes, elems);
+      scales, qzeros, packed, (int)n, (int)k, group, block_bytes, gated, elems);
   return cudaGetLastError();
 }
 
@@ -118,7 +122,7 @@ cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
 // in consecutive nibbles.
 __global__ void repack_mxfp4_kernel(const uint8_t* __restrict__ codes,
                                     const uint8_t* __restrict__ scales, uint8_t* __restrict__ out,
-                                    int n, int k, long long vecs, long long words) {
+                                    int n, int k, int gated, long long vecs, long long words) {
   constexpr int kBlock = packed_block_bytes(true, 1, false);
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int KT = k / kTileK, NT = n / kTileN;
@@ -130,7 +134,7 @@ __global__ void repack_mxfp4_kernel(const uint8_t* __restrict__ codes,
     const int v = (int)(rem % 512);
     const int nt = (int)(blk / KT), kt = (int)(blk % KT);
     const int t = v & 31, j = (v >> 5) & 3, qd = v >> 7;
-    const long long row = (long long)nt * kTileN + qd * 32 + t;
+    const long long row = packed_source_col(nt, qd * 32 + t, n, gated);
     const uint8_t* src = codes + (ex * n + row) * (k / 2) + (kt * kTileK + j * 32) / 2;
     *reinterpret_cast<uint4*>(out + (ex * ((long long)NT * KT) + blk) * kBlock + v * 16) =
         *reinterpret_cast<const uint4*>(src);
@@ -142,20 +146,21 @@ __global__ void repack_mxfp4_kernel(const uint8_t* __restrict__ codes,
     const int r = (int)(rem % kTileN);
     const long long blk = rem / kTileN;
     const int nt = (int)(blk / KT), kt = (int)(blk % KT);
-    const long long row = (long long)nt * kTileN + r;
+    const long long row = packed_source_col(nt, r, n, gated);
     reinterpret_cast<uint32_t*>(out + (ex * ((long long)NT * KT) + blk) * kBlock + kTileBytes)[r] =
         *reinterpret_cast<const uint32_t*>(scales + (ex * n + row) * (k / 32) + kt * 4);
   }
 }
 
 cudaError_t launch_repack_mxfp4(const uint8_t* codes, const uint8_t* scales, uint8_t* packed,
-                                int64_t n, int64_t k, int experts, cudaStream_t stream) {
+                                int64_t n, int64_t k, int experts, int gated,
+                                cudaStream_t stream) {
   const long long tiles = (long long)experts * (n / kTileN) * (k / kTileK);
   const long long vecs = tiles * 512, words = tiles * kTileN;
   const long long total = vecs > words ? vecs : words;
   const int threads = 256;
   repack_mxfp4_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, stream>>>(
-      codes, scales, packed, (int)n, (int)k, vecs, words);
+      codes, scales, packed, (int)n, (int)k, gated, vecs, words);
   return cudaGetLastError();
 }
 

@@ -101,7 +101,7 @@ struct Schedule {
     c = c_;
     W = T / G;
     U = (T - W * G) * KT;
-    Gs = U < G ? U : G;
+    Gs = p.whole_tiles ? U / KT : (U < G ? U : G);   // whole tiles: one per CTA
     fast = false;
     dkt = p.div_kt;
     start();
@@ -768,6 +768,56 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         o[i] = to_out<FP16>(v + bias);
       }
       const int valid = tc.rows - m0;
+      if constexpr (!FP16) {
+        if (p.gated) {
+          // Lanes 2j and 2j+1 hold the gate and the up value of output column
+          // 64 nt + 16 q + j for the chunk's 16 rows; they swap halves so that
+          // the even lane forms rows 0..7 of the gated product, the odd lane
+          // rows 8..15.
+          const int odd = lane & 1;
+          uint32_t pk[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) pk[j] = (uint32_t)o[2 * j] | ((uint32_t)o[2 * j + 1] << 16);
+          uint32_t hw[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t mine = odd ? pk[4 + j] : pk[j];
+            const uint32_t theirs = __shfl_xor_sync(0xffffffffu, odd ? pk[j] : pk[4 + j], 1);
+            const uint32_t gw = odd ? theirs : mine, uw = odd ? mine : theirs;
+            const float h0 = silu_mul_f32(__uint_as_float(gw << 16), __uint_as_float(uw << 16));
+            const float h1 = silu_mul_f32(__uint_as_float(gw & 0xFFFF0000u),
+                                          __uint_as_float(uw & 0xFFFF0000u));
+            hw[j] = (uint32_t)to_out<false>(h0) | ((uint32_t)to_out<false>(h1) << 16);
+          }
+          const int r0 = odd * 8, hcol = lane >> 1;
+          if (!GROUPED || valid >= 16) {
+            uint16_t* sb = stg + sbuf * (16 * 32);   // 16 rows x 16 columns
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              sb[(r0 + 2 * j) * 16 + hcol] = (uint16_t)(hw[j] & 0xFFFF);
+              sb[(r0 + 2 * j + 1) * 16 + hcol] = (uint16_t)(hw[j] >> 16);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_c, sb, tc.nt * (kTileN / 2) + q * 16, tc.row0 + m0);
+              bulk_commit_group();
+            }
+            sbuf ^= 1;
+          } else {
+            const int nh = p.n >> 1;
+            uint16_t* dst = p.c + (long long)(tc.row0 + m0 + r0) * nh + tc.nt * (kTileN / 2) +
+                            q * 16 + hcol;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (r0 + j < valid)
+                dst[(long long)j * nh] = (uint16_t)((hw[j >> 1] >> (16 * (j & 1))) & 0xFFFF);
+          }
+          return;
+        }
+      }
       if (!GROUPED || valid >= 16) {
         uint16_t* sb = stg + sbuf * (16 * 32);
         if (lane == 0) bulk_wait_group_read<1>();   // this buffer's previous store has read it
@@ -794,7 +844,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const bool whole = (wi.k0 == 0 && wi.k1 == p.kt);
       if (!mbar_wait(&acc_full[acc], accphase, abort_flag, p.status, lim, kStatusTimeout)) break;
       tc_fence_after();
-      const int n = tc.nt * kTileN + col;
+      const int n = packed_source_col(tc.nt, col, p.n, p.gated);
       const float bias = p.bias ? from_out<FP16>(p.bias[(long long)tc.e * p.n + n]) : 0.f;
       const uint32_t tbase = tmem_base + lane_addr + kAccCol + acc * BT;
       // Split tiles.  Partial tiles are column-major [col][BT] (this thread's
@@ -1042,7 +1092,7 @@ cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
 // out[k, n] = the value the GEMM kernel feeds the tensor core for W^[k, n].
 template <bool FP16>
 __global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n, int k,
-                                     int group, int has_zp) {
+                                     int group, int has_zp, int gated) {
   const int KT = k / kTileK;
   const long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // one 16-byte vector
   const long long total = (long long)(n / kTileN) * KT * 512;
@@ -1062,7 +1112,7 @@ __global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n
   constexpr uint32_t magic16 = FP16 ? 0x6400u : 0x4300u;
   uint32_t o[16];
   dequant_vec<FP16>(wv, (magic16 + zq) * 0x00010001u, sbits * 0x00010001u, o);
-  const int nn = nt * kTileN + row;
+  const int nn = packed_source_col(nt, row, n, gated);
 #pragma unroll
   for (int c = 0; c < 16; ++c) {
     const int kk = kt * kTileK + j * 32 + 2 * c;
@@ -1072,22 +1122,22 @@ __global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n
 }
 
 cudaError_t launch_debug_dequant(const uint8_t* packed, uint16_t* out, int64_t n, int64_t k,
-                                 int group, int has_zp, bool fp16, cudaStream_t stream) {
+                                 int group, int has_zp, bool fp16, int gated, cudaStream_t stream) {
   const long long total = (n / kTileN) * (k / kTileK) * 512;
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   if (fp16)
     debug_dequant_kernel<true><<<blocks, threads, 0, stream>>>(packed, out, (int)n, (int)k,
-                                                                group, has_zp);
+                                                                group, has_zp, gated);
   else
     debug_dequant_kernel<false><<<blocks, threads, 0, stream>>>(packed, out, (int)n, (int)k,
-                                                                 group, has_zp);
+                                                                 group, has_zp, gated);
   return cudaGetLastError();
 }
 
 // out[k, n] = the e4m3 byte the W4A8 kernel writes to tensor memory for the
 // code of W[k, n] (the e8m0 block scale is applied by the MMA, not here).
-__global__ void debug_mx_codes_kernel(const uint8_t* w, uint8_t* out, int n, int k) {
+__global__ void debug_mx_codes_kernel(const uint8_t* w, uint8_t* out, int n, int k, int gated) {
   const int KT = k / kTileK;
   const long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long total = (long long)(n / kTileN) * KT * 512;
@@ -1099,7 +1149,7 @@ __global__ void debug_mx_codes_kernel(const uint8_t* w, uint8_t* out, int n, int
   uint32_t o[8];
   dequant_vec_mx(reinterpret_cast<const uint4*>(w + blk * packed_block_bytes(true, 1, false))[v],
                  o);
-  const int nn = nt * kTileN + q * 32 + t;
+  const int nn = packed_source_col(nt, q * 32 + t, n, gated);
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     const int kk = kt * kTileK + j * 32 + c;
@@ -1108,10 +1158,10 @@ __global__ void debug_mx_codes_kernel(const uint8_t* w, uint8_t* out, int n, int
 }
 
 cudaError_t launch_debug_mx_codes(const uint8_t* w, uint8_t* out_kn, int64_t n, int64_t k,
-                                  cudaStream_t stream) {
+                                  int gated, cudaStream_t stream) {
   const long long total = (n / kTileN) * (k / kTileK) * 512;
   debug_mx_codes_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(w, out_kn, (int)n,
-                                                                           (int)k);
+                                                                           (int)k, gated);
   return cudaGetLastError();
 }
 

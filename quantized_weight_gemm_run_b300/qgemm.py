@@ -28,6 +28,7 @@ QGEMM_S_FP16, QGEMM_S_BF16, QGEMM_S_E8M0 = 0, 1, 2
 QGEMM_Z_NONE, QGEMM_Z_UINT4 = 0, 1
 QGEMM_FP16, QGEMM_BF16, QGEMM_FP8E4M3 = 0, 1, 2
 QGEMM_GEMM_DENSE, QGEMM_GEMM_GROUPED = 0, 1
+QGEMM_ACT_NONE, QGEMM_ACT_SILU_GLU = 0, 1
 
 
 class qgemm_layer_config(ctypes.Structure):
@@ -35,7 +36,7 @@ class qgemm_layer_config(ctypes.Structure):
                 ("weight_format", ctypes.c_int32), ("scale_format", ctypes.c_int32),
                 ("zero_format", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("has_bias", ctypes.c_int32),
-                ("num_experts", ctypes.c_int32)]
+                ("num_experts", ctypes.c_int32), ("gated_act", ctypes.c_int32)]
 
 
 class qgemm_compute_config(ctypes.Structure):
@@ -136,9 +137,9 @@ def check(status: int) -> None:
 
 
 def layer_config(n, k, group_size, weight_format, scale_format, zero_format, act_dtype,
-                 out_dtype, has_bias=0, num_experts=1) -> qgemm_layer_config:
+                 out_dtype, has_bias=0, num_experts=1, gated_act=0) -> qgemm_layer_config:
     return qgemm_layer_config(n, k, group_size, weight_format, scale_format, zero_format,
-                              act_dtype, out_dtype, has_bias, num_experts)
+                              act_dtype, out_dtype, has_bias, num_experts, gated_act)
 
 
 def compute_config(gemm_type=QGEMM_GEMM_DENSE, batch_invariant=0,

@@ -59,6 +59,10 @@ def test_packed_size_host_only(Q):
                                        scale_format=Q.QGEMM_S_E8M0, group_size=32,
                                        act_dtype=Q.QGEMM_FP8E4M3, out_dtype=Q.QGEMM_BF16))
     assert st == Q.QGEMM_OK and b == blocks * (8192 + 512)
+    # the gate/up interleave of a gated layer moves columns, it adds no bytes
+    st, b = Q.qgemm_packed_size(_layer(Q, act_dtype=Q.QGEMM_BF16, out_dtype=Q.QGEMM_BF16,
+                                       scale_format=Q.QGEMM_S_BF16, gated_act=1))
+    assert st == Q.QGEMM_OK and b == blocks * (8192 + 256)
 
 
 @pytest.mark.parametrize("bad,code", [
@@ -75,6 +79,8 @@ def test_packed_size_host_only(Q):
     (dict(n=0), "INVALID_ARG"),
     (dict(num_experts=0), "INVALID_ARG"),
     (dict(has_bias=2), "INVALID_ARG"),
+    (dict(gated_act=2), "INVALID_ARG"),
+    (dict(gated_act=1), "UNSUPPORTED"),             # a gated output must be bf16
 ])
 def test_rejections_are_clear(Q, bad, code):
     st, _ = Q.qgemm_packed_size(_layer(Q, **bad))
@@ -95,3 +101,19 @@ def test_pack_rejects_missing_pointers_before_launch(Q):
                   act_dtype=Q.QGEMM_BF16, out_dtype=Q.QGEMM_BF16, scale_format=Q.QGEMM_S_BF16)
     # zero-point tensors are required for UINT4
     assert Q.qgemm_pack_weights(asym, 16, 16, None, 16, 0) == Q.QGEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["qgemm_layer_config", "qgemm_compute_config",
+                                  "qgemm_tuning_config"])
+def test_binding_structs_match_header(Q, name):
+    """The ctypes mirrors list the header's fields in the same order and widths."""
+    src = open(os.path.join(ROOT, "include", "qgemm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    body = re.search(r"typedef struct\s*\{([^}]*)\}\s*" + name + r"\s*;", src).group(1)
+    fields = re.findall(r"(int32_t|int64_t)\s+(\w+)\s*;", body)
+    cls = getattr(Q, name)
+    got = [(f, ctypes_t) for f, ctypes_t in cls._fields_]
+    assert [f for f, _ in got] == [f for _, f in fields]
+    import ctypes
+    width = {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64}
+    assert [t for _, t in got] == [width[t] for t, _ in fields]

@@ -147,7 +147,7 @@ class MoEWeights:
             self._c2[i] = quant.dequant_int(self.q2[i], self.s2[i], None, self.g, "bf16")
         return self._c2[i]
 
-    def layer(self, topk):
+    def layer(self, topk, gated=True):
         from quantized_weight_gemm_run_b300.api import MoELayer, W4A16Linear
 
         def stack(qs, ss):
@@ -156,7 +156,7 @@ class MoEWeights:
             return torch.from_numpy(qw).to(DEV), torch.from_numpy(sc).to(DEV)
 
         l1 = W4A16Linear(*stack(self.q1, self.s1), None, 2 * self.inter, self.hidden, self.g,
-                         torch.bfloat16, num_experts=self.e)
+                         torch.bfloat16, num_experts=self.e, gated=gated)
         l2 = W4A16Linear(*stack(self.q2, self.s2), None, self.hidden, self.inter, self.g,
                          torch.bfloat16, num_experts=self.e)
         return MoELayer(l1, l2, self.e, topk), l1, l2
@@ -171,7 +171,7 @@ def moe_full():
 
 def test_moe_layer_small_all_stages(Q):
     w = MoEWeights(8, 256, 128, 128, seed=17)
-    layer, l1, l2 = w.layer(3)
+    layer, l1, l2 = w.layer(3, gated=False)   # the unfused path keeps GU for the check
     g = synth.rng(18)
     t = 45
     x = codecs.bf16(synth.activations_fp32(g, t, 256))
@@ -194,10 +194,11 @@ def test_moe_layer_small_all_stages(Q):
     assert_close(to_np(y), ref["y"], what="layer")
 
 
+@pytest.mark.parametrize("gated", [True, False])
 @pytest.mark.parametrize("t", [16, 256])
-def test_moe_layer_full_config(Q, moe_full, t):
+def test_moe_layer_full_config(Q, moe_full, t, gated):
     s = synth.MOE_SHAPE
-    layer, l1, l2 = moe_full.layer(s["topk"])
+    layer, l1, l2 = moe_full.layer(s["topk"], gated=gated)
     g = synth.rng(synth.SEED_MOE + t)
     x = codecs.bf16(synth.activations_fp32(g, t, s["hidden"]))
     ids, wts = moe.route(synth.router_logits_fp32(g, t, s["experts"]), s["topk"])

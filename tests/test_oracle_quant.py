@@ -252,3 +252,53 @@ def test_packed_mxfp4_scalar_spec():
         nib = (byte >> 4) if rr % 2 else (byte & 0xF)
         assert nib == (codes[nn, kk // 2] >> (4 * (kk % 2))) & 0xF
         assert buf[base + 8192 + 4 * nl + j] == b[nn, kk // 32]
+
+
+@pytest.mark.parametrize("n", [128, 384, 1024])
+def test_glu_column_order_pairs_gate_with_up(n):
+    """The gated pack order is a permutation in which every tile-row pair
+    (2i, 2i+1) holds a gate column and its up column (n/2 apart), and each
+    tile's gate columns are 64 consecutive output columns."""
+    order = layout.glu_column_order(n)
+    assert sorted(order.tolist()) == list(range(n))
+    pairs = order.reshape(-1, 2)
+    assert np.all(pairs[:, 0] < n // 2) and np.all(pairs[:, 1] - pairs[:, 0] == n // 2)
+    gate_per_tile = pairs[:, 0].reshape(n // 128, 64)
+    assert np.array_equal(gate_per_tile, np.arange(n // 2).reshape(n // 128, 64))
+
+
+def test_glu_interleave_gives_the_same_gated_product():
+    """Pairing neighbouring columns of the interleaved GU reproduces
+    silu(G) * U of the standard layout exactly."""
+    from oracle import moe
+    g = np.random.default_rng(23)
+    inter = 192
+    gu = codecs.bf16(g.standard_normal((7, 2 * inter)) * 3)
+    gi = layout.glu_interleave_columns(gu)
+    paired = np.concatenate([gi[:, 0::2], gi[:, 1::2]], axis=1)   # [G | U] again
+    assert np.array_equal(moe.silu_mul(paired, inter), moe.silu_mul(gu, inter))
+    assert np.array_equal(paired, gu)
+
+
+def test_gated_packed_buffer_scalar_spec():
+    """Row 2i + s of n-tile nt of a gated layer's packed codes and scales holds
+    standard column s * N/2 + 64 nt + i."""
+    g = np.random.default_rng(24)
+    k, n, gsize = 256, 384, 128
+    q = g.integers(0, 16, (k, n))
+    sb = g.integers(0, 65535, (k // gsize, n)).astype(np.uint16)
+    z = g.integers(0, 16, (k // gsize, n))
+    il = layout.glu_interleave_columns
+    buf = layout.packed_w4(il(q), il(sb), il(z), gsize, signed=False)
+    blk = 8192 + 256 + 128
+    for _ in range(800):
+        kk, nt, i, s = (int(g.integers(0, k)), int(g.integers(0, n // 128)),
+                        int(g.integers(0, 64)), int(g.integers(0, 2)))
+        src = s * (n // 2) + 64 * nt + i
+        r = 2 * i + s
+        kt, kl = divmod(kk, 128)
+        base = (nt * (k // 128) + kt) * blk
+        assert _nibble_at(buf[base: base + 8192], r, kl, 1) == q[kk, src]
+        sbyte = base + 8192 + 2 * r
+        assert int(buf[sbyte]) | (int(buf[sbyte + 1]) << 8) == sb[kk // gsize, src]
+        assert buf[base + 8192 + 256 + r] == z[kk // gsize, src]

@@ -1,6 +1,7 @@
 """The persistent GEMM kernel's work split, restated on the host: whole tiles
 round-robin over the grid, then the remaining tiles' K-tiles split evenly
-over min(grid, units) CTAs.  Checks that every (tile, k-tile) unit is owned by
+over min(grid, units) CTAs (with splitting turned off, over as many CTAs as
+there are remaining tiles, one tile each).  Checks that every (tile, k-tile) unit is owned by
 exactly one CTA, that the CTAs sharing a split tile are exactly the
 contiguous range the kernel's reducer sums over, and that the partial-tile
 slots (two per CTA) never collide."""
@@ -10,10 +11,10 @@ import itertools
 import pytest
 
 
-def schedule(T, KT, G):
+def schedule(T, KT, G, whole=False):
     W = T // G
     U = (T - W * G) * KT
-    Gs = U if U < G else G
+    Gs = U // KT if whole else (U if U < G else G)
 
     def sk_begin(c):
         return (c * U) // Gs
@@ -42,19 +43,29 @@ def schedule(T, KT, G):
                 which = 0 if sk_begin(c) >= us else 1
                 assert (c, which) not in slots
                 slots.add((c, which))
-    return W, cta_of_unit, owner
+    return W, cta_of_unit, owner, items_of
 
 
 @pytest.mark.parametrize("T,KT,G", list(itertools.product(
     [1, 2, 3, 8, 32, 149, 150, 256, 300, 4096], [1, 2, 3, 32, 64], [1, 7, 37, 148])))
 def test_schedule_partition(T, KT, G):
-    W, cta_of_unit, owner = schedule(T, KT, G)
+    W, cta_of_unit, owner, _ = schedule(T, KT, G)
     assert len(owner) == T * KT
     for t in range(W * G, T):
         us = (t - W * G) * KT
         owners = {owner[(t, k)] for k in range(KT)}
         if len(owners) > 1:
             assert owners == set(range(cta_of_unit(us), cta_of_unit(us + KT - 1) + 1))
+
+
+@pytest.mark.parametrize("T,KT,G", list(itertools.product(
+    [1, 3, 149, 150, 300, 4096], [1, 3, 32], [1, 7, 148])))
+def test_schedule_whole_tiles_never_split(T, KT, G):
+    _, _, owner, items_of = schedule(T, KT, G, whole=True)
+    assert len(owner) == T * KT
+    items = [it for its in items_of.values() for it in its]
+    assert all(k0 == 0 and k1 == KT for _, k0, k1 in items)
+    assert sorted(t for t, _, _ in items) == list(range(T))
 
 
 def _fastdiv(d):
