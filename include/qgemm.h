@@ -117,7 +117,14 @@ typedef struct {
 /*
  * Compute config: what computation.
  *   gemm_type       QGEMM_GEMM_DENSE or QGEMM_GEMM_GROUPED
- *   batch_invariant reserved, must be 0
+ *   batch_invariant 0: the heuristic may split a tile's K range across CTAs,
+ *                   at boundaries that depend on the problem's tile count and
+ *                   so on m (or, grouped, on the rows of every expert).
+ *                   1: no tile is split (each output is one CTA's sum over
+ *                   k-tiles 0, 1, ... in order), so a row's result is
+ *                   bitwise the same whatever the other rows of the call are
+ *                   and whatever m is.  Slower at small m, where split-K is
+ *                   what fills the GPU.
  *   deterministic   0: when a tile's K range is split across CTAs, the fp32
  *                   partial sums are added into an L2-resident accumulator by
  *                   atomic reductions (fastest; the order of those fp32

@@ -34,10 +34,12 @@ class W4A16Linear:
     qweight int32 [E*K/8, N], scales [E*K/g, N] (act dtype), qzeros int32
     [E*K/g, N/8] or None: the standard format of ``include/qgemm.h``.
     gated=True: the N columns are an MoE gate half and up half and the layer
-    writes silu(gate) * up, [rows, N/2] (bf16 only)."""
+    writes silu(gate) * up, [rows, N/2] (bf16 only).  batch_invariant=True:
+    a row's result does not depend on the other rows of a call."""
 
     def __init__(self, qweight, scales, qzeros, n, k, group, act_dtype, num_experts=1,
-                 bias=None, tuning=None, deterministic=False, gated=False):
+                 bias=None, tuning=None, deterministic=False, gated=False,
+                 batch_invariant=False):
         self.n, self.k, self.group, self.num_experts = n, k, group, num_experts
         self.gated = gated
         self.n_out = n // 2 if gated else n
@@ -61,8 +63,10 @@ class W4A16Linear:
         self.tuning = tuning
         self.ws = Workspace(dev)
         det = 1 if deterministic else 0
-        self.dense = Q.compute_config(Q.QGEMM_GEMM_DENSE, deterministic=det)
-        self.grouped = Q.compute_config(Q.QGEMM_GEMM_GROUPED, deterministic=det)
+        inv = 1 if batch_invariant else 0
+        self.dense = Q.compute_config(Q.QGEMM_GEMM_DENSE, batch_invariant=inv, deterministic=det)
+        self.grouped = Q.compute_config(Q.QGEMM_GEMM_GROUPED, batch_invariant=inv,
+                                        deterministic=det)
 
     def __call__(self, a: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
         a = a.contiguous()
@@ -105,7 +109,7 @@ class W4A8Linear:
     W4A16Linear, silu(gate) * up of the two column halves, [rows, N/2])."""
 
     def __init__(self, codes, scales, n, k, num_experts=1, bias=None, tuning=None,
-                 deterministic=False, gated=False):
+                 deterministic=False, gated=False, batch_invariant=False):
         self.n, self.k, self.num_experts = n, k, num_experts
         self.gated = gated
         self.n_out = n // 2 if gated else n
@@ -122,8 +126,10 @@ class W4A8Linear:
         self.bias, self.tuning = bias, tuning
         self.ws = Workspace(dev)
         det = 1 if deterministic else 0
-        self.dense = Q.compute_config(Q.QGEMM_GEMM_DENSE, deterministic=det)
-        self.grouped = Q.compute_config(Q.QGEMM_GEMM_GROUPED, deterministic=det)
+        inv = 1 if batch_invariant else 0
+        self.dense = Q.compute_config(Q.QGEMM_GEMM_DENSE, batch_invariant=inv, deterministic=det)
+        self.grouped = Q.compute_config(Q.QGEMM_GEMM_GROUPED, batch_invariant=inv,
+                                        deterministic=det)
         self._act = {}
 
     def quantize(self, x: torch.Tensor):

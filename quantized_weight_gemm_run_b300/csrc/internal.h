@@ -161,8 +161,8 @@ cudaError_t launch_combine(const uint16_t* y2, const int32_t* inv_perm, const fl
 // thread's error message, and the bytes of a dense GEMM's workspace that must
 // be zero before a launch (status word and split-K counters) and in total.
 int set_last_error(int status, const char* message);
-int dense_workspace_bytes(const void* layer, const void* tuning, int64_t m, size_t* must_clear,
-                          size_t* total);
+int dense_workspace_bytes(const void* layer, const void* compute, const void* tuning, int64_t m,
+                          size_t* must_clear, size_t* total);
 
 bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     const uint64_t dims[3], const uint64_t strides_bytes[2],

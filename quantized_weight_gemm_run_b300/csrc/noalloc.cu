@@ -76,7 +76,7 @@ extern "C" qgemm_status qgemm_run_noalloc(const qgemm_layer_config* layer,
   if (m == 0)
     return qgemm_run(layer, compute, tuning, 0, a, a_scale, packed, bias, c, nullptr, 0, stream);
   size_t must_clear = 0, need = 0;
-  const int st = dense_workspace_bytes(layer, tuning, m, &must_clear, &need);
+  const int st = dense_workspace_bytes(layer, compute, tuning, m, &must_clear, &need);
   if (st != QGEMM_OK) return qgemm_status(st);
   if (need > kNoAllocScratchBytes) {
     char msg[256];

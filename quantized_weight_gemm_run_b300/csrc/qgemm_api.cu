@@ -140,8 +140,8 @@ static qgemm_status check_layer(const qgemm_layer_config* L) {
 static qgemm_status check_compute(const qgemm_compute_config* C, const qgemm_layer_config* L,
                                   bool grouped_call) {
   if (!C) return fail(QGEMM_ERR_INVALID_ARG, "compute config is NULL");
-  if (C->batch_invariant != 0)
-    return fail(QGEMM_ERR_UNSUPPORTED, "batch-invariant mode is not available");
+  if (C->batch_invariant != 0 && C->batch_invariant != 1)
+    return fail(QGEMM_ERR_INVALID_ARG, "batch_invariant must be 0 or 1");
   if (C->deterministic != 0 && C->deterministic != 1)
     return fail(QGEMM_ERR_INVALID_ARG, "deterministic must be 0 or 1");
   if (C->gemm_type != (grouped_call ? QGEMM_GEMM_GROUPED : QGEMM_GEMM_DENSE))
@@ -220,8 +220,13 @@ struct Plan {
   WorkspaceLayout ws;
 };
 
+// C may be null (the default compute config).
 static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_config* T,
-                              int64_t rows, bool grouped, Plan* P) {
+                              const qgemm_compute_config* C, int64_t rows, bool grouped,
+                              Plan* P) {
+  // whole tiles only: asked for by the tuning, or implied by batch
+  // invariance (a split's K boundaries depend on the tile count, so on M)
+  const bool whole = (T && T->split_k == 1) || (C && C->batch_invariant == 1);
   const int sms = device_sm_count();
   if (sms <= 0) return fail(QGEMM_ERR_CUDA, "no CUDA device");
   const int E = L->num_experts;
@@ -255,11 +260,11 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   if (!grouped) {
     const int64_t units = tiles_bound * kt;
     if (units < grid) grid = (int)(units > 0 ? units : 1);
-    if (T && T->split_k == 1 && tiles_bound < grid) grid = (int)(tiles_bound > 0 ? tiles_bound : 1);
+    if (whole && tiles_bound < grid) grid = (int)(tiles_bound > 0 ? tiles_bound : 1);
   }
   P->bt = bt;
   P->grid = grid;
-  P->whole_tiles = (T && T->split_k == 1) ? 1 : 0;
+  P->whole_tiles = whole ? 1 : 0;
   P->st = st;
   P->off_s = kTileBytes;                                   // inside a packed block
   P->off_z = kTileBytes + packed_scale_bytes(is_mx(L), st);
@@ -323,7 +328,7 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 // ------------------------------------------------------------ the W4A16 run
 
 static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_config* T,
-                              bool deterministic, bool grouped, const int32_t* offsets,
+                              const qgemm_compute_config* C, bool grouped, const int32_t* offsets,
                               int64_t rows, const void* a, const float* a_scale, const void* w,
                               const void* bias, void* c, void* workspace, size_t ws_bytes,
                               cudaStream_t stream) {
@@ -343,7 +348,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
       !aligned16(workspace))
     return fail(QGEMM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
   Plan P;
-  qgemm_status st = make_plan(L, T, rows, grouped, &P);
+  qgemm_status st = make_plan(L, T, C, rows, grouped, &P);
   if (st != QGEMM_OK) return st;
   if (!workspace || ws_bytes < P.ws.total)
     return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", P.ws.total,
@@ -396,7 +401,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.status = reinterpret_cast<int*>(ws);
   p.counters = reinterpret_cast<int*>(ws + P.ws.counters_off);
   p.partials = reinterpret_cast<float*>(ws + P.ws.partials_off);
-  p.deterministic = deterministic ? 1 : 0;
+  p.deterministic = C->deterministic ? 1 : 0;
   p.max_tiles = P.max_tiles;
   p.x_stages = P.g.x_stages;
   p.x_bytes = P.g.x_bytes;
@@ -449,13 +454,14 @@ int set_last_error(int status, const char* message) {
   return status;
 }
 
-int dense_workspace_bytes(const void* layer, const void* tuning, int64_t m, size_t* must_clear,
-                          size_t* total) {
+int dense_workspace_bytes(const void* layer, const void* compute, const void* tuning, int64_t m,
+                          size_t* must_clear, size_t* total) {
   const qgemm_layer_config* L = static_cast<const qgemm_layer_config*>(layer);
   qgemm_status st = check_layer(L);
   if (st != QGEMM_OK) return st;
   Plan P;
-  st = make_plan(L, static_cast<const qgemm_tuning_config*>(tuning), m > 0 ? m : 1, false, &P);
+  st = make_plan(L, static_cast<const qgemm_tuning_config*>(tuning),
+                 static_cast<const qgemm_compute_config*>(compute), m > 0 ? m : 1, false, &P);
   if (st != QGEMM_OK) return st;
   // the status word and tile counters start at zero, and so do the split-K
   // accumulators of the atomic reduction
@@ -523,7 +529,7 @@ qgemm_status qgemm_workspace_size(const qgemm_layer_config* layer,
   if (st != QGEMM_OK) return st;
   if (m < 0) return fail(QGEMM_ERR_INVALID_ARG, "m is negative");
   Plan P;
-  st = make_plan(layer, tuning, m > 0 ? m : 1, grouped, &P);
+  st = make_plan(layer, tuning, compute, m > 0 ? m : 1, grouped, &P);
   if (st != QGEMM_OK) return st;
   *bytes = P.ws.total;
   return ok();
@@ -544,7 +550,7 @@ qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_conf
   if (st != QGEMM_OK) return st;
   st = check_compute(compute, layer, false);
   if (st != QGEMM_OK) return st;
-  return run_w4a16(layer, tuning, compute->deterministic != 0, false, nullptr, m, a, a_scale,
+  return run_w4a16(layer, tuning, compute, false, nullptr, m, a, a_scale,
                    packed, bias, c, workspace,
                    workspace_bytes, static_cast<cudaStream_t>(stream));
 }
@@ -559,7 +565,7 @@ qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
   if (st != QGEMM_OK) return st;
   st = check_compute(compute, layer, true);
   if (st != QGEMM_OK) return st;
-  return run_w4a16(layer, tuning, compute->deterministic != 0, true, expert_offsets,
+  return run_w4a16(layer, tuning, compute, true, expert_offsets,
                    total_rows, a, a_scale, packed, bias, c,
                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
@@ -675,7 +681,7 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
     rec = std::string("rejected: ") + g_last_error;
   } else {
     Plan P;
-    st = make_plan(layer, nullptr, m > 0 ? m : 1, grouped, &P);
+    st = make_plan(layer, nullptr, compute, m > 0 ? m : 1, grouped, &P);
     if (st != QGEMM_OK) {
       rec = std::string("rejected: ") + g_last_error;
     } else {
@@ -685,14 +691,15 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
       snprintf(tmp, sizeof(tmp),
                "kernel=%s%s weights=%s group=%d act=%s out=%s n=%lld k=%lld "
                "m=%lld experts=%d block_tok=%d act_slots=%d weight_slots=%dx%d grid=%d smem=%d "
-               "workspace=%zu epilogue=%s "
+               "workspace=%zu epilogue=%s split=%s "
                "device=sm_103",
                is_mx(layer) ? "w4a8_tcgen05_mxf8f6f4_swapab" : "w4a16_tcgen05_swapab",
                grouped ? "_grouped" : "", wf[layer->weight_format], layer->group_size,
                dt[layer->act_dtype], dt[layer->out_dtype], (long long)layer->n,
                (long long)layer->k, (long long)m, layer->num_experts, P.bt, P.g.x_stages,
                P.g.w_stages, P.g.rw, P.grid, P.g.smem, P.ws.total,
-               layer->gated_act ? "silu_glu" : "plain");
+               layer->gated_act ? "silu_glu" : "plain",
+               P.whole_tiles ? "whole_tiles" : "stream_k");
       rec = tmp;
     }
   }

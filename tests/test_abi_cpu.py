@@ -117,3 +117,11 @@ def test_binding_structs_match_header(Q, name):
     import ctypes
     width = {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64}
     assert [t for _, t in got] == [width[t] for t, _ in fields]
+
+
+def test_compute_config_rejections_before_any_device_work(Q):
+    layer = _layer(Q)
+    for bad in (Q.compute_config(batch_invariant=2), Q.compute_config(deterministic=3),
+                Q.compute_config(gemm_type=7)):
+        st, _ = Q.qgemm_workspace_size(layer, bad, None, 16)
+        assert st == Q.QGEMM_ERR_INVALID_ARG, Q.last_error()
