@@ -146,7 +146,10 @@ typedef struct {
  *   block_tok  tokens per tile (the MMA N extent): 16, 32, 64 or 128
  *   stages     shared-memory pipeline depth (2 .. 16)
  *   max_ctas   upper bound on the persistent grid (<= number of SMs)
- *   split_k    1 = never split a tile's K range across CTAs; 0 = allowed
+ *   split_k    0 = the heuristic's choice of stream-K split; s = 1..64:
+ *              the tiles left over after the whole waves are each split
+ *              across min(s, grid / tiles left) CTAs at k-tile boundaries
+ *              (1 = never split a tile's K range)
  *   cta_pair   reserved, must be 0
  */
 typedef struct {

@@ -66,7 +66,7 @@ struct W4A16Params {
   int sg_shift;              // scale group of 32-wide k chunk j is j >> sg_shift
   int has_zp;
   int gated;                 // 1: SiLU-gated output from interleaved gate/up rows
-  int whole_tiles;           // 1: never split a tile's K range across CTAs
+  int split_cap;             // most CTAs sharing a tile's K range (0: no cap)
   const int* expert_offsets; // device [E+1] or null (dense)
   int num_experts;
   long long w_expert_stride; // bytes between experts' packed blocks
@@ -82,6 +82,7 @@ struct W4A16Params {
   int off_w, off_epi, off_bar;   // shared-memory offsets of the weight ring, staging, barriers
   int w_reuse;               // 1: several token tiles read each weight block (keep it in L2)
   int fix_smem;              // 1: the activation ring can hold a split tile's fp32 sum
+  int last_stage;            // 1: ... and, after it, 2 KB per 16-row chunk of a tile
   // dense schedule, computed on the host: tiles, whole waves, stream-K units,
   // CTAs sharing them, and dividers for the schedule's invariant divisors
   int sk_t, sk_w, sk_u, sk_gs;

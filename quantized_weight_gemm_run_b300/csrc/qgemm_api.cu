@@ -214,7 +214,7 @@ static bool make_geometry(int bt, int st, int has_zp, bool mx, int experts, int 
 
 struct Plan {
   int bt, grid, st, off_s, off_z;
-  int whole_tiles;   // 1: no tile's K range is split across CTAs
+  int split_cap;     // most CTAs sharing one tile's K range (0: no cap, 1: whole tiles)
   Geometry g;
   int64_t max_tiles;
   WorkspaceLayout ws;
@@ -224,9 +224,10 @@ struct Plan {
 static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_config* T,
                               const qgemm_compute_config* C, int64_t rows, bool grouped,
                               Plan* P) {
-  // whole tiles only: asked for by the tuning, or implied by batch
-  // invariance (a split's K boundaries depend on the tile count, so on M)
-  const bool whole = (T && T->split_k == 1) || (C && C->batch_invariant == 1);
+  // most CTAs per tile: from the tuning; 1 (whole tiles) under batch
+  // invariance, since a split's K boundaries depend on the tile count (so on M)
+  int cap = T ? T->split_k : 0;
+  if (C && C->batch_invariant == 1) cap = 1;
   const int sms = device_sm_count();
   if (sms <= 0) return fail(QGEMM_ERR_CUDA, "no CUDA device");
   const int E = L->num_experts;
@@ -235,8 +236,8 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   if (bt != 16 && bt != 32 && bt != 64 && bt != 128)
     return fail(QGEMM_ERR_UNSUPPORTED, "block_tok %d not in {16, 32, 64, 128}", bt);
   if (T && (T->cta_pair != 0)) return fail(QGEMM_ERR_UNSUPPORTED, "cta_pair is reserved");
-  if (T && T->split_k != 0 && T->split_k != 1)
-    return fail(QGEMM_ERR_INVALID_ARG, "split_k must be 0 or 1");
+  if (T && (T->split_k < 0 || T->split_k > 64))
+    return fail(QGEMM_ERR_INVALID_ARG, "split_k must be in [0, 64]");
   const int st = st_of(L->group_size);
   const int has_zp = L->zero_format == QGEMM_Z_UINT4;
   const int w_cap = (T && T->stages) ? T->stages : 16;
@@ -260,11 +261,12 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   if (!grouped) {
     const int64_t units = tiles_bound * kt;
     if (units < grid) grid = (int)(units > 0 ? units : 1);
-    if (whole && tiles_bound < grid) grid = (int)(tiles_bound > 0 ? tiles_bound : 1);
+    if (cap > 0 && tiles_bound * cap < grid)
+      grid = (int)(tiles_bound > 0 ? tiles_bound * cap : 1);
   }
   P->bt = bt;
   P->grid = grid;
-  P->whole_tiles = whole ? 1 : 0;
+  P->split_cap = cap;
   P->st = st;
   P->off_s = kTileBytes;                                   // inside a packed block
   P->off_z = kTileBytes + packed_scale_bytes(is_mx(L), st);
@@ -390,7 +392,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.sg_shift = L->group_size == 32 ? 0 : L->group_size == 64 ? 1 : 2;
   p.has_zp = has_zp ? 1 : 0;
   p.gated = L->gated_act != 0;
-  p.whole_tiles = P.whole_tiles;
+  p.split_cap = P.split_cap;
   p.expert_offsets = offsets;
   p.num_experts = E;
   p.w_expert_stride = (long long)(wb / E);
@@ -420,13 +422,24 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   {
     const int64_t T = grouped ? 0 : ((rows + P.bt - 1) / P.bt) * (L->n / kTileN);
     const int64_t G = P.grid;
-    const int64_t W = T / G;
+    int64_t W = T / G;
+    // uncapped: one whole wave fewer when tiles are left over, so that every
+    // CTA's stream-K range spans at least a tile and each split tile has two
+    // contributors, the later of which meets it as its first item
+    if (P.split_cap == 0 && W > 0 && T % G) --W;
     const int64_t U = (T - W * G) * p.kt;
     p.sk_t = (int)T;
     p.sk_w = (int)W;
     p.sk_u = (int)U;
-    // whole tiles only: the r remaining tiles go to r CTAs, one each
-    p.sk_gs = (int)(P.whole_tiles ? U / p.kt : (U < G ? U : G));
+    // the r remaining tiles' units go to min(G, U) CTAs; with a cap, each
+    // tile to exactly min(cap, G / r) CTAs (tile-aligned; 1: whole tiles)
+    int64_t gs = U < G ? U : G;
+    if (P.split_cap > 0 && U > 0) {
+      const int64_t r = U / p.kt;
+      const int64_t per = P.split_cap < G / r ? P.split_cap : G / r;
+      if (r * per < gs) gs = r * per;
+    }
+    p.sk_gs = (int)gs;
     p.div_kt = make_fastdiv((uint32_t)p.kt);
     p.div_nt = make_fastdiv((uint32_t)p.nt);
     p.div_gs = make_fastdiv(p.sk_gs > 0 ? (uint32_t)p.sk_gs : 1u);
@@ -435,6 +448,9 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   // a split tile's finisher copies the other contributors' fp32 sum (BT x 128)
   // into the activation ring when it is large enough
   p.fix_smem = (int64_t)P.g.x_stages * P.g.x_bytes >= (int64_t)P.bt * kTileN * 4;
+  // the last item's per-chunk staging: BT * 512 bytes of sums, then 4 warps x
+  // BT/16 chunks x 2 KB
+  p.last_stage = (int64_t)P.g.x_stages * P.g.x_bytes >= (int64_t)P.bt * 1024;
   p.wait_limit_ns = g_wait_limit_ns;
   // output [rows, n] of 16-bit values, written by 16-row x 32-column tensor
   // stores; a gated output [rows, n/2] by 16-row x 16-column ones
@@ -699,7 +715,7 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
                (long long)layer->k, (long long)m, layer->num_experts, P.bt, P.g.x_stages,
                P.g.w_stages, P.g.rw, P.grid, P.g.smem, P.ws.total,
                layer->gated_act ? "silu_glu" : "plain",
-               P.whole_tiles ? "whole_tiles" : "stream_k");
+               P.split_cap == 1 ? "whole_tiles" : "stream_k");
       rec = tmp;
     }
   }

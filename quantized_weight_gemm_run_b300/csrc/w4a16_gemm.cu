@@ -100,8 +100,14 @@ struct Schedule {
     G = gridDim.x;
     c = c_;
     W = T / G;
+    if (p.split_cap == 0 && W > 0 && T % G) --W;   // stream-K over the last two waves
     U = (T - W * G) * KT;
-    Gs = p.whole_tiles ? U / KT : (U < G ? U : G);   // whole tiles: one per CTA
+    Gs = U < G ? U : G;
+    if (p.split_cap > 0 && U > 0) {   // each remaining tile to min(cap, G / r) CTAs
+      const int r = U / KT;
+      const int per = min(p.split_cap, G / r);
+      Gs = min(Gs, r * per);
+    }
     fast = false;
     dkt = p.div_kt;
     start();
@@ -182,13 +188,6 @@ __device__ __forceinline__ void grid_dependency_wait() {
 
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Fire-and-forget fp32 vector reduction into global memory (performed at L2).
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a),
-               "f"(b), "f"(c), "f"(d)
-               : "memory");
 }
 
 __device__ __forceinline__ void red_release_add_gpu(int* addr, int v) {
@@ -758,6 +757,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // expert); its rows are stored one by one instead.
     uint16_t* stg = epi_stage + q * (2 * 16 * 32);
     int sbuf = 0;
+    // The CTA's last item (the end of the kernel's critical path) stages each
+    // 16-row chunk in its own 2 KB slot of the then idle activation ring,
+    // after the finisher's copied sums, so no chunk waits for an earlier
+    // store or reduction to finish reading its buffer.
+    uint8_t* last_stage = x_base + BT * 512 + q * (BT / 16) * 2048;
+    bool last = false;
     auto emit = [&](const TileCoord<BT>& tc, int m0, const float (&f)[16], float bias) {
       uint16_t o[16];
 #pragma unroll
@@ -791,8 +796,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           const int r0 = odd * 8, hcol = lane >> 1;
           if (!GROUPED || valid >= 16) {
-            uint16_t* sb = stg + sbuf * (16 * 32);   // 16 rows x 16 columns
-            if (lane == 0) bulk_wait_group_read<1>();
+            uint16_t* sb = last ? reinterpret_cast<uint16_t*>(last_stage + (m0 / 16) * 2048)
+                                : stg + sbuf * (16 * 32);   // 16 rows x 16 columns
+            if (lane == 0 && !last) bulk_wait_group_read<1>();
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -819,8 +825,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
       }
       if (!GROUPED || valid >= 16) {
-        uint16_t* sb = stg + sbuf * (16 * 32);
-        if (lane == 0) bulk_wait_group_read<1>();   // this buffer's previous store has read it
+        uint16_t* sb = last ? reinterpret_cast<uint16_t*>(last_stage + (m0 / 16) * 2048)
+                            : stg + sbuf * (16 * 32);
+        if (lane == 0 && !last) bulk_wait_group_read<1>();   // the buffer's previous store read it
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 16; ++i) sb[i * 32 + lane] = o[i];
@@ -842,13 +849,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     while (sched.next(wi)) {
       const TileCoord<BT> tc = coords(wi.tile);
       const bool whole = (wi.k0 == 0 && wi.k1 == p.kt);
+      bool final_item;
+      {
+        Schedule peek = sched;
+        WorkItem nx;
+        final_item = !peek.next(nx);
+      }
       if (!mbar_wait(&acc_full[acc], accphase, abort_flag, p.status, lim, kStatusTimeout)) break;
+      // after the last item's accumulator is full, every MMA (and so every
+      // read of the activation ring) of this CTA has completed
+      last = p.last_stage && final_item;
       tc_fence_after();
       const int n = packed_source_col(tc.nt, col, p.n, p.gated);
       const float bias = p.bias ? from_out<FP16>(p.bias[(long long)tc.e * p.n + n]) : 0.f;
       const uint32_t tbase = tmem_base + lane_addr + kAccCol + acc * BT;
-      // Split tiles.  Partial tiles are column-major [col][BT] (this thread's
-      // column contiguous), so a 32-column quadrant is one contiguous block.
+      // Split tiles.  A tile's fp32 accumulator is four quadrant blocks of
+      // [BT rows][32 columns]: each block is contiguous (one bulk copy for the
+      // finisher) and each 8-row slice of it is one 1 KB bulk reduction.
       const int tl = wi.tile - sched.W * sched.G;
       const int u_start = tl * p.kt;
       const int c_first = whole ? 0 : sched.cta_of_unit(u_start);
@@ -858,9 +875,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const bool finisher = !whole && !p.deterministic && c_first == (int)blockIdx.x;
       if (whole || (!p.deterministic && !finisher)) {
         // whole tile: output; atomic-mode contributor: add into the tile's
-        // accumulator.  Only 16-row chunks holding output rows are read, so
-        // rows past the end stay untouched (zero) in the accumulator.
-        float* acc_col = whole ? nullptr : p.partials + (long long)tl * (BT * kTileN) + col * BT;
+        // accumulator, 8 rows x 32 columns (1 KB) per bulk reduction through
+        // the staging buffers.  Only slices holding output rows are added, so
+        // rows past the end stay zero in the accumulator.
+        float* quad_acc = p.partials + (long long)tl * (BT * kTileN) + q * 32 * BT;
 #pragma unroll 1
         for (int mc = 0; mc < BT / 16 && mc * 16 < tc.rows; ++mc) {
           uint32_t v[16];
@@ -872,19 +890,35 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             emit(tc, mc * 16, f, bias);
           } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              red_add_v4(acc_col + mc * 16 + 4 * i, __uint_as_float(v[4 * i]),
-                         __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
-                         __uint_as_float(v[4 * i + 3]));
+            for (int h = 0; h < 2; ++h) {
+              if (mc * 16 + h * 8 >= tc.rows) break;
+              float* sb = last ? reinterpret_cast<float*>(last_stage + mc * 2048 + h * 1024)
+                               : reinterpret_cast<float*>(stg + sbuf * (16 * 32));
+              if (lane == 0 && !last) bulk_wait_group_read<1>();   // the buffer's previous op read it
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 8; ++i) sb[i * 32 + lane] = __uint_as_float(v[8 * h + i]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                bulk_reduce_add_f32(quad_acc + (mc * 16 + h * 8) * 32, sb, 8 * 32 * 4);
+                bulk_commit_group();
+              }
+              sbuf ^= 1;
+            }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&acc_empty[acc]);
-          // the warp's reductions (ordered before this by the warp barrier)
-          // become visible before the count: release
-          if (!whole) red_release_add_gpu(counter, 1);
+          if (!whole) {
+            // the reductions complete, then are ordered before the count
+            // (async proxy -> generic proxy -> release)
+            bulk_wait_group_all();
+            fence_proxy_async_global();
+            red_release_add_gpu(counter, 1);
+          }
         }
       } else if (finisher) {
         // Atomic-mode finisher: the CTA holding the tile's first k-tiles,
@@ -894,9 +928,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // quadrant (into the activation ring, idle after the last item's
         // MMAs) or read directly, added, written out, and the accumulator
         // and counter are left at zero for the next launch.
-        Schedule peek = sched;
-        WorkItem nx;
-        const bool via_smem = p.fix_smem && !peek.next(nx);
+        const bool via_smem = p.fix_smem && final_item;
         float* quad = p.partials + (long long)tl * (BT * kTileN) + q * 32 * BT;
         bool ok = true;
         if (lane == 0) {
@@ -915,7 +947,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
         __syncwarp();   // orders every lane's reads after lane 0's acquire
-        const float* sum_col = quad + lane * BT;
+        const float* sum_col = quad + lane;   // row m of this column at [m * 32]
         if (ok && via_smem) {
           float* fsm = reinterpret_cast<float*>(x_base) + q * 32 * BT;
           if (lane == 0) {
@@ -929,23 +961,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             volatile int no_abort = 0;
             mbar_wait(&fix_bar[q], 0, &no_abort, nullptr, 100000000ull, 0);
           }
-          sum_col = fsm + lane * BT;
+          sum_col = fsm + lane;
         }
         if (ok) {
 #pragma unroll 1
           for (int mc = 0; mc < BT / 16 && mc * 16 < tc.rows; ++mc) {
             uint32_t v[16];
             tmem_ld16_wait(tbase + mc * 16, v);
-            const float4* s4 = reinterpret_cast<const float4*>(sum_col + mc * 16);
+            const float* s1 = sum_col + mc * 16 * 32;
             float f[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float4 a4 = via_smem ? s4[j] : __ldcg(s4 + j);
-              f[4 * j] = __uint_as_float(v[4 * j]) + a4.x;
-              f[4 * j + 1] = __uint_as_float(v[4 * j + 1]) + a4.y;
-              f[4 * j + 2] = __uint_as_float(v[4 * j + 2]) + a4.z;
-              f[4 * j + 3] = __uint_as_float(v[4 * j + 3]) + a4.w;
-            }
+            for (int i = 0; i < 16; ++i)
+              f[i] = __uint_as_float(v[i]) + (via_smem ? s1[i * 32] : __ldcg(s1 + i * 32));
             emit(tc, mc * 16, f, bias);
           }
           // leave the quadrant's accumulator zeroed (coalesced) and the count reset

@@ -11,10 +11,17 @@ import itertools
 import pytest
 
 
-def schedule(T, KT, G, whole=False):
+def schedule(T, KT, G, whole=False, cap=0):
     W = T // G
+    if whole:
+        cap = 1
+    if cap == 0 and W > 0 and T % G:
+        W -= 1          # stream-K over the last two waves
     U = (T - W * G) * KT
-    Gs = U // KT if whole else (U if U < G else G)
+    Gs = U if U < G else G
+    if cap and U:
+        r = U // KT
+        Gs = min(Gs, r * min(cap, G // r))
 
     def sk_begin(c):
         return (c * U) // Gs
@@ -60,12 +67,43 @@ def test_schedule_partition(T, KT, G):
 
 @pytest.mark.parametrize("T,KT,G", list(itertools.product(
     [1, 3, 149, 150, 300, 4096], [1, 3, 32], [1, 7, 148])))
+def test_two_wave_stream_k_has_two_contributors_per_split_tile(T, KT, G):
+    """With at least one whole wave and tiles left over, the stream-K region
+    spans more than G tiles, so every split tile has exactly two contributors
+    and the later one meets it as its first item."""
+    W, cta_of_unit, owner, items_of = schedule(T, KT, G)
+    if T // G == 0 or T % G == 0 or KT == 1:
+        return
+    for t in range(W * G, T):
+        owners = sorted({owner[(t, k)] for k in range(KT)})
+        assert len(owners) <= 2
+        if len(owners) == 2:
+            later = owners[1]
+            first_split = next(it for it in items_of[later] if not (it[1] == 0 and it[2] == KT))
+            assert first_split[0] == t
+
+
+@pytest.mark.parametrize("T,KT,G", list(itertools.product(
+    [1, 3, 149, 150, 300, 4096], [1, 3, 32], [1, 7, 148])))
 def test_schedule_whole_tiles_never_split(T, KT, G):
     _, _, owner, items_of = schedule(T, KT, G, whole=True)
     assert len(owner) == T * KT
     items = [it for its in items_of.values() for it in its]
     assert all(k0 == 0 and k1 == KT for _, k0, k1 in items)
     assert sorted(t for t, _, _ in items) == list(range(T))
+
+
+@pytest.mark.parametrize("T,KT,G,cap", list(itertools.product(
+    [1, 3, 64, 149, 256, 300], [1, 3, 32, 64], [7, 148], [2, 3, 4, 64])))
+def test_schedule_split_cap(T, KT, G, cap):
+    """With a cap, every leftover tile is shared by exactly min(cap, G/r, KT)
+    CTAs (r leftover tiles)."""
+    W, _, owner, _ = schedule(T, KT, G, cap=cap)
+    assert len(owner) == T * KT
+    r = T - W * G
+    for t in range(W * G, T):
+        owners = {owner[(t, k)] for k in range(KT)}
+        assert len(owners) == min(cap, G // r, KT)
 
 
 def _fastdiv(d):
