@@ -15,18 +15,18 @@
 
 namespace qg {
 
-// Programmatic dependent launch for the auxiliary kernels: each lets the next
-// grid on the stream begin launching at once (its start-up overlaps this
-// grid), and waits for the previous grid to complete, memory included,
-// before it touches memory (a no-op when it was launched without the
-// attribute).  A grid completes only after its own wait, so the chain keeps
-// stream order.  Only the activation quantization is launched with the
-// attribute: it lets the W4A8 GEMM's start-up overlap it.  The MoE kernels
-// measured slightly slower (0.5-1.5 % per layer on B300) when their own
-// launches overlapped the previous grid, so they launch plainly.
-__device__ __forceinline__ void pdl_enter() {
+// Programmatic dependent launch for the auxiliary kernels.  Each waits for
+// the previous grid on the stream to complete, memory included, before it
+// touches memory (a no-op when launched without the attribute).  The
+// activation quantization also lets the next grid begin launching at once,
+// so the W4A8 GEMM's start-up (barriers, tensor memory, the first weight
+// copy) overlaps it; it is launched with the attribute itself.  The MoE
+// kernels neither overlap their own launch nor let the next grid start
+// early: both measured 0.5-1.5 % slower per layer on B300.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <typename... KArgs, typename... Args>
@@ -50,7 +50,8 @@ static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cud
 // row), code = e4m3_rn_satfinite(x / s) with an IEEE fp32 divide.
 __global__ void act_quant_fp8_kernel(const uint16_t* __restrict__ x, int k,
                                      uint8_t* __restrict__ a8, float* __restrict__ scale) {
-  pdl_enter();
+  pdl_trigger();
+  pdl_wait();
   const long long row = blockIdx.x;
   const uint16_t* xr = x + row * k;
   float amax = 0.f;
@@ -109,7 +110,7 @@ __device__ __forceinline__ int sort_bucket(const int32_t* ids, int i, int E) {
 __global__ void __launch_bounds__(1024) moe_count_kernel(const int32_t* __restrict__ ids,
                                                          int n_slots, int E,
                                                          int32_t* __restrict__ hist) {
-  pdl_enter();
+  pdl_wait();
   constexpr int NB = kMaxPermuteExperts + 1;
   __shared__ int h[NB];
   const int B = E + 1;
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(1024) moe_place_kernel(const int32_t* __restri
                                                          int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ perm,
                                                          int32_t* __restrict__ inv_perm) {
-  pdl_enter();
+  pdl_wait();
   constexpr int NB = kMaxPermuteExperts + 1;
   __shared__ int cnt[32][NB];   // per-warp counts, then per-warp running bases
   __shared__ int start[NB];     // this block's first place per bucket
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(1024) moe_place_kernel(const int32_t* __restri
 // a_perm[r] = a[perm[r] / topk]: one warp per row, 16-byte vectors.
 __global__ void gather_rows_kernel(const uint4* __restrict__ a, const int32_t* __restrict__ perm,
                                    uint4* __restrict__ a_perm, int rows, int topk, int vecs) {
-  pdl_enter();
+  pdl_wait();
   const int warps = blockDim.x >> 5;
   const int r = blockIdx.x * warps + (threadIdx.x >> 5);
   if (r >= rows) return;
@@ -244,7 +245,7 @@ cudaError_t launch_moe_permute(const int32_t* ids, int64_t t, int topk, int e, i
 // silu(g) = g / (1 + exp(-g)).  Eight elements per thread.
 __global__ void silu_mul_kernel(const uint16_t* __restrict__ gu, uint16_t* __restrict__ h,
                                 long long rows, int inter) {
-  pdl_enter();
+  pdl_wait();
   const int per_row = inter / 8;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= rows * per_row) return;
@@ -278,7 +279,7 @@ cudaError_t launch_silu_mul(const uint16_t* gu, int64_t rows, int64_t inter, uin
 __global__ void combine_kernel(const uint16_t* __restrict__ y2, const int32_t* __restrict__ inv_perm,
                                const float* __restrict__ w, uint16_t* __restrict__ y, int topk,
                                int hidden) {
-  pdl_enter();
+  pdl_wait();
   const int t = blockIdx.x;
   const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
   if (c >= hidden) return;
