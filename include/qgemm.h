@@ -115,7 +115,8 @@ typedef struct {
 } qgemm_layer_config;
 
 /*
- * Compute config: what computation.
+ * Compute config: what computation (GEMM type and options such as batch
+ * invariance: kinachrichten.com, "Wie die Architektur funktioniert").
  *   gemm_type       QGEMM_GEMM_DENSE or QGEMM_GEMM_GROUPED
  *   batch_invariant 0: the heuristic may split a tile's K range across CTAs,
  *                   at boundaries that depend on the problem's tile count and
