@@ -39,6 +39,17 @@ MXFP4 tiled layout (same tiling):
     exponents of row n = 128 nt + r for k = 128 kt + [0, 32), [32, 64),
     [64, 96), [96, 128) in that order.
 
+NVFP4 layout (same tiling; block size 8192 + 2048 bytes):
+
+  weights: the MXFP4 code vectors above (32 consecutive codes of one row per
+    16-byte vector, standard nibble order).
+  scales: the W4A16 scale stream with g = 16 (ST = 8): word sg * 128 + r is
+    the e4m3 block scale of row r for k = 128 kt + 16 sg .. + 15, written as
+    the activation dtype's bit pattern (every e4m3 value is exact in bf16 and
+    fp16, so this re-encodes without changing the value).
+  tensor scales: after the last expert's blocks, one fp32 per expert, padded
+    to a multiple of 16 bytes.
+
 Gated layers (an MoE expert's gate|up projection, N = 2I: gate columns
 [0, I), up columns [I, 2I)): the SiLU gate multiplies gate column i by up
 column I + i, so the pack places the pair in one tile, on neighbouring rows:
@@ -202,6 +213,24 @@ def packed_w4(q, s_bits, z, g: int, signed: bool) -> np.ndarray:
     if z is not None:
         pieces.append((tiled_zeros(z, g, k), 128 * st))
     return interleave_blocks(*pieces)
+
+
+def packed_nvfp4(codes_nk, sb_nk, adt: str) -> np.ndarray:
+    """Standard NVFP4 codes [N, K/2] and e4m3 scales [N, K/16] of one matrix ->
+    its packed blocks (the tensor-scale tail is ``nvfp4_tail``)."""
+    from . import codecs
+    sb = np.asarray(sb_nk, dtype=np.uint8)
+    k = sb.shape[1] * 16
+    bits = codecs.dtype_bits(adt, codecs.decode_e4m3(sb)).T     # [K/16, N]
+    return interleave_blocks((tiled_mxfp4_weights(codes_nk), 8192),
+                             (tiled_scales(bits, 16, k), 2048))
+
+
+def nvfp4_tail(tensor_scales) -> np.ndarray:
+    """The per-expert fp32 tensor scales as bytes, padded to 16-byte multiples."""
+    t = np.asarray(tensor_scales, dtype=np.float32).reshape(-1)
+    pad = (-t.size) % 4
+    return np.concatenate([t, np.zeros(pad, dtype=np.float32)]).view(np.uint8)
 
 
 def packed_mxfp4(codes_nk, b_nk) -> np.ndarray:

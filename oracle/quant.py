@@ -32,6 +32,20 @@ MXFP4 (one e8m0 exponent per 32 consecutive k of one column; OCP MX v1.0):
     c    = e2m1_rne_saturating(W / 2^E)
     w^   = e2m1(c) * 2^E          exact in float64
 
+NVFP4 (the pages name NVFP4 as a format whose number format and scaling
+differ from INT4's: kinachrichten.com, "Warum quantisierte Kernel wichtig
+sind"; they give no definition, so the common one is read: e2m1 elements, one
+e4m3 scale per 16 consecutive k of one column, one fp32 scale per tensor):
+    t    = fp32(max |W| / (6 * 448))   (6 = e2m1 max, 448 = e4m3 max;
+                                        1 when W is all zero)
+    s    = e4m3_rne_satfinite(amax / (6 t))   over the block of 16
+    c    = e2m1_rne_saturating(W / (s t))     (all 0 when s == 0)
+    w^   = e2m1(c) * s * t        exact in float64; the kernel feeds the
+                                  exact product e2m1(c) * s (at most five
+                                  significant bits, so exact in bf16 and
+                                  fp16) to the tensor core and multiplies
+                                  the fp32 sum by t
+
 ``rint`` rounds half to even.  The product (q - z) * s is exact in float64
 (a 5-bit integer times an 8- or 11-bit significand), so w^ is rounded once.
 
@@ -45,6 +59,8 @@ Standard-format encoding (the tensors the library's pack entry point takes):
     MXFP4:  codes uint8 [N, K/2]: byte (n, j) holds k = 2j in the low nibble
             and k = 2j + 1 in the high nibble; e2m1 bits are s|e1 e0|m.
             scales uint8 e8m0 [N, K/32].
+    NVFP4:  codes as MXFP4; scales uint8 e4m3 [N, K/16]; the tensor scale
+            t is one fp32 per matrix (per expert).
 """
 
 from __future__ import annotations
@@ -106,6 +122,25 @@ def quantize_mxfp4(w):
     return codes.reshape(w.shape).astype(np.uint8), b.astype(np.uint8)
 
 
+def quantize_nvfp4(w):
+    """NVFP4 quantization along K in blocks of 16.  Returns (codes uint8 [K, N]
+    e2m1 nibbles, sb uint8 [K/16, N] e4m3 block-scale bytes, t float)."""
+    w = np.asarray(w, dtype=np.float64)
+    amax_t = float(np.max(np.abs(w))) if w.size else 0.0
+    t = float(np.float32(amax_t / (6.0 * 448.0))) if amax_t > 0 else 1.0
+    if t == 0.0:                                   # underflow of the fp32 tensor scale
+        t = 1.0
+    wg = _grouped(w, 16)
+    amax = np.max(np.abs(wg), axis=1)
+    s = codecs.e4m3(amax / (6.0 * t))
+    sb = codecs.encode_e4m3(s)
+    denom = s * t                                  # exact: two short significands
+    scaled = wg / np.where(denom > 0, denom, 1.0)[:, None, :]
+    codes = codecs.encode_e2m1(scaled)
+    codes = np.where((denom > 0)[:, None, :], codes, 0)
+    return codes.reshape(w.shape).astype(np.uint8), sb.astype(np.uint8), t
+
+
 # ------------------------------------------------------------ dequantization
 
 def dequant_int(q, s, z, g: int, adt: str) -> np.ndarray:
@@ -137,6 +172,17 @@ def dequant_mxfp4(codes, b) -> np.ndarray:
 
 
 # ------------------------------------------------------------ standard format
+
+def nvfp4_operand(codes, sb) -> np.ndarray:
+    """e2m1(codes[k, n]) * e4m3(sb[k/16, n]): the exact value the kernels feed
+    to the tensor core (the tensor scale multiplies the fp32 sum)."""
+    return codecs.decode_e2m1(codes) * np.repeat(codecs.decode_e4m3(sb), 16, axis=0)
+
+
+def dequant_nvfp4(codes, sb, t: float) -> np.ndarray:
+    """w^[k, n] = e2m1(codes[k, n]) * e4m3(sb[k/16, n]) * t, exact in float64."""
+    return nvfp4_operand(codes, sb) * float(t)
+
 
 def pack_int4_kn(q, signed: bool) -> np.ndarray:
     """Codes [K, N] -> qweight int32 [K/8, N], k = 8j + i in bits [4i, 4i+4)."""
@@ -207,6 +253,25 @@ def unpack_mxfp4(packed_nk, b_nk):
     c[:, 0::2] = p & 0xF
     c[:, 1::2] = p >> 4
     return np.ascontiguousarray(c.T), np.ascontiguousarray(np.asarray(b_nk, dtype=np.uint8).T)
+
+
+def pack_nvfp4(codes_kn, sb_kn):
+    """NVFP4 codes [K, N] and e4m3 scales [K/16, N] -> (uint8 [N, K/2] with the
+    even k in the low nibble, uint8 [N, K/16])."""
+    c = np.asarray(codes_kn, dtype=np.uint8).T
+    packed = (c[:, 0::2] & 0xF) | ((c[:, 1::2] & 0xF) << 4)
+    return np.ascontiguousarray(packed.astype(np.uint8)), np.ascontiguousarray(
+        np.asarray(sb_kn, dtype=np.uint8).T)
+
+
+def unpack_nvfp4(packed_nk, sb_nk):
+    """Inverse of ``pack_nvfp4``: -> (codes [K, N], sb [K/16, N])."""
+    p = np.asarray(packed_nk, dtype=np.uint8)
+    n, kh = p.shape
+    codes = np.empty((n, 2 * kh), dtype=np.uint8)
+    codes[:, 0::2] = p & 0xF
+    codes[:, 1::2] = p >> 4
+    return codes.T.copy(), np.asarray(sb_nk, dtype=np.uint8).T.copy()
 
 
 def scales_bits(s, sdt: str) -> np.ndarray:

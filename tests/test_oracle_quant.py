@@ -16,9 +16,14 @@ def test_dequant_golden_cases():
             got = quant.dequant_int(np.array([[int(q)]]), np.array([[float(s)]]),
                                     np.array([[int(z)]]), 1, adt)
             assert float(got[0, 0]) == float(want), row
-        else:
+        elif row[0] == "mx":
             _, code, b, want = row
             got = quant.dequant_mxfp4(np.full((32, 1), int(code)), np.array([[int(b)]]))
+            assert float(got[0, 0]) == float(want), row
+        else:
+            _, code, sbyte, t, want = row
+            got = quant.dequant_nvfp4(np.full((16, 1), int(code)),
+                                      np.array([[int(sbyte, 16)]]), float(t))
             assert float(got[0, 0]) == float(want), row
 
 
@@ -302,3 +307,117 @@ def test_gated_packed_buffer_scalar_spec():
         sbyte = base + 8192 + 2 * r
         assert int(buf[sbyte]) | (int(buf[sbyte + 1]) << 8) == sb[kk // gsize, src]
         assert buf[base + 8192 + 256 + r] == z[kk // gsize, src]
+
+
+# ------------------------------------------------------------------ NVFP4
+
+def test_nvfp4_round_trip_on_the_grid():
+    """Weights built exactly on the NVFP4 grid (a +-6 element in every block,
+    one block with scale 448 to fix the tensor scale) quantize back to the
+    codes, scales and tensor scale they were built from."""
+    g = np.random.default_rng(41)
+    k, n = 128, 32
+    t = 2.0 ** -7
+    sb = g.choice(np.arange(0x08, 0x7F), size=(k // 16, n)).astype(np.uint8)   # normal e4m3
+    sb[0, 0] = 0x7E                                                            # 448
+    codes = g.integers(0, 16, (k, n)).astype(np.uint8)
+    codes[0::16, :] = 7                                                        # +6 in each block
+    w = quant.dequant_nvfp4(codes, sb, t)
+    c2, sb2, t2 = quant.quantize_nvfp4(w)
+    assert t2 == t
+    assert np.array_equal(sb2, sb)
+    # -0 and +0 decode alike; compare values
+    assert np.array_equal(codecs.decode_e2m1(c2), codecs.decode_e2m1(codes))
+
+
+def test_nvfp4_error_bound_and_ranges():
+    """Random weights: codes and scales in range, block scales <= 448, and
+    |w - w^| <= s * t (one grid unit of the block: e2m1's largest gap is 2)."""
+    g = np.random.default_rng(42)
+    w = g.standard_normal((512, 64)) * 0.03
+    w[::7, 5] *= 40.0                                     # a few large outliers
+    codes, sb, t = quant.quantize_nvfp4(w)
+    assert codes.max() <= 15 and sb.max() <= 0x7E
+    s = codecs.decode_e4m3(sb)
+    assert np.all(s >= 0) and np.all(s <= 448)
+    err = np.abs(w - quant.dequant_nvfp4(codes, sb, t))
+    bound = np.repeat(s * t, 16, axis=0)
+    assert np.all(err <= bound * (1 + 1e-12))
+    assert t == float(np.float32(np.max(np.abs(w)) / 2688.0))
+
+
+def test_nvfp4_zero_blocks_and_zero_matrix():
+    w = np.zeros((32, 16))
+    w[16:, 3] = 2688.0 * 2.0 ** -10          # t = 2^-10 exactly, s = 448, code 6
+    codes, sb, t = quant.quantize_nvfp4(w)
+    assert np.all(codes[:16] == 0) and np.all(sb[0] == 0)
+    assert np.array_equal(quant.dequant_nvfp4(codes, sb, t), w)
+    codes, sb, t = quant.quantize_nvfp4(np.zeros((16, 4)))
+    assert t == 1.0 and not codes.any() and not sb.any()
+
+
+def test_nvfp4_operand_is_exact_in_both_16_bit_types():
+    """Every e2m1 x e4m3 product is a bf16 and an fp16 value (<= 5 significant
+    bits, magnitude <= 2688, >= 2^-10): the kernel's dequant needs no rounding."""
+    codes = np.repeat(np.arange(16, dtype=np.uint8), 16)[:, None]               # [256, 1]
+    for sbyte in range(0x00, 0x7F):
+        sb = np.full((16, 1), sbyte, dtype=np.uint8)
+        v = quant.nvfp4_operand(codes, sb)
+        codecs.bf16_bits(v)
+        codecs.fp16_bits(v)
+
+
+def test_nvfp4_brute_force_dequant():
+    g = np.random.default_rng(43)
+    codes = g.integers(0, 16, (32, 3)).astype(np.uint8)
+    sb = g.integers(0, 0x7F, (2, 3)).astype(np.uint8)
+    t = 0.375
+    got = quant.dequant_nvfp4(codes, sb, t)
+    for kk in range(32):
+        for nn in range(3):
+            c = int(codes[kk, nn])
+            mag = [0, 0.5, 1, 1.5, 2, 3, 4, 6][c & 7]
+            e4 = int(sb[kk // 16, nn])
+            e, m = (e4 >> 3) & 15, e4 & 7
+            sv = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+            want = (-mag if c & 8 else mag) * sv * t
+            assert got[kk, nn] == want
+
+
+def test_nvfp4_standard_pack_round_trip():
+    g = np.random.default_rng(44)
+    codes = g.integers(0, 16, (64, 8)).astype(np.uint8)
+    sb = g.integers(0, 0x7F, (4, 8)).astype(np.uint8)
+    cn, sn = quant.pack_nvfp4(codes, sb)
+    assert cn.shape == (8, 32) and sn.shape == (8, 4)
+    assert (cn[2, 5] & 0xF) == codes[10, 2] and (cn[2, 5] >> 4) == codes[11, 2]
+    c2, s2 = quant.unpack_nvfp4(cn, sn)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, sb)
+
+
+@pytest.mark.parametrize("adt", ["bf16", "fp16"])
+def test_packed_nvfp4_scalar_spec(adt):
+    """Block (nt, kt) is [codes 8192][scales 2048]: the codes as MXFP4's, the
+    scale of (row r, 16-k group sg) at word sg * 128 + r in the activation
+    dtype's bits; the tail holds the fp32 tensor scales."""
+    g = np.random.default_rng(45)
+    n, k = 256, 256
+    codes = g.integers(0, 256, (n, k // 2)).astype(np.uint8)
+    sb = g.integers(0, 0x7F, (n, k // 16)).astype(np.uint8)
+    buf = layout.packed_nvfp4(codes, sb, adt)
+    kt_count = k // 128
+    assert buf.size == (n // 128) * kt_count * 10240
+    for _ in range(1500):
+        nn, kk = int(g.integers(0, n)), int(g.integers(0, k))
+        nt, nl = divmod(nn, 128)
+        kt, kl = divmod(kk, 128)
+        qd, t = divmod(nl, 32)
+        j, rr = divmod(kl, 32)
+        base = (nt * kt_count + kt) * 10240
+        byte = int(buf[base + ((qd * 4 + j) * 32 + t) * 16 + rr // 2])
+        assert ((byte >> 4) if rr % 2 else (byte & 0xF)) == (codes[nn, kk // 2] >> (4 * (kk % 2))) & 0xF
+        word = base + 8192 + 2 * ((kl // 16) * 128 + nl)
+        bits = int(buf[word]) | (int(buf[word + 1]) << 8)
+        assert codecs.dtype_from_bits(adt, np.array([bits]))[0] == codecs.decode_e4m3(sb[nn, kk // 16])
+    tail = layout.nvfp4_tail([0.5, 2.0, -1.0])
+    assert tail.size == 16 and list(tail.view(np.float32)) == [0.5, 2.0, -1.0, 0.0]
