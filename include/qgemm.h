@@ -62,9 +62,9 @@ typedef enum {
 } qgemm_status;
 
 /* weight formats */
-enum { QGEMM_W_INT4_SYM = 0, QGEMM_W_UINT4_ZP = 1, QGEMM_W_MXFP4 = 2 };
+enum { QGEMM_W_INT4_SYM = 0, QGEMM_W_UINT4_ZP = 1, QGEMM_W_MXFP4 = 2, QGEMM_W_NVFP4 = 3 };
 /* scale formats */
-enum { QGEMM_S_FP16 = 0, QGEMM_S_BF16 = 1, QGEMM_S_E8M0 = 2 };
+enum { QGEMM_S_FP16 = 0, QGEMM_S_BF16 = 1, QGEMM_S_E8M0 = 2, QGEMM_S_E4M3 = 3 };
 /* zero-point formats */
 enum { QGEMM_Z_NONE = 0, QGEMM_Z_UINT4 = 1 };
 /* activation / output data types */
@@ -79,9 +79,13 @@ enum { QGEMM_ACT_NONE = 0, QGEMM_ACT_SILU_GLU = 1 };
  * layer has num_experts = 1.
  *   n, k          output features, input features (C[M,N] = A[M,K] W[K,N])
  *   group_size    K-extent of one scale (W4A16: 32, 64 or a multiple of 128
- *                 dividing K; MXFP4: must be 32)
+ *                 dividing K; MXFP4: must be 32; NVFP4: must be 16)
  *   weight_format QGEMM_W_*;  scale_format QGEMM_S_*;  zero_format QGEMM_Z_*
- *   act_dtype     activation dtype: QGEMM_FP16 / QGEMM_BF16 (W4A16) or
+ *   act_dtype     activation dtype: QGEMM_FP16 / QGEMM_BF16 (W4A16, and
+ *                 NVFP4 weights: e2m1 codes, one e4m3 scale per 16 k, one
+ *                 fp32 tensor scale; the pages name NVFP4 as a format whose
+ *                 number format and scaling differ from INT4's,
+ *                 kinachrichten.com "Warum quantisierte Kernel wichtig sind") or
  *                 QGEMM_FP8E4M3 (W4A8; the caller passes e4m3 codes and
  *                 per-row fp32 scales from qgemm_quantize_act_fp8)
  *   out_dtype     output dtype: equal to act_dtype for W4A16, QGEMM_BF16 for W4A8
@@ -179,6 +183,12 @@ typedef struct {
  *              k = 2j + 1 (high nibble) as e2m1 (sign | 2 exponent | 1 mantissa)
  *     scales   uint8 e8m0 [N, K/32]: the block scale 2^(b - 127); 255 is invalid
  *     meaning  w[k, n] = e2m1(code) * 2^(b - 127)
+ *   NVFP4:
+ *     codes    as MXFP4
+ *     scales   uint8 e4m3 [N, K/16]: one block scale per 16 k (NaN codes
+ *              0x7F / 0xFF are invalid)
+ *     tensor   fp32 [E]: one scale per expert, passed in the qzeros argument
+ *     meaning  w[k, n] = e2m1(code) * e4m3(scale) * tensor
  */
 
 /*
@@ -194,9 +204,12 @@ qgemm_status qgemm_packed_size(const qgemm_layer_config* layer, size_t* bytes);
  * aligned).  Per expert, the buffer holds one block per (128-row n-tile,
  * 128-deep k-tile), n-tile major: the tile's codes, then its scales, then its
  * zero points, so that consecutive k-tiles of a tile are contiguous.  INT4
- * codes are re-encoded as offset binary (q + 8); nothing else changes value,
- * so the packed buffer means exactly what the standard tensors mean.  qzeros
- * must be NULL unless zero_format = QGEMM_Z_UINT4.  Runs once per layer; the
+ * codes are re-encoded as offset binary (q + 8) and NVFP4 block scales as the
+ * activation dtype's bit pattern of the same value; nothing changes value, so
+ * the packed buffer means exactly what the standard tensors mean.  NVFP4
+ * buffers end with the fp32 tensor scales (16-byte padded).  qzeros must be
+ * NULL unless zero_format = QGEMM_Z_UINT4 (zero points) or the weights are
+ * NVFP4 (the tensor scales, required).  Runs once per layer; the
  * buffer is read-only afterwards.  For a gated layer (gated_act != 0) row
  * 2i + s of n-tile nt holds the standard column s * N/2 + 64 nt + i (gate
  * columns on even rows, the matching up columns on odd rows).
@@ -334,7 +347,8 @@ qgemm_status qgemm_moe_combine(const void* y2, const int32_t* inv_perm,
  * Debug: the weights of a packed layer (expert 0 or the dense layer) as the
  * kernels feed them to the tensor core, written as out[k, n] (device, [K, N]):
  * W4A16 the dequantized values in act_dtype, computed with exactly the
- * kernels' arithmetic; MXFP4 the e4m3 byte of each e2m1 code (the e8m0 block
+ * kernels' arithmetic (NVFP4: e2m1 x block scale; the tensor scale multiplies
+ * the fp32 sum); MXFP4 the e4m3 byte of each e2m1 code (the e8m0 block
  * scale is applied inside the MMA).  Columns are in the standard order for
  * gated layers too (the pack's gate/up interleave is undone).
  */

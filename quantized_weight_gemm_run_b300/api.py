@@ -102,6 +102,40 @@ class W4A16Linear:
         return Q.qgemm_check_status(self.ws.get(256))
 
 
+class NVFP4Linear(W4A16Linear):
+    """A packed layer of NVFP4 weights against fp16/bf16 activations: e2m1
+    codes uint8 [E*N, K/2] (standard nibble order), e4m3 block scales uint8
+    [E*N, K/16] and fp32 tensor scales [E].  Runs, grouped runs and the
+    dequantized view are those of ``W4A16Linear``."""
+
+    def __init__(self, codes, scales, tensor_scales, n, k, act_dtype, num_experts=1, bias=None,
+                 tuning=None, deterministic=False, gated=False, batch_invariant=False):
+        self.n, self.k, self.group, self.num_experts = n, k, 16, num_experts
+        self.gated = gated
+        self.n_out = n // 2 if gated else n
+        self.act_dtype = act_dtype
+        adt = _DT[act_dtype]
+        self.layer = Q.layer_config(
+            n, k, 16, Q.QGEMM_W_NVFP4, Q.QGEMM_S_E4M3, Q.QGEMM_Z_NONE, adt, adt,
+            1 if bias is not None else 0, num_experts,
+            Q.QGEMM_ACT_SILU_GLU if gated else Q.QGEMM_ACT_NONE)
+        st, nbytes = Q.qgemm_packed_size(self.layer)
+        Q.check(st)
+        dev = codes.device
+        codes, scales = codes.contiguous(), scales.contiguous()
+        tensor_scales = tensor_scales.to(torch.float32).contiguous()
+        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        Q.check(Q.qgemm_pack_weights(self.layer, codes, scales, tensor_scales, self.packed))
+        self.bias = bias
+        self.tuning = tuning
+        self.ws = Workspace(dev)
+        det = 1 if deterministic else 0
+        inv = 1 if batch_invariant else 0
+        self.dense = Q.compute_config(Q.QGEMM_GEMM_DENSE, batch_invariant=inv, deterministic=det)
+        self.grouped = Q.compute_config(Q.QGEMM_GEMM_GROUPED, batch_invariant=inv,
+                                        deterministic=det)
+
+
 class W4A8Linear:
     """A packed W4A8-MXFP4 layer: e2m1 codes uint8 [E*N, K/2] and e8m0 scales
     uint8 [E*N, K/32] in the standard format; activations are quantized per

@@ -66,6 +66,7 @@ struct W4A16Params {
   int sg_shift;              // scale group of 32-wide k chunk j is j >> sg_shift
   int has_zp;
   int gated;                 // 1: SiLU-gated output from interleaved gate/up rows
+  const float* t_scales;     // NVFP4: per-expert fp32 tensor scales (packed buffer tail)
   int split_cap;             // most CTAs sharing a tile's K range (0: no cap)
   const int* expert_offsets; // device [E+1] or null (dense)
   int num_experts;
@@ -93,7 +94,8 @@ struct W4A16Params {
 
 // Host-side plan for one W4A16 launch.
 int device_sm_count();
-// fmt: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 x e4m3, bf16 out)
+// fmt: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 x e4m3, bf16 out),
+//      3 = NVFP4 weights x bf16, 4 = NVFP4 weights x fp16
 cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
                          const W4A16Params& p, int block_tok, int fmt, bool grouped, int grid,
                          cudaStream_t stream);
@@ -143,7 +145,12 @@ cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
                              cudaStream_t stream);
 
 cudaError_t launch_debug_dequant(const uint8_t* packed, uint16_t* out, int64_t n, int64_t k,
-                                 int group, int has_zp, bool fp16, int gated, cudaStream_t stream);
+                                 int group, int has_zp, bool fp16, bool nv, int gated,
+                                 cudaStream_t stream);
+
+cudaError_t launch_repack_nvfp4(const uint8_t* codes, const uint8_t* scales,
+                               const float* tensor_scales, uint8_t* packed, int64_t n, int64_t k,
+                               int experts, bool fp16, int gated, cudaStream_t stream);
 
 cudaError_t launch_act_quant_fp8(const uint16_t* x, int64_t m, int64_t k, uint8_t* a8,
                                  float* scale, cudaStream_t stream);

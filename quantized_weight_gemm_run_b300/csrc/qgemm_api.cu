@@ -124,6 +124,16 @@ static qgemm_status check_layer(const qgemm_layer_config* L) {
         return fail(QGEMM_ERR_UNSUPPORTED, "UINT4 needs uint4 zero points");
       return ok();
     }
+    case QGEMM_W_NVFP4:
+      if (L->zero_format != QGEMM_Z_NONE)
+        return fail(QGEMM_ERR_UNSUPPORTED, "NVFP4 takes no zero points");
+      if (L->scale_format != QGEMM_S_E4M3 || L->group_size != 16)
+        return fail(QGEMM_ERR_UNSUPPORTED, "NVFP4 needs e4m3 scales per 16 k");
+      if (L->act_dtype != QGEMM_FP16 && L->act_dtype != QGEMM_BF16)
+        return fail(QGEMM_ERR_UNSUPPORTED, "NVFP4 weights run against fp16 or bf16 activations");
+      if (L->out_dtype != L->act_dtype)
+        return fail(QGEMM_ERR_UNSUPPORTED, "the output dtype must equal the activation dtype");
+      return ok();
     case QGEMM_W_MXFP4:
       if (L->zero_format != QGEMM_Z_NONE)
         return fail(QGEMM_ERR_UNSUPPORTED, "MXFP4 takes no zero points");
@@ -154,6 +164,15 @@ static qgemm_status check_compute(const qgemm_compute_config* C, const qgemm_lay
 static int st_of(int group) { return group < kTileK ? kTileK / group : 1; }
 
 static bool is_mx(const qgemm_layer_config* L) { return L->weight_format == QGEMM_W_MXFP4; }
+static bool is_nv(const qgemm_layer_config* L) { return L->weight_format == QGEMM_W_NVFP4; }
+
+// Bytes of one expert's packed blocks (an NVFP4 buffer adds the tensor-scale
+// tail after the last expert).
+static size_t expert_packed_bytes(const qgemm_layer_config* L) {
+  const size_t tiles = (size_t)(L->n / kTileN) * (size_t)(L->k / kTileK);
+  return tiles * (size_t)packed_block_bytes(is_mx(L), st_of(L->group_size),
+                                            L->zero_format == QGEMM_Z_UINT4);
+}
 
 // ------------------------------------------------------------ plans
 
@@ -373,8 +392,6 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
       a, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!tmap_ok)
     return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the activation tensor");
-  size_t wb = 0;
-  qgemm_packed_size(L, &wb);
   const int E = L->num_experts;
   W4A16Params p;
   memset(&p, 0, sizeof(p));
@@ -395,7 +412,10 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.split_cap = P.split_cap;
   p.expert_offsets = offsets;
   p.num_experts = E;
-  p.w_expert_stride = (long long)(wb / E);
+  p.w_expert_stride = (long long)expert_packed_bytes(L);
+  p.t_scales = is_nv(L) ? reinterpret_cast<const float*>(static_cast<const uint8_t*>(w) +
+                                                         (size_t)E * expert_packed_bytes(L))
+                        : nullptr;
   p.block_bytes = packed_block_bytes(mx, P.st, has_zp);
   p.s_off = P.off_s;
   p.z_off = P.off_z;
@@ -460,7 +480,8 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
                       n_out * 2, p.gated ? 16 : 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
     return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the output tensor");
   cudaError_t e =
-      launch_w4a16(tmap, tmap_c, p, P.bt, mx ? 2 : fp16 ? 1 : 0, grouped, P.grid, stream);
+      launch_w4a16(tmap, tmap_c, p, P.bt, mx ? 2 : is_nv(L) ? (fp16 ? 4 : 3) : fp16 ? 1 : 0,
+                   grouped, P.grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "W4A16 GEMM launch");
   return ok();
 }
@@ -496,10 +517,8 @@ qgemm_status qgemm_packed_size(const qgemm_layer_config* layer, size_t* bytes) {
   qgemm_status st = check_layer(layer);
   if (st != QGEMM_OK) return st;
   if (!bytes) return fail(QGEMM_ERR_INVALID_ARG, "bytes is NULL");
-  const size_t tiles = (size_t)(layer->n / kTileN) * (size_t)(layer->k / kTileK);
-  *bytes = (size_t)layer->num_experts * tiles *
-           (size_t)packed_block_bytes(is_mx(layer), st_of(layer->group_size),
-                                      layer->zero_format == QGEMM_Z_UINT4);
+  *bytes = (size_t)layer->num_experts * expert_packed_bytes(layer);
+  if (is_nv(layer)) *bytes += (size_t)((layer->num_experts + 3) / 4) * 16;   // tensor scales
   return ok();
 }
 
@@ -509,14 +528,23 @@ qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qwe
   qgemm_status st = check_layer(layer);
   if (st != QGEMM_OK) return st;
   const bool has_zp = layer->zero_format == QGEMM_Z_UINT4;
-  if (!qweight || !scales || !packed || (has_zp && !qzeros))
+  const bool nv = is_nv(layer);   // qzeros carries the fp32 tensor scales
+  if (!qweight || !scales || !packed || ((has_zp || nv) && !qzeros))
     return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (!has_zp && qzeros)
+  if (!has_zp && !nv && qzeros)
     return fail(QGEMM_ERR_INVALID_ARG, "zero points given for a format without");
   if (!aligned16(packed) || !aligned16(qweight))
     return fail(QGEMM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
   cudaError_t e;
-  if (is_mx(layer)) {
+  if (nv) {
+    if ((reinterpret_cast<uintptr_t>(qzeros) & 3u) != 0)
+      return fail(QGEMM_ERR_INVALID_ARG, "NVFP4 tensor scales must be 4-byte aligned");
+    e = launch_repack_nvfp4(static_cast<const uint8_t*>(qweight),
+                            static_cast<const uint8_t*>(scales), static_cast<const float*>(qzeros),
+                            static_cast<uint8_t*>(packed), layer->n, layer->k,
+                            layer->num_experts, layer->act_dtype == QGEMM_FP16,
+                            layer->gated_act != 0, static_cast<cudaStream_t>(stream));
+  } else if (is_mx(layer)) {
     if ((reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
       return fail(QGEMM_ERR_INVALID_ARG, "MXFP4 scales must be 4-byte aligned");
     e = launch_repack_mxfp4(static_cast<const uint8_t*>(qweight),
@@ -660,8 +688,8 @@ qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* pa
     e = launch_debug_dequant(static_cast<const uint8_t*>(packed), static_cast<uint16_t*>(out_kn),
                              layer->n, layer->k, layer->group_size,
                              layer->zero_format == QGEMM_Z_UINT4 ? 1 : 0,
-                             layer->act_dtype == QGEMM_FP16, layer->gated_act != 0,
-                             static_cast<cudaStream_t>(stream));
+                             layer->act_dtype == QGEMM_FP16, is_nv(layer),
+                             layer->gated_act != 0, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
   return ok();
 }
@@ -701,7 +729,7 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
     if (st != QGEMM_OK) {
       rec = std::string("rejected: ") + g_last_error;
     } else {
-      static const char* wf[] = {"int4_sym", "uint4_zp", "mxfp4"};
+      static const char* wf[] = {"int4_sym", "uint4_zp", "mxfp4", "nvfp4"};
       static const char* dt[] = {"fp16", "bf16", "fp8e4m3"};
       char tmp[512];
       snprintf(tmp, sizeof(tmp),

@@ -27,6 +27,10 @@
 // of the standard tensors are coalesced along N (in two runs per warp when
 // gated).
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "internal.h"
 
 namespace qg {
@@ -161,6 +165,72 @@ cudaError_t launch_repack_mxfp4(const uint8_t* codes, const uint8_t* scales, uin
   const int threads = 256;
   repack_mxfp4_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, stream>>>(
       codes, scales, packed, (int)n, (int)k, gated, vecs, words);
+  return cudaGetLastError();
+}
+
+// NVFP4: standard codes [N, K/2] (as MXFP4) and e4m3 block scales [N, K/16]
+// -> packed blocks: the code vectors exactly as MXFP4's, the block scales as
+// the activation dtype's 16-bit pattern of the same value (every e4m3 value is
+// a bf16 and an fp16 value) at word sg * 128 + r, sg the 16-k group within the
+// k-tile; the per-expert fp32 tensor scales follow the last block.
+__global__ void repack_nvfp4_kernel(const uint8_t* __restrict__ codes,
+                                    const uint8_t* __restrict__ scales,
+                                    const float* __restrict__ tensor_scales,
+                                    uint8_t* __restrict__ out, int n, int k, int experts, int fp16,
+                                    int gated, long long vecs, long long words) {
+  constexpr int kBlock = packed_block_bytes(false, 8, false);
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int KT = k / kTileK, NT = n / kTileN;
+  if (idx < vecs) {
+    const long long per_expert = (long long)NT * KT * 512;
+    const long long ex = idx / per_expert;
+    const long long rem = idx - ex * per_expert;
+    const long long blk = rem / 512;
+    const int v = (int)(rem % 512);
+    const int nt = (int)(blk / KT), kt = (int)(blk % KT);
+    const int t = v & 31, j = (v >> 5) & 3, qd = v >> 7;
+    const long long row = packed_source_col(nt, qd * 32 + t, n, gated);
+    const uint8_t* src = codes + (ex * n + row) * (k / 2) + (kt * kTileK + j * 32) / 2;
+    *reinterpret_cast<uint4*>(out + (ex * ((long long)NT * KT) + blk) * kBlock + v * 16) =
+        *reinterpret_cast<const uint4*>(src);
+  }
+  if (idx < words) {
+    const long long per_expert = (long long)NT * KT * 8 * kTileN;
+    const long long ex = idx / per_expert;
+    const long long rem = idx - ex * per_expert;
+    const int r = (int)(rem % kTileN);
+    const long long rest = rem / kTileN;
+    const int sg = (int)(rest % 8);
+    const long long blk = rest / 8;
+    const int nt = (int)(blk / KT), kt = (int)(blk % KT);
+    const long long row = packed_source_col(nt, r, n, gated);
+    const uint8_t e4 = scales[(ex * n + row) * (k / 16) + kt * 8 + sg];
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw(e4, __NV_E4M3);
+    uint16_t bits = hr.x;
+    if (!fp16) {
+      const __nv_bfloat16 b = __float2bfloat16_rn(__half2float(__half(hr)));   // exact
+      bits = *reinterpret_cast<const uint16_t*>(&b);
+    }
+    reinterpret_cast<uint16_t*>(out + (ex * ((long long)NT * KT) + blk) * kBlock +
+                                kTileBytes)[sg * kTileN + r] = bits;
+  }
+  if (idx < ((experts + 3) & ~3)) {   // the tail, zero-padded to 16 bytes
+    float* tail = reinterpret_cast<float*>(out + (long long)experts * NT * KT * kBlock);
+    tail[idx] = idx < experts ? tensor_scales[idx] : 0.f;
+  }
+}
+
+cudaError_t launch_repack_nvfp4(const uint8_t* codes, const uint8_t* scales,
+                               const float* tensor_scales, uint8_t* packed, int64_t n, int64_t k,
+                               int experts, bool fp16, int gated, cudaStream_t stream) {
+  const long long tiles = (long long)experts * (n / kTileN) * (k / kTileK);
+  const long long vecs = tiles * 512, words = tiles * 8 * kTileN;
+  long long total = vecs > words ? vecs : words;
+  if (total < ((experts + 3) & ~3)) total = (experts + 3) & ~3;
+  const int threads = 256;
+  repack_nvfp4_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, stream>>>(
+      codes, scales, tensor_scales, packed, (int)n, (int)k, experts, fp16 ? 1 : 0, gated, vecs,
+      words);
   return cudaGetLastError();
 }
 

@@ -266,6 +266,57 @@ __device__ __forceinline__ void dequant_vec_mx(const uint4 v, uint32_t (&out)[8]
 }
 
 template <bool FP16>
+__device__ __forceinline__ uint32_t mul_pair(uint32_t bits, uint32_t scale2) {
+  if constexpr (FP16) {
+    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&bits), *reinterpret_cast<__half2*>(&scale2));
+    return *reinterpret_cast<uint32_t*>(&r);
+  } else {
+    __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&bits),
+                               *reinterpret_cast<__nv_bfloat162*>(&scale2));
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
+}
+
+// NVFP4: 32 e2m1 codes (one 16-byte vector, k in nibble order, low nibble
+// first) -> 16 packed 16-bit pairs (k, k+1) of e2m1 value x block scale,
+// exactly: every e2m1 x e4m3 product is a bf16 and an fp16 value.  prmt looks
+// up the bytes of each code magnitude's 16-bit pattern in 8-entry byte tables
+// (fp16: the low byte is always 0), a sign-replicating prmt turns each code's
+// sign bit into bit 6 of a byte, and one lop3 moves it into the sign of the
+// high byte.  Words 0-1 hold k 0..15 (scale sA2), words 2-3 k 16..31 (sB2).
+template <bool FP16>
+__device__ __forceinline__ void dequant_vec_nv(const uint4 v, uint32_t sA2, uint32_t sB2,
+                                               uint32_t (&out)[16]) {
+  const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {   // codes 4 hh .. 4 hh + 3 of the word
+      const uint32_t c16 = wds[w] >> (16 * hh);
+      const uint32_t sel = c16 & 0x7777u;
+      uint32_t sgn, hi, p0, p1;
+      asm("prmt.b32 %0, %1, %1, %2;" : "=r"(sgn) : "r"(0x80808080u), "r"(c16));
+      if constexpr (FP16) {   // high bytes of fp16 0, 0.5, 1, 1.5 | 2, 3, 4, 6
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3E3C3800u), "r"(0x46444240u), "r"(sel));
+        hi = lop3_and_or(sgn << 1, 0x80808080u, hi);
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p0) : "r"(hi), "r"(0u), "r"(0x1404u));
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p1) : "r"(hi), "r"(0u), "r"(0x3424u));
+      } else {                // bf16: high and low bytes of the same eight values
+        uint32_t lo;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3F3F3F00u), "r"(0x40404040u), "r"(sel));
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0xC0800000u), "r"(0xC0804000u), "r"(sel));
+        hi = lop3_and_or(sgn << 1, 0x80808080u, hi);
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p0) : "r"(lo), "r"(hi), "r"(0x5140u));
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p1) : "r"(lo), "r"(hi), "r"(0x7362u));
+      }
+      const uint32_t s2 = w < 2 ? sA2 : sB2;
+      out[w * 4 + hh * 2] = mul_pair<FP16>(p0, s2);
+      out[w * 4 + hh * 2 + 1] = mul_pair<FP16>(p1, s2);
+    }
+  }
+}
+
+template <bool FP16>
 __device__ __forceinline__ uint16_t to_out(float v) {
   if constexpr (FP16) {
     __half h = __float2half_rn(v);
@@ -301,8 +352,9 @@ template <int BT, int FMT, bool GROUPED>
 __global__ void __launch_bounds__(kNumThreads, 1)
     w4a16_kernel(const __grid_constant__ CUtensorMap tmap_a,
                  const __grid_constant__ CUtensorMap tmap_c, const W4A16Params p) {
-  constexpr bool FP16 = FMT == 1;
-  constexpr bool MX = FMT == 2;
+  constexpr bool FP16 = FMT == 1 || FMT == 4;   // 16-bit activations and output: fp16
+  constexpr bool MX = FMT == 2;                  // W4A8-MXFP4
+  constexpr bool NV = FMT >= 3;                  // NVFP4 weights, 16-bit activations
   constexpr int RX = units_per_stage(BT);
   // tensor-memory columns: dequantized weight slots, then (MX) the A and B
   // scale factors, accumulators from column 256
@@ -677,10 +729,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               const uint8_t* zv = bp + p.z_off;
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                const int sg = j >> p.sg_shift;
-                scale2[t][j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
-                const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
-                zero2[t][j] = (magic16 + zq) * 0x00010001u;
+                if constexpr (NV) {   // two 16-k block scales per 32-k chunk
+                  scale2[t][j] = (uint32_t)sv[(2 * j) * kTileN + row] * 0x00010001u;
+                  zero2[t][j] = (uint32_t)sv[(2 * j + 1) * kTileN + row] * 0x00010001u;
+                } else {
+                  const int sg = j >> p.sg_shift;
+                  scale2[t][j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
+                  const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
+                  zero2[t][j] = (magic16 + zq) * 0x00010001u;
+                }
               }
             }
           }
@@ -717,7 +774,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               uint32_t out[16];
-              dequant_vec<FP16>(v[t][j], zero2[t][j], scale2[t][j], out);
+              if constexpr (NV)
+                dequant_vec_nv<FP16>(v[t][j], scale2[t][j], zero2[t][j], out);
+              else
+                dequant_vec<FP16>(v[t][j], zero2[t][j], scale2[t][j], out);
               tmem_st16(tbase + j * 16, out);
             }
           }
@@ -770,6 +830,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         float v = f[i];
         if constexpr (MX)   // W4A8: the per-row activation scale multiplies the fp32 sum
           v *= (m0 + i < tc.rows) ? p.a_scale[tc.row0 + m0 + i] : 0.f;
+        if constexpr (NV)   // NVFP4: the expert's tensor scale multiplies the fp32 sum
+          v *= p.t_scales[tc.e];
         o[i] = to_out<FP16>(v + bias);
       }
       const int valid = tc.rows - m0;
@@ -1110,14 +1172,19 @@ cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
                            : launch_bt<1, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
     case 2: return grouped ? launch_bt<2, true>(tmap_a, tmap_c, p, block_tok, grid, stream)
                            : launch_bt<2, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
+    case 3: return grouped ? launch_bt<3, true>(tmap_a, tmap_c, p, block_tok, grid, stream)
+                           : launch_bt<3, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
+    case 4: return grouped ? launch_bt<4, true>(tmap_a, tmap_c, p, block_tok, grid, stream)
+                           : launch_bt<4, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 // ------------------------------------------------------------ debug dequant
 
-// out[k, n] = the value the GEMM kernel feeds the tensor core for W^[k, n].
-template <bool FP16>
+// out[k, n] = the value the GEMM kernel feeds the tensor core for W^[k, n]
+// (NVFP4: e2m1 x block scale; the tensor scale is applied to the fp32 sum).
+template <bool FP16, bool NV>
 __global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n, int k,
                                      int group, int has_zp, int gated) {
   const int KT = k / kTileK;
@@ -1138,7 +1205,13 @@ __global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n
       has_zp ? (uint32_t)(bp + kTileBytes + packed_scale_bytes(false, st))[sg * kTileN + row] : 8u;
   constexpr uint32_t magic16 = FP16 ? 0x6400u : 0x4300u;
   uint32_t o[16];
-  dequant_vec<FP16>(wv, (magic16 + zq) * 0x00010001u, sbits * 0x00010001u, o);
+  if constexpr (NV) {   // two 16-k block scales for the vector's 32 k
+    const uint16_t* sv = reinterpret_cast<const uint16_t*>(bp + kTileBytes);
+    dequant_vec_nv<FP16>(wv, (uint32_t)sv[(2 * j) * kTileN + row] * 0x00010001u,
+                         (uint32_t)sv[(2 * j + 1) * kTileN + row] * 0x00010001u, o);
+  } else {
+    dequant_vec<FP16>(wv, (magic16 + zq) * 0x00010001u, sbits * 0x00010001u, o);
+  }
   const int nn = packed_source_col(nt, row, n, gated);
 #pragma unroll
   for (int c = 0; c < 16; ++c) {
@@ -1149,16 +1222,14 @@ __global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n
 }
 
 cudaError_t launch_debug_dequant(const uint8_t* packed, uint16_t* out, int64_t n, int64_t k,
-                                 int group, int has_zp, bool fp16, int gated, cudaStream_t stream) {
+                                 int group, int has_zp, bool fp16, bool nv, int gated,
+                                 cudaStream_t stream) {
   const long long total = (n / kTileN) * (k / kTileK) * 512;
   const int threads = 256;
-  const long long blocks = (total + threads - 1) / threads;
-  if (fp16)
-    debug_dequant_kernel<true><<<blocks, threads, 0, stream>>>(packed, out, (int)n, (int)k,
-                                                                group, has_zp, gated);
-  else
-    debug_dequant_kernel<false><<<blocks, threads, 0, stream>>>(packed, out, (int)n, (int)k,
-                                                                 group, has_zp, gated);
+  const unsigned blocks = (unsigned)((total + threads - 1) / threads);
+  auto kern = fp16 ? (nv ? debug_dequant_kernel<true, true> : debug_dequant_kernel<true, false>)
+                   : (nv ? debug_dequant_kernel<false, true> : debug_dequant_kernel<false, false>);
+  kern<<<blocks, threads, 0, stream>>>(packed, out, (int)n, (int)k, group, has_zp, gated);
   return cudaGetLastError();
 }
 

@@ -23,8 +23,8 @@ QGEMM_ERR_CUDA = 4
 QGEMM_ERR_TIMEOUT = 5
 QGEMM_ERR_DEVICE = 6
 # weight / scale / zero formats, dtypes, GEMM types
-QGEMM_W_INT4_SYM, QGEMM_W_UINT4_ZP, QGEMM_W_MXFP4 = 0, 1, 2
-QGEMM_S_FP16, QGEMM_S_BF16, QGEMM_S_E8M0 = 0, 1, 2
+QGEMM_W_INT4_SYM, QGEMM_W_UINT4_ZP, QGEMM_W_MXFP4, QGEMM_W_NVFP4 = 0, 1, 2, 3
+QGEMM_S_FP16, QGEMM_S_BF16, QGEMM_S_E8M0, QGEMM_S_E4M3 = 0, 1, 2, 3
 QGEMM_Z_NONE, QGEMM_Z_UINT4 = 0, 1
 QGEMM_FP16, QGEMM_BF16, QGEMM_FP8E4M3 = 0, 1, 2
 QGEMM_GEMM_DENSE, QGEMM_GEMM_GROUPED = 0, 1

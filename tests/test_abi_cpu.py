@@ -59,6 +59,13 @@ def test_packed_size_host_only(Q):
                                        scale_format=Q.QGEMM_S_E8M0, group_size=32,
                                        act_dtype=Q.QGEMM_FP8E4M3, out_dtype=Q.QGEMM_BF16))
     assert st == Q.QGEMM_OK and b == blocks * (8192 + 512)
+    # NVFP4: codes + 8 x 128 16-bit block scales per block, then the fp32 tensor
+    # scales of the experts padded to 16 bytes
+    st, b = Q.qgemm_packed_size(_layer(Q, weight_format=Q.QGEMM_W_NVFP4,
+                                       scale_format=Q.QGEMM_S_E4M3, group_size=16,
+                                       act_dtype=Q.QGEMM_BF16, out_dtype=Q.QGEMM_BF16,
+                                       num_experts=5))
+    assert st == Q.QGEMM_OK and b == 5 * blocks * (8192 + 2048) + 32
     # the gate/up interleave of a gated layer moves columns, it adds no bytes
     st, b = Q.qgemm_packed_size(_layer(Q, act_dtype=Q.QGEMM_BF16, out_dtype=Q.QGEMM_BF16,
                                        scale_format=Q.QGEMM_S_BF16, gated_act=1))
@@ -80,6 +87,9 @@ def test_packed_size_host_only(Q):
     (dict(num_experts=0), "INVALID_ARG"),
     (dict(has_bias=2), "INVALID_ARG"),
     (dict(gated_act=2), "INVALID_ARG"),
+    (dict(weight_format=3, scale_format=3, group_size=32), "UNSUPPORTED"),   # NVFP4 is per 16
+    (dict(weight_format=3, scale_format=0, group_size=16), "UNSUPPORTED"),   # needs e4m3 scales
+    (dict(weight_format=3, scale_format=3, group_size=16, zero_format=1), "UNSUPPORTED"),
     (dict(gated_act=1), "UNSUPPORTED"),             # a gated output must be bf16
 ])
 def test_rejections_are_clear(Q, bad, code):
