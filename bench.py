@@ -72,6 +72,12 @@ def workload_points(name):
         return sweep_points(), dict(workload="w4a16_asym_sweep", shapes=synth.W4A16_ASYM_SHAPES,
                                     ms=synth.W4A16_ASYM_MS, group=128, weights="uint4+zp",
                                     act="bf16")
+    if name == "nvfp4":
+        # the sweep's shapes with NVFP4 weights (e2m1 + e4m3 per 16 k + fp32 tensor scale)
+        return ([dict(p, kind="nvfp4", g=16, asym=False) for p in sweep_points()],
+                dict(workload="w4a16_nvfp4_sweep", shapes=synth.W4A16_ASYM_SHAPES,
+                     ms=synth.W4A16_ASYM_MS, group=16, weights="nvfp4 (e2m1 + e4m3/16 + fp32)",
+                     act="bf16"))
     if name == "w4a16_m16":
         s = synth.W4A16_SYM_SHAPE
         return [dict(m=s["m"], n=s["n"], k=s["k"], g=128, asym=False, adt="fp16")], dict(
@@ -105,6 +111,9 @@ def point_bytes(p):
     if kind == "w4a8":
         # act quant: read bf16 x, write e4m3 + scale; GEMM: codes, e8m0, a8, scale, bf16 out
         return (2 * m * k + m * k + 4 * m) + (n * k // 2 + n * k // 32 + m * k + 4 * m + 2 * m * n)
+    if kind == "nvfp4":
+        # codes, block scales as the kernel reads them (16-bit per 16 k), activations, output
+        return n * k // 2 + (k // 16) * n * 2 + m * k * 2 + m * n * 2
     if kind == "moe":
         s = synth.MOE_SHAPE
         e, h, i, topk = s["experts"], s["hidden"], s["inter"], s["topk"]
@@ -204,7 +213,7 @@ class GemmPoint:
     def __init__(self, p, seed, device, host=False, src=None):
         import torch
         from quantized_weight_gemm_run_b300 import qgemm as Q
-        from quantized_weight_gemm_run_b300.api import W4A16Linear, W4A8Linear
+        from quantized_weight_gemm_run_b300.api import NVFP4Linear, W4A16Linear, W4A8Linear
         self.p, self.Q = p, Q
         self.mx = p.get("kind") == "w4a8"
         m, n, k, gs = p["m"], p["n"], p["k"], p["g"]
@@ -216,6 +225,12 @@ class GemmPoint:
                 b = torch.from_numpy(synth.random_bytes(g, (n, k // 32), 116, 124)).to(device)
                 self.lin = W4A8Linear(codes, b, n, k)
                 del codes, b
+            elif p.get("kind") == "nvfp4":
+                codes = torch.from_numpy(synth.random_bytes(g, (n, k // 2))).to(device)
+                sb = torch.from_numpy(synth.random_bytes(g, (n, k // 16), 0x30, 0x48)).to(device)
+                ts = torch.full((1,), 2.0 ** -9, dtype=torch.float32, device=device)
+                self.lin = NVFP4Linear(codes, sb, ts, n, k, dt)
+                del codes, sb
             else:
                 qweight = torch.from_numpy(synth.random_words(g, (k // 8, n))).to(device)
                 scales = torch.from_numpy(
@@ -377,7 +392,8 @@ def kernel_name(p):
         return "moe_layer (sort, gather, SiLU-gated grouped GEMM, grouped GEMM, combine)"
     m = p["m"]
     bt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
-    fmt = "w4a8_mxf8f6f4" if kind == "w4a8" else ("fp16" if p["adt"] == "fp16" else "bf16")
+    fmt = ("w4a8_mxf8f6f4" if kind == "w4a8" else "nvfp4_bf16" if kind == "nvfp4"
+           else "fp16" if p["adt"] == "fp16" else "bf16")
     return f"w4a16_kernel<{bt},{fmt},dense>"
 
 
@@ -595,6 +611,13 @@ def _oracle_point(p, seed):
         a8, sc = gemm.act_quant_fp8(x)
         gemm.w4a8_output(a8, sc, ckn, bkn)
         return point_flops(p)
+    if kind == "nvfp4":
+        codes = synth.random_bytes(g, (n, k // 2))
+        sb = synth.random_bytes(g, (n, k // 16), 0x30, 0x48)
+        ckn, skn = quant.unpack_nvfp4(codes, sb)
+        a = codecs.bf16(synth.activations_fp32(g, m, k))
+        gemm.w4a16_output(a, quant.dequant_nvfp4(ckn, skn, 2.0 ** -9), "bf16")
+        return point_flops(p)
     if kind == "moe":
         s = synth.MOE_SHAPE
         e, h, i, topk, t = s["experts"], s["hidden"], s["inter"], s["topk"], 2
@@ -690,7 +713,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sweep",
-                    help="sweep | w4a16_m16 | large | w4a8 | moe16 | moe256 | moe4096 | "
+                    help="sweep | nvfp4 | w4a16_m16 | large | w4a8 | moe16 | moe256 | moe4096 | "
                          "shape:M,N,K[,sym|asym][,bf16|fp16]")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()
