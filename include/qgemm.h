@@ -151,7 +151,9 @@ typedef struct {
  *   block_tok  tokens per tile (the MMA N extent): 16, 32, 64 or 128
  *   stages     shared-memory pipeline depth (2 .. 16)
  *   max_ctas   upper bound on the persistent grid (<= number of SMs)
- *   split_k    0 = the heuristic's choice of stream-K split; s = 1..64:
+ *   split_k    0 = the heuristic's choice (without max_ctas: whole tiles or
+ *              stream-K, by a cost model of the split; with max_ctas:
+ *              stream-K); s = 1..64:
  *              the tiles left over after the whole waves are each split
  *              across min(s, grid / tiles left) CTAs at k-tile boundaries
  *              (1 = never split a tile's K range)

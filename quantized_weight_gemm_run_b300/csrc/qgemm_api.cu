@@ -280,6 +280,22 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   if (!grouped) {
     const int64_t units = tiles_bound * kt;
     if (units < grid) grid = (int)(units > 0 ? units : 1);
+    // Heuristic (16-bit MMA formats, neither a split cap nor a CTA cap
+    // asked): whole tiles when the
+    // k-tiles per CTA that stream-K saves over whole waves are worth less than
+    // the fixed cost of its split tiles (the finishers' copy-in, add and store
+    // at the end, the extra epilogue passes).  Measured on B300 per token tile
+    // (BT 16 / 32 / 64 / 128): ~0.30 / 0.33 / 0.38 / 0.47 us per k-tile and
+    // ~2.5 / 3 / 4.5 / 7 us of split cost: break-even at ~8 / 9 / 12 / 15.
+    if (!is_mx(L) && cap == 0 && !(T && T->max_ctas > 0) && tiles_bound > 0) {
+      const int64_t G = grid, Tt = tiles_bound;
+      const double whole_units = (double)((Tt + G - 1) / G) * kt;
+      int64_t W = Tt / G;
+      if (W > 0 && Tt % G) --W;   // the two-wave stream-K of the device schedule
+      const double sk_units = (double)W * kt + (double)(Tt - W * G) * kt / (double)G;
+      const double breakeven = bt == 16 ? 8.0 : bt == 32 ? 9.0 : bt == 64 ? 12.0 : 15.0;
+      if (whole_units - sk_units < breakeven) cap = 1;
+    }
     if (cap > 0 && tiles_bound * cap < grid)
       grid = (int)(tiles_bound > 0 ? tiles_bound * cap : 1);
   }
