@@ -345,13 +345,15 @@ def make_point(p, seed, device, host=False):
 
 
 def kernel_source_digest():
-    """Digest of the GEMM kernel's sources; a committed ncu traffic figure is
-    used only while it matches."""
+    """Digest of the library's sources (kernels and the planner that picks
+    them); a committed ncu traffic figure is used only while it matches."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("w4a16_gemm.cu", "ptx.cuh", "internal.h"):
-        with open(os.path.join(ROOT, "quantized_weight_gemm_run_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    d = os.path.join(ROOT, "quantized_weight_gemm_run_b300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -391,6 +393,9 @@ def kernel_name(p):
     if kind == "moe":
         return "moe_layer (sort, gather, SiLU-gated grouped GEMM, grouped GEMM, combine)"
     m = p["m"]
+    if kind == "w4a16" and m <= 16 and p["n"] // 128 <= 5 * 148:
+        # the planner's default for dense INT4/UINT4 GEMMs of at most 16 rows
+        return f"w4a16_mma_kernel<{'fp16' if p['adt'] == 'fp16' else 'bf16'}>"
     bt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
     fmt = ("w4a8_mxf8f6f4" if kind == "w4a8" else "nvfp4_bf16" if kind == "nvfp4"
            else "fp16" if p["adt"] == "fp16" else "bf16")

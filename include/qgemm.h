@@ -158,6 +158,11 @@ typedef struct {
  *              across min(s, grid / tiles left) CTAs at k-tile boundaries
  *              (1 = never split a tile's K range)
  *   cta_pair   reserved, must be 0
+ *   kernel     0 = the heuristic's choice, 1 = the persistent tcgen05 kernel,
+ *              2 = the small-M kernel (cp.async + mma.sync, split K; dense
+ *              INT4 / UINT4 with m <= 16 only, not gated, deterministic or
+ *              batch-invariant; split_k, when set, is its number of K
+ *              slices per n-tile; it ignores the other tuning fields)
  */
 typedef struct {
   int32_t block_tok;
@@ -165,6 +170,7 @@ typedef struct {
   int32_t max_ctas;
   int32_t split_k;
   int32_t cta_pair;
+  int32_t kernel;
 } qgemm_tuning_config;
 
 /*

@@ -92,6 +92,22 @@ struct W4A16Params {
   unsigned long long wait_limit_ns;
 };
 
+// The small-M kernel (mma.sync, M <= 16, INT4 / UINT4): n-tiles x splits
+// CTAs, each a K slice of one n-tile; fp32 partials meet in acc[nt] (16 x 128
+// per n-tile) with a per-n-tile count, both left at zero.
+struct W4A16MmaParams {
+  const uint8_t* w;          // packed blocks (one expert)
+  const uint16_t* a;         // activations [m, k]
+  uint16_t* c;               // output [m, n]
+  const uint16_t* bias;      // [n] or null
+  float* acc;                // [nt][128][16] fp32, zero
+  int* counters;             // [nt], zero
+  int m, n, k, kt, nt, splits;
+  int block_bytes, w_slot_bytes, s_off, z_off, sg_shift, has_zp;
+};
+cudaError_t launch_w4a16_mma(const W4A16MmaParams& p, bool fp16, cudaStream_t stream);
+int mma_smem_bytes(int block_bytes);
+
 // Host-side plan for one W4A16 launch.
 int device_sm_count();
 // fmt: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 x e4m3, bf16 out),

@@ -232,6 +232,8 @@ static bool make_geometry(int bt, int st, int has_zp, bool mx, int experts, int 
 }
 
 struct Plan {
+  int kernel;        // 1: the persistent tcgen05 kernel, 2: the small-M mma.sync kernel
+  int mma_splits;    // small-M kernel: K slices per n-tile
   int bt, grid, st, off_s, off_z;
   int split_cap;     // most CTAs sharing one tile's K range (0: no cap, 1: whole tiles)
   Geometry g;
@@ -243,6 +245,7 @@ struct Plan {
 static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_config* T,
                               const qgemm_compute_config* C, int64_t rows, bool grouped,
                               Plan* P) {
+  *P = Plan();
   // most CTAs per tile: from the tuning; 1 (whole tiles) under batch
   // invariance, since a split's K boundaries depend on the tile count (so on M)
   int cap = T ? T->split_k : 0;
@@ -259,6 +262,56 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
     return fail(QGEMM_ERR_INVALID_ARG, "split_k must be in [0, 64]");
   const int st = st_of(L->group_size);
   const int has_zp = L->zero_format == QGEMM_Z_UINT4;
+  if (T && (T->kernel < 0 || T->kernel > 2))
+    return fail(QGEMM_ERR_INVALID_ARG, "kernel must be 0, 1 or 2");
+  const bool mma_ok = !grouped && !is_mx(L) && !is_nv(L) && L->gated_act == 0 && rows <= 16 &&
+                      !(C && (C->deterministic || C->batch_invariant));
+  const int want = T ? T->kernel : 0;
+  if (want == 2 && !mma_ok)
+    return fail(QGEMM_ERR_UNSUPPORTED,
+                "the small-M kernel takes dense INT4/UINT4 GEMMs with m <= 16 that are not "
+                "gated, deterministic or batch-invariant");
+  P->kernel = 1;
+  P->mma_splits = 0;
+  const int64_t ntl = L->n / kTileN, ktl = L->k / kTileK;
+  // Heuristic: with no tuning field for the tcgen05 kernel set, the small-M
+  // kernel takes the GEMMs it can run in one wave of CTAs.  Measured on B300
+  // at M = 1..16 it beats the persistent kernel on every shape of the sweep
+  // (4096^2: 8.0-8.1 -> 7.2-7.7 us; 4096 x 11008: 12.5 -> 11.65 us; 11008 x
+  // 4096: 12.5 -> 12.3 us): no tensor-memory set-up and no split-tile finish
+  // at the end.
+  const bool k1_tuned = T && (T->block_tok || T->stages || T->max_ctas || T->split_k);
+  const bool use_mma = want == 2 || (want == 0 && mma_ok && !k1_tuned && ntl <= 5LL * sms);
+  if (use_mma) {
+    // K slices per n-tile: as many as fill five 128-thread CTAs per SM in
+    // one wave (measured best on every sweep shape; a partial second wave
+    // costs 20-30 %)
+    int64_t S = (5LL * sms) / ntl;
+    if (want == 2 && T->split_k > 0) S = T->split_k;   // explicit slice count
+    if (S > ktl) S = ktl;
+    if (S < 1) S = 1;
+    if (ntl * S >= (int64_t(1) << 31)) return fail(QGEMM_ERR_UNSUPPORTED, "grid too large");
+    if (mma_smem_bytes(packed_block_bytes(false, st, has_zp)) > device_max_smem())
+      return fail(QGEMM_ERR_UNSUPPORTED, "tile does not fit shared memory");
+    P->kernel = 2;
+    P->mma_splits = (int)S;
+    P->bt = 16;
+    P->grid = (int)(ntl * S);
+    P->split_cap = 0;
+    P->st = st;
+    P->off_s = kTileBytes;
+    P->off_z = kTileBytes + packed_scale_bytes(false, st);
+    P->max_tiles = ntl;
+    // status word, a count per n-tile, a 16 x 128 fp32 accumulator per n-tile
+    WorkspaceLayout w;
+    w.counters_off = 256;
+    w.counters_bytes = ((size_t)ntl * sizeof(int) + 255) & ~size_t(255);
+    w.partials_off = w.counters_off + w.counters_bytes;
+    w.partials_bytes = (size_t)ntl * 16 * kTileN * sizeof(float);
+    w.total = w.partials_off + w.partials_bytes;
+    P->ws = w;
+    return ok();
+  }
   const int w_cap = (T && T->stages) ? T->stages : 16;
   if (w_cap < 2 || w_cap > 16) return fail(QGEMM_ERR_INVALID_ARG, "stages must be in [2, 16]");
   Geometry g;
@@ -391,6 +444,32 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
     return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", P.ws.total,
                 ws_bytes);
   const bool fp16 = L->act_dtype == QGEMM_FP16;
+  if (P.kernel == 2) {
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    W4A16MmaParams q;
+    memset(&q, 0, sizeof(q));
+    q.w = static_cast<const uint8_t*>(w);
+    q.a = static_cast<const uint16_t*>(a);
+    q.c = static_cast<uint16_t*>(c);
+    q.bias = static_cast<const uint16_t*>(bias);
+    q.acc = reinterpret_cast<float*>(wsb + P.ws.partials_off);
+    q.counters = reinterpret_cast<int*>(wsb + P.ws.counters_off);
+    q.m = (int)rows;
+    q.n = (int)L->n;
+    q.k = (int)L->k;
+    q.kt = (int)(L->k / kTileK);
+    q.nt = (int)(L->n / kTileN);
+    q.splits = P.mma_splits;
+    q.block_bytes = packed_block_bytes(false, P.st, has_zp);
+    q.w_slot_bytes = (q.block_bytes + 15) & ~15;
+    q.s_off = P.off_s;
+    q.z_off = P.off_z;
+    q.sg_shift = L->group_size == 32 ? 0 : L->group_size == 64 ? 1 : 2;
+    q.has_zp = has_zp ? 1 : 0;
+    cudaError_t e = launch_w4a16_mma(q, fp16, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "small-M GEMM launch");
+    return ok();
+  }
   CUtensorMap tmap;
   // activation boxes [chunk][row][128 bytes]: the K axis split into 128-byte
   // chunks (64 16-bit or 128 e4m3 values) as the outermost box dimension, so
@@ -753,13 +832,14 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
                "m=%lld experts=%d block_tok=%d act_slots=%d weight_slots=%dx%d grid=%d smem=%d "
                "workspace=%zu epilogue=%s split=%s "
                "device=sm_103",
-               is_mx(layer) ? "w4a8_tcgen05_mxf8f6f4_swapab" : "w4a16_tcgen05_swapab",
+               P.kernel == 2 ? "w4a16_mma_sync_smallm"
+               : is_mx(layer) ? "w4a8_tcgen05_mxf8f6f4_swapab" : "w4a16_tcgen05_swapab",
                grouped ? "_grouped" : "", wf[layer->weight_format], layer->group_size,
                dt[layer->act_dtype], dt[layer->out_dtype], (long long)layer->n,
                (long long)layer->k, (long long)m, layer->num_experts, P.bt, P.g.x_stages,
                P.g.w_stages, P.g.rw, P.grid, P.g.smem, P.ws.total,
                layer->gated_act ? "silu_glu" : "plain",
-               P.split_cap == 1 ? "whole_tiles" : "stream_k");
+               P.kernel == 2 ? "k_slices" : P.split_cap == 1 ? "whole_tiles" : "stream_k");
       rec = tmp;
     }
   }

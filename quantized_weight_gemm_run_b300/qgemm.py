@@ -47,7 +47,7 @@ class qgemm_compute_config(ctypes.Structure):
 class qgemm_tuning_config(ctypes.Structure):
     _fields_ = [("block_tok", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("split_k", ctypes.c_int32),
-                ("cta_pair", ctypes.c_int32)]
+                ("cta_pair", ctypes.c_int32), ("kernel", ctypes.c_int32)]
 
 
 class QGemmError(RuntimeError):
@@ -147,8 +147,8 @@ def compute_config(gemm_type=QGEMM_GEMM_DENSE, batch_invariant=0,
     return qgemm_compute_config(gemm_type, batch_invariant, deterministic)
 
 
-def tuning_config(block_tok=0, stages=0, max_ctas=0, split_k=0, cta_pair=0):
-    return qgemm_tuning_config(block_tok, stages, max_ctas, split_k, cta_pair)
+def tuning_config(block_tok=0, stages=0, max_ctas=0, split_k=0, cta_pair=0, kernel=0):
+    return qgemm_tuning_config(block_tok, stages, max_ctas, split_k, cta_pair, kernel)
 
 
 # ------------------------------------------------------------- entry points
