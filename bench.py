@@ -344,16 +344,29 @@ def make_point(p, seed, device, host=False):
     return GemmPoint(p, seed, device, host)
 
 
-def kernel_source_digest():
+def source_without_comments(text: str) -> str:
+    """C/C++ source with its comments and blank lines removed (string
+    literals holding comment markers are not expected in the kernels)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
+def kernel_source_digest(read=None):
     """Digest of the library's sources (kernels and the planner that picks
-    them); a committed ncu traffic figure is used only while it matches."""
+    them), comments ignored; a committed ncu traffic figure is used only while
+    it matches.  ``read(name)`` returns a file's text (default: the tree)."""
     import hashlib
-    h = hashlib.sha256()
     d = os.path.join(ROOT, "quantized_weight_gemm_run_b300", "csrc")
+    if read is None:
+        def read(name):
+            with open(os.path.join(d, name)) as fh:
+                return fh.read()
+    h = hashlib.sha256()
     for f in sorted(os.listdir(d)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+            h.update(source_without_comments(read(f)).encode())
     return h.hexdigest()[:16]
 
 

@@ -4,9 +4,10 @@
 // dequantization/scaling, tensor-core compute and output processing
 // (kinachrichten.com, "Kompilierzeiten und geraetespezifisches Tuning"), with
 // a TMA + UMMA pipeline for larger batches and a multi-stage cp.async + MMA
-// pipeline for small ones (same article, section "Kompilierzeiten...",
-// paragraph on small vs larger batch sizes).  This kernel is the B300 design
-// of those five components, one kernel for every M:
+// pipeline for small ones (same article, section "Wie die Architektur
+// funktioniert").  This kernel is the B300 design of those five components
+// for every M and format (the cp.async + mma.sync kernel in w4a16_mma.cu
+// takes dense INT4/UINT4 GEMMs of at most 16 rows):
 //
 //   swap-AB:  the MMA computes D[n, m] = W^[n, :] . A[m, :], so the 128 output
 //             features of a tile are the MMA M extent and the tokens are the
