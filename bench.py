@@ -475,10 +475,10 @@ def run_ours(args, rank, world, device):
     is_moe = pts[0].get("kind") == "moe"
     if is_moe:
         tokens_step = sum(gm.p["m"] for gm in gemms)
-        value = world * tokens_step * args.steps / (ms_total * 1e-3)
+        value = whole_job_rate(tokens_step, args.steps, ms_total, world)
         unit = "tokens/s"
     else:
-        value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
+        value = whole_job_rate(flops_step, args.steps, ms_total, world) / 1e12
         unit = "TFLOP/s"
 
     # per-GEMM device times (dominant kernel and the per-M table): each GEMM
@@ -566,9 +566,9 @@ def run_ours(args, rank, world, device):
     e2e_ms = reduce_max(b0.elapsed_time(b1), world)
     flops_pts = sum(point_flops(p) for p in pts)
     if is_moe:
-        e2e_val = world * sum(p["m"] for p in pts) * e2e_steps / (e2e_ms * 1e-3)
+        e2e_val = whole_job_rate(sum(p["m"] for p in pts), e2e_steps, e2e_ms, world)
     else:
-        e2e_val = world * flops_pts * e2e_steps / (e2e_ms * 1e-3) / 1e12
+        e2e_val = whole_job_rate(flops_pts, e2e_steps, e2e_ms, world) / 1e12
 
     line = {
         "metric": "W4A16 GEMM TFLOP/s and HBM GB/s vs M (frac of B300 roofline); MoE tokens/s",
@@ -602,13 +602,21 @@ def run_ours(args, rank, world, device):
 
 
 def reduce_max(x, world):
+    """The maximum of x over the ranks (NCCL: a device tensor; gloo: host)."""
     if world <= 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step, steps, ms_max, world):
+    """Whole-job throughput: every rank processes units_per_rank_step per step
+    (weak scaling), and the job takes the slowest rank's time."""
+    return world * units_per_rank_step * steps / (ms_max * 1e-3)
 
 
 # ------------------------------------------------------------------ CPU oracle
