@@ -17,11 +17,11 @@
 // with one LOP3 against a magic exponent.  Activations come through ldmatrix
 // from a padded shared-memory tile (conflict-free rows).
 //
-// Work split.  Grid = n-tiles x S K-slices, about four CTAs of 128 threads
+// Work split.  Grid = n-tiles x S K-slices, about five CTAs of 128 threads
 // per SM; a CTA issues cp.async copies for its slice's k-tiles through a ring
 // of kStages slots (the whole slice up front when it fits), weights before
 // the wait on the previous grid, activations after it.  Partials: the CTA's
-// 16 x 128 fp32 result is staged in shared memory and added into the
+// m x 128 fp32 result rows are staged in shared memory and added into the
 // n-tile's accumulator in L2 with one bulk reduction; the CTA then counts in
 // with an acquire-release add, and the last of the S arrivals adds the bias,
 // rounds, writes the output rows and re-zeroes the accumulator and counter.
@@ -218,25 +218,28 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(const W4A16MmaPa
   }
   cp_async_wait<0>();
 
-  // the CTA's partial as [feature][16 tokens] fp32 in slot 0
+  // the CTA's partial as [token][128 features] fp32 in slot 0: the m live
+  // token rows are contiguous, so only they are reduced, read and re-zeroed
   float* cs = reinterpret_cast<float*>(smem);
 #pragma unroll
   for (int b = 0; b < 2; ++b)
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int f = warp * 32 + b * 16 + g, tk = c * 8 + 2 * t;
-      *reinterpret_cast<float2*>(cs + f * 16 + tk) = make_float2(acc[b][c][0], acc[b][c][1]);
-      *reinterpret_cast<float2*>(cs + (f + 8) * 16 + tk) = make_float2(acc[b][c][2], acc[b][c][3]);
+      cs[tk * kTileN + f] = acc[b][c][0];
+      cs[(tk + 1) * kTileN + f] = acc[b][c][1];
+      cs[tk * kTileN + f + 8] = acc[b][c][2];
+      cs[(tk + 1) * kTileN + f + 8] = acc[b][c][3];
     }
   fence_proxy_async_smem();   // every writer, before the bulk reduction reads the tile
   __syncthreads();
 
   __shared__ int last;
-  const float* sum = cs;   // where the finished fp32 tile is read from
+  const float* sum = cs;   // where the finished fp32 rows are read from
   if (p.splits > 1) {
     float* tile = p.acc + (long long)nt * (kTileN * 16);
     if (tid == 0) {
-      bulk_reduce_add_f32(tile, cs, kTileN * 16 * 4);
+      bulk_reduce_add_f32(tile, cs, p.m * kTileN * 4);
       bulk_commit_group();
       bulk_wait_group_all();
       asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -260,16 +263,13 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(const W4A16MmaPa
     bias = FP16 ? __half2float(*reinterpret_cast<const __half*>(&bb))
                 : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(&bb));
   }
+  // every live row's sum is loaded before the first output store (the stores
+  // could alias the loads as far as the compiler knows, which would serialize
+  // them one L2 round trip each)
   float v[16];
-  const float4* s4 = reinterpret_cast<const float4*>(sum + f * 16);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 x = p.splits > 1 ? __ldcg(s4 + i) : s4[i];
-    v[4 * i] = x.x;
-    v[4 * i + 1] = x.y;
-    v[4 * i + 2] = x.z;
-    v[4 * i + 3] = x.w;
-  }
+  for (int r = 0; r < 16; ++r)
+    v[r] = r < p.m ? (p.splits > 1 ? __ldcg(sum + r * kTileN + f) : sum[r * kTileN + f]) : 0.f;
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     if (r < p.m) {
@@ -284,10 +284,11 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(const W4A16MmaPa
       p.c[(long long)r * p.n + n] = o;
     }
   }
-  if (p.splits > 1) {   // leave the accumulator and the count at zero
-    float4* z4 = reinterpret_cast<float4*>(p.acc + (long long)nt * (kTileN * 16) + f * 16);
+  if (p.splits > 1) {   // leave the accumulator rows and the count at zero
+    float* z = p.acc + (long long)nt * (kTileN * 16) + f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < 16; ++r)
+      if (r < p.m) z[r * kTileN] = 0.f;
     if (tid == 0) p.counters[nt] = 0;
   }
 }
