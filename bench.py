@@ -65,13 +65,21 @@ def workload_points(name):
         m, n, k = (int(v) for v in f[:3])
         asym = "asym" in f[3:]
         adt = "fp16" if "fp16" in f[3:] else "bf16"
-        return [dict(m=m, n=n, k=k, g=128, asym=asym, adt=adt)], dict(
-            workload=f"w4a16_{'asym' if asym else 'sym'}_{m}x{n}x{k}", m=m, n=n, k=k, group=128,
-            weights="uint4+zp" if asym else "int4", act=adt)
+        sdt = "fp16" if "f16s" in f[3:] else adt     # f16s: fp16 scales (bf16 activations)
+        return [dict(m=m, n=n, k=k, g=128, asym=asym, adt=adt, sdt=sdt)], dict(
+            workload=f"w4a16_{'asym' if asym else 'sym'}_{m}x{n}x{k}"
+                     + ("_f16scales" if sdt != adt else ""), m=m, n=n, k=k, group=128,
+            weights="uint4+zp" if asym else "int4", scales=sdt, act=adt)
     if name == "sweep":
         return sweep_points(), dict(workload="w4a16_asym_sweep", shapes=synth.W4A16_ASYM_SHAPES,
                                     ms=synth.W4A16_ASYM_MS, group=128, weights="uint4+zp",
                                     act="bf16")
+    if name == "f16s":
+        # the sweep with fp16 scales against bf16 activations
+        return ([dict(p, sdt="fp16") for p in sweep_points()],
+                dict(workload="w4a16_asym_f16scales_sweep", shapes=synth.W4A16_ASYM_SHAPES,
+                     ms=synth.W4A16_ASYM_MS, group=128, weights="uint4+zp", scales="fp16",
+                     act="bf16"))
     if name == "nvfp4":
         # the sweep's shapes with NVFP4 weights (e2m1 + e4m3 per 16 k + fp32 tensor scale)
         return ([dict(p, kind="nvfp4", g=16, asym=False) for p in sweep_points()],
@@ -233,11 +241,12 @@ class GemmPoint:
                 del codes, sb
             else:
                 qweight = torch.from_numpy(synth.random_words(g, (k // 8, n))).to(device)
+                sdt = torch.float16 if p.get("sdt", p["adt"]) == "fp16" else torch.bfloat16
                 scales = torch.from_numpy(
-                    synth.random_scales_fp32(g, (k // gs, n))).to(dt).to(device)
+                    synth.random_scales_fp32(g, (k // gs, n))).to(sdt).to(device)
                 qzeros = (torch.from_numpy(synth.random_words(g, (k // gs, n // 8))).to(device)
                           if p["asym"] else None)
-                self.lin = W4A16Linear(qweight, scales, qzeros, n, k, gs, dt)
+                self.lin = W4A16Linear(qweight, scales, qzeros, n, k, gs, dt, scale_dtype=sdt)
                 del qweight, scales, qzeros
             self.a = torch.from_numpy(synth.activations_fp32(g, m, k)).to(dt).to(device)
         else:
@@ -391,8 +400,13 @@ def committed_traffic():
     return out
 
 
+def f16_scales(p):
+    return p.get("sdt", p["adt"]) != p["adt"]
+
+
 def shape_key(p):
     return (f"{p['m']}x{p['n']}x{p['k']},{'asym' if p.get('asym') else 'sym'},{p['adt']}"
+            + (",f16s" if f16_scales(p) else "")
             if p.get("kind", "w4a16") == "w4a16" else None)
 
 
@@ -406,12 +420,12 @@ def kernel_name(p):
     if kind == "moe":
         return "moe_layer (sort, gather, SiLU-gated grouped GEMM, grouped GEMM, combine)"
     m = p["m"]
-    if kind == "w4a16" and m <= 16 and p["n"] // 128 <= 5 * 148:
+    if kind == "w4a16" and m <= 16 and p["n"] // 128 <= 5 * 148 and not f16_scales(p):
         # the planner's default for dense INT4/UINT4 GEMMs of at most 16 rows
         return f"w4a16_mma_kernel<{'fp16' if p['adt'] == 'fp16' else 'bf16'}>"
     bt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
     fmt = ("w4a8_mxf8f6f4" if kind == "w4a8" else "nvfp4_bf16" if kind == "nvfp4"
-           else "fp16" if p["adt"] == "fp16" else "bf16")
+           else "bf16_f16scales" if f16_scales(p) else "fp16" if p["adt"] == "fp16" else "bf16")
     return f"w4a16_kernel<{bt},{fmt},dense>"
 
 
@@ -659,7 +673,8 @@ def _oracle_point(p, seed):
         moe.moe_layer(x, ids, wts, w_hat(h, 2 * i), w_hat(i, h), e, i)
         return t
     qw = synth.random_words(g, (k // 8, n))
-    s = codecs.bf16(synth.random_scales_fp32(g, (k // gs, n)).astype(np.float64))
+    s = codecs.round_dtype(p.get("sdt", p["adt"]))(
+        synth.random_scales_fp32(g, (k // gs, n)).astype(np.float64))
     q = quant.unpack_int4_kn(qw, signed=not p["asym"])
     z = quant.unpack_zeros(synth.random_words(g, (k // gs, n // 8))) if p["asym"] else None
     a = codecs.bf16(synth.activations_fp32(g, m, k))
@@ -739,8 +754,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sweep",
-                    help="sweep | nvfp4 | w4a16_m16 | large | w4a8 | moe16 | moe256 | moe4096 | "
-                         "shape:M,N,K[,sym|asym][,bf16|fp16]")
+                    help="sweep | f16s | nvfp4 | w4a16_m16 | large | w4a8 | moe16 | moe256 | "
+                         "moe4096 | shape:M,N,K[,sym|asym][,bf16|fp16][,f16s]")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -180,12 +180,17 @@ typedef struct {
  *     qweight  int32 [K/8, N]: word (j, n) holds k = 8j + i in bits [4i, 4i+4),
  *              least significant nibble first; INT4 as 4-bit two's complement,
  *              UINT4 as raw 0..15
- *     scales   fp16 or bf16 [K/g, N], row-major (group-major)
+ *     scales   fp16 or bf16 [K/g, N], row-major (group-major); fp16 scales
+ *              serve fp16 or bf16 activations, bf16 scales bf16 activations
+ *              (the pages count the representation of the scales among the
+ *              axes along which formats vary: kinachrichten.com, "Warum
+ *              quantisierte Kernel wichtig sind")
  *     qzeros   int32 [K/g, N/8] (UINT4_ZP only): nibble i of word (G, j) is the
  *              zero point (0..15) of column 8j + i; the stored value is the
  *              true zero point
  *     meaning  w[k, n] = (q - z) * s, rounded once to the activation dtype
- *              (z = 0 for INT4)
+ *              (z = 0 for INT4; an fp16 scale with bf16 activations is not
+ *              rounded to bf16 first)
  *   MXFP4:
  *     codes    uint8 [N, K/2]: byte (n, j) holds k = 2j (low nibble) and
  *              k = 2j + 1 (high nibble) as e2m1 (sign | 2 exponent | 1 mantissa)

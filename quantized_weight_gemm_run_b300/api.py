@@ -31,24 +31,27 @@ class Workspace:
 class W4A16Linear:
     """A packed W4A16 layer (dense, or the stacked experts of a grouped layer).
 
-    qweight int32 [E*K/8, N], scales [E*K/g, N] (act dtype), qzeros int32
-    [E*K/g, N/8] or None: the standard format of ``include/qgemm.h``.
-    gated=True: the N columns are an MoE gate half and up half and the layer
-    writes silu(gate) * up, [rows, N/2] (bf16 only).  batch_invariant=True:
-    a row's result does not depend on the other rows of a call."""
+    qweight int32 [E*K/8, N], scales [E*K/g, N] (16-bit: the bits of
+    ``scale_dtype``, which defaults to the activation dtype; fp16 scales
+    also serve bf16 activations), qzeros int32 [E*K/g, N/8] or None: the
+    standard format of ``include/qgemm.h``.  gated=True: the N columns are an
+    MoE gate half and up half and the layer writes silu(gate) * up, [rows,
+    N/2] (bf16 only).  batch_invariant=True: a row's result does not depend on
+    the other rows of a call."""
 
     def __init__(self, qweight, scales, qzeros, n, k, group, act_dtype, num_experts=1,
                  bias=None, tuning=None, deterministic=False, gated=False,
-                 batch_invariant=False):
+                 batch_invariant=False, scale_dtype=None):
         self.n, self.k, self.group, self.num_experts = n, k, group, num_experts
         self.gated = gated
         self.n_out = n // 2 if gated else n
         self.act_dtype = act_dtype
         asym = qzeros is not None
         adt = _DT[act_dtype]
+        sdt = adt if scale_dtype is None else _DT[scale_dtype]
         self.layer = Q.layer_config(
             n, k, group, Q.QGEMM_W_UINT4_ZP if asym else Q.QGEMM_W_INT4_SYM,
-            Q.QGEMM_S_FP16 if adt == Q.QGEMM_FP16 else Q.QGEMM_S_BF16,
+            Q.QGEMM_S_FP16 if sdt == Q.QGEMM_FP16 else Q.QGEMM_S_BF16,
             Q.QGEMM_Z_UINT4 if asym else Q.QGEMM_Z_NONE, adt, adt,
             1 if bias is not None else 0, num_experts,
             Q.QGEMM_ACT_SILU_GLU if gated else Q.QGEMM_ACT_NONE)

@@ -111,7 +111,8 @@ int mma_smem_bytes(int block_bytes);
 // Host-side plan for one W4A16 launch.
 int device_sm_count();
 // fmt: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 x e4m3, bf16 out),
-//      3 = NVFP4 weights x bf16, 4 = NVFP4 weights x fp16
+//      3 = NVFP4 weights x bf16, 4 = NVFP4 weights x fp16,
+//      5 = W4A16 bf16 with fp16 scales
 cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
                          const W4A16Params& p, int block_tok, int fmt, bool grouped, int grid,
                          cudaStream_t stream);
@@ -161,8 +162,8 @@ cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
                              cudaStream_t stream);
 
 cudaError_t launch_debug_dequant(const uint8_t* packed, uint16_t* out, int64_t n, int64_t k,
-                                 int group, int has_zp, bool fp16, bool nv, int gated,
-                                 cudaStream_t stream);
+                                 int group, int has_zp, bool fp16, bool nv, bool f16s,
+                                 int gated, cudaStream_t stream);
 
 cudaError_t launch_repack_nvfp4(const uint8_t* codes, const uint8_t* scales,
                                const float* tensor_scales, uint8_t* packed, int64_t n, int64_t k,

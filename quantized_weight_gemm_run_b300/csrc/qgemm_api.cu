@@ -111,9 +111,8 @@ static qgemm_status check_layer(const qgemm_layer_config* L) {
         return fail(QGEMM_ERR_UNSUPPORTED, "W4A16 output dtype must equal the activation dtype");
       if (L->scale_format != QGEMM_S_FP16 && L->scale_format != QGEMM_S_BF16)
         return fail(QGEMM_ERR_UNSUPPORTED, "W4A16 scales must be fp16 or bf16");
-      if ((L->scale_format == QGEMM_S_FP16) != (L->act_dtype == QGEMM_FP16))
-        return fail(QGEMM_ERR_UNSUPPORTED,
-                    "W4A16 scale dtype must equal the activation dtype (dequant runs in it)");
+      if (L->scale_format == QGEMM_S_BF16 && L->act_dtype == QGEMM_FP16)
+        return fail(QGEMM_ERR_UNSUPPORTED, "bf16 scales need bf16 activations");
       const int g = L->group_size;
       const bool g_ok = g == 32 || g == 64 || (g >= 128 && g % 128 == 0);
       if (!g_ok) return fail(QGEMM_ERR_UNSUPPORTED, "group size %d not in {32, 64, 128j}", g);
@@ -165,6 +164,10 @@ static int st_of(int group) { return group < kTileK ? kTileK / group : 1; }
 
 static bool is_mx(const qgemm_layer_config* L) { return L->weight_format == QGEMM_W_MXFP4; }
 static bool is_nv(const qgemm_layer_config* L) { return L->weight_format == QGEMM_W_NVFP4; }
+// W4A16 with fp16 scales against bf16 activations
+static bool is_f16s(const qgemm_layer_config* L) {
+  return !is_mx(L) && !is_nv(L) && L->scale_format == QGEMM_S_FP16 && L->act_dtype == QGEMM_BF16;
+}
 
 // Bytes of one expert's packed blocks (an NVFP4 buffer adds the tensor-scale
 // tail after the last expert).
@@ -264,13 +267,14 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   const int has_zp = L->zero_format == QGEMM_Z_UINT4;
   if (T && (T->kernel < 0 || T->kernel > 2))
     return fail(QGEMM_ERR_INVALID_ARG, "kernel must be 0, 1 or 2");
-  const bool mma_ok = !grouped && !is_mx(L) && !is_nv(L) && L->gated_act == 0 && rows <= 16 &&
-                      !(C && (C->deterministic || C->batch_invariant));
+  const bool mma_ok = !grouped && !is_mx(L) && !is_nv(L) && !is_f16s(L) && L->gated_act == 0 &&
+                      rows <= 16 && !(C && (C->deterministic || C->batch_invariant));
   const int want = T ? T->kernel : 0;
   if (want == 2 && !mma_ok)
     return fail(QGEMM_ERR_UNSUPPORTED,
-                "the small-M kernel takes dense INT4/UINT4 GEMMs with m <= 16 that are not "
-                "gated, deterministic or batch-invariant");
+                "the small-M kernel takes dense INT4/UINT4 GEMMs with m <= 16 whose scales are "
+                "in the activation dtype and that are not gated, deterministic or "
+                "batch-invariant");
   P->kernel = 1;
   P->mma_splits = 0;
   const int64_t ntl = L->n / kTileN, ktl = L->k / kTileK;
@@ -575,8 +579,9 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
                       n_out * 2, p.gated ? 16 : 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
     return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the output tensor");
   cudaError_t e =
-      launch_w4a16(tmap, tmap_c, p, P.bt, mx ? 2 : is_nv(L) ? (fp16 ? 4 : 3) : fp16 ? 1 : 0,
-                   grouped, P.grid, stream);
+      launch_w4a16(tmap, tmap_c, p, P.bt,
+                   mx ? 2 : is_nv(L) ? (fp16 ? 4 : 3) : is_f16s(L) ? 5 : fp16 ? 1 : 0, grouped,
+                   P.grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "W4A16 GEMM launch");
   return ok();
 }
@@ -783,7 +788,7 @@ qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* pa
     e = launch_debug_dequant(static_cast<const uint8_t*>(packed), static_cast<uint16_t*>(out_kn),
                              layer->n, layer->k, layer->group_size,
                              layer->zero_format == QGEMM_Z_UINT4 ? 1 : 0,
-                             layer->act_dtype == QGEMM_FP16, is_nv(layer),
+                             layer->act_dtype == QGEMM_FP16, is_nv(layer), is_f16s(layer),
                              layer->gated_act != 0, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
   return ok();
@@ -826,16 +831,17 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
     } else {
       static const char* wf[] = {"int4_sym", "uint4_zp", "mxfp4", "nvfp4"};
       static const char* dt[] = {"fp16", "bf16", "fp8e4m3"};
+      static const char* sf[] = {"fp16", "bf16", "e8m0", "e4m3"};
       char tmp[512];
       snprintf(tmp, sizeof(tmp),
-               "kernel=%s%s weights=%s group=%d act=%s out=%s n=%lld k=%lld "
+               "kernel=%s%s weights=%s group=%d scales=%s act=%s out=%s n=%lld k=%lld "
                "m=%lld experts=%d block_tok=%d act_slots=%d weight_slots=%dx%d grid=%d smem=%d "
                "workspace=%zu epilogue=%s split=%s "
                "device=sm_103",
                P.kernel == 2 ? "w4a16_mma_sync_smallm"
                : is_mx(layer) ? "w4a8_tcgen05_mxf8f6f4_swapab" : "w4a16_tcgen05_swapab",
                grouped ? "_grouped" : "", wf[layer->weight_format], layer->group_size,
-               dt[layer->act_dtype], dt[layer->out_dtype], (long long)layer->n,
+               sf[layer->scale_format], dt[layer->act_dtype], dt[layer->out_dtype], (long long)layer->n,
                (long long)layer->k, (long long)m, layer->num_experts, P.bt, P.g.x_stages,
                P.g.w_stages, P.g.rw, P.grid, P.g.smem, P.ws.total,
                layer->gated_act ? "silu_glu" : "plain",

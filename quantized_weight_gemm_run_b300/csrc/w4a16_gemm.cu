@@ -242,6 +242,33 @@ __device__ __forceinline__ void dequant_vec(const uint4 v, uint32_t zero2, uint3
   }
 }
 
+// bf16 activations with fp16 scales: w^ = bf16((q - z) * s), one rounding.
+// The bf16 pair (128 + u, 128 + u') minus the zero pair gives the integers
+// q - z exactly; each widens to fp32 by moving its 16 bits up, and its
+// product with the scale (an fp16 value held in fp32) is exact (at most 5 x
+// 11 significant bits), so cvt.rn rounds the exact value once.  Non-finite
+// scales give the products IEEE arithmetic gives.
+__device__ __forceinline__ void dequant_vec_f16s(const uint4 v, uint32_t zero2, float s,
+                                                 uint32_t (&out)[16]) {
+  constexpr uint32_t magic = 0x43004300u;
+  const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+  const __nv_bfloat162 zz = *reinterpret_cast<const __nv_bfloat162*>(&zero2);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t x = lop3_and_or(wds[w] >> (4 * i), 0x000F000Fu, magic);
+      __nv_bfloat162 d2 = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&x), zz);
+      const uint32_t d = *reinterpret_cast<uint32_t*>(&d2);
+      const float lo = __uint_as_float(d << 16) * s;
+      const float hi = __uint_as_float(d & 0xFFFF0000u) * s;
+      uint32_t r;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+      out[w * 4 + i] = r;
+    }
+  }
+}
+
 // 32 e2m1 codes (one 16-byte vector, k in nibble order, low nibble first) ->
 // 32 e4m3 bytes, exactly (every e2m1 value is an e4m3 value).  prmt looks up
 // the e4m3 byte of the 3-bit magnitude in an 8-entry byte table; a second
@@ -338,7 +365,9 @@ __device__ __forceinline__ float from_out(uint16_t b) {
 }
 
 // FMT: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 weights, e4m3
-// activations with per-row fp32 scales, block-scaled MMA, bf16 output).
+// activations with per-row fp32 scales, block-scaled MMA, bf16 output),
+// 3 / 4 = NVFP4 weights with bf16 / fp16 activations, 5 = W4A16 bf16
+// activations with fp16 scales.
 //
 // Shared memory holds two rings that turn over independently:
 //   activation slots: RX = units_per_stage(BT) consecutive k-tiles ("units")
@@ -355,7 +384,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                  const __grid_constant__ CUtensorMap tmap_c, const W4A16Params p) {
   constexpr bool FP16 = FMT == 1 || FMT == 4;   // 16-bit activations and output: fp16
   constexpr bool MX = FMT == 2;                  // W4A8-MXFP4
-  constexpr bool NV = FMT >= 3;                  // NVFP4 weights, 16-bit activations
+  constexpr bool NV = FMT == 3 || FMT == 4;      // NVFP4 weights, 16-bit activations
+  constexpr bool F16S = FMT == 5;                // bf16 activations, fp16 scales
   constexpr int RX = units_per_stage(BT);
   // tensor-memory columns: dequantized weight slots, then (MX) the A and B
   // scale factors, accumulators from column 256
@@ -735,7 +765,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                   zero2[t][j] = (uint32_t)sv[(2 * j + 1) * kTileN + row] * 0x00010001u;
                 } else {
                   const int sg = j >> p.sg_shift;
-                  scale2[t][j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
+                  if constexpr (F16S)   // the fp16 scale, widened (exactly) to fp32
+                    scale2[t][j] =
+                        __float_as_uint(__half2float(__ushort_as_half(sv[sg * kTileN + row])));
+                  else
+                    scale2[t][j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
                   const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
                   zero2[t][j] = (magic16 + zq) * 0x00010001u;
                 }
@@ -777,6 +811,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               uint32_t out[16];
               if constexpr (NV)
                 dequant_vec_nv<FP16>(v[t][j], scale2[t][j], zero2[t][j], out);
+              else if constexpr (F16S)
+                dequant_vec_f16s(v[t][j], zero2[t][j], __uint_as_float(scale2[t][j]), out);
               else
                 dequant_vec<FP16>(v[t][j], zero2[t][j], scale2[t][j], out);
               tmem_st16(tbase + j * 16, out);
@@ -1177,6 +1213,8 @@ cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
                            : launch_bt<3, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
     case 4: return grouped ? launch_bt<4, true>(tmap_a, tmap_c, p, block_tok, grid, stream)
                            : launch_bt<4, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
+    case 5: return grouped ? launch_bt<5, true>(tmap_a, tmap_c, p, block_tok, grid, stream)
+                           : launch_bt<5, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1185,7 +1223,8 @@ cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
 
 // out[k, n] = the value the GEMM kernel feeds the tensor core for W^[k, n]
 // (NVFP4: e2m1 x block scale; the tensor scale is applied to the fp32 sum).
-template <bool FP16, bool NV>
+// F16S: bf16 output from fp16 scales.
+template <bool FP16, bool NV, bool F16S>
 __global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n, int k,
                                      int group, int has_zp, int gated) {
   const int KT = k / kTileK;
@@ -1210,6 +1249,9 @@ __global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n
     const uint16_t* sv = reinterpret_cast<const uint16_t*>(bp + kTileBytes);
     dequant_vec_nv<FP16>(wv, (uint32_t)sv[(2 * j) * kTileN + row] * 0x00010001u,
                          (uint32_t)sv[(2 * j + 1) * kTileN + row] * 0x00010001u, o);
+  } else if constexpr (F16S) {
+    dequant_vec_f16s(wv, (magic16 + zq) * 0x00010001u,
+                     __half2float(__ushort_as_half((uint16_t)sbits)), o);
   } else {
     dequant_vec<FP16>(wv, (magic16 + zq) * 0x00010001u, sbits * 0x00010001u, o);
   }
@@ -1223,13 +1265,16 @@ __global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n
 }
 
 cudaError_t launch_debug_dequant(const uint8_t* packed, uint16_t* out, int64_t n, int64_t k,
-                                 int group, int has_zp, bool fp16, bool nv, int gated,
-                                 cudaStream_t stream) {
+                                 int group, int has_zp, bool fp16, bool nv, bool f16s,
+                                 int gated, cudaStream_t stream) {
   const long long total = (n / kTileN) * (k / kTileK) * 512;
   const int threads = 256;
   const unsigned blocks = (unsigned)((total + threads - 1) / threads);
-  auto kern = fp16 ? (nv ? debug_dequant_kernel<true, true> : debug_dequant_kernel<true, false>)
-                   : (nv ? debug_dequant_kernel<false, true> : debug_dequant_kernel<false, false>);
+  auto kern = fp16   ? (nv ? debug_dequant_kernel<true, true, false>
+                           : debug_dequant_kernel<true, false, false>)
+              : nv   ? debug_dequant_kernel<false, true, false>
+              : f16s ? debug_dequant_kernel<false, false, true>
+                     : debug_dequant_kernel<false, false, false>;
   kern<<<blocks, threads, 0, stream>>>(packed, out, (int)n, (int)k, group, has_zp, gated);
   return cudaGetLastError();
 }

@@ -16,18 +16,20 @@ DEV = "cuda"
 class Case:
     """One W4A16 problem, quantized by the oracle from seeded fp32 data."""
 
-    def __init__(self, m, n, k, g, adt, sym, seed=0, bias=False):
+    def __init__(self, m, n, k, g, adt, sym, seed=0, bias=False, sdt=None):
         r = synth.rng(seed)
         w = synth.weights_fp32(r, k, n)
+        sdt = adt if sdt is None else sdt             # the scale dtype
         self.a = codecs.round_dtype(adt)(synth.activations_fp32(r, m, k))
         if sym:
-            self.q, self.s = quant.quantize_int4_sym(w, g, adt)
+            self.q, self.s = quant.quantize_int4_sym(w, g, sdt)
             self.z = None
         else:
-            self.q, self.s, self.z = quant.quantize_uint4_asym(w, g, adt)
+            self.q, self.s, self.z = quant.quantize_uint4_asym(w, g, sdt)
         self.m, self.n, self.k, self.g, self.adt, self.sym = m, n, k, g, adt, sym
+        self.sdt = sdt
         self.qweight = quant.pack_int4_kn(self.q, sym)
-        self.s_bits = codecs.dtype_bits(adt, self.s)
+        self.s_bits = codecs.dtype_bits(sdt, self.s)
         self.qzeros = None if self.z is None else quant.pack_zeros(self.z)
         self.w_hat = quant.dequant_int(self.q, self.s, self.z, g, adt)
         self.bias = codecs.round_dtype(adt)(r.standard_normal(n) * 0.5) if bias else None
@@ -55,7 +57,7 @@ def linear(case: Case, tuning=None, deterministic=False):
     from quantized_weight_gemm_run_b300.api import W4A16Linear
     qw, sc, qz = case.dev_weights()
     return W4A16Linear(qw, sc, qz, case.n, case.k, case.g, TD[case.adt], bias=case.dev_bias(),
-                       tuning=tuning, deterministic=deterministic)
+                       tuning=tuning, deterministic=deterministic, scale_dtype=TD[case.sdt])
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:

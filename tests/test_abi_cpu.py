@@ -70,6 +70,10 @@ def test_packed_size_host_only(Q):
     st, b = Q.qgemm_packed_size(_layer(Q, act_dtype=Q.QGEMM_BF16, out_dtype=Q.QGEMM_BF16,
                                        scale_format=Q.QGEMM_S_BF16, gated_act=1))
     assert st == Q.QGEMM_OK and b == blocks * (8192 + 256)
+    # fp16 scales against bf16 activations: the scales keep their 16 bits
+    st, b = Q.qgemm_packed_size(_layer(Q, act_dtype=Q.QGEMM_BF16, out_dtype=Q.QGEMM_BF16,
+                                       scale_format=Q.QGEMM_S_FP16))
+    assert st == Q.QGEMM_OK and b == blocks * (8192 + 256)
 
 
 @pytest.mark.parametrize("bad,code", [
@@ -79,7 +83,7 @@ def test_packed_size_host_only(Q):
     (dict(group_size=384), "UNSUPPORTED"),          # does not divide K = 4096
     (dict(zero_format=1), "UNSUPPORTED"),           # zeros with symmetric INT4
     (dict(out_dtype=1), "UNSUPPORTED"),             # W4A16 output dtype differs
-    (dict(scale_format=1), "UNSUPPORTED"),          # scale dtype differs from act dtype
+    (dict(scale_format=1), "UNSUPPORTED"),          # bf16 scales with fp16 activations
     (dict(weight_format=2, scale_format=2, group_size=32, act_dtype=2, out_dtype=1,
           zero_format=1), "UNSUPPORTED"),          # zero points with MXFP4
     (dict(weight_format=9), "UNSUPPORTED"),

@@ -61,6 +61,25 @@ def test_int4_sym_brute_force_small():
                 assert q[32 * gi + i, n] == qq
 
 
+def test_fp16_scales_with_bf16_activations_every_scale():
+    """Every integer q - z in [-15, 15] against every finite fp16 scale: the
+    oracle's one rounding to bf16 equals torch's round-to-nearest-even cast of
+    the fp32 product (exact: 5 x 11 significant bits), and differs from
+    rounding the scale to bf16 first on many of them."""
+    import torch
+    s16 = np.arange(1 << 16, dtype=np.uint16).view(np.float16)
+    s16 = s16[np.isfinite(s16)].astype(np.float64)
+    d = np.arange(-15, 16, dtype=np.float64)
+    q = np.repeat(d[:, None], s16.size, axis=1)
+    s = np.repeat(s16[None, :], d.size, axis=0)
+    got = quant.dequant_int(q, s, None, 1, "bf16")
+    prod = torch.from_numpy(q).float() * torch.from_numpy(s).float()
+    want = prod.to(torch.bfloat16).double().numpy()
+    assert np.array_equal(got, want)
+    pre = quant.dequant_int(q, codecs.round_dtype("bf16")(s), None, 1, "bf16")
+    assert (pre != got).sum() > 1000
+
+
 def test_int4_zero_group_scale_is_one():
     w = np.zeros((128, 8), dtype=np.float32)
     q, s = quant.quantize_int4_sym(w, 128, "bf16")
