@@ -243,28 +243,44 @@ __device__ __forceinline__ void dequant_vec(const uint4 v, uint32_t zero2, uint3
 }
 
 // bf16 activations with fp16 scales: w^ = bf16((q - z) * s), one rounding.
-// The bf16 pair (128 + u, 128 + u') minus the zero pair gives the integers
-// q - z exactly; each widens to fp32 by moving its 16 bits up, and its
-// product with the scale (an fp16 value held in fp32) is exact (at most 5 x
-// 11 significant bits), so cvt.rn rounds the exact value once.  Non-finite
-// scales give the products IEEE arithmetic gives.
-__device__ __forceinline__ void dequant_vec_f16s(const uint4 v, uint32_t zero2, float s,
-                                                 uint32_t (&out)[16]) {
+// The scale is split into s_hi, its leading 8 significant bits (a bf16), and
+// the rest s_lo = s - s_hi, which has at most 3 significant bits (an fp16 has
+// 11) and the sign of s, so it is a bf16 too.  With d = q - z (an integer of
+// at most 4 bits, exact in bf16), t = d * s_lo has at most 7 significant bits
+// and is exact, and fma(d, s_hi, t) rounds the exact d * s once.  Zero
+// results carry the sign of d * s: both terms are then zeros of that sign.
+__device__ __forceinline__ void split_f16_scale(uint16_t bits, uint32_t& hi2, uint32_t& lo2) {
+  const float s = __half2float(__ushort_as_half(bits));
+  uint32_t hi, lo;
+  if (isfinite(s)) {
+    const uint32_t sb = __float_as_uint(s);
+    const float rest = s - __uint_as_float(sb & 0xFFFF0000u);   // exact
+    hi = sb >> 16;
+    lo = (__float_as_uint(rest) >> 16) | ((sb >> 16) & 0x8000u);
+  } else {   // inf or NaN: the products d * s of IEEE arithmetic
+    const __nv_bfloat16 b = __float2bfloat16_rn(s);
+    hi = *reinterpret_cast<const uint16_t*>(&b);
+    lo = 0;
+  }
+  hi2 = hi * 0x00010001u;
+  lo2 = lo * 0x00010001u;
+}
+
+__device__ __forceinline__ void dequant_vec_f16s(const uint4 v, uint32_t zero2, uint32_t hi2,
+                                                 uint32_t lo2, uint32_t (&out)[16]) {
   constexpr uint32_t magic = 0x43004300u;
   const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
   const __nv_bfloat162 zz = *reinterpret_cast<const __nv_bfloat162*>(&zero2);
+  const __nv_bfloat162 sh = *reinterpret_cast<const __nv_bfloat162*>(&hi2);
+  const __nv_bfloat162 sl = *reinterpret_cast<const __nv_bfloat162*>(&lo2);
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       uint32_t x = lop3_and_or(wds[w] >> (4 * i), 0x000F000Fu, magic);
-      __nv_bfloat162 d2 = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&x), zz);
-      const uint32_t d = *reinterpret_cast<uint32_t*>(&d2);
-      const float lo = __uint_as_float(d << 16) * s;
-      const float hi = __uint_as_float(d & 0xFFFF0000u) * s;
-      uint32_t r;
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-      out[w * 4 + i] = r;
+      const __nv_bfloat162 d = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&x), zz);
+      __nv_bfloat162 r = __hfma2(d, sh, __hmul2(d, sl));
+      out[w * 4 + i] = *reinterpret_cast<uint32_t*>(&r);
     }
   }
 }
@@ -745,6 +761,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const int i0 = ((unit & 1) == h) ? 0 : 1;   // this group's units: i0, i0 + 2
         uint4 v[2][4];
         uint32_t scale2[2][4], zero2[2][4], sf[2];
+        [[maybe_unused]] uint32_t lo2[2][4];   // F16S: the scales' low terms
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int i = i0 + 2 * t;
@@ -765,9 +782,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                   zero2[t][j] = (uint32_t)sv[(2 * j + 1) * kTileN + row] * 0x00010001u;
                 } else {
                   const int sg = j >> p.sg_shift;
-                  if constexpr (F16S)   // the fp16 scale, widened (exactly) to fp32
-                    scale2[t][j] =
-                        __float_as_uint(__half2float(__ushort_as_half(sv[sg * kTileN + row])));
+                  if constexpr (F16S)   // the fp16 scale as two bf16 terms (pairs)
+                    split_f16_scale(sv[sg * kTileN + row], scale2[t][j], lo2[t][j]);
                   else
                     scale2[t][j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
                   const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
@@ -812,7 +828,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               if constexpr (NV)
                 dequant_vec_nv<FP16>(v[t][j], scale2[t][j], zero2[t][j], out);
               else if constexpr (F16S)
-                dequant_vec_f16s(v[t][j], zero2[t][j], __uint_as_float(scale2[t][j]), out);
+                dequant_vec_f16s(v[t][j], zero2[t][j], scale2[t][j], lo2[t][j], out);
               else
                 dequant_vec<FP16>(v[t][j], zero2[t][j], scale2[t][j], out);
               tmem_st16(tbase + j * 16, out);
@@ -1250,8 +1266,9 @@ __global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n
     dequant_vec_nv<FP16>(wv, (uint32_t)sv[(2 * j) * kTileN + row] * 0x00010001u,
                          (uint32_t)sv[(2 * j + 1) * kTileN + row] * 0x00010001u, o);
   } else if constexpr (F16S) {
-    dequant_vec_f16s(wv, (magic16 + zq) * 0x00010001u,
-                     __half2float(__ushort_as_half((uint16_t)sbits)), o);
+    uint32_t hi2, lo2;
+    split_f16_scale((uint16_t)sbits, hi2, lo2);
+    dequant_vec_f16s(wv, (magic16 + zq) * 0x00010001u, hi2, lo2, o);
   } else {
     dequant_vec<FP16>(wv, (magic16 + zq) * 0x00010001u, sbits * 0x00010001u, o);
   }
