@@ -49,6 +49,16 @@ e4m3 scale per 16 consecutive k of one column, one fp32 scale per tensor):
 ``rint`` rounds half to even.  The product (q - z) * s is exact in float64
 (a 5-bit integer times an 8- or 11-bit significand), so w^ is rounded once.
 
+Other integer widths b (the pages list weight-only formats WNA16 with N
+free, kinachrichten.com "Warum quantisierte Kernel wichtig sind", and name
+GPTQ INT3 as a format the library serves, jetabc.cn post "怎么使用"; they
+define neither, so the INT4 rules above are read with 2^b levels):
+    symmetric:  s = sdt(amax / (2^(b-1) - 1)),  q = clip(rint(W/s), -2^(b-1), 2^(b-1) - 1)
+    asymmetric: s = sdt((hi - lo) / (2^b - 1)), z = clip(rint(-lo/s), 0, 2^b - 1),
+                q = clip(rint(W/s) + z, 0, 2^b - 1)
+    w^ = adt((q - z) * s), one rounding (at most 9 x 11 significant bits for
+    b = 8, exact in float64).
+
 Standard-format encoding (the tensors the library's pack entry point takes):
     qweight int32 [K/8, N]: word (j, n) holds k = 8j + i in bits [4i, 4i+4),
             least significant nibble first; INT4 as 4-bit two's complement,
@@ -56,6 +66,14 @@ Standard-format encoding (the tensors the library's pack entry point takes):
     scales  [K/g, N] row-major (group-major), in the scale dtype.
     qzeros  int32 [K/g, N/8]: nibble i of word (G, j) is the zero of column
             8j + i (the stored zero is the true zero, no "-1" offset).
+    INT8 / UINT8 (W8A16): qweight int32 [K/4, N]: word (j, n) holds
+            k = 4j + i in bits [8i, 8i+8) (two's complement or raw);
+            qzeros int32 [K/g, N/4], column 4j + i in byte i of word (G, j).
+    INT3 / UINT3 (GPTQ): 32 consecutive codes of a column fill three int32
+            words as one little-endian 96-bit stream: k = 32j + i occupies
+            bits [3i, 3i+3) of word(3j) | word(3j+1) << 32 | word(3j+2) << 64,
+            so qweight is int32 [3K/32, N]; qzeros int32 [K/g, 3N/32] holds
+            32 consecutive columns' zeros the same way.
     MXFP4:  codes uint8 [N, K/2]: byte (n, j) holds k = 2j in the low nibble
             and k = 2j + 1 in the high nibble; e2m1 bits are s|e1 e0|m.
             scales uint8 e8m0 [N, K/32].
@@ -103,6 +121,35 @@ def quantize_uint4_asym(w, g: int, sdt: str):
     s = np.where(hi == lo, 1.0, s)
     z = np.clip(np.rint(-lo / s), 0, 15)
     q = np.clip(np.rint(wg / s[:, None, :]) + z[:, None, :], 0, 15)
+    return q.reshape(w.shape).astype(np.int64), s, z.astype(np.int64)
+
+
+def quantize_int_sym(w, g: int, sdt: str, bits: int):
+    """Symmetric b-bit integer quantization (b = 3, 4 or 8).  Returns
+    (q int64 [K,N] in [-2^(b-1), 2^(b-1) - 1], s float64 [K/g, N])."""
+    w = np.asarray(w, dtype=np.float64)
+    wg = _grouped(w, g)
+    top = 2 ** (bits - 1) - 1
+    amax = np.max(np.abs(wg), axis=1)
+    s = codecs.round_dtype(sdt)(amax / top)
+    s = np.where(amax == 0, 1.0, s)
+    q = np.clip(np.rint(wg / s[:, None, :]), -top - 1, top)
+    return q.reshape(w.shape).astype(np.int64), s
+
+
+def quantize_uint_asym(w, g: int, sdt: str, bits: int):
+    """Asymmetric b-bit quantization with min/max range (b = 3, 4 or 8).
+    Returns (q int64 [K,N] in [0, 2^b - 1], s float64 [K/g,N], z int64
+    [K/g,N] in [0, 2^b - 1])."""
+    w = np.asarray(w, dtype=np.float64)
+    wg = _grouped(w, g)
+    top = 2 ** bits - 1
+    lo = np.min(wg, axis=1)
+    hi = np.max(wg, axis=1)
+    s = codecs.round_dtype(sdt)((hi - lo) / top)
+    s = np.where(hi == lo, 1.0, s)
+    z = np.clip(np.rint(-lo / s), 0, top)
+    q = np.clip(np.rint(wg / s[:, None, :]) + z[:, None, :], 0, top)
     return q.reshape(w.shape).astype(np.int64), s, z.astype(np.int64)
 
 
@@ -234,6 +281,70 @@ def unpack_zeros(qzeros) -> np.ndarray:
     for i in range(8):
         out[:, :, i] = (w >> np.uint64(4 * i)) & np.uint64(0xF)
     return out.reshape(gk, nw * 8)
+
+
+def pack_bits(v, bits: int) -> np.ndarray:
+    """Codes v [L, ...] (as raw b-bit patterns, 0 <= v < 2^b) -> int32 words
+    [L*b/32, ...]: code i of the stream occupies bits [b*i, b*i + b) of the
+    little-endian concatenation of the words (a code may straddle two)."""
+    v = np.asarray(v, dtype=np.int64)
+    if (v.shape[0] * bits) % 32:
+        raise ValueError("the stream must fill whole words")
+    if v.min(initial=0) < 0 or v.max(initial=0) >= 2 ** bits:
+        raise ValueError("code out of range")
+    words = np.zeros((v.shape[0] * bits // 32,) + v.shape[1:], dtype=np.uint64)
+    for i in range(v.shape[0]):
+        bit = bits * i
+        wi, off = bit // 32, bit % 32
+        x = v[i].astype(np.uint64)
+        words[wi] |= (x << np.uint64(off)) & np.uint64(0xFFFFFFFF)
+        if off + bits > 32:
+            words[wi + 1] |= x >> np.uint64(32 - off)
+    return words.astype(np.uint32).view(np.int32)
+
+
+def unpack_bits(words, bits: int) -> np.ndarray:
+    """Inverse of ``pack_bits``: int32 words [W, ...] -> codes [32*W/b, ...]."""
+    w = np.asarray(words).view(np.uint32).astype(np.uint64)
+    count = w.shape[0] * 32 // bits
+    out = np.empty((count,) + w.shape[1:], dtype=np.int64)
+    mask = np.uint64(2 ** bits - 1)
+    for i in range(count):
+        bit = bits * i
+        wi, off = bit // 32, bit % 32
+        x = w[wi] >> np.uint64(off)
+        if off + bits > 32:
+            x |= w[wi + 1] << np.uint64(32 - off)
+        out[i] = (x & mask).astype(np.int64)
+    return out
+
+
+def pack_int_kn(q, bits: int, signed: bool) -> np.ndarray:
+    """Codes [K, N] of b bits -> qweight int32 [K*b/32, N] (b = 8: four codes
+    a word; b = 3: 32 codes in three words), two's complement when signed."""
+    q = np.asarray(q, dtype=np.int64)
+    lo, hi = (-(2 ** (bits - 1)), 2 ** (bits - 1) - 1) if signed else (0, 2 ** bits - 1)
+    if q.min(initial=lo) < lo or q.max(initial=hi) > hi:
+        raise ValueError("code out of range")
+    return pack_bits(q & (2 ** bits - 1), bits)
+
+
+def unpack_int_kn(qweight, bits: int, signed: bool) -> np.ndarray:
+    """Inverse of ``pack_int_kn``."""
+    out = unpack_bits(qweight, bits)
+    if signed:
+        out = np.where(out >= 2 ** (bits - 1), out - 2 ** bits, out)
+    return out
+
+
+def pack_zeros_bits(z, bits: int) -> np.ndarray:
+    """Zeros [K/g, N] of b bits -> qzeros int32 [K/g, N*b/32], packed along N
+    like ``pack_bits`` (b = 4 gives ``pack_zeros``)."""
+    return np.ascontiguousarray(pack_bits(np.asarray(z).T, bits).T)
+
+
+def unpack_zeros_bits(qzeros, bits: int) -> np.ndarray:
+    return np.ascontiguousarray(unpack_bits(np.asarray(qzeros).T, bits).T)
 
 
 def pack_mxfp4(codes_kn, b_kn):

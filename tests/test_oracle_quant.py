@@ -440,3 +440,103 @@ def test_packed_nvfp4_scalar_spec(adt):
         assert codecs.dtype_from_bits(adt, np.array([bits]))[0] == codecs.decode_e4m3(sb[nn, kk // 16])
     tail = layout.nvfp4_tail([0.5, 2.0, -1.0])
     assert tail.size == 16 and list(tail.view(np.float32)) == [0.5, 2.0, -1.0, 0.0]
+
+
+# ------------------------------------------------ other integer widths (8 and 3 bits)
+
+def test_bitstream_handbuilt_words():
+    # INT3: the codes 0..7 repeated over 32 k are the octal digits 76543210
+    # (0xFAC688) four times over 96 bits, least significant code first:
+    # 0xFAC688FAC688FAC688FAC688 -> words (low first) 88FAC688, C688FAC6, FAC688FA.
+    q = np.tile(np.arange(8), 4)[:, None]
+    words = quant.pack_int_kn(q, 3, signed=False)[:, 0].view(np.uint32)
+    assert [int(x) for x in words] == [0x88FAC688, 0xC688FAC6, 0xFAC688FA]
+    assert np.array_equal(quant.unpack_int_kn(words.view(np.int32)[:, None], 3, False), q)
+    # signed INT3 -4..3 are the raw patterns 4, 5, 6, 7, 0, 1, 2, 3: octal
+    # 32107654 = 0x688FAC per eight codes
+    sq = np.tile(np.array([-4, -3, -2, -1, 0, 1, 2, 3]), 4)[:, None]
+    sw = quant.pack_int_kn(sq, 3, signed=True)[:, 0].view(np.uint32)
+    assert [int(x) for x in sw] == [0xAC688FAC, 0x8FAC688F, 0x688FAC68]
+    assert np.array_equal(quant.unpack_int_kn(sw.view(np.int32)[:, None], 3, True), sq)
+    # INT8: the bytes of k = 0..3, least significant first
+    q8 = np.array([[0], [1], [127], [-128]])
+    assert int(quant.pack_int_kn(q8, 8, signed=True)[0, 0].view(np.uint32)) == 0x807F0100
+    assert int(quant.pack_int_kn(np.array([[1], [2], [3], [4]]), 8, False)[0, 0]) == 0x04030201
+    # zeros pack along N the same way: a zero of 5 in 32 columns is the bit
+    # pattern 101 repeated from bit 0 (nibbles D, 6, B, ...)
+    zw = quant.pack_zeros_bits(np.full((1, 32), 5), 3)[0].view(np.uint32)
+    assert [int(x) for x in zw] == [0x6DB6DB6D, 0xDB6DB6DB, 0xB6DB6DB6]
+
+
+def test_bitstream_of_four_bits_is_the_nibble_layout():
+    g = synth.rng(11)
+    q = g.integers(-8, 8, size=(64, 24))
+    assert np.array_equal(quant.pack_int_kn(q, 4, signed=True), quant.pack_int4_kn(q, True))
+    z = g.integers(0, 16, size=(3, 32))
+    assert np.array_equal(quant.pack_zeros_bits(z, 4), quant.pack_zeros(z))
+
+
+@pytest.mark.parametrize("bits", [3, 8])
+@pytest.mark.parametrize("signed", [True, False])
+def test_bitstream_round_trip_every_code(bits, signed):
+    lo = -(2 ** (bits - 1)) if signed else 0
+    k = 32 * 2 ** bits // 8 if bits == 8 else 96
+    g = synth.rng(12 + bits)
+    q = (np.arange(k * 5).reshape(k, 5) % (2 ** bits)) + lo
+    q = g.permuted(q, axis=0)
+    words = quant.pack_int_kn(q, bits, signed)
+    assert words.shape == (k * bits // 32, 5) and words.dtype == np.int32
+    assert np.array_equal(quant.unpack_int_kn(words, bits, signed), q)
+    z = g.integers(0, 2 ** bits, size=(4, 64))
+    assert np.array_equal(quant.unpack_zeros_bits(quant.pack_zeros_bits(z, bits), bits), z)
+    with pytest.raises(ValueError):
+        quant.pack_int_kn(q[:, :1] * 0 + (2 ** bits if not signed else 2 ** (bits - 1)), bits,
+                          signed)
+
+
+def test_four_bit_quantizers_are_the_int4_ones():
+    g = synth.rng(13)
+    w = synth.weights_fp32(g, 256, 16)
+    q, s = quant.quantize_int_sym(w, 64, "bf16", 4)
+    q4, s4 = quant.quantize_int4_sym(w, 64, "bf16")
+    assert np.array_equal(q, q4) and np.array_equal(s, s4)
+    q, s, z = quant.quantize_uint_asym(w, 64, "fp16", 4)
+    q4, s4, z4 = quant.quantize_uint4_asym(w, 64, "fp16")
+    assert np.array_equal(q, q4) and np.array_equal(s, s4) and np.array_equal(z, z4)
+
+
+@pytest.mark.parametrize("bits", [3, 8])
+def test_int_quantizer_invariants(bits):
+    g = synth.rng(14 + bits)
+    w = synth.weights_fp32(g, 512, 48)
+    top = 2 ** (bits - 1) - 1
+    q, s = quant.quantize_int_sym(w, 128, "fp16", bits)
+    assert q.min() >= -top - 1 and q.max() <= top
+    assert np.array_equal(codecs.round_dtype("fp16")(s), s)
+    full = np.repeat(s, 128, axis=0)
+    err = np.abs(w.astype(np.float64) - q * full)
+    inside = (q > -top - 1) & (q < top)
+    assert np.all(err[inside] <= full[inside] / 2 * (1 + 1e-12))
+    arg = np.abs(w.astype(np.float64)).reshape(4, 128, 48).argmax(axis=1)
+    peak = np.take_along_axis(q.reshape(4, 128, 48), arg[:, None, :], axis=1)[:, 0, :]
+    assert np.all(np.abs(peak) >= top)
+    q, s, z = quant.quantize_uint_asym(w, 128, "bf16", bits)
+    assert q.min() >= 0 and q.max() <= 2 ** bits - 1 and z.min() >= 0 and z.max() <= 2 ** bits - 1
+    full_z = np.repeat(z, 128, axis=0)
+    full = np.repeat(s, 128, axis=0)
+    err = np.abs(w.astype(np.float64) - (q - full_z) * full)
+    inside = (q > 0) & (q < 2 ** bits - 1)
+    assert np.all(err[inside] <= full[inside] / 2 * (1 + 1e-12))
+
+
+def test_int8_sym_brute_force_small():
+    g = synth.rng(15)
+    w = synth.weights_fp32(g, 64, 4)
+    q, s = quant.quantize_int_sym(w, 32, "bf16", 8)
+    for gi in range(2):
+        for n in range(4):
+            col = [float(w[k, n]) for k in range(32 * gi, 32 * gi + 32)]
+            sv = float(codecs.bf16(np.array(max(abs(v) for v in col) / 127.0)))
+            assert s[gi, n] == sv
+            for i, v in enumerate(col):
+                assert q[32 * gi + i, n] == max(-128, min(127, int(np.rint(v / sv))))
