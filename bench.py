@@ -74,6 +74,11 @@ def workload_points(name):
         return sweep_points(), dict(workload="w4a16_asym_sweep", shapes=synth.W4A16_ASYM_SHAPES,
                                     ms=synth.W4A16_ASYM_MS, group=128, weights="uint4+zp",
                                     act="bf16")
+    if name == "w8a16":
+        # the sweep's shapes with 8-bit weights (UINT8 + zero points)
+        return ([dict(p, kind="w8a16") for p in sweep_points()],
+                dict(workload="w8a16_asym_sweep", shapes=synth.W4A16_ASYM_SHAPES,
+                     ms=synth.W4A16_ASYM_MS, group=128, weights="uint8+zp", act="bf16"))
     if name == "f16s":
         # the sweep with fp16 scales against bf16 activations
         return ([dict(p, sdt="fp16") for p in sweep_points()],
@@ -119,6 +124,9 @@ def point_bytes(p):
     if kind == "w4a8":
         # act quant: read bf16 x, write e4m3 + scale; GEMM: codes, e8m0, a8, scale, bf16 out
         return (2 * m * k + m * k + 4 * m) + (n * k // 2 + n * k // 32 + m * k + 4 * m + 2 * m * n)
+    if kind == "w8a16":
+        # 8-bit codes, scales, 8-bit zero points, activations, output
+        return n * k + (k // g) * n * 2 + (k // g) * n + m * k * 2 + m * n * 2
     if kind == "nvfp4":
         # codes, block scales as the kernel reads them (16-bit per 16 k), activations, output
         return n * k // 2 + (k // 16) * n * 2 + m * k * 2 + m * n * 2
@@ -221,7 +229,8 @@ class GemmPoint:
     def __init__(self, p, seed, device, host=False, src=None):
         import torch
         from quantized_weight_gemm_run_b300 import qgemm as Q
-        from quantized_weight_gemm_run_b300.api import NVFP4Linear, W4A16Linear, W4A8Linear
+        from quantized_weight_gemm_run_b300.api import (NVFP4Linear, W4A16Linear, W4A8Linear,
+                                                         W8A16Linear)
         self.p, self.Q = p, Q
         self.mx = p.get("kind") == "w4a8"
         m, n, k, gs = p["m"], p["n"], p["k"], p["g"]
@@ -233,6 +242,13 @@ class GemmPoint:
                 b = torch.from_numpy(synth.random_bytes(g, (n, k // 32), 116, 124)).to(device)
                 self.lin = W4A8Linear(codes, b, n, k)
                 del codes, b
+            elif p.get("kind") == "w8a16":
+                qweight = torch.from_numpy(synth.random_words(g, (k // 4, n))).to(device)
+                scales = torch.from_numpy(
+                    synth.random_scales_fp32(g, (k // gs, n))).to(dt).to(device)
+                qzeros = torch.from_numpy(synth.random_words(g, (k // gs, n // 4))).to(device)
+                self.lin = W8A16Linear(qweight, scales, qzeros, n, k, gs, dt)
+                del qweight, scales, qzeros
             elif p.get("kind") == "nvfp4":
                 codes = torch.from_numpy(synth.random_bytes(g, (n, k // 2))).to(device)
                 sb = torch.from_numpy(synth.random_bytes(g, (n, k // 16), 0x30, 0x48)).to(device)
@@ -425,6 +441,7 @@ def kernel_name(p):
         return f"w4a16_mma_kernel<{'fp16' if p['adt'] == 'fp16' else 'bf16'}>"
     bt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
     fmt = ("w4a8_mxf8f6f4" if kind == "w4a8" else "nvfp4_bf16" if kind == "nvfp4"
+           else f"int8_{p['adt']}" if kind == "w8a16"
            else "bf16_f16scales" if f16_scales(p) else "fp16" if p["adt"] == "fp16" else "bf16")
     return f"w4a16_kernel<{bt},{fmt},dense>"
 
@@ -597,7 +614,7 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None,
         "dtype": ("bf16 x e4m3 (fp32 acc)" if pts[0].get("kind") == "w4a8"
                   else "bf16" if pts[0]["adt"] == "bf16" else "fp16"),
-        "data": "synthetic (seeded random 4-bit codes, scales, zero points, N(0,1) activations)",
+        "data": "synthetic (seeded random codes, scales, zero points, N(0,1) activations)",
         "config": dict(cfg, gemms_per_step=len(gemms), bytes_per_step=bytes_step,
                        l2="operands of every GEMM are distinct buffers; a step touches "
                           f"{bytes_step / 1e6:.0f} MB > 2x L2, so every GEMM reads cold",
@@ -650,6 +667,14 @@ def _oracle_point(p, seed):
         x = codecs.bf16(synth.activations_fp32(g, m, k))
         a8, sc = gemm.act_quant_fp8(x)
         gemm.w4a8_output(a8, sc, ckn, bkn)
+        return point_flops(p)
+    if kind == "w8a16":
+        q = quant.unpack_int_kn(synth.random_words(g, (k // 4, n)), 8, signed=False)
+        s = codecs.round_dtype(p["adt"])(
+            synth.random_scales_fp32(g, (k // gs, n)).astype(np.float64))
+        z = quant.unpack_zeros_bits(synth.random_words(g, (k // gs, n // 4)), 8)
+        a = codecs.round_dtype(p["adt"])(synth.activations_fp32(g, m, k))
+        gemm.w4a16_output(a, quant.dequant_int(q, s, z, gs, p["adt"]), p["adt"])
         return point_flops(p)
     if kind == "nvfp4":
         codes = synth.random_bytes(g, (n, k // 2))
@@ -754,8 +779,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sweep",
-                    help="sweep | f16s | nvfp4 | w4a16_m16 | large | w4a8 | moe16 | moe256 | "
-                         "moe4096 | shape:M,N,K[,sym|asym][,bf16|fp16][,f16s]")
+                    help="sweep | f16s | w8a16 | nvfp4 | w4a16_m16 | large | w4a8 | moe16 | "
+                         "moe256 | moe4096 | shape:M,N,K[,sym|asym][,bf16|fp16][,f16s]")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()
     if args.warmup < 3:

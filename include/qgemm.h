@@ -62,11 +62,18 @@ typedef enum {
 } qgemm_status;
 
 /* weight formats */
-enum { QGEMM_W_INT4_SYM = 0, QGEMM_W_UINT4_ZP = 1, QGEMM_W_MXFP4 = 2, QGEMM_W_NVFP4 = 3 };
+enum {
+  QGEMM_W_INT4_SYM = 0,
+  QGEMM_W_UINT4_ZP = 1,
+  QGEMM_W_MXFP4 = 2,
+  QGEMM_W_NVFP4 = 3,
+  QGEMM_W_INT8_SYM = 4,   /* W8A16 */
+  QGEMM_W_UINT8_ZP = 5
+};
 /* scale formats */
 enum { QGEMM_S_FP16 = 0, QGEMM_S_BF16 = 1, QGEMM_S_E8M0 = 2, QGEMM_S_E4M3 = 3 };
 /* zero-point formats */
-enum { QGEMM_Z_NONE = 0, QGEMM_Z_UINT4 = 1 };
+enum { QGEMM_Z_NONE = 0, QGEMM_Z_UINT4 = 1, QGEMM_Z_UINT8 = 2 };
 /* activation / output data types */
 enum { QGEMM_FP16 = 0, QGEMM_BF16 = 1, QGEMM_FP8E4M3 = 2 };
 /* GEMM types (compute config) */
@@ -78,10 +85,15 @@ enum { QGEMM_ACT_NONE = 0, QGEMM_ACT_SILU_GLU = 1 };
  * Layer config: what the layer is.  Shapes are those of one expert; a dense
  * layer has num_experts = 1.
  *   n, k          output features, input features (C[M,N] = A[M,K] W[K,N])
- *   group_size    K-extent of one scale (W4A16: 32, 64 or a multiple of 128
- *                 dividing K; MXFP4: must be 32; NVFP4: must be 16)
+ *   group_size    K-extent of one scale (W4A16 and W8A16: 32, 64 or a
+ *                 multiple of 128 dividing K; MXFP4: must be 32; NVFP4: must
+ *                 be 16)
  *   weight_format QGEMM_W_*;  scale_format QGEMM_S_*;  zero_format QGEMM_Z_*
- *   act_dtype     activation dtype: QGEMM_FP16 / QGEMM_BF16 (W4A16, and
+ *   act_dtype     activation dtype: QGEMM_FP16 / QGEMM_BF16 (W4A16, W8A16
+ *                 with 8-bit integer weights and scales in the activation
+ *                 dtype: the pages list weight-only formats WNA16,
+ *                 kinachrichten.com "Warum quantisierte Kernel wichtig
+ *                 sind", and
  *                 NVFP4 weights: e2m1 codes, one e4m3 scale per 16 k, one
  *                 fp32 tensor scale; the pages name NVFP4 as a format whose
  *                 number format and scaling differ from INT4's,
@@ -191,6 +203,13 @@ typedef struct {
  *     meaning  w[k, n] = (q - z) * s, rounded once to the activation dtype
  *              (z = 0 for INT4; an fp16 scale with bf16 activations is not
  *              rounded to bf16 first)
+ *   INT8 / UINT8 (W8A16):
+ *     qweight  int32 [K/4, N]: word (j, n) holds k = 4j + i in bits [8i, 8i+8),
+ *              INT8 as two's complement, UINT8 as raw 0..255
+ *     scales   as INT4, in the activation dtype
+ *     qzeros   int32 [K/g, N/4] (UINT8_ZP only): byte i of word (G, j) is the
+ *              zero point (0..255) of column 4j + i
+ *     meaning  as INT4
  *   MXFP4:
  *     codes    uint8 [N, K/2]: byte (n, j) holds k = 2j (low nibble) and
  *              k = 2j + 1 (high nibble) as e2m1 (sign | 2 exponent | 1 mantissa)
@@ -217,11 +236,12 @@ qgemm_status qgemm_packed_size(const qgemm_layer_config* layer, size_t* bytes);
  * aligned).  Per expert, the buffer holds one block per (128-row n-tile,
  * 128-deep k-tile), n-tile major: the tile's codes, then its scales, then its
  * zero points, so that consecutive k-tiles of a tile are contiguous.  INT4
- * codes are re-encoded as offset binary (q + 8) and NVFP4 block scales as the
+ * and INT8 codes are re-encoded as offset binary (q + 8, q + 128) and NVFP4
+ * block scales as the
  * activation dtype's bit pattern of the same value; nothing changes value, so
  * the packed buffer means exactly what the standard tensors mean.  NVFP4
  * buffers end with the fp32 tensor scales (16-byte padded).  qzeros must be
- * NULL unless zero_format = QGEMM_Z_UINT4 (zero points) or the weights are
+ * NULL unless zero_format is QGEMM_Z_UINT4 or QGEMM_Z_UINT8 (zero points) or the weights are
  * NVFP4 (the tensor scales, required).  Runs once per layer; the
  * buffer is read-only afterwards.  For a gated layer (gated_act != 0) row
  * 2i + s of n-tile nt holds the standard column s * N/2 + 64 nt + i (gate

@@ -29,6 +29,14 @@ W4A16 tiled layout (N and K multiples of 128; KT = K / 128 k-tiles):
   zeros (UINT4 only): one block of 128 * ST bytes per (nt, kt), byte
     sg * 128 + r is the zero point (0..15) of the same (group, row).
 
+INT8 / UINT8 tiled layout (W8A16; same tiling):
+
+  weights: one 16384-byte block per (nt, kt); vector v = (qd * 8 + j) * 32 + t
+    holds row n = 128 nt + 32 qd + t and the 16 values k = 128 kt + 16 j +
+    [0, 16), byte c holding k-offset c.  Byte value: offset binary q + 128
+    for signed INT8, the raw code for UINT8.
+  scales, zeros: as W4A16 (zero points 0..255).
+
 MXFP4 tiled layout (same tiling):
 
   weights: one 8192-byte block per (nt, kt), vector v = (qd * 4 + j) * 32 + t
@@ -62,7 +70,7 @@ interleaved block by block, so that block (nt, kt) is one contiguous run of
 bytes [weights block][scales block][zeros block] and the blocks follow in the
 same nt-major order; experts follow one another, each expert's blocks
 contiguous.  Block sizes: 8192 + 256 ST (+ 128 ST with zeros) bytes for
-INT4/UINT4, 8192 + 512 for MXFP4.
+INT4/UINT4, 16384 + 256 ST (+ 128 ST) for INT8/UINT8, 8192 + 512 for MXFP4.
 """
 
 from __future__ import annotations
@@ -114,8 +122,26 @@ def tiled_scales(s_bits, g: int, k: int) -> np.ndarray:
     return out.reshape(-1)
 
 
+def tiled_weights8(q, signed: bool) -> np.ndarray:
+    """8-bit codes q[K, N] -> the tiled byte stream (uint8, N*K bytes)."""
+    q = np.asarray(q, dtype=np.int64)
+    k, n = q.shape
+    byte = (q + 128) if signed else q.copy()
+    if byte.min() < 0 or byte.max() > 255:
+        raise ValueError("code out of range")
+    kt_n, nt_n = k // TILE_K, n // TILE_N
+    out = np.zeros((nt_n, kt_n, 4, 8, 32, 16), dtype=np.uint8)   # [nt, kt, qd, j, t, c]
+    for qd in range(4):
+        for j in range(8):
+            for c in range(16):
+                kl = 16 * j + c
+                rows = byte.reshape(kt_n, TILE_K, nt_n, TILE_N)[:, kl, :, 32 * qd: 32 * qd + 32]
+                out[:, :, qd, j, :, c] = rows.transpose(1, 0, 2)
+    return out.reshape(-1)
+
+
 def tiled_zeros(z, g: int, k: int) -> np.ndarray:
-    """Zero points [K/g, N] (0..15) -> tiled uint8 stream."""
+    """Zero points [K/g, N] (0..15, or 0..255 for UINT8) -> tiled uint8 stream."""
     z = np.asarray(z, dtype=np.int64)
     n = z.shape[1]
     st = scale_groups_per_tile(g)
@@ -210,6 +236,17 @@ def packed_w4(q, s_bits, z, g: int, signed: bool) -> np.ndarray:
     k = np.asarray(q).shape[0]
     st = scale_groups_per_tile(g)
     pieces = [(tiled_weights(q, signed), 8192), (tiled_scales(s_bits, g, k), 256 * st)]
+    if z is not None:
+        pieces.append((tiled_zeros(z, g, k), 128 * st))
+    return interleave_blocks(*pieces)
+
+
+def packed_w8(q, s_bits, z, g: int, signed: bool) -> np.ndarray:
+    """8-bit codes q[K, N], scale bits [K/g, N] and zero points [K/g, N] (None
+    for signed INT8) -> the packed buffer of one matrix."""
+    k = np.asarray(q).shape[0]
+    st = scale_groups_per_tile(g)
+    pieces = [(tiled_weights8(q, signed), 16384), (tiled_scales(s_bits, g, k), 256 * st)]
     if z is not None:
         pieces.append((tiled_zeros(z, g, k), 128 * st))
     return interleave_blocks(*pieces)

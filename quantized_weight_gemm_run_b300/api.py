@@ -55,6 +55,11 @@ class W4A16Linear:
             Q.QGEMM_Z_UINT4 if asym else Q.QGEMM_Z_NONE, adt, adt,
             1 if bias is not None else 0, num_experts,
             Q.QGEMM_ACT_SILU_GLU if gated else Q.QGEMM_ACT_NONE)
+        self._pack(qweight, scales, qzeros, bias, tuning, deterministic, batch_invariant)
+
+    def _pack(self, qweight, scales, qzeros, bias, tuning, deterministic, batch_invariant):
+        """Packs the standard-format tensors for ``self.layer`` (qzeros: the
+        zero points, NVFP4's tensor scales, or None) and sets up the configs."""
         st, nbytes = Q.qgemm_packed_size(self.layer)
         Q.check(st)
         dev = qweight.device
@@ -105,6 +110,31 @@ class W4A16Linear:
         return Q.qgemm_check_status(self.ws.get(256))
 
 
+class W8A16Linear(W4A16Linear):
+    """A packed layer of 8-bit integer weights against fp16/bf16 activations:
+    qweight int32 [E*K/4, N] (four codes a word along K; INT8 two's complement,
+    or UINT8 with qzeros int32 [E*K/g, N/4]), scales [E*K/g, N] in the
+    activation dtype.  Runs, grouped runs and the dequantized view are those
+    of ``W4A16Linear``."""
+
+    def __init__(self, qweight, scales, qzeros, n, k, group, act_dtype, num_experts=1,
+                 bias=None, tuning=None, deterministic=False, gated=False,
+                 batch_invariant=False):
+        self.n, self.k, self.group, self.num_experts = n, k, group, num_experts
+        self.gated = gated
+        self.n_out = n // 2 if gated else n
+        self.act_dtype = act_dtype
+        asym = qzeros is not None
+        adt = _DT[act_dtype]
+        self.layer = Q.layer_config(
+            n, k, group, Q.QGEMM_W_UINT8_ZP if asym else Q.QGEMM_W_INT8_SYM,
+            Q.QGEMM_S_FP16 if adt == Q.QGEMM_FP16 else Q.QGEMM_S_BF16,
+            Q.QGEMM_Z_UINT8 if asym else Q.QGEMM_Z_NONE, adt, adt,
+            1 if bias is not None else 0, num_experts,
+            Q.QGEMM_ACT_SILU_GLU if gated else Q.QGEMM_ACT_NONE)
+        self._pack(qweight, scales, qzeros, bias, tuning, deterministic, batch_invariant)
+
+
 class NVFP4Linear(W4A16Linear):
     """A packed layer of NVFP4 weights against fp16/bf16 activations: e2m1
     codes uint8 [E*N, K/2] (standard nibble order), e4m3 block scales uint8
@@ -122,21 +152,8 @@ class NVFP4Linear(W4A16Linear):
             n, k, 16, Q.QGEMM_W_NVFP4, Q.QGEMM_S_E4M3, Q.QGEMM_Z_NONE, adt, adt,
             1 if bias is not None else 0, num_experts,
             Q.QGEMM_ACT_SILU_GLU if gated else Q.QGEMM_ACT_NONE)
-        st, nbytes = Q.qgemm_packed_size(self.layer)
-        Q.check(st)
-        dev = codes.device
-        codes, scales = codes.contiguous(), scales.contiguous()
-        tensor_scales = tensor_scales.to(torch.float32).contiguous()
-        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-        Q.check(Q.qgemm_pack_weights(self.layer, codes, scales, tensor_scales, self.packed))
-        self.bias = bias
-        self.tuning = tuning
-        self.ws = Workspace(dev)
-        det = 1 if deterministic else 0
-        inv = 1 if batch_invariant else 0
-        self.dense = Q.compute_config(Q.QGEMM_GEMM_DENSE, batch_invariant=inv, deterministic=det)
-        self.grouped = Q.compute_config(Q.QGEMM_GEMM_GROUPED, batch_invariant=inv,
-                                        deterministic=det)
+        self._pack(codes, scales, tensor_scales.to(torch.float32), bias, tuning, deterministic,
+                   batch_invariant)
 
 
 class W4A8Linear:

@@ -112,7 +112,7 @@ int mma_smem_bytes(int block_bytes);
 int device_sm_count();
 // fmt: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 x e4m3, bf16 out),
 //      3 = NVFP4 weights x bf16, 4 = NVFP4 weights x fp16,
-//      5 = W4A16 bf16 with fp16 scales
+//      5 = W4A16 bf16 with fp16 scales, 6 / 7 = W8A16 bf16 / fp16
 cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
                          const W4A16Params& p, int block_tok, int fmt, bool grouped, int grid,
                          cudaStream_t stream);
@@ -123,14 +123,18 @@ cudaError_t launch_repack_mxfp4(const uint8_t* codes, const uint8_t* scales, uin
 cudaError_t launch_debug_mx_codes(const uint8_t* w, uint8_t* out_kn, int64_t n, int64_t k,
                                   int gated, cudaStream_t stream);
 
-// Packed block of one (n-tile, k-tile): 8192 bytes of codes, then the scales
-// (W4A16: 128 * st 16-bit words; MXFP4: 128 32-bit words), then the zero
-// points (128 * st bytes) when the format has them.
+// Packed block of one (n-tile, k-tile): the codes (8192 bytes of 4-bit
+// codes, 16384 bytes of 8-bit ones), then the scales (128 * st 16-bit words;
+// MXFP4: 128 32-bit words), then the zero points (128 * st bytes) when the
+// format has them.
+__host__ __device__ constexpr int packed_code_bytes(bool w8) {
+  return w8 ? 2 * kTileBytes : kTileBytes;
+}
 __host__ __device__ constexpr int packed_scale_bytes(bool mx, int st) {
   return mx ? kTileN * 4 : st * kTileN * 2;
 }
-__host__ __device__ constexpr int packed_block_bytes(bool mx, int st, bool zp) {
-  return kTileBytes + packed_scale_bytes(mx, st) + (zp ? st * kTileN : 0);
+__host__ __device__ constexpr int packed_block_bytes(bool mx, int st, bool zp, bool w8 = false) {
+  return packed_code_bytes(w8) + packed_scale_bytes(mx, st) + (zp ? st * kTileN : 0);
 }
 
 // Gated layers: packed row r of n-tile nt holds standard column
@@ -160,10 +164,16 @@ cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
                              const int32_t* qzeros, uint8_t* packed, int64_t n, int64_t k,
                              int group, int signed_q, int experts, int gated,
                              cudaStream_t stream);
+// INT8 / UINT8: standard qweight int32 [K/4, N], scales [K/g, N], qzeros
+// int32 [K/g, N/4] or null -> packed blocks of 16384 code bytes.
+cudaError_t launch_repack_w8(const int32_t* qweight, const uint16_t* scales,
+                             const int32_t* qzeros, uint8_t* packed, int64_t n, int64_t k,
+                             int group, int signed_q, int experts, int gated,
+                             cudaStream_t stream);
 
 cudaError_t launch_debug_dequant(const uint8_t* packed, uint16_t* out, int64_t n, int64_t k,
                                  int group, int has_zp, bool fp16, bool nv, bool f16s,
-                                 int gated, cudaStream_t stream);
+                                 bool w8, int gated, cudaStream_t stream);
 
 cudaError_t launch_repack_nvfp4(const uint8_t* codes, const uint8_t* scales,
                                const float* tensor_scales, uint8_t* packed, int64_t n, int64_t k,

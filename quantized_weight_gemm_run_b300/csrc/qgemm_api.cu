@@ -123,6 +123,26 @@ static qgemm_status check_layer(const qgemm_layer_config* L) {
         return fail(QGEMM_ERR_UNSUPPORTED, "UINT4 needs uint4 zero points");
       return ok();
     }
+    case QGEMM_W_INT8_SYM:
+    case QGEMM_W_UINT8_ZP: {
+      if (L->act_dtype != QGEMM_FP16 && L->act_dtype != QGEMM_BF16)
+        return fail(QGEMM_ERR_UNSUPPORTED, "W8A16 needs fp16 or bf16 activations");
+      if (L->out_dtype != L->act_dtype)
+        return fail(QGEMM_ERR_UNSUPPORTED, "W8A16 output dtype must equal the activation dtype");
+      if ((L->scale_format == QGEMM_S_FP16 ? QGEMM_FP16 : L->scale_format == QGEMM_S_BF16
+                                                              ? QGEMM_BF16
+                                                              : -1) != L->act_dtype)
+        return fail(QGEMM_ERR_UNSUPPORTED, "W8A16 scales must be in the activation dtype");
+      const int g = L->group_size;
+      if (!(g == 32 || g == 64 || (g >= 128 && g % 128 == 0)))
+        return fail(QGEMM_ERR_UNSUPPORTED, "group size %d not in {32, 64, 128j}", g);
+      if (L->k % g) return fail(QGEMM_ERR_UNSUPPORTED, "k must be a multiple of the group size");
+      if (L->weight_format == QGEMM_W_INT8_SYM && L->zero_format != QGEMM_Z_NONE)
+        return fail(QGEMM_ERR_UNSUPPORTED, "symmetric INT8 takes no zero points");
+      if (L->weight_format == QGEMM_W_UINT8_ZP && L->zero_format != QGEMM_Z_UINT8)
+        return fail(QGEMM_ERR_UNSUPPORTED, "UINT8 needs uint8 zero points");
+      return ok();
+    }
     case QGEMM_W_NVFP4:
       if (L->zero_format != QGEMM_Z_NONE)
         return fail(QGEMM_ERR_UNSUPPORTED, "NVFP4 takes no zero points");
@@ -164,17 +184,25 @@ static int st_of(int group) { return group < kTileK ? kTileK / group : 1; }
 
 static bool is_mx(const qgemm_layer_config* L) { return L->weight_format == QGEMM_W_MXFP4; }
 static bool is_nv(const qgemm_layer_config* L) { return L->weight_format == QGEMM_W_NVFP4; }
+static bool is_w8(const qgemm_layer_config* L) {
+  return L->weight_format == QGEMM_W_INT8_SYM || L->weight_format == QGEMM_W_UINT8_ZP;
+}
+// integer formats with zero points (UINT4, UINT8)
+static bool has_zeros(const qgemm_layer_config* L) {
+  return L->zero_format == QGEMM_Z_UINT4 || L->zero_format == QGEMM_Z_UINT8;
+}
 // W4A16 with fp16 scales against bf16 activations
 static bool is_f16s(const qgemm_layer_config* L) {
-  return !is_mx(L) && !is_nv(L) && L->scale_format == QGEMM_S_FP16 && L->act_dtype == QGEMM_BF16;
+  return !is_mx(L) && !is_nv(L) && !is_w8(L) && L->scale_format == QGEMM_S_FP16 &&
+         L->act_dtype == QGEMM_BF16;
 }
 
 // Bytes of one expert's packed blocks (an NVFP4 buffer adds the tensor-scale
 // tail after the last expert).
 static size_t expert_packed_bytes(const qgemm_layer_config* L) {
   const size_t tiles = (size_t)(L->n / kTileN) * (size_t)(L->k / kTileK);
-  return tiles * (size_t)packed_block_bytes(is_mx(L), st_of(L->group_size),
-                                            L->zero_format == QGEMM_Z_UINT4);
+  return tiles * (size_t)packed_block_bytes(is_mx(L), st_of(L->group_size), has_zeros(L),
+                                            is_w8(L));
 }
 
 // ------------------------------------------------------------ plans
@@ -211,12 +239,12 @@ static int tail_smem(int sx, int sw, int experts) {
   return (2 * sx + 2 * sw + 2 * kASlots + 4 + 2 + 4) * 8 + 32 + 2 * (experts + 1) * 4 + 64;
 }
 
-static bool make_geometry(int bt, int st, int has_zp, bool mx, int experts, int w_cap,
+static bool make_geometry(int bt, int st, int has_zp, bool mx, bool w8, int experts, int w_cap,
                           int smem_cap, Geometry* g) {
   const int rx = units_per_stage(bt);
   g->rw = weight_units_per_slot(bt);
   g->x_bytes = (rx * bt * kTileK * (mx ? 1 : 2) + 1023) & ~1023;
-  g->w_bytes = g->rw * packed_block_bytes(mx, st, has_zp != 0);
+  g->w_bytes = g->rw * packed_block_bytes(mx, st, has_zp != 0, w8);
   for (int sx = bt <= 32 ? 3 : 4; sx >= 2; --sx) {
     const int fixed = 1024 /* alignment slack */ + sx * g->x_bytes + 1023 + kEpiStageBytes +
                       tail_smem(sx, 16, experts);
@@ -264,11 +292,12 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   if (T && (T->split_k < 0 || T->split_k > 64))
     return fail(QGEMM_ERR_INVALID_ARG, "split_k must be in [0, 64]");
   const int st = st_of(L->group_size);
-  const int has_zp = L->zero_format == QGEMM_Z_UINT4;
+  const int has_zp = has_zeros(L);
   if (T && (T->kernel < 0 || T->kernel > 2))
     return fail(QGEMM_ERR_INVALID_ARG, "kernel must be 0, 1 or 2");
-  const bool mma_ok = !grouped && !is_mx(L) && !is_nv(L) && !is_f16s(L) && L->gated_act == 0 &&
-                      rows <= 16 && !(C && (C->deterministic || C->batch_invariant));
+  const bool mma_ok = !grouped && !is_mx(L) && !is_nv(L) && !is_f16s(L) && !is_w8(L) &&
+                      L->gated_act == 0 && rows <= 16 &&
+                      !(C && (C->deterministic || C->batch_invariant));
   const int want = T ? T->kernel : 0;
   if (want == 2 && !mma_ok)
     return fail(QGEMM_ERR_UNSUPPORTED,
@@ -319,7 +348,7 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   const int w_cap = (T && T->stages) ? T->stages : 16;
   if (w_cap < 2 || w_cap > 16) return fail(QGEMM_ERR_INVALID_ARG, "stages must be in [2, 16]");
   Geometry g;
-  if (!make_geometry(bt, st, has_zp, is_mx(L), E, w_cap, device_max_smem(), &g))
+  if (!make_geometry(bt, st, has_zp, is_mx(L), is_w8(L), E, w_cap, device_max_smem(), &g))
     return fail(QGEMM_ERR_UNSUPPORTED, "tile does not fit shared memory");
   const int64_t kt = L->k / kTileK, nt = L->n / kTileN;
   int64_t tiles_bound;
@@ -360,8 +389,8 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   P->grid = grid;
   P->split_cap = cap;
   P->st = st;
-  P->off_s = kTileBytes;                                   // inside a packed block
-  P->off_z = kTileBytes + packed_scale_bytes(is_mx(L), st);
+  P->off_s = packed_code_bytes(is_w8(L));                  // inside a packed block
+  P->off_z = P->off_s + packed_scale_bytes(is_mx(L), st);
   P->g = g;
   P->max_tiles = tiles_bound;
   P->ws = workspace_layout(tiles_bound, grid, bt);
@@ -430,7 +459,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   if (rows > (1 << 30)) return fail(QGEMM_ERR_UNSUPPORTED, "row count above 2^30");
   if (rows == 0) return ok();
   if (!device_is_sm103()) return fail(QGEMM_ERR_UNSUPPORTED, "this library runs on sm_103 only");
-  const bool has_zp = L->zero_format == QGEMM_Z_UINT4;
+  const bool has_zp = has_zeros(L);
   if (!a || !w || !c || (L->has_bias && !bias) || (grouped && !offsets))
     return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
   if (!L->has_bias && bias) return fail(QGEMM_ERR_INVALID_ARG, "bias given with has_bias = 0");
@@ -515,7 +544,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.t_scales = is_nv(L) ? reinterpret_cast<const float*>(static_cast<const uint8_t*>(w) +
                                                          (size_t)E * expert_packed_bytes(L))
                         : nullptr;
-  p.block_bytes = packed_block_bytes(mx, P.st, has_zp);
+  p.block_bytes = packed_block_bytes(mx, P.st, has_zp, is_w8(L));
   p.s_off = P.off_s;
   p.z_off = P.off_z;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -578,10 +607,12 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   if (!encode_tmap_2d(&tmap_c, CU_TENSOR_MAP_DATA_TYPE_UINT16, c, n_out, (uint64_t)rows,
                       n_out * 2, p.gated ? 16 : 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
     return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the output tensor");
-  cudaError_t e =
-      launch_w4a16(tmap, tmap_c, p, P.bt,
-                   mx ? 2 : is_nv(L) ? (fp16 ? 4 : 3) : is_f16s(L) ? 5 : fp16 ? 1 : 0, grouped,
-                   P.grid, stream);
+  int fmt = fp16 ? 1 : 0;
+  if (mx) fmt = 2;
+  else if (is_nv(L)) fmt = fp16 ? 4 : 3;
+  else if (is_f16s(L)) fmt = 5;
+  else if (is_w8(L)) fmt = fp16 ? 7 : 6;
+  cudaError_t e = launch_w4a16(tmap, tmap_c, p, P.bt, fmt, grouped, P.grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "W4A16 GEMM launch");
   return ok();
 }
@@ -627,7 +658,7 @@ qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qwe
                                 void* stream) {
   qgemm_status st = check_layer(layer);
   if (st != QGEMM_OK) return st;
-  const bool has_zp = layer->zero_format == QGEMM_Z_UINT4;
+  const bool has_zp = has_zeros(layer);
   const bool nv = is_nv(layer);   // qzeros carries the fp32 tensor scales
   if (!qweight || !scales || !packed || ((has_zp || nv) && !qzeros))
     return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
@@ -651,6 +682,12 @@ qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qwe
                             static_cast<const uint8_t*>(scales), static_cast<uint8_t*>(packed),
                             layer->n, layer->k, layer->num_experts, layer->gated_act != 0,
                             static_cast<cudaStream_t>(stream));
+  } else if (is_w8(layer)) {
+    e = launch_repack_w8(static_cast<const int32_t*>(qweight),
+                         static_cast<const uint16_t*>(scales), static_cast<const int32_t*>(qzeros),
+                         static_cast<uint8_t*>(packed), layer->n, layer->k, layer->group_size,
+                         layer->weight_format == QGEMM_W_INT8_SYM ? 1 : 0, layer->num_experts,
+                         layer->gated_act != 0, static_cast<cudaStream_t>(stream));
   } else {
     e = launch_repack_w4(static_cast<const int32_t*>(qweight),
                          static_cast<const uint16_t*>(scales), static_cast<const int32_t*>(qzeros),
@@ -787,8 +824,9 @@ qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* pa
   else
     e = launch_debug_dequant(static_cast<const uint8_t*>(packed), static_cast<uint16_t*>(out_kn),
                              layer->n, layer->k, layer->group_size,
-                             layer->zero_format == QGEMM_Z_UINT4 ? 1 : 0,
+                             has_zeros(layer) ? 1 : 0,
                              layer->act_dtype == QGEMM_FP16, is_nv(layer), is_f16s(layer),
+                             is_w8(layer),
                              layer->gated_act != 0, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
   return ok();
@@ -829,7 +867,8 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
     if (st != QGEMM_OK) {
       rec = std::string("rejected: ") + g_last_error;
     } else {
-      static const char* wf[] = {"int4_sym", "uint4_zp", "mxfp4", "nvfp4"};
+      static const char* wf[] = {"int4_sym", "uint4_zp", "mxfp4",
+                                 "nvfp4",    "int8_sym", "uint8_zp"};
       static const char* dt[] = {"fp16", "bf16", "fp8e4m3"};
       static const char* sf[] = {"fp16", "bf16", "e8m0", "e4m3"};
       char tmp[512];

@@ -16,11 +16,14 @@
 //            {0,2,4,6,1,3,5,7}[p], so a single 0x000F000F mask extracts two
 //            consecutive k; INT4 codes are stored offset binary (q + 8).
 //            MXFP4: the 16 bytes of the row's 32 codes in standard order.
+//            INT8/UINT8: 16384 bytes, 1024 vectors, vector (qd*8 + j)*32 + t =
+//            row 32qd + t, k = 16j .. 16j+15 in byte order; INT8 codes are
+//            stored offset binary (q + 128).
 //   scales   INT4/UINT4: 128 * ST 16-bit words (ST = max(1, 128/g)), word
 //            sg*128 + r the scale of row r for the sg-th group of the tile.
 //            MXFP4: 128 32-bit words, byte j of word r the e8m0 exponent of
 //            row r for k = 32j .. 32j+31 of the tile.
-//   zeros    UINT4 only: 128 * ST bytes, same order, zero point 0..15.
+//   zeros    UINT4 / UINT8 only: 128 * ST bytes, same order, the zero point.
 //
 // A gated layer's rows are taken in the gate/up interleaved order
 // (glu_source_col).  Every thread writes one output vector / element; reads
@@ -72,10 +75,12 @@ __global__ void repack_weights_kernel(const int32_t* __restrict__ qweight, uint8
   *reinterpret_cast<uint4*>(out + gblk * block_bytes + v * 16) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// One thread per (block, group slot, row): the scale and (UINT4 / UINT8)
+// the zero point; the codes take code_bytes at the start of each block.
 __global__ void repack_scales_kernel(const uint16_t* __restrict__ scales,
                                      const int32_t* __restrict__ qzeros, uint8_t* __restrict__ out,
-                                     int n, int k, int group, int block_bytes, int gated,
-                                     long long total) {
+                                     int n, int k, int group, int block_bytes, int code_bytes,
+                                     int zero_bits, int gated, long long total) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= total) return;
   const int KT = k / kTileK, NT = n / kTileN;
@@ -93,13 +98,44 @@ __global__ void repack_scales_kernel(const uint16_t* __restrict__ scales,
   const int col = packed_source_col(nt, r, n, gated);
   const long long groups = k / group;
   uint8_t* bp = out + (ex * ((long long)NT * KT) + blk) * block_bytes;
-  reinterpret_cast<uint16_t*>(bp + kTileBytes)[sg * kTileN + r] =
+  reinterpret_cast<uint16_t*>(bp + code_bytes)[sg * kTileN + r] =
       scales[ex * groups * n + (long long)grp * n + col];
   if (qzeros) {
-    const uint32_t word = (uint32_t)qzeros[ex * groups * (n / 8) + (long long)grp * (n / 8) + col / 8];
-    bp[kTileBytes + packed_scale_bytes(false, st) + sg * kTileN + r] =
-        (uint8_t)((word >> (4 * (col % 8))) & 0xFu);
+    const int per_word = 32 / zero_bits;   // zero points per int32 word along N
+    const uint32_t word = (uint32_t)qzeros[ex * groups * (n / per_word) +
+                                           (long long)grp * (n / per_word) + col / per_word];
+    bp[code_bytes + packed_scale_bytes(false, st) + sg * kTileN + r] =
+        (uint8_t)((word >> (zero_bits * (col % per_word))) & ((1u << zero_bits) - 1u));
   }
+}
+
+// INT8 / UINT8 codes: output vector v of a block takes four standard words
+// (16 consecutive k of one column) unchanged in byte order; INT8 bytes move
+// to offset binary.
+__global__ void repack_weights8_kernel(const int32_t* __restrict__ qweight,
+                                       uint8_t* __restrict__ out, int n, int k, int signed_q,
+                                       int block_bytes, int gated, long long total) {
+  const long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (vec >= total) return;
+  const int KT = k / kTileK, NT = n / kTileN;
+  const long long per_expert = (long long)NT * KT * 1024;
+  const long long ex = vec / per_expert;
+  const long long rem = vec - ex * per_expert;
+  const long long blk = rem / 1024;
+  const int v = (int)(rem % 1024);
+  const int nt = (int)(blk / KT), kt = (int)(blk % KT);
+  const int t = v & 31, j = (v >> 5) & 7, qd = v >> 8;
+  const int col = packed_source_col(nt, qd * 32 + t, n, gated);
+  const long long word_row0 = (long long)(kt * kTileK + j * 16) / 4;   // first K/4 row
+  const int32_t* src = qweight + ex * (long long)(k / 4) * n;
+  uint32_t o[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t in = (uint32_t)src[(word_row0 + w) * n + col];
+    o[w] = signed_q ? in ^ 0x80808080u : in;   // two's complement byte -> q + 128
+  }
+  const long long gblk = ex * ((long long)NT * KT) + blk;
+  *reinterpret_cast<uint4*>(out + gblk * block_bytes + v * 16) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
@@ -116,7 +152,27 @@ cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
   if (err != cudaSuccess) return err;
   const long long elems = (long long)experts * (n / kTileN) * (k / kTileK) * st * kTileN;
   repack_scales_kernel<<<(unsigned)((elems + threads - 1) / threads), threads, 0, stream>>>(
-      scales, qzeros, packed, (int)n, (int)k, group, block_bytes, gated, elems);
+      scales, qzeros, packed, (int)n, (int)k, group, block_bytes, packed_code_bytes(false), 4,
+      gated, elems);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_w8(const int32_t* qweight, const uint16_t* scales,
+                             const int32_t* qzeros, uint8_t* packed, int64_t n, int64_t k,
+                             int group, int signed_q, int experts, int gated,
+                             cudaStream_t stream) {
+  const int threads = 256;
+  const int st = group < kTileK ? kTileK / group : 1;
+  const int block_bytes = packed_block_bytes(false, st, qzeros != nullptr, true);
+  const long long vecs = (long long)experts * (n / kTileN) * (k / kTileK) * 1024;
+  repack_weights8_kernel<<<(unsigned)((vecs + threads - 1) / threads), threads, 0, stream>>>(
+      qweight, packed, (int)n, (int)k, signed_q, block_bytes, gated, vecs);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const long long elems = (long long)experts * (n / kTileN) * (k / kTileK) * st * kTileN;
+  repack_scales_kernel<<<(unsigned)((elems + threads - 1) / threads), threads, 0, stream>>>(
+      scales, qzeros, packed, (int)n, (int)k, group, block_bytes, packed_code_bytes(true), 8,
+      gated, elems);
   return cudaGetLastError();
 }
 

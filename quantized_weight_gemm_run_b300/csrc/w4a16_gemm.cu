@@ -285,6 +285,44 @@ __device__ __forceinline__ void dequant_vec_f16s(const uint4 v, uint32_t zero2, 
   }
 }
 
+// 16 8-bit codes (one 16-byte vector of the tiled layout, k in byte order)
+// -> 8 packed 16-bit pairs (k, k+1) of (u - z) * s, rounded once.  fp16: a
+// prmt pairs two code bytes with 0x64 high bytes, so each half reads
+// 1024 + u exactly (the unit in the last place is 1 up to 2048); the
+// subtraction of 1024 + z is exact and the multiply rounds once.  bf16 has
+// too few mantissa bits for 8-bit codes, so each code goes through fp32: a
+// prmt places it in byte 1 of 0x47000000, which reads 2^15 + u; minus
+// 2^15 + z is exact, the product with the scale (9 x 8 significant bits) is
+// exact, and cvt.rn rounds each pair once.  Zero results carry the sign of
+// the scale, as the products do.
+template <bool FP16>
+__device__ __forceinline__ void dequant_vec8(const uint4 v, uint32_t zero, uint32_t scale,
+                                             uint32_t (&out)[8]) {
+  const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    if constexpr (FP16) {
+      uint32_t x0, x1;
+      asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(x0) : "r"(wds[w]), "r"(0x64646464u));
+      asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(x1) : "r"(wds[w]), "r"(0x64646464u));
+      out[2 * w] = dq_pair<true>(x0, zero, scale);
+      out[2 * w + 1] = dq_pair<true>(x1, zero, scale);
+    } else {
+      const float zf = __uint_as_float(zero), sf = __uint_as_float(scale);
+      uint32_t x[4];
+      asm("prmt.b32 %0, %1, %2, 0x7604;" : "=r"(x[0]) : "r"(wds[w]), "r"(0x47000000u));
+      asm("prmt.b32 %0, %1, %2, 0x7614;" : "=r"(x[1]) : "r"(wds[w]), "r"(0x47000000u));
+      asm("prmt.b32 %0, %1, %2, 0x7624;" : "=r"(x[2]) : "r"(wds[w]), "r"(0x47000000u));
+      asm("prmt.b32 %0, %1, %2, 0x7634;" : "=r"(x[3]) : "r"(wds[w]), "r"(0x47000000u));
+      float f[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) f[c] = __fmul_rn(__fsub_rn(__uint_as_float(x[c]), zf), sf);
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out[2 * w]) : "f"(f[1]), "f"(f[0]));
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out[2 * w + 1]) : "f"(f[3]), "f"(f[2]));
+    }
+  }
+}
+
 // 32 e2m1 codes (one 16-byte vector, k in nibble order, low nibble first) ->
 // 32 e4m3 bytes, exactly (every e2m1 value is an e4m3 value).  prmt looks up
 // the e4m3 byte of the 3-bit magnitude in an 8-entry byte table; a second
@@ -383,7 +421,8 @@ __device__ __forceinline__ float from_out(uint16_t b) {
 // FMT: 0 = W4A16 bf16, 1 = W4A16 fp16, 2 = W4A8 (MXFP4 weights, e4m3
 // activations with per-row fp32 scales, block-scaled MMA, bf16 output),
 // 3 / 4 = NVFP4 weights with bf16 / fp16 activations, 5 = W4A16 bf16
-// activations with fp16 scales.
+// activations with fp16 scales, 6 / 7 = W8A16 (8-bit integer codes) with
+// bf16 / fp16 activations.
 //
 // Shared memory holds two rings that turn over independently:
 //   activation slots: RX = units_per_stage(BT) consecutive k-tiles ("units")
@@ -398,10 +437,11 @@ template <int BT, int FMT, bool GROUPED>
 __global__ void __launch_bounds__(kNumThreads, 1)
     w4a16_kernel(const __grid_constant__ CUtensorMap tmap_a,
                  const __grid_constant__ CUtensorMap tmap_c, const W4A16Params p) {
-  constexpr bool FP16 = FMT == 1 || FMT == 4;   // 16-bit activations and output: fp16
+  constexpr bool FP16 = FMT == 1 || FMT == 4 || FMT == 7;   // 16-bit activations and output: fp16
   constexpr bool MX = FMT == 2;                  // W4A8-MXFP4
   constexpr bool NV = FMT == 3 || FMT == 4;      // NVFP4 weights, 16-bit activations
   constexpr bool F16S = FMT == 5;                // bf16 activations, fp16 scales
+  constexpr bool W8 = FMT == 6 || FMT == 7;      // 8-bit integer codes
   constexpr int RX = units_per_stage(BT);
   // tensor-memory columns: dequantized weight slots, then (MX) the A and B
   // scale factors, accumulators from column 256
@@ -759,85 +799,150 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         const uint8_t* sp = w_base + ws * p.w_bytes;
         const int i0 = ((unit & 1) == h) ? 0 : 1;   // this group's units: i0, i0 + 2
-        uint4 v[2][4];
-        uint32_t scale2[2][4], zero2[2][4], sf[2];
-        [[maybe_unused]] uint32_t lo2[2][4];   // F16S: the scales' low terms
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int i = i0 + 2 * t;
-          if (i < r) {
+        if constexpr (W8) {
+          // 8-bit codes: a unit's row is 128 bytes, so the group's units are
+          // read, dequantized and stored one at a time, and the slot goes back
+          // once the last of them is in registers
+          const int mine = i0 < r ? (r - i0 + 1) / 2 : 0;   // units i0, i0 + 2 below r
+          if (mine == 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&w_empty[ws]);
+          }
+          for (int t = 0; t < mine; ++t) {
+            const int i = i0 + 2 * t;
             const uint8_t* bp = sp + i * blk_bytes;   // this unit's packed block
             const uint4* wv = reinterpret_cast<const uint4*>(bp);
+            const uint16_t* sv = reinterpret_cast<const uint16_t*>(bp + p.s_off);
+            const uint8_t* zv = bp + p.z_off;
+            uint32_t sc[4], ze[4];   // per 32 k (a group spans at least 32 k)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[t][j] = wv[(q * 4 + j) * 32 + lane];
-            if constexpr (MX) {
-              sf[t] = reinterpret_cast<const uint32_t*>(bp + p.s_off)[row];
-            } else {
-              const uint16_t* sv = reinterpret_cast<const uint16_t*>(bp + p.s_off);
-              const uint8_t* zv = bp + p.z_off;
+            for (int c = 0; c < 4; ++c) {
+              const int sg = c >> p.sg_shift;
+              const uint32_t sbits = sv[sg * kTileN + row];
+              const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 128u;
+              if constexpr (FP16) {
+                sc[c] = sbits * 0x00010001u;
+                ze[c] = (0x6400u + zq) * 0x00010001u;   // 1024 + z, a pair
+              } else {
+                sc[c] = sbits << 16;                      // the bf16 scale as fp32
+                ze[c] = __float_as_uint(32768.0f + (float)zq);
+              }
+            }
+            const int g = unit + i;                    // unit index within the CTA
+            const int slot = g & (kASlots - 1);
+            const uint32_t aphase = (uint32_t)(g / kASlots) & 1u;
+            const uint32_t tbase = tmem_base + lane_addr + slot * kSlotCols;
+            // the row's 128 codes in two halves of four vectors (16 k each),
+            // so that only one half is held in registers
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                if constexpr (NV) {   // two 16-k block scales per 32-k chunk
-                  scale2[t][j] = (uint32_t)sv[(2 * j) * kTileN + row] * 0x00010001u;
-                  zero2[t][j] = (uint32_t)sv[(2 * j + 1) * kTileN + row] * 0x00010001u;
-                } else {
-                  const int sg = j >> p.sg_shift;
-                  if constexpr (F16S)   // the fp16 scale as two bf16 terms (pairs)
-                    split_f16_scale(sv[sg * kTileN + row], scale2[t][j], lo2[t][j]);
-                  else
-                    scale2[t][j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
-                  const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
-                  zero2[t][j] = (magic16 + zq) * 0x00010001u;
+            for (int hf = 0; hf < 2; ++hf) {
+              uint4 v8[4];
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) v8[jj] = wv[(q * 8 + 4 * hf + jj) * 32 + lane];
+              if (hf == 1 && t == mine - 1) {   // every read of the slot by this warp is done
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&w_empty[ws]);
+              }
+              if (hf == 0 && !mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
+                                        kStatusTimeout)) {
+                ok = false;
+                break;
+              }
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {   // 16 k -> 8 columns each
+                const int j = 4 * hf + jj;
+                uint32_t out[8];
+                dequant_vec8<FP16>(v8[jj], ze[j >> 1], sc[j >> 1], out);
+                tmem_st8(tbase + j * 8, out);
+              }
+            }
+            if (!ok) break;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[slot]);
+          }
+        } else {
+          uint4 v[2][4];
+          uint32_t scale2[2][4], zero2[2][4], sf[2];
+          [[maybe_unused]] uint32_t lo2[2][4];   // F16S: the scales' low terms
+  #pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int i = i0 + 2 * t;
+            if (i < r) {
+              const uint8_t* bp = sp + i * blk_bytes;   // this unit's packed block
+              const uint4* wv = reinterpret_cast<const uint4*>(bp);
+  #pragma unroll
+              for (int j = 0; j < 4; ++j) v[t][j] = wv[(q * 4 + j) * 32 + lane];
+              if constexpr (MX) {
+                sf[t] = reinterpret_cast<const uint32_t*>(bp + p.s_off)[row];
+              } else {
+                const uint16_t* sv = reinterpret_cast<const uint16_t*>(bp + p.s_off);
+                const uint8_t* zv = bp + p.z_off;
+  #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  if constexpr (NV) {   // two 16-k block scales per 32-k chunk
+                    scale2[t][j] = (uint32_t)sv[(2 * j) * kTileN + row] * 0x00010001u;
+                    zero2[t][j] = (uint32_t)sv[(2 * j + 1) * kTileN + row] * 0x00010001u;
+                  } else {
+                    const int sg = j >> p.sg_shift;
+                    if constexpr (F16S)   // the fp16 scale as two bf16 terms (pairs)
+                      split_f16_scale(sv[sg * kTileN + row], scale2[t][j], lo2[t][j]);
+                    else
+                      scale2[t][j] = (uint32_t)sv[sg * kTileN + row] * 0x00010001u;
+                    const uint32_t zq = p.has_zp ? (uint32_t)zv[sg * kTileN + row] : 8u;
+                    zero2[t][j] = (magic16 + zq) * 0x00010001u;
+                  }
                 }
               }
             }
           }
-        }
-        // every read of the slot by this warp is done (or it holds none of
-        // the group's units)
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&w_empty[ws]);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int i = i0 + 2 * t;
-          if (i >= r) break;
-          const int g = unit + i;                    // unit index within the CTA
-          const int slot = g & (kASlots - 1);
-          const uint32_t aphase = (uint32_t)(g / kASlots) & 1u;
-          if (!mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
-                         kStatusTimeout)) {
-            ok = false;
-            break;
-          }
-          if constexpr (MX) {
-            // 128 e2m1 codes of this row -> 128 e4m3 bytes (32 columns), and
-            // its four e8m0 block scales -> the slot's four scale columns
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t o8[8];
-              dequant_vec_mx(v[t][j], o8);
-              tmem_st8(tmem_base + lane_addr + slot * kSlotCols + j * 8, o8);
-            }
-            const uint32_t sf4[4] = {sf[t], sf[t], sf[t], sf[t]};
-            tmem_st4(tmem_base + lane_addr + kSfaCol + slot * 4, sf4);
-          } else {
-            const uint32_t tbase = tmem_base + lane_addr + slot * kSlotCols;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t out[16];
-              if constexpr (NV)
-                dequant_vec_nv<FP16>(v[t][j], scale2[t][j], zero2[t][j], out);
-              else if constexpr (F16S)
-                dequant_vec_f16s(v[t][j], zero2[t][j], scale2[t][j], lo2[t][j], out);
-              else
-                dequant_vec<FP16>(v[t][j], zero2[t][j], scale2[t][j], out);
-              tmem_st16(tbase + j * 16, out);
-            }
-          }
-          tmem_wait_st();
-          tc_fence_before();
+          // every read of the slot by this warp is done (or it holds none of
+          // the group's units)
           __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[slot]);
+          if (lane == 0) mbar_arrive(&w_empty[ws]);
+  #pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int i = i0 + 2 * t;
+            if (i >= r) break;
+            const int g = unit + i;                    // unit index within the CTA
+            const int slot = g & (kASlots - 1);
+            const uint32_t aphase = (uint32_t)(g / kASlots) & 1u;
+            if (!mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
+                           kStatusTimeout)) {
+              ok = false;
+              break;
+            }
+            if constexpr (MX) {
+              // 128 e2m1 codes of this row -> 128 e4m3 bytes (32 columns), and
+              // its four e8m0 block scales -> the slot's four scale columns
+  #pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t o8[8];
+                dequant_vec_mx(v[t][j], o8);
+                tmem_st8(tmem_base + lane_addr + slot * kSlotCols + j * 8, o8);
+              }
+              const uint32_t sf4[4] = {sf[t], sf[t], sf[t], sf[t]};
+              tmem_st4(tmem_base + lane_addr + kSfaCol + slot * 4, sf4);
+            } else {
+              const uint32_t tbase = tmem_base + lane_addr + slot * kSlotCols;
+  #pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t out[16];
+                if constexpr (NV)
+                  dequant_vec_nv<FP16>(v[t][j], scale2[t][j], zero2[t][j], out);
+                else if constexpr (F16S)
+                  dequant_vec_f16s(v[t][j], zero2[t][j], scale2[t][j], lo2[t][j], out);
+                else
+                  dequant_vec<FP16>(v[t][j], zero2[t][j], scale2[t][j], out);
+                tmem_st16(tbase + j * 16, out);
+              }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[slot]);
+          }
         }
         unit += r;
         if (++ws == SW) {
@@ -1231,6 +1336,10 @@ cudaError_t launch_w4a16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
                            : launch_bt<4, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
     case 5: return grouped ? launch_bt<5, true>(tmap_a, tmap_c, p, block_tok, grid, stream)
                            : launch_bt<5, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
+    case 6: return grouped ? launch_bt<6, true>(tmap_a, tmap_c, p, block_tok, grid, stream)
+                           : launch_bt<6, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
+    case 7: return grouped ? launch_bt<7, true>(tmap_a, tmap_c, p, block_tok, grid, stream)
+                           : launch_bt<7, false>(tmap_a, tmap_c, p, block_tok, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1281,11 +1390,54 @@ __global__ void debug_dequant_kernel(const uint8_t* packed, uint16_t* out, int n
   }
 }
 
+// W8A16: the 8-bit blocks' 1024 vectors (16 k of one row each).
+template <bool FP16>
+__global__ void debug_dequant8_kernel(const uint8_t* packed, uint16_t* out, int n, int k,
+                                      int group, int has_zp, int gated) {
+  const int KT = k / kTileK;
+  const long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long total = (long long)(n / kTileN) * KT * 1024;
+  if (vec >= total) return;
+  const long long blk = vec / 1024;
+  const int v = (int)(vec % 1024);
+  const int nt = (int)(blk / KT), kt = (int)(blk % KT);
+  const int t = v & 31, j = (v >> 5) & 7, q = v >> 8;
+  const int row = q * 32 + t;
+  const int st = group < kTileK ? kTileK / group : 1;
+  const int sg = group < kTileK ? (16 * j) / group : 0;
+  const uint8_t* bp = packed + blk * packed_block_bytes(false, st, has_zp != 0, true);
+  const uint4 wv = reinterpret_cast<const uint4*>(bp)[v];
+  const uint32_t sbits =
+      reinterpret_cast<const uint16_t*>(bp + packed_code_bytes(true))[sg * kTileN + row];
+  const uint32_t zq =
+      has_zp ? (uint32_t)(bp + packed_code_bytes(true) + packed_scale_bytes(false, st))[sg * kTileN + row]
+             : 128u;
+  uint32_t o[8];
+  if constexpr (FP16)
+    dequant_vec8<true>(wv, (0x6400u + zq) * 0x00010001u, sbits * 0x00010001u, o);
+  else
+    dequant_vec8<false>(wv, __float_as_uint(32768.0f + (float)zq), sbits << 16, o);
+  const int nn = packed_source_col(nt, row, n, gated);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int kk = kt * kTileK + j * 16 + 2 * c;
+    out[(long long)kk * n + nn] = (uint16_t)(o[c] & 0xFFFF);
+    out[(long long)(kk + 1) * n + nn] = (uint16_t)(o[c] >> 16);
+  }
+}
+
 cudaError_t launch_debug_dequant(const uint8_t* packed, uint16_t* out, int64_t n, int64_t k,
                                  int group, int has_zp, bool fp16, bool nv, bool f16s,
-                                 int gated, cudaStream_t stream) {
-  const long long total = (n / kTileN) * (k / kTileK) * 512;
+                                 bool w8, int gated, cudaStream_t stream) {
   const int threads = 256;
+  if (w8) {
+    const long long total8 = (n / kTileN) * (k / kTileK) * 1024;
+    auto kern8 = fp16 ? debug_dequant8_kernel<true> : debug_dequant8_kernel<false>;
+    kern8<<<(unsigned)((total8 + threads - 1) / threads), threads, 0, stream>>>(
+        packed, out, (int)n, (int)k, group, has_zp, gated);
+    return cudaGetLastError();
+  }
+  const long long total = (n / kTileN) * (k / kTileK) * 512;
   const unsigned blocks = (unsigned)((total + threads - 1) / threads);
   auto kern = fp16   ? (nv ? debug_dequant_kernel<true, true, false>
                            : debug_dequant_kernel<true, false, false>)

@@ -70,6 +70,13 @@ def test_packed_size_host_only(Q):
     st, b = Q.qgemm_packed_size(_layer(Q, act_dtype=Q.QGEMM_BF16, out_dtype=Q.QGEMM_BF16,
                                        scale_format=Q.QGEMM_S_BF16, gated_act=1))
     assert st == Q.QGEMM_OK and b == blocks * (8192 + 256)
+    # W8A16: 16384 code bytes per block, the scales and zero points as INT4
+    st, b = Q.qgemm_packed_size(_layer(Q, weight_format=Q.QGEMM_W_INT8_SYM))
+    assert st == Q.QGEMM_OK and b == blocks * (16384 + 256)
+    st, b = Q.qgemm_packed_size(_layer(Q, weight_format=Q.QGEMM_W_UINT8_ZP,
+                                       zero_format=Q.QGEMM_Z_UINT8, group_size=64,
+                                       num_experts=2))
+    assert st == Q.QGEMM_OK and b == 2 * blocks * (16384 + 2 * 256 + 2 * 128)
     # fp16 scales against bf16 activations: the scales keep their 16 bits
     st, b = Q.qgemm_packed_size(_layer(Q, act_dtype=Q.QGEMM_BF16, out_dtype=Q.QGEMM_BF16,
                                        scale_format=Q.QGEMM_S_FP16))
@@ -95,6 +102,10 @@ def test_packed_size_host_only(Q):
     (dict(weight_format=3, scale_format=0, group_size=16), "UNSUPPORTED"),   # needs e4m3 scales
     (dict(weight_format=3, scale_format=3, group_size=16, zero_format=1), "UNSUPPORTED"),
     (dict(gated_act=1), "UNSUPPORTED"),             # a gated output must be bf16
+    (dict(weight_format=4, zero_format=2), "UNSUPPORTED"),   # zeros with symmetric INT8
+    (dict(weight_format=5, zero_format=1), "UNSUPPORTED"),   # UINT8 needs 8-bit zeros
+    (dict(weight_format=4, act_dtype=1, out_dtype=1), "UNSUPPORTED"),   # fp16 scales, bf16 act
+    (dict(weight_format=4, group_size=48), "UNSUPPORTED"),
 ])
 def test_rejections_are_clear(Q, bad, code):
     st, _ = Q.qgemm_packed_size(_layer(Q, **bad))

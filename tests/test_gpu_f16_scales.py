@@ -47,9 +47,8 @@ def test_every_code_zero_and_scale(Q):
     scale of either sign (subnormals included)."""
     from quantized_weight_gemm_run_b300.api import W4A16Linear
     k, n, g = 4096, 512, 32
-    q = np.tile(np.arange(16), (k * n) // 16).reshape(k, n)
-    q = np.roll(q, 3, axis=1)
-    z = (np.arange((k // g) * n) % 16).reshape(k // g, n)
+    q = (np.arange(k)[:, None] + np.arange(n)[None, :]) % 16   # every code in every group
+    z = np.repeat((np.arange(k // g) % 16)[:, None], n, axis=1)   # one zero point per group
     finite = np.concatenate([np.arange(0x7C00), 0x8000 + np.arange(0x7C00)]).astype(np.uint16)
     bits = np.resize(np.random.default_rng(7).permutation(finite), (k // g) * n)
     s = bits.view(np.float16).astype(np.float64).reshape(k // g, n)

@@ -540,3 +540,34 @@ def test_int8_sym_brute_force_small():
             assert s[gi, n] == sv
             for i, v in enumerate(col):
                 assert q[32 * gi + i, n] == max(-128, min(127, int(np.rint(v / sv))))
+
+
+@pytest.mark.parametrize("gsize,zp", [(32, True), (128, False), (256, True)])
+def test_packed_w8_scalar_spec(gsize, zp):
+    """8-bit packed blocks are [codes 16384][scales 256 ST][zeros 128 ST]: the
+    byte of (k, n) is byte 16 v + c of its block with v = (qd*8 + j)*32 + t,
+    row 32 qd + t, k-offset 16 j + c; read single entries back by address."""
+    g = np.random.default_rng(18)
+    k, n = 512, 256
+    q = g.integers(0, 256, (k, n)) if zp else g.integers(-128, 128, (k, n))
+    sb = g.integers(0, 65535, (k // gsize, n)).astype(np.uint16)
+    z = g.integers(0, 256, (k // gsize, n)) if zp else None
+    buf = layout.packed_w8(q, sb, z, gsize, signed=not zp)
+    st = max(1, 128 // gsize)
+    blk = 16384 + 256 * st + (128 * st if zp else 0)
+    kt_count = k // 128
+    assert buf.size == kt_count * (n // 128) * blk
+    for _ in range(1500):
+        kk, nn = int(g.integers(0, k)), int(g.integers(0, n))
+        nt, r = divmod(nn, 128)
+        kt, kl = divmod(kk, 128)
+        base = (nt * kt_count + kt) * blk
+        qd, t = divmod(r, 32)
+        j, c = divmod(kl, 16)
+        v = (qd * 8 + j) * 32 + t
+        assert buf[base + 16 * v + c] == (q[kk, nn] if zp else q[kk, nn] + 128)
+        sg = kl // gsize if gsize < 128 else 0
+        sbyte = base + 16384 + 2 * (sg * 128 + r)
+        assert int(buf[sbyte]) | (int(buf[sbyte + 1]) << 8) == sb[kk // gsize, nn]
+        if zp:
+            assert buf[base + 16384 + 256 * st + sg * 128 + r] == z[kk // gsize, nn]
