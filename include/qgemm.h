@@ -1,12 +1,13 @@
 /*
  * qgemm.h -- C ABI of the B300 (sm_103a) quantized-weight GEMM library.
  *
- * The library runs the hot path of a mixed-precision GEMM over 4-bit quantized
+ * The library runs the hot path of a mixed-precision GEMM over quantized
  * weights: W4A16 (INT4 / UINT4 codes with per-group fp16 or bf16 scales and
  * optional zero points, dequantized in registers and fed to 16-bit tensor-core
- * MMA with fp32 accumulation), W4A8-MXFP4 (e2m1 codes with e8m0 per-32 scales
- * against per-token FP8 e4m3 activations) and the grouped-MoE variant that
- * runs one such GEMM per expert over router-permuted tokens.
+ * MMA with fp32 accumulation; also NVFP4 codes, and 8-bit INT8 / UINT8 codes
+ * as W8A16), W4A8-MXFP4 (e2m1 codes with e8m0 per-32 scales against per-token
+ * FP8 e4m3 activations) and the grouped-MoE variant that runs one such GEMM
+ * per expert over router-permuted tokens.
  *
  * Where the operations come from (the Humming pages; titles and sections):
  *   - kinachrichten.com, "Ant Group und vLLM stellen Humming als Open Source
@@ -379,7 +380,7 @@ qgemm_status qgemm_moe_combine(const void* y2, const int32_t* inv_perm,
 /*
  * Debug: the weights of a packed layer (expert 0 or the dense layer) as the
  * kernels feed them to the tensor core, written as out[k, n] (device, [K, N]):
- * W4A16 the dequantized values in act_dtype, computed with exactly the
+ * W4A16 and W8A16 the dequantized values in act_dtype, computed with exactly the
  * kernels' arithmetic (NVFP4: e2m1 x block scale; the tensor scale multiplies
  * the fp32 sum); MXFP4 the e4m3 byte of each e2m1 code (the e8m0 block
  * scale is applied inside the MMA).  Columns are in the standard order for
