@@ -489,9 +489,9 @@ def test_bitstream_round_trip_every_code(bits, signed):
     assert np.array_equal(quant.unpack_int_kn(words, bits, signed), q)
     z = g.integers(0, 2 ** bits, size=(4, 64))
     assert np.array_equal(quant.unpack_zeros_bits(quant.pack_zeros_bits(z, bits), bits), z)
+    too_big = 2 ** (bits - 1) if signed else 2 ** bits     # one past the largest code
     with pytest.raises(ValueError):
-        quant.pack_int_kn(q[:, :1] * 0 + (2 ** bits if not signed else 2 ** (bits - 1)), bits,
-                          signed)
+        quant.pack_int_kn(np.full((k, 1), too_big), bits, signed)
 
 
 def test_four_bit_quantizers_are_the_int4_ones():
