@@ -173,9 +173,10 @@ typedef struct {
  *   cta_pair   reserved, must be 0
  *   kernel     0 = the heuristic's choice, 1 = the persistent tcgen05 kernel,
  *              2 = the small-M kernel (cp.async + mma.sync, split K; dense
- *              INT4 / UINT4 with m <= 16 only, not gated, deterministic or
- *              batch-invariant; split_k, when set, is its number of K
- *              slices per n-tile; it ignores the other tuning fields)
+ *              INT4 / UINT4 with scales in the activation dtype and m <= 16
+ *              only, not gated, deterministic or batch-invariant; split_k,
+ *              when set, is its number of K slices per n-tile; it ignores
+ *              the other tuning fields)
  */
 typedef struct {
   int32_t block_tok;
