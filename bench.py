@@ -5,7 +5,7 @@ UINT4 weights with bf16 group-128 scales and uint4 zero points, bf16
 activations, (N, K) in {(4096, 4096), (11008, 4096), (4096, 11008)} x
 M in {1, 4, 16, 64, 256, 1024}.  One step runs all 18 GEMMs once through the
 library's C ABI; every GEMM has its own weight and activation buffers, so a
-step touches ~330 MB and each GEMM reads its operands cold from HBM (the
+step touches ~438 MB and each GEMM reads its operands cold from HBM (the
 126 MB L2 is flushed by the rest of the step).  The step is captured in a
 CUDA graph and replayed.
 
@@ -157,13 +157,14 @@ def point_flops(p):
 
 class ClockSampler:
     """SM clock and clock-event reasons sampled through NVML (read-only queries)
-    every 50 ms on a background thread while the timed region runs."""
+    every `period` seconds on a background thread while the timed region runs."""
 
     REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
                "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, index):
+    def __init__(self, index, period=0.005):
         self.index = index
+        self.period = period
         self.samples = []
         self.max_mhz = None
         self._stop = None
@@ -199,7 +200,7 @@ class ClockSampler:
                     self.samples.append(sample())
                 except Exception as e:
                     self.error = str(e)
-                self._stop.wait(0.05)
+                self._stop.wait(self.period)
 
         self._thread = threading.Thread(target=run, daemon=True)
         self._thread.start()
@@ -446,6 +447,143 @@ def kernel_name(p):
     return f"w4a16_kernel<{bt},{fmt},dense>"
 
 
+EXTRA_WORKLOADS = ["w4a16_m16", "w4a8", "moe16", "moe256", "moe4096", "large"]
+REPLAYS = 7
+
+
+def graph_time_us(launch, n_launch, stream, replays=REPLAYS):
+    """Median over `replays` replays of a graph holding n_launch back-to-back
+    launches (`launch(j)` issues the j-th), per launch, by CUDA events on the
+    launching stream after three warm-up replays."""
+    import torch
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=stream):
+        for j in range(n_launch):
+            launch(j)
+    torch.cuda.synchronize()
+    ts = []
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g2.replay()
+        for _ in range(replays):
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            g2.replay()
+            a1.record(stream)
+            ts.append((a0, a1))
+    torch.cuda.synchronize()
+    us = sorted(a0.elapsed_time(a1) * 1e3 / n_launch for a0, a1 in ts)
+    del g2
+    return us[len(us) // 2], us[0], us[-1]
+
+
+def cublas_context_us(p, stream):
+    """torch.matmul (cuBLAS) of the same shape in the activation dtype on
+    dense 16-bit weights, over a rotation of cold copies: the library
+    comparison point of the pages' small-batch claim.  Context only."""
+    import torch
+    if p.get("kind") == "moe":
+        return None
+    m, n, k = p["m"], p["n"], p["k"]
+    dt = torch.float16 if p["adt"] == "fp16" else torch.bfloat16
+    per = 2 * (m * k + k * n + m * n)
+    copies = int(np.ceil(2 * L2_BYTES / per)) + 1
+    bufs = [(torch.randn(m, k, device="cuda").to(dt), torch.randn(k, n, device="cuda").to(dt),
+             torch.empty(m, n, device="cuda", dtype=dt)) for _ in range(copies)]
+    r = max(20, copies)
+
+    def launch(j):
+        a, b, c = bufs[j % copies]
+        torch.matmul(a, b, out=c)
+    med, _, _ = graph_time_us(launch, r, stream)
+    del bufs
+    torch.cuda.empty_cache()
+    return med
+
+
+def measure_point(bp, p, peaks, stream):
+    """One point of the table: the launch timed back to back over a rotation
+    of cold clones in a graph (median of REPLAYS replays), with its rates and
+    fractions of the measured peaks, and the cuBLAS context time."""
+    import torch
+    is_moe = p.get("kind") == "moe"
+    copies = [bp] + ([] if is_moe else [bp.clone() for _ in range(cold_copies(p) - 1)])
+    r = max(20, len(copies))
+    med, lo, hi = graph_time_us(lambda j: copies[j % len(copies)].launch(), r, stream)
+    del copies
+    torch.cuda.empty_cache()
+    fl, by = point_flops(p), point_bytes(p)
+    d = dict(m=p["m"], n=p["n"], k=p["k"], us=round(med, 3), us_min=round(lo, 3),
+             us_max=round(hi, 3), tflops=round(fl / med / 1e6, 2),
+             gbs=round(by / med / 1e3, 1), hbm_frac=round(by / med / 1e3 / peaks["hbm_gbs"], 3),
+             kernel=kernel_name(p))
+    if p.get("kind") == "w4a8":
+        fp8 = peaks.get("fp8_tflops")
+        d["fp8_tensor_frac"] = round(fl / med / 1e6 / fp8, 3) if fp8 else None
+    else:
+        d["tensor_frac"] = round(fl / med / 1e6 / peaks["bf16_tflops"], 3)
+    if is_moe:
+        d["tokens_per_s"] = round(p["m"] / (med * 1e-6), 1)
+        d.pop("n"), d.pop("k")
+        d["tokens"] = d.pop("m")
+    else:
+        cb = cublas_context_us(p, stream)
+        d["cublas_bf16_us"] = round(cb, 3)
+        d["speedup_vs_cublas"] = round(cb / med, 2)
+    return d
+
+
+def launch_floor_us(stream):
+    """The harness floor: a one-element fill kernel launched back to back in
+    the same graph harness (no data, no dependency beyond stream order)."""
+    import torch
+    x = torch.empty(1, device="cuda")
+    med, _, _ = graph_time_us(lambda j: x.fill_(float(j)), 40, stream)
+    return round(med, 3)
+
+
+def marginal_rates(per_point, pts):
+    """Marginal HBM rate per M between the 4096 x 4096 GEMM and the two
+    larger ones: extra algorithmic bytes / extra time (GB/s).  Separates the
+    fixed cost of a launch from its streaming rate."""
+    out = []
+    by = {(p["m"], p["n"], p["k"]): (pp["us"], point_bytes(p)) for pp, p in zip(per_point, pts)}
+    for m in sorted({p["m"] for p in pts}):
+        base = by.get((m, 4096, 4096))
+        if not base:
+            continue
+        for nk in [(11008, 4096), (4096, 11008)]:
+            other = by.get((m,) + nk)
+            if other and other[0] > base[0]:
+                out.append(dict(m=m, vs=f"{nk[0]}x{nk[1]}",
+                                gbs=round((other[1] - base[1]) / (other[0] - base[0]) / 1e3, 1)))
+    return out
+
+
+def measured_peaks_here(stream, peaks):
+    """The dense FP8 e4m3 tensor peak, measured once per run (torch._scaled_mm,
+    8192^3, best of 10 replays of 10 launches; read-only), so that W4A8 gets a
+    tensor fraction; stored into `peaks` as fp8_tflops."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device="cuda")
+
+        def launch(_):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        launch(0)
+        torch.cuda.synchronize()
+        _, best, _ = graph_time_us(launch, 10, stream, replays=10)
+        tf = 2 * n ** 3 / best / 1e6
+        peaks["fp8_tflops"] = round(tf, 1)
+        return {"fp8_tflops": round(tf, 1), "how": "torch._scaled_mm e4m3 8192^3, best of 10"}
+    except Exception as e:   # no FP8 GEMM in this torch build
+        return {"fp8_tflops": None, "error": str(e)[:120]}
+
+
 def run_ours(args, rank, world, device):
     import torch
     pts, cfg = workload_points(args.workload)
@@ -512,36 +650,25 @@ def run_ours(args, rank, world, device):
         value = whole_job_rate(flops_step, args.steps, ms_total, world) / 1e12
         unit = "TFLOP/s"
 
-    # per-GEMM device times (dominant kernel and the per-M table): each GEMM
-    # launched back to back over a rotation of cold clones, inside a graph
-    per_point = []
-    for i, p in enumerate(pts):
-        copies = [base[i]] + ([] if is_moe else
-                              [base[i].clone() for _ in range(cold_copies(p) - 1)])
-        r = max(20, len(copies))
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g2, stream=stream):
-            for j in range(r):
-                copies[j % len(copies)].launch()
-        torch.cuda.synchronize()
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                g2.replay()
-            a0.record(stream)
-            g2.replay()
-            a1.record(stream)
-        torch.cuda.synchronize()
-        us = a0.elapsed_time(a1) * 1e3 / r
-        per_point.append(dict(m=p["m"], n=p["n"], k=p["k"], us=round(us, 3),
-                              tflops=round(point_flops(p) / us / 1e6, 2),
-                              gbs=round(point_bytes(p) / us / 1e3, 1),
-                              hbm_frac=round(point_bytes(p) / us / 1e3 / peaks["hbm_gbs"], 3),
-                              tensor_frac=round(point_flops(p) / us / 1e6 / peaks["bf16_tflops"], 3),
-                              kernel=kernel_name(p)))
-        del g2, copies
-        torch.cuda.empty_cache()
+    # per-GEMM device times (dominant kernel and the per-M table)
+    peaks_here = measured_peaks_here(stream, peaks)
+    clocks_pts = ClockSampler(torch.cuda.current_device())
+    clocks_pts.start()
+    per_point = [measure_point(bp, p, peaks, stream) for bp, p in zip(base, pts)]
+    # the other configurations of the workload set, each timed the same way
+    extra_points = []
+    if not args.no_extra and args.workload == "sweep":
+        for wl in EXTRA_WORKLOADS:
+            xpts, xcfg = workload_points(wl)
+            for i, p in enumerate(xpts):
+                bp = make_point(p, 2000 + i, device)
+                torch.cuda.synchronize()
+                d = measure_point(bp, p, peaks, stream)
+                d["workload"] = xcfg["workload"]
+                extra_points.append(d)
+                del bp
+                torch.cuda.empty_cache()
+    clk_pts = clocks_pts.stop()
     # dominant kernel: the instantiation with the largest share of step time
     share = {}
     for pp, p in zip(per_point, pts):
@@ -550,7 +677,7 @@ def run_ours(args, rank, world, device):
         share[pp["kernel"]][1] += point_flops(p)
         share[pp["kernel"]][2] += point_bytes(p)
         share[pp["kernel"]][3].append(p["m"])
-    dom = max(share.items(), key=lambda kv: kv[1][0])
+    dom = max(share.items(), key=lambda kv: kv[1][0])   # over the workload's own GEMMs
     dom_us, dom_flops, dom_bytes, dom_ms = dom[1]
     dom_launches = len(dom_ms)
     tensor_bound = (dom_flops / dom_bytes) > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -621,7 +748,11 @@ def run_ours(args, rank, world, device):
                        parallelism=f"replicas x{world}"),
         "hbm_gbs": round(world * bytes_step * args.steps / (ms_total * 1e-3) / 1e9, 1),
         "roofline": roof,
-        "points": per_point,
+        "points": per_point + extra_points,
+        "floor_us": launch_floor_us(stream),
+        "marginal": marginal_rates(per_point, pts),
+        "peaks_here": peaks_here,
+        "clocks_points": clk_pts,
         "e2e": {"value": round(e2e_val, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": sum(gm.launches for gm in gemms) * args.steps,
@@ -782,6 +913,8 @@ def main():
                     help="sweep | f16s | w8a16 | nvfp4 | w4a16_m16 | large | w4a8 | moe16 | "
                          "moe256 | moe4096 | shape:M,N,K[,sym|asym][,bf16|fp16][,f16s]")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="sweep only: skip timing the other configurations")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

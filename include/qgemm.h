@@ -228,10 +228,23 @@ typedef struct {
 /*
  * Bytes of the packed (kernel-layout) buffer of one layer (all experts).
  * Returns INVALID_ARG / UNSUPPORTED on a bad config.
+ * Source: the preprocessing step that checks the parameters and repacks the
+ * tensors for the target kernel (kinachrichten.com, "Wie die Architektur
+ * funktioniert"); the buffer's size is that of the repacked tensors.
  */
 qgemm_status qgemm_packed_size(const qgemm_layer_config* layer, size_t* bytes);
 
 /*
+ * Source: the standard format that every export is converted into
+ * (jetabc.cn, "Humming 的做法", item 1) and the preprocessing that checks
+ * the parameters and repacks the tensors for the target kernel
+ * (kinachrichten.com, "Wie die Architektur funktioniert"); repacking changes
+ * the arrangement, never the meaning of the values (retrivium.ai, "vLLM
+ * Humming: why shared quantization still needs specialized kernels",
+ * section "Representation answers a different question"); preparation is
+ * kept apart from repeated execution (retrivium.ai, "humming-format-kernel-
+ * contract-release", section "Compilation and measurement boundaries").
+ *
  * Preprocessing (the "repack for the target kernel" step): validates the
  * config and rearranges the standard-format tensors (device, layout above)
  * into one packed device buffer (`packed`, qgemm_packed_size bytes, 16-byte
@@ -260,12 +273,19 @@ qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qwe
  * zero-filled once before first use (qgemm_workspace_init); every successful
  * call leaves the counters at zero again.  One workspace must not be used by
  * two calls that can run at the same time.
+ * Source: its size follows the plan that the device heuristic picks from the
+ * tuning config (tile shapes, pipeline stages) for the input-size range, and
+ * the scheduling component that splits the K range of a tile across CTAs
+ * (kinachrichten.com, "Wie die Architektur funktioniert" and "Kompilierzeiten
+ * und geraetespezifisches Tuning").  The caller owns the memory: the library
+ * allocates none.
  */
 qgemm_status qgemm_workspace_size(const qgemm_layer_config* layer,
                                   const qgemm_compute_config* compute,
                                   const qgemm_tuning_config* tuning, int64_t m, size_t* bytes);
 
-/* Zero-fill a workspace on `stream` (asynchronous). */
+/* Zero-fill a workspace on `stream` (asynchronous).  A helper of this
+ * library's workspace convention; the pages have no counterpart. */
 qgemm_status qgemm_workspace_init(void* workspace, size_t bytes, void* stream);
 
 /*
@@ -279,6 +299,18 @@ qgemm_status qgemm_workspace_init(void* workspace, size_t bytes, void* stream);
  *   workspace device, >= qgemm_workspace_size bytes, zero-initialised once
  * With compute->deterministic = 1 the split-K reduction runs in a fixed order
  * and results are bitwise reproducible for a given (config, m, tuning, device).
+ * Source: one kernel described by a layer config (shapes, data types,
+ * quantization parameters), a compute config (the GEMM type and options such
+ * as batch invariance) and a tuning config chosen by device heuristics, with
+ * different kernels for different input-size ranges (kinachrichten.com, "Wie
+ * die Architektur funktioniert"), built from scheduling, data movement,
+ * dequantization and scaling, tensor-core compute and output processing
+ * (same page, "Kompilierzeiten und geraetespezifisches Tuning", which also
+ * describes the W4A8-MXFP4 path); the W4A16 and W4A8-MXFP4 kernel families
+ * (jetabc.cn, "跑得有多快", items 1, 2 and 4).  Unsupported combinations are
+ * rejected with a clear status (retrivium.ai, "vLLM Humming: why shared
+ * quantization still needs specialized kernels", section "The architectural
+ * gain is a smaller maintenance surface").
  */
 qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_config* compute,
                        const qgemm_tuning_config* tuning, int64_t m, const void* a,
@@ -292,23 +324,38 @@ qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_conf
  * every device byte, start-up or recovery paths that must not touch the
  * allocator).  The Humming pages have no counterpart to this entry point.
  * It allocates nothing: the split-K scratch is a fixed 32 MiB array inside
- * the library that every GPU loading the library holds until the process
- * exits.  Arguments and results are those of qgemm_run (dense GEMMs only).
- *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ * the library, held on each GPU until the process exits.  Arguments and
+ * results are those of qgemm_run (dense GEMMs only).
+ *   - The runtime may load the library's device code lazily: the array
+ *     becomes resident on a device when the first call made with that device
+ *     current looks up its address.  That lookup can fail for lack of device
+ *     memory (QGEMM_ERR_CUDA; the next call tries again), so make the first
+ *     call on each device early, and before any stream capture.
  *   - All calls share the array and it keeps the last call's contents: calls
  *     that can overlap on the GPU race and must be serialised by the caller.
- *     Each call zeroes the scratch its launch uses (status word, split-K
- *     counters and accumulators; cudaMemsetAsync on `stream`) first.
+ *     Each call, after every argument check has passed, zeroes the scratch its
+ *     launch uses (status word, split-K counters and accumulators;
+ *     cudaMemsetAsync on `stream`) just before the launch; a call that fails a
+ *     check queues nothing.
  *   - A problem needing more than 32 MiB of scratch is rejected with
  *     QGEMM_ERR_UNSUPPORTED before anything is launched (qgemm_last_error
- *     names the size); kernel-side timeouts are not reported by this call.
+ *     names the size).
+ *   - A kernel-side timeout is reported by qgemm_noalloc_check_status.
  */
 qgemm_status qgemm_run_noalloc(const qgemm_layer_config* layer,
                                const qgemm_compute_config* compute,
                                const qgemm_tuning_config* tuning, int64_t m, const void* a,
                                const float* a_scale, const void* packed, const void* bias,
                                void* c, void* stream);
+
+/*
+ * qgemm_check_status for the scratch of qgemm_run_noalloc on the current
+ * device: synchronizes `stream`, reads and clears the status word that the
+ * last such call's kernel left, and returns QGEMM_OK, QGEMM_ERR_TIMEOUT or
+ * QGEMM_ERR_DEVICE.  No workspace needs re-zeroing afterwards (every
+ * qgemm_run_noalloc call clears its scratch).  The pages have no counterpart.
+ */
+qgemm_status qgemm_noalloc_check_status(void* stream);
 
 /*
  * Grouped (MoE) quantized GEMM over router-permuted rows: for each expert e,
@@ -321,6 +368,12 @@ qgemm_status qgemm_run_noalloc(const qgemm_layer_config* layer,
  *   c              device [total_rows, N] ([total_rows, N/2] when gated)
  * The tile schedule is built on the device from expert_offsets: no host
  * synchronization is needed between the permute and the GEMM.
+ * Source: MoE models, where each token activates only some experts while all
+ * expert weights stay resident (kinachrichten.com, "Warum quantisierte
+ * Kernel wichtig sind"); dense and MoE workloads served by one architecture
+ * (same page, "Was Humming bietet"); the GEMM type of the compute config
+ * (same page, "Wie die Architektur funktioniert"); the grouped-MoE path on
+ * B300 (jetabc.cn, "跑得有多快", item 3).
  */
 qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
                                const qgemm_compute_config* compute,
@@ -335,6 +388,14 @@ qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
  *   a8[r, k]   = e4m3(x[r, k] / a_scale[r]), IEEE fp32 divide, round to
  *                nearest even, saturating at +-448
  *   x device bf16 [m, k]; a8 device uint8 [m, k]; a_scale device fp32 [m].
+ *   k must be a multiple of 8 (QGEMM_ERR_UNSUPPORTED otherwise); x must be
+ *   16-byte aligned, a8 8-byte aligned, a_scale 4-byte aligned.
+ * Source: quantization lowers the precision of activations as well as weights
+ * (kinachrichten.com, "Warum quantisierte Kernel wichtig sind"); the
+ * W4A8-MXFP4 path with 8-bit activations (same page, "Kompilierzeiten und
+ * geraetespezifisches Tuning"; jetabc.cn, "跑得有多快", item 4).  The pages do
+ * not define the activation scale: the per-token absmax / 448 rule above is
+ * this library's reading.
  */
 qgemm_status qgemm_quantize_act_fp8(const void* x, int64_t m, int64_t k, void* a8,
                                     float* a_scale, void* stream);
@@ -355,6 +416,11 @@ qgemm_status qgemm_quantize_act_fp8(const void* x, int64_t m, int64_t k, void* a
  *   a_perm      device [t*topk, hidden] (output): a_perm[r] = a[perm[r] / topk];
  *               it also holds the sort's per-block histograms until the
  *               gather overwrites it, so it must not overlap a or the ids
+ * Source: the MoE routing in which each token activates only a subset of the
+ * experts (kinachrichten.com, "Warum quantisierte Kernel wichtig sind"),
+ * served by the MoE backend (jetabc.cn, "怎么使用") and the grouped-MoE path
+ * (jetabc.cn, "跑得有多快", item 3).  The pages do not define the permute:
+ * a stable sort by expert is this library's reading.
  */
 qgemm_status qgemm_moe_permute(const int32_t* topk_ids, int64_t t, int32_t topk, int32_t e,
                                int32_t* offsets, int32_t* perm, int32_t* inv_perm,
@@ -363,6 +429,10 @@ qgemm_status qgemm_moe_permute(const int32_t* topk_ids, int64_t t, int32_t topk,
 /*
  * SiLU gate: h[r, i] = bf16(silu(gu[r, i]) * gu[r, inter + i]) in fp32,
  * gu device bf16 [rows, 2*inter], h device bf16 [rows, inter].
+ * Source: the output-processing component of a kernel (kinachrichten.com,
+ * "Kompilierzeiten und geraetespezifisches Tuning") in the MoE workloads the
+ * library serves (same page, "Warum quantisierte Kernel wichtig sind").  The
+ * gated activation itself is this library's reading of an MoE expert.
  */
 qgemm_status qgemm_moe_silu_mul(const void* gu, int64_t rows, int64_t inter, void* h,
                                 void* stream);
@@ -373,6 +443,10 @@ qgemm_status qgemm_moe_silu_mul(const void* gu, int64_t rows, int64_t inter, voi
  *   y2 device bf16 [t*topk, hidden]; inv_perm device int32 [t*topk] (from
  *   qgemm_moe_permute); topk_weights device fp32 [t, topk]; y device bf16
  *   [t, hidden].
+ * Source: the MoE layer's last step, where each token's expert outputs are
+ * merged (kinachrichten.com, "Warum quantisierte Kernel wichtig sind";
+ * jetabc.cn, "跑得有多快", item 3).  The weighted sum in slot order is this
+ * library's reading.
  */
 qgemm_status qgemm_moe_combine(const void* y2, const int32_t* inv_perm,
                                const float* topk_weights, int64_t t, int32_t topk,
@@ -386,6 +460,9 @@ qgemm_status qgemm_moe_combine(const void* y2, const int32_t* inv_perm,
  * the fp32 sum); MXFP4 the e4m3 byte of each e2m1 code (the e8m0 block
  * scale is applied inside the MMA).  Columns are in the standard order for
  * gated layers too (the pack's gate/up interleave is undone).
+ * Source: the dequantization-and-scaling component (kinachrichten.com,
+ * "Kompilierzeiten und geraetespezifisches Tuning"), exposed so that tests
+ * can check it bit for bit.
  */
 qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* packed,
                                  void* out_kn, void* stream);
@@ -395,6 +472,8 @@ qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* pa
  * kernels, clears it and returns QGEMM_OK, QGEMM_ERR_TIMEOUT (a bounded wait
  * gave up) or QGEMM_ERR_DEVICE.  After a timeout the caller must zero the
  * workspace again (qgemm_workspace_init) before reuse.
+ * The pages have no counterpart: this reports the bounded waits of the
+ * kernels.
  */
 qgemm_status qgemm_check_status(void* workspace, void* stream);
 
@@ -411,6 +490,10 @@ void qgemm_set_wait_limit_ns(uint64_t ns);
  * (layer, compute, m) on the current device, or why the combination is
  * rejected.  Returns the status the corresponding run call would return for
  * the configuration checks.
+ * Source: the compatibility record that names the weight representation,
+ * activation type, device and shapes and which implementation serves them
+ * (retrivium.ai, "humming-format-kernel-contract-release", section "A
+ * compatibility example").
  */
 qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
                                  const qgemm_compute_config* compute, int64_t m, char* buf,

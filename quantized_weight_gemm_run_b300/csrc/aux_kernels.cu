@@ -46,44 +46,77 @@ static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cud
 }
 
 // ----------------------------------------------------------- FP8 act quant
-// One CTA per row: s = max|x| / 448 (fp32, IEEE divide; 1 for an all-zero
-// row), code = e4m3_rn_satfinite(x / s) with an IEEE fp32 divide.
-__global__ void act_quant_fp8_kernel(const uint16_t* __restrict__ x, int k,
-                                     uint8_t* __restrict__ a8, float* __restrict__ scale) {
+// One warp per row, eight rows per CTA: s = max|x| / 448 (fp32, IEEE divide;
+// 1 for an all-zero row), code = e4m3_rn_satfinite(x / s) with an IEEE fp32
+// divide.  Lanes take 16-byte vectors (8 bf16) of the row in turn; the first
+// kActVecs vectors of each lane stay in registers between the max and the
+// quantization (a 2048-wide row in one pass), the rest of a longer row is read
+// again.  Codes leave as 8-byte stores.
+constexpr int kActVecs = 8;
+constexpr int kActRowsPerCta = 8;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float absmax8(float amax, const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  return amax;
+}
+
+__device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = __nv_cvt_float_to_fp8(__fdiv_rn(bf16_lo(w[i]), s), __NV_SATFINITE,
+                                              __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float_to_fp8(__fdiv_rn(bf16_hi(w[i]), s), __NV_SATFINITE,
+                                              __NV_E4M3);
+    o[i >> 1] |= (lo | (hi << 8)) << (16 * (i & 1));
+  }
+  return make_uint2(o[0], o[1]);
+}
+
+__global__ void __launch_bounds__(32 * kActRowsPerCta)
+    act_quant_fp8_kernel(const uint4* __restrict__ x, int m, int kv, uint2* __restrict__ a8,
+                         float* __restrict__ scale) {
   pdl_trigger();
   pdl_wait();
-  const long long row = blockIdx.x;
-  const uint16_t* xr = x + row * k;
+  const int row = blockIdx.x * kActRowsPerCta + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= m) return;
+  const uint4* xr = x + (long long)row * kv;
+  uint2* out = a8 + (long long)row * kv;
+  uint4 v[kActVecs];
   float amax = 0.f;
-  for (int i = threadIdx.x; i < k; i += blockDim.x) {
-    uint16_t b = xr[i];
-    amax = fmaxf(amax, fabsf(__bfloat162float(*reinterpret_cast<__nv_bfloat16*>(&b))));
+#pragma unroll
+  for (int c = 0; c < kActVecs; ++c) {
+    const int i = lane + 32 * c;
+    v[c] = i < kv ? __ldg(xr + i) : make_uint4(0u, 0u, 0u, 0u);
   }
+#pragma unroll
+  for (int c = 0; c < kActVecs; ++c) amax = absmax8(amax, v[c]);
+  for (int i = lane + 32 * kActVecs; i < kv; i += 32) amax = absmax8(amax, __ldg(xr + i));
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  __shared__ float red[32];
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (threadIdx.x == 0) red[0] = v;
-  }
-  __syncthreads();
-  amax = red[0];
   const float s = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
-  if (threadIdx.x == 0) scale[row] = s;
-  for (int i = threadIdx.x; i < k; i += blockDim.x) {
-    uint16_t b = xr[i];
-    const float v = __fdiv_rn(__bfloat162float(*reinterpret_cast<__nv_bfloat16*>(&b)), s);
-    a8[row * k + i] = (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+  if (lane == 0) scale[row] = s;
+#pragma unroll
+  for (int c = 0; c < kActVecs; ++c) {
+    const int i = lane + 32 * c;
+    if (i < kv) out[i] = quant8(v[c], s);
   }
+  for (int i = lane + 32 * kActVecs; i < kv; i += 32) out[i] = quant8(__ldg(xr + i), s);
 }
 
 cudaError_t launch_act_quant_fp8(const uint16_t* x, int64_t m, int64_t k, uint8_t* a8,
                                  float* scale, cudaStream_t stream) {
   if (m == 0) return cudaSuccess;
-  return launch_pdl(act_quant_fp8_kernel, dim3((unsigned)m), dim3(256), stream, true, x, (int)k,
-                    a8, scale);
+  const unsigned ctas = (unsigned)((m + kActRowsPerCta - 1) / kActRowsPerCta);
+  return launch_pdl(act_quant_fp8_kernel, dim3(ctas), dim3(32 * kActRowsPerCta), stream, true,
+                    reinterpret_cast<const uint4*>(x), (int)m, (int)(k / 8),
+                    reinterpret_cast<uint2*>(a8), scale);
 }
 
 // ----------------------------------------------------------- MoE permute

@@ -198,6 +198,13 @@ cudaError_t launch_combine(const uint16_t* y2, const int32_t* inv_perm, const fl
 int set_last_error(int status, const char* message);
 int dense_workspace_bytes(const void* layer, const void* compute, const void* tuning, int64_t m,
                           size_t* must_clear, size_t* total);
+// qgemm_run that, once every argument check has passed and just before the
+// launch, zeroes the first clear_bytes of the workspace on the stream (0: no
+// clear).  A call rejected by a check queues nothing.
+int run_dense_clearing(const void* layer, const void* compute, const void* tuning, int64_t m,
+                       const void* a, const float* a_scale, const void* packed, const void* bias,
+                       void* c, void* workspace, size_t ws_bytes, size_t clear_bytes,
+                       cudaStream_t stream);
 
 bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     const uint64_t dims[3], const uint64_t strides_bytes[2],

@@ -9,17 +9,20 @@
 // that lives inside the library image: it allocates nothing and calls no
 // allocating routine.
 //
-// The array is kNoAllocScratchBytes (32 MiB) on every GPU that loads the
-// library, held until the process exits.  Its device address is looked up
-// once per device, by the first call made with that device current; that
-// first call should therefore come before any CUDA stream capture.  All calls
-// share the one array and it keeps what the last call left in it: calls that
-// can overlap on the GPU (different streams, or different host threads) race
-// on it and must be serialised by the caller.  Each call zeroes the part of
+// The array is kNoAllocScratchBytes (32 MiB) per GPU, held until the process
+// exits.  The CUDA runtime may load the library's device code lazily, so the
+// array becomes resident on a device when the first call made with that
+// device current looks up its address; that lookup can fail for lack of
+// device memory, in which case the call returns QGEMM_ERR_CUDA and the next
+// call tries again.  Make that first call early, before any CUDA stream
+// capture.  All calls share the one array and it keeps what the last call
+// left in it: calls that can overlap on the GPU (different streams, or
+// different host threads) race on it and must be serialised by the caller.
+// Each call, once its arguments have passed every check, zeroes the part of
 // the array its launch needs (status word, split-K tile counters and split-K
-// accumulators; cudaMemsetAsync on its stream, which allocates nothing)
-// before the launch.  A problem whose scratch exceeds the array is rejected
-// with QGEMM_ERR_UNSUPPORTED before anything is launched.
+// accumulators; cudaMemsetAsync on its stream, which allocates nothing) just
+// before the launch; a rejected call queues nothing.  A problem whose scratch
+// exceeds the array is rejected with QGEMM_ERR_UNSUPPORTED.
 
 #include <cstdio>
 #include <mutex>
@@ -37,23 +40,30 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 void* g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
+bool g_scratch_ok[kMaxDevices];
+std::mutex g_scratch_mu[kMaxDevices];
 
 // Device address of the scratch array on the current device.  The name of a
 // __device__ array in host code is only a host-side stand-in, so the address
-// comes from the runtime, once per device, with that device current.
+// comes from the runtime, with that device current.  Only a successful
+// lookup is kept; a failed one (say the module could not be loaded for lack
+// of memory) is retried by the next call.
 cudaError_t scratch_for_current_device(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_scratch_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_scratch_mu[dev]);
+  if (!g_scratch_ok[dev]) {
     void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      cudaGetLastError();   // do not leave the error for the caller's next CUDA call
+      return e;
+    }
     g_scratch_ptr[dev] = p;
-  });
-  if (g_scratch_err[dev] != cudaSuccess) return g_scratch_err[dev];
+    g_scratch_ok[dev] = true;
+  }
   *out = g_scratch_ptr[dev];
   return cudaSuccess;
 }
@@ -90,9 +100,17 @@ extern "C" qgemm_status qgemm_run_noalloc(const qgemm_layer_config* layer,
   cudaError_t e = scratch_for_current_device(&scratch);
   if (e != cudaSuccess)
     return qgemm_status(set_last_error(QGEMM_ERR_CUDA, cudaGetErrorString(e)));
-  e = cudaMemsetAsync(scratch, 0, must_clear, static_cast<cudaStream_t>(stream));
+  // the remaining checks run before the clear, so a rejected call queues nothing
+  return qgemm_status(run_dense_clearing(layer, compute, tuning, m, a, a_scale, packed, bias, c,
+                                         scratch, kNoAllocScratchBytes, must_clear,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" qgemm_status qgemm_noalloc_check_status(void* stream) {
+  using namespace qg;
+  void* scratch = nullptr;
+  cudaError_t e = scratch_for_current_device(&scratch);
   if (e != cudaSuccess)
     return qgemm_status(set_last_error(QGEMM_ERR_CUDA, cudaGetErrorString(e)));
-  return qgemm_run(layer, compute, tuning, m, a, a_scale, packed, bias, c, scratch,
-                   kNoAllocScratchBytes, stream);
+  return qgemm_check_status(scratch, stream);
 }

@@ -454,7 +454,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
                               const qgemm_compute_config* C, bool grouped, const int32_t* offsets,
                               int64_t rows, const void* a, const float* a_scale, const void* w,
                               const void* bias, void* c, void* workspace, size_t ws_bytes,
-                              cudaStream_t stream) {
+                              size_t clear_bytes, cudaStream_t stream) {
   if (rows < 0) return fail(QGEMM_ERR_INVALID_ARG, "row count is negative");
   if (rows > (1 << 30)) return fail(QGEMM_ERR_UNSUPPORTED, "row count above 2^30");
   if (rows == 0) return ok();
@@ -499,6 +499,10 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
     q.z_off = P.off_z;
     q.sg_shift = L->group_size == 32 ? 0 : L->group_size == 64 ? 1 : 2;
     q.has_zp = has_zp ? 1 : 0;
+    if (clear_bytes) {
+      cudaError_t ce = cudaMemsetAsync(workspace, 0, clear_bytes, stream);
+      if (ce != cudaSuccess) return cuda_fail(ce, "workspace clear");
+    }
     cudaError_t e = launch_w4a16_mma(q, fp16, stream);
     if (e != cudaSuccess) return cuda_fail(e, "small-M GEMM launch");
     return ok();
@@ -612,9 +616,27 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   else if (is_nv(L)) fmt = fp16 ? 4 : 3;
   else if (is_f16s(L)) fmt = 5;
   else if (is_w8(L)) fmt = fp16 ? 7 : 6;
+  if (clear_bytes) {
+    cudaError_t ce = cudaMemsetAsync(workspace, 0, clear_bytes, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "workspace clear");
+  }
   cudaError_t e = launch_w4a16(tmap, tmap_c, p, P.bt, fmt, grouped, P.grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "W4A16 GEMM launch");
   return ok();
+}
+
+int run_dense_clearing(const void* layer, const void* compute, const void* tuning, int64_t m,
+                       const void* a, const float* a_scale, const void* packed, const void* bias,
+                       void* c, void* workspace, size_t ws_bytes, size_t clear_bytes,
+                       cudaStream_t stream) {
+  const qgemm_layer_config* L = static_cast<const qgemm_layer_config*>(layer);
+  const qgemm_compute_config* C = static_cast<const qgemm_compute_config*>(compute);
+  qgemm_status st = check_layer(L);
+  if (st != QGEMM_OK) return st;
+  st = check_compute(C, L, false);
+  if (st != QGEMM_OK) return st;
+  return run_w4a16(L, static_cast<const qgemm_tuning_config*>(tuning), C, false, nullptr, m, a,
+                   a_scale, packed, bias, c, workspace, ws_bytes, clear_bytes, stream);
 }
 
 int set_last_error(int status, const char* message) {
@@ -733,7 +755,7 @@ qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_conf
   if (st != QGEMM_OK) return st;
   return run_w4a16(layer, tuning, compute, false, nullptr, m, a, a_scale,
                    packed, bias, c, workspace,
-                   workspace_bytes, static_cast<cudaStream_t>(stream));
+                   workspace_bytes, 0, static_cast<cudaStream_t>(stream));
 }
 
 qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
@@ -748,14 +770,19 @@ qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
   if (st != QGEMM_OK) return st;
   return run_w4a16(layer, tuning, compute, true, expert_offsets,
                    total_rows, a, a_scale, packed, bias, c,
-                   workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+                   workspace, workspace_bytes, 0, static_cast<cudaStream_t>(stream));
 }
 
 qgemm_status qgemm_quantize_act_fp8(const void* x, int64_t m, int64_t k, void* a8,
                                     float* a_scale, void* stream) {
   if (m < 0 || k <= 0) return fail(QGEMM_ERR_INVALID_ARG, "bad shape");
+  if (k % 8) return fail(QGEMM_ERR_UNSUPPORTED, "k must be a multiple of 8");
+  if (m > (1 << 30) || k > (1 << 30)) return fail(QGEMM_ERR_UNSUPPORTED, "m or k above 2^30");
   if (m == 0) return ok();
   if (!x || !a8 || !a_scale) return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(a8) & 7u) ||
+      (reinterpret_cast<uintptr_t>(a_scale) & 3u))
+    return fail(QGEMM_ERR_INVALID_ARG, "x must be 16-byte, a8 8-byte, a_scale 4-byte aligned");
   cudaError_t e = launch_act_quant_fp8(static_cast<const uint16_t*>(x), m, k,
                                        static_cast<uint8_t*>(a8), a_scale,
                                        static_cast<cudaStream_t>(stream));

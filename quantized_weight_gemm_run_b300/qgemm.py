@@ -88,6 +88,7 @@ _SIGS = {
     "qgemm_moe_combine": [_P, _P, _P, _I64, _I32, _I64, _P, _P],
     "qgemm_debug_dequant": [_L, _P, _P, _P],
     "qgemm_check_status": [_P, _P],
+    "qgemm_noalloc_check_status": [_P],
     "qgemm_describe_plan": [_L, _C, _I64, ctypes.c_char_p, _SZ],
 }
 for _name, _args in _SIGS.items():
@@ -223,6 +224,10 @@ def qgemm_debug_dequant(layer, packed, out_kn, stream=None):
 
 def qgemm_check_status(workspace, stream=None):
     return lib.qgemm_check_status(_ptr(workspace), _stream(stream))
+
+
+def qgemm_noalloc_check_status(stream=None):
+    return lib.qgemm_noalloc_check_status(_stream(stream))
 
 
 def qgemm_set_wait_limit_ns(ns: int) -> None:

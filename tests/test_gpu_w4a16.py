@@ -128,18 +128,17 @@ def test_full_size_w4a16_asym_sweep(Q, n, k):
         assert_close(to_np(out), ref[:m], what=f"M={m} N={n} K={k}")
 
 
-def test_full_size_large_sampled_rows(Q):
+def test_full_size_large_every_row(Q):
+    """8192^3 INT4 bf16, every one of the 67M outputs against the oracle
+    (about 1.1 TFLOP of float64 on the host)."""
     s = synth.LARGE_SHAPE
     c = Case(s["m"], s["n"], s["k"], s["group"], "bf16", True, seed=synth.SEED_LARGE)
     lin = linear(c)
     out = lin(c.dev_act())
     assert lin.status() == Q.QGEMM_OK
-    g = np.random.default_rng(1)
-    rows = np.sort(g.choice(s["m"], 384, replace=False))
-    got = to_np(out[torch.from_numpy(rows).to(DEV)])
-    assert_close(got, c.reference(rows), what="8192^3 sampled rows")
-    # every element: finite, and the full output's statistics match a rows sample
-    assert torch.isfinite(out.float()).all()
+    got = to_np(out)
+    del out
+    assert_close(got, c.reference(), what="8192^3 every row")
 
 
 def test_timeout_path_reports_and_recovers(Q):

@@ -45,6 +45,56 @@ def test_noalloc_matches_workspace_entry_point(Q, m, n, k, g, adt, sym):
         assert_close(to_np(out), c.reference(), what="noalloc vs oracle")
 
 
+def test_noalloc_second_plan_finds_its_scratch_clear(Q):
+    """A split-K plan with a large scratch (the small-M kernel on 16x4096x4096:
+    a count and a 16 x 128 accumulator per n-tile), then a different plan
+    (the persistent kernel on a ragged 37-row problem), then the first again:
+    each call must clear whatever the previous, different plan left."""
+    cases = [Case(16, 4096, 4096, 128, "fp16", True, seed=5),
+             Case(37, 384, 1024, 64, "bf16", False, seed=6)]
+    lins = [linear(c) for c in cases]
+    xs = [c.dev_act() for c in cases]
+    refs = [lin(x) for lin, x in zip(lins, xs)]
+    for lin in lins:
+        assert lin.status() == Q.QGEMM_OK
+    for i in (0, 1, 0, 1):
+        c, lin, x = cases[i], lins[i], xs[i]
+        out = torch.full_like(refs[i], float("nan"))
+        st = Q.qgemm_run_noalloc(lin.layer, lin.dense, None, c.m, x, None, lin.packed, None, out)
+        assert st == Q.QGEMM_OK, Q.last_error()
+        assert Q.qgemm_noalloc_check_status() == Q.QGEMM_OK
+        assert_close(to_np(out), to_np(refs[i]), what=f"noalloc plan {i} vs qgemm_run")
+
+
+def test_noalloc_reports_a_timeout_and_recovers(Q):
+    """A wait limit of 0 makes the persistent kernel's first unready wait give
+    up (it records the status, drains its copies and exits: no fault, no
+    hang).  A call rejected by an argument check in between must queue
+    nothing, so the status word it would otherwise have cleared still says
+    timeout; the status call reports it, and the next call runs clean."""
+    c = Case(40, 256, 1024, 128, "bf16", True, seed=3)
+    lin = linear(c)
+    x = c.dev_act()
+    ref = lin(x)
+    assert lin.status() == Q.QGEMM_OK
+    out = torch.empty_like(ref)
+    Q.qgemm_set_wait_limit_ns(0)
+    try:
+        st = Q.qgemm_run_noalloc(lin.layer, lin.dense, None, c.m, x, None, lin.packed, None, out)
+        assert st == Q.QGEMM_OK, Q.last_error()
+        torch.cuda.synchronize()
+    finally:
+        Q.qgemm_set_wait_limit_ns(1_000_000_000)
+    st = Q.qgemm_run_noalloc(lin.layer, lin.dense, None, c.m, x.data_ptr() + 2, None,
+                             lin.packed, None, out)            # misaligned: rejected
+    assert st == Q.QGEMM_ERR_INVALID_ARG
+    assert Q.qgemm_noalloc_check_status() == Q.QGEMM_ERR_TIMEOUT
+    st = Q.qgemm_run_noalloc(lin.layer, lin.dense, None, c.m, x, None, lin.packed, None, out)
+    assert st == Q.QGEMM_OK, Q.last_error()
+    assert Q.qgemm_noalloc_check_status() == Q.QGEMM_OK
+    assert_close(to_np(out), to_np(ref), what="noalloc after a timeout")
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch(Q):
     # 2^20 rows x 16384 columns needs more split-K counters than 32 MiB holds
     layer = Q.layer_config(16384, 4096, 128, Q.QGEMM_W_INT4_SYM, Q.QGEMM_S_BF16, Q.QGEMM_Z_NONE,
