@@ -92,21 +92,30 @@ struct W4A16Params {
   unsigned long long wait_limit_ns;
 };
 
-// The small-M kernel (mma.sync, M <= 16, INT4 / UINT4): n-tiles x splits
-// CTAs, each a K slice of one n-tile; fp32 partials meet in acc[nt] (16 x 128
-// per n-tile) with a per-n-tile count, both left at zero.
+// The small-M kernel (mma.sync, M <= 16, INT4 / UINT4): one cluster of
+// `splits` CTAs per n-tile, each CTA a contiguous K slice of at most nk_max
+// k-tiles streamed through a ring of `ring` weight slots; the slices' fp32
+// partials are summed through distributed shared memory.  The workspace holds
+// only the status word.
 struct W4A16MmaParams {
   const uint8_t* w;          // packed blocks (one expert)
   const uint16_t* a;         // activations [m, k]
   uint16_t* c;               // output [m, n]
   const uint16_t* bias;      // [n] or null
-  float* acc;                // [nt][128][16] fp32, zero
-  int* counters;             // [nt], zero
-  int m, n, k, kt, nt, splits;
-  int block_bytes, w_slot_bytes, s_off, z_off, sg_shift, has_zp;
+  int* status;               // workspace status word (bounded waits report here)
+  int m, n, k, kt, nt;
+  int splits;                // K slices per n-tile = CTAs per cluster (1, 2, 4, 8, 16)
+  int ring;                  // weight slots per CTA
+  int nk_max;                // most k-tiles in one slice
+  int block_bytes, s_off, z_off, sg_shift, has_zp;
+  unsigned long long wait_limit_ns;
 };
-cudaError_t launch_w4a16_mma(const W4A16MmaParams& p, bool fp16, cudaStream_t stream);
-int mma_smem_bytes(int block_bytes);
+// tmap_a: activations as {64 k, m rows, K / 64 chunks}, 128-byte swizzle,
+// box {64, 8 or 16 rows, 2 nk_max chunks}
+cudaError_t launch_w4a16_mma(const CUtensorMap& tmap_a, const W4A16MmaParams& p, bool fp16,
+                             cudaStream_t stream);
+// dynamic shared memory of one small-M CTA (rows: 8 for M <= 8, else 16)
+int mma_smem_bytes(int block_bytes, int ring, int nk_max, int rows);
 
 // Host-side plan for one W4A16 launch.
 int device_sm_count();

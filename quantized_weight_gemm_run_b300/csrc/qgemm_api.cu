@@ -264,7 +264,9 @@ static bool make_geometry(int bt, int st, int has_zp, bool mx, bool w8, int expe
 
 struct Plan {
   int kernel;        // 1: the persistent tcgen05 kernel, 2: the small-M mma.sync kernel
-  int mma_splits;    // small-M kernel: K slices per n-tile
+  int mma_splits;    // small-M kernel: K slices per n-tile (CTAs per cluster)
+  int mma_ring;      // small-M kernel: weight slots per CTA
+  int mma_nk_max;    // small-M kernel: most k-tiles in one slice
   int bt, grid, st, off_s, off_z;
   int split_cap;     // most CTAs sharing one tile's K range (0: no cap, 1: whole tiles)
   Geometry g;
@@ -295,39 +297,57 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   const int has_zp = has_zeros(L);
   if (T && (T->kernel < 0 || T->kernel > 2))
     return fail(QGEMM_ERR_INVALID_ARG, "kernel must be 0, 1 or 2");
+  const int64_t ntl = L->n / kTileN, ktl = L->k / kTileK;
+  // small-M kernel: K slices per n-tile (a power of two, at most 16 and at
+  // most the k-tiles), and weight slots per CTA
+  int64_t S = 0;
+  if (T && T->kernel == 2 && T->split_k > 0) {
+    S = T->split_k;
+  } else {
+    // Heuristic, measured on B300 over the sweep's shapes at M = 1 and 16
+    // (slices x weight slots: 4096^2 8 x 4: 6.4 / 6.9 us; 11008 x 4096
+    // 8 x 2 at M <= 8, 9.8 us, else 4 x 4, 12.0 us; 4096 x 11008 8 x 8 at
+    // M <= 8, 11.6 us, else 8 x 4, 13.2 us): eight slices per n-tile, four
+    // when there are more n-tiles than SMs half-way and two n8 token blocks
+    S = (rows > 8 && 2 * ntl > sms) ? 4 : 8;
+    while (S > ktl) S /= 2;
+  }
+  const bool s_ok = S >= 1 && S <= 16 && (S & (S - 1)) == 0 && S <= ktl;
+  const int64_t nk_max = s_ok ? (ktl + S - 1) / S : 0;
+  const int64_t ctas_per_sm = s_ok ? (ntl * S + sms - 1) / sms : 1;
+  int ring = 4;
+  if (T && T->kernel == 2 && T->stages) ring = T->stages;
+  else if (rows <= 8 && ctas_per_sm > 2) ring = 2;      // many CTAs: small ones
+  else if (rows <= 8 && nk_max > 4 && ctas_per_sm <= 2) ring = 8;   // long slices
+  if (ring > nk_max) ring = (int)nk_max;
+  if (ring < 1) ring = 1;
+  const int mma_smem =
+      s_ok ? mma_smem_bytes(packed_block_bytes(false, st, has_zp), ring, (int)nk_max,
+                            rows <= 8 ? 8 : 16)
+           : 0;
+  const bool mma_fits = s_ok && nk_max <= 64 && mma_smem <= device_max_smem();
   const bool mma_ok = !grouped && !is_mx(L) && !is_nv(L) && !is_f16s(L) && !is_w8(L) &&
-                      L->gated_act == 0 && rows <= 16 &&
-                      !(C && (C->deterministic || C->batch_invariant));
+                      L->gated_act == 0 && rows <= 16 && !(C && C->batch_invariant) &&
+                      mma_fits;
   const int want = T ? T->kernel : 0;
   if (want == 2 && !mma_ok)
     return fail(QGEMM_ERR_UNSUPPORTED,
                 "the small-M kernel takes dense INT4/UINT4 GEMMs with m <= 16 whose scales are "
-                "in the activation dtype and that are not gated, deterministic or "
-                "batch-invariant");
+                "in the activation dtype, that are not gated or batch-invariant, with split_k a "
+                "power of two <= 16 and <= k/128 and a slice that fits shared memory");
   P->kernel = 1;
   P->mma_splits = 0;
-  const int64_t ntl = L->n / kTileN, ktl = L->k / kTileK;
   // Heuristic: with no tuning field for the tcgen05 kernel set, the small-M
-  // kernel takes the GEMMs it can run in one wave of CTAs.  Measured on B300
-  // at M = 1..16 it beats the persistent kernel on every shape of the sweep
-  // (4096^2: 8.0-8.1 -> 7.2-7.7 us; 4096 x 11008: 12.5 -> 11.65 us; 11008 x
-  // 4096: 12.5 -> 12.3 us): no tensor-memory set-up and no split-tile finish
-  // at the end.
+  // kernel takes every GEMM it can run (no tensor-memory set-up, no
+  // split-tile finish through L2).
   const bool k1_tuned = T && (T->block_tok || T->stages || T->max_ctas || T->split_k);
-  const bool use_mma = want == 2 || (want == 0 && mma_ok && !k1_tuned && ntl <= 5LL * sms);
+  const bool use_mma = want == 2 || (want == 0 && mma_ok && !k1_tuned);
   if (use_mma) {
-    // K slices per n-tile: as many as fill five 128-thread CTAs per SM in
-    // one wave (measured best on every sweep shape; a partial second wave
-    // costs 20-30 %)
-    int64_t S = (5LL * sms) / ntl;
-    if (want == 2 && T->split_k > 0) S = T->split_k;   // explicit slice count
-    if (S > ktl) S = ktl;
-    if (S < 1) S = 1;
     if (ntl * S >= (int64_t(1) << 31)) return fail(QGEMM_ERR_UNSUPPORTED, "grid too large");
-    if (mma_smem_bytes(packed_block_bytes(false, st, has_zp)) > device_max_smem())
-      return fail(QGEMM_ERR_UNSUPPORTED, "tile does not fit shared memory");
     P->kernel = 2;
     P->mma_splits = (int)S;
+    P->mma_ring = ring;
+    P->mma_nk_max = (int)nk_max;
     P->bt = 16;
     P->grid = (int)(ntl * S);
     P->split_cap = 0;
@@ -335,13 +355,13 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
     P->off_s = kTileBytes;
     P->off_z = kTileBytes + packed_scale_bytes(false, st);
     P->max_tiles = ntl;
-    // status word, a count per n-tile, a 16 x 128 fp32 accumulator per n-tile
+    // the status word only: the slices meet in distributed shared memory
     WorkspaceLayout w;
     w.counters_off = 256;
-    w.counters_bytes = ((size_t)ntl * sizeof(int) + 255) & ~size_t(255);
-    w.partials_off = w.counters_off + w.counters_bytes;
-    w.partials_bytes = (size_t)ntl * 16 * kTileN * sizeof(float);
-    w.total = w.partials_off + w.partials_bytes;
+    w.counters_bytes = 0;
+    w.partials_off = 256;
+    w.partials_bytes = 0;
+    w.total = 256;
     P->ws = w;
     return ok();
   }
@@ -485,16 +505,17 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
     q.a = static_cast<const uint16_t*>(a);
     q.c = static_cast<uint16_t*>(c);
     q.bias = static_cast<const uint16_t*>(bias);
-    q.acc = reinterpret_cast<float*>(wsb + P.ws.partials_off);
-    q.counters = reinterpret_cast<int*>(wsb + P.ws.counters_off);
+    q.status = reinterpret_cast<int*>(wsb);
     q.m = (int)rows;
     q.n = (int)L->n;
     q.k = (int)L->k;
     q.kt = (int)(L->k / kTileK);
     q.nt = (int)(L->n / kTileN);
     q.splits = P.mma_splits;
+    q.ring = P.mma_ring;
+    q.nk_max = P.mma_nk_max;
+    q.wait_limit_ns = g_wait_limit_ns;
     q.block_bytes = packed_block_bytes(false, P.st, has_zp);
-    q.w_slot_bytes = (q.block_bytes + 15) & ~15;
     q.s_off = P.off_s;
     q.z_off = P.off_z;
     q.sg_shift = L->group_size == 32 ? 0 : L->group_size == 64 ? 1 : 2;
@@ -503,7 +524,17 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
       cudaError_t ce = cudaMemsetAsync(workspace, 0, clear_bytes, stream);
       if (ce != cudaSuccess) return cuda_fail(ce, "workspace clear");
     }
-    cudaError_t e = launch_w4a16_mma(q, fp16, stream);
+    // activations {64 k, rows, K / 64 chunks}: one box holds a slice's k-tiles
+    CUtensorMap tmap_mma;
+    const uint64_t rb = (uint64_t)L->k * 2;
+    const uint64_t dims3[3] = {64, (uint64_t)rows, rb / 128};
+    const uint64_t str3[2] = {rb, 128};
+    const uint32_t box3[3] = {64, (uint32_t)(rows <= 8 ? 8 : 16), (uint32_t)(2 * P.mma_nk_max)};
+    if (!encode_tmap_3d(&tmap_mma,
+                        fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        a, dims3, str3, box3, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the activation tensor");
+    cudaError_t e = launch_w4a16_mma(tmap_mma, q, fp16, stream);
     if (e != cudaSuccess) return cuda_fail(e, "small-M GEMM launch");
     return ok();
   }

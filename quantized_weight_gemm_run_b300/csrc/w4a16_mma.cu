@@ -8,24 +8,39 @@
 // INT4 / UINT4 formats, on the same packed weight buffer as the tcgen05
 // kernel.
 //
-// Shape.  Swap-AB again: D[n, m] = W^[n, :] . A[m, :], the 128 features of
-// an n-tile as MMA rows (8 m16 blocks, two per warp) and the <= 16 tokens as
-// two n8 blocks.  Dequantized weights go straight from registers into the A
-// fragments: in the packed layout, lane t of a quad finds its (k, k+1) pairs
-// at nibble positions t and t+4 of every 32-bit word, so a quad's four lanes
-// read the same 16-byte vector (one broadcast) and each extracts its own pairs
-// with one LOP3 against a magic exponent.  Activations come through ldmatrix
-// from a padded shared-memory tile (conflict-free rows).
+// Shape.  Swap-AB: D[n, m] = W^[n, :] . A[m, :], the 128 features of an
+// n-tile as MMA rows (8 m16 blocks, two per warp) and the tokens as one n8
+// block (M <= 8) or two.  Dequantized weights go straight from registers into
+// the A fragments: in the packed layout, lane t of a quad finds its (k, k+1)
+// pairs at nibble positions t and t+4 of every 32-bit word, so a quad's four
+// lanes read the same 16-byte vector (one broadcast) and each extracts its
+// own pairs with one LOP3 against a magic exponent.  Activations come through
+// ldmatrix from a padded shared-memory tile (conflict-free rows).
 //
-// Work split.  Grid = n-tiles x S K-slices, about five CTAs of 128 threads
-// per SM; a CTA issues cp.async copies for its slice's k-tiles through a ring
-// of kStages slots (the whole slice up front when it fits), weights before
-// the wait on the previous grid, activations after it.  Partials: the CTA's
-// m x 128 fp32 result rows are staged in shared memory and added into the
-// n-tile's accumulator in L2 with one bulk reduction; the CTA then counts in
-// with an acquire-release add, and the last of the S arrivals adds the bias,
-// rounds, writes the output rows and re-zeroes the accumulator and counter.
-// Nothing waits on another CTA, so no wait needs a time limit.
+// Work split.  One thread-block cluster of S CTAs per n-tile; CTA r of the
+// cluster takes the r-th of S contiguous K slices.  Data movement is the TMA
+// engine completing on mbarriers: the CTA's first weight blocks go out at
+// entry as bulk copies, before the wait on the previous grid (packed weights
+// are read-only layer data), together with an L2 prefetch of its activation
+// rows; after the wait one 3-D tensor copy lands the slice's activations
+// (rows past M and k past K read as zeros) in the 128-byte-swizzled layout
+// that ldmatrix reads without bank conflicts.  When the ring is shorter than
+// the slice, each warp releases a slot on an mbarrier and warp s % 4 refills
+// slot s once all four have.  Each warp keeps two accumulator sets (even and
+// odd k16 steps) so that its MMA chains are half as long.
+//
+// Reduction.  Each CTA pushes feature slice r of its [tokens][128] fp32
+// partial into cluster peer r's receive buffer (st.async, counted on the
+// peer's mbarrier, armed before a cluster barrier at entry); CTA r sums the S
+// slices it receives in cluster-rank order (fixed order: the bits repeat run
+// to run and do not depend on M), adds the bias, rounds and stores.  No
+// workspace accumulators, no global atomics, no barrier at the end.
+//
+// Waits.  Every mbarrier wait is bounded (the process-wide wait limit); a CTA
+// that gives up records a timeout in the workspace status word, skips the
+// rest of its work but still sends its (meaningless) slices so that every
+// peer completes, and waits (with a fixed bound) for its own copies and
+// incoming slices to land before it exits.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -37,147 +52,233 @@ namespace qg {
 
 namespace {
 
-constexpr int kMmaThreads = 128;
-constexpr int kStages = 3;
-constexpr int kARowBytes = 272;                 // 128 k x 2 B, padded by 16 B
-constexpr int kATileBytes = 16 * kARowBytes;    // 16 tokens
+// four warps: warp w takes rows 32 w .. 32 w + 31 of the n-tile
+constexpr int kMmaWarps = 4;
+constexpr int kMmaThreads = 32 * kMmaWarps;
+constexpr unsigned long long kDrainLimitNs = 100000000ull;
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// Not volatile: the compiler may interleave these with the independent
+// dequant chains (a warp issues in order, so the schedule is what hides the
+// latencies); the memory clobber keeps them after the barrier waits that
+// publish the activation tile.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(addr)
+      : "memory");
 }
 
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
+__device__ __forceinline__ void ldmatrix_x2(uint32_t (&r)[2], uint32_t addr) {
+  asm("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+      : "=r"(r[0]), "=r"(r[1])
+      : "r"(addr)
+      : "memory");
 }
 
 template <bool FP16>
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
+  // register-only: free for the compiler to schedule
   if constexpr (FP16) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
         "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
         "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
 }
 
-// (magic + q) pair -> ((magic + q) - (magic + z)) * s, one rounding
+// The dequant of a (k, k+1) pair, in three stages:
+// nibbles at bits 0-3 and 16-19 -> (magic + q) pair (exact), minus the
+// (magic + z) pair (exact: q - z), times the scale pair (the one rounding).
 template <bool FP16>
-__device__ __forceinline__ uint32_t dq2(uint32_t word_shifted, uint32_t zero2, uint32_t scale2) {
+__device__ __forceinline__ uint32_t nib_pairs(uint32_t word_shifted) {
   constexpr uint32_t magic = FP16 ? 0x64006400u : 0x43004300u;
   uint32_t x;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;"
       : "=r"(x)
       : "r"(word_shifted), "r"(0x000F000Fu), "r"(magic));
+  return x;
+}
+
+template <bool FP16>
+__device__ __forceinline__ uint32_t sub2(uint32_t x, uint32_t zero2) {
   if constexpr (FP16) {
-    __half2 r = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&x),
-                                *reinterpret_cast<__half2*>(&zero2)),
-                        *reinterpret_cast<__half2*>(&scale2));
+    __half2 r = __hsub2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<__half2*>(&zero2));
     return *reinterpret_cast<uint32_t*>(&r);
   } else {
-    __nv_bfloat162 r = __hmul2(__hsub2(*reinterpret_cast<__nv_bfloat162*>(&x),
-                                       *reinterpret_cast<__nv_bfloat162*>(&zero2)),
+    __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&x),
+                               *reinterpret_cast<__nv_bfloat162*>(&zero2));
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
+}
+
+template <bool FP16>
+__device__ __forceinline__ uint32_t mul2(uint32_t x, uint32_t scale2) {
+  if constexpr (FP16) {
+    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<__half2*>(&scale2));
+    return *reinterpret_cast<uint32_t*>(&r);
+  } else {
+    __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&x),
                                *reinterpret_cast<__nv_bfloat162*>(&scale2));
     return *reinterpret_cast<uint32_t*>(&r);
   }
 }
 
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// L2 prefetch of a global range (16-byte aligned start, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Store 16 bytes into a cluster peer's shared memory, completing 16 bytes of
+// transaction count on the peer's mbarrier (both addresses from mapa).
+__device__ __forceinline__ void st_async_f4(uint32_t dst, const float4& v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(dst),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+
 }  // namespace
 
-// ONE_GROUP: the group size is >= 128, so one scale (and zero) per row
-// serves the whole k-tile.
-template <bool FP16, bool ONE_GROUP>
-__global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(const W4A16MmaParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+// Shared-memory geometry of one CTA: the activation tile (one TMA box:
+// 2 nk_max chunks of 64 k x rows x 128 bytes, 128-byte swizzled, at offset 0
+// for the swizzle's 1 KB alignment), the weight ring, the receive buffer of
+// the reduction ([S][rows][128 / S] fp32), then barriers and counters.
+__host__ __device__ inline int mma_act_bytes(int nk_max, int rows) { return nk_max * rows * 256; }
+
+int mma_smem_bytes(int block_bytes, int ring, int nk_max, int rows) {
+  return 1024 /* alignment slack */ + mma_act_bytes(nk_max, rows) + ring * block_bytes +
+         rows * kTileN * 4 + 8 * (2 * ring + 2) + 16;
+}
+
+// NB: n8 token blocks (1: M <= 8, 2: M <= 16).  ONE_GROUP: the group size is
+// >= 128, so one scale (and zero) per row serves the whole k-tile.
+template <bool FP16, int NB, bool ONE_GROUP>
+__global__ void __launch_bounds__(kMmaThreads, 4)
+    w4a16_mma_kernel(const __grid_constant__ CUtensorMap tmap_a, const W4A16MmaParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled activation box needs a 1 KB aligned start
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  constexpr int ROWS = 8 * NB;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rg = warp;   // row group
   const int g = lane >> 2, t = lane & 3;
-  const int nt = blockIdx.x / p.splits, sl = blockIdx.x - nt * p.splits;
-  const int kt0 = (int)((long long)sl * p.kt / p.splits);
-  const int kt1 = (int)((long long)(sl + 1) * p.kt / p.splits);
+  const int S = p.splits;
+  const int sl = blockIdx.x % S;   // rank in the cluster (clusters are S x 1 x 1)
+  const int nt = blockIdx.x / S;
+  const int kt0 = sl * p.kt / S, kt1 = (sl + 1) * p.kt / S;
   const int nk = kt1 - kt0;
-  const int slot_bytes = p.w_slot_bytes + kATileBytes;
-  const uint8_t* wsrc = p.w + ((long long)nt * p.kt + kt0) * p.block_bytes;
+  const int R = p.ring;
+  const int BB = p.block_bytes;
+  const int F = kTileN / S;        // features this CTA finishes
+  uint8_t* act = smem;
+  uint8_t* ring = smem + mma_act_bytes(p.nk_max, ROWS);
+  float* recv = reinterpret_cast<float*>(ring + R * BB);          // [S][ROWS][F]
+  uint64_t* full = reinterpret_cast<uint64_t*>(recv + ROWS * kTileN);
+  uint64_t* empty = full + R;          // one arrival per warp when it is done with a slot
+  uint64_t* act_full = empty + R;
+  uint64_t* recv_full = act_full + 1;
+  int* issued = reinterpret_cast<int*>(recv_full + 1);   // weight blocks issued so far
+  volatile int* abort_flag = issued + 1;
+  const uint8_t* wsrc = p.w + ((long long)nt * p.kt + kt0) * BB;
+  const int live = p.m < ROWS ? p.m : ROWS;
+  const uint16_t* asrc = p.a + (long long)kt0 * kTileK;   // row r at asrc + r * k
 
-  // stage s (k-tile kt0 + s): weight block into slot s % kStages, then its
-  // activation tile (16 rows, zero-filled past m)
-  auto issue_w = [&](int s) {
-    if (s < nk) {
-      uint8_t* dst = smem + (s % kStages) * slot_bytes;
-      const uint8_t* src = wsrc + (long long)s * p.block_bytes;
-      for (int c = tid; c < p.block_bytes / 16; c += kMmaThreads)
-        cp_async16(dst + c * 16, src + c * 16, 16);
+  if (tid == 0) {
+    for (int s = 0; s < R; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kMmaWarps);
     }
-  };
-  auto issue_a = [&](int s) {
-    if (s < nk) {
-      uint8_t* dst = smem + (s % kStages) * slot_bytes + p.w_slot_bytes;
-      const int kbase = (kt0 + s) * kTileK;
-      for (int c = tid; c < 16 * 16; c += kMmaThreads) {   // 16 rows x 16 chunks of 16 B
-        const int r = c >> 4, ch = c & 15;
-        const bool live = r < p.m;
-        const uint16_t* src = p.a + (long long)(live ? r : 0) * p.k + kbase + ch * 8;
-        cp_async16(dst + r * kARowBytes + ch * 16, src, live ? 16 : 0);
-      }
+    mbar_init(act_full, 1);
+    mbar_init(recv_full, 1);
+    fence_barrier_init();
+    // the first weight blocks: issued before anything waits on the previous grid
+    const int first = nk < R ? nk : R;
+    const uint64_t pol = policy_evict_first();
+    for (int s = 0; s < first; ++s) {
+      mbar_arrive_expect_tx(&full[s], BB);
+      bulk_load(ring + s * BB, wsrc + (long long)s * BB, BB, &full[s], pol);
     }
-  };
-
-  // weights are read-only layer data: stream them before the wait
-#pragma unroll 1
-  for (int s = 0; s < kStages - 1; ++s) issue_w(s);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+    *issued = first;
+    *abort_flag = 0;
+    // the slices of the cluster's other CTAs (and this one's own) land here
+    mbar_arrive_expect_tx(recv_full, (uint32_t)(S * live * F * 4));
+    prefetch_tmap(&tmap_a);
+  }
+  // the activation rows: an L2 prefetch now (the previous grid may still be
+  // writing them; L2 is where its writes land, so a prefetched line is never
+  // stale), the copy into shared memory after the wait
+  if (warp == 1 && lane < live)
+    prefetch_l2_bulk(asrc + (long long)lane * p.k, (uint32_t)nk * 256);
+  __syncthreads();
+  cluster_sync_all();   // every receive barrier of the cluster is armed
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-#pragma unroll 1
-  for (int s = 0; s < kStages - 1; ++s) {
-    issue_a(s);
-    cp_async_commit();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0) {
+    // one box: 2 nk_max chunks of 64 k x ROWS rows (rows past m and k past K
+    // read as zeros)
+    mbar_arrive_expect_tx(act_full, (uint32_t)mma_act_bytes(p.nk_max, ROWS));
+    tma_load_3d_hint(act, &tmap_a, act_full, 0, 0, 2 * kt0, policy_evict_first());
   }
 
-  float acc[2][2][4];
+  float acc[2][2][NB][4];   // [k16 step parity][m16 block][n8 block]
 #pragma unroll
-  for (int b = 0; b < 2; ++b)
+  for (int h = 0; h < 2; ++h)
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
+    for (int b = 0; b < 2; ++b)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[b][c][i] = 0.f;
+      for (int c = 0; c < NB; ++c)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[h][b][c][i] = 0.f;
 
   constexpr uint32_t magic16 = FP16 ? 0x6400u : 0x4300u;
+  // ldmatrix rows: lane l reads token (l & 7) + 8 (l >> 4) at k offset
+  // 8 ((l >> 3) & 1); in the swizzled box, 16-byte unit u of row r of a chunk
+  // sits at unit u ^ (r & 7)
+  const int a_tok = (lane & 7) + 8 * (NB == 2 ? (lane >> 4) : 0);
+  const uint32_t a_row = smem_u32(act) + (uint32_t)(a_tok * 128);
+  const int a_x = a_tok & 7, a_k8 = (lane >> 3) & 1;
+  bool ok = mbar_wait(act_full, 0, abort_flag, p.status, p.wait_limit_ns, kStatusTimeout);
+  int slot = 0;
+  uint32_t phase = 0;
 #pragma unroll 1
-  for (int s = 0; s < nk; ++s) {
-    issue_w(s + kStages - 1);
-    issue_a(s + kStages - 1);
-    cp_async_commit();
-    cp_async_wait<kStages - 1>();   // stage s has landed
-    __syncthreads();
-    const uint8_t* slot = smem + (s % kStages) * slot_bytes;
-    const uint4* wv = reinterpret_cast<const uint4*>(slot);
-    const uint16_t* sv = reinterpret_cast<const uint16_t*>(slot + p.s_off);
-    const uint8_t* zv = slot + p.z_off;
-    const uint8_t* at = slot + p.w_slot_bytes;
+  for (int s = 0; s < nk && ok; ++s) {
+    if (!mbar_wait(&full[slot], phase, abort_flag, p.status, p.wait_limit_ns, kStatusTimeout)) {
+      ok = false;
+      break;
+    }
+    const uint8_t* blk = ring + slot * BB;
+    const uint4* wv = reinterpret_cast<const uint4*>(blk);
+    const uint16_t* sv = reinterpret_cast<const uint16_t*>(blk + p.s_off);
+    const uint8_t* zv = blk + p.z_off;
     // per-row scale and zero pairs of rows (b, g) and (b, g + 8), group sg
     auto row_consts = [&](int sg, uint32_t (&sc)[2][2], uint32_t (&zc)[2][2]) {
 #pragma unroll
       for (int b = 0; b < 2; ++b)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int r = warp * 32 + b * 16 + g + 8 * e;
+          const int r = rg * 32 + b * 16 + g + 8 * e;
           sc[b][e] = (uint32_t)sv[sg * kTileN + r] * 0x00010001u;
           zc[b][e] = (magic16 + (p.has_zp ? (uint32_t)zv[sg * kTileN + r] : 8u)) * 0x00010001u;
         }
@@ -185,141 +286,215 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(const W4A16MmaPa
     uint32_t sc[2][2], zc[2][2];
     if constexpr (ONE_GROUP) row_consts(0, sc, zc);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {   // 32-k chunk
-      // B fragments of the chunk's two k16 steps, tokens 0-7 and 8-15
+    for (int j = 0; j < 4; ++j) {   // 32-k chunk of the k-tile
+      // B fragments of the chunk's two k16 steps: 64-k box chunk 2 s + j / 2,
+      // 16-byte units 4 (j & 1) + 2 h + a_k8
+      const uint32_t chunk = a_row + (uint32_t)((2 * s + (j >> 1)) * (ROWS * 128));
       uint32_t bf[2][4];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int mi = lane >> 3;   // matrix: (tokens 8 (mi >> 1) .., k + 8 (mi & 1))
-        const int tok = (mi >> 1) * 8 + (lane & 7);
-        ldmatrix_x4(bf[h], at + tok * kARowBytes + (j * 32 + h * 16 + (mi & 1) * 8) * 2);
-      }
-      if constexpr (!ONE_GROUP) row_consts(j >> p.sg_shift, sc, zc);
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {   // m16 block: rows 32 warp + 16 b + {g, g + 8}
-        const uint4 v0 = wv[(warp * 4 + j) * 32 + b * 16 + g];
-        const uint4 v1 = wv[(warp * 4 + j) * 32 + b * 16 + g + 8];
-        const uint32_t s0 = sc[b][0], s1 = sc[b][1], z0 = zc[b][0], z1 = zc[b][1];
-        const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
-        const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {   // k16 step: words 2h (k 0-7) and 2h+1 (k 8-15)
-          uint32_t af[4];
-          af[0] = dq2<FP16>(w0[2 * h] >> (4 * t), z0, s0);
-          af[1] = dq2<FP16>(w1[2 * h] >> (4 * t), z1, s1);
-          af[2] = dq2<FP16>(w0[2 * h + 1] >> (4 * t), z0, s0);
-          af[3] = dq2<FP16>(w1[2 * h + 1] >> (4 * t), z1, s1);
-          mma16816<FP16>(acc[b][0], af, bf[h][0], bf[h][1]);
-          mma16816<FP16>(acc[b][1], af, bf[h][2], bf[h][3]);
+        const uint32_t addr = chunk + (uint32_t)((((4 * (j & 1) + 2 * h + a_k8) ^ a_x)) * 16);
+        if constexpr (NB == 2) {
+          ldmatrix_x4(bf[h], addr);
+        } else {
+          uint32_t b2[2];
+          ldmatrix_x2(b2, addr);
+          bf[h][0] = b2[0];
+          bf[h][1] = b2[1];
+          bf[h][2] = bf[h][3] = 0u;
         }
       }
+      if constexpr (!ONE_GROUP) row_consts(j >> p.sg_shift, sc, zc);
+      // m16 block b: rows 32 warp + 16 b + {g, g + 8} (e = 0, 1), 32 k each
+      uint4 v[2][2];
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) v[b][e] = wv[(rg * 4 + j) * 32 + b * 16 + g + 8 * e];
+      // A fragments of both blocks and both k16 steps, one stage at a time so
+      // that the 16 independent chains interleave: fragment register i of
+      // step h holds rows e = i & 1 of word 2h + (i >> 1) (k 8 (i >> 1) + 2t)
+      uint32_t x[2][2][4];
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            x[b][h][i] = nib_pairs<FP16>(word_of(v[b][i & 1], 2 * h + (i >> 1)) >> (4 * t));
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) x[b][h][i] = sub2<FP16>(x[b][h][i], zc[b][i & 1]);
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) x[b][h][i] = mul2<FP16>(x[b][h][i], sc[b][i & 1]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          mma16816<FP16>(acc[h][b][0], x[b][h], bf[h][0], bf[h][1]);
+          if constexpr (NB == 2) mma16816<FP16>(acc[h][b][1], x[b][h], bf[h][2], bf[h][3]);
+        }
     }
-    __syncthreads();   // the slot is rewritten by the next issue
+    // a ring shorter than the slice: every warp releases the slot, and warp
+    // s % 4 refills it with block s + R once all four have
+    if (R < nk) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      if ((s & (kMmaWarps - 1)) == warp && s + R < nk) {
+        if (lane == 0 &&
+            mbar_wait(&empty[slot], phase, abort_flag, p.status, p.wait_limit_ns,
+                      kStatusTimeout)) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(&full[slot], BB);
+          bulk_load(ring + slot * BB, wsrc + (long long)(s + R) * BB, BB, &full[slot],
+                    policy_evict_first());
+          atomicAdd(issued, 1);
+        }
+        __syncwarp();
+      }
+    }
+    if (++slot == R) {
+      slot = 0;
+      phase ^= 1u;
+    }
   }
-  cp_async_wait<0>();
+  __syncthreads();   // every warp is done with the ring (and every refill issued)
+  const bool aborted = *abort_flag != 0;
+  if (aborted && tid == 0) {
+    // let every copy this CTA issued land before shared memory is reused
+    volatile int no_abort = 0;
+    const int n_issued = *issued;
+    for (int s = n_issued - R < 0 ? 0 : n_issued - R; s < n_issued; ++s)
+      mbar_wait(&full[s % R], (uint32_t)((s / R) & 1), &no_abort, nullptr, kDrainLimitNs, 0);
+    mbar_wait(act_full, 0, &no_abort, nullptr, kDrainLimitNs, 0);
+  }
+  __syncthreads();
 
-  // the CTA's partial as [token][128 features] fp32 in slot 0: the m live
-  // token rows are contiguous, so only they are reduced, read and re-zeroed
-  float* cs = reinterpret_cast<float*>(smem);
+  // the CTA's partial as [token][128 features] fp32 at the start of the ring
+  float* part = reinterpret_cast<float*>(ring);
 #pragma unroll
   for (int b = 0; b < 2; ++b)
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int f = warp * 32 + b * 16 + g, tk = c * 8 + 2 * t;
-      cs[tk * kTileN + f] = acc[b][c][0];
-      cs[(tk + 1) * kTileN + f] = acc[b][c][1];
-      cs[tk * kTileN + f + 8] = acc[b][c][2];
-      cs[(tk + 1) * kTileN + f + 8] = acc[b][c][3];
+    for (int c = 0; c < NB; ++c) {
+      const int f = rg * 32 + b * 16 + g, tk = c * 8 + 2 * t;
+      part[tk * kTileN + f] = acc[0][b][c][0] + acc[1][b][c][0];
+      part[(tk + 1) * kTileN + f] = acc[0][b][c][1] + acc[1][b][c][1];
+      part[tk * kTileN + f + 8] = acc[0][b][c][2] + acc[1][b][c][2];
+      part[(tk + 1) * kTileN + f + 8] = acc[0][b][c][3] + acc[1][b][c][3];
     }
-  fence_proxy_async_smem();   // every writer, before the bulk reduction reads the tile
   __syncthreads();
-
-  __shared__ int last;
-  const float* sum = cs;   // where the finished fp32 rows are read from
-  if (p.splits > 1) {
-    float* tile = p.acc + (long long)nt * (kTileN * 16);
-    if (tid == 0) {
-      bulk_reduce_add_f32(tile, cs, p.m * kTileN * 4);
-      bulk_commit_group();
-      bulk_wait_group_all();
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      int old;
-      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
-                   : "=r"(old)
-                   : "l"(p.counters + nt)
-                   : "memory");
-      last = (old == p.splits - 1);
-    }
-    __syncthreads();
-    if (!last) return;
-    sum = tile;
+  // push: features [r F, r F + F) of the live rows go to cluster rank r's
+  // receive slot sl (an aborted CTA still sends, so every receiver completes)
+  for (int i = tid; i < live * (kTileN / 4); i += kMmaThreads) {
+    const int tk = i >> 5, f = (i & 31) * 4;
+    const int r = f / F, off = f - r * F;
+    const float4 v = *reinterpret_cast<const float4*>(part + tk * kTileN + f);
+    const uint32_t dst = map_to_rank(smem_u32(recv + (sl * ROWS + tk) * F + off), (uint32_t)r);
+    const uint32_t bar = map_to_rank(smem_u32(recv_full), (uint32_t)r);
+    st_async_f4(dst, v, bar);
   }
-  // finish: thread f owns feature f of the n-tile
-  const int f = tid;
-  const int n = nt * kTileN + f;
-  float bias = 0.f;
-  if (p.bias) {
-    const uint16_t bb = p.bias[n];
-    bias = FP16 ? __half2float(*reinterpret_cast<const __half*>(&bb))
-                : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(&bb));
-  }
-  // every live row's sum is loaded before the first output store (the stores
-  // could alias the loads as far as the compiler knows, which would serialize
-  // them one L2 round trip each)
-  float v[16];
-#pragma unroll
-  for (int r = 0; r < 16; ++r)
-    v[r] = r < p.m ? (p.splits > 1 ? __ldcg(sum + r * kTileN + f) : sum[r * kTileN + f]) : 0.f;
-#pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    if (r < p.m) {
-      uint16_t o;
-      if constexpr (FP16) {
-        const __half h = __float2half_rn(v[r] + bias);
-        o = *reinterpret_cast<const uint16_t*>(&h);
-      } else {
-        const __nv_bfloat16 h = __float2bfloat16_rn(v[r] + bias);
-        o = *reinterpret_cast<const uint16_t*>(&h);
+  // finish features [sl F, sl F + F): the S slices summed in cluster-rank order
+  const bool got = mbar_wait(recv_full, 0, abort_flag, p.status, p.wait_limit_ns, kStatusTimeout);
+  if (!aborted && got) {
+    const int q4 = F / 4;
+    for (int i = tid; i < live * q4; i += kMmaThreads) {
+      const int tk = i / q4, off = (i - tk * q4) * 4;
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int q = 0; q < S; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(recv + (q * ROWS + tk) * F + off);
+        o[0] += v.x;
+        o[1] += v.y;
+        o[2] += v.z;
+        o[3] += v.w;
       }
-      p.c[(long long)r * p.n + n] = o;
+      const int n = nt * kTileN + sl * F + off;
+      if (p.bias) {
+        const uint2 bb = *reinterpret_cast<const uint2*>(p.bias + n);
+        const uint32_t bw[2] = {bb.x, bb.y};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint16_t h = (uint16_t)(bw[e >> 1] >> (16 * (e & 1)));
+          o[e] += FP16 ? __half2float(__ushort_as_half(h))
+                       : __bfloat162float(__ushort_as_bfloat16(h));
+        }
+      }
+      uint32_t out[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        if constexpr (FP16) {
+          const __half2 h2 = __floats2half2_rn(o[2 * e], o[2 * e + 1]);
+          out[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        } else {
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * e], o[2 * e + 1]);
+          out[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      }
+      *reinterpret_cast<uint2*>(p.c + (long long)tk * p.n + n) = make_uint2(out[0], out[1]);
     }
   }
-  if (p.splits > 1) {   // leave the accumulator rows and the count at zero
-    float* z = p.acc + (long long)nt * (kTileN * 16) + f;
-#pragma unroll
-    for (int r = 0; r < 16; ++r)
-      if (r < p.m) z[r * kTileN] = 0.f;
-    if (tid == 0) p.counters[nt] = 0;
+  if (!got) {
+    // every peer sends, so the slices arrive; a receiver that gave up still
+    // waits (bounded) for them before its shared memory is released
+    volatile int no_abort = 0;
+    mbar_wait(recv_full, 0, &no_abort, nullptr, kDrainLimitNs, 0);
   }
 }
 
-int mma_smem_bytes(int block_bytes) {
-  return kStages * (((block_bytes + 15) & ~15) + kATileBytes);
-}
-
-cudaError_t launch_w4a16_mma(const W4A16MmaParams& p, bool fp16, cudaStream_t stream) {
-  const int smem = mma_smem_bytes(p.block_bytes);
-  const bool one = p.sg_shift == 2;   // group >= 128
-  auto kern = fp16 ? (one ? w4a16_mma_kernel<true, true> : w4a16_mma_kernel<true, false>)
-                   : (one ? w4a16_mma_kernel<false, true> : w4a16_mma_kernel<false, false>);
-  static int attr_set[4] = {0, 0, 0, 0};
-  int& done = attr_set[(fp16 ? 2 : 0) + (one ? 1 : 0)];
-  if (smem > done) {
+template <bool FP16, int NB, bool ONE>
+static cudaError_t launch_one(const CUtensorMap& tmap, const W4A16MmaParams& p, int smem,
+                              cudaStream_t stream) {
+  auto kern = w4a16_mma_kernel<FP16, NB, ONE>;
+  static int smem_set = 0;
+  static bool nonportable_set = false;
+  if (smem > smem_set) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    done = smem;
+    smem_set = smem;
+  }
+  if (p.splits > 8 && !nonportable_set) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (err != cudaSuccess) return err;
+    nonportable_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.nt * p.splits));
   cfg.blockDim = dim3(kMmaThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)p.splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tmap, p);
+}
+
+cudaError_t launch_w4a16_mma(const CUtensorMap& tmap, const W4A16MmaParams& p, bool fp16,
+                             cudaStream_t stream) {
+  const bool one = p.sg_shift == 2;   // group >= 128
+  const int nb = p.m <= 8 ? 1 : 2;
+  const int smem = mma_smem_bytes(p.block_bytes, p.ring, p.nk_max, 8 * nb);
+  if (fp16) {
+    if (nb == 1) return one ? launch_one<true, 1, true>(tmap, p, smem, stream)
+                            : launch_one<true, 1, false>(tmap, p, smem, stream);
+    return one ? launch_one<true, 2, true>(tmap, p, smem, stream)
+               : launch_one<true, 2, false>(tmap, p, smem, stream);
+  }
+  if (nb == 1) return one ? launch_one<false, 1, true>(tmap, p, smem, stream)
+                          : launch_one<false, 1, false>(tmap, p, smem, stream);
+  return one ? launch_one<false, 2, true>(tmap, p, smem, stream)
+             : launch_one<false, 2, false>(tmap, p, smem, stream);
 }
 
 }  // namespace qg
