@@ -69,12 +69,14 @@ enum {
   QGEMM_W_MXFP4 = 2,
   QGEMM_W_NVFP4 = 3,
   QGEMM_W_INT8_SYM = 4,   /* W8A16 */
-  QGEMM_W_UINT8_ZP = 5
+  QGEMM_W_UINT8_ZP = 5,
+  QGEMM_W_INT3_SYM = 6,   /* GPTQ INT3 (W3A16) */
+  QGEMM_W_UINT3_ZP = 7
 };
 /* scale formats */
 enum { QGEMM_S_FP16 = 0, QGEMM_S_BF16 = 1, QGEMM_S_E8M0 = 2, QGEMM_S_E4M3 = 3 };
 /* zero-point formats */
-enum { QGEMM_Z_NONE = 0, QGEMM_Z_UINT4 = 1, QGEMM_Z_UINT8 = 2 };
+enum { QGEMM_Z_NONE = 0, QGEMM_Z_UINT4 = 1, QGEMM_Z_UINT8 = 2, QGEMM_Z_UINT3 = 3 };
 /* activation / output data types */
 enum { QGEMM_FP16 = 0, QGEMM_BF16 = 1, QGEMM_FP8E4M3 = 2 };
 /* GEMM types (compute config) */
@@ -161,7 +163,9 @@ typedef struct {
  * Tuning config: how to run it on this device.  Pass NULL for the built-in
  * B300 heuristic (token tile chosen by the M range).  Fields left 0 are chosen
  * by the heuristic.
- *   block_tok  tokens per tile (the MMA N extent): 16, 32, 64 or 128
+ *   block_tok  tokens per tile (the MMA N extent): 16, 32, 64, 128 or 256
+ *              (256: INT4 / UINT4 weights with scales in the activation
+ *              dtype only; one accumulator buffer)
  *   stages     shared-memory pipeline depth (2 .. 16)
  *   max_ctas   upper bound on the persistent grid (<= number of SMs)
  *   split_k    0 = the heuristic's choice (without max_ctas: whole tiles or
@@ -205,6 +209,20 @@ typedef struct {
  *     meaning  w[k, n] = (q - z) * s, rounded once to the activation dtype
  *              (z = 0 for INT4; an fp16 scale with bf16 activations is not
  *              rounded to bf16 first)
+ *   INT3 / UINT3 (GPTQ 3-bit codes, W3A16):
+ *     qweight  int32 [3K/32, N]: the codes of column n form a little-endian
+ *              bit stream along K, code k in bits [3k, 3k+3) of the column's
+ *              stream (word 3j + w of the column holds stream bits
+ *              [32 (3j + w), 32 (3j + w) + 32)), so 32 codes fill three words
+ *              and a code may straddle two; INT3 as 3-bit two's complement
+ *              (-4..3), UINT3 as raw 0..7
+ *     scales   as INT4
+ *     qzeros   int32 [K/g, 3N/32] (UINT3_ZP only): each group row's zero
+ *              points as a bit stream along N, column c in bits [3c, 3c+3)
+ *     meaning  as INT4.  The pages name GPTQ INT3 among the formats served
+ *              (jetabc.cn, "怎么使用").  The pack repacks the codes into the
+ *              4-bit blocks (INT3 as offset binary q + 8, UINT3 and its zero
+ *              points unchanged), so every 4-bit kernel runs them.
  *   INT8 / UINT8 (W8A16):
  *     qweight  int32 [K/4, N]: word (j, n) holds k = 4j + i in bits [8i, 8i+8),
  *              INT8 as two's complement, UINT8 as raw 0..255

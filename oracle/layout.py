@@ -241,6 +241,25 @@ def packed_w4(q, s_bits, z, g: int, signed: bool) -> np.ndarray:
     return interleave_blocks(*pieces)
 
 
+def packed_w3(q, s_bits, z, g: int, signed: bool) -> np.ndarray:
+    """The packed buffer of a 3-bit integer layer (GPTQ INT3 / UINT3).
+
+    Reading (the pages name GPTQ INT3 among the served formats and fix no
+    kernel layout): the 3-bit codes take the 4-bit blocks of ``packed_w4``
+    unchanged in value.  An INT3 code q in [-4, 3] is a 4-bit two's
+    complement value too, so it is stored as the offset-binary nibble q + 8
+    like an INT4 code; a UINT3 code and its zero point (0..7) are stored as
+    they are.  The dequantized value (q - z) * s is therefore the same in
+    both representations."""
+    q = np.asarray(q)
+    lo, hi = (-4, 3) if signed else (0, 7)
+    if q.min(initial=0) < lo or q.max(initial=0) > hi:
+        raise ValueError("codes out of the 3-bit range")
+    if z is not None and (np.asarray(z).min(initial=0) < 0 or np.asarray(z).max(initial=0) > 7):
+        raise ValueError("zero points out of the 3-bit range")
+    return packed_w4(q, s_bits, z, g, signed)
+
+
 def packed_w8(q, s_bits, z, g: int, signed: bool) -> np.ndarray:
     """8-bit codes q[K, N], scale bits [K/g, N] and zero points [K/g, N] (None
     for signed INT8) -> the packed buffer of one matrix."""

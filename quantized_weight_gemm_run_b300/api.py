@@ -135,6 +135,34 @@ class W8A16Linear(W4A16Linear):
         self._pack(qweight, scales, qzeros, bias, tuning, deterministic, batch_invariant)
 
 
+class W3A16Linear(W4A16Linear):
+    """A packed layer of 3-bit integer weights (GPTQ INT3, or UINT3 with zero
+    points) against fp16/bf16 activations: qweight int32 [E*3K/32, N] (each
+    column's codes a bit stream along K), scales [E*K/g, N] (16-bit:
+    ``scale_dtype``, default the activation dtype), qzeros int32
+    [E*K/g, 3N/32] or None.  The pack stores the codes in the 4-bit blocks,
+    so runs, grouped runs and the dequantized view are those of
+    ``W4A16Linear``."""
+
+    def __init__(self, qweight, scales, qzeros, n, k, group, act_dtype, num_experts=1,
+                 bias=None, tuning=None, deterministic=False, gated=False,
+                 batch_invariant=False, scale_dtype=None):
+        self.n, self.k, self.group, self.num_experts = n, k, group, num_experts
+        self.gated = gated
+        self.n_out = n // 2 if gated else n
+        self.act_dtype = act_dtype
+        asym = qzeros is not None
+        adt = _DT[act_dtype]
+        sdt = adt if scale_dtype is None else _DT[scale_dtype]
+        self.layer = Q.layer_config(
+            n, k, group, Q.QGEMM_W_UINT3_ZP if asym else Q.QGEMM_W_INT3_SYM,
+            Q.QGEMM_S_FP16 if sdt == Q.QGEMM_FP16 else Q.QGEMM_S_BF16,
+            Q.QGEMM_Z_UINT3 if asym else Q.QGEMM_Z_NONE, adt, adt,
+            1 if bias is not None else 0, num_experts,
+            Q.QGEMM_ACT_SILU_GLU if gated else Q.QGEMM_ACT_NONE)
+        self._pack(qweight, scales, qzeros, bias, tuning, deterministic, batch_invariant)
+
+
 class NVFP4Linear(W4A16Linear):
     """A packed layer of NVFP4 weights against fp16/bf16 activations: e2m1
     codes uint8 [E*N, K/2] (standard nibble order), e4m3 block scales uint8

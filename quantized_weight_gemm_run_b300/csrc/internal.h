@@ -169,9 +169,12 @@ __device__ __forceinline__ float silu_mul_f32(float g, float u) {
 }
 #endif
 
+// code_bits 4: INT4 / UINT4 (qweight int32 [K/8, N], qzeros [K/g, N/8]);
+// 3: INT3 / UINT3 bit streams (qweight int32 [3K/32, N], qzeros [K/g, 3N/32]),
+// repacked into the same 4-bit blocks.
 cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
                              const int32_t* qzeros, uint8_t* packed, int64_t n, int64_t k,
-                             int group, int signed_q, int experts, int gated,
+                             int group, int signed_q, int experts, int gated, int code_bits,
                              cudaStream_t stream);
 // INT8 / UINT8: standard qweight int32 [K/4, N], scales [K/g, N], qzeros
 // int32 [K/g, N/4] or null -> packed blocks of 16384 code bytes.

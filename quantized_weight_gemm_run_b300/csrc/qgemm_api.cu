@@ -103,8 +103,12 @@ static qgemm_status check_layer(const qgemm_layer_config* L) {
   if (L->gated_act != QGEMM_ACT_NONE && L->out_dtype != QGEMM_BF16)
     return fail(QGEMM_ERR_UNSUPPORTED, "a gated output must be bf16");
   switch (L->weight_format) {
+    case QGEMM_W_INT3_SYM:
+    case QGEMM_W_UINT3_ZP:
     case QGEMM_W_INT4_SYM:
     case QGEMM_W_UINT4_ZP: {
+      const bool w3 = L->weight_format == QGEMM_W_INT3_SYM || L->weight_format == QGEMM_W_UINT3_ZP;
+      const bool sym = L->weight_format == QGEMM_W_INT4_SYM || L->weight_format == QGEMM_W_INT3_SYM;
       if (L->act_dtype != QGEMM_FP16 && L->act_dtype != QGEMM_BF16)
         return fail(QGEMM_ERR_UNSUPPORTED, "W4A16 needs fp16 or bf16 activations");
       if (L->out_dtype != L->act_dtype)
@@ -117,10 +121,11 @@ static qgemm_status check_layer(const qgemm_layer_config* L) {
       const bool g_ok = g == 32 || g == 64 || (g >= 128 && g % 128 == 0);
       if (!g_ok) return fail(QGEMM_ERR_UNSUPPORTED, "group size %d not in {32, 64, 128j}", g);
       if (L->k % g) return fail(QGEMM_ERR_UNSUPPORTED, "k must be a multiple of the group size");
-      if (L->weight_format == QGEMM_W_INT4_SYM && L->zero_format != QGEMM_Z_NONE)
-        return fail(QGEMM_ERR_UNSUPPORTED, "symmetric INT4 takes no zero points");
-      if (L->weight_format == QGEMM_W_UINT4_ZP && L->zero_format != QGEMM_Z_UINT4)
-        return fail(QGEMM_ERR_UNSUPPORTED, "UINT4 needs uint4 zero points");
+      if (sym && L->zero_format != QGEMM_Z_NONE)
+        return fail(QGEMM_ERR_UNSUPPORTED, "symmetric integer weights take no zero points");
+      if (!sym && L->zero_format != (w3 ? QGEMM_Z_UINT3 : QGEMM_Z_UINT4))
+        return fail(QGEMM_ERR_UNSUPPORTED, w3 ? "UINT3 needs uint3 zero points"
+                                                : "UINT4 needs uint4 zero points");
       return ok();
     }
     case QGEMM_W_INT8_SYM:
@@ -189,7 +194,12 @@ static bool is_w8(const qgemm_layer_config* L) {
 }
 // integer formats with zero points (UINT4, UINT8)
 static bool has_zeros(const qgemm_layer_config* L) {
-  return L->zero_format == QGEMM_Z_UINT4 || L->zero_format == QGEMM_Z_UINT8;
+  return L->zero_format == QGEMM_Z_UINT4 || L->zero_format == QGEMM_Z_UINT8 ||
+         L->zero_format == QGEMM_Z_UINT3;
+}
+// 3-bit integer codes (GPTQ INT3 / UINT3), repacked into the 4-bit blocks
+static bool is_w3(const qgemm_layer_config* L) {
+  return L->weight_format == QGEMM_W_INT3_SYM || L->weight_format == QGEMM_W_UINT3_ZP;
 }
 // W4A16 with fp16 scales against bf16 activations
 static bool is_f16s(const qgemm_layer_config* L) {
@@ -288,8 +298,11 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   const int E = L->num_experts;
   int bt = (T && T->block_tok) ? T->block_tok
                                : heuristic_block_tok(grouped ? (rows + E - 1) / E : rows);
-  if (bt != 16 && bt != 32 && bt != 64 && bt != 128)
-    return fail(QGEMM_ERR_UNSUPPORTED, "block_tok %d not in {16, 32, 64, 128}", bt);
+  if (bt != 16 && bt != 32 && bt != 64 && bt != 128 && bt != 256)
+    return fail(QGEMM_ERR_UNSUPPORTED, "block_tok %d not in {16, 32, 64, 128, 256}", bt);
+  if (bt == 256 && (is_mx(L) || is_nv(L) || is_f16s(L) || is_w8(L)))
+    return fail(QGEMM_ERR_UNSUPPORTED,
+                "block_tok 256 takes INT4 / UINT4 weights with scales in the activation dtype");
   if (T && (T->cta_pair != 0)) return fail(QGEMM_ERR_UNSUPPORTED, "cta_pair is reserved");
   if (T && (T->split_k < 0 || T->split_k > 64))
     return fail(QGEMM_ERR_INVALID_ARG, "split_k must be in [0, 64]");
@@ -745,8 +758,12 @@ qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qwe
     e = launch_repack_w4(static_cast<const int32_t*>(qweight),
                          static_cast<const uint16_t*>(scales), static_cast<const int32_t*>(qzeros),
                          static_cast<uint8_t*>(packed), layer->n, layer->k, layer->group_size,
-                         layer->weight_format == QGEMM_W_INT4_SYM ? 1 : 0, layer->num_experts,
-                         layer->gated_act != 0, static_cast<cudaStream_t>(stream));
+                         (layer->weight_format == QGEMM_W_INT4_SYM ||
+                          layer->weight_format == QGEMM_W_INT3_SYM)
+                             ? 1
+                             : 0,
+                         layer->num_experts, layer->gated_act != 0, is_w3(layer) ? 3 : 4,
+                         static_cast<cudaStream_t>(stream));
   }
   if (e != cudaSuccess) return cuda_fail(e, "repack launch");
   return ok();
@@ -925,8 +942,8 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
     if (st != QGEMM_OK) {
       rec = std::string("rejected: ") + g_last_error;
     } else {
-      static const char* wf[] = {"int4_sym", "uint4_zp", "mxfp4",
-                                 "nvfp4",    "int8_sym", "uint8_zp"};
+      static const char* wf[] = {"int4_sym", "uint4_zp", "mxfp4",    "nvfp4",
+                                 "int8_sym", "uint8_zp", "int3_sym", "uint3_zp"};
       static const char* dt[] = {"fp16", "bf16", "fp8e4m3"};
       static const char* sf[] = {"fp16", "bf16", "e8m0", "e4m3"};
       char tmp[512];

@@ -23,7 +23,14 @@
 //            sg*128 + r the scale of row r for the sg-th group of the tile.
 //            MXFP4: 128 32-bit words, byte j of word r the e8m0 exponent of
 //            row r for k = 32j .. 32j+31 of the tile.
-//   zeros    UINT4 / UINT8 only: 128 * ST bytes, same order, the zero point.
+//   zeros    UINT4 / UINT8 / UINT3 only: 128 * ST bytes, same order, the zero point.
+//
+// INT3 / UINT3 (GPTQ's 3-bit codes; the standard format is each column's
+// codes as a little-endian bit stream along K, 32 codes in three words) are
+// repacked into the 4-bit layout: an INT3 code q in [-4, 3] becomes the
+// offset-binary nibble q + 8, exactly as an INT4 code does, and a UINT3 code
+// and its zero point are stored as they are.  The 4-bit kernels then read
+// them unchanged; every value means what the 3-bit code means.
 //
 // A gated layer's rows are taken in the gate/up interleaved order
 // (glu_source_col).  Every thread writes one output vector / element; reads
@@ -101,12 +108,64 @@ __global__ void repack_scales_kernel(const uint16_t* __restrict__ scales,
   reinterpret_cast<uint16_t*>(bp + code_bytes)[sg * kTileN + r] =
       scales[ex * groups * n + (long long)grp * n + col];
   if (qzeros) {
-    const int per_word = 32 / zero_bits;   // zero points per int32 word along N
-    const uint32_t word = (uint32_t)qzeros[ex * groups * (n / per_word) +
-                                           (long long)grp * (n / per_word) + col / per_word];
+    // the zero points of a group row are a little-endian bit stream along N:
+    // column c's at bits [b c, b c + b), possibly straddling two words (b = 3)
+    const long long row_words = (long long)n * zero_bits / 32;
+    const int32_t* zr = qzeros + (ex * groups + grp) * row_words;
+    const long long bit = (long long)zero_bits * col;
+    const int off = (int)(bit & 31);
+    uint64_t word = (uint32_t)zr[bit >> 5];
+    if (off + zero_bits > 32) word |= (uint64_t)(uint32_t)zr[(bit >> 5) + 1] << 32;
     bp[code_bytes + packed_scale_bytes(false, st) + sg * kTileN + r] =
-        (uint8_t)((word >> (zero_bits * (col % per_word))) & ((1u << zero_bits) - 1u));
+        (uint8_t)((word >> off) & ((1u << zero_bits) - 1u));
   }
+}
+
+// INT3 / UINT3 codes: output vector v of a block (row 32qd + t, k = 32j ..
+// 32j + 31) takes the three standard words holding those 32 codes of the
+// column (bits [3i, 3i + 3) of the 96-bit run for k = 32j + i) and writes
+// them in the 4-bit vector's nibble order; INT3 codes become q + 8.
+__global__ void repack_weights3_kernel(const int32_t* __restrict__ qweight,
+                                       uint8_t* __restrict__ out, int n, int k, int signed_q,
+                                       int block_bytes, int gated, long long total) {
+  const long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (vec >= total) return;
+  const int KT = k / kTileK, NT = n / kTileN;
+  const long long per_expert = (long long)NT * KT * 512;
+  const long long ex = vec / per_expert;
+  const long long rem = vec - ex * per_expert;
+  const long long blk = rem / 512;
+  const int v = (int)(rem % 512);
+  const int nt = (int)(blk / KT), kt = (int)(blk % KT);
+  const int t = v & 31, j = (v >> 5) & 3, qd = v >> 7;
+  const int col = packed_source_col(nt, qd * 32 + t, n, gated);
+  const long long word_row0 = (long long)(kt * kTileK + j * 32) / 32 * 3;   // 3 words / 32 k
+  const int32_t* src = qweight + ex * (long long)(k / 32 * 3) * n;
+  const uint32_t w0 = (uint32_t)src[(word_row0 + 0) * n + col];
+  const uint32_t w1 = (uint32_t)src[(word_row0 + 1) * n + col];
+  const uint32_t w2 = (uint32_t)src[(word_row0 + 2) * n + col];
+  auto code = [&](int i) -> uint32_t {   // the 3-bit code of k = 32j + i
+    const int b = 3 * i;
+    uint64_t x = b < 32 ? ((uint64_t)w0 | ((uint64_t)w1 << 32)) >> b
+                        : ((uint64_t)w1 | ((uint64_t)w2 << 32)) >> (b - 32);
+    const uint32_t c = (uint32_t)x & 7u;
+    // two's complement q = c - 8 [c >= 4] -> q + 8 = (c ^ 4) + 4
+    return signed_q ? (c ^ 4u) + 4u : c;
+  };
+  uint32_t o[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    // nibble position p takes k-offset {0,2,4,6,1,3,5,7}[p] of the word's 8 k
+    uint32_t r = 0;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const int koff = p < 4 ? 2 * p : 2 * (p - 4) + 1;
+      r |= code(8 * w + koff) << (4 * p);
+    }
+    o[w] = r;
+  }
+  const long long gblk = ex * ((long long)NT * KT) + blk;
+  *reinterpret_cast<uint4*>(out + gblk * block_bytes + v * 16) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // INT8 / UINT8 codes: output vector v of a block takes four standard words
@@ -140,20 +199,24 @@ __global__ void repack_weights8_kernel(const int32_t* __restrict__ qweight,
 
 cudaError_t launch_repack_w4(const int32_t* qweight, const uint16_t* scales,
                              const int32_t* qzeros, uint8_t* packed, int64_t n, int64_t k,
-                             int group, int signed_q, int experts, int gated,
+                             int group, int signed_q, int experts, int gated, int code_bits,
                              cudaStream_t stream) {
   const int threads = 256;
   const int st = group < kTileK ? kTileK / group : 1;
   const int block_bytes = packed_block_bytes(false, st, qzeros != nullptr);
   const long long vecs = (long long)experts * (n / kTileN) * (k / kTileK) * 512;
-  repack_weights_kernel<<<(unsigned)((vecs + threads - 1) / threads), threads, 0, stream>>>(
-      qweight, packed, (int)n, (int)k, signed_q, block_bytes, gated, vecs);
+  if (code_bits == 3)
+    repack_weights3_kernel<<<(unsigned)((vecs + threads - 1) / threads), threads, 0, stream>>>(
+        qweight, packed, (int)n, (int)k, signed_q, block_bytes, gated, vecs);
+  else
+    repack_weights_kernel<<<(unsigned)((vecs + threads - 1) / threads), threads, 0, stream>>>(
+        qweight, packed, (int)n, (int)k, signed_q, block_bytes, gated, vecs);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const long long elems = (long long)experts * (n / kTileN) * (k / kTileK) * st * kTileN;
   repack_scales_kernel<<<(unsigned)((elems + threads - 1) / threads), threads, 0, stream>>>(
-      scales, qzeros, packed, (int)n, (int)k, group, block_bytes, packed_code_bytes(false), 4,
-      gated, elems);
+      scales, qzeros, packed, (int)n, (int)k, group, block_bytes, packed_code_bytes(false),
+      code_bits, gated, elems);
   return cudaGetLastError();
 }
 

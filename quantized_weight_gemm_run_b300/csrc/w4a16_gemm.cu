@@ -448,6 +448,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   constexpr int kSlotCols = MX ? 32 : kASlotCols;
   constexpr uint32_t kSfaCol = 128, kSfbCol = 160, kAccCol = 256;
   constexpr uint32_t kActUnit = BT * kTileK * (MX ? 1 : 2);   // bytes of one unit's activations
+  // accumulator buffers of BT columns from column 256: two (the epilogue of
+  // one tile overlaps the next tile's MMAs) up to 128 tokens, one at 256
+  constexpr int NACC = BT == 256 ? 1 : 2;
+  static_assert(BT <= 128 || !MX, "256-token tiles take 16-bit formats only");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles
@@ -763,7 +767,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         if (!ok) break;
         mma_commit(&acc_full[acc]);
-        if (++acc == 2) {
+        if (++acc == NACC) {
           acc = 0;
           accphase ^= 1;
         }
@@ -1266,7 +1270,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           if (lane == 0) *counter = 0;   // ready for the next launch
         }
       }
-      if (++acc == 2) {
+      if (++acc == NACC) {
         acc = 0;
         accphase ^= 1;
       }
@@ -1316,6 +1320,10 @@ static cudaError_t launch_bt(const CUtensorMap& tmap, const CUtensorMap& tmap_c,
     case 32: return launch_t<32, FMT, GROUPED>(tmap, tmap_c, p, grid, stream);
     case 64: return launch_t<64, FMT, GROUPED>(tmap, tmap_c, p, grid, stream);
     case 128: return launch_t<128, FMT, GROUPED>(tmap, tmap_c, p, grid, stream);
+    case 256:
+      if constexpr (FMT == 0 || FMT == 1)
+        return launch_t<256, FMT, GROUPED>(tmap, tmap_c, p, grid, stream);
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }

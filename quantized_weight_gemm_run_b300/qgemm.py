@@ -25,8 +25,9 @@ QGEMM_ERR_DEVICE = 6
 # weight / scale / zero formats, dtypes, GEMM types
 QGEMM_W_INT4_SYM, QGEMM_W_UINT4_ZP, QGEMM_W_MXFP4, QGEMM_W_NVFP4 = 0, 1, 2, 3
 QGEMM_W_INT8_SYM, QGEMM_W_UINT8_ZP = 4, 5
+QGEMM_W_INT3_SYM, QGEMM_W_UINT3_ZP = 6, 7
 QGEMM_S_FP16, QGEMM_S_BF16, QGEMM_S_E8M0, QGEMM_S_E4M3 = 0, 1, 2, 3
-QGEMM_Z_NONE, QGEMM_Z_UINT4, QGEMM_Z_UINT8 = 0, 1, 2
+QGEMM_Z_NONE, QGEMM_Z_UINT4, QGEMM_Z_UINT8, QGEMM_Z_UINT3 = 0, 1, 2, 3
 QGEMM_FP16, QGEMM_BF16, QGEMM_FP8E4M3 = 0, 1, 2
 QGEMM_GEMM_DENSE, QGEMM_GEMM_GROUPED = 0, 1
 QGEMM_ACT_NONE, QGEMM_ACT_SILU_GLU = 0, 1

@@ -71,7 +71,7 @@ def test_gated_gemm_parity(Q, m, n, k, g, sym, bias):
     assert_close(to_np(out), _gated_ref(c), what=f"gated {m}x{n}x{k}")
 
 
-@pytest.mark.parametrize("bt", [16, 32, 64, 128])
+@pytest.mark.parametrize("bt", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("det,max_ctas", [(False, 7), (True, 7), (False, 0)])
 def test_gated_split_tiles(Q, bt, det, max_ctas):
     """Split-K tiles (few CTAs, many k-tiles) reach the gated output through

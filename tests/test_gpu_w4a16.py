@@ -66,7 +66,7 @@ def test_gemm_bias(Q):
 
 
 @pytest.mark.parametrize("det", [False, True])
-@pytest.mark.parametrize("bt", [16, 32, 64, 128])
+@pytest.mark.parametrize("bt", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("split_k,max_ctas", [(0, 0), (1, 0), (0, 7)])
 def test_tuning_overrides_same_result(Q, bt, split_k, max_ctas, det):
     c = Case(70, 384, 768, 128, "bf16", False, seed=9)
@@ -75,6 +75,29 @@ def test_tuning_overrides_same_result(Q, bt, split_k, max_ctas, det):
     out = lin(c.dev_act())
     assert lin.status() == Q.QGEMM_OK
     assert_close(to_np(out), c.reference(), what=f"bt={bt} split_k={split_k} ctas={max_ctas}")
+
+
+@pytest.mark.parametrize("m,adt,sym,split_k,max_ctas", [
+    (600, "bf16", True, 0, 0),      # ragged last 256-token tile, stream-K
+    (600, "fp16", False, 1, 0),     # whole tiles
+    (1024, "bf16", False, 0, 5),    # few CTAs: long stream-K ranges
+])
+def test_256_token_tiles(Q, m, adt, sym, split_k, max_ctas):
+    """The 256-token tile (one 256-column accumulator, N = 256 MMAs) over
+    several token tiles, a ragged last tile, split and whole tiles."""
+    c = Case(m, 640, 1536, 128, adt, sym, seed=m + 3)
+    lin = linear(c, tuning=Q.tuning_config(block_tok=256, split_k=split_k, max_ctas=max_ctas))
+    out = lin(c.dev_act())
+    assert lin.status() == Q.QGEMM_OK
+    assert_close(to_np(out), c.reference(), what=f"bt=256 m={m} {adt}")
+
+
+def test_256_token_tiles_reject_other_formats(Q):
+    layer = Q.layer_config(256, 256, 32, Q.QGEMM_W_MXFP4, Q.QGEMM_S_E8M0, Q.QGEMM_Z_NONE,
+                           Q.QGEMM_FP8E4M3, Q.QGEMM_BF16)
+    st, _ = Q.qgemm_workspace_size(layer, Q.compute_config(Q.QGEMM_GEMM_DENSE),
+                                   Q.tuning_config(block_tok=256), 512)
+    assert st == Q.QGEMM_ERR_UNSUPPORTED
 
 
 def test_deterministic_mode_bits_repeat(Q):

@@ -571,3 +571,40 @@ def test_packed_w8_scalar_spec(gsize, zp):
         assert int(buf[sbyte]) | (int(buf[sbyte + 1]) << 8) == sb[kk // gsize, nn]
         if zp:
             assert buf[base + 16384 + 256 * st + sg * 128 + r] == z[kk // gsize, nn]
+
+
+@pytest.mark.parametrize("zp", [False, True])
+def test_packed_w3_scalar_spec(zp):
+    """3-bit codes in the 4-bit blocks: an INT3 code q reads back as the
+    nibble q + 8 and a UINT3 code (and its zero point) as itself, at the byte
+    addresses of the 4-bit layout; codes from the standard bit stream."""
+    g = np.random.default_rng(31)
+    k, n, gsize = 256, 256, 64
+    q = g.integers(0, 8, (k, n)) if zp else g.integers(-4, 4, (k, n))
+    # through the standard format (bit stream along K) and back
+    q = quant.unpack_int_kn(quant.pack_int_kn(q, 3, not zp), 3, not zp)
+    sb = g.integers(0, 65535, (k // gsize, n)).astype(np.uint16)
+    z = g.integers(0, 8, (k // gsize, n)) if zp else None
+    buf = layout.packed_w3(q, sb, z, gsize, signed=not zp)
+    st = 128 // gsize
+    blk = 8192 + 256 * st + (128 * st if zp else 0)
+    for _ in range(1500):
+        kk, nn = int(g.integers(0, k)), int(g.integers(0, n))
+        nt, r = divmod(nn, 128)
+        kt, kl = divmod(kk, 128)
+        base = (nt * (k // 128) + kt) * blk
+        want = q[kk, nn] if zp else q[kk, nn] + 8
+        assert _nibble_at(buf[base: base + 8192], r, kl, 1) == want
+        if zp:
+            assert buf[base + 8192 + 256 * st + (kl // gsize) * 128 + r] == z[kk // gsize, nn]
+
+
+def test_packed_w3_rejects_codes_out_of_range():
+    q = np.zeros((128, 128), dtype=np.int64)
+    sb = np.zeros((1, 128), dtype=np.uint16)
+    q[5, 7] = -5
+    with pytest.raises(ValueError):
+        layout.packed_w3(q, sb, None, 128, signed=True)
+    q[5, 7] = 8
+    with pytest.raises(ValueError):
+        layout.packed_w3(q, sb, np.zeros((1, 128), dtype=np.int64), 128, signed=False)
