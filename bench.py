@@ -379,10 +379,16 @@ def source_without_comments(text: str) -> str:
     return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
+# the sources that decide what the tcgen05 GEMM kernel does: the kernel, its
+# PTX wrappers and shared declarations, and the planner that configures it
+TRAFFIC_SOURCES = ("internal.h", "ptx.cuh", "qgemm_api.cu", "w4a16_gemm.cu")
+
+
 def kernel_source_digest(read=None):
-    """Digest of the library's sources (kernels and the planner that picks
-    them), comments ignored; a committed ncu traffic figure is used only while
-    it matches.  ``read(name)`` returns a file's text (default: the tree)."""
+    """Digest of the tcgen05 GEMM kernel's sources (TRAFFIC_SOURCES: the
+    kernel and the planner that configures it), comments ignored; a committed
+    ncu traffic figure of that kernel is used only while it matches.
+    ``read(name)`` returns a file's text (default: the tree)."""
     import hashlib
     d = os.path.join(ROOT, "quantized_weight_gemm_run_b300", "csrc")
     if read is None:
@@ -390,9 +396,8 @@ def kernel_source_digest(read=None):
             with open(os.path.join(d, name)) as fh:
                 return fh.read()
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(source_without_comments(read(f)).encode())
+    for f in TRAFFIC_SOURCES:
+        h.update(source_without_comments(read(f)).encode())
     return h.hexdigest()[:16]
 
 
