@@ -46,14 +46,14 @@ static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cud
 }
 
 // ----------------------------------------------------------- FP8 act quant
-// One warp per row, eight rows per CTA: s = max|x| / 448 (fp32, IEEE divide;
+// One warp per row, four rows per CTA (spread over more SMs): s = max|x| / 448 (fp32, IEEE divide;
 // 1 for an all-zero row), code = e4m3_rn_satfinite(x / s) with an IEEE fp32
 // divide.  Lanes take 16-byte vectors (8 bf16) of the row in turn; the first
 // kActVecs vectors of each lane stay in registers between the max and the
 // quantization (a 2048-wide row in one pass), the rest of a longer row is read
 // again.  Codes leave as 8-byte stores.
 constexpr int kActVecs = 8;
-constexpr int kActRowsPerCta = 8;
+constexpr int kActRowsPerCta = 4;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
