@@ -224,8 +224,9 @@ class GemmPoint:
     """Buffers of one GEMM of the workload (own weights, activations, output).
 
     ``clone()`` duplicates every device buffer, so that a rotation of clones
-    reads its operands cold from HBM.  A W4A8 point's launch is the per-token
-    FP8 quantization of its bf16 activations followed by the GEMM."""
+    reads its operands cold from HBM.  A W4A8 point's launch is one library
+    call on its bf16 activations: the per-token FP8 quantization runs inside
+    the small-M kernel at M <= 16, else as its own kernel ahead of the GEMM."""
 
     def __init__(self, p, seed, device, host=False, src=None):
         import torch
@@ -271,17 +272,15 @@ class GemmPoint:
             self.lin = copy.copy(src.lin)
             self.lin.packed = src.lin.packed.clone()
             self.a = src.a.clone()
-        if self.mx:
-            self.a8 = torch.empty(m, k, dtype=torch.uint8, device=device)
-            self.a_scale = torch.empty(max(m, 1), dtype=torch.float32, device=device)
+        self.layer = self.lin.layer_bf16 if self.mx else self.lin.layer
         self.c = torch.empty(m, n, dtype=dt, device=device)
-        st, nbytes = Q.qgemm_workspace_size(self.lin.layer, self.lin.dense, None, m)
+        st, nbytes = Q.qgemm_workspace_size(self.layer, self.lin.dense, None, m)
         Q.check(st)
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
         if host:
             self.a_host = self.a.cpu().pin_memory()
             self.c_host = torch.empty(m, n, dtype=dt).pin_memory()
-        self.launches = 2 if self.mx else 1
+        self.launches = 2 if self.mx and m > 16 else 1
 
     def clone(self):
         return GemmPoint(self.p, 0, self.c.device, src=self)
@@ -289,13 +288,8 @@ class GemmPoint:
     def launch(self):
         Q = self.Q
         m = self.p["m"]
-        if self.mx:
-            Q.check(Q.qgemm_quantize_act_fp8(self.a, m, self.p["k"], self.a8, self.a_scale))
-            Q.check(Q.qgemm_run(self.lin.layer, self.lin.dense, None, m, self.a8, self.a_scale,
-                                self.lin.packed, None, self.c, self.ws, self.ws.numel()))
-        else:
-            Q.check(Q.qgemm_run(self.lin.layer, self.lin.dense, None, m, self.a, None,
-                                self.lin.packed, None, self.c, self.ws, self.ws.numel()))
+        Q.check(Q.qgemm_run(self.layer, self.lin.dense, None, m, self.a, None,
+                            self.lin.packed, None, self.c, self.ws, self.ws.numel()))
 
     def copy_in(self):
         self.a.copy_(self.a_host, non_blocking=True)
@@ -444,15 +438,17 @@ def kernel_name(p):
     if kind == "moe":
         return "moe_layer (sort, gather, SiLU-gated grouped GEMM, grouped GEMM, combine)"
     m = p["m"]
-    if kind == "w4a16" and m <= 16 and not f16_scales(p):
-        # the planner's default for dense INT4/UINT4 GEMMs of at most 16 rows
-        return (f"w4a16_mma_kernel<{'fp16' if p['adt'] == 'fp16' else 'bf16'},"
-                f"{1 if m <= 8 else 2}>")
+    if kind in ("w4a16", "w4a8") and m <= 16 and not f16_scales(p):
+        # the planner's default for dense INT4/UINT4 and W4A8 GEMMs of at most 16 rows
+        dt = ("w4a8_fused_act_quant" if kind == "w4a8"
+              else "fp16" if p["adt"] == "fp16" else "bf16")
+        return f"w4a16_mma_kernel<{dt},{1 if m <= 8 else 2}>"
     bt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
     fmt = ("w4a8_mxf8f6f4" if kind == "w4a8" else "nvfp4_bf16" if kind == "nvfp4"
            else f"int8_{p['adt']}" if kind == "w8a16"
            else "bf16_f16scales" if f16_scales(p) else "fp16" if p["adt"] == "fp16" else "bf16")
-    return f"w4a16_kernel<{bt},{fmt},dense>"
+    name = f"w4a16_kernel<{bt},{fmt},dense>"
+    return "act_quant_fp8_kernel + " + name if kind == "w4a8" else name
 
 
 EXTRA_WORKLOADS = ["w4a16_m16", "w4a8", "moe16", "moe256", "moe4096", "large"]

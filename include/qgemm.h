@@ -102,7 +102,12 @@ enum { QGEMM_ACT_NONE = 0, QGEMM_ACT_SILU_GLU = 1 };
  *                 number format and scaling differ from INT4's,
  *                 kinachrichten.com "Warum quantisierte Kernel wichtig sind") or
  *                 QGEMM_FP8E4M3 (W4A8; the caller passes e4m3 codes and
- *                 per-row fp32 scales from qgemm_quantize_act_fp8)
+ *                 per-row fp32 scales from qgemm_quantize_act_fp8) or
+ *                 QGEMM_BF16 with MXFP4 weights (W4A8 whose bf16 activations
+ *                 the library quantizes with the qgemm_quantize_act_fp8 rule:
+ *                 at m <= 16 inside the small-M kernel, above in a separate
+ *                 kernel into the workspace; results are bitwise those of the
+ *                 two-call form)
  *   out_dtype     output dtype: equal to act_dtype for W4A16, QGEMM_BF16 for W4A8
  *   has_bias      1: add bias[N] (out_dtype) in fp32 before the final rounding
  *   num_experts   1 for a dense layer, E for a grouped (MoE) layer
@@ -309,8 +314,10 @@ qgemm_status qgemm_workspace_init(void* workspace, size_t bytes, void* stream);
 /*
  * Dense quantized GEMM: C[m, n] = out_dtype(A[m, :] . W[:, n] (+ bias[n])).
  *   m         rows of A and C (0 is allowed and launches nothing)
- *   a         device, [m, K] in act_dtype (e4m3 codes for W4A8)
- *   a_scale   device fp32 [m] per-row activation scales (W4A8), else NULL
+ *   a         device, [m, K] in act_dtype (e4m3 codes for W4A8 with
+ *             act_dtype QGEMM_FP8E4M3)
+ *   a_scale   device fp32 [m] per-row activation scales (W4A8 with e4m3
+ *             activations), else NULL (also for W4A8 with bf16 activations)
  *   packed    device packed buffer from qgemm_pack_weights
  *   bias      device [N] in out_dtype, or NULL when has_bias = 0
  *   c         device, [m, N] in out_dtype ([m, N/2] for a gated layer)

@@ -188,17 +188,22 @@ class W4A8Linear:
     """A packed W4A8-MXFP4 layer: e2m1 codes uint8 [E*N, K/2] and e8m0 scales
     uint8 [E*N, K/32] in the standard format; activations are quantized per
     row to e4m3 by the library and the output is bf16 (gated=True: as for
-    W4A16Linear, silu(gate) * up of the two column halves, [rows, N/2])."""
+    W4A16Linear, silu(gate) * up of the two column halves, [rows, N/2]).
+    Calling the layer on bf16 activations is one library call (the layer
+    config with bf16 activations: the quantization runs inside the small-M
+    kernel, or as its own kernel ahead of the tcgen05 one); ``quantize`` and
+    ``run_quantized`` are the two-call form with caller-held e4m3 codes."""
 
     def __init__(self, codes, scales, n, k, num_experts=1, bias=None, tuning=None,
                  deterministic=False, gated=False, batch_invariant=False):
         self.n, self.k, self.num_experts = n, k, num_experts
         self.gated = gated
         self.n_out = n // 2 if gated else n
-        self.layer = Q.layer_config(n, k, 32, Q.QGEMM_W_MXFP4, Q.QGEMM_S_E8M0, Q.QGEMM_Z_NONE,
-                                    Q.QGEMM_FP8E4M3, Q.QGEMM_BF16,
-                                    1 if bias is not None else 0, num_experts,
-                                    Q.QGEMM_ACT_SILU_GLU if gated else Q.QGEMM_ACT_NONE)
+        cfg = (n, k, 32, Q.QGEMM_W_MXFP4, Q.QGEMM_S_E8M0, Q.QGEMM_Z_NONE)
+        tail = (Q.QGEMM_BF16, 1 if bias is not None else 0, num_experts,
+                Q.QGEMM_ACT_SILU_GLU if gated else Q.QGEMM_ACT_NONE)
+        self.layer = Q.layer_config(*cfg, Q.QGEMM_FP8E4M3, *tail)      # e4m3 activations
+        self.layer_bf16 = Q.layer_config(*cfg, Q.QGEMM_BF16, *tail)    # library-quantized
         st, nbytes = Q.qgemm_packed_size(self.layer)
         Q.check(st)
         dev = codes.device
@@ -234,6 +239,20 @@ class W4A8Linear:
         return out
 
     def __call__(self, x: torch.Tensor, out=None) -> torch.Tensor:
+        """x bf16 [M, K] -> bf16 [M, N] in one library call."""
+        x = x.contiguous()
+        m = x.shape[0]
+        if out is None:
+            out = torch.empty(m, self.n_out, dtype=torch.bfloat16, device=x.device)
+        st, nbytes = Q.qgemm_workspace_size(self.layer_bf16, self.dense, self.tuning, max(m, 1))
+        Q.check(st)
+        ws = self.ws.get(nbytes)
+        Q.check(Q.qgemm_run(self.layer_bf16, self.dense, self.tuning, m, x, None, self.packed,
+                            self.bias, out, ws, ws.numel()))
+        return out
+
+    def two_call(self, x: torch.Tensor, out=None) -> torch.Tensor:
+        """The same product through qgemm_quantize_act_fp8, then qgemm_run."""
         a8, sc = self.quantize(x.contiguous())
         return self.run_quantized(a8, sc, out)
 

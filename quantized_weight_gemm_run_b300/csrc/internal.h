@@ -29,7 +29,12 @@ constexpr int kMaxPermuteExperts = 256; // MoE permutation
 // Workspace layout (bytes): [0, 256) status word and padding; then `counters`
 // int32 per 32-column quarter of every output tile; then fp32 partial tiles, two per CTA.
 struct WorkspaceLayout {
-  size_t counters_off, counters_bytes, partials_off, partials_bytes, total;
+  size_t counters_off, counters_bytes, partials_off, partials_bytes;
+  // W4A8 with bf16 activations above the small-M kernel: the e4m3 codes
+  // [rows, K] and the per-row fp32 scales the library quantizes into (last,
+  // outside the part that must start zeroed; aq_bytes 0 otherwise)
+  size_t aq_off, aq_bytes, aq_scale_off;
+  size_t total;
 };
 
 WorkspaceLayout workspace_layout(int64_t max_tiles, int grid, int block_tok);
@@ -108,14 +113,22 @@ struct W4A16MmaParams {
   int ring;                  // weight slots per CTA
   int nk_max;                // most k-tiles in one slice
   int block_bytes, s_off, z_off, sg_shift, has_zp;
+  int mx;                    // 1: W4A8 (MXFP4 weights, e4m3 activations, bf16 output)
+  const float* a_scale;      // W4A8: per-row activation scales [m] (quant_act: unused)
+  int quant_act;             // W4A8: 1 = a is bf16 and the kernel quantizes it per row
   unsigned long long wait_limit_ns;
 };
-// tmap_a: activations as {64 k, m rows, K / 64 chunks}, 128-byte swizzle,
-// box {64, 8 or 16 rows, 2 nk_max chunks}
+// tmap_a: activations as {128 bytes of k, m rows, chunks}, 128-byte swizzle,
+// box {128 bytes, 8 or 16 rows, nk_max k-tiles of chunks} (16-bit, also bf16
+// activations that the kernel quantizes: 64 k per chunk, two chunks a k-tile;
+// e4m3: 128 k, one)
 cudaError_t launch_w4a16_mma(const CUtensorMap& tmap_a, const W4A16MmaParams& p, bool fp16,
                              cudaStream_t stream);
-// dynamic shared memory of one small-M CTA (rows: 8 for M <= 8, else 16)
-int mma_smem_bytes(int block_bytes, int ring, int nk_max, int rows);
+// dynamic shared memory of one small-M CTA (rows: 8 for M <= 8, else 16;
+// elem_bytes: 2 for 16-bit activations, 1 for e4m3; quant: bf16 activations
+// quantized to e4m3 in the kernel)
+int mma_smem_bytes(int block_bytes, int ring, int nk_max, int rows, int elem_bytes,
+                   bool quant = false);
 
 // Host-side plan for one W4A16 launch.
 int device_sm_count();

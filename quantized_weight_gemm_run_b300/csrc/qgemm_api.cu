@@ -163,8 +163,12 @@ static qgemm_status check_layer(const qgemm_layer_config* L) {
         return fail(QGEMM_ERR_UNSUPPORTED, "MXFP4 takes no zero points");
       if (L->scale_format != QGEMM_S_E8M0 || L->group_size != 32)
         return fail(QGEMM_ERR_UNSUPPORTED, "MXFP4 needs e8m0 scales per 32 k");
-      if (L->act_dtype != QGEMM_FP8E4M3 || L->out_dtype != QGEMM_BF16)
-        return fail(QGEMM_ERR_UNSUPPORTED, "MXFP4 runs against e4m3 activations, bf16 output");
+      // e4m3 activations with the caller's per-row scales, or bf16 ones that
+      // the library quantizes per row
+      if ((L->act_dtype != QGEMM_FP8E4M3 && L->act_dtype != QGEMM_BF16) ||
+          L->out_dtype != QGEMM_BF16)
+        return fail(QGEMM_ERR_UNSUPPORTED,
+                    "MXFP4 runs against e4m3 or bf16 activations, bf16 output");
       return ok();
     default:
       return fail(QGEMM_ERR_UNSUPPORTED, "unknown weight format %d", L->weight_format);
@@ -189,6 +193,10 @@ static int st_of(int group) { return group < kTileK ? kTileK / group : 1; }
 
 static bool is_mx(const qgemm_layer_config* L) { return L->weight_format == QGEMM_W_MXFP4; }
 static bool is_nv(const qgemm_layer_config* L) { return L->weight_format == QGEMM_W_NVFP4; }
+// W4A8 whose bf16 activations the library quantizes per row to e4m3
+static bool quant_in_lib(const qgemm_layer_config* L) {
+  return is_mx(L) && L->act_dtype == QGEMM_BF16;
+}
 static bool is_w8(const qgemm_layer_config* L) {
   return L->weight_format == QGEMM_W_INT8_SYM || L->weight_format == QGEMM_W_UINT8_ZP;
 }
@@ -224,7 +232,20 @@ WorkspaceLayout workspace_layout(int64_t max_tiles, int grid, int block_tok) {
   w.partials_off = w.counters_off + w.counters_bytes;
   w.partials_bytes = (size_t)2 * grid * block_tok * kTileN * sizeof(float);
   w.total = w.partials_off + w.partials_bytes;
+  w.aq_off = w.aq_scale_off = w.total;
+  w.aq_bytes = 0;
   return w;
+}
+
+// Appends the region of the library-quantized activations (rows x k e4m3
+// codes, then rows fp32 scales).
+static void add_act_quant_region(WorkspaceLayout* w, int64_t rows, int64_t k) {
+  const size_t codes = ((size_t)rows * (size_t)k + 255) & ~size_t(255);
+  const size_t scales = ((size_t)rows * sizeof(float) + 255) & ~size_t(255);
+  w->aq_off = w->total;
+  w->aq_scale_off = w->aq_off + codes;
+  w->aq_bytes = codes + scales;
+  w->total += w->aq_bytes;
 }
 
 static int heuristic_block_tok(int64_t rows_per_group) {
@@ -335,19 +356,20 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   if (ring > nk_max) ring = (int)nk_max;
   if (ring < 1) ring = 1;
   const int mma_smem =
-      s_ok ? mma_smem_bytes(packed_block_bytes(false, st, has_zp), ring, (int)nk_max,
-                            rows <= 8 ? 8 : 16)
+      s_ok ? mma_smem_bytes(packed_block_bytes(is_mx(L), st, has_zp), ring, (int)nk_max,
+                            rows <= 8 ? 8 : 16, is_mx(L) ? 1 : 2, quant_in_lib(L))
            : 0;
   const bool mma_fits = s_ok && nk_max <= 64 && mma_smem <= device_max_smem();
-  const bool mma_ok = !grouped && !is_mx(L) && !is_nv(L) && !is_f16s(L) && !is_w8(L) &&
+  const bool mma_ok = !grouped && !is_nv(L) && !is_f16s(L) && !is_w8(L) &&
                       L->gated_act == 0 && rows <= 16 && !(C && C->batch_invariant) &&
                       mma_fits;
   const int want = T ? T->kernel : 0;
   if (want == 2 && !mma_ok)
     return fail(QGEMM_ERR_UNSUPPORTED,
-                "the small-M kernel takes dense INT4/UINT4 GEMMs with m <= 16 whose scales are "
-                "in the activation dtype, that are not gated or batch-invariant, with split_k a "
-                "power of two <= 16 and <= k/128 and a slice that fits shared memory");
+                "the small-M kernel takes dense INT4/UINT4/INT3/UINT3 GEMMs with scales in the "
+                "activation dtype and W4A8-MXFP4 GEMMs, with m <= 16, not gated or "
+                "batch-invariant, split_k a power of two <= 16 and <= k/128 and a slice that "
+                "fits shared memory");
   P->kernel = 1;
   P->mma_splits = 0;
   // Heuristic: with no tuning field for the tcgen05 kernel set, the small-M
@@ -366,15 +388,18 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
     P->split_cap = 0;
     P->st = st;
     P->off_s = kTileBytes;
-    P->off_z = kTileBytes + packed_scale_bytes(false, st);
+    P->off_z = kTileBytes + packed_scale_bytes(is_mx(L), st);
     P->max_tiles = ntl;
-    // the status word only: the slices meet in distributed shared memory
+    // the status word only: the slices meet in distributed shared memory (and
+    // bf16 activations of a W4A8 layer are quantized inside the kernel)
     WorkspaceLayout w;
     w.counters_off = 256;
     w.counters_bytes = 0;
     w.partials_off = 256;
     w.partials_bytes = 0;
     w.total = 256;
+    w.aq_off = w.aq_scale_off = 256;
+    w.aq_bytes = 0;
     P->ws = w;
     return ok();
   }
@@ -427,6 +452,7 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   P->g = g;
   P->max_tiles = tiles_bound;
   P->ws = workspace_layout(tiles_bound, grid, bt);
+  if (quant_in_lib(L)) add_act_quant_region(&P->ws, rows, L->k);
   return ok();
 }
 
@@ -497,8 +523,12 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
     return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
   if (!L->has_bias && bias) return fail(QGEMM_ERR_INVALID_ARG, "bias given with has_bias = 0");
   const bool mx = is_mx(L);
-  if (mx && !a_scale)
+  const bool qa = quant_in_lib(L);
+  if (mx && !qa && !a_scale)
     return fail(QGEMM_ERR_INVALID_ARG, "the W4A8 path needs the per-row activation scales");
+  if (qa && a_scale)
+    return fail(QGEMM_ERR_INVALID_ARG,
+                "a_scale must be NULL with bf16 activations (the library computes the scales)");
   if (!mx && a_scale) return fail(QGEMM_ERR_INVALID_ARG, "a_scale is only used by the W4A8 path");
   if (!aligned16(a) || !aligned16(w) || !aligned16(c) || (bias && !aligned16(bias)) ||
       !aligned16(workspace))
@@ -528,7 +558,10 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
     q.ring = P.mma_ring;
     q.nk_max = P.mma_nk_max;
     q.wait_limit_ns = g_wait_limit_ns;
-    q.block_bytes = packed_block_bytes(false, P.st, has_zp);
+    q.block_bytes = packed_block_bytes(mx, P.st, has_zp);
+    q.mx = mx ? 1 : 0;
+    q.a_scale = a_scale;
+    q.quant_act = qa ? 1 : 0;
     q.s_off = P.off_s;
     q.z_off = P.off_z;
     q.sg_shift = L->group_size == 32 ? 0 : L->group_size == 64 ? 1 : 2;
@@ -537,19 +570,32 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
       cudaError_t ce = cudaMemsetAsync(workspace, 0, clear_bytes, stream);
       if (ce != cudaSuccess) return cuda_fail(ce, "workspace clear");
     }
-    // activations {64 k, rows, K / 64 chunks}: one box holds a slice's k-tiles
+    // activations {128 bytes of k, rows, K / 128-byte chunks}: one box holds a
+    // slice's k-tiles (16-bit: two chunks a k-tile; e4m3: one)
     CUtensorMap tmap_mma;
-    const uint64_t rb = (uint64_t)L->k * 2;
-    const uint64_t dims3[3] = {64, (uint64_t)rows, rb / 128};
+    const int eb = mx && !qa ? 1 : 2;
+    const uint64_t rb = (uint64_t)L->k * eb;
+    const uint64_t dims3[3] = {(uint64_t)(128 / eb), (uint64_t)rows, rb / 128};
     const uint64_t str3[2] = {rb, 128};
-    const uint32_t box3[3] = {64, (uint32_t)(rows <= 8 ? 8 : 16), (uint32_t)(2 * P.mma_nk_max)};
+    const uint32_t box3[3] = {(uint32_t)(128 / eb), (uint32_t)(rows <= 8 ? 8 : 16),
+                              (uint32_t)(eb * P.mma_nk_max)};
     if (!encode_tmap_3d(&tmap_mma,
-                        fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                        : fp16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         a, dims3, str3, box3, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the activation tensor");
     cudaError_t e = launch_w4a16_mma(tmap_mma, q, fp16, stream);
     if (e != cudaSuccess) return cuda_fail(e, "small-M GEMM launch");
     return ok();
+  }
+  // bf16 activations of a W4A8 layer: quantized per row into the workspace
+  // (launched with the GEMM below, after every check), then run as e4m3 ones
+  const void* a_bf16 = a;
+  if (qa) {
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    a = wsb + P.ws.aq_off;
+    a_scale = reinterpret_cast<const float*>(wsb + P.ws.aq_scale_off);
   }
   CUtensorMap tmap;
   // activation boxes [chunk][row][128 bytes]: the K axis split into 128-byte
@@ -664,6 +710,12 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
     cudaError_t ce = cudaMemsetAsync(workspace, 0, clear_bytes, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "workspace clear");
   }
+  if (qa) {   // the GEMM waits on this grid before it reads the codes and scales
+    cudaError_t qe = launch_act_quant_fp8(
+        static_cast<const uint16_t*>(a_bf16), rows, L->k,
+        static_cast<uint8_t*>(const_cast<void*>(a)), const_cast<float*>(a_scale), stream);
+    if (qe != cudaSuccess) return cuda_fail(qe, "activation quantization launch");
+  }
   cudaError_t e = launch_w4a16(tmap, tmap_c, p, P.bt, fmt, grouped, P.grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "W4A16 GEMM launch");
   return ok();
@@ -698,8 +750,9 @@ int dense_workspace_bytes(const void* layer, const void* compute, const void* tu
                  static_cast<const qgemm_compute_config*>(compute), m > 0 ? m : 1, false, &P);
   if (st != QGEMM_OK) return st;
   // the status word and tile counters start at zero, and so do the split-K
-  // accumulators of the atomic reduction
-  *must_clear = P.ws.total;
+  // accumulators of the atomic reduction (the quantized activations, last,
+  // are written in full before they are read)
+  *must_clear = P.ws.total - P.ws.aq_bytes;
   *total = P.ws.total;
   return QGEMM_OK;
 }
@@ -950,7 +1003,7 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
       snprintf(tmp, sizeof(tmp),
                "kernel=%s%s weights=%s group=%d scales=%s act=%s out=%s n=%lld k=%lld "
                "m=%lld experts=%d block_tok=%d act_slots=%d weight_slots=%dx%d grid=%d smem=%d "
-               "workspace=%zu epilogue=%s split=%s "
+               "workspace=%zu epilogue=%s split=%s act_quant=%s "
                "device=sm_103",
                P.kernel == 2 ? "w4a16_mma_sync_smallm"
                : is_mx(layer) ? "w4a8_tcgen05_mxf8f6f4_swapab" : "w4a16_tcgen05_swapab",
@@ -959,7 +1012,8 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
                (long long)layer->k, (long long)m, layer->num_experts, P.bt, P.g.x_stages,
                P.g.w_stages, P.g.rw, P.grid, P.g.smem, P.ws.total,
                layer->gated_act ? "silu_glu" : "plain",
-               P.kernel == 2 ? "k_slices" : P.split_cap == 1 ? "whole_tiles" : "stream_k");
+               P.kernel == 2 ? "k_slices" : P.split_cap == 1 ? "whole_tiles" : "stream_k",
+               !quant_in_lib(layer) ? "none" : P.kernel == 2 ? "fused" : "separate_kernel");
       rec = tmp;
     }
   }

@@ -44,6 +44,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -133,6 +134,35 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// D = A . B (fresh: C = 0), m16n8k32, e4m3 operands, fp32 result.
+__device__ __forceinline__ void mma16832_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Four e2m1 codes (bits 0-15 of c16, k in nibble order from the low end) ->
+// four e4m3 bytes in k order, exactly (every e2m1 value is an e4m3 value):
+// a byte-table lookup of the 3-bit magnitude's e4m3 byte, a sign-replicating
+// byte permute that turns each code's sign bit into bit 6 of its byte, and
+// one LOP3 that moves it to bit 7.  Only the selector's low 16 bits count.
+__device__ __forceinline__ uint32_t e2m1x4_e4m3(uint32_t c16) {
+  constexpr uint32_t kLo = 0x3C383000u;   // e4m3 of 0, 0.5, 1, 1.5
+  constexpr uint32_t kHi = 0x4C484440u;   // e4m3 of 2, 3, 4, 6
+  uint32_t mag, sgn, out;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(mag) : "r"(kLo), "r"(kHi), "r"(c16 & 0x7777u));
+  asm("prmt.b32 %0, %1, %1, %2;" : "=r"(sgn) : "r"(0x80808080u), "r"(c16));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(out) : "r"(sgn << 1), "r"(0x80808080u), "r"(mag));
+  return out;
+}
+
+// An e8m0 block scale 2^(b - 127) as fp32 (b = 0: the subnormal 2^-127).
+__device__ __forceinline__ float e8m0_f32(uint32_t b) {
+  return __uint_as_float(b ? b << 23 : 0x00400000u);
+}
+
 // L2 prefetch of a global range (16-byte aligned start, size a multiple of 16).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -165,22 +195,43 @@ __device__ __forceinline__ void st_async_f4(uint32_t dst, const float4& v, uint3
 // 2 nk_max chunks of 64 k x rows x 128 bytes, 128-byte swizzled, at offset 0
 // for the swizzle's 1 KB alignment), the weight ring, the receive buffer of
 // the reduction ([S][rows][128 / S] fp32), then barriers and counters.
-__host__ __device__ inline int mma_act_bytes(int nk_max, int rows) { return nk_max * rows * 256; }
+__host__ __device__ inline int mma_act_bytes(int nk_max, int rows, int elem_bytes) {
+  return nk_max * rows * kTileK * elem_bytes;
+}
 
-int mma_smem_bytes(int block_bytes, int ring, int nk_max, int rows) {
-  return 1024 /* alignment slack */ + mma_act_bytes(nk_max, rows) + ring * block_bytes +
-         rows * kTileN * 4 + 8 * (2 * ring + 2) + 16;
+int mma_smem_bytes(int block_bytes, int ring, int nk_max, int rows, int elem_bytes,
+                   bool quant) {
+  // quant: the bf16 box, then the e4m3 tile quantized from it, the partial
+  // row maxima of the S slices and the rows' scales
+  const int act = quant ? mma_act_bytes(nk_max, rows, 2) + mma_act_bytes(nk_max, rows, 1)
+                        : mma_act_bytes(nk_max, rows, elem_bytes);
+  return 1024 /* alignment slack */ + act + ring * block_bytes + rows * kTileN * 4 +
+         (quant ? (16 + 1) * rows * 4 : 0) + 8 * (2 * ring + 3) + 16;
 }
 
 // NB: n8 token blocks (1: M <= 8, 2: M <= 16).  ONE_GROUP: the group size is
-// >= 128, so one scale (and zero) per row serves the whole k-tile.
-template <bool FP16, int NB, bool ONE_GROUP>
+// >= 128, so one scale (and zero) per row serves the whole k-tile.  MX: W4A8
+// (MXFP4 weights against e4m3 activations with per-row fp32 scales, bf16
+// output): the codes become e4m3 bytes exactly, each 32-k block is one
+// m16n8k32 e4m3 MMA into a fresh fp32 partial, and the partial is added with
+// the block's scale 2^E (an exact power-of-two multiply) into the accumulator;
+// the per-row activation scale multiplies the finished sum.
+// QA (with MX): the activations arrive as bf16 and are quantized here, per
+// row to e4m3 with the fp32 scale max|x| / 448, exactly as the standalone
+// quantizer does: each CTA takes the maximum over its K slice, the cluster's S
+// slices exchange their maxima through distributed shared memory (the max is
+// exact, so every CTA derives the same scale), and each CTA quantizes its own
+// slice into the e4m3 tile the MMAs read.
+template <bool FP16, int NB, bool ONE_GROUP, bool MX, bool QA = false>
 __global__ void __launch_bounds__(kMmaThreads, 4)
     w4a16_mma_kernel(const __grid_constant__ CUtensorMap tmap_a, const W4A16MmaParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the swizzled activation box needs a 1 KB aligned start
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   constexpr int ROWS = 8 * NB;
+  static_assert(!QA || MX, "activation quantization serves the W4A8 path");
+  constexpr int AB = MX ? 1 : 2;   // bytes per activation element the MMAs read
+  constexpr int AIN = QA ? 2 : AB;  // bytes per activation element in HBM
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rg = warp;   // row group
   const int g = lane >> 2, t = lane & 3;
@@ -192,18 +243,24 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
   const int R = p.ring;
   const int BB = p.block_bytes;
   const int F = kTileN / S;        // features this CTA finishes
-  uint8_t* act = smem;
-  uint8_t* ring = smem + mma_act_bytes(p.nk_max, ROWS);
+  // QA: act16 is the bf16 box, act the e4m3 tile quantized from it
+  uint8_t* act16 = smem;
+  uint8_t* act = QA ? smem + mma_act_bytes(p.nk_max, ROWS, 2) : smem;
+  uint8_t* ring = act + mma_act_bytes(p.nk_max, ROWS, AB);
   float* recv = reinterpret_cast<float*>(ring + R * BB);          // [S][ROWS][F]
-  uint64_t* full = reinterpret_cast<uint64_t*>(recv + ROWS * kTileN);
+  float* amax_in = recv + ROWS * kTileN;          // QA: [S][ROWS] partial row maxima
+  float* row_scale = amax_in + (QA ? 16 * ROWS : 0);   // QA: [ROWS]
+  uint64_t* full = reinterpret_cast<uint64_t*>(row_scale + (QA ? ROWS : 0));
   uint64_t* empty = full + R;          // one arrival per warp when it is done with a slot
   uint64_t* act_full = empty + R;
   uint64_t* recv_full = act_full + 1;
-  int* issued = reinterpret_cast<int*>(recv_full + 1);   // weight blocks issued so far
+  uint64_t* amax_full = recv_full + 1;   // QA: the S slices' maxima have landed
+  int* issued = reinterpret_cast<int*>(amax_full + 1);   // weight blocks issued so far
   volatile int* abort_flag = issued + 1;
   const uint8_t* wsrc = p.w + ((long long)nt * p.kt + kt0) * BB;
   const int live = p.m < ROWS ? p.m : ROWS;
-  const uint16_t* asrc = p.a + (long long)kt0 * kTileK;   // row r at asrc + r * k
+  // row r of the slice's activations at asrc + r * k * AIN
+  const uint8_t* asrc = reinterpret_cast<const uint8_t*>(p.a) + (long long)kt0 * kTileK * AIN;
 
   if (tid == 0) {
     for (int s = 0; s < R; ++s) {
@@ -212,6 +269,7 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
     }
     mbar_init(act_full, 1);
     mbar_init(recv_full, 1);
+    mbar_init(amax_full, 1);
     fence_barrier_init();
     // the first weight blocks: issued before anything waits on the previous grid
     const int first = nk < R ? nk : R;
@@ -224,22 +282,23 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
     *abort_flag = 0;
     // the slices of the cluster's other CTAs (and this one's own) land here
     mbar_arrive_expect_tx(recv_full, (uint32_t)(S * live * F * 4));
+    if constexpr (QA) mbar_arrive_expect_tx(amax_full, (uint32_t)(S * live * 4));
     prefetch_tmap(&tmap_a);
   }
   // the activation rows: an L2 prefetch now (the previous grid may still be
   // writing them; L2 is where its writes land, so a prefetched line is never
   // stale), the copy into shared memory after the wait
   if (warp == 1 && lane < live)
-    prefetch_l2_bulk(asrc + (long long)lane * p.k, (uint32_t)nk * 256);
+    prefetch_l2_bulk(asrc + (long long)lane * p.k * AIN, (uint32_t)(nk * kTileK * AIN));
   __syncthreads();
   cluster_sync_all();   // every receive barrier of the cluster is armed
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) {
-    // one box: 2 nk_max chunks of 64 k x ROWS rows (rows past m and k past K
-    // read as zeros)
-    mbar_arrive_expect_tx(act_full, (uint32_t)mma_act_bytes(p.nk_max, ROWS));
-    tma_load_3d_hint(act, &tmap_a, act_full, 0, 0, 2 * kt0, policy_evict_first());
+    // one box: nk_max k-tiles (AIN 128-byte chunks each) x ROWS rows (rows
+    // past m and k past K read as zeros)
+    mbar_arrive_expect_tx(act_full, (uint32_t)mma_act_bytes(p.nk_max, ROWS, AIN));
+    tma_load_3d_hint(act16, &tmap_a, act_full, 0, 0, AIN * kt0, policy_evict_first());
   }
 
   float acc[2][2][NB][4];   // [k16 step parity][m16 block][n8 block]
@@ -260,6 +319,77 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
   const uint32_t a_row = smem_u32(act) + (uint32_t)(a_tok * 128);
   const int a_x = a_tok & 7, a_k8 = (lane >> 3) & 1;
   bool ok = mbar_wait(act_full, 0, abort_flag, p.status, p.wait_limit_ns, kStatusTimeout);
+  bool got_amax = true;
+  if constexpr (QA) {
+    // the slice's maximum |x| of each live row (the box may hold k-tiles of
+    // the next slice or zeros past K: a maximum is unchanged by either), sent
+    // to every CTA of the cluster (an aborted CTA sends too, so peers complete)
+    const int units = 2 * p.nk_max * 8;   // 16-byte units of a row in the box
+    for (int r = warp; r < live; r += kMmaWarps) {
+      float mx_ = 0.f;
+      for (int u = lane; u < units; u += 32) {
+        const uint4 v = *reinterpret_cast<const uint4*>(act16 + (u >> 3) * (ROWS * 128) +
+                                                        r * 128 + ((u & 7) << 4));
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          mx_ = fmaxf(mx_, fmaxf(fabsf(__uint_as_float(w4[i] << 16)),
+                                 fabsf(__uint_as_float(w4[i] & 0xFFFF0000u))));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx_ = fmaxf(mx_, __shfl_xor_sync(0xffffffffu, mx_, o));
+      if (lane < S) {
+        const uint32_t dst = map_to_rank(smem_u32(amax_in + sl * ROWS + r), (uint32_t)lane);
+        const uint32_t bar = map_to_rank(smem_u32(amax_full), (uint32_t)lane);
+        asm volatile(
+            "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst),
+            "r"(__float_as_uint(mx_)), "r"(bar)
+            : "memory");
+      }
+    }
+    got_amax = mbar_wait(amax_full, 0, abort_flag, p.status, p.wait_limit_ns, kStatusTimeout);
+    ok = ok && got_amax;
+    // the rows' scales: the maximum over the S slices, then max / 448 (1 for
+    // an all-zero row), an IEEE divide, as the standalone quantizer computes it
+    if (tid < ROWS) {
+      float s_ = 1.f;
+      if (tid < live) {
+        float a_ = 0.f;
+        for (int q = 0; q < S; ++q) a_ = fmaxf(a_, amax_in[q * ROWS + tid]);
+        s_ = a_ == 0.f ? 1.f : __fdiv_rn(a_, 448.f);
+      }
+      row_scale[tid] = s_;
+    }
+    __syncthreads();
+    // e4m3 codes of the box: 16 k (two bf16 units, one e4m3 unit) per item;
+    // rows past m stay zero
+    const int items = ROWS * p.nk_max * 8;
+    for (int i = tid; i < items; i += kMmaThreads) {
+      const int r = i % ROWS, rest = i / ROWS, v8 = rest & 7, kt = rest >> 3;
+      uint4 out = make_uint4(0u, 0u, 0u, 0u);
+      if (r < live) {
+        const float sc_ = row_scale[r];
+        const uint8_t* c16 = act16 + (2 * kt + (v8 >> 2)) * (ROWS * 128) + r * 128;
+        const int u0 = 2 * (v8 & 3);
+        const uint4 x0 = *reinterpret_cast<const uint4*>(c16 + ((u0 ^ (r & 7)) << 4));
+        const uint4 x1 = *reinterpret_cast<const uint4*>(c16 + (((u0 + 1) ^ (r & 7)) << 4));
+        const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        uint32_t ow[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t hb = (xw[e >> 1] >> (16 * (e & 1))) << 16;
+          const uint32_t code =
+              __nv_cvt_float_to_fp8(__fdiv_rn(__uint_as_float(hb), sc_), __NV_SATFINITE,
+                                    __NV_E4M3);
+          ow[e >> 2] |= code << (8 * (e & 3));
+        }
+        out = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      }
+      *reinterpret_cast<uint4*>(act + kt * (ROWS * 128) + r * 128 + ((v8 ^ (r & 7)) << 4)) =
+          out;
+    }
+    __syncthreads();
+  }
   int slot = 0;
   uint32_t phase = 0;
 #pragma unroll 1
@@ -270,6 +400,55 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
     }
     const uint8_t* blk = ring + slot * BB;
     const uint4* wv = reinterpret_cast<const uint4*>(blk);
+    if constexpr (MX) {
+      // per row r: the four e8m0 scales of the k-tile's 32-k blocks (byte j)
+      const uint32_t* sfw = reinterpret_cast<const uint32_t*>(blk + p.s_off);
+      uint32_t sf[2][2];
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) sf[b][e] = sfw[rg * 32 + b * 16 + g + 8 * e];
+      // the chunk (one per k-tile) of the e4m3 box; a 32-k block j is units
+      // 2j (k 0-15: fragment b0) and 2j + 1 (k 16-31: b1)
+      const uint32_t chunk = a_row + (uint32_t)(s * (ROWS * 128));
+      const int sh = 16 * (t & 1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t bf[4];
+        const uint32_t addr = chunk + (uint32_t)(((2 * j + a_k8) ^ a_x) * 16);
+        if constexpr (NB == 2) {
+          ldmatrix_x4(bf, addr);
+        } else {
+          uint32_t b2[2];
+          ldmatrix_x2(b2, addr);
+          bf[0] = b2[0];
+          bf[1] = b2[1];
+          bf[2] = bf[3] = 0u;
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          // rows g, g + 8: the row's 32 codes, 16 bytes; lane t takes the codes
+          // of k 4t..4t+3 (bytes 2t, 2t+1) and of k 16+4t.. (bytes 8+2t, 9+2t)
+          const uint4 v0 = wv[(rg * 4 + j) * 32 + b * 16 + g];
+          const uint4 v1 = wv[(rg * 4 + j) * 32 + b * 16 + g + 8];
+          const uint32_t lo0 = (t & 2) ? v0.y : v0.x, hi0 = (t & 2) ? v0.w : v0.z;
+          const uint32_t lo1 = (t & 2) ? v1.y : v1.x, hi1 = (t & 2) ? v1.w : v1.z;
+          const uint32_t af[4] = {e2m1x4_e4m3(lo0 >> sh), e2m1x4_e4m3(lo1 >> sh),
+                                  e2m1x4_e4m3(hi0 >> sh), e2m1x4_e4m3(hi1 >> sh)};
+          const float s0 = e8m0_f32((sf[b][0] >> (8 * j)) & 0xFFu);
+          const float s1 = e8m0_f32((sf[b][1] >> (8 * j)) & 0xFFu);
+#pragma unroll
+          for (int c = 0; c < NB; ++c) {
+            float d[4];
+            mma16832_e4m3(d, af, bf[2 * c], bf[2 * c + 1]);
+            acc[j & 1][b][c][0] = fmaf(d[0], s0, acc[j & 1][b][c][0]);
+            acc[j & 1][b][c][1] = fmaf(d[1], s0, acc[j & 1][b][c][1]);
+            acc[j & 1][b][c][2] = fmaf(d[2], s1, acc[j & 1][b][c][2]);
+            acc[j & 1][b][c][3] = fmaf(d[3], s1, acc[j & 1][b][c][3]);
+          }
+        }
+      }
+    } else {
     const uint16_t* sv = reinterpret_cast<const uint16_t*>(blk + p.s_off);
     const uint8_t* zv = blk + p.z_off;
     // per-row scale and zero pairs of rows (b, g) and (b, g + 8), group sg
@@ -342,6 +521,7 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
           if constexpr (NB == 2) mma16816<FP16>(acc[h][b][1], x[b][h], bf[h][2], bf[h][3]);
         }
     }
+    }   // 16-bit path
     // a ring shorter than the slice: every warp releases the slot, and warp
     // s % 4 refills it with block s + R once all four have
     if (R < nk) {
@@ -374,6 +554,7 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
     for (int s = n_issued - R < 0 ? 0 : n_issued - R; s < n_issued; ++s)
       mbar_wait(&full[s % R], (uint32_t)((s / R) & 1), &no_abort, nullptr, kDrainLimitNs, 0);
     mbar_wait(act_full, 0, &no_abort, nullptr, kDrainLimitNs, 0);
+    if (QA && !got_amax) mbar_wait(amax_full, 0, &no_abort, nullptr, kDrainLimitNs, 0);
   }
   __syncthreads();
 
@@ -415,6 +596,11 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
         o[3] += v.w;
       }
       const int n = nt * kTileN + sl * F + off;
+      if constexpr (MX) {   // the row's activation scale multiplies the fp32 sum
+        const float as = QA ? row_scale[tk] : p.a_scale[tk];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] *= as;
+      }
       if (p.bias) {
         const uint2 bb = *reinterpret_cast<const uint2*>(p.bias + n);
         const uint32_t bw[2] = {bb.x, bb.y};
@@ -447,10 +633,10 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
   }
 }
 
-template <bool FP16, int NB, bool ONE>
+template <bool FP16, int NB, bool ONE, bool MX = false, bool QA = false>
 static cudaError_t launch_one(const CUtensorMap& tmap, const W4A16MmaParams& p, int smem,
                               cudaStream_t stream) {
-  auto kern = w4a16_mma_kernel<FP16, NB, ONE>;
+  auto kern = w4a16_mma_kernel<FP16, NB, ONE, MX, QA>;
   static int smem_set = 0;
   static bool nonportable_set = false;
   if (smem > smem_set) {
@@ -484,7 +670,14 @@ cudaError_t launch_w4a16_mma(const CUtensorMap& tmap, const W4A16MmaParams& p, b
                              cudaStream_t stream) {
   const bool one = p.sg_shift == 2;   // group >= 128
   const int nb = p.m <= 8 ? 1 : 2;
-  const int smem = mma_smem_bytes(p.block_bytes, p.ring, p.nk_max, 8 * nb);
+  const int smem =
+      mma_smem_bytes(p.block_bytes, p.ring, p.nk_max, 8 * nb, p.mx ? 1 : 2, p.quant_act != 0);
+  if (p.mx && p.quant_act)
+    return nb == 1 ? launch_one<false, 1, true, true, true>(tmap, p, smem, stream)
+                   : launch_one<false, 2, true, true, true>(tmap, p, smem, stream);
+  if (p.mx)
+    return nb == 1 ? launch_one<false, 1, true, true>(tmap, p, smem, stream)
+                   : launch_one<false, 2, true, true>(tmap, p, smem, stream);
   if (fp16) {
     if (nb == 1) return one ? launch_one<true, 1, true>(tmap, p, smem, stream)
                             : launch_one<true, 1, false>(tmap, p, smem, stream);
