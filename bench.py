@@ -297,6 +297,10 @@ class GemmPoint:
     def copy_out(self):
         self.c_host.copy_(self.c, non_blocking=True)
 
+    def status(self):
+        """The library status of this point's launches so far (and clears it)."""
+        return self.Q.qgemm_check_status(self.ws)
+
 
 class MoEPoint:
     """One grouped-MoE W4A16 layer (E=64, top-8, hidden 2048, intermediate
@@ -350,6 +354,10 @@ class MoEPoint:
 
     def copy_out(self):
         self.y_host.copy_(self.y, non_blocking=True)
+
+    def status(self):
+        st1, st2 = self.l1.status(), self.l2.status()
+        return st1 if st1 != self.Q.QGEMM_OK else st2
 
     @property
     def a(self):
@@ -518,6 +526,7 @@ def measure_point(bp, p, peaks, stream):
     copies = [bp] + ([] if is_moe else [bp.clone() for _ in range(cold_copies(p) - 1)])
     r = max(20, len(copies))
     med, lo, hi = graph_time_us(lambda j: copies[j % len(copies)].launch(), r, stream)
+    bad = sum(1 for c in {id(c): c for c in copies}.values() if c.status() != 0)
     del copies
     torch.cuda.empty_cache()
     fl, by = point_flops(p), point_bytes(p)
@@ -525,6 +534,9 @@ def measure_point(bp, p, peaks, stream):
              us_max=round(hi, 3), tflops=round(fl / med / 1e6, 2),
              gbs=round(by / med / 1e3, 1), hbm_frac=round(by / med / 1e3 / peaks["hbm_gbs"], 3),
              kernel=kernel_name(p))
+    if bad:   # a kernel gave up a bounded wait: the time is not a valid measurement
+        d["kernel_timeouts"] = bad
+        print(f"warning: {bad} workspace(s) of point {p} report a timeout", file=sys.stderr)
     if p.get("kind") == "w4a8":
         fp8 = peaks.get("fp8_tflops")
         d["fp8_tensor_frac"] = round(fl / med / 1e6 / fp8, 3) if fp8 else None
@@ -643,6 +655,11 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
+    # a kernel that gave up a bounded wait makes the step time invalid
+    step_timeouts = sum(1 for gm in {id(g): g for g in gemms}.values() if gm.status() != 0)
+    if step_timeouts:
+        print(f"warning: {step_timeouts} workspace(s) of the timed step report a timeout",
+              file=sys.stderr)
     ms_total = e0.elapsed_time(e1)
     ms_total = reduce_max(ms_total, world)
     flops_step = sum(point_flops(gm.p) for gm in gemms)
@@ -803,6 +820,7 @@ def run_ours(args, rank, world, device):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": sum(gm.launches for gm in gemms) * args.steps,
         "clocks": clk,
+        "kernel_timeouts": step_timeouts,
     }
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(pts) if not args.no_cpu else None

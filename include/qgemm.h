@@ -173,19 +173,27 @@ typedef struct {
  *              dtype only; one accumulator buffer)
  *   stages     shared-memory pipeline depth (2 .. 16)
  *   max_ctas   upper bound on the persistent grid (<= number of SMs)
- *   split_k    0 = the heuristic's choice (without max_ctas: whole tiles or
- *              stream-K, by a cost model of the split; with max_ctas:
- *              stream-K); s = 1..64:
+ *   split_k    0 = the heuristic's choice (without max_ctas: whole tiles,
+ *              stream-K or, for a dense GEMM, the cluster split, by a cost
+ *              model of each; with max_ctas: stream-K); s = 1..64:
  *              the tiles left over after the whole waves are each split
  *              across min(s, grid / tiles left) CTAs at k-tile boundaries
  *              (1 = never split a tile's K range)
  *   cta_pair   reserved, must be 0
- *   kernel     0 = the heuristic's choice, 1 = the persistent tcgen05 kernel,
- *              2 = the small-M kernel (cp.async + mma.sync, split K; dense
- *              INT4 / UINT4 with scales in the activation dtype and m <= 16
- *              only, not gated, deterministic or batch-invariant; split_k,
- *              when set, is its number of K slices per n-tile; it ignores
- *              the other tuning fields)
+ *   kernel     0 = the heuristic's choice, 1 = the tcgen05 kernel,
+ *              2 = the small-M kernel (bulk-copied weights, mma.sync, K
+ *              slices reduced inside a thread-block cluster; dense INT4 /
+ *              UINT4 / INT3 / UINT3 with scales in the activation dtype and
+ *              W4A8-MXFP4, m <= 16 only, not gated or batch-invariant;
+ *              split_k, when set, is its number of K slices per n-tile, a
+ *              power of two <= 16; stages its weight slots; it ignores the
+ *              other fields),
+ *              3 = the tcgen05 kernel with the cluster split (dense, not
+ *              batch-invariant, block_tok <= 128, max_ctas 0): each output
+ *              tile's K range in split_k slices (2..8, <= K/128; 0 = the
+ *              heuristic's count), one CTA each, the slices of a tile summed
+ *              in a fixed order through distributed shared memory, so the
+ *              bits repeat from call to call
  */
 typedef struct {
   int32_t block_tok;

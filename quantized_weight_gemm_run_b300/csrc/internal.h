@@ -23,6 +23,20 @@ __host__ __device__ constexpr int weight_units_per_slot(int bt) { return bt <= 3
 constexpr int kEpiStageBytes = 4 * 2 * 16 * 32 * 2;   // output staging: 4 warps x 2 x 16 x 32
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusDevice = 2;
+// With kStatusTimeout, the tcgen05 kernel also sets the bit of the wait that
+// gave up first in its CTA (bits 8 and up), for the error message.
+constexpr int kSiteWeightSlot = 1 << 8;     // weight producer: a free weight slot
+constexpr int kSiteActSlot = 1 << 9;        // activation producer: a free activation slot
+constexpr int kSiteScaleFactors = 1 << 10;  // MMA: the W4A8 B scale factors
+constexpr int kSiteAccEmpty = 1 << 11;      // MMA: a free accumulator
+constexpr int kSiteActFull = 1 << 12;       // MMA: activations landed
+constexpr int kSiteDequantFull = 1 << 13;   // MMA: a dequantized weight tile
+constexpr int kSiteWeightFull = 1 << 14;    // dequant: weights landed
+constexpr int kSiteTmemSlot = 1 << 15;      // dequant: a free tensor-memory slot
+constexpr int kSiteAccFull = 1 << 16;       // epilogue: a finished accumulator
+constexpr int kSiteClusterRecv = 1 << 17;   // epilogue: the cluster peers' slices
+constexpr int kSiteSplitCount = 1 << 18;    // split-K finisher: the contributors' count
+constexpr int kSiteSplitCopy = 1 << 19;     // split-K finisher: the copied sum
 constexpr int kMaxExperts = 1024;      // grouped GEMM
 constexpr int kMaxPermuteExperts = 256; // MoE permutation
 
@@ -94,6 +108,10 @@ struct W4A16Params {
   int sk_t, sk_w, sk_u, sk_gs;
   FastDiv div_kt, div_nt, div_gs, div_u;
   int smem_bytes;            // total dynamic shared memory
+  // cluster split (dense): S > 1 CTAs per tile in clusters of S, one K slice
+  // each, reduced through distributed shared memory into receive slots at
+  // off_recv; 0 otherwise
+  int cluster, off_recv;
   unsigned long long wait_limit_ns;
 };
 
@@ -129,6 +147,11 @@ cudaError_t launch_w4a16_mma(const CUtensorMap& tmap_a, const W4A16MmaParams& p,
 // quantized to e4m3 in the kernel)
 int mma_smem_bytes(int block_bytes, int ring, int nk_max, int rows, int elem_bytes,
                    bool quant = false);
+
+// Clusters of S CTAs of the dense tcgen05 kernel (token tile bt, format fmt,
+// smem bytes of dynamic shared memory) that can be resident at once; 0 if
+// unknown.
+int w4a16_max_clusters(int bt, int fmt, int S, int smem);
 
 // Host-side plan for one W4A16 launch.
 int device_sm_count();

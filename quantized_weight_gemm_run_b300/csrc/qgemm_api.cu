@@ -13,6 +13,7 @@
 // compatibility example"): representation, activation type, device and shape,
 // and which implementation serves them.
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -215,6 +216,16 @@ static bool is_f16s(const qgemm_layer_config* L) {
          L->act_dtype == QGEMM_BF16;
 }
 
+// The tcgen05 kernel's format instantiation (see launch_w4a16).
+static int fmt_of(const qgemm_layer_config* L) {
+  const bool fp16 = L->act_dtype == QGEMM_FP16;
+  if (is_mx(L)) return 2;
+  if (is_nv(L)) return fp16 ? 4 : 3;
+  if (is_f16s(L)) return 5;
+  if (is_w8(L)) return fp16 ? 7 : 6;
+  return fp16 ? 1 : 0;
+}
+
 // Bytes of one expert's packed blocks (an NVFP4 buffer adds the tensor-scale
 // tail after the last expert).
 static size_t expert_packed_bytes(const qgemm_layer_config* L) {
@@ -262,23 +273,25 @@ static int heuristic_block_tok(int64_t rows_per_group) {
 // activation ring gets enough slots to cover a copy's latency at the tensor
 // rate; the weight ring gets the rest of shared memory (at most w_cap slots),
 // since it is what streams from HBM at small M.
+// A cluster-split launch adds the receive slots of the other slices
+// (recv_bytes) after the staging buffers.
 struct Geometry {
-  int x_bytes, x_stages, w_bytes, w_stages, rw, off_w, off_epi, off_bar, smem;
+  int x_bytes, x_stages, w_bytes, w_stages, rw, off_w, off_epi, off_recv, off_bar, smem;
 };
 
 static int tail_smem(int sx, int sw, int experts) {
-  return (2 * sx + 2 * sw + 2 * kASlots + 4 + 2 + 4) * 8 + 32 + 2 * (experts + 1) * 4 + 64;
+  return (2 * sx + 2 * sw + 2 * kASlots + 4 + 2 + 4 + 1) * 8 + 32 + 2 * (experts + 1) * 4 + 64;
 }
 
 static bool make_geometry(int bt, int st, int has_zp, bool mx, bool w8, int experts, int w_cap,
-                          int smem_cap, Geometry* g) {
+                          int smem_cap, int recv_bytes, Geometry* g) {
   const int rx = units_per_stage(bt);
   g->rw = weight_units_per_slot(bt);
   g->x_bytes = (rx * bt * kTileK * (mx ? 1 : 2) + 1023) & ~1023;
   g->w_bytes = g->rw * packed_block_bytes(mx, st, has_zp != 0, w8);
   for (int sx = bt <= 32 ? 3 : 4; sx >= 2; --sx) {
     const int fixed = 1024 /* alignment slack */ + sx * g->x_bytes + 1023 + kEpiStageBytes +
-                      tail_smem(sx, 16, experts);
+                      recv_bytes + tail_smem(sx, 16, experts);
     int sw = (smem_cap - fixed) / g->w_bytes;
     if (sw > w_cap) sw = w_cap;
     if (sw < 2) continue;
@@ -286,7 +299,8 @@ static bool make_geometry(int bt, int st, int has_zp, bool mx, bool w8, int expe
     g->w_stages = sw;
     g->off_w = sx * g->x_bytes;
     g->off_epi = (g->off_w + sw * g->w_bytes + 1023) & ~1023;
-    g->off_bar = g->off_epi + kEpiStageBytes;
+    g->off_recv = g->off_epi + kEpiStageBytes;
+    g->off_bar = g->off_recv + recv_bytes;
     g->smem = 1024 + g->off_bar + tail_smem(sx, sw, experts);
     if (g->smem <= smem_cap) return true;
   }
@@ -300,6 +314,7 @@ struct Plan {
   int mma_nk_max;    // small-M kernel: most k-tiles in one slice
   int bt, grid, st, off_s, off_z;
   int split_cap;     // most CTAs sharing one tile's K range (0: no cap, 1: whole tiles)
+  int cluster;       // tcgen05 kernel: S > 1 = cluster split of S CTAs per tile, else 0
   Geometry g;
   int64_t max_tiles;
   WorkspaceLayout ws;
@@ -329,8 +344,8 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
     return fail(QGEMM_ERR_INVALID_ARG, "split_k must be in [0, 64]");
   const int st = st_of(L->group_size);
   const int has_zp = has_zeros(L);
-  if (T && (T->kernel < 0 || T->kernel > 2))
-    return fail(QGEMM_ERR_INVALID_ARG, "kernel must be 0, 1 or 2");
+  if (T && (T->kernel < 0 || T->kernel > 3))
+    return fail(QGEMM_ERR_INVALID_ARG, "kernel must be 0, 1, 2 or 3");
   const int64_t ntl = L->n / kTileN, ktl = L->k / kTileK;
   // small-M kernel: K slices per n-tile (a power of two, at most 16 and at
   // most the k-tiles), and weight slots per CTA
@@ -406,7 +421,7 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   const int w_cap = (T && T->stages) ? T->stages : 16;
   if (w_cap < 2 || w_cap > 16) return fail(QGEMM_ERR_INVALID_ARG, "stages must be in [2, 16]");
   Geometry g;
-  if (!make_geometry(bt, st, has_zp, is_mx(L), is_w8(L), E, w_cap, device_max_smem(), &g))
+  if (!make_geometry(bt, st, has_zp, is_mx(L), is_w8(L), E, w_cap, device_max_smem(), 0, &g))
     return fail(QGEMM_ERR_UNSUPPORTED, "tile does not fit shared memory");
   const int64_t kt = L->k / kTileK, nt = L->n / kTileN;
   int64_t tiles_bound;
@@ -443,15 +458,86 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
     if (cap > 0 && tiles_bound * cap < grid)
       grid = (int)(tiles_bound > 0 ? tiles_bound * cap : 1);
   }
+  // Cluster split: each tile's K range in S slices, one CTA each, the S CTAs
+  // of a tile in one cluster summing their slices through distributed shared
+  // memory (no workspace round trip, no wait on another tile's CTAs).
+  // tuning.kernel = 3 asks for it (split_k = S, or 0 for the heuristic's);
+  // otherwise the heuristic takes it for a dense GEMM when the tiles x S CTAs
+  // fit the device at once and its estimate beats the persistent schedule's.
+  const bool want_cl = T && T->kernel == 3;
+  const bool cl_allowed = !grouped && !(C && C->batch_invariant) && bt <= 128 &&
+                          !(T && T->max_ctas > 0) && tiles_bound > 0;
+  if (want_cl && !cl_allowed)
+    return fail(QGEMM_ERR_UNSUPPORTED,
+                "the cluster split takes dense GEMMs with block_tok <= 128, not batch-invariant, "
+                "without max_ctas");
+  const int s_fixed = want_cl ? T->split_k : 0;
+  if (want_cl && s_fixed != 0 && (s_fixed < 2 || s_fixed > 8 || s_fixed > kt))
+    return fail(QGEMM_ERR_UNSUPPORTED, "a cluster split_k must be in [2, 8] and <= k/128");
+  int cl = 0;
+  Geometry gc;
+  if (cl_allowed && (want_cl || !(T && T->split_k > 0))) {
+    int S = s_fixed ? s_fixed
+                    : (int)std::min<int64_t>(std::min<int64_t>(8, kt),
+                                             std::max<int64_t>(1, sms / tiles_bound));
+    for (; S >= 2; --S) {
+      const int nu = (4 * (bt / 16) + S - 1) / S;   // 16-row chunks this CTA finishes
+      if (!make_geometry(bt, st, has_zp, is_mx(L), is_w8(L), E, w_cap, device_max_smem(),
+                         nu * (S - 1) * 2048, &gc)) {
+        if (s_fixed) break;
+        continue;
+      }
+      // a forced split may take several waves; the heuristic's must fit at once
+      if (want_cl || tiles_bound <= w4a16_max_clusters(bt, fmt_of(L), S, gc.smem)) {
+        cl = S;
+        break;
+      }
+      if (s_fixed) break;
+    }
+    if (want_cl && cl == 0)
+      return fail(QGEMM_ERR_UNSUPPORTED, "no cluster split of this tile fits shared memory");
+    if (cl && !want_cl) {
+      // Heuristic: per-CTA k-tiles at the measured per-k-tile cost (above),
+      // plus ~1 us for the exchange and the rank-ordered sums, against the
+      // persistent schedule's whole waves or stream-K with its split cost.
+      const double c = bt == 16 ? 0.30 : bt == 32 ? 0.33 : bt == 64 ? 0.38 : 0.47;
+      const double split = bt == 16 ? 2.5 : bt == 32 ? 3.0 : bt == 64 ? 4.5 : 7.0;
+      const int64_t G = grid, Tt = tiles_bound;
+      const double whole = (double)((Tt + G - 1) / G) * kt * c;
+      int64_t W = Tt / G;
+      if (W > 0 && Tt % G) --W;
+      const double sk = ((double)W * kt + (double)(Tt - W * G) * kt / (double)G) * c + split;
+      const double t_sk = cap == 1 ? whole : std::min(whole, sk);
+      const double t_cl = (double)((kt + cl - 1) / cl) * c + 1.0;
+      if (!(t_cl < t_sk)) cl = 0;
+    }
+    if (cl) {
+      g = gc;
+      cap = cl;
+      grid = (int)(tiles_bound * cl);
+    }
+  }
   P->bt = bt;
   P->grid = grid;
   P->split_cap = cap;
+  P->cluster = cl;
   P->st = st;
   P->off_s = packed_code_bytes(is_w8(L));                  // inside a packed block
   P->off_z = P->off_s + packed_scale_bytes(is_mx(L), st);
   P->g = g;
   P->max_tiles = tiles_bound;
-  P->ws = workspace_layout(tiles_bound, grid, bt);
+  if (cl) {
+    // the status word only: the slices meet in distributed shared memory
+    WorkspaceLayout w;
+    w.counters_off = w.partials_off = 256;
+    w.counters_bytes = w.partials_bytes = 0;
+    w.total = 256;
+    w.aq_off = w.aq_scale_off = 256;
+    w.aq_bytes = 0;
+    P->ws = w;
+  } else {
+    P->ws = workspace_layout(tiles_bound, grid, bt);
+  }
   if (quant_in_lib(L)) add_act_quant_region(&P->ws, rows, L->k);
   return ok();
 }
@@ -655,6 +741,8 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   p.off_w = P.g.off_w;
   p.off_epi = P.g.off_epi;
   p.off_bar = P.g.off_bar;
+  p.off_recv = P.g.off_recv;
+  p.cluster = P.cluster;
   p.smem_bytes = P.g.smem;
   // several token tiles per weight block: keep weights in L2 rather than
   // marking them first to evict
@@ -701,11 +789,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   if (!encode_tmap_2d(&tmap_c, CU_TENSOR_MAP_DATA_TYPE_UINT16, c, n_out, (uint64_t)rows,
                       n_out * 2, p.gated ? 16 : 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
     return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for the output tensor");
-  int fmt = fp16 ? 1 : 0;
-  if (mx) fmt = 2;
-  else if (is_nv(L)) fmt = fp16 ? 4 : 3;
-  else if (is_f16s(L)) fmt = 5;
-  else if (is_w8(L)) fmt = fp16 ? 7 : 6;
+  const int fmt = fmt_of(L);
   if (clear_bytes) {
     cudaError_t ce = cudaMemsetAsync(workspace, 0, clear_bytes, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "workspace clear");
@@ -972,7 +1056,8 @@ qgemm_status qgemm_check_status(void* workspace, void* stream) {
     const int zero = 0;
     e = cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "status clear");
-    if (word & kStatusTimeout) return fail(QGEMM_ERR_TIMEOUT, "a kernel gave up a bounded wait");
+    if (word & kStatusTimeout)
+      return fail(QGEMM_ERR_TIMEOUT, "a kernel gave up a bounded wait (status 0x%x)", word);
     return fail(QGEMM_ERR_DEVICE, "a kernel reported inconsistent inputs (status %d)", word);
   }
   return ok();
@@ -1012,7 +1097,16 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
                (long long)layer->k, (long long)m, layer->num_experts, P.bt, P.g.x_stages,
                P.g.w_stages, P.g.rw, P.grid, P.g.smem, P.ws.total,
                layer->gated_act ? "silu_glu" : "plain",
-               P.kernel == 2 ? "k_slices" : P.split_cap == 1 ? "whole_tiles" : "stream_k",
+               P.kernel == 2     ? "k_slices"
+               : P.cluster > 1   ? (P.cluster == 2   ? "cluster_k2"
+                                    : P.cluster == 3 ? "cluster_k3"
+                                    : P.cluster == 4 ? "cluster_k4"
+                                    : P.cluster == 5 ? "cluster_k5"
+                                    : P.cluster == 6 ? "cluster_k6"
+                                    : P.cluster == 7 ? "cluster_k7"
+                                                     : "cluster_k8")
+               : P.split_cap == 1 ? "whole_tiles"
+                                  : "stream_k",
                !quant_in_lib(layer) ? "none" : P.kernel == 2 ? "fused" : "separate_kernel");
       rec = tmp;
     }

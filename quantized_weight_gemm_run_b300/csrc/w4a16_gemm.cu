@@ -45,6 +45,10 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -474,7 +478,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint64_t* drain = acc_empty + 2;
   uint64_t* sfb_ready = drain + 1;
   uint64_t* fix_bar = sfb_ready + 1;   // one per epilogue warp: split-K sum copied in
-  SharedState* sh = reinterpret_cast<SharedState*>(fix_bar + 4);
+  uint64_t* recv_full = fix_bar + 4;   // cluster split: the peers' slices have landed
+  SharedState* sh = reinterpret_cast<SharedState*>(recv_full + 1);
   int* mt_prefix = reinterpret_cast<int*>(sh + 1);     // grouped: m-tile prefix [E+1]
   int* offs = mt_prefix + (GROUPED ? (p.num_experts + 1) : 0);   // grouped: offsets [E+1]
 
@@ -538,7 +543,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // barrier initialization spread over the warp's lanes: lane i sets up
     // barrier i of the contiguous array (arrival counts by the array it is in);
     // a dense GEMM's first weight slot barriers are set up already
-    const int nb = 2 * SX + 2 * SW + 2 * kASlots + 4 + 2 + 4;
+    const int nb = 2 * SX + 2 * SW + 2 * kASlots + 4 + 2 + 4 + 1;
     for (int i = lane; i < nb; i += 32) {
       if (!GROUPED && (i == 2 * SX || i == 2 * SX + SW)) continue;
       uint32_t count = 1;
@@ -553,6 +558,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     if (lane == 0) sh->abort_flag = 0;
     fence_barrier_init();
+    if (!GROUPED && p.cluster > 1) {
+      // cluster split: this CTA finishes the 16-row chunks u = 32 q / 16 +
+      // chunk with u % S == its rank and receives the S - 1 other slices of
+      // each (2 KB apiece; chunks past the tile's rows are not sent)
+      __syncwarp();
+      if (lane == 0) {
+        const int S = p.cluster, sl = (int)(blockIdx.x % (unsigned)S);
+        const int tile = (int)(blockIdx.x / (unsigned)S);
+        const int rows = min(BT, p.rows - fdiv(tile, p.div_nt) * BT);
+        const int nlive = (rows + 15) / 16;
+        int owned = 0;
+        for (int u = 0; u < 4 * (BT / 16); ++u)
+          if (u % S == sl && u % (BT / 16) < nlive) ++owned;
+        mbar_arrive_expect_tx(recv_full, (uint32_t)(owned * (S - 1) * 2048));
+      }
+    }
   }
   if (warp == 2) {
     tmem_alloc(&sh->tmem_base, 512);
@@ -619,6 +640,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     asm volatile("bar.sync 1, %0;" ::"n"(kNumThreads) : "memory");
   }
   tc_fence_after();
+  // cluster split: every receive barrier of the cluster is set up once this
+  // barrier phase completes (waited for before the first send)
+  bool cl_waited = false;
+  if (!GROUPED && p.cluster > 1) cluster_arrive();
   const uint32_t tmem_base = (!GROUPED && warp == 0) ? 0u : sh->tmem_base;
   const long long T = (!GROUPED && warp == 0)
                           ? (long long)((p.rows + BT - 1) / BT) * p.nt
@@ -653,13 +678,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                              ((long long)tc.nt * p.kt + wi.k0) * blk_bytes;
         for (int kt = wi.k0; kt < wi.k1; kt += RW) {
           const int r = min(RW, wi.k1 - kt);
-          if (!mbar_wait(&w_empty[ws], wph ^ 1, abort_flag, p.status, lim, kStatusTimeout)) {
-            ok = false;
-            break;
-          }
           if (skip_first) {
-            skip_first = false;   // went out at the start of the kernel
+            // went out at the start of the kernel.  No wait for the slot: the
+            // dequant warps may have consumed and released it already, and
+            // the release completes the slot's first phase, so a wait for
+            // "free" here would wait for its second release instead
+            skip_first = false;
           } else {
+            if (!mbar_wait(&w_empty[ws], wph ^ 1, abort_flag, p.status, lim,
+                           kStatusTimeout | kSiteWeightSlot)) {
+              ok = false;
+              break;
+            }
             mbar_arrive_expect_tx(&w_full[ws], r * blk_bytes);
             bulk_load(w_base + ws * p.w_bytes, src + (long long)(kt - wi.k0) * blk_bytes,
                       r * blk_bytes, &w_full[ws], pol);
@@ -687,7 +717,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       while (ok && sched.next(wi)) {
         const TileCoord<BT> tc = coords(wi.tile);
         for (int kt = wi.k0; kt < wi.k1; kt += RX) {
-          if (!mbar_wait(&x_empty[xs], xph ^ 1, abort_flag, p.status, lim, kStatusTimeout)) {
+          if (!mbar_wait(&x_empty[xs], xph ^ 1, abort_flag, p.status, lim, kStatusTimeout | kSiteActSlot)) {
             ok = false;
             break;
           }
@@ -713,22 +743,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       WorkItem wi;
       bool ok = true;
       if constexpr (MX)   // the B scale factors (all 1.0) are written by the epilogue warps
-        ok = mbar_wait(sfb_ready, 0, abort_flag, p.status, lim, kStatusTimeout);
+        ok = mbar_wait(sfb_ready, 0, abort_flag, p.status, lim, kStatusTimeout | kSiteScaleFactors);
       while (ok && sched.next(wi)) {
         if (!mbar_wait(&acc_empty[acc], accphase ^ 1, abort_flag, p.status, lim,
-                       kStatusTimeout))
+                       kStatusTimeout | kSiteAccEmpty))
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + kAccCol + acc * BT;
         for (int kt0 = wi.k0; ok && kt0 < wi.k1; kt0 += RX) {
           const int r = min(RX, wi.k1 - kt0);
-          if (!mbar_wait(&x_full[xs], xph, abort_flag, p.status, lim, kStatusTimeout)) {
+          if (!mbar_wait(&x_full[xs], xph, abort_flag, p.status, lim, kStatusTimeout | kSiteActFull)) {
             ok = false;
             break;
           }
           const uint32_t sbase = smem_u32(x_base + xs * p.x_bytes);
           for (int i = 0; i < r; ++i) {
-            if (!mbar_wait(&a_full[slot], aphase, abort_flag, p.status, lim, kStatusTimeout)) {
+            if (!mbar_wait(&a_full[slot], aphase, abort_flag, p.status, lim, kStatusTimeout | kSiteDequantFull)) {
               ok = false;
               break;
             }
@@ -797,7 +827,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     while (ok && sched.next(wi)) {
       for (int kt0 = wi.k0; ok && kt0 < wi.k1; kt0 += RW) {
         const int r = min(RW, wi.k1 - kt0);
-        if (!mbar_wait(&w_full[ws], wph, abort_flag, p.status, lim, kStatusTimeout)) {
+        if (!mbar_wait(&w_full[ws], wph, abort_flag, p.status, lim, kStatusTimeout | kSiteWeightFull)) {
           ok = false;
           break;
         }
@@ -848,7 +878,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (lane == 0) mbar_arrive(&w_empty[ws]);
               }
               if (hf == 0 && !mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
-                                        kStatusTimeout)) {
+                                        kStatusTimeout | kSiteTmemSlot)) {
                 ok = false;
                 break;
               }
@@ -913,7 +943,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int slot = g & (kASlots - 1);
             const uint32_t aphase = (uint32_t)(g / kASlots) & 1u;
             if (!mbar_wait(&a_empty[slot], aphase ^ 1, abort_flag, p.status, lim,
-                           kStatusTimeout)) {
+                           kStatusTimeout | kSiteTmemSlot)) {
               ok = false;
               break;
             }
@@ -1079,7 +1109,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         WorkItem nx;
         final_item = !peek.next(nx);
       }
-      if (!mbar_wait(&acc_full[acc], accphase, abort_flag, p.status, lim, kStatusTimeout)) break;
+      if (!mbar_wait(&acc_full[acc], accphase, abort_flag, p.status, lim, kStatusTimeout | kSiteAccFull)) break;
       // after the last item's accumulator is full, every MMA (and so every
       // read of the activation ring) of this CTA has completed
       last = p.last_stage && final_item;
@@ -1097,7 +1127,75 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int contributors = (int)(c_last - c_first + 1);
       int* counter = &p.counters[(long long)wi.tile * 4 + q];
       const bool finisher = !whole && !p.deterministic && c_first == (int)blockIdx.x;
-      if (whole || (!p.deterministic && !finisher)) {
+      if (!GROUPED && p.cluster > 1) {
+        // Cluster split: the cluster's S CTAs hold the tile's S K slices (this
+        // item is the CTA's only one).  16-row chunk mc of quadrant q is unit
+        // u = q * BT / 16 + mc, finished by cluster rank u % S: the others
+        // send their fp32 partial of it (this lane's feature, 16 rows, 64
+        // bytes) into that rank's receive slots, which sums the S slices in
+        // rank order (the result does not depend on timing) and stores it.
+        constexpr int NCH = BT / 16;
+        const int S = p.cluster, sl = (int)(blockIdx.x % (unsigned)S);
+        const int nlive = (tc.rows + 15) / 16;
+        float* recv = reinterpret_cast<float*>(smem + p.off_recv);   // [u / S][S - 1][32][16]
+        if (!cl_waited) {
+          cluster_wait();
+          cl_waited = true;
+        }
+        for (int mc = 0; mc < nlive; ++mc) {
+          const int u = q * NCH + mc, owner = u % S;
+          if (owner == sl) continue;
+          uint32_t v[16];
+          tmem_ld16_wait(tbase + mc * 16, v);
+          const int slot = (u / S) * (S - 1) + (sl < owner ? sl : sl - 1);
+          const uint32_t dst = map_to_rank(smem_u32(recv + (slot * 32 + lane) * 16), owner);
+          const uint32_t bar = map_to_rank(smem_u32(recv_full), owner);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            st_async_f4(dst + 16 * i,
+                        make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
+                        bar);
+        }
+        if (mbar_wait(recv_full, 0, abort_flag, p.status, lim, kStatusTimeout | kSiteClusterRecv)) {
+#pragma unroll 1
+          for (int mc = 0; mc < nlive; ++mc) {
+            const int u = q * NCH + mc;
+            if (u % S != sl) continue;
+            uint32_t v[16];
+            tmem_ld16_wait(tbase + mc * 16, v);
+            float f[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f[i] = 0.f;
+            for (int r = 0; r < S; ++r) {
+              if (r == sl) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) f[i] += __uint_as_float(v[i]);
+              } else {
+                const int slot = (u / S) * (S - 1) + (r < sl ? r : r - 1);
+                const float4* s4 = reinterpret_cast<const float4*>(recv + (slot * 32 + lane) * 16);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float4 x = s4[i];
+                  f[4 * i] += x.x;
+                  f[4 * i + 1] += x.y;
+                  f[4 * i + 2] += x.z;
+                  f[4 * i + 3] += x.w;
+                }
+              }
+            }
+            emit(tc, mc * 16, f, bias);
+          }
+        } else {
+          // every peer sends, so the slices still arrive: wait (bounded) for
+          // them before this CTA's shared memory is released
+          volatile int no_abort = 0;
+          mbar_wait(recv_full, 0, &no_abort, nullptr, 100000000ull, 0);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      } else if (whole || (!p.deterministic && !finisher)) {
         // whole tile: output; atomic-mode contributor: add into the tile's
         // accumulator, 8 rows x 32 columns (1 KB) per bulk reduction through
         // the staging buffers.  Only slices holding output rows are added, so
@@ -1161,7 +1259,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (*abort_flag || globaltimer() - t0 >= lim) {
               if (!*abort_flag) {
                 *abort_flag = 1;
-                atomicOr(p.status, kStatusTimeout);
+                atomicOr(p.status, kStatusTimeout | kSiteSplitCount);
               }
               ok = false;
               break;
@@ -1180,7 +1278,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             bulk_load(fsm, quad, BT * 128, &fix_bar[q], policy_evict_first());
           }
           __syncwarp();
-          ok = mbar_wait(&fix_bar[q], 0, abort_flag, p.status, lim, kStatusTimeout);
+          ok = mbar_wait(&fix_bar[q], 0, abort_flag, p.status, lim, kStatusTimeout | kSiteSplitCopy);
           if (!ok) {   // never leave the copy writing shared memory the CTA is leaving
             volatile int no_abort = 0;
             mbar_wait(&fix_bar[q], 0, &no_abort, nullptr, 100000000ull, 0);
@@ -1280,6 +1378,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   }
 
   __syncwarp();
+  if (!GROUPED && p.cluster > 1) {
+    // No CTA leaves while a peer may still send into its shared memory: the
+    // epilogue warps (the last senders) wait for every thread of the cluster
+    // to arrive; the others arrive and block in the CTA barrier below, which
+    // leaves the issue slots to the epilogue warps meanwhile.
+    if (!cl_waited) cluster_wait();
+    cluster_arrive();
+    if (warp >= 12) cluster_wait();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1304,12 +1411,84 @@ static cudaError_t launch_t(const CUtensorMap& tmap, const CUtensorMap& tmap_c,
   cfg.blockDim = dim3(kNumThreads);
   cfg.dynamicSmemBytes = p.smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = p.cluster > 1 ? (unsigned)p.cluster : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (!GROUPED && p.cluster > 1) ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_c, p);
+}
+
+// Clusters of S CTAs of the dense kernel (with smem bytes of dynamic shared
+// memory) that fit on the device at once.
+template <int BT, int FMT>
+static int max_clusters_t(int S, int smem) {
+  auto kern = w4a16_kernel<BT, FMT, false>;
+  int cap = 0;
+  if (cudaDeviceGetAttribute(&cap, cudaDevAttrMaxSharedMemoryPerBlockOptin, 0) != cudaSuccess)
+    return 0;
+  // the largest size any launch asks for, so a later launch is never refused
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cap) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(S * 64));
+  cfg.blockDim = dim3(kNumThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_c, p);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int FMT>
+static int max_clusters_bt(int bt, int S, int smem) {
+  switch (bt) {
+    case 16: return max_clusters_t<16, FMT>(S, smem);
+    case 32: return max_clusters_t<32, FMT>(S, smem);
+    case 64: return max_clusters_t<64, FMT>(S, smem);
+    case 128: return max_clusters_t<128, FMT>(S, smem);
+    default: return 0;
+  }
+}
+
+int w4a16_max_clusters(int bt, int fmt, int S, int smem) {
+  // one GPU model per process (the library runs on sm_103 only)
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int>, int> cache;
+  const auto key = std::make_tuple(bt, fmt, S, smem);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int n = 0;
+  switch (fmt) {
+    case 0: n = max_clusters_bt<0>(bt, S, smem); break;
+    case 1: n = max_clusters_bt<1>(bt, S, smem); break;
+    case 2: n = max_clusters_bt<2>(bt, S, smem); break;
+    case 3: n = max_clusters_bt<3>(bt, S, smem); break;
+    case 4: n = max_clusters_bt<4>(bt, S, smem); break;
+    case 5: n = max_clusters_bt<5>(bt, S, smem); break;
+    case 6: n = max_clusters_bt<6>(bt, S, smem); break;
+    case 7: n = max_clusters_bt<7>(bt, S, smem); break;
+    default: n = 0;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = n;
+  return n;
 }
 
 template <int FMT, bool GROUPED>

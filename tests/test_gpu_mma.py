@@ -139,6 +139,6 @@ def test_small_m_kernel_rejections(Q):
         st, _ = Q.qgemm_workspace_size(lin.layer, lin.dense, Q.tuning_config(kernel=2,
                                                                              split_k=bad), 8)
         assert st in (Q.QGEMM_ERR_UNSUPPORTED, Q.QGEMM_ERR_INVALID_ARG), bad
-    # unknown kernel id
-    st, _ = Q.qgemm_workspace_size(lin.layer, lin.dense, Q.tuning_config(kernel=3), 8)
+    # unknown kernel id (3 is the tcgen05 kernel's cluster split)
+    st, _ = Q.qgemm_workspace_size(lin.layer, lin.dense, Q.tuning_config(kernel=4), 8)
     assert st == Q.QGEMM_ERR_INVALID_ARG
