@@ -1015,6 +1015,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // store or reduction to finish reading its buffer.
     uint8_t* last_stage = x_base + BT * 512 + q * (BT / 16) * 2048;
     bool last = false;
+    uint32_t staged = 0;   // chunks of the final item staged and not yet stored
     auto emit = [&](const TileCoord<BT>& tc, int m0, const float (&f)[16], float bias) {
       uint16_t o[16];
 #pragma unroll
@@ -1078,10 +1079,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           return;
         }
       }
-      if (!GROUPED || valid >= 16) {
-        uint16_t* sb = last ? reinterpret_cast<uint16_t*>(last_stage + (m0 / 16) * 2048)
-                            : stg + sbuf * (16 * 32);
-        if (lane == 0 && !last) bulk_wait_group_read<1>();   // the buffer's previous store read it
+      if ((!GROUPED || valid >= 16) && last) {
+        // the final item's chunks each have a staging slot of their own:
+        // staged now, stored together after the item's last chunk (one
+        // proxy fence and one bulk group for the whole item)
+        uint16_t* sb = reinterpret_cast<uint16_t*>(last_stage + (m0 / 16) * 2048);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sb[i * 32 + lane] = o[i];
+        staged |= 1u << (m0 / 16);
+      } else if (!GROUPED || valid >= 16) {
+        uint16_t* sb = stg + sbuf * (16 * 32);
+        if (lane == 0) bulk_wait_group_read<1>();   // the buffer's previous store read it
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 16; ++i) sb[i * 32 + lane] = o[i];
@@ -1201,16 +1209,31 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // the staging buffers.  Only slices holding output rows are added, so
         // rows past the end stay zero in the accumulator.
         float* quad_acc = p.partials + (long long)tl * (BT * kTileN) + q * 32 * BT;
+        if (whole) {
+          // two 16-row chunks per tensor-memory load (one load latency each;
+          // past an odd last chunk the load reads unused columns, inside the
+          // allocation: BT / 16 is even from BT = 32 on, and at BT = 16 both
+          // accumulators end 32 columns before the allocation does)
+          const int nch = min(BT / 16, (tc.rows + 15) / 16);
 #pragma unroll 1
-        for (int mc = 0; mc < BT / 16 && mc * 16 < tc.rows; ++mc) {
+          for (int mc = 0; mc < nch; mc += 2) {
+            uint32_t v[32];
+            tmem_ld32_wait(tbase + mc * 16, v);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (mc + h >= nch) break;
+              float f[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[16 * h + i]);
+              emit(tc, (mc + h) * 16, f, bias);
+            }
+          }
+        }
+#pragma unroll 1
+        for (int mc = 0; !whole && mc < BT / 16 && mc * 16 < tc.rows; ++mc) {
           uint32_t v[16];
           tmem_ld16_wait(tbase + mc * 16, v);
-          if (whole) {
-            float f[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
-            emit(tc, mc * 16, f, bias);
-          } else {
+          {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               if (mc * 16 + h * 8 >= tc.rows) break;
@@ -1367,6 +1390,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           if (lane == 0) *counter = 0;   // ready for the next launch
         }
+      }
+      if (staged) {   // the final item's staged chunks
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (uint32_t b = staged; b; b &= b - 1) {
+            const int mc = __ffs((int)b) - 1;
+            tma_store_2d(&tmap_c, last_stage + mc * 2048, tc.nt * kTileN + q * 32,
+                         tc.row0 + mc * 16);
+          }
+          bulk_commit_group();
+        }
+        staged = 0;
       }
       if (++acc == NACC) {
         acc = 0;
