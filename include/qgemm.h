@@ -518,6 +518,34 @@ qgemm_status qgemm_check_status(void* workspace, void* stream);
 void qgemm_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * Checked build.  libqgemm_checked.so is this library compiled with
+ * QGEMM_CHECKED: before every global-memory access whose index the kernels
+ * compute from their inputs or schedule (weight blocks, split-K counters and
+ * accumulators, cluster receive slots, output rows and columns, bias and
+ * activation-scale entries, the MoE permutation, gather and combine indexes),
+ * the kernel tests the index against the problem's extents.  A failed test
+ * skips the access and records QGEMM_ERR_DEVICE instead of trapping: in the
+ * workspace status word (read by qgemm_check_status or
+ * qgemm_noalloc_check_status) for the GEMM kernels, and in a word of the
+ * library (read by qgemm_checked_status) for the MoE support kernels.  Results
+ * of inputs that pass every test are bitwise those of the unchecked build.
+ *   qgemm_checked_build     1 in the checked build, 0 otherwise.
+ *   qgemm_checked_status    synchronizes `stream`, reads and clears the word
+ *                           of the MoE support kernels: QGEMM_OK or
+ *                           QGEMM_ERR_DEVICE (QGEMM_OK always in the
+ *                           unchecked build).
+ *   qgemm_checked_selftest  launches on `stream` one index test that fails by
+ *                           construction (nothing is accessed), recording into
+ *                           the workspace status word (device, 16-byte
+ *                           aligned); QGEMM_ERR_UNSUPPORTED in the unchecked
+ *                           build.
+ * The pages have no counterpart: this is a debugging aid of this library.
+ */
+int qgemm_checked_build(void);
+qgemm_status qgemm_checked_status(void* stream);
+qgemm_status qgemm_checked_selftest(void* workspace, void* stream);
+
+/*
  * The compatibility record of a call: writes into buf (NUL-terminated, at most
  * len bytes) which kernel variant and tuning the heuristic picks for this
  * (layer, compute, m) on the current device, or why the combination is

@@ -15,6 +15,32 @@
 
 namespace qg {
 
+// The checked build's word for the kernels of this file (they have no
+// workspace); never written by the unchecked build.
+__device__ int g_check_word = 0;
+
+int checked_word_read_and_clear() {
+  int w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_check_word, sizeof(int)) != cudaSuccess) return -1;
+  const int zero = 0;
+  if (w && cudaMemcpyToSymbol(g_check_word, &zero, sizeof(int)) != cudaSuccess) return -1;
+  return w;
+}
+
+// One index test that fails by construction (index 1 against an extent of
+// 1); nothing is accessed through it.
+__global__ void check_selftest_kernel(int* word, int extent) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    const int index = 1;
+    if (qg_check(index < extent, word)) word[1] = index;   // never taken
+  }
+}
+
+cudaError_t launch_check_selftest(int* word, cudaStream_t stream) {
+  check_selftest_kernel<<<1, 32, 0, stream>>>(word, 1);
+  return cudaGetLastError();
+}
+
 // Programmatic dependent launch for the auxiliary kernels.  Each waits for
 // the previous grid on the stream to complete, memory included, before it
 // touches memory (a no-op when launched without the attribute).  The
@@ -225,8 +251,10 @@ __global__ void __launch_bounds__(1024) moe_place_kernel(const int32_t* __restri
     const unsigned same = __match_any_sync(0xffffffffu, e);
     if (e >= 0) {
       const int pos = start[e] + cnt[warp][e] + __popc(same & lt_mask);
-      perm[pos] = i;
-      inv_perm[i] = pos;
+      if (qg_check(pos >= 0 && pos < n_slots, &g_check_word)) {
+        perm[pos] = i;
+        inv_perm[i] = pos;
+      }
     }
     __syncwarp();
     if (e >= 0 && (same & lt_mask) == 0) cnt[warp][e] += __popc(same);
@@ -241,6 +269,7 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ a, const int32_t* _
   const int warps = blockDim.x >> 5;
   const int r = blockIdx.x * warps + (threadIdx.x >> 5);
   if (r >= rows) return;
+  if (!qg_check(perm[r] >= 0 && perm[r] < rows, &g_check_word)) return;
   const int src = perm[r] / topk;
   const uint4* s = a + (long long)src * vecs;
   uint4* d = a_perm + (long long)r * vecs;
@@ -332,7 +361,11 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y2, const int32_t* _
     uint4 v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (j0 + j < topk) v[j] = *reinterpret_cast<const uint4*>(y2 + (long long)r[j] * hidden + c);
+      if (j0 + j < topk &&
+          qg_check(r[j] >= 0 && r[j] < (int)gridDim.x * topk, &g_check_word))
+        v[j] = *reinterpret_cast<const uint4*>(y2 + (long long)r[j] * hidden + c);
+      else
+        v[j] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j0 + j < topk) {

@@ -23,6 +23,32 @@ __host__ __device__ constexpr int weight_units_per_slot(int bt) { return bt <= 3
 constexpr int kEpiStageBytes = 4 * 2 * 16 * 32 * 2;   // output staging: 4 warps x 2 x 16 x 32
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusDevice = 2;
+// Checked build (compiled with -DQGEMM_CHECKED): the kernels test the
+// global-memory indexes they compute from their inputs and their schedule
+// against the problem's extents before each access.  A failed test skips the
+// access and records kStatusDevice | kStatusCheck (in the workspace status
+// word, or in the checked-build word of kernels that have no workspace)
+// instead of trapping; the unchecked build compiles the tests away.
+#ifdef QGEMM_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+constexpr int kStatusCheck = 1 << 24;
+__device__ __forceinline__ bool qg_check(bool ok, int* word) {
+  if constexpr (kChecked) {
+    if (!ok) {
+      atomicOr(word, kStatusDevice | kStatusCheck);
+      return false;
+    }
+  }
+  return true;
+}
+// The checked-build word of the kernels without a workspace (permute, gather,
+// combine): read and cleared by qgemm_checked_status.
+int checked_word_read_and_clear();
+// Launches a kernel whose one index test fails on purpose (no access is made).
+cudaError_t launch_check_selftest(int* word, cudaStream_t stream);
 // With kStatusTimeout, the tcgen05 kernel also sets the bit of the wait that
 // gave up first in its CTA (bits 8 and up), for the error message.
 constexpr int kSiteWeightSlot = 1 << 8;     // weight producer: a free weight slot

@@ -1058,12 +1058,38 @@ qgemm_status qgemm_check_status(void* workspace, void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "status clear");
     if (word & kStatusTimeout)
       return fail(QGEMM_ERR_TIMEOUT, "a kernel gave up a bounded wait (status 0x%x)", word);
+    if (word & kStatusCheck)
+      return fail(QGEMM_ERR_DEVICE, "an index check of the checked build failed (status 0x%x)",
+                  word);
     return fail(QGEMM_ERR_DEVICE, "a kernel reported inconsistent inputs (status %d)", word);
   }
   return ok();
 }
 
 void qgemm_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
+
+int qgemm_checked_build(void) { return kChecked ? 1 : 0; }
+
+qgemm_status qgemm_checked_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  const int word = checked_word_read_and_clear();
+  if (word < 0) return fail(QGEMM_ERR_CUDA, "check word read");
+  if (word & kStatusCheck)
+    return fail(QGEMM_ERR_DEVICE, "an index check of the checked build failed (status 0x%x)",
+                word);
+  return ok();
+}
+
+qgemm_status qgemm_checked_selftest(void* workspace, void* stream) {
+  if (!kChecked) return fail(QGEMM_ERR_UNSUPPORTED, "this is not the checked build");
+  if (!workspace || !aligned16(workspace))
+    return fail(QGEMM_ERR_INVALID_ARG, "workspace must be a 16-byte aligned device pointer");
+  cudaError_t e = launch_check_selftest(static_cast<int*>(workspace),
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return ok();
+}
 
 qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
                                  const qgemm_compute_config* compute, int64_t m, char* buf,

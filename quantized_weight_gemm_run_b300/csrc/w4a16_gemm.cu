@@ -533,10 +533,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (s0.next(w0)) {
       const int nt0 = w0.tile - fdiv(w0.tile, p.div_nt) * p.nt;
       const int r = min(RW, w0.k1 - w0.k0);
+    if (qg_check(nt0 >= 0 && nt0 < p.nt && w0.k0 >= 0 && w0.k0 + r <= p.kt, p.status)) {
       mbar_arrive_expect_tx(&w_full[0], r * blk_bytes);
       bulk_load(w_base, p.w + ((long long)nt0 * p.kt + w0.k0) * blk_bytes, r * blk_bytes,
                 &w_full[0], p.w_reuse ? policy_evict_normal() : policy_evict_first());
       first_issued = true;
+    }
     }
   }
   if (warp == 0) {
@@ -687,6 +689,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           } else {
             if (!mbar_wait(&w_empty[ws], wph ^ 1, abort_flag, p.status, lim,
                            kStatusTimeout | kSiteWeightSlot)) {
+              ok = false;
+              break;
+            }
+            if (!qg_check(tc.e >= 0 && tc.e < p.num_experts && tc.nt >= 0 && tc.nt < p.nt &&
+                              kt >= 0 && kt + r <= p.kt,
+                          p.status)) {
+              *abort_flag = 1;   // the slot is not filled: every waiter gives up
               ok = false;
               break;
             }
@@ -1022,7 +1031,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       for (int i = 0; i < 16; ++i) {
         float v = f[i];
         if constexpr (MX)   // W4A8: the per-row activation scale multiplies the fp32 sum
-          v *= (m0 + i < tc.rows) ? p.a_scale[tc.row0 + m0 + i] : 0.f;
+          v *= (m0 + i < tc.rows && qg_check(tc.row0 + m0 + i < p.rows, p.status))
+                   ? p.a_scale[tc.row0 + m0 + i]
+                   : 0.f;
         if constexpr (NV)   // NVFP4: the expert's tensor scale multiplies the fp32 sum
           v *= p.t_scales[tc.e];
         o[i] = to_out<FP16>(v + bias);
@@ -1071,9 +1082,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int nh = p.n >> 1;
             uint16_t* dst = p.c + (long long)(tc.row0 + m0 + r0) * nh + tc.nt * (kTileN / 2) +
                             q * 16 + hcol;
+            const bool in = qg_check(tc.nt * (kTileN / 2) + q * 16 + hcol < nh &&
+                                         tc.row0 + m0 + min(valid, 16) <= p.rows,
+                                     p.status);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              if (r0 + j < valid)
+              if (in && r0 + j < valid)
                 dst[(long long)j * nh] = (uint16_t)((hw[j >> 1] >> (16 * (j & 1))) & 0xFFFF);
           }
           return;
@@ -1102,7 +1116,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         sbuf ^= 1;
       } else {
         uint16_t* dst = p.c + (long long)(tc.row0 + m0) * p.n + tc.nt * kTileN + col;
-        for (int i = 0; i < valid; ++i) dst[(long long)i * p.n] = o[i];
+        if (qg_check(tc.nt * kTileN + col < p.n && tc.row0 + m0 + valid <= p.rows, p.status))
+          for (int i = 0; i < valid; ++i) dst[(long long)i * p.n] = o[i];
       }
     };
     int acc = 0;
@@ -1123,7 +1138,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       last = p.last_stage && final_item;
       tc_fence_after();
       const int n = packed_source_col(tc.nt, col, p.n, p.gated);
-      const float bias = p.bias ? from_out<FP16>(p.bias[(long long)tc.e * p.n + n]) : 0.f;
+      const float bias =
+          (p.bias && qg_check(tc.e >= 0 && tc.e < p.num_experts && n >= 0 && n < p.n, p.status))
+              ? from_out<FP16>(p.bias[(long long)tc.e * p.n + n])
+              : 0.f;
       const uint32_t tbase = tmem_base + lane_addr + kAccCol + acc * BT;
       // Split tiles.  A tile's fp32 accumulator is four quadrant blocks of
       // [BT rows][32 columns]: each block is contiguous (one bulk copy for the
@@ -1133,9 +1151,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int c_first = whole ? 0 : sched.cta_of_unit(u_start);
       const int c_last = whole ? 0 : sched.cta_of_unit(u_start + p.kt - 1);
       const int contributors = (int)(c_last - c_first + 1);
+      // split-K bookkeeping of a split tile: its counters and accumulator
+      // (atomic mode: one per split tile, at most 2 per CTA; fixed order:
+      // two slots per CTA)
+      const bool split_ok =
+          whole || p.cluster > 1 ||
+          qg_check(wi.tile >= 0 && (long long)wi.tile < p.max_tiles && tl >= 0 &&
+                       tl < 2 * (int)gridDim.x,
+                   p.status);
       int* counter = &p.counters[(long long)wi.tile * 4 + q];
       const bool finisher = !whole && !p.deterministic && c_first == (int)blockIdx.x;
-      if (!GROUPED && p.cluster > 1) {
+      if (!split_ok) {
+        // out-of-range split bookkeeping (checked build): the tile is skipped
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      } else if (!GROUPED && p.cluster > 1) {
         // Cluster split: the cluster's S CTAs hold the tile's S K slices (this
         // item is the CTA's only one).  16-row chunk mc of quadrant q is unit
         // u = q * BT / 16 + mc, finished by cluster rank u % S: the others
@@ -1156,6 +1187,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           uint32_t v[16];
           tmem_ld16_wait(tbase + mc * 16, v);
           const int slot = (u / S) * (S - 1) + (sl < owner ? sl : sl - 1);
+          if (!qg_check(owner < S && slot < ((4 * NCH + S - 1) / S) * (S - 1), p.status))
+            continue;   // (the owner then gives up its bounded wait)
           const uint32_t dst = map_to_rank(smem_u32(recv + (slot * 32 + lane) * 16), owner);
           const uint32_t bar = map_to_rank(smem_u32(recv_full), owner);
 #pragma unroll

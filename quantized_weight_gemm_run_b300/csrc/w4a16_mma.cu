@@ -250,15 +250,17 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
     mbar_init(recv_full, 1);
     mbar_init(amax_full, 1);
     fence_barrier_init();
-    // the first weight blocks: issued before anything waits on the previous grid
-    const int first = nk < R ? nk : R;
+    // the first weight blocks: issued before anything waits on the previous
+    // grid (the slice's blocks, checked build: inside the layer's)
+    const bool in = qg_check(nt < p.nt && kt0 >= 0 && kt1 <= p.kt, p.status);
+    const int first = !in ? 0 : nk < R ? nk : R;
     const uint64_t pol = policy_evict_first();
     for (int s = 0; s < first; ++s) {
       mbar_arrive_expect_tx(&full[s], BB);
       bulk_load(ring + s * BB, wsrc + (long long)s * BB, BB, &full[s], pol);
     }
     *issued = first;
-    *abort_flag = 0;
+    *abort_flag = in ? 0 : 1;
     // the slices of the cluster's other CTAs (and this one's own) land here
     mbar_arrive_expect_tx(recv_full, (uint32_t)(S * live * F * 4));
     if constexpr (QA) mbar_arrive_expect_tx(amax_full, (uint32_t)(S * live * 4));
@@ -580,7 +582,7 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[e] *= as;
       }
-      if (p.bias) {
+      if (p.bias && qg_check(n + 4 <= p.n, p.status)) {
         const uint2 bb = *reinterpret_cast<const uint2*>(p.bias + n);
         const uint32_t bw[2] = {bb.x, bb.y};
 #pragma unroll
@@ -601,7 +603,8 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
           out[e] = *reinterpret_cast<const uint32_t*>(&h2);
         }
       }
-      *reinterpret_cast<uint2*>(p.c + (long long)tk * p.n + n) = make_uint2(out[0], out[1]);
+      if (qg_check(tk < p.m && n + 4 <= p.n, p.status))
+        *reinterpret_cast<uint2*>(p.c + (long long)tk * p.n + n) = make_uint2(out[0], out[1]);
     }
   }
   if (!got) {

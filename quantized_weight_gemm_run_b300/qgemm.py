@@ -12,7 +12,10 @@ from __future__ import annotations
 import ctypes
 import os
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqgemm.so")
+# QGEMM_LIBRARY=checked selects the checked build (index tests in every
+# kernel; see include/qgemm.h)
+_LIB_NAME = "libqgemm_checked.so" if os.environ.get("QGEMM_LIBRARY") == "checked" else "libqgemm.so"
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), _LIB_NAME)
 
 # status codes
 QGEMM_OK = 0
@@ -61,7 +64,8 @@ class QGemmError(RuntimeError):
 def _load():
     if not os.path.exists(_LIB_PATH):
         raise ImportError(f"{_LIB_PATH} is missing: build it with "
-                          "`python -m quantized_weight_gemm_run_b300.build`")
+                          "`python -m quantized_weight_gemm_run_b300.build`"
+                          + (" --checked" if _LIB_NAME != "libqgemm.so" else ""))
     return ctypes.CDLL(_LIB_PATH)
 
 
@@ -90,6 +94,8 @@ _SIGS = {
     "qgemm_debug_dequant": [_L, _P, _P, _P],
     "qgemm_check_status": [_P, _P],
     "qgemm_noalloc_check_status": [_P],
+    "qgemm_checked_status": [_P],
+    "qgemm_checked_selftest": [_P, _P],
     "qgemm_describe_plan": [_L, _C, _I64, ctypes.c_char_p, _SZ],
 }
 for _name, _args in _SIGS.items():
@@ -102,6 +108,8 @@ lib.qgemm_status_string.argtypes = [ctypes.c_int]
 lib.qgemm_status_string.restype = ctypes.c_char_p
 lib.qgemm_last_error.argtypes = []
 lib.qgemm_last_error.restype = ctypes.c_char_p
+lib.qgemm_checked_build.argtypes = []
+lib.qgemm_checked_build.restype = ctypes.c_int
 
 
 def _ptr(x):
@@ -229,6 +237,18 @@ def qgemm_check_status(workspace, stream=None):
 
 def qgemm_noalloc_check_status(stream=None):
     return lib.qgemm_noalloc_check_status(_stream(stream))
+
+
+def qgemm_checked_build() -> int:
+    return lib.qgemm_checked_build()
+
+
+def qgemm_checked_status(stream=None):
+    return lib.qgemm_checked_status(_stream(stream))
+
+
+def qgemm_checked_selftest(workspace, stream=None):
+    return lib.qgemm_checked_selftest(_ptr(workspace), _stream(stream))
 
 
 def qgemm_set_wait_limit_ns(ns: int) -> None:

@@ -150,3 +150,22 @@ def test_compute_config_rejections_before_any_device_work(Q):
                 Q.compute_config(gemm_type=7)):
         st, _ = Q.qgemm_workspace_size(layer, bad, None, 16)
         assert st == Q.QGEMM_ERR_INVALID_ARG, Q.last_error()
+
+
+def test_checked_build_exports_the_same_symbols_and_says_so(Q):
+    """The checked build (index tests in every kernel) is the same boundary:
+    every declared entry point, and qgemm_checked_build tells the two apart
+    (host calls only)."""
+    import ctypes
+    path = os.path.join(ROOT, "quantized_weight_gemm_run_b300", "libqgemm_checked.so")
+    assert os.path.exists(path), "build() also builds the checked library"
+    lib = ctypes.CDLL(path)
+    missing = [n for n in _header_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    lib.qgemm_checked_build.restype = ctypes.c_int
+    assert lib.qgemm_checked_build() == 1
+    assert Q.qgemm_checked_build() == 0
+
+
+def test_selftest_is_refused_by_the_unchecked_build(Q):
+    assert Q.qgemm_checked_selftest(16, 0) == Q.QGEMM_ERR_UNSUPPORTED
