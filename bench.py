@@ -101,10 +101,12 @@ def workload_points(name):
         return [dict(m=s["m"], n=s["n"], k=s["k"], g=128, asym=False, adt="bf16")], dict(
             workload="w4a16_sym_8192x8192x8192", m=8192, n=8192, k=8192, group=128,
             weights="int4", act="bf16")
-    if name == "w4a8":
+    if name == "w4a8" or name.startswith("w4a8:"):
+        # w4a8:M: one M of the set (kernel studies, profiling)
         s = synth.W4A8_SHAPE
+        ms = [int(name[5:])] if name.startswith("w4a8:") else synth.W4A8_MS
         return ([dict(kind="w4a8", m=m, n=s["n"], k=s["k"], g=32, asym=False, adt="bf16")
-                 for m in synth.W4A8_MS],
+                 for m in ms],
                 dict(workload="w4a8_mxfp4_7168x2048", n=s["n"], k=s["k"], ms=synth.W4A8_MS,
                      weights="mxfp4 (e2m1 + e8m0/32)", act="bf16 -> e4m3 per token"))
     if name.startswith("moe"):
@@ -122,8 +124,12 @@ def point_bytes(p):
     m, n, k, g = p["m"], p["n"], p["k"], p["g"]
     kind = p.get("kind", "w4a16")
     if kind == "w4a8":
-        # act quant: read bf16 x, write e4m3 + scale; GEMM: codes, e8m0, a8, scale, bf16 out
-        return (2 * m * k + m * k + 4 * m) + (n * k // 2 + n * k // 32 + m * k + 4 * m + 2 * m * n)
+        # GEMM: bf16 activations read once, codes, e8m0 scales, bf16 out; above
+        # 16 rows the per-token quantization is its own kernel (bf16 in, e4m3
+        # and scales out, read back by the GEMM), at most 16 rows it runs
+        # inside the small-M kernel
+        gemm = 2 * m * k + n * k // 2 + n * k // 32 + 2 * m * n
+        return gemm + (m * k + 4 * m) * 2 if m > 16 else gemm
     if kind == "w8a16":
         # 8-bit codes, scales, 8-bit zero points, activations, output
         return n * k + (k // g) * n * 2 + (k // g) * n + m * k * 2 + m * n * 2
