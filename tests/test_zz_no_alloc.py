@@ -112,3 +112,31 @@ def test_noalloc_refuses_grouped(Q):
     st = Q.qgemm_run_noalloc(layer, Q.compute_config(Q.QGEMM_GEMM_GROUPED), None, 8, 16, None,
                              16, None, 16)
     assert st == Q.QGEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("m", [5, 70])
+def test_noalloc_w4a8_on_bf16_activations(Q, m):
+    """W4A8 layers on bf16 activations through the allocation-free entry point:
+    at m <= 16 the quantization runs inside the small-M kernel, above it the
+    quantized rows and scales live in the library's scratch (after the part
+    that is cleared) before the tcgen05 kernel reads them."""
+    import synth
+    from oracle import codecs, quant
+    from quantized_weight_gemm_run_b300.api import W4A8Linear
+    g = synth.rng(40 + m)
+    n, k = 384, 1024
+    ckn, bkn = quant.quantize_mxfp4(synth.weights_fp32(g, k, n))
+    cnk, bnk = quant.pack_mxfp4(ckn, bkn)
+    lin = W4A8Linear(torch.from_numpy(cnk).to(DEV), torch.from_numpy(bnk).to(DEV), n, k)
+    x = torch.from_numpy(codecs.bf16(synth.activations_fp32(g, m, k)).astype(np.float32)).to(
+        torch.bfloat16).to(DEV)
+    ref = lin(x)
+    assert lin.status() == Q.QGEMM_OK
+    for _ in range(2):
+        out = torch.full_like(ref, float("nan"))
+        st = Q.qgemm_run_noalloc(lin.layer_bf16, lin.dense, None, m, x, None, lin.packed, None,
+                                 out)
+        assert st == Q.QGEMM_OK, Q.last_error()
+        assert Q.qgemm_noalloc_check_status() == Q.QGEMM_OK
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
