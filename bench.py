@@ -458,6 +458,8 @@ def kernel_name(p):
               else "fp16" if p["adt"] == "fp16" else "bf16")
         return f"w4a16_mma_kernel<{dt},{1 if m <= 8 else 2}>"
     bt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
+    if kind == "w4a8" and bt == 128 and -(-m // 64) * (p["n"] // 128) <= 148:
+        bt = 64   # the planner's one-wave 64-token tiles for W4A8
     fmt = ("w4a8_mxf8f6f4" if kind == "w4a8" else "nvfp4_bf16" if kind == "nvfp4"
            else f"int8_{p['adt']}" if kind == "w8a16"
            else "bf16_f16scales" if f16_scales(p) else "fp16" if p["adt"] == "fp16" else "bf16")

@@ -107,7 +107,8 @@ enum { QGEMM_ACT_NONE = 0, QGEMM_ACT_SILU_GLU = 1 };
  *                 the library quantizes with the qgemm_quantize_act_fp8 rule:
  *                 at m <= 16 inside the small-M kernel, above in a separate
  *                 kernel into the workspace; results are bitwise those of the
- *                 two-call form)
+ *                 two-call form; such a layer's workspace then holds its
+ *                 quantized rows, so it must not be shared with other layers)
  *   out_dtype     output dtype: equal to act_dtype for W4A16, QGEMM_BF16 for W4A8
  *   has_bias      1: add bias[N] (out_dtype) in fp32 before the final rounding
  *   num_experts   1 for a dense layer, E for a grouped (MoE) layer

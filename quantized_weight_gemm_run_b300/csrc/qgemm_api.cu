@@ -334,6 +334,11 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   const int E = L->num_experts;
   int bt = (T && T->block_tok) ? T->block_tok
                                : heuristic_block_tok(grouped ? (rows + E - 1) / E : rows);
+  // W4A8 (measured on B300, N = 7168, K = 2048, M = 128): 64-token whole tiles
+  // in one wave beat 128-token tiles when they fit (13.2 against 15.3 us)
+  if (is_mx(L) && !grouped && !(T && T->block_tok) && bt == 128 &&
+      ((rows + 63) / 64) * (L->n / kTileN) <= device_sm_count())
+    bt = 64;
   if (bt != 16 && bt != 32 && bt != 64 && bt != 128 && bt != 256)
     return fail(QGEMM_ERR_UNSUPPORTED, "block_tok %d not in {16, 32, 64, 128, 256}", bt);
   if (bt == 256 && (is_mx(L) || is_nv(L) || is_f16s(L) || is_w8(L)))
@@ -455,9 +460,15 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
       const double breakeven = bt == 16 ? 8.0 : bt == 32 ? 9.0 : bt == 64 ? 12.0 : 15.0;
       if (whole_units - sk_units < breakeven) cap = 1;
     }
+    // W4A8: whole tiles unless a tuning asks for splits (measured on B300,
+    // N = 7168, K = 2048: M = 256 / 512 / 1024 15.9 / 24.0 / 36.3 us against
+    // 24.3 / 28.9 / 39.7 with stream-K); they also keep no split-K state in
+    // the workspace, where a layer on bf16 activations keeps its quantized rows
+    if (is_mx(L) && cap == 0 && !(T && T->max_ctas > 0)) cap = 1;
     if (cap > 0 && tiles_bound * cap < grid)
       grid = (int)(tiles_bound > 0 ? tiles_bound * cap : 1);
   }
+  if (grouped && quant_in_lib(L) && cap == 0 && !(T && T->max_ctas > 0)) cap = 1;
   // Cluster split: each tile's K range in S slices, one CTA each, the S CTAs
   // of a tile in one cluster summing their slices through distributed shared
   // memory (no workspace round trip, no wait on another tile's CTAs).
@@ -792,6 +803,15 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
   const int fmt = fmt_of(L);
   if (clear_bytes) {
     cudaError_t ce = cudaMemsetAsync(workspace, 0, clear_bytes, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "workspace clear");
+  }
+  if (qa && P.split_cap != 1 && P.cluster == 0) {
+    // a split-K plan asked for by a tuning on a layer whose quantized rows share
+    // the workspace: another plan's rows may lie where this plan keeps its
+    // counters and accumulators, so they start cleared
+    cudaError_t ce = cudaMemsetAsync(static_cast<uint8_t*>(workspace) + P.ws.counters_off, 0,
+                                     P.ws.partials_off + P.ws.partials_bytes - P.ws.counters_off,
+                                     stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "workspace clear");
   }
   if (qa) {   // the GEMM waits on this grid before it reads the codes and scales

@@ -309,3 +309,44 @@ def test_w4a8_bf16_grouped_matches_per_expert(Q):
         a8, s = gemm.act_quant_fp8(x[lo:hi])
         want = gemm.w4a8_reference(a8, s, c.codes_kn, c.b_kn)
         assert_close(got[lo:hi], want, frob=2e-2, what=f"grouped w4a8 bf16 expert {i}")
+
+
+def test_w4a8_bf16_one_workspace_across_plans(Q):
+    """A layer on bf16 activations keeps its quantized rows in the workspace,
+    at an offset that depends on the plan.  Calls that switch plans on one
+    workspace (the cluster split and the small-M kernel put the rows where a
+    stream-K plan keeps its split-K counters and accumulator) must each give
+    the right result: the stream-K plan, which only a tuning selects for these
+    layers, clears its state first."""
+    c = MxCase(64, 1024, 2048, seed=120)
+    lin = _lin(Q, c)
+    x = c.x_dev()
+    ref = c.reference()
+    plans = {"cluster": (64, Q.tuning_config(kernel=3, split_k=2)),
+             "stream_k": (64, Q.tuning_config(block_tok=32, max_ctas=37)),
+             "small_m": (16, Q.tuning_config(kernel=2)),
+             "default": (64, None)}
+    need = max(Q.qgemm_workspace_size(lin.layer_bf16, lin.dense, t, m)[1] for m, t in plans.values())
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for name in ("stream_k", "cluster", "stream_k", "small_m", "stream_k", "default", "stream_k"):
+        m, tun = plans[name]
+        out = torch.full((m, c.n), float("nan"), dtype=torch.bfloat16, device=DEV)
+        st = Q.qgemm_run(lin.layer_bf16, lin.dense, tun, m, x[:m].contiguous(), None, lin.packed,
+                         None, out, ws, need)
+        assert st == Q.QGEMM_OK, (name, Q.last_error())
+        assert Q.qgemm_check_status(ws) == Q.QGEMM_OK, (name, Q.last_error())
+        assert_close(to_np(out), ref[:m], frob=2e-2, what=f"w4a8 plan {name}")
+
+
+@pytest.mark.parametrize("m", [100, 256, 512])
+def test_w4a8_planner_takes_whole_tiles(Q, m):
+    c = MxCase(m, 7168, 2048, seed=130 + m)
+    lin = _lin(Q, c)
+    st, plan = Q.qgemm_describe_plan(lin.layer_bf16, lin.dense, m)
+    assert st == Q.QGEMM_OK
+    assert "split=whole_tiles" in plan or "split=cluster" in plan, plan
+    if m == 100:
+        assert "block_tok=64" in plan, plan
+    out = lin(c.x_dev())
+    assert lin.status() == Q.QGEMM_OK
+    assert_close(to_np(out), c.reference(), frob=2e-2, what=f"w4a8 m={m}")
