@@ -488,9 +488,12 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   int cl = 0;
   Geometry gc;
   if (cl_allowed && (want_cl || !(T && T->split_k > 0))) {
+    // a forced split with no count asked for takes at least two slices (in
+    // several waves if the tiles need them)
     int S = s_fixed ? s_fixed
                     : (int)std::min<int64_t>(std::min<int64_t>(8, kt),
-                                             std::max<int64_t>(1, sms / tiles_bound));
+                                             std::max<int64_t>(want_cl ? 2 : 1,
+                                                               sms / tiles_bound));
     for (; S >= 2; --S) {
       const int nu = (4 * (bt / 16) + S - 1) / S;   // 16-row chunks this CTA finishes
       if (!make_geometry(bt, st, has_zp, is_mx(L), is_w8(L), E, w_cap, device_max_smem(),
@@ -509,8 +512,9 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
       return fail(QGEMM_ERR_UNSUPPORTED, "no cluster split of this tile fits shared memory");
     if (cl && !want_cl) {
       // Heuristic: per-CTA k-tiles at the measured per-k-tile cost (above),
-      // plus ~1 us for the exchange and the rank-ordered sums, against the
-      // persistent schedule's whole waves or stream-K with its split cost.
+      // plus the exchange, the rank-ordered sums and the stores (measured on
+      // B300 at ~0.85 of stream-K's split cost: ~4 us at BT 64, ~6 us at BT
+      // 128), against the persistent schedule's whole waves or stream-K.
       const double c = bt == 16 ? 0.30 : bt == 32 ? 0.33 : bt == 64 ? 0.38 : 0.47;
       const double split = bt == 16 ? 2.5 : bt == 32 ? 3.0 : bt == 64 ? 4.5 : 7.0;
       const int64_t G = grid, Tt = tiles_bound;
@@ -519,7 +523,7 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
       if (W > 0 && Tt % G) --W;
       const double sk = ((double)W * kt + (double)(Tt - W * G) * kt / (double)G) * c + split;
       const double t_sk = cap == 1 ? whole : std::min(whole, sk);
-      const double t_cl = (double)((kt + cl - 1) / cl) * c + 1.0;
+      const double t_cl = (double)((kt + cl - 1) / cl) * c + 0.85 * split;
       if (!(t_cl < t_sk)) cl = 0;
     }
     if (cl) {

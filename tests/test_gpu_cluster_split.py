@@ -138,7 +138,7 @@ def test_cluster_split_nvfp4(Q):
     assert_close(to_np(out), ref, what="cluster nvfp4")
 
 
-@pytest.mark.parametrize("m,n,k", [(64, 4096, 4096), (256, 4096, 4096), (64, 4096, 11008)])
+@pytest.mark.parametrize("m,n,k", [(64, 4096, 4096), (256, 4096, 4096)])
 def test_planner_takes_cluster_split_at_medium_m(Q, m, n, k):
     """The default plan of the medium-M sweep shapes whose tiles fit the device
     in clusters, and the parity of that default call."""
@@ -188,3 +188,13 @@ def test_cluster_split_timeout_reports_and_recovers(Q):
     assert lin.status() == Q.QGEMM_OK
     torch.cuda.synchronize()
     assert torch.equal(again, ref)
+
+
+def test_forced_cluster_split_without_a_count_takes_two_slices(Q):
+    """kernel = 3 with split_k = 0 on a problem whose tiles alone fill the
+    device: two slices per tile, in several waves."""
+    c = Case(64, 11008, 1024, 128, "bf16", False, seed=41)
+    lin = linear(c, tuning=Q.tuning_config(kernel=3))
+    out = lin(c.dev_act())
+    assert lin.status() == Q.QGEMM_OK
+    assert_close(to_np(out), c.reference(), what="forced cluster, 86 tiles")
