@@ -611,6 +611,13 @@ def measured_peaks_here(stream, peaks):
         return {"fp8_tflops": None, "error": str(e)[:120]}
 
 
+def nvtx(name):
+    """An NVTX range around a phase of the run (for timeline tools; no cost
+    inside the timed loops, which it only brackets)."""
+    import torch
+    return torch.cuda.nvtx.range(name)
+
+
 def run_ours(args, rank, world, device):
     import torch
     pts, cfg = workload_points(args.workload)
@@ -655,7 +662,7 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream), nvtx("timed steps"):
         e0.record(stream)
         for _ in range(args.steps):
             graph.replay()
@@ -685,7 +692,8 @@ def run_ours(args, rank, world, device):
     # per-GEMM device times (dominant kernel and the per-M table)
     clocks_pts = ClockSampler(torch.cuda.current_device())
     clocks_pts.start()
-    per_point = [measure_point(bp, p, peaks, stream) for bp, p in zip(base, pts)]
+    with nvtx("points"):
+        per_point = [measure_point(bp, p, peaks, stream) for bp, p in zip(base, pts)]
     # the other configurations of the workload set, each timed the same way
     extra_points = []
     if not args.no_extra and args.workload == "sweep":
