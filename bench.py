@@ -656,7 +656,8 @@ def run_ours(args, rank, world, device):
             import torch.distributed as dist
             dist.barrier()
 
-    clocks = ClockSampler(torch.cuda.current_device())
+    # the timed region can be a few ms: sample every millisecond
+    clocks = ClockSampler(torch.cuda.current_device(), period=0.001)
     clocks.start()
     barrier()
     torch.cuda.synchronize()
