@@ -5,6 +5,10 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#ifdef __CUDACC__
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#endif
 
 namespace qg {
 
@@ -160,6 +164,7 @@ struct W4A16MmaParams {
   int mx;                    // 1: W4A8 (MXFP4 weights, e4m3 activations, bf16 output)
   const float* a_scale;      // W4A8: per-row activation scales [m] (quant_act: unused)
   int quant_act;             // W4A8: 1 = a is bf16 and the kernel quantizes it per row
+  int f16s;                  // 1: bf16 activations with fp16 scales
   unsigned long long wait_limit_ns;
 };
 // tmap_a: activations as {128 bytes of k, m rows, chunks}, 128-byte swizzle,
@@ -228,6 +233,30 @@ __host__ __device__ inline int packed_source_col(int nt, int r, int n, int gated
 // standalone kernel produce the same bits from the same rounded inputs.
 __device__ __forceinline__ float silu_mul_f32(float g, float u) {
   return __fmul_rn(__fdividef(g, __fadd_rn(1.f, __expf(-g))), u);
+}
+
+// bf16 activations with fp16 scales: w^ = bf16((q - z) * s), one rounding.
+// The scale is split into s_hi, its leading 8 significant bits (a bf16), and
+// the rest s_lo = s - s_hi, which has at most 3 significant bits (an fp16 has
+// 11) and the sign of s, so it is a bf16 too.  With d = q - z (an integer of
+// at most 4 bits, exact in bf16), t = d * s_lo has at most 7 significant bits
+// and is exact, and fma(d, s_hi, t) rounds the exact d * s once.  Zero
+// results carry the sign of d * s: both terms are then zeros of that sign.
+__device__ __forceinline__ void split_f16_scale(uint16_t bits, uint32_t& hi2, uint32_t& lo2) {
+  const float s = __half2float(__ushort_as_half(bits));
+  uint32_t hi, lo;
+  if (isfinite(s)) {
+    const uint32_t sb = __float_as_uint(s);
+    const float rest = s - __uint_as_float(sb & 0xFFFF0000u);   // exact
+    hi = sb >> 16;
+    lo = (__float_as_uint(rest) >> 16) | ((sb >> 16) & 0x8000u);
+  } else {   // inf or NaN: the products d * s of IEEE arithmetic
+    const __nv_bfloat16 b = __float2bfloat16_rn(s);
+    hi = *reinterpret_cast<const uint16_t*>(&b);
+    lo = 0;
+  }
+  hi2 = hi * 0x00010001u;
+  lo2 = lo * 0x00010001u;
 }
 #endif
 

@@ -380,14 +380,15 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
                             rows <= 8 ? 8 : 16, is_mx(L) ? 1 : 2, quant_in_lib(L))
            : 0;
   const bool mma_fits = s_ok && nk_max <= 64 && mma_smem <= device_max_smem();
-  const bool mma_ok = !grouped && !is_nv(L) && !is_f16s(L) && !is_w8(L) &&
+  const bool mma_ok = !grouped && !is_nv(L) && !is_w8(L) &&
                       L->gated_act == 0 && rows <= 16 && !(C && C->batch_invariant) &&
                       mma_fits;
   const int want = T ? T->kernel : 0;
   if (want == 2 && !mma_ok)
     return fail(QGEMM_ERR_UNSUPPORTED,
                 "the small-M kernel takes dense INT4/UINT4/INT3/UINT3 GEMMs with scales in the "
-                "activation dtype and W4A8-MXFP4 GEMMs, with m <= 16, not gated or "
+                "activation dtype (or fp16 scales with bf16 activations) and W4A8-MXFP4 GEMMs, "
+                "with m <= 16, not gated or "
                 "batch-invariant, split_k a power of two <= 16 and <= k/128 and a slice that "
                 "fits shared memory");
   P->kernel = 1;
@@ -663,6 +664,7 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
     q.mx = mx ? 1 : 0;
     q.a_scale = a_scale;
     q.quant_act = qa ? 1 : 0;
+    q.f16s = is_f16s(L) ? 1 : 0;
     q.s_off = P.off_s;
     q.z_off = P.off_z;
     q.sg_shift = L->group_size == 32 ? 0 : L->group_size == 64 ? 1 : 2;

@@ -246,30 +246,7 @@ __device__ __forceinline__ void dequant_vec(const uint4 v, uint32_t zero2, uint3
   }
 }
 
-// bf16 activations with fp16 scales: w^ = bf16((q - z) * s), one rounding.
-// The scale is split into s_hi, its leading 8 significant bits (a bf16), and
-// the rest s_lo = s - s_hi, which has at most 3 significant bits (an fp16 has
-// 11) and the sign of s, so it is a bf16 too.  With d = q - z (an integer of
-// at most 4 bits, exact in bf16), t = d * s_lo has at most 7 significant bits
-// and is exact, and fma(d, s_hi, t) rounds the exact d * s once.  Zero
-// results carry the sign of d * s: both terms are then zeros of that sign.
-__device__ __forceinline__ void split_f16_scale(uint16_t bits, uint32_t& hi2, uint32_t& lo2) {
-  const float s = __half2float(__ushort_as_half(bits));
-  uint32_t hi, lo;
-  if (isfinite(s)) {
-    const uint32_t sb = __float_as_uint(s);
-    const float rest = s - __uint_as_float(sb & 0xFFFF0000u);   // exact
-    hi = sb >> 16;
-    lo = (__float_as_uint(rest) >> 16) | ((sb >> 16) & 0x8000u);
-  } else {   // inf or NaN: the products d * s of IEEE arithmetic
-    const __nv_bfloat16 b = __float2bfloat16_rn(s);
-    hi = *reinterpret_cast<const uint16_t*>(&b);
-    lo = 0;
-  }
-  hi2 = hi * 0x00010001u;
-  lo2 = lo * 0x00010001u;
-}
-
+// bf16 activations with fp16 scales (split_f16_scale, internal.h): one rounding.
 __device__ __forceinline__ void dequant_vec_f16s(const uint4 v, uint32_t zero2, uint32_t hi2,
                                                  uint32_t lo2, uint32_t (&out)[16]) {
   constexpr uint32_t magic = 0x43004300u;

@@ -201,7 +201,10 @@ int mma_smem_bytes(int block_bytes, int ring, int nk_max, int rows, int elem_byt
 // slices exchange their maxima through distributed shared memory (the max is
 // exact, so every CTA derives the same scale), and each CTA quantizes its own
 // slice into the e4m3 tile the MMAs read.
-template <bool FP16, int NB, bool ONE_GROUP, bool MX, bool QA = false>
+// F16S: bf16 activations with fp16 scales; each scale is split once per row
+// into two bf16 terms (split_f16_scale) and w^ = fma(d, s_hi, d s_lo) rounds
+// (q - z) s once, the dequantized values of the tcgen05 kernel's FMT 5.
+template <bool FP16, int NB, bool ONE_GROUP, bool MX, bool QA = false, bool F16S = false>
 __global__ void __launch_bounds__(kMmaThreads, 4)
     w4a16_mma_kernel(const __grid_constant__ CUtensorMap tmap_a, const W4A16MmaParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -209,6 +212,7 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   constexpr int ROWS = 8 * NB;
   static_assert(!QA || MX, "activation quantization serves the W4A8 path");
+  static_assert(!F16S || (!FP16 && !MX), "fp16 scales serve bf16 activations");
   constexpr int AB = MX ? 1 : 2;   // bytes per activation element the MMAs read
   constexpr int AIN = QA ? 2 : AB;  // bytes per activation element in HBM
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -433,13 +437,18 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
     const uint16_t* sv = reinterpret_cast<const uint16_t*>(blk + p.s_off);
     const uint8_t* zv = blk + p.z_off;
     // per-row scale and zero pairs of rows (b, g) and (b, g + 8), group sg
+    // (F16S: sc the scales' high bf16 terms, sl the low ones)
+    [[maybe_unused]] uint32_t sl[2][2];
     auto row_consts = [&](int sg, uint32_t (&sc)[2][2], uint32_t (&zc)[2][2]) {
 #pragma unroll
       for (int b = 0; b < 2; ++b)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int r = rg * 32 + b * 16 + g + 8 * e;
-          sc[b][e] = (uint32_t)sv[sg * kTileN + r] * 0x00010001u;
+          if constexpr (F16S)
+            split_f16_scale(sv[sg * kTileN + r], sc[b][e], sl[b][e]);
+          else
+            sc[b][e] = (uint32_t)sv[sg * kTileN + r] * 0x00010001u;
           zc[b][e] = (magic16 + (p.has_zp ? (uint32_t)zv[sg * kTileN + r] : 8u)) * 0x00010001u;
         }
     };
@@ -493,7 +502,17 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) x[b][h][i] = mul2<FP16>(x[b][h][i], sc[b][i & 1]);
+          for (int i = 0; i < 4; ++i) {
+            if constexpr (F16S) {
+              const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&x[b][h][i]);
+              const __nv_bfloat162 r =
+                  __hfma2(d, *reinterpret_cast<const __nv_bfloat162*>(&sc[b][i & 1]),
+                          __hmul2(d, *reinterpret_cast<const __nv_bfloat162*>(&sl[b][i & 1])));
+              x[b][h][i] = *reinterpret_cast<const uint32_t*>(&r);
+            } else {
+              x[b][h][i] = mul2<FP16>(x[b][h][i], sc[b][i & 1]);
+            }
+          }
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -615,10 +634,10 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
   }
 }
 
-template <bool FP16, int NB, bool ONE, bool MX = false, bool QA = false>
+template <bool FP16, int NB, bool ONE, bool MX = false, bool QA = false, bool F16S = false>
 static cudaError_t launch_one(const CUtensorMap& tmap, const W4A16MmaParams& p, int smem,
                               cudaStream_t stream) {
-  auto kern = w4a16_mma_kernel<FP16, NB, ONE, MX, QA>;
+  auto kern = w4a16_mma_kernel<FP16, NB, ONE, MX, QA, F16S>;
   static int smem_set = 0;
   static bool nonportable_set = false;
   if (smem > smem_set) {
@@ -660,6 +679,13 @@ cudaError_t launch_w4a16_mma(const CUtensorMap& tmap, const W4A16MmaParams& p, b
   if (p.mx)
     return nb == 1 ? launch_one<false, 1, true, true>(tmap, p, smem, stream)
                    : launch_one<false, 2, true, true>(tmap, p, smem, stream);
+  if (p.f16s) {
+    if (nb == 1)
+      return one ? launch_one<false, 1, true, false, false, true>(tmap, p, smem, stream)
+                 : launch_one<false, 1, false, false, false, true>(tmap, p, smem, stream);
+    return one ? launch_one<false, 2, true, false, false, true>(tmap, p, smem, stream)
+               : launch_one<false, 2, false, false, false, true>(tmap, p, smem, stream);
+  }
   if (fp16) {
     if (nb == 1) return one ? launch_one<true, 1, true>(tmap, p, smem, stream)
                             : launch_one<true, 1, false>(tmap, p, smem, stream);

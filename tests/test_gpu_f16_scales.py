@@ -4,7 +4,8 @@ not rounded to bf16 first.  The pack and the values fed to the tensor core
 bit for bit (every code and zero point under every finite scale), the GEMM within
 |gpu - ref| <= 1e-2 + 1e-2 |ref| per element and relative Frobenius error
 <= 5e-3: dense at small and full sizes, split-K, grouped and gated; the
-planner routes these layers to the tcgen05 kernel at every m."""
+planner routes dense layers of at most 16 rows to the small-M kernel, which
+must feed the MMA the same operand bits, and the rest to the tcgen05 kernel."""
 
 import numpy as np
 import pytest
@@ -133,12 +134,47 @@ def test_full_size_m16_and_m256(Q):
         assert_close(to_np(out), c.reference(), what=f"f16 scales {m}x4096x4096")
 
 
-def test_plan_takes_tcgen05_kernel_and_rejects_small_m_kernel(Q):
+def test_plan_takes_small_m_kernel_up_to_16_rows(Q):
     c = _case(8, 256, 256, 128, True, seed=144)
     lin = linear(c)
-    st, rec = Q.qgemm_describe_plan(lin.layer, lin.dense, 8)
-    assert st == Q.QGEMM_OK
-    assert "kernel=w4a16_tcgen05_swapab" in rec and "scales=fp16 act=bf16" in rec
-    forced = linear(c, tuning=Q.tuning_config(kernel=2))
-    with pytest.raises(Q.QGemmError):
-        forced(c.dev_act())
+    for m, kern in ((8, "w4a16_mma_sync_smallm"), (16, "w4a16_mma_sync_smallm"),
+                    (17, "w4a16_tcgen05_swapab")):
+        st, rec = Q.qgemm_describe_plan(lin.layer, lin.dense, m)
+        assert st == Q.QGEMM_OK
+        assert f"kernel={kern}" in rec and "scales=fp16 act=bf16" in rec, rec
+    # forced onto either kernel, the two agree within the GEMM tolerance
+    x = c.dev_act()
+    small = linear(c, tuning=Q.tuning_config(kernel=2))(x)
+    big = linear(c, tuning=Q.tuning_config(kernel=1))(x)
+    assert_close(to_np(small), c.reference(), what="f16 scales small-M kernel")
+    assert_close(to_np(big), c.reference(), what="f16 scales tcgen05 kernel")
+
+
+def test_small_m_kernel_operands_every_code_zero_and_scale(Q):
+    """The small-M kernel's own dequant of fp16 scales against bf16
+    activations: one-hot activation rows pick single weight rows, so each
+    output is one dequantized weight (the product with 1.0 and the fp32 sums
+    of zeros are exact).  Eight calls of 16 rows take one row of every group:
+    every code against every zero point under every finite fp16 scale of
+    either sign, compared with the oracle's bf16((q - z) s) (+0 and -0 equal)."""
+    from quantized_weight_gemm_run_b300.api import W4A16Linear
+    k, n, g = 4096, 512, 32
+    q = (np.arange(k)[:, None] + np.arange(n)[None, :]) % 16
+    z = np.repeat((np.arange(k // g) % 16)[:, None], n, axis=1)
+    finite = np.concatenate([np.arange(0x7C00), 0x8000 + np.arange(0x7C00)]).astype(np.uint16)
+    bits = np.resize(np.random.default_rng(9).permutation(finite), (k // g) * n)
+    s = bits.view(np.float16).astype(np.float64).reshape(k // g, n)
+    lin = W4A16Linear(torch.from_numpy(quant.pack_int4_kn(q, False)).to(DEV),
+                      torch.from_numpy(bits.view(np.int16).reshape(k // g, n)).to(DEV),
+                      torch.from_numpy(quant.pack_zeros(z)).to(DEV), n, k, g, torch.bfloat16,
+                      scale_dtype=torch.float16, tuning=Q.tuning_config(kernel=2))
+    w_hat = quant.dequant_int(q, s, z, g, "bf16")
+    groups = k // g
+    for call in range(groups // 16):
+        rows = [(call * 16 + i) * g + (call * 7 + i) % g for i in range(16)]
+        x = np.zeros((16, k), dtype=np.float32)
+        x[np.arange(16), rows] = 1.0
+        out = lin(torch.from_numpy(x).to(torch.bfloat16).to(DEV))
+        assert lin.status() == Q.QGEMM_OK
+        got = out.float().cpu().numpy().astype(np.float64)
+        assert np.array_equal(got, w_hat[rows]), f"call {call}"
