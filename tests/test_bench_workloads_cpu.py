@@ -45,8 +45,10 @@ def test_kernel_names_follow_the_planner():
     # dense INT4/UINT4 with scales in the activation dtype: small-M kernel up to 16 rows
     assert bench.kernel_name(dict(_pt("sweep"), m=16)).startswith("w4a16_mma_kernel")
     assert bench.kernel_name(dict(_pt("sweep"), m=17)) == "w4a16_kernel<32,bf16,dense>"
-    # fp16 scales with bf16 activations and 8-bit codes: the tcgen05 kernel at every m
-    assert bench.kernel_name(dict(_pt("f16s"), m=1)) == "w4a16_kernel<16,bf16_f16scales,dense>"
+    # fp16 scales with bf16 activations: small-M kernel up to 16 rows, as for the sweep
+    assert bench.kernel_name(dict(_pt("f16s"), m=1)) == "w4a16_mma_kernel<bf16_f16scales,1>"
+    assert bench.kernel_name(dict(_pt("f16s"), m=64)) == "w4a16_kernel<64,bf16_f16scales,dense>"
+    # 8-bit codes and NVFP4 weights: the tcgen05 kernel at every m
     assert bench.kernel_name(dict(_pt("w8a16"), m=1)) == "w4a16_kernel<16,int8_bf16,dense>"
     assert bench.kernel_name(dict(_pt("w8a16"), m=1024)) == "w4a16_kernel<128,int8_bf16,dense>"
     assert bench.kernel_name(dict(_pt("nvfp4"), m=256)) == "w4a16_kernel<128,nvfp4_bf16,dense>"
