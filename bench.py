@@ -452,10 +452,12 @@ def kernel_name(p):
     if kind == "moe":
         return "moe_layer (sort, gather, SiLU-gated grouped GEMM, grouped GEMM, combine)"
     m = p["m"]
-    if kind in ("w4a16", "w4a8") and m <= 16:
-        # the planner's default for dense INT4/UINT4 and W4A8 GEMMs of at most 16 rows
-        dt = ("w4a8_fused_act_quant" if kind == "w4a8" else "bf16_f16scales" if f16_scales(p)
-              else "fp16" if p["adt"] == "fp16" else "bf16")
+    nv_small = kind == "nvfp4" and (p["n"] * p["k"] <= 1 << 24 or (m <= 8 and p["k"] <= 4096))
+    if (kind in ("w4a16", "w4a8") or nv_small) and m <= 16:
+        # the planner's default for dense INT4/UINT4 and W4A8 GEMMs of at most
+        # 16 rows, and for NVFP4 ones up to 2^24 weights or 8 rows with K <= 4096
+        dt = ("w4a8_fused_act_quant" if kind == "w4a8" else "nvfp4_" + p["adt"] if nv_small
+              else "bf16_f16scales" if f16_scales(p) else "fp16" if p["adt"] == "fp16" else "bf16")
         return f"w4a16_mma_kernel<{dt},{1 if m <= 8 else 2}>"
     bt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
     if kind == "w4a8" and bt == 128 and -(-m // 64) * (p["n"] // 128) <= 148:

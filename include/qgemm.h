@@ -185,8 +185,8 @@ typedef struct {
  *              2 = the small-M kernel (bulk-copied weights, mma.sync, K
  *              slices reduced inside a thread-block cluster; dense INT4 /
  *              UINT4 / INT3 / UINT3 with scales in the activation dtype or
- *              fp16 scales against bf16 activations, and W4A8-MXFP4, m <= 16
- *              only, not gated or batch-invariant;
+ *              fp16 scales against bf16 activations, NVFP4 weights, and
+ *              W4A8-MXFP4, m <= 16 only, not gated or batch-invariant;
  *              split_k, when set, is its number of K slices per n-tile, a
  *              power of two <= 16; stages its weight slots; it ignores the
  *              other fields),

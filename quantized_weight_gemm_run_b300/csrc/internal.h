@@ -165,6 +165,8 @@ struct W4A16MmaParams {
   const float* a_scale;      // W4A8: per-row activation scales [m] (quant_act: unused)
   int quant_act;             // W4A8: 1 = a is bf16 and the kernel quantizes it per row
   int f16s;                  // 1: bf16 activations with fp16 scales
+  int nv;                    // 1: NVFP4 weights (16-bit block scales in the blocks)
+  const float* t_scales;     // NVFP4: the fp32 tensor scale (the packed buffer's tail)
   unsigned long long wait_limit_ns;
 };
 // tmap_a: activations as {128 bytes of k, m rows, chunks}, 128-byte swizzle,
@@ -242,6 +244,33 @@ __device__ __forceinline__ float silu_mul_f32(float g, float u) {
 // at most 4 bits, exact in bf16), t = d * s_lo has at most 7 significant bits
 // and is exact, and fma(d, s_hi, t) rounds the exact d * s once.  Zero
 // results carry the sign of d * s: both terms are then zeros of that sign.
+// Four e2m1 codes (bits 0-15, code c at bits 4c..4c+3) -> two packed 16-bit
+// pairs of their values, exactly (every e2m1 value is an fp16 and a bf16
+// value): p0 = (code 0, code 1), p1 = (code 2, code 3), the lower k in the low
+// half.  prmt looks up the bytes of each code magnitude's 16-bit pattern in
+// 8-entry byte tables (fp16: the low byte is always 0), a sign-replicating
+// prmt turns each code's sign bit into bit 6 of a byte, and one lop3 moves it
+// into the sign of the high byte.
+template <bool FP16>
+__device__ __forceinline__ void e2m1x4_pairs(uint32_t c16, uint32_t& p0, uint32_t& p1) {
+  const uint32_t sel = c16 & 0x7777u;
+  uint32_t sgn, hi;
+  asm("prmt.b32 %0, %1, %1, %2;" : "=r"(sgn) : "r"(0x80808080u), "r"(c16));
+  if constexpr (FP16) {   // high bytes of fp16 0, 0.5, 1, 1.5 | 2, 3, 4, 6
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3E3C3800u), "r"(0x46444240u), "r"(sel));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(hi) : "r"(sgn << 1), "r"(0x80808080u), "r"(hi));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p0) : "r"(hi), "r"(0u), "r"(0x1404u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p1) : "r"(hi), "r"(0u), "r"(0x3424u));
+  } else {                // bf16: high and low bytes of the same eight values
+    uint32_t lo;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3F3F3F00u), "r"(0x40404040u), "r"(sel));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0xC0800000u), "r"(0xC0804000u), "r"(sel));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(hi) : "r"(sgn << 1), "r"(0x80808080u), "r"(hi));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p0) : "r"(lo), "r"(hi), "r"(0x5140u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p1) : "r"(lo), "r"(hi), "r"(0x7362u));
+  }
+}
+
 __device__ __forceinline__ void split_f16_scale(uint16_t bits, uint32_t& hi2, uint32_t& lo2) {
   const float s = __half2float(__ushort_as_half(bits));
   uint32_t hi, lo;

@@ -380,14 +380,15 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
                             rows <= 8 ? 8 : 16, is_mx(L) ? 1 : 2, quant_in_lib(L))
            : 0;
   const bool mma_fits = s_ok && nk_max <= 64 && mma_smem <= device_max_smem();
-  const bool mma_ok = !grouped && !is_nv(L) && !is_w8(L) &&
+  const bool mma_ok = !grouped && !is_w8(L) &&
                       L->gated_act == 0 && rows <= 16 && !(C && C->batch_invariant) &&
                       mma_fits;
   const int want = T ? T->kernel : 0;
   if (want == 2 && !mma_ok)
     return fail(QGEMM_ERR_UNSUPPORTED,
                 "the small-M kernel takes dense INT4/UINT4/INT3/UINT3 GEMMs with scales in the "
-                "activation dtype (or fp16 scales with bf16 activations) and W4A8-MXFP4 GEMMs, "
+                "activation dtype (or fp16 scales with bf16 activations), NVFP4 and W4A8-MXFP4 "
+                "GEMMs, "
                 "with m <= 16, not gated or "
                 "batch-invariant, split_k a power of two <= 16 and <= k/128 and a slice that "
                 "fits shared memory");
@@ -397,7 +398,15 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   // kernel takes every GEMM it can run (no tensor-memory set-up, no
   // split-tile finish through L2).
   const bool k1_tuned = T && (T->block_tok || T->stages || T->max_ctas || T->split_k);
-  const bool use_mma = want == 2 || (want == 0 && mma_ok && !k1_tuned);
+  // NVFP4 weights cost about three integer operations per weight to decode,
+  // which makes the small-M kernel issue-bound on large layers.  Measured on
+  // B300 (bf16, us, small-M / tcgen05): 4096^2 8.4 / 9.5 at every M <= 16;
+  // 11008 x 4096 13.1 / 14.1 at M <= 8, 18.8 / 14.3 at M = 16; 4096 x 11008
+  // 14.7 / 14.5 at M = 1, 16.3 / 14.6 at M = 4.  So by default it takes them
+  // up to 2^24 weights, or at M <= 8 with K <= 4096.
+  const bool nv_small = !is_nv(L) || L->n * L->k <= (int64_t(1) << 24) ||
+                        (rows <= 8 && L->k <= 4096);
+  const bool use_mma = want == 2 || (want == 0 && mma_ok && !k1_tuned && nv_small);
   if (use_mma) {
     if (ntl * S >= (int64_t(1) << 31)) return fail(QGEMM_ERR_UNSUPPORTED, "grid too large");
     P->kernel = 2;
@@ -665,6 +674,10 @@ static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_co
     q.a_scale = a_scale;
     q.quant_act = qa ? 1 : 0;
     q.f16s = is_f16s(L) ? 1 : 0;
+    q.nv = is_nv(L) ? 1 : 0;
+    q.t_scales = is_nv(L) ? reinterpret_cast<const float*>(static_cast<const uint8_t*>(w) +
+                                                           expert_packed_bytes(L))
+                          : nullptr;
     q.s_off = P.off_s;
     q.z_off = P.off_z;
     q.sg_shift = L->group_size == 32 ? 0 : L->group_size == 64 ? 1 : 2;

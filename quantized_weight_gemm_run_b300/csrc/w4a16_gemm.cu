@@ -342,11 +342,9 @@ __device__ __forceinline__ uint32_t mul_pair(uint32_t bits, uint32_t scale2) {
 
 // NVFP4: 32 e2m1 codes (one 16-byte vector, k in nibble order, low nibble
 // first) -> 16 packed 16-bit pairs (k, k+1) of e2m1 value x block scale,
-// exactly: every e2m1 x e4m3 product is a bf16 and an fp16 value.  prmt looks
-// up the bytes of each code magnitude's 16-bit pattern in 8-entry byte tables
-// (fp16: the low byte is always 0), a sign-replicating prmt turns each code's
-// sign bit into bit 6 of a byte, and one lop3 moves it into the sign of the
-// high byte.  Words 0-1 hold k 0..15 (scale sA2), words 2-3 k 16..31 (sB2).
+// exactly: every e2m1 x e4m3 product is a bf16 and an fp16 value (the code
+// values by e2m1x4_pairs, internal.h).  Words 0-1 hold k 0..15 (scale sA2),
+// words 2-3 k 16..31 (sB2).
 template <bool FP16>
 __device__ __forceinline__ void dequant_vec_nv(const uint4 v, uint32_t sA2, uint32_t sB2,
                                                uint32_t (&out)[16]) {
@@ -355,23 +353,8 @@ __device__ __forceinline__ void dequant_vec_nv(const uint4 v, uint32_t sA2, uint
   for (int w = 0; w < 4; ++w) {
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {   // codes 4 hh .. 4 hh + 3 of the word
-      const uint32_t c16 = wds[w] >> (16 * hh);
-      const uint32_t sel = c16 & 0x7777u;
-      uint32_t sgn, hi, p0, p1;
-      asm("prmt.b32 %0, %1, %1, %2;" : "=r"(sgn) : "r"(0x80808080u), "r"(c16));
-      if constexpr (FP16) {   // high bytes of fp16 0, 0.5, 1, 1.5 | 2, 3, 4, 6
-        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3E3C3800u), "r"(0x46444240u), "r"(sel));
-        hi = lop3_and_or(sgn << 1, 0x80808080u, hi);
-        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p0) : "r"(hi), "r"(0u), "r"(0x1404u));
-        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p1) : "r"(hi), "r"(0u), "r"(0x3424u));
-      } else {                // bf16: high and low bytes of the same eight values
-        uint32_t lo;
-        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3F3F3F00u), "r"(0x40404040u), "r"(sel));
-        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0xC0800000u), "r"(0xC0804000u), "r"(sel));
-        hi = lop3_and_or(sgn << 1, 0x80808080u, hi);
-        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p0) : "r"(lo), "r"(hi), "r"(0x5140u));
-        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p1) : "r"(lo), "r"(hi), "r"(0x7362u));
-      }
+      uint32_t p0, p1;
+      e2m1x4_pairs<FP16>(wds[w] >> (16 * hh), p0, p1);
       const uint32_t s2 = w < 2 ? sA2 : sB2;
       out[w * 4 + hh * 2] = mul_pair<FP16>(p0, s2);
       out[w * 4 + hh * 2 + 1] = mul_pair<FP16>(p1, s2);

@@ -204,7 +204,15 @@ int mma_smem_bytes(int block_bytes, int ring, int nk_max, int rows, int elem_byt
 // F16S: bf16 activations with fp16 scales; each scale is split once per row
 // into two bf16 terms (split_f16_scale) and w^ = fma(d, s_hi, d s_lo) rounds
 // (q - z) s once, the dequantized values of the tcgen05 kernel's FMT 5.
-template <bool FP16, int NB, bool ONE_GROUP, bool MX, bool QA = false, bool F16S = false>
+// NV: NVFP4 weights (e2m1 codes in nibble order, one 16-bit block scale per
+// 16 k, an fp32 tensor scale) against 16-bit activations: a lane's two codes
+// of k 2t, 2t + 1 (and 2t + 8, 2t + 9) are byte t of words 2h and 2h + 1 of
+// its row's vector; one prmt gathers both bytes, e2m1x4_pairs gives the exact
+// 16-bit pairs, one multiply by the block scale rounds nothing (the products
+// are exact), and the tensor scale multiplies the finished sum, as in the
+// tcgen05 kernel.
+template <bool FP16, int NB, bool ONE_GROUP, bool MX, bool QA = false, bool F16S = false,
+          bool NV = false>
 __global__ void __launch_bounds__(kMmaThreads, 4)
     w4a16_mma_kernel(const __grid_constant__ CUtensorMap tmap_a, const W4A16MmaParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -213,6 +221,7 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
   constexpr int ROWS = 8 * NB;
   static_assert(!QA || MX, "activation quantization serves the W4A8 path");
   static_assert(!F16S || (!FP16 && !MX), "fp16 scales serve bf16 activations");
+  static_assert(!NV || (!MX && !F16S), "NVFP4 weights take 16-bit activations");
   constexpr int AB = MX ? 1 : 2;   // bytes per activation element the MMAs read
   constexpr int AIN = QA ? 2 : AB;  // bytes per activation element in HBM
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -473,7 +482,7 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
           bf[h][2] = bf[h][3] = 0u;
         }
       }
-      if constexpr (!ONE_GROUP) row_consts(j >> p.sg_shift, sc, zc);
+      if constexpr (!ONE_GROUP && !NV) row_consts(j >> p.sg_shift, sc, zc);
       // m16 block b: rows 32 warp + 16 b + {g, g + 8} (e = 0, 1), 32 k each
       uint4 v[2][2];
 #pragma unroll
@@ -484,6 +493,26 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
       // that the 16 independent chains interleave: fragment register i of
       // step h holds rows e = i & 1 of word 2h + (i >> 1) (k 8 (i >> 1) + 2t)
       uint32_t x[2][2][4];
+      if constexpr (NV) {
+        // block scales of rows (b, e): the 16-k blocks 2j + h of the k-tile
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const uint32_t s2 =
+                  (uint32_t)sv[(2 * j + h) * kTileN + rg * 32 + b * 16 + g + 8 * e] * 0x00010001u;
+              uint32_t c16, p0, p1;
+              asm("prmt.b32 %0, %1, %2, %3;"
+                  : "=r"(c16)
+                  : "r"(word_of(v[b][e], 2 * h)), "r"(word_of(v[b][e], 2 * h + 1)),
+                    "r"((uint32_t)(t | ((4 + t) << 4))));
+              e2m1x4_pairs<FP16>(c16, p0, p1);
+              x[b][h][e] = mul2<FP16>(p0, s2);
+              x[b][h][2 + e] = mul2<FP16>(p1, s2);
+            }
+      } else {
 #pragma unroll
       for (int b = 0; b < 2; ++b)
 #pragma unroll
@@ -513,6 +542,7 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
               x[b][h][i] = mul2<FP16>(x[b][h][i], sc[b][i & 1]);
             }
           }
+      }   // integer codes
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -601,6 +631,11 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[e] *= as;
       }
+      if constexpr (NV) {   // the tensor scale multiplies the fp32 sum
+        const float ts = p.t_scales[0];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] *= ts;
+      }
       if (p.bias && qg_check(n + 4 <= p.n, p.status)) {
         const uint2 bb = *reinterpret_cast<const uint2*>(p.bias + n);
         const uint32_t bw[2] = {bb.x, bb.y};
@@ -634,10 +669,11 @@ __global__ void __launch_bounds__(kMmaThreads, 4)
   }
 }
 
-template <bool FP16, int NB, bool ONE, bool MX = false, bool QA = false, bool F16S = false>
+template <bool FP16, int NB, bool ONE, bool MX = false, bool QA = false, bool F16S = false,
+          bool NV = false>
 static cudaError_t launch_one(const CUtensorMap& tmap, const W4A16MmaParams& p, int smem,
                               cudaStream_t stream) {
-  auto kern = w4a16_mma_kernel<FP16, NB, ONE, MX, QA, F16S>;
+  auto kern = w4a16_mma_kernel<FP16, NB, ONE, MX, QA, F16S, NV>;
   static int smem_set = 0;
   static bool nonportable_set = false;
   if (smem > smem_set) {
@@ -679,6 +715,13 @@ cudaError_t launch_w4a16_mma(const CUtensorMap& tmap, const W4A16MmaParams& p, b
   if (p.mx)
     return nb == 1 ? launch_one<false, 1, true, true>(tmap, p, smem, stream)
                    : launch_one<false, 2, true, true>(tmap, p, smem, stream);
+  if (p.nv) {
+    if (fp16)
+      return nb == 1 ? launch_one<true, 1, false, false, false, false, true>(tmap, p, smem, stream)
+                     : launch_one<true, 2, false, false, false, false, true>(tmap, p, smem, stream);
+    return nb == 1 ? launch_one<false, 1, false, false, false, false, true>(tmap, p, smem, stream)
+                   : launch_one<false, 2, false, false, false, false, true>(tmap, p, smem, stream);
+  }
   if (p.f16s) {
     if (nb == 1)
       return one ? launch_one<false, 1, true, false, false, true>(tmap, p, smem, stream)

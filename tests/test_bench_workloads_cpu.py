@@ -48,10 +48,16 @@ def test_kernel_names_follow_the_planner():
     # fp16 scales with bf16 activations: small-M kernel up to 16 rows, as for the sweep
     assert bench.kernel_name(dict(_pt("f16s"), m=1)) == "w4a16_mma_kernel<bf16_f16scales,1>"
     assert bench.kernel_name(dict(_pt("f16s"), m=64)) == "w4a16_kernel<64,bf16_f16scales,dense>"
-    # 8-bit codes and NVFP4 weights: the tcgen05 kernel at every m
+    # 8-bit codes: the tcgen05 kernel at every m
     assert bench.kernel_name(dict(_pt("w8a16"), m=1)) == "w4a16_kernel<16,int8_bf16,dense>"
     assert bench.kernel_name(dict(_pt("w8a16"), m=1024)) == "w4a16_kernel<128,int8_bf16,dense>"
-    assert bench.kernel_name(dict(_pt("nvfp4"), m=256)) == "w4a16_kernel<128,nvfp4_bf16,dense>"
+    # NVFP4 weights: the small-M kernel up to 2^24 weights, or at m <= 8 with k <= 4096
+    nv = _pt("nvfp4")
+    assert bench.kernel_name(dict(nv, m=16, n=4096, k=4096)) == "w4a16_mma_kernel<nvfp4_bf16,2>"
+    assert bench.kernel_name(dict(nv, m=8, n=11008, k=4096)) == "w4a16_mma_kernel<nvfp4_bf16,1>"
+    assert bench.kernel_name(dict(nv, m=9, n=11008, k=4096)) == "w4a16_kernel<16,nvfp4_bf16,dense>"
+    assert bench.kernel_name(dict(nv, m=1, n=4096, k=11008)) == "w4a16_kernel<16,nvfp4_bf16,dense>"
+    assert bench.kernel_name(dict(nv, m=256)) == "w4a16_kernel<128,nvfp4_bf16,dense>"
 
 
 def test_traffic_keys_separate_formats():

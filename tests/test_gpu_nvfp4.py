@@ -178,3 +178,65 @@ def test_nvfp4_m_zero_and_missing_tensor_scales(Q):
     assert Q.qgemm_pack_weights(lin.layer, torch.from_numpy(codes).to(DEV),
                                 torch.from_numpy(sb).to(DEV), None, packed) == \
         Q.QGEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("adt", ["bf16", "fp16"])
+def test_small_m_kernel_operands_every_code_and_scale(Q, adt):
+    """The small-M kernel's own NVFP4 path (m <= 16): one-hot activation rows
+    pick single weight rows, so each output is one operand times the tensor
+    scale 2^-3 (exact, as are the fp32 sums of zeros).  16 calls of 16 rows
+    cover one row of every 16-k block: every code in every nibble position
+    against every e4m3 scale byte, compared with the oracle's operand."""
+    from quantized_weight_gemm_run_b300.api import NVFP4Linear
+    k, n = 128 * 16, 128
+    codes = np.tile(np.arange(16, dtype=np.uint8), (k * n) // 16).reshape(k, n)
+    codes = np.roll(codes, 5, axis=1)
+    sb = (np.arange((k // 16) * n) % 0x7F).astype(np.uint8).reshape(k // 16, n)
+    cn, sn = quant.pack_nvfp4(codes, sb)
+    ts = 0.125
+    lin = NVFP4Linear(torch.from_numpy(cn).to(DEV), torch.from_numpy(sn).to(DEV),
+                      torch.full((1,), ts, dtype=torch.float32, device=DEV), n, k, TD[adt],
+                      tuning=Q.tuning_config(kernel=2))
+    st, rec = Q.qgemm_describe_plan(lin.layer, lin.dense, 16)
+    assert "kernel=w4a16_mma_sync_smallm" in rec, rec
+    want = quant.nvfp4_operand(codes, sb) * ts
+    blocks = k // 16
+    for call in range(blocks // 16):
+        rows = [(call * 16 + i) * 16 + (call * 5 + 3 * i) % 16 for i in range(16)]
+        x = np.zeros((16, k), dtype=np.float32)
+        x[np.arange(16), rows] = 1.0
+        out = lin(torch.from_numpy(x).to(TD[adt]).to(DEV))
+        assert lin.status() == Q.QGEMM_OK
+        got = out.float().cpu().numpy().astype(np.float64)
+        assert np.array_equal(got, codecs.round_dtype(adt)(want[rows])), f"{adt} call {call}"
+
+
+@pytest.mark.parametrize("m", [1, 9, 16])
+def test_small_m_kernel_matches_oracle_and_tcgen05(Q, m):
+    c = NvCase(m, 384, 1024, "bf16", seed=200 + m, bias=True)
+    small = c.layer(tuning=Q.tuning_config(kernel=2))
+    big = c.layer(tuning=Q.tuning_config(kernel=1))
+    x = c.a_dev()
+    o2 = small(x)
+    o1 = big(x)
+    assert small.status() == Q.QGEMM_OK and big.status() == Q.QGEMM_OK
+    ref = c.reference()
+    assert_close(to_np(o2), ref, what=f"nvfp4 small-M m={m}")
+    assert_close(to_np(o1), ref, what=f"nvfp4 tcgen05 m={m}")
+
+
+def test_plan_routes_nvfp4_by_layer_size(Q):
+    """The small-M kernel takes NVFP4 layers of up to 2^24 weights at m <= 16,
+    and larger ones at m <= 8 when K <= 4096; the rest go to the tcgen05 kernel."""
+    import copy
+    lin = NvCase(4, 256, 256, "bf16", seed=231).layer()
+    for m, n, k, kern in ((16, 4096, 4096, "w4a16_mma_sync_smallm"),
+                          (8, 11008, 4096, "w4a16_mma_sync_smallm"),
+                          (9, 11008, 4096, "w4a16_tcgen05_swapab"),
+                          (1, 4096, 11008, "w4a16_tcgen05_swapab"),
+                          (17, 4096, 4096, "w4a16_tcgen05_swapab")):
+        cfg = copy.copy(lin.layer)
+        cfg.n, cfg.k = n, k
+        st, rec = Q.qgemm_describe_plan(cfg, lin.dense, m)
+        assert st == Q.QGEMM_OK
+        assert f"kernel={kern}" in rec, (m, n, k, rec)
