@@ -19,7 +19,8 @@ Modules:
   codecs  -- bf16 / fp16 / e4m3 / e2m1 / e8m0 encode and decode
   quant   -- quantizers, the standard-format packing, dequantization
   layout  -- the kernel-side packed layout the repack step must produce
-  gemm    -- W4A16 and W4A8 GEMM references, per-token FP8 activation quant
+  gemm    -- W4A16, W4A8 and W4A4 GEMM references, per-token FP8 and NVFP4
+             activation quantizers
   moe     -- routing, permutation, SiLU-gate, combine, the full MoE layer
 
 Parity status: every function is pinned by tests under ``tests/`` (tables,
