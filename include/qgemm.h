@@ -78,7 +78,7 @@ enum { QGEMM_S_FP16 = 0, QGEMM_S_BF16 = 1, QGEMM_S_E8M0 = 2, QGEMM_S_E4M3 = 3 };
 /* zero-point formats */
 enum { QGEMM_Z_NONE = 0, QGEMM_Z_UINT4 = 1, QGEMM_Z_UINT8 = 2, QGEMM_Z_UINT3 = 3 };
 /* activation / output data types */
-enum { QGEMM_FP16 = 0, QGEMM_BF16 = 1, QGEMM_FP8E4M3 = 2 };
+enum { QGEMM_FP16 = 0, QGEMM_BF16 = 1, QGEMM_FP8E4M3 = 2, QGEMM_NVFP4 = 3 };
 /* GEMM types (compute config) */
 enum { QGEMM_GEMM_DENSE = 0, QGEMM_GEMM_GROUPED = 1 };
 /* gated activation fused into the output (layer config) */
@@ -109,7 +109,18 @@ enum { QGEMM_ACT_NONE = 0, QGEMM_ACT_SILU_GLU = 1 };
  *                 kernel into the workspace; results are bitwise those of the
  *                 two-call form; such a layer's workspace then holds its
  *                 quantized rows, so it must not be shared with other layers)
+ *                 or QGEMM_NVFP4 with NVFP4 weights (W4A4: the pages list
+ *                 W4A4 among the common configurations, kinachrichten.com
+ *                 "Warum quantisierte Kernel wichtig sind"; the caller passes
+ *                 bf16 activations and, as a_scale, one fp32 activation
+ *                 tensor scale on the device, and the library quantizes each
+ *                 token to e2m1 codes with an e4m3 scale per 16 k by the
+ *                 qgemm_quantize_act_nvfp4 rule into the workspace, then runs
+ *                 both operands packed through the FP4 tensor cores; dense,
+ *                 ungated, k a multiple of 256, bf16 output; the workspace
+ *                 holds the quantized rows and must not be shared)
  *   out_dtype     output dtype: equal to act_dtype for W4A16, QGEMM_BF16 for W4A8
+ *                 and W4A4
  *   has_bias      1: add bias[N] (out_dtype) in fp32 before the final rounding
  *   num_experts   1 for a dense layer, E for a grouped (MoE) layer
  *   gated_act     QGEMM_ACT_NONE: C[M, N] = A W (+ bias).
@@ -256,6 +267,9 @@ typedef struct {
  *              0x7F / 0xFF are invalid)
  *     tensor   fp32 [E]: one scale per expert, passed in the qzeros argument
  *     meaning  w[k, n] = e2m1(code) * e4m3(scale) * tensor
+ *   NVFP4 for W4A4 (act_dtype QGEMM_NVFP4): the same tensors (E = 1); the
+ *     packed buffer is codes [N, K/2], then scales [N, K/16], then the
+ *     tensor scale, end to end (the FP4 tensor cores read them as they are)
  */
 
 /*
@@ -327,7 +341,9 @@ qgemm_status qgemm_workspace_init(void* workspace, size_t bytes, void* stream);
  *   a         device, [m, K] in act_dtype (e4m3 codes for W4A8 with
  *             act_dtype QGEMM_FP8E4M3)
  *   a_scale   device fp32 [m] per-row activation scales (W4A8 with e4m3
- *             activations), else NULL (also for W4A8 with bf16 activations)
+ *             activations); W4A4: device fp32 [1], the activations' tensor
+ *             scale (positive and finite); else NULL (also for W4A8 with
+ *             bf16 activations)
  *   packed    device packed buffer from qgemm_pack_weights
  *   bias      device [N] in out_dtype, or NULL when has_bias = 0
  *   c         device, [m, N] in out_dtype ([m, N/2] for a gated layer)
@@ -434,6 +450,28 @@ qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
  */
 qgemm_status qgemm_quantize_act_fp8(const void* x, int64_t m, int64_t k, void* a8,
                                     float* a_scale, void* stream);
+
+/*
+ * Per-token NVFP4 activation quantization (W4A4 path), in blocks of 16 along
+ * k, against the caller's tensor scale a_ts (device fp32 [1], positive and
+ * finite); every step is an fp32 operation:
+ *   block_scales[r, b] = e4m3(amax_b / (6 a_ts)), amax_b = max |x[r, 16b..16b+15]|,
+ *                        round to nearest even, saturating at 448
+ *   codes[r, k]        = e2m1(x[r, k] / (s a_ts)), s the block's e4m3 value,
+ *                        IEEE fp32 divide, round to nearest even, saturating
+ *                        at +-6, the sign of x kept (a block whose s is 0
+ *                        takes code 0 throughout)
+ *   x device bf16 [m, k]; codes device uint8 [m, k/2] (k = 2j in the low
+ *   nibble of byte j, as the standard NVFP4 weight codes); block_scales
+ *   device uint8 [m, k/16].  k must be a multiple of 16; x must be 16-byte
+ *   aligned, codes 8-byte aligned, a_ts 4-byte aligned.
+ * Source: the pages list W4A4 among the common configurations and name NVFP4
+ * (kinachrichten.com, "Warum quantisierte Kernel wichtig sind"); they do not
+ * say how activations are quantized: NVFP4's two-level scaling with a
+ * caller-supplied tensor scale is this library's reading.
+ */
+qgemm_status qgemm_quantize_act_nvfp4(const void* x, int64_t m, int64_t k, const float* a_ts,
+                                      void* codes, void* block_scales, void* stream);
 
 /*
  * MoE permutation: stable counting sort of the t*topk (token, slot) pairs by

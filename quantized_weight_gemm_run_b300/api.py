@@ -266,6 +266,56 @@ class W4A8Linear:
         return Q.qgemm_check_status(self.ws.get(256))
 
 
+class W4A4Linear:
+    """A packed W4A4 layer: NVFP4 weights (e2m1 codes uint8 [N, K/2] in the
+    standard nibble order, e4m3 block scales uint8 [N, K/16], one fp32 tensor
+    scale) against activations the library quantizes to NVFP4 per token
+    against ``act_scale`` (a device fp32 [1] tensor scale).  Calling the layer
+    on bf16 activations is one library call (the quantization kernel, then the
+    FP4 tensor-core GEMM); ``quantize`` exposes the quantization alone."""
+
+    def __init__(self, codes, scales, tensor_scale, act_scale, n, k, bias=None, tuning=None):
+        self.n, self.k, self.n_out = n, k, n
+        self.layer = Q.layer_config(n, k, 16, Q.QGEMM_W_NVFP4, Q.QGEMM_S_E4M3, Q.QGEMM_Z_NONE,
+                                    Q.QGEMM_NVFP4, Q.QGEMM_BF16, 1 if bias is not None else 0, 1,
+                                    Q.QGEMM_ACT_NONE)
+        st, nbytes = Q.qgemm_packed_size(self.layer)
+        Q.check(st)
+        dev = codes.device
+        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        ts = tensor_scale.to(torch.float32).reshape(-1)[:1].contiguous()
+        Q.check(Q.qgemm_pack_weights(self.layer, codes.contiguous(), scales.contiguous(), ts,
+                                     self.packed))
+        self.act_scale = act_scale.to(torch.float32).reshape(-1)[:1].contiguous()
+        self.bias, self.tuning = bias, tuning
+        self.ws = Workspace(dev)
+        self.dense = Q.compute_config(Q.QGEMM_GEMM_DENSE)
+
+    def quantize(self, x: torch.Tensor):
+        """x bf16 [M, K] -> (e2m1 codes uint8 [M, K/2], e4m3 block scales uint8 [M, K/16])."""
+        m = x.shape[0]
+        codes = torch.empty(max(m, 1), self.k // 2, dtype=torch.uint8, device=x.device)
+        sb = torch.empty(max(m, 1), self.k // 16, dtype=torch.uint8, device=x.device)
+        Q.check(Q.qgemm_quantize_act_nvfp4(x.contiguous(), m, self.k, self.act_scale, codes, sb))
+        return codes[:m], sb[:m]
+
+    def __call__(self, x: torch.Tensor, out=None) -> torch.Tensor:
+        """x bf16 [M, K] -> bf16 [M, N]."""
+        x = x.contiguous()
+        m = x.shape[0]
+        if out is None:
+            out = torch.empty(m, self.n, dtype=torch.bfloat16, device=x.device)
+        st, nbytes = Q.qgemm_workspace_size(self.layer, self.dense, self.tuning, max(m, 1))
+        Q.check(st)
+        ws = self.ws.get(nbytes)
+        Q.check(Q.qgemm_run(self.layer, self.dense, self.tuning, m, x, self.act_scale,
+                            self.packed, self.bias, out, ws, ws.numel()))
+        return out
+
+    def status(self) -> int:
+        return Q.qgemm_check_status(self.ws.get(256))
+
+
 class MoELayer:
     """Grouped-MoE W4A16 layer: permute -> GEMM1 (gate|up) -> SiLU gate ->
     GEMM2 (down) -> combine, all on the current stream, no host sync.  When

@@ -67,6 +67,10 @@ constexpr int kSiteAccFull = 1 << 16;       // epilogue: a finished accumulator
 constexpr int kSiteClusterRecv = 1 << 17;   // epilogue: the cluster peers' slices
 constexpr int kSiteSplitCount = 1 << 18;    // split-K finisher: the contributors' count
 constexpr int kSiteSplitCopy = 1 << 19;     // split-K finisher: the copied sum
+constexpr int kSiteW4A4Slot = 1 << 20;      // W4A4 producer: a free pipeline stage
+constexpr int kSiteW4A4Full = 1 << 21;      // W4A4 scale stager / MMA: a landed stage
+constexpr int kSiteW4A4Scales = 1 << 22;    // W4A4 MMA: a stage's scale factors in TMEM
+constexpr int kSiteW4A4Acc = 1 << 23;       // W4A4 epilogue: the finished accumulator
 constexpr int kMaxExperts = 1024;      // grouped GEMM
 constexpr int kMaxPermuteExperts = 256; // MoE permutation
 
@@ -185,6 +189,32 @@ int mma_smem_bytes(int block_bytes, int ring, int nk_max, int rows, int elem_byt
 // smem bytes of dynamic shared memory) that can be resident at once; 0 if
 // unknown.
 int w4a16_max_clusters(int bt, int fmt, int S, int smem);
+
+// W4A4 (NVFP4 weights x NVFP4 activations, kind::mxf4nvf4): one CTA per
+// (token tile, 128-feature tile), the whole K range in 256-k stages.  The
+// four tensor maps are uint8: weight codes {K/2, N} and activation codes
+// {K/2, M} in 128-byte boxes with the 128-byte swizzle, weight and
+// activation block scales {K/16, N} and {K/16, M} in 16-byte boxes.
+struct W4A4Params {
+  int m, n, k;               // k a multiple of 256
+  int kt, nt, mt;            // 256-k stages, 128-feature tiles, token tiles
+  const float* a_ts;         // activation tensor scale (one fp32, device)
+  const float* w_ts;         // weight tensor scale (one fp32, device)
+  const uint16_t* bias;      // [n] bf16 or null
+  uint16_t* c;               // [m, n] bf16
+  int* status;               // workspace status word
+  unsigned long long wait_limit_ns;
+};
+constexpr int kW4A4TileK = 256;
+int w4a4_smem_bytes(int block_tok);
+cudaError_t launch_w4a4(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const CUtensorMap& tm_ws,
+                        const CUtensorMap& tm_as, const W4A4Params& p, int block_tok,
+                        cudaStream_t stream);
+// Per-token NVFP4 quantization of bf16 activations x[m, k] (k % 16 == 0):
+// codes [m, k/2] (k = 2i in the low nibble of byte i), e4m3 block scales
+// [m, k/16]; a_ts is the caller's fp32 tensor scale on the device.
+cudaError_t launch_act_quant_nvfp4(const uint16_t* x, int64_t m, int64_t k, const float* a_ts,
+                                   uint8_t* codes, uint8_t* sb, cudaStream_t stream);
 
 // Host-side plan for one W4A16 launch.
 int device_sm_count();

@@ -346,6 +346,28 @@ __host__ __device__ constexpr uint32_t idesc_mxf8f6f4_e4m3(uint32_t n) {
   return (0u << 7) | (0u << 10) | ((n >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24);
 }
 
+// D[tmem] (+)= (A[smem] * sfa) . (B[smem] * sfb), kind::mxf4nvf4 with one
+// ue4m3 scale per 16 K (scale_vec::4X): A and B packed e2m1 (two codes a
+// byte) in K-major shared-memory tiles, one 32-bit scale column per
+// K=64 step holding the four 16-k blocks' scales, fp32 accumulate.
+__device__ __forceinline__ void mma_ss_mxf4nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t sfa_tmem,
+                                                uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, block-scaled kind::mxf4nvf4: A and B e2m1 (format
+// 1 of this kind), K-major, ue4m3 scale factors (bit 23 clear), M = 128,
+// N = n, scale factor ids 0 (scale_vec::4X uses all four bytes).
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4_e2m1(uint32_t n) {
+  return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | (0u << 23) | ((128u >> 4) << 24);
+}
+
 __host__ __device__ constexpr uint32_t idesc_with_sf_ids(uint32_t idesc, uint32_t a_id,
                                                          uint32_t b_id) {
   return idesc | (b_id << 4) | (a_id << 29);

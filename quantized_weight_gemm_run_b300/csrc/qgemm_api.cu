@@ -154,6 +154,15 @@ static qgemm_status check_layer(const qgemm_layer_config* L) {
         return fail(QGEMM_ERR_UNSUPPORTED, "NVFP4 takes no zero points");
       if (L->scale_format != QGEMM_S_E4M3 || L->group_size != 16)
         return fail(QGEMM_ERR_UNSUPPORTED, "NVFP4 needs e4m3 scales per 16 k");
+      if (L->act_dtype == QGEMM_NVFP4) {   // W4A4
+        if (L->out_dtype != QGEMM_BF16)
+          return fail(QGEMM_ERR_UNSUPPORTED, "W4A4 writes a bf16 output");
+        if (L->k % kW4A4TileK)
+          return fail(QGEMM_ERR_UNSUPPORTED, "W4A4 needs k a multiple of 256");
+        if (L->num_experts != 1 || L->gated_act != QGEMM_ACT_NONE)
+          return fail(QGEMM_ERR_UNSUPPORTED, "W4A4 runs dense, ungated GEMMs");
+        return ok();
+      }
       if (L->act_dtype != QGEMM_FP16 && L->act_dtype != QGEMM_BF16)
         return fail(QGEMM_ERR_UNSUPPORTED, "NVFP4 weights run against fp16 or bf16 activations");
       if (L->out_dtype != L->act_dtype)
@@ -194,6 +203,10 @@ static int st_of(int group) { return group < kTileK ? kTileK / group : 1; }
 
 static bool is_mx(const qgemm_layer_config* L) { return L->weight_format == QGEMM_W_MXFP4; }
 static bool is_nv(const qgemm_layer_config* L) { return L->weight_format == QGEMM_W_NVFP4; }
+// W4A4: NVFP4 weights against activations the library quantizes to NVFP4
+static bool is_w4a4(const qgemm_layer_config* L) {
+  return is_nv(L) && L->act_dtype == QGEMM_NVFP4;
+}
 // W4A8 whose bf16 activations the library quantizes per row to e4m3
 static bool quant_in_lib(const qgemm_layer_config* L) {
   return is_mx(L) && L->act_dtype == QGEMM_BF16;
@@ -618,6 +631,97 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
   return r == CUDA_SUCCESS;
 }
 
+// ------------------------------------------------------------ the W4A4 run
+
+// Workspace: the status word, then the quantized activations (codes
+// [rows, K/2], then e4m3 block scales [rows, K/16]).
+struct W4A4Plan {
+  int bt = 0;
+  int64_t grid = 0;
+  size_t codes_off = 0, sb_off = 0, total = 0;
+};
+
+static qgemm_status w4a4_plan(const qgemm_layer_config* L, const qgemm_tuning_config* T,
+                              int64_t rows, W4A4Plan* P) {
+  *P = W4A4Plan();
+  if (T && (T->stages || T->max_ctas || T->split_k || T->cta_pair || T->kernel > 1 ||
+            T->kernel < 0))
+    return fail(QGEMM_ERR_UNSUPPORTED, "a W4A4 tuning may set block_tok (and kernel = 1) only");
+  const int bt = (T && T->block_tok) ? T->block_tok
+                 : rows <= 16        ? 16
+                 : rows <= 32        ? 32
+                 : rows <= 64        ? 64
+                                     : 128;
+  if (bt != 16 && bt != 32 && bt != 64 && bt != 128)
+    return fail(QGEMM_ERR_UNSUPPORTED, "W4A4 block_tok %d not in {16, 32, 64, 128}", bt);
+  P->bt = bt;
+  P->grid = ((rows + bt - 1) / bt) * (L->n / kTileN);
+  if (P->grid >= (int64_t(1) << 31)) return fail(QGEMM_ERR_UNSUPPORTED, "grid too large");
+  P->codes_off = 256;
+  P->sb_off = P->codes_off + (((size_t)rows * (size_t)(L->k / 2) + 255) & ~size_t(255));
+  P->total = P->sb_off + (((size_t)rows * (size_t)(L->k / 16) + 255) & ~size_t(255));
+  return ok();
+}
+
+static qgemm_status run_w4a4(const qgemm_layer_config* L, const qgemm_tuning_config* T,
+                             int64_t rows, const void* a, const float* a_scale, const void* w,
+                             const void* bias, void* c, void* workspace, size_t ws_bytes,
+                             cudaStream_t stream) {
+  if (rows < 0 || rows > 0x7FFFFFFF) return fail(QGEMM_ERR_INVALID_ARG, "bad row count");
+  if (rows == 0) return ok();
+  if (!device_is_sm103()) return fail(QGEMM_ERR_UNSUPPORTED, "this library runs on sm_103 only");
+  if (!a || !w || !c || (L->has_bias && !bias))
+    return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!a_scale)
+    return fail(QGEMM_ERR_INVALID_ARG, "W4A4 needs a_scale: the activations' fp32 tensor scale");
+  if (!L->has_bias && bias) return fail(QGEMM_ERR_INVALID_ARG, "bias given with has_bias = 0");
+  if (!aligned16(a) || !aligned16(w) || !aligned16(c) || (bias && !aligned16(bias)) ||
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(a_scale) & 3u))
+    return fail(QGEMM_ERR_INVALID_ARG, "pointers must be 16-byte aligned (a_scale 4-byte)");
+  W4A4Plan P;
+  qgemm_status st = w4a4_plan(L, T, rows, &P);
+  if (st != QGEMM_OK) return st;
+  if (!workspace || ws_bytes < P.total)
+    return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", P.total,
+                ws_bytes);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  uint8_t* codes = wsb + P.codes_off;
+  uint8_t* sb = wsb + P.sb_off;
+  const uint64_t n = (uint64_t)L->n, k = (uint64_t)L->k;
+  const uint8_t* wc = static_cast<const uint8_t*>(w);
+  const uint8_t* wsc = wc + n * k / 2;
+  CUtensorMap tm_w, tm_a, tm_ws, tm_as;
+  if (!encode_tmap_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wc, k / 2, n, k / 2, 128, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, k / 2, (uint64_t)rows, k / 2,
+                      128, (uint32_t)P.bt, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&tm_ws, CU_TENSOR_MAP_DATA_TYPE_UINT8, wsc, k / 16, n, k / 16, 16, 128,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tmap_2d(&tm_as, CU_TENSOR_MAP_DATA_TYPE_UINT8, sb, k / 16, (uint64_t)rows, k / 16,
+                      16, (uint32_t)P.bt, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed for a W4A4 operand");
+  W4A4Params p;
+  memset(&p, 0, sizeof(p));
+  p.m = (int)rows;
+  p.n = (int)L->n;
+  p.k = (int)L->k;
+  p.kt = (int)(L->k / kW4A4TileK);
+  p.nt = (int)(L->n / kTileN);
+  p.mt = (int)((rows + P.bt - 1) / P.bt);
+  p.a_ts = a_scale;
+  p.w_ts = reinterpret_cast<const float*>(wsc + n * k / 16);
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.c = static_cast<uint16_t*>(c);
+  p.status = reinterpret_cast<int*>(wsb);
+  p.wait_limit_ns = g_wait_limit_ns;
+  cudaError_t e = launch_act_quant_nvfp4(static_cast<const uint16_t*>(a), rows, (int64_t)k,
+                                         a_scale, codes, sb, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "NVFP4 activation quantization launch");
+  e = launch_w4a4(tm_w, tm_a, tm_ws, tm_as, p, P.bt, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "W4A4 GEMM launch");
+  return ok();
+}
+
 // ------------------------------------------------------------ the W4A16 run
 
 static qgemm_status run_w4a16(const qgemm_layer_config* L, const qgemm_tuning_config* T,
@@ -854,6 +958,14 @@ int run_dense_clearing(const void* layer, const void* compute, const void* tunin
   if (st != QGEMM_OK) return st;
   st = check_compute(C, L, false);
   if (st != QGEMM_OK) return st;
+  if (is_w4a4(L)) {
+    if (clear_bytes && workspace) {
+      cudaError_t ce = cudaMemsetAsync(workspace, 0, clear_bytes, stream);
+      if (ce != cudaSuccess) return cuda_fail(ce, "workspace clear");
+    }
+    return run_w4a4(L, static_cast<const qgemm_tuning_config*>(tuning), m, a, a_scale, packed,
+                    bias, c, workspace, ws_bytes, stream);
+  }
   return run_w4a16(L, static_cast<const qgemm_tuning_config*>(tuning), C, false, nullptr, m, a,
                    a_scale, packed, bias, c, workspace, ws_bytes, clear_bytes, stream);
 }
@@ -868,6 +980,14 @@ int dense_workspace_bytes(const void* layer, const void* compute, const void* tu
   const qgemm_layer_config* L = static_cast<const qgemm_layer_config*>(layer);
   qgemm_status st = check_layer(L);
   if (st != QGEMM_OK) return st;
+  if (is_w4a4(L)) {   // only the status word starts at zero
+    W4A4Plan W;
+    st = w4a4_plan(L, static_cast<const qgemm_tuning_config*>(tuning), m > 0 ? m : 1, &W);
+    if (st != QGEMM_OK) return st;
+    *must_clear = 256;
+    *total = W.total;
+    return QGEMM_OK;
+  }
   Plan P;
   st = make_plan(L, static_cast<const qgemm_tuning_config*>(tuning),
                  static_cast<const qgemm_compute_config*>(compute), m > 0 ? m : 1, false, &P);
@@ -890,6 +1010,10 @@ qgemm_status qgemm_packed_size(const qgemm_layer_config* layer, size_t* bytes) {
   qgemm_status st = check_layer(layer);
   if (st != QGEMM_OK) return st;
   if (!bytes) return fail(QGEMM_ERR_INVALID_ARG, "bytes is NULL");
+  if (is_w4a4(layer)) {   // codes [N, K/2], block scales [N, K/16], the tensor scale
+    *bytes = (size_t)layer->n * (size_t)layer->k / 2 + (size_t)layer->n * (size_t)layer->k / 16 + 16;
+    return ok();
+  }
   *bytes = (size_t)layer->num_experts * expert_packed_bytes(layer);
   if (is_nv(layer)) *bytes += (size_t)((layer->num_experts + 3) / 4) * 16;   // tensor scales
   return ok();
@@ -909,7 +1033,19 @@ qgemm_status qgemm_pack_weights(const qgemm_layer_config* layer, const void* qwe
   if (!aligned16(packed) || !aligned16(qweight))
     return fail(QGEMM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
   cudaError_t e;
-  if (nv) {
+  if (is_w4a4(layer)) {
+    // W4A4 reads the standard format as it is: the copy lays codes, block
+    // scales and the tensor scale end to end
+    if ((reinterpret_cast<uintptr_t>(qzeros) & 3u) != 0)
+      return fail(QGEMM_ERR_INVALID_ARG, "NVFP4 tensor scales must be 4-byte aligned");
+    const size_t cb = (size_t)layer->n * (size_t)layer->k / 2;
+    const size_t sbb = (size_t)layer->n * (size_t)layer->k / 16;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* dst = static_cast<uint8_t*>(packed);
+    e = cudaMemcpyAsync(dst, qweight, cb, cudaMemcpyDefault, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst + cb, scales, sbb, cudaMemcpyDefault, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst + cb + sbb, qzeros, sizeof(float), cudaMemcpyDefault, s);
+  } else if (nv) {
     if ((reinterpret_cast<uintptr_t>(qzeros) & 3u) != 0)
       return fail(QGEMM_ERR_INVALID_ARG, "NVFP4 tensor scales must be 4-byte aligned");
     e = launch_repack_nvfp4(static_cast<const uint8_t*>(qweight),
@@ -955,6 +1091,14 @@ qgemm_status qgemm_workspace_size(const qgemm_layer_config* layer,
   st = check_compute(compute, layer, grouped);
   if (st != QGEMM_OK) return st;
   if (m < 0) return fail(QGEMM_ERR_INVALID_ARG, "m is negative");
+  if (is_w4a4(layer)) {
+    if (grouped) return fail(QGEMM_ERR_UNSUPPORTED, "W4A4 runs dense GEMMs");
+    W4A4Plan W;
+    st = w4a4_plan(layer, tuning, m > 0 ? m : 1, &W);
+    if (st != QGEMM_OK) return st;
+    *bytes = W.total;
+    return ok();
+  }
   Plan P;
   st = make_plan(layer, tuning, compute, m > 0 ? m : 1, grouped, &P);
   if (st != QGEMM_OK) return st;
@@ -977,6 +1121,9 @@ qgemm_status qgemm_run(const qgemm_layer_config* layer, const qgemm_compute_conf
   if (st != QGEMM_OK) return st;
   st = check_compute(compute, layer, false);
   if (st != QGEMM_OK) return st;
+  if (is_w4a4(layer))
+    return run_w4a4(layer, tuning, m, a, a_scale, packed, bias, c, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream));
   return run_w4a16(layer, tuning, compute, false, nullptr, m, a, a_scale,
                    packed, bias, c, workspace,
                    workspace_bytes, 0, static_cast<cudaStream_t>(stream));
@@ -992,6 +1139,7 @@ qgemm_status qgemm_grouped_run(const qgemm_layer_config* layer,
   if (st != QGEMM_OK) return st;
   st = check_compute(compute, layer, true);
   if (st != QGEMM_OK) return st;
+  if (is_w4a4(layer)) return fail(QGEMM_ERR_UNSUPPORTED, "W4A4 runs dense GEMMs");
   return run_w4a16(layer, tuning, compute, true, expert_offsets,
                    total_rows, a, a_scale, packed, bias, c,
                    workspace, workspace_bytes, 0, static_cast<cudaStream_t>(stream));
@@ -1011,6 +1159,25 @@ qgemm_status qgemm_quantize_act_fp8(const void* x, int64_t m, int64_t k, void* a
                                        static_cast<uint8_t*>(a8), a_scale,
                                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "activation quantization launch");
+  return ok();
+}
+
+qgemm_status qgemm_quantize_act_nvfp4(const void* x, int64_t m, int64_t k, const float* a_ts,
+                                      void* codes, void* block_scales, void* stream) {
+  if (m < 0 || k <= 0) return fail(QGEMM_ERR_INVALID_ARG, "bad shape");
+  if (k % 16) return fail(QGEMM_ERR_UNSUPPORTED, "k must be a multiple of 16");
+  if (m > (1 << 30) || k > (1 << 30)) return fail(QGEMM_ERR_UNSUPPORTED, "m or k above 2^30");
+  if (m == 0) return ok();
+  if (!x || !a_ts || !codes || !block_scales)
+    return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u) ||
+      (reinterpret_cast<uintptr_t>(a_ts) & 3u))
+    return fail(QGEMM_ERR_INVALID_ARG, "x must be 16-byte, codes 8-byte, a_ts 4-byte aligned");
+  cudaError_t e = launch_act_quant_nvfp4(static_cast<const uint16_t*>(x), m, k, a_ts,
+                                         static_cast<uint8_t*>(codes),
+                                         static_cast<uint8_t*>(block_scales),
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "NVFP4 activation quantization launch");
   return ok();
 }
 
@@ -1067,6 +1234,8 @@ qgemm_status qgemm_debug_dequant(const qgemm_layer_config* layer, const void* pa
   qgemm_status st = check_layer(layer);
   if (st != QGEMM_OK) return st;
   if (!packed || !out_kn) return fail(QGEMM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (is_w4a4(layer))
+    return fail(QGEMM_ERR_UNSUPPORTED, "a W4A4 buffer holds the standard tensors as they are");
   cudaError_t e;
   if (is_mx(layer))
     e = launch_debug_mx_codes(static_cast<const uint8_t*>(packed), static_cast<uint8_t*>(out_kn),
@@ -1137,8 +1306,22 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
   qgemm_status st = check_layer(layer);
   const bool grouped = compute && compute->gemm_type == QGEMM_GEMM_GROUPED;
   if (st == QGEMM_OK) st = check_compute(compute, layer, grouped);
+  W4A4Plan W;
+  if (st == QGEMM_OK && is_w4a4(layer))
+    st = grouped ? fail(QGEMM_ERR_UNSUPPORTED, "W4A4 runs dense GEMMs")
+                 : w4a4_plan(layer, nullptr, m > 0 ? m : 1, &W);
   if (st != QGEMM_OK) {
     rec = std::string("rejected: ") + g_last_error;
+  } else if (is_w4a4(layer)) {
+    char tmp[384];
+    snprintf(tmp, sizeof(tmp),
+             "kernel=w4a4_tcgen05_mxf4nvf4 weights=nvfp4 group=16 scales=e4m3 act=nvfp4 out=bf16 "
+             "n=%lld k=%lld m=%lld experts=1 block_tok=%d stages=6 grid=%lld smem=%d "
+             "workspace=%zu epilogue=%s split=whole_tiles act_quant=separate_kernel "
+             "device=sm_103",
+             (long long)layer->n, (long long)layer->k, (long long)m, W.bt, (long long)W.grid,
+             w4a4_smem_bytes(W.bt), W.total, layer->has_bias ? "bias" : "plain");
+    rec = tmp;
   } else {
     Plan P;
     st = make_plan(layer, nullptr, compute, m > 0 ? m : 1, grouped, &P);
@@ -1147,7 +1330,7 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
     } else {
       static const char* wf[] = {"int4_sym", "uint4_zp", "mxfp4",    "nvfp4",
                                  "int8_sym", "uint8_zp", "int3_sym", "uint3_zp"};
-      static const char* dt[] = {"fp16", "bf16", "fp8e4m3"};
+      static const char* dt[] = {"fp16", "bf16", "fp8e4m3", "nvfp4"};
       static const char* sf[] = {"fp16", "bf16", "e8m0", "e4m3"};
       char tmp[512];
       snprintf(tmp, sizeof(tmp),

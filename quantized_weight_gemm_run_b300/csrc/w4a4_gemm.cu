@@ -1,0 +1,313 @@
+// W4A4: NVFP4 weights against NVFP4 activations on the block-scaled FP4
+// tensor cores (tcgen05.mma kind::mxf4nvf4).  The pages list W4A4 among the
+// common configurations and name NVFP4 (e2m1 codes with an e4m3 scale per 16
+// elements and an fp32 tensor scale) as a format whose number format and
+// scaling differ from INT4's (kinachrichten.com, "Warum quantisierte Kernel
+// wichtig sind").
+//
+// Two kernels:
+//   act_quant_nvfp4_kernel  bf16 activations -> e2m1 codes and e4m3 block
+//                           scales per 16 k of each token, against the
+//                           caller's fp32 tensor scale (every decision in
+//                           fp32: d = 6 a_ts, t = amax / d, s = e4m3(t),
+//                           q = x / (s a_ts), code = e2m1(q))
+//   w4a4_kernel<BT>         one CTA per (BT-token, 128-feature) tile over the
+//                           whole K range: both operands stay packed (two
+//                           codes a byte) from HBM to the tensor core, the
+//                           block scales go to tensor memory, and the
+//                           epilogue multiplies the fp32 sums by the two
+//                           tensor scales.
+//
+// Roles of the 8 warps: 0 TMA producer, 1 MMA issuer, 2 tensor-memory
+// allocation, 4-7 block scales into tensor memory, then the epilogue (warp w
+// owns tensor-memory lanes 32 (w - 4) ... + 31).
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qg {
+namespace {
+
+constexpr int kStages = 6;      // pipeline depth (256 k a stage)
+constexpr int kThreads = 256;
+
+template <int BT>
+struct Lay {
+  static constexpr int kA = 128 * 128;   // weight codes: 128 features x 128 bytes (256 k)
+  static constexpr int kB = BT * 128;    // activation codes
+  static constexpr int kSA = 128 * 16;   // weight block scales: 128 x 16 bytes
+  static constexpr int kSB = BT * 16;    // activation block scales
+  static constexpr int kOffB = kA;
+  static constexpr int kOffSA = kA + kB;
+  static constexpr int kOffSB = kA + kB + kSA;
+  static constexpr int kBytes = kA + kB + kSA + kSB;           // TMA bytes a stage
+  static constexpr int kStage = (kBytes + 1023) / 1024 * 1024;  // 1 KB aligned (swizzle atoms)
+  static constexpr int kBar = kStages * kStage;
+  static constexpr int kSmem = 1024 + kBar + 256;   // alignment slack, ring, barriers
+  // tensor memory: the accumulator in columns [0, BT), then per stage and
+  // K=64 step a group of four columns of weight scales and a group of four
+  // of activation scales.  A group holds the 32-bit scale words (byte i: the
+  // scale of the step's 16-k block i) of 128 rows, row r in column r / 32 at
+  // lane r mod 32 of every 32-lane quadrant (each quadrant of the tensor
+  // core reads its own copy); a group starts on a multiple of four columns.
+  static constexpr int kColSA = BT;
+  static constexpr int kColSB = BT + 16 * kStages;
+  static constexpr int kUsed = BT + 32 * kStages;
+  static constexpr int kCols = kUsed <= 128 ? 128 : kUsed <= 256 ? 256 : 512;
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         const W4A4Params& p, int site) {
+  return mbar_wait(bar, parity, abort_flag, p.status, p.wait_limit_ns, kStatusTimeout | site);
+}
+
+// Bounded wait that ignores the abort flag: at exit, lets the copies and
+// MMAs already issued finish before their shared or tensor memory goes away.
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_test_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer();
+  while (globaltimer() - t0 < limit_ns)
+    if (mbar_try_wait(bar, parity)) return;
+}
+
+template <int BT>
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
+                const __grid_constant__ CUtensorMap tm_ws,
+                const __grid_constant__ CUtensorMap tm_as, const W4A4Params p) {
+  using L = Lay<BT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* empty = full + kStages;
+  uint64_t* sf_full = empty + kStages;
+  uint64_t* acc_full = sf_full + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nt = blockIdx.x % p.nt, mt = blockIdx.x / p.nt;
+  const int n0 = nt * 128, m0 = mt * BT;
+  const uint64_t drain_ns = p.wait_limit_ns + 1000000000ull;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&sf_full[s], 4);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, L::kCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_ws);
+    prefetch_tmap(&tm_as);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kt = 0; kt < p.kt; ++kt) {
+        const int s = kt % kStages;
+        if (kt >= kStages &&
+            !wait_bar(&empty[s], ((kt / kStages) - 1) & 1, abort_flag, p, kSiteW4A4Slot))
+          break;
+        uint8_t* st = smem + s * L::kStage;
+        mbar_arrive_expect_tx(&full[s], L::kBytes);
+        tma_load_2d(st, &tm_w, &full[s], kt * 128, n0);
+        tma_load_2d(st + L::kOffB, &tm_a, &full[s], kt * 128, m0);
+        tma_load_2d(st + L::kOffSA, &tm_ws, &full[s], kt * 16, n0);
+        tma_load_2d(st + L::kOffSB, &tm_as, &full[s], kt * 16, m0);
+        ++issued;
+      }
+      for (int kt = issued > kStages ? issued - kStages : 0; kt < issued; ++kt)
+        drain_bar(&full[kt % kStages], (kt / kStages) & 1, drain_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t idesc = idesc_mxf4nvf4_e2m1(BT);
+      for (int kt = 0; kt < p.kt; ++kt) {
+        const int s = kt % kStages;
+        const uint32_t ph = (kt / kStages) & 1;
+        if (!wait_bar(&full[s], ph, abort_flag, p, kSiteW4A4Full)) break;
+        if (!wait_bar(&sf_full[s], ph, abort_flag, p, kSiteW4A4Scales)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(smem + s * L::kStage), b0 = a0 + L::kOffB;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)   // four K=64 steps of 32 bytes through each 128-byte row
+          mma_ss_mxf4nvf4(tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j), idesc,
+                          tmem + L::kColSA + 16 * s + 4 * j, tmem + L::kColSB + 16 * s + 4 * j,
+                          (kt > 0 || j > 0) ? 1u : 0u);
+        mma_commit(&empty[s]);
+      }
+      mma_commit(acc_full);   // arrives once every MMA issued above has finished
+      drain_bar(acc_full, 0, drain_ns);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------ block scales, then the epilogue
+    const int q = warp - 4;
+    const int r = q * 32 + lane;   // this thread's tensor-memory lane (epilogue: feature row)
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    bool ok = true;
+    for (int kt = 0; kt < p.kt && ok; ++kt) {
+      const int s = kt % kStages;
+      if (lane == 0) ok = wait_bar(&full[s], (kt / kStages) & 1, abort_flag, p, kSiteW4A4Full);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      const uint8_t* st = smem + s * L::kStage;
+      // this quadrant's copy of the stage's four scale groups: column 4j + c
+      // holds word j (the scales of step j's four 16-k blocks) of row
+      // 32 c + lane; activation rows past the tile hold zero
+      uint32_t va[16], vb[16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int row = 32 * c + lane;
+        const uint4 a4 = *reinterpret_cast<const uint4*>(st + L::kOffSA + row * 16);
+        uint4 b4 = make_uint4(0u, 0u, 0u, 0u);
+        if (row < BT) b4 = *reinterpret_cast<const uint4*>(st + L::kOffSB + row * 16);
+        va[c] = a4.x, va[4 + c] = a4.y, va[8 + c] = a4.z, va[12 + c] = a4.w;
+        vb[c] = b4.x, vb[4 + c] = b4.y, vb[8 + c] = b4.z, vb[12 + c] = b4.w;
+      }
+      tmem_st16(tmem + lane_addr + L::kColSA + 16 * s, va);
+      tmem_st16(tmem + lane_addr + L::kColSB + 16 * s, vb);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sf_full[s]);
+    }
+    if (ok) {
+      if (lane == 0) ok = wait_bar(acc_full, 0, abort_flag, p, kSiteW4A4Acc);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float sc = __fmul_rn(*p.a_ts, *p.w_ts);
+      const int n = n0 + r;
+      float bias = 0.f;
+      if (p.bias && qg_check(n < p.n, p.status)) bias = __bfloat162float(__ushort_as_bfloat16(p.bias[n]));
+#pragma unroll 1
+      for (int c0 = 0; c0 < BT; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16_wait(tmem + lane_addr + c0, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = m0 + c0 + j;
+          if (tok < p.m && qg_check(n < p.n, p.status)) {
+            const float o = fmaf(__uint_as_float(v[j]), sc, bias);
+            p.c[(long long)tok * p.n + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, L::kCols);
+}
+
+// One thread per 16-k block of a token: two 16-byte loads, the block maximum,
+// the e4m3 scale, sixteen fp32 divides and e2m1 conversions, one 8-byte code
+// store and one scale byte.
+__global__ void __launch_bounds__(256)
+    act_quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t m, int64_t k,
+                           const float* __restrict__ a_ts, uint8_t* __restrict__ codes,
+                           uint8_t* __restrict__ sb) {
+  const int64_t nb = k >> 4;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= m * nb) return;
+  const int64_t row = i / nb, b = i - row * nb;
+  const uint4* src = reinterpret_cast<const uint4*>(x + row * k + b * 16);
+  const uint4 u0 = src[0], u1 = src[1];
+  const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  float f[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {   // bf16 -> fp32 is exact: the bits move up
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  const float ts = *a_ts;
+  const float t = __fdiv_rn(amax, __fmul_rn(6.0f, ts));
+  const __nv_fp8_storage_t sbyte = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+  const float s = __half2float(__half(__nv_cvt_fp8_to_halfraw(sbyte, __NV_E4M3)));
+  const float den = __fmul_rn(s, ts);
+  uint32_t lo = 0, hi = 0;
+  if (den > 0.f) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 qq = make_float2(__fdiv_rn(f[2 * j], den), __fdiv_rn(f[2 * j + 1], den));
+      const uint32_t byte = __nv_cvt_float2_to_fp4x2(qq, __NV_E2M1, cudaRoundNearest);
+      if (j < 4) lo |= byte << (8 * j);
+      else hi |= byte << (8 * (j - 4));
+    }
+  }
+  *reinterpret_cast<uint2*>(codes + row * (k >> 1) + b * 8) = make_uint2(lo, hi);
+  sb[row * nb + b] = sbyte;
+}
+
+template <int BT>
+cudaError_t launch_bt(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const CUtensorMap& tm_ws,
+                      const CUtensorMap& tm_as, const W4A4Params& p, cudaStream_t stream) {
+  using L = Lay<BT>;
+  cudaError_t e = cudaFuncSetAttribute(w4a4_kernel<BT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  if (e != cudaSuccess) return e;
+  w4a4_kernel<BT><<<p.mt * p.nt, kThreads, L::kSmem, stream>>>(tm_w, tm_a, tm_ws, tm_as, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int w4a4_smem_bytes(int block_tok) {
+  switch (block_tok) {
+    case 16: return Lay<16>::kSmem;
+    case 32: return Lay<32>::kSmem;
+    case 64: return Lay<64>::kSmem;
+    case 128: return Lay<128>::kSmem;
+    default: return 0;
+  }
+}
+
+cudaError_t launch_w4a4(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const CUtensorMap& tm_ws,
+                        const CUtensorMap& tm_as, const W4A4Params& p, int block_tok,
+                        cudaStream_t stream) {
+  switch (block_tok) {
+    case 16: return launch_bt<16>(tm_w, tm_a, tm_ws, tm_as, p, stream);
+    case 32: return launch_bt<32>(tm_w, tm_a, tm_ws, tm_as, p, stream);
+    case 64: return launch_bt<64>(tm_w, tm_a, tm_ws, tm_as, p, stream);
+    case 128: return launch_bt<128>(tm_w, tm_a, tm_ws, tm_as, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_act_quant_nvfp4(const uint16_t* x, int64_t m, int64_t k, const float* a_ts,
+                                   uint8_t* codes, uint8_t* sb, cudaStream_t stream) {
+  const int64_t blocks = m * (k >> 4);
+  if (blocks == 0) return cudaSuccess;
+  const int64_t grid = (blocks + 255) / 256;
+  if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  act_quant_nvfp4_kernel<<<(unsigned)grid, 256, 0, stream>>>(x, m, k, a_ts, codes, sb);
+  return cudaGetLastError();
+}
+
+}  // namespace qg

@@ -31,7 +31,7 @@ QGEMM_W_INT8_SYM, QGEMM_W_UINT8_ZP = 4, 5
 QGEMM_W_INT3_SYM, QGEMM_W_UINT3_ZP = 6, 7
 QGEMM_S_FP16, QGEMM_S_BF16, QGEMM_S_E8M0, QGEMM_S_E4M3 = 0, 1, 2, 3
 QGEMM_Z_NONE, QGEMM_Z_UINT4, QGEMM_Z_UINT8, QGEMM_Z_UINT3 = 0, 1, 2, 3
-QGEMM_FP16, QGEMM_BF16, QGEMM_FP8E4M3 = 0, 1, 2
+QGEMM_FP16, QGEMM_BF16, QGEMM_FP8E4M3, QGEMM_NVFP4 = 0, 1, 2, 3
 QGEMM_GEMM_DENSE, QGEMM_GEMM_GROUPED = 0, 1
 QGEMM_ACT_NONE, QGEMM_ACT_SILU_GLU = 0, 1
 
@@ -88,6 +88,7 @@ _SIGS = {
     "qgemm_run_noalloc": [_L, _C, _T, _I64, _P, _P, _P, _P, _P, _P],
     "qgemm_grouped_run": [_L, _C, _T, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "qgemm_quantize_act_fp8": [_P, _I64, _I64, _P, _P, _P],
+    "qgemm_quantize_act_nvfp4": [_P, _I64, _I64, _P, _P, _P, _P],
     "qgemm_moe_permute": [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _I64, _P],
     "qgemm_moe_silu_mul": [_P, _I64, _I64, _P, _P],
     "qgemm_moe_combine": [_P, _P, _P, _I64, _I32, _I64, _P, _P],
@@ -209,6 +210,11 @@ def qgemm_grouped_run(layer, compute, tuning, expert_offsets, total_rows, a, a_s
 
 def qgemm_quantize_act_fp8(x, m, k, a8, a_scale, stream=None):
     return lib.qgemm_quantize_act_fp8(_ptr(x), m, k, _ptr(a8), _ptr(a_scale), _stream(stream))
+
+
+def qgemm_quantize_act_nvfp4(x, m, k, a_ts, codes, block_scales, stream=None):
+    return lib.qgemm_quantize_act_nvfp4(_ptr(x), m, k, _ptr(a_ts), _ptr(codes),
+                                        _ptr(block_scales), _stream(stream))
 
 
 def qgemm_moe_permute(topk_ids, t, topk, e, offsets, perm, inv_perm, a, a_perm, hidden,
