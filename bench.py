@@ -11,6 +11,7 @@ CUDA graph and replayed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload sweep|w4a16_m16|large|w4a8|moe16|moe256|moe4096|
+                              f16s|w8a16|nvfp4|w4a4|w4a4_large|
                               shape:M,N,K[,sym|asym][,bf16|fp16]]
 
 Other workloads (--workload) are for kernel studies and print the same line
@@ -91,6 +92,18 @@ def workload_points(name):
                 dict(workload="w4a16_nvfp4_sweep", shapes=synth.W4A16_ASYM_SHAPES,
                      ms=synth.W4A16_ASYM_MS, group=16, weights="nvfp4 (e2m1 + e4m3/16 + fp32)",
                      act="bf16"))
+    if name == "w4a4":
+        # the sweep's shapes with NVFP4 weights and NVFP4 activations
+        return ([dict(p, kind="w4a4", g=16, asym=False) for p in sweep_points()],
+                dict(workload="w4a4_nvfp4_sweep", shapes=synth.W4A16_ASYM_SHAPES,
+                     ms=synth.W4A16_ASYM_MS, group=16,
+                     weights="nvfp4 (e2m1 + e4m3/16 + fp32)",
+                     act="bf16 -> nvfp4 per token (e2m1 + e4m3/16, fp32 tensor scale)"))
+    if name == "w4a4_large":
+        s = synth.LARGE_SHAPE
+        return ([dict(kind="w4a4", m=s["m"], n=s["n"], k=s["k"], g=16, asym=False, adt="bf16")],
+                dict(workload="w4a4_nvfp4_8192x8192x8192", m=s["m"], n=s["n"], k=s["k"],
+                     weights="nvfp4", act="bf16 -> nvfp4 per token"))
     if name == "w4a16_m16":
         s = synth.W4A16_SYM_SHAPE
         return [dict(m=s["m"], n=s["n"], k=s["k"], g=128, asym=False, adt="fp16")], dict(
@@ -136,6 +149,10 @@ def point_bytes(p):
     if kind == "nvfp4":
         # codes, block scales as the kernel reads them (16-bit per 16 k), activations, output
         return n * k // 2 + (k // 16) * n * 2 + m * k * 2 + m * n * 2
+    if kind == "w4a4":
+        # bf16 activations read by the quantizer, its codes and block scales
+        # written and read back by the GEMM, weight codes and block scales, output
+        return 2 * m * k + 2 * (m * k // 2 + m * k // 16) + n * k // 2 + n * k // 16 + 2 * m * n
     if kind == "moe":
         s = synth.MOE_SHAPE
         e, h, i, topk = s["experts"], s["hidden"], s["inter"], s["topk"]
@@ -257,6 +274,15 @@ class GemmPoint:
                 qzeros = torch.from_numpy(synth.random_words(g, (k // gs, n // 4))).to(device)
                 self.lin = W8A16Linear(qweight, scales, qzeros, n, k, gs, dt)
                 del qweight, scales, qzeros
+            elif p.get("kind") == "w4a4":
+                from quantized_weight_gemm_run_b300.api import W4A4Linear
+                codes = torch.from_numpy(synth.random_bytes(g, (n, k // 2))).to(device)
+                sb = torch.from_numpy(synth.random_bytes(g, (n, k // 16), 0x30, 0x48)).to(device)
+                ts = torch.full((1,), 2.0 ** -9, dtype=torch.float32, device=device)
+                # activations ~ N(0, 1): a tensor scale that maps |x| = 6 to 448 * 6
+                a_ts = torch.full((1,), 6.0 / (6 * 448), dtype=torch.float32, device=device)
+                self.lin = W4A4Linear(codes, sb, ts, a_ts, n, k)
+                del codes, sb
             elif p.get("kind") == "nvfp4":
                 codes = torch.from_numpy(synth.random_bytes(g, (n, k // 2))).to(device)
                 sb = torch.from_numpy(synth.random_bytes(g, (n, k // 16), 0x30, 0x48)).to(device)
@@ -279,6 +305,7 @@ class GemmPoint:
             self.lin.packed = src.lin.packed.clone()
             self.a = src.a.clone()
         self.layer = self.lin.layer_bf16 if self.mx else self.lin.layer
+        self.a_scale = self.lin.act_scale if p.get("kind") == "w4a4" else None
         self.c = torch.empty(m, n, dtype=dt, device=device)
         st, nbytes = Q.qgemm_workspace_size(self.layer, self.lin.dense, None, m)
         Q.check(st)
@@ -286,7 +313,7 @@ class GemmPoint:
         if host:
             self.a_host = self.a.cpu().pin_memory()
             self.c_host = torch.empty(m, n, dtype=dt).pin_memory()
-        self.launches = 2 if self.mx and m > 16 else 1
+        self.launches = 2 if (self.mx and m > 16) or p.get("kind") == "w4a4" else 1
 
     def clone(self):
         return GemmPoint(self.p, 0, self.c.device, src=self)
@@ -294,7 +321,7 @@ class GemmPoint:
     def launch(self):
         Q = self.Q
         m = self.p["m"]
-        Q.check(Q.qgemm_run(self.layer, self.lin.dense, None, m, self.a, None,
+        Q.check(Q.qgemm_run(self.layer, self.lin.dense, None, m, self.a, self.a_scale,
                             self.lin.packed, None, self.c, self.ws, self.ws.numel()))
 
     def copy_in(self):
@@ -452,6 +479,9 @@ def kernel_name(p):
     if kind == "moe":
         return "moe_layer (sort, gather, SiLU-gated grouped GEMM, grouped GEMM, combine)"
     m = p["m"]
+    if kind == "w4a4":
+        bt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
+        return f"act_quant_nvfp4_kernel + w4a4_kernel<{bt}>"
     nv_small = kind == "nvfp4" and (p["n"] * p["k"] <= 1 << 24 or (m <= 8 and p["k"] <= 4096))
     if (kind in ("w4a16", "w4a8") or nv_small) and m <= 16:
         # the planner's default for dense INT4/UINT4 and W4A8 GEMMs of at most
@@ -469,7 +499,7 @@ def kernel_name(p):
     return "act_quant_fp8_kernel + " + name if kind == "w4a8" else name
 
 
-EXTRA_WORKLOADS = ["w4a16_m16", "w4a8", "moe16", "moe256", "moe4096", "large"]
+EXTRA_WORKLOADS = ["w4a16_m16", "w4a8", "moe16", "moe256", "moe4096", "large", "w4a4_large"]
 REPLAYS = 7
 
 
@@ -550,6 +580,10 @@ def measure_point(bp, p, peaks, stream):
     if p.get("kind") == "w4a8":
         fp8 = peaks.get("fp8_tflops")
         d["fp8_tensor_frac"] = round(fl / med / 1e6 / fp8, 3) if fp8 else None
+    elif p.get("kind") == "w4a4":
+        # dense FP4 peak: the measured bf16 peak times the nominal FP4 / bf16
+        # ratio (13.5 / 2.25 PFLOP/s)
+        d["fp4_tensor_frac"] = round(fl / med / 1e6 / (peaks["bf16_tflops"] * 6.0), 3)
     else:
         d["tensor_frac"] = round(fl / med / 1e6 / peaks["bf16_tflops"], 3)
     if is_moe:
@@ -728,12 +762,15 @@ def run_ours(args, rank, world, device):
     dom = max(share.items(), key=lambda kv: kv[1][0])   # over the workload's own GEMMs
     dom_us, dom_flops, dom_bytes, dom_ms = dom[1]
     dom_launches = len(dom_ms)
-    tensor_bound = (dom_flops / dom_bytes) > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    # W4A4 runs on the FP4 tensor cores: its peak is the measured bf16 peak
+    # times the nominal dense FP4 / bf16 ratio (13.5 / 2.25 PFLOP/s)
+    fp4 = pts[0].get("kind") == "w4a4"
+    t_peak = peaks["bf16_tflops"] * (6.0 if fp4 else 1.0)
+    tensor_bound = (dom_flops / dom_bytes) > t_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if tensor_bound:
         achieved = dom_flops / dom_us / 1e6
-        roof = dict(bound="tensor", achieved=round(achieved, 2), peak=peaks["bf16_tflops"],
-                    unit="TFLOP/s", frac=round(achieved / peaks["bf16_tflops"], 4),
-                    traffic=None)
+        roof = dict(bound="tensor", achieved=round(achieved, 2), peak=round(t_peak, 1),
+                    unit="TFLOP/s", frac=round(achieved / t_peak, 4), traffic=None)
     else:
         achieved = dom_bytes / dom_us / 1e3
         roof = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
@@ -748,7 +785,7 @@ def run_ours(args, rank, world, device):
         roof["traffic"] = int(sum(traffic[k][0] for k in keys) / len(keys))
     roof.update(kernel=dom[0], launches_per_step=dom_launches,
                 per_launch="algorithmic bytes/flops of its GEMMs / mean CUDA-event time per launch",
-                peak_source=f"{peak_src} ({'bf16 burst' if tensor_bound else 'copy bandwidth'})")
+                peak_source=f"{peak_src} ({'copy bandwidth' if not tensor_bound else 'bf16 burst x 6, the nominal FP4 / bf16 ratio' if fp4 else 'bf16 burst'})")
 
     # end to end through the C ABI with host buffers (pinned), copies inside the
     # timed region: every step copies each GEMM's activations in and its output
@@ -897,6 +934,15 @@ def _oracle_point(p, seed):
         a = codecs.bf16(synth.activations_fp32(g, m, k))
         gemm.w4a16_output(a, quant.dequant_nvfp4(ckn, skn, 2.0 ** -9), "bf16")
         return point_flops(p)
+    if kind == "w4a4":
+        codes = synth.random_bytes(g, (n, k // 2))
+        sb = synth.random_bytes(g, (n, k // 16), 0x30, 0x48)
+        ckn, skn = quant.unpack_nvfp4(codes, sb)
+        x = codecs.bf16(synth.activations_fp32(g, m, k))
+        a_ts = 6.0 / (6 * 448)
+        ac, asb = gemm.act_quant_nvfp4(x, a_ts)
+        gemm.w4a4_output(ac, asb, a_ts, ckn, skn, 2.0 ** -9)
+        return point_flops(p)
     if kind == "moe":
         s = synth.MOE_SHAPE
         e, h, i, topk, t = s["experts"], s["hidden"], s["inter"], s["topk"], 2
@@ -993,8 +1039,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sweep",
-                    help="sweep | f16s | w8a16 | nvfp4 | w4a16_m16 | large | w4a8 | moe16 | "
-                         "moe256 | moe4096 | shape:M,N,K[,sym|asym][,bf16|fp16][,f16s]")
+                    help="sweep | f16s | w8a16 | nvfp4 | w4a4 | w4a4_large | w4a16_m16 | large | "
+                         "w4a8 | moe16 | moe256 | moe4096 | "
+                         "shape:M,N,K[,sym|asym][,bf16|fp16][,f16s]")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-extra", action="store_true",
                     help="sweep only: skip timing the other configurations")

@@ -11,16 +11,18 @@
 //                           caller's fp32 tensor scale (every decision in
 //                           fp32: d = 6 a_ts, t = amax / d, s = e4m3(t),
 //                           q = x / (s a_ts), code = e2m1(q))
-//   w4a4_kernel<BT>         one CTA per (BT-token, 128-feature) tile over the
-//                           whole K range: both operands stay packed (two
-//                           codes a byte) from HBM to the tensor core, the
-//                           block scales go to tensor memory, and the
-//                           epilogue multiplies the fp32 sums by the two
-//                           tensor scales.
+//   w4a4_kernel<BT>         persistent, one CTA per SM over the (BT-token,
+//                           128-feature) tiles, each over the whole K range:
+//                           both operands stay packed (two codes a byte) from
+//                           HBM to the tensor core, the block scales go to
+//                           tensor memory, and the epilogue multiplies the
+//                           fp32 sums by the two tensor scales; two
+//                           accumulators let a tile's epilogue run under the
+//                           next tile's MMAs.
 //
-// Roles of the 8 warps: 0 TMA producer, 1 MMA issuer, 2 tensor-memory
-// allocation, 4-7 block scales into tensor memory, then the epilogue (warp w
-// owns tensor-memory lanes 32 (w - 4) ... + 31).
+// Roles of the 12 warps: 0 TMA producer, 1 MMA issuer, 2 tensor-memory
+// allocation, 4-7 block scales into tensor memory, 8-11 the epilogue (warps
+// w and w + 4 own tensor-memory lanes 32 (w - 4) ... + 31).
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
@@ -31,7 +33,7 @@ namespace qg {
 namespace {
 
 constexpr int kStages = 6;      // pipeline depth (256 k a stage)
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 
 template <int BT>
 struct Lay {
@@ -46,15 +48,15 @@ struct Lay {
   static constexpr int kStage = (kBytes + 1023) / 1024 * 1024;  // 1 KB aligned (swizzle atoms)
   static constexpr int kBar = kStages * kStage;
   static constexpr int kSmem = 1024 + kBar + 256;   // alignment slack, ring, barriers
-  // tensor memory: the accumulator in columns [0, BT), then per stage and
+  // tensor memory: two accumulators in columns [0, 2 BT), then per stage and
   // K=64 step a group of four columns of weight scales and a group of four
   // of activation scales.  A group holds the 32-bit scale words (byte i: the
   // scale of the step's 16-k block i) of 128 rows, row r in column r / 32 at
   // lane r mod 32 of every 32-lane quadrant (each quadrant of the tensor
   // core reads its own copy); a group starts on a multiple of four columns.
-  static constexpr int kColSA = BT;
-  static constexpr int kColSB = BT + 16 * kStages;
-  static constexpr int kUsed = BT + 32 * kStages;
+  static constexpr int kColSA = 2 * BT;
+  static constexpr int kColSB = 2 * BT + 16 * kStages;
+  static constexpr int kUsed = 2 * BT + 32 * kStages;
   static constexpr int kCols = kUsed <= 128 ? 128 : kUsed <= 256 ? 256 : 512;
 };
 
@@ -84,13 +86,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* empty = full + kStages;
   uint64_t* sf_full = empty + kStages;
-  uint64_t* acc_full = sf_full + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* acc_full = sf_full + kStages;   // two accumulator buffers
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int nt = blockIdx.x % p.nt, mt = blockIdx.x / p.nt;
-  const int n0 = nt * 128, m0 = mt * BT;
+  const int tiles = p.mt * p.nt;
   const uint64_t drain_ns = p.wait_limit_ns + 1000000000ull;
 
   if (threadIdx.x == 0) {
@@ -99,7 +102,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
       mbar_init(&sf_full[s], 4);
     }
-    mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -118,94 +125,123 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Persistent: CTA b takes tiles b, b + grid, ...; tile t is (token tile
+  // t / nt, feature tile t % nt).  The stage ring runs on across tiles
+  // (stage use g = the CTA's running count of 256-k stages).
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
-      for (int kt = 0; kt < p.kt; ++kt) {
-        const int s = kt % kStages;
-        if (kt >= kStages &&
-            !wait_bar(&empty[s], ((kt / kStages) - 1) & 1, abort_flag, p, kSiteW4A4Slot))
-          break;
-        uint8_t* st = smem + s * L::kStage;
-        mbar_arrive_expect_tx(&full[s], L::kBytes);
-        tma_load_2d(st, &tm_w, &full[s], kt * 128, n0);
-        tma_load_2d(st + L::kOffB, &tm_a, &full[s], kt * 128, m0);
-        tma_load_2d(st + L::kOffSA, &tm_ws, &full[s], kt * 16, n0);
-        tma_load_2d(st + L::kOffSB, &tm_as, &full[s], kt * 16, m0);
-        ++issued;
+      int g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+        const int n0 = (t % p.nt) * 128, m0 = (t / p.nt) * BT;
+        for (int kt = 0; kt < p.kt; ++kt, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages &&
+              !wait_bar(&empty[s], ((g / kStages) - 1) & 1, abort_flag, p, kSiteW4A4Slot)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * L::kStage;
+          mbar_arrive_expect_tx(&full[s], L::kBytes);
+          tma_load_2d(st, &tm_w, &full[s], kt * 128, n0);
+          tma_load_2d(st + L::kOffB, &tm_a, &full[s], kt * 128, m0);
+          tma_load_2d(st + L::kOffSA, &tm_ws, &full[s], kt * 16, n0);
+          tma_load_2d(st + L::kOffSB, &tm_as, &full[s], kt * 16, m0);
+        }
       }
-      for (int kt = issued > kStages ? issued - kStages : 0; kt < issued; ++kt)
-        drain_bar(&full[kt % kStages], (kt / kStages) & 1, drain_ns);
+      // let the copies already issued land before the CTA may exit
+      for (int u = g > kStages ? g - kStages : 0; u < g; ++u)
+        drain_bar(&full[u % kStages], (u / kStages) & 1, drain_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (elect_one()) {
       constexpr uint32_t idesc = idesc_mxf4nvf4_e2m1(BT);
-      for (int kt = 0; kt < p.kt; ++kt) {
-        const int s = kt % kStages;
-        const uint32_t ph = (kt / kStages) & 1;
-        if (!wait_bar(&full[s], ph, abort_flag, p, kSiteW4A4Full)) break;
-        if (!wait_bar(&sf_full[s], ph, abort_flag, p, kSiteW4A4Scales)) break;
+      int g = 0, i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++i) {
+        const int b = i & 1;
+        if (!wait_bar(&acc_empty[b], ((i >> 1) & 1) ^ 1, abort_flag, p, kSiteW4A4Acc)) break;
         tc_fence_after();
-        const uint32_t a0 = smem_u32(smem + s * L::kStage), b0 = a0 + L::kOffB;
+        const uint32_t d_tmem = tmem + b * BT;
+        for (int kt = 0; kt < p.kt; ++kt, ++g) {
+          const int s = g % kStages;
+          const uint32_t ph = (g / kStages) & 1;
+          if (!wait_bar(&full[s], ph, abort_flag, p, kSiteW4A4Full) ||
+              !wait_bar(&sf_full[s], ph, abort_flag, p, kSiteW4A4Scales)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * L::kStage), b0 = a0 + L::kOffB;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)   // four K=64 steps of 32 bytes through each 128-byte row
-          mma_ss_mxf4nvf4(tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j), idesc,
-                          tmem + L::kColSA + 16 * s + 4 * j, tmem + L::kColSB + 16 * s + 4 * j,
-                          (kt > 0 || j > 0) ? 1u : 0u);
-        mma_commit(&empty[s]);
+          for (int j = 0; j < 4; ++j)   // four K=64 steps of 32 bytes through each 128-byte row
+            mma_ss_mxf4nvf4(d_tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j),
+                            idesc, tmem + L::kColSA + 16 * s + 4 * j,
+                            tmem + L::kColSB + 16 * s + 4 * j, (kt > 0 || j > 0) ? 1u : 0u);
+          mma_commit(&empty[s]);
+        }
+        if (ok) mma_commit(&acc_full[b]);
       }
-      mma_commit(acc_full);   // arrives once every MMA issued above has finished
-      drain_bar(acc_full, 0, drain_ns);
+      mma_commit(drain);   // arrives once every MMA issued above has finished
+      drain_bar(drain, 0, drain_ns);
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ------------------------------------------------ block scales, then the epilogue
-    const int q = warp - 4;
-    const int r = q * 32 + lane;   // this thread's tensor-memory lane (epilogue: feature row)
-    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------ block scales into tensor memory
+    const uint32_t lane_addr = (uint32_t)((warp - 4) * 32) << 16;
     bool ok = true;
-    for (int kt = 0; kt < p.kt && ok; ++kt) {
-      const int s = kt % kStages;
-      if (lane == 0) ok = wait_bar(&full[s], (kt / kStages) & 1, abort_flag, p, kSiteW4A4Full);
+    int g = 0;
+    for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+      for (int kt = 0; kt < p.kt; ++kt, ++g) {
+        const int s = g % kStages;
+        if (lane == 0) ok = wait_bar(&full[s], (g / kStages) & 1, abort_flag, p, kSiteW4A4Full);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        const uint8_t* st = smem + s * L::kStage;
+        // this quadrant's copy of the stage's four scale groups: column
+        // 4j + c holds word j (the scales of step j's four 16-k blocks) of
+        // row 32 c + lane; activation rows past the tile hold zero
+        uint32_t va[16], vb[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int row = 32 * c + lane;
+          const uint4 a4 = *reinterpret_cast<const uint4*>(st + L::kOffSA + row * 16);
+          uint4 b4 = make_uint4(0u, 0u, 0u, 0u);
+          if (row < BT) b4 = *reinterpret_cast<const uint4*>(st + L::kOffSB + row * 16);
+          va[c] = a4.x, va[4 + c] = a4.y, va[8 + c] = a4.z, va[12 + c] = a4.w;
+          vb[c] = b4.x, vb[4 + c] = b4.y, vb[8 + c] = b4.z, vb[12 + c] = b4.w;
+        }
+        tmem_st16(tmem + lane_addr + L::kColSA + 16 * s, va);
+        tmem_st16(tmem + lane_addr + L::kColSB + 16 * s, vb);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_full[s]);
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------ epilogue
+    const int q = warp - 8;
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    const float sc = __fmul_rn(*p.a_ts, *p.w_ts);
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      bool ok = true;
+      if (lane == 0) ok = wait_bar(&acc_full[b], (i >> 1) & 1, abort_flag, p, kSiteW4A4Acc);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
-      const uint8_t* st = smem + s * L::kStage;
-      // this quadrant's copy of the stage's four scale groups: column 4j + c
-      // holds word j (the scales of step j's four 16-k blocks) of row
-      // 32 c + lane; activation rows past the tile hold zero
-      uint32_t va[16], vb[16];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int row = 32 * c + lane;
-        const uint4 a4 = *reinterpret_cast<const uint4*>(st + L::kOffSA + row * 16);
-        uint4 b4 = make_uint4(0u, 0u, 0u, 0u);
-        if (row < BT) b4 = *reinterpret_cast<const uint4*>(st + L::kOffSB + row * 16);
-        va[c] = a4.x, va[4 + c] = a4.y, va[8 + c] = a4.z, va[12 + c] = a4.w;
-        vb[c] = b4.x, vb[4 + c] = b4.y, vb[8 + c] = b4.z, vb[12 + c] = b4.w;
-      }
-      tmem_st16(tmem + lane_addr + L::kColSA + 16 * s, va);
-      tmem_st16(tmem + lane_addr + L::kColSB + 16 * s, vb);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sf_full[s]);
-    }
-    if (ok) {
-      if (lane == 0) ok = wait_bar(acc_full, 0, abort_flag, p, kSiteW4A4Acc);
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    }
-    if (ok) {
       tc_fence_after();
-      const float sc = __fmul_rn(*p.a_ts, *p.w_ts);
-      const int n = n0 + r;
+      const int n = (t % p.nt) * 128 + q * 32 + lane, m0 = (t / p.nt) * BT;
       float bias = 0.f;
-      if (p.bias && qg_check(n < p.n, p.status)) bias = __bfloat162float(__ushort_as_bfloat16(p.bias[n]));
+      if (p.bias && qg_check(n < p.n, p.status))
+        bias = __bfloat162float(__ushort_as_bfloat16(p.bias[n]));
 #pragma unroll 1
       for (int c0 = 0; c0 < BT; c0 += 16) {
         uint32_t v[16];
-        tmem_ld16_wait(tmem + lane_addr + c0, v);
+        tmem_ld16_wait(tmem + lane_addr + b * BT + c0, v);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int tok = m0 + c0 + j;
@@ -215,6 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
     }
   }
   tc_fence_before();
@@ -272,7 +311,10 @@ cudaError_t launch_bt(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const CU
   cudaError_t e = cudaFuncSetAttribute(w4a4_kernel<BT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
-  w4a4_kernel<BT><<<p.mt * p.nt, kThreads, L::kSmem, stream>>>(tm_w, tm_a, tm_ws, tm_as, p);
+  const int tiles = p.mt * p.nt;
+  const int sms = device_sm_count();
+  const int grid = sms > 0 && tiles > sms ? sms : tiles;   // one persistent CTA per SM
+  w4a4_kernel<BT><<<grid, kThreads, L::kSmem, stream>>>(tm_w, tm_a, tm_ws, tm_as, p);
   return cudaGetLastError();
 }
 
