@@ -207,6 +207,11 @@ typedef struct {
  *              heuristic's count), one CTA each, the slices of a tile summed
  *              in a fixed order through distributed shared memory, so the
  *              bits repeat from call to call
+ * W4A4 layers (act_dtype QGEMM_NVFP4) take block_tok (16, 32, 64 or 128),
+ * split_k and kernel = 1 only: split_k = s (1 .. min(64, K/256)) cuts every
+ * tile's K range into s slices, one work item each, whose fp32 partials the
+ * last slice to finish sums in slice order (1 = whole tiles; 0 = the
+ * heuristic: slices only while the tiles leave SMs idle at small M).
  */
 typedef struct {
   int32_t block_tok;

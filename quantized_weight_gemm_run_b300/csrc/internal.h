@@ -204,6 +204,14 @@ struct W4A4Params {
   uint16_t* c;               // [m, n] bf16
   int* status;               // workspace status word
   unsigned long long wait_limit_ns;
+  // K split: each tile's stages in `splits` contiguous slices, one work item
+  // each; with splits > 1 every slice writes its fp32 partial tile to
+  // part[(tile * splits + slice) * BT * 128 ...] and the last of a tile's
+  // slices to count in (per 32-feature quadrant, cnt[tile * 4 + q], zero at
+  // launch) sums the slices in slice order and stores the output
+  int splits;
+  float* part;
+  int* cnt;
 };
 constexpr int kW4A4TileK = 256;
 int w4a4_smem_bytes(int block_tok);
@@ -212,9 +220,12 @@ cudaError_t launch_w4a4(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const 
                         cudaStream_t stream);
 // Per-token NVFP4 quantization of bf16 activations x[m, k] (k % 16 == 0):
 // codes [m, k/2] (k = 2i in the low nibble of byte i), e4m3 block scales
-// [m, k/16]; a_ts is the caller's fp32 tensor scale on the device.
+// [m, k/16]; a_ts is the caller's fp32 tensor scale on the device.  The
+// kernel also sets zero_words[0 .. n_zero) to zero (the W4A4 GEMM's K-split
+// counters; null and 0 for none).
 cudaError_t launch_act_quant_nvfp4(const uint16_t* x, int64_t m, int64_t k, const float* a_ts,
-                                   uint8_t* codes, uint8_t* sb, cudaStream_t stream);
+                                   uint8_t* codes, uint8_t* sb, cudaStream_t stream,
+                                   int* zero_words = nullptr, int n_zero = 0);
 
 // Host-side plan for one W4A16 launch.
 int device_sm_count();

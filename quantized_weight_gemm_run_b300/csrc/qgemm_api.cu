@@ -345,8 +345,14 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   const int sms = device_sm_count();
   if (sms <= 0) return fail(QGEMM_ERR_CUDA, "no CUDA device");
   const int E = L->num_experts;
+  // Grouped: expert row counts scatter around the mean, and a tile shorter
+  // than an expert's rows dequantizes that expert's weights once per tile, so
+  // the tile is sized for 1.5 x the mean (measured on B300, E = 64, top-8,
+  // hidden 2048, T = 256: 64-token tiles 128-131 us against 150-152 us with
+  // 32; T = 16 and 4096 keep 16 and 128)
   int bt = (T && T->block_tok) ? T->block_tok
-                               : heuristic_block_tok(grouped ? (rows + E - 1) / E : rows);
+                               : heuristic_block_tok(grouped ? (3 * rows + 2 * E - 1) / (2 * E)
+                                                             : rows);
   // W4A8 (measured on B300, N = 7168, K = 2048, M = 128): 64-token whole tiles
   // in one wave beat 128-token tiles when they fit (13.2 against 15.3 us)
   if (is_mx(L) && !grouped && !(T && T->block_tok) && bt == 128 &&
@@ -633,20 +639,23 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 
 // ------------------------------------------------------------ the W4A4 run
 
-// Workspace: the status word, then the quantized activations (codes
-// [rows, K/2], then e4m3 block scales [rows, K/16]).
+// Workspace: the status word, the K split's per-quadrant tile counters
+// (cleared by each call's quantization kernel), its fp32 partial tiles, then
+// the quantized activations (codes [rows, K/2], then e4m3 block scales
+// [rows, K/16]).
 struct W4A4Plan {
   int bt = 0;
+  int splits = 1;
   int64_t grid = 0;
-  size_t codes_off = 0, sb_off = 0, total = 0;
+  size_t cnt_off = 0, part_off = 0, codes_off = 0, sb_off = 0, total = 0;
 };
 
 static qgemm_status w4a4_plan(const qgemm_layer_config* L, const qgemm_tuning_config* T,
                               int64_t rows, W4A4Plan* P) {
   *P = W4A4Plan();
-  if (T && (T->stages || T->max_ctas || T->split_k || T->cta_pair || T->kernel > 1 ||
-            T->kernel < 0))
-    return fail(QGEMM_ERR_UNSUPPORTED, "a W4A4 tuning may set block_tok (and kernel = 1) only");
+  if (T && (T->stages || T->max_ctas || T->cta_pair || T->kernel > 1 || T->kernel < 0))
+    return fail(QGEMM_ERR_UNSUPPORTED,
+                "a W4A4 tuning may set block_tok, split_k (and kernel = 1) only");
   const int bt = (T && T->block_tok) ? T->block_tok
                  : rows <= 16        ? 16
                  : rows <= 32        ? 32
@@ -654,10 +663,32 @@ static qgemm_status w4a4_plan(const qgemm_layer_config* L, const qgemm_tuning_co
                                      : 128;
   if (bt != 16 && bt != 32 && bt != 64 && bt != 128)
     return fail(QGEMM_ERR_UNSUPPORTED, "W4A4 block_tok %d not in {16, 32, 64, 128}", bt);
+  const int64_t kt = L->k / kW4A4TileK;
+  const int64_t tiles = ((rows + bt - 1) / bt) * (L->n / kTileN);
+  // K slices per tile: the tuning's, else (few tiles of at most 64 tokens,
+  // and 16-token tiles or K of at least 32 stages) as many as fill the SMs,
+  // at least four stages each.  Measured on B300, us, whole tiles / split:
+  // M = 1 4096^2 11.7 / 10.4 (4 slices); M = 1 / 16 / 64 4096 x 11008 19.6
+  // / 20.1 / 22.3 against 13.9 / 14.6 / 20.6; M = 64 4096^2 14.4 / 17.8
+  // and M = 256 (2 slices) 17.7 / 23.3: there the slices' partial round trip
+  // costs more than the shorter K loop saves
+  int64_t S = 1;
+  if (T && T->split_k) {
+    S = T->split_k;
+    if (S < 1 || S > 64 || S > kt)
+      return fail(QGEMM_ERR_UNSUPPORTED, "W4A4 split_k %d not in [1, min(64, k / 256)]",
+                  T->split_k);
+  } else if (tiles > 0 && tiles < device_sm_count() && bt <= 64 && (bt <= 16 || kt >= 32)) {
+    S = std::min<int64_t>(std::min<int64_t>(16, kt / 4), device_sm_count() / tiles);
+    if (S < 1) S = 1;
+  }
   P->bt = bt;
-  P->grid = ((rows + bt - 1) / bt) * (L->n / kTileN);
+  P->splits = (int)S;
+  P->grid = tiles * S;
   if (P->grid >= (int64_t(1) << 31)) return fail(QGEMM_ERR_UNSUPPORTED, "grid too large");
-  P->codes_off = 256;
+  P->cnt_off = 256;
+  P->part_off = P->cnt_off + (S > 1 ? (((size_t)tiles * 16 + 255) & ~size_t(255)) : 0);
+  P->codes_off = P->part_off + (S > 1 ? (size_t)tiles * (size_t)S * (size_t)bt * 128 * 4 : 0);
   P->sb_off = P->codes_off + (((size_t)rows * (size_t)(L->k / 2) + 255) & ~size_t(255));
   P->total = P->sb_off + (((size_t)rows * (size_t)(L->k / 16) + 255) & ~size_t(255));
   return ok();
@@ -714,8 +745,13 @@ static qgemm_status run_w4a4(const qgemm_layer_config* L, const qgemm_tuning_con
   p.c = static_cast<uint16_t*>(c);
   p.status = reinterpret_cast<int*>(wsb);
   p.wait_limit_ns = g_wait_limit_ns;
+  p.splits = P.splits;
+  p.cnt = reinterpret_cast<int*>(wsb + P.cnt_off);
+  p.part = reinterpret_cast<float*>(wsb + P.part_off);
+  // the quantization kernel also clears the K split's counters
+  const int64_t n_cnt = P.splits > 1 ? P.grid / P.splits * 4 : 0;
   cudaError_t e = launch_act_quant_nvfp4(static_cast<const uint16_t*>(a), rows, (int64_t)k,
-                                         a_scale, codes, sb, stream);
+                                         a_scale, codes, sb, stream, p.cnt, (int)n_cnt);
   if (e != cudaSuccess) return cuda_fail(e, "NVFP4 activation quantization launch");
   e = launch_w4a4(tm_w, tm_a, tm_ws, tm_as, p, P.bt, stream);
   if (e != cudaSuccess) return cuda_fail(e, "W4A4 GEMM launch");
@@ -980,7 +1016,7 @@ int dense_workspace_bytes(const void* layer, const void* compute, const void* tu
   const qgemm_layer_config* L = static_cast<const qgemm_layer_config*>(layer);
   qgemm_status st = check_layer(L);
   if (st != QGEMM_OK) return st;
-  if (is_w4a4(L)) {   // only the status word starts at zero
+  if (is_w4a4(L)) {   // only the status word starts at zero (the call clears its counters)
     W4A4Plan W;
     st = w4a4_plan(L, static_cast<const qgemm_tuning_config*>(tuning), m > 0 ? m : 1, &W);
     if (st != QGEMM_OK) return st;
@@ -1313,14 +1349,20 @@ qgemm_status qgemm_describe_plan(const qgemm_layer_config* layer,
   if (st != QGEMM_OK) {
     rec = std::string("rejected: ") + g_last_error;
   } else if (is_w4a4(layer)) {
-    char tmp[384];
+    char tmp[384], split[48];
+    if (W.splits > 1)
+      snprintf(split, sizeof(split), "k_slices_%d_last_arrival_sum", W.splits);
+    else
+      snprintf(split, sizeof(split), "whole_tiles");
+    const int sms = device_sm_count();
     snprintf(tmp, sizeof(tmp),
              "kernel=w4a4_tcgen05_mxf4nvf4 weights=nvfp4 group=16 scales=e4m3 act=nvfp4 out=bf16 "
-             "n=%lld k=%lld m=%lld experts=1 block_tok=%d stages=6 grid=%lld smem=%d "
-             "workspace=%zu epilogue=%s split=whole_tiles act_quant=separate_kernel "
+             "n=%lld k=%lld m=%lld experts=1 block_tok=%d stages=6 items=%lld grid=%lld smem=%d "
+             "workspace=%zu epilogue=%s split=%s act_quant=separate_kernel "
              "device=sm_103",
              (long long)layer->n, (long long)layer->k, (long long)m, W.bt, (long long)W.grid,
-             w4a4_smem_bytes(W.bt), W.total, layer->has_bias ? "bias" : "plain");
+             (long long)(sms > 0 && W.grid > sms ? sms : W.grid), w4a4_smem_bytes(W.bt), W.total,
+             layer->has_bias ? "bias" : "plain", split);
     rec = tmp;
   } else {
     Plan P;

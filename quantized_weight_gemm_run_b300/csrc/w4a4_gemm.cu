@@ -11,20 +11,29 @@
 //                           caller's fp32 tensor scale (every decision in
 //                           fp32: d = 6 a_ts, t = amax / d, s = e4m3(t),
 //                           q = x / (s a_ts), code = e2m1(q))
-//   w4a4_kernel<BT>         persistent, one CTA per SM over the (BT-token,
-//                           128-feature) tiles, each over the whole K range:
-//                           both operands stay packed (two codes a byte) from
-//                           HBM to the tensor core, the block scales go to
-//                           tensor memory, and the epilogue multiplies the
-//                           fp32 sums by the two tensor scales; two
-//                           accumulators let a tile's epilogue run under the
-//                           next tile's MMAs.
+//   w4a4_kernel<BT>         persistent, one CTA per SM over the work items
+//                           (a BT-token, 128-feature tile, or one of its S
+//                           contiguous K slices): both operands stay packed
+//                           (two codes a byte) from HBM to the tensor core,
+//                           the block scales go to tensor memory, and the
+//                           epilogue multiplies the fp32 sums by the two
+//                           tensor scales; two accumulators let an item's
+//                           epilogue run under the next item's MMAs.  With
+//                           S > 1 (few tiles: small M) each slice's epilogue
+//                           writes its fp32 partial to the workspace and the
+//                           last slice of a tile to count in sums the S
+//                           partials in slice order (the bits do not depend
+//                           on which slice finishes last) before the scales,
+//                           bias and rounding; its counters are cleared by
+//                           the quantization kernel ahead of it.
 //
 // Roles of the 12 warps: 0 TMA producer, 1 MMA issuer, 2 tensor-memory
 // allocation, 4-7 block scales into tensor memory, 8-11 the epilogue (warps
 // w and w + 4 own tensor-memory lanes 32 (w - 4) ... + 31).
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
+
+#include <algorithm>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -65,6 +74,15 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return mbar_wait(bar, parity, abort_flag, p.status, p.wait_limit_ns, kStatusTimeout | site);
 }
 
+__device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 // Bounded wait that ignores the abort flag: at exit, lets the copies and
 // MMAs already issued finish before their shared or tensor memory goes away.
 __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -93,7 +111,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int tiles = p.mt * p.nt;
+  const int S = p.splits;
+  const int items = p.mt * p.nt * S;
+  // item -> tile t = item / S, its K slice [kt_lo, kt_hi) of 256-k stages
+  auto kt_lo = [&](int item) { return (item % S) * p.kt / S; };
+  auto kt_hi = [&](int item) { return (item % S + 1) * p.kt / S; };
   const uint64_t drain_ns = p.wait_limit_ns + 1000000000ull;
 
   if (threadIdx.x == 0) {
@@ -125,17 +147,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Persistent: CTA b takes tiles b, b + grid, ...; tile t is (token tile
-  // t / nt, feature tile t % nt).  The stage ring runs on across tiles
-  // (stage use g = the CTA's running count of 256-k stages).
+  // Persistent: CTA b takes items b, b + grid, ...; item it is slice it % S
+  // of tile t = it / S, and tile t is (token tile t / nt, feature tile
+  // t % nt).  The stage ring runs on across items (stage use g = the CTA's
+  // running count of 256-k stages).
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
+      // The first item's first stages of weights (read-only layer data) go
+      // out before the wait on the quantization kernel ahead on the stream
+      // (programmatic dependent launch); the activations after it.
+      const int it0 = blockIdx.x;   // < items: the grid is at most the items
+      const int pre = min(kStages, kt_hi(it0) - kt_lo(it0));
+      {
+        const int n0 = ((it0 / S) % p.nt) * 128;
+        for (int u = 0; u < pre; ++u) {
+          uint8_t* st = smem + u * L::kStage;
+          mbar_arrive_expect_tx(&full[u], L::kBytes);
+          tma_load_2d(st, &tm_w, &full[u], (kt_lo(it0) + u) * 128, n0);
+          tma_load_2d(st + L::kOffSA, &tm_ws, &full[u], (kt_lo(it0) + u) * 16, n0);
+        }
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       int g = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+      for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+        const int t = it / S;
         const int n0 = (t % p.nt) * 128, m0 = (t / p.nt) * BT;
-        for (int kt = 0; kt < p.kt; ++kt, ++g) {
+        for (int kt = kt_lo(it); kt < kt_hi(it); ++kt, ++g) {
           const int s = g % kStages;
           if (g >= kStages &&
               !wait_bar(&empty[s], ((g / kStages) - 1) & 1, abort_flag, p, kSiteW4A4Slot)) {
@@ -143,10 +182,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* st = smem + s * L::kStage;
-          mbar_arrive_expect_tx(&full[s], L::kBytes);
-          tma_load_2d(st, &tm_w, &full[s], kt * 128, n0);
+          if (g >= pre) {   // else its weights went out before the wait
+            mbar_arrive_expect_tx(&full[s], L::kBytes);
+            tma_load_2d(st, &tm_w, &full[s], kt * 128, n0);
+            tma_load_2d(st + L::kOffSA, &tm_ws, &full[s], kt * 16, n0);
+          }
           tma_load_2d(st + L::kOffB, &tm_a, &full[s], kt * 128, m0);
-          tma_load_2d(st + L::kOffSA, &tm_ws, &full[s], kt * 16, n0);
           tma_load_2d(st + L::kOffSB, &tm_as, &full[s], kt * 16, m0);
         }
       }
@@ -160,12 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_mxf4nvf4_e2m1(BT);
       int g = 0, i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++i) {
+      for (int it = blockIdx.x; ok && it < items; it += gridDim.x, ++i) {
         const int b = i & 1;
         if (!wait_bar(&acc_empty[b], ((i >> 1) & 1) ^ 1, abort_flag, p, kSiteW4A4Acc)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + b * BT;
-        for (int kt = 0; kt < p.kt; ++kt, ++g) {
+        const int k_first = kt_lo(it);
+        for (int kt = k_first; kt < kt_hi(it); ++kt, ++g) {
           const int s = g % kStages;
           const uint32_t ph = (g / kStages) & 1;
           if (!wait_bar(&full[s], ph, abort_flag, p, kSiteW4A4Full) ||
@@ -179,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j)   // four K=64 steps of 32 bytes through each 128-byte row
             mma_ss_mxf4nvf4(d_tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j),
                             idesc, tmem + L::kColSA + 16 * s + 4 * j,
-                            tmem + L::kColSB + 16 * s + 4 * j, (kt > 0 || j > 0) ? 1u : 0u);
+                            tmem + L::kColSB + 16 * s + 4 * j,
+                            (kt > k_first || j > 0) ? 1u : 0u);
           mma_commit(&empty[s]);
         }
         if (ok) mma_commit(&acc_full[b]);
@@ -193,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = (uint32_t)((warp - 4) * 32) << 16;
     bool ok = true;
     int g = 0;
-    for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-      for (int kt = 0; kt < p.kt; ++kt, ++g) {
+    for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+      for (int kt = kt_lo(it); kt < kt_hi(it); ++kt, ++g) {
         const int s = g % kStages;
         if (lane == 0) ok = wait_bar(&full[s], (g / kStages) & 1, abort_flag, p, kSiteW4A4Full);
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -224,36 +267,97 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 8) {
     // ------------------------------------------------ epilogue
     const int q = warp - 8;
+    const int col = q * 32 + lane;   // feature within the tile
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    // the counters and the output: after the quantization kernel is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float sc = __fmul_rn(*p.a_ts, *p.w_ts);
     int i = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+    for (int it = blockIdx.x; it < items; it += gridDim.x, ++i) {
+      const int t = it / S;
       const int b = i & 1;
       bool ok = true;
       if (lane == 0) ok = wait_bar(&acc_full[b], (i >> 1) & 1, abort_flag, p, kSiteW4A4Acc);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const int n = (t % p.nt) * 128 + q * 32 + lane, m0 = (t / p.nt) * BT;
+      const int n = (t % p.nt) * 128 + col, m0 = (t / p.nt) * BT;
+      const int live = min(BT, p.m - m0);   // tokens of this tile
       float bias = 0.f;
       if (p.bias && qg_check(n < p.n, p.status))
         bias = __bfloat162float(__ushort_as_bfloat16(p.bias[n]));
+      // this slice's partial (item it = t * S + slice), [token][128 features]
+      float* slot = p.part + (size_t)it * (BT * 128) + col;
 #pragma unroll 1
       for (int c0 = 0; c0 < BT; c0 += 16) {
         uint32_t v[16];
         tmem_ld16_wait(tmem + lane_addr + b * BT + c0, v);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int tok = m0 + c0 + j;
-          if (tok < p.m && qg_check(n < p.n, p.status)) {
-            const float o = fmaf(__uint_as_float(v[j]), sc, bias);
-            p.c[(long long)tok * p.n + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+          const int tl = c0 + j;
+          if (tl < live && qg_check(n < p.n, p.status)) {
+            if (S == 1) {
+              const float o = fmaf(__uint_as_float(v[j]), sc, bias);
+              p.c[(long long)(m0 + tl) * p.n + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+            } else {
+              __stcg(slot + tl * 128, __uint_as_float(v[j]));
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
+      if (S > 1) {
+        // count this quadrant's slice in; the last of the S sums them
+        __threadfence();
+        __syncwarp();
+        int before = 0;
+        if (lane == 0) before = atomic_add_acq_rel(p.cnt + t * 4 + q, 1);
+        __syncwarp();
+        before = __shfl_sync(0xFFFFFFFFu, before, 0);
+        if (before == S - 1) {
+          __threadfence();
+          // 16 rows at a time, the S slices added in slice order; two slices'
+          // loads (32 per lane) are in flight at once
+          const float* base = p.part + (size_t)t * S * (BT * 128) + col;
+          constexpr size_t kSl = (size_t)BT * 128;   // floats between slices
+#pragma unroll 1
+          for (int c0 = 0; c0 < live; c0 += 16) {
+            const float* b0 = base + (size_t)c0 * 128;
+            float acc[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = c0 + j < live ? __ldcg(b0 + j * 128) : 0.f;
+            int sl = 1;
+#pragma unroll 1
+            for (; sl + 1 < S; sl += 2) {
+              float v1[16], v2[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                v1[j] = c0 + j < live ? __ldcg(b0 + sl * kSl + j * 128) : 0.f;
+                v2[j] = c0 + j < live ? __ldcg(b0 + (sl + 1) * kSl + j * 128) : 0.f;
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) acc[j] = (acc[j] + v1[j]) + v2[j];
+            }
+            if (sl < S) {
+              float v1[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                v1[j] = c0 + j < live ? __ldcg(b0 + sl * kSl + j * 128) : 0.f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) acc[j] += v1[j];
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < live && qg_check(n < p.n, p.status)) {
+                const float o = fmaf(acc[j], sc, bias);
+                p.c[(long long)(m0 + c0 + j) * p.n + n] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(o));
+              }
+          }
+        }
+      }
     }
   }
   tc_fence_before();
@@ -264,13 +368,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // One thread per 16-k block of a token: two 16-byte loads, the block maximum,
 // the e4m3 scale, sixteen fp32 divides and e2m1 conversions, one 8-byte code
-// store and one scale byte.
+// store and one scale byte.  Threads 0 .. n_zero - 1 also clear the GEMM's
+// K-split counters (the GEMM that follows on the stream counts from zero,
+// whatever another plan left in the workspace).
 __global__ void __launch_bounds__(256)
     act_quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t m, int64_t k,
                            const float* __restrict__ a_ts, uint8_t* __restrict__ codes,
-                           uint8_t* __restrict__ sb) {
+                           uint8_t* __restrict__ sb, int* __restrict__ zero_words,
+                           int n_zero) {
+  // programmatic dependent launch: the previous grid's memory first; the
+  // GEMM that follows may start its set-up and weight copies at once
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t nb = k >> 4;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n_zero) zero_words[i] = 0;
   if (i >= m * nb) return;
   const int64_t row = i / nb, b = i - row * nb;
   const uint4* src = reinterpret_cast<const uint4*>(x + row * k + b * 16);
@@ -311,11 +423,20 @@ cudaError_t launch_bt(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const CU
   cudaError_t e = cudaFuncSetAttribute(w4a4_kernel<BT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
-  const int tiles = p.mt * p.nt;
+  const int items = p.mt * p.nt * p.splits;
   const int sms = device_sm_count();
-  const int grid = sms > 0 && tiles > sms ? sms : tiles;   // one persistent CTA per SM
-  w4a4_kernel<BT><<<grid, kThreads, L::kSmem, stream>>>(tm_w, tm_a, tm_ws, tm_as, p);
-  return cudaGetLastError();
+  const int grid = sms > 0 && items > sms ? sms : items;   // one persistent CTA per SM
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w4a4_kernel<BT>, tm_w, tm_a, tm_ws, tm_as, p);
 }
 
 }  // namespace
@@ -343,13 +464,23 @@ cudaError_t launch_w4a4(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const 
 }
 
 cudaError_t launch_act_quant_nvfp4(const uint16_t* x, int64_t m, int64_t k, const float* a_ts,
-                                   uint8_t* codes, uint8_t* sb, cudaStream_t stream) {
-  const int64_t blocks = m * (k >> 4);
+                                   uint8_t* codes, uint8_t* sb, cudaStream_t stream,
+                                   int* zero_words, int n_zero) {
+  const int64_t blocks = std::max<int64_t>(m * (k >> 4), n_zero);
   if (blocks == 0) return cudaSuccess;
   const int64_t grid = (blocks + 255) / 256;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  act_quant_nvfp4_kernel<<<(unsigned)grid, 256, 0, stream>>>(x, m, k, a_ts, codes, sb);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, act_quant_nvfp4_kernel, x, m, k, a_ts, codes, sb, zero_words,
+                            n_zero);
 }
 
 }  // namespace qg

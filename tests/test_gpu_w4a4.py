@@ -141,8 +141,10 @@ def test_w4a4_plan_and_rejections(Q):
         assert st == Q.QGEMM_OK
         assert "kernel=w4a4_tcgen05_mxf4nvf4" in rec and f"block_tok={bt}" in rec, rec
     x = _bf16_dev(np.zeros((4, 512)))
-    for tun in (Q.tuning_config(split_k=2), Q.tuning_config(kernel=2),
-                Q.tuning_config(block_tok=256), Q.tuning_config(stages=3)):
+    # k = 512 is two 256-k stages: at most two K slices
+    for tun in (Q.tuning_config(split_k=3), Q.tuning_config(split_k=65),
+                Q.tuning_config(kernel=2), Q.tuning_config(block_tok=256),
+                Q.tuning_config(stages=3)):
         lin.tuning = tun
         with pytest.raises(Q.QGemmError):
             lin(x)
@@ -164,6 +166,54 @@ def test_w4a4_plan_and_rejections(Q):
     assert st == Q.QGEMM_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("m,n,k,s", [(1, 512, 4096, 1), (1, 512, 4096, 4), (16, 384, 2560, 3),
+                                     (45, 256, 3072, 5), (130, 256, 1024, 2), (7, 128, 512, 2)])
+def test_w4a4_k_split(Q, m, n, k, s):
+    """K slices of a tile summed by the last slice to count in: even and
+    uneven slices, ragged M, bias, against the oracle."""
+    g = synth.rng(360 + m + s)
+    x = codecs.bf16(synth.activations_fp32(g, m, k))
+    a_ts = float(np.float32(np.max(np.abs(x)) / (6 * 448)))
+    wc, wsb, w_ts = quant.quantize_nvfp4(synth.weights_fp32(g, k, n))
+    bias = codecs.bf16(g.standard_normal(n))
+    lin = _layer(wc, wsb, w_ts, a_ts, n, k, bias=bias, tuning=Q.tuning_config(split_k=s))
+    _check(Q, lin, x, a_ts, wc, wsb, w_ts, bias=bias, what=f"w4a4 split {s} {m}x{n}x{k}")
+
+
+def test_w4a4_k_split_plan_repeats_and_reuses_workspace(Q):
+    """The default plan splits K when the tiles leave SMs idle; the slices are
+    summed in a fixed order (the bits repeat), and each call clears its own
+    counters, so one workspace serves plans whose counters lie where another
+    plan's partial tiles or quantized activations were."""
+    g = synth.rng(370)
+    n, k = 1024, 4096
+    wc, wsb, w_ts = quant.quantize_nvfp4(synth.weights_fp32(g, k, n))
+    xs = [codecs.bf16(synth.activations_fp32(g, m, k)) for m in (16, 300, 3)]
+    a_ts = float(np.float32(max(np.max(np.abs(x)) for x in xs) / (6 * 448)))
+    lin = _layer(wc, wsb, w_ts, a_ts, n, k)
+    st, rec = Q.qgemm_describe_plan(lin.layer, lin.dense, 16)
+    assert st == Q.QGEMM_OK and "split=k_slices_4_" in rec, rec   # 8 tiles, 16 stages
+    st, rec = Q.qgemm_describe_plan(lin.layer, lin.dense, 8192)
+    assert st == Q.QGEMM_OK and "split=whole_tiles" in rec, rec
+    lin.ws.get(64 << 20)   # one workspace, large enough for every plan below
+    first = {}
+    for rnd in range(2):
+        for x in xs:
+            for tun in (None, Q.tuning_config(split_k=2), Q.tuning_config(split_k=16)):
+                lin.tuning = tun
+                out = lin(_bf16_dev(x))
+                assert lin.status() == Q.QGEMM_OK
+                key = (x.shape[0], None if tun is None else tun.split_k)
+                got = to_np(out)
+                if rnd == 0:
+                    ac, asb = gemm.act_quant_nvfp4(x, a_ts)
+                    ref = gemm.w4a4_reference(ac, asb, a_ts, wc, wsb, w_ts, None)
+                    assert_close(got, ref, what=f"w4a4 reuse {key}")
+                    first[key] = got
+                else:
+                    assert np.array_equal(got, first[key]), key
+
+
 def test_w4a4_zero_rows_and_timeout(Q):
     g = synth.rng(350)
     n, k, m = 256, 1024, 33
@@ -183,6 +233,8 @@ def test_w4a4_zero_rows_and_timeout(Q):
     finally:
         Q.qgemm_set_wait_limit_ns(1_000_000_000)
     assert lin.status() == Q.QGEMM_ERR_TIMEOUT
+    # no re-zeroing: each call clears the K split's counters (1 x 2 tiles here,
+    # split across K), whatever an abandoned launch left in them
     again = lin(xd)
     assert lin.status() == Q.QGEMM_OK
     torch.cuda.synchronize()
