@@ -481,6 +481,8 @@ def kernel_name(p):
     m = p["m"]
     if kind == "w4a4":
         bt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
+        if m > 16:   # the planner's smaller tile while the tiles fit one wave on 148 SMs
+            bt = next((b for b in (32, 64) if b < bt and -(-m // b) * (p["n"] // 128) <= 148), bt)
         return f"act_quant_nvfp4_kernel + w4a4_kernel<{bt}>"
     nv_small = kind == "nvfp4" and (p["n"] * p["k"] <= 1 << 24 or (m <= 8 and p["k"] <= 4096))
     if (kind in ("w4a16", "w4a8") or nv_small) and m <= 16:

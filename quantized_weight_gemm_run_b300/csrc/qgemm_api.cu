@@ -656,11 +656,22 @@ static qgemm_status w4a4_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   if (T && (T->stages || T->max_ctas || T->cta_pair || T->kernel > 1 || T->kernel < 0))
     return fail(QGEMM_ERR_UNSUPPORTED,
                 "a W4A4 tuning may set block_tok, split_k (and kernel = 1) only");
-  const int bt = (T && T->block_tok) ? T->block_tok
-                 : rows <= 16        ? 16
-                 : rows <= 32        ? 32
-                 : rows <= 64        ? 64
-                                     : 128;
+  // Token tile: the tuning's; else the M range's, or above 16 rows the
+  // smallest of 32 / 64 / 128 (up to the M range's) whose tiles still fit one
+  // wave on the SMs, so that medium M keeps more SMs streaming.  Measured on
+  // B300 (us, M range's tile / this): M = 64 4096^2 12.5 / 11.2 (32 tokens),
+  // 4096 x 11008 20.4 / 17.4; M = 256 4096^2 16.0 / 13.4 (64), 4096 x 11008
+  // 25.4 / 22.8; 11008 x 4096 keeps the M range's tile (86 feature tiles)
+  int bt = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
+  if (T && T->block_tok) {
+    bt = T->block_tok;
+  } else if (rows > 16) {
+    for (int b = 32; b < bt; b *= 2)
+      if (((rows + b - 1) / b) * (L->n / kTileN) <= device_sm_count()) {
+        bt = b;
+        break;
+      }
+  }
   if (bt != 16 && bt != 32 && bt != 64 && bt != 128)
     return fail(QGEMM_ERR_UNSUPPORTED, "W4A4 block_tok %d not in {16, 32, 64, 128}", bt);
   const int64_t kt = L->k / kW4A4TileK;

@@ -136,7 +136,9 @@ def test_w4a4_plan_and_rejections(Q):
     g = synth.rng(340)
     wc, wsb, w_ts = _weights(g, 512, 256, False, 1.0)
     lin = _layer(wc, wsb, w_ts, 1.0, 256, 512)
-    for m, bt in ((1, 16), (32, 32), (64, 64), (65, 128), (4096, 128)):
+    # the M range's tile, or a smaller one while the tiles fit one wave (two
+    # feature tiles here): 4096 rows in 64-token tiles are 128 tiles
+    for m, bt in ((1, 16), (32, 32), (64, 32), (65, 32), (4096, 64), (8192, 128)):
         st, rec = Q.qgemm_describe_plan(lin.layer, lin.dense, m)
         assert st == Q.QGEMM_OK
         assert "kernel=w4a4_tcgen05_mxf4nvf4" in rec and f"block_tok={bt}" in rec, rec
