@@ -12,7 +12,7 @@ CUDA graph and replayed.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload sweep|w4a16_m16|large|w4a8|moe16|moe256|moe4096|
                               f16s|w8a16|nvfp4|w4a4|w4a4_large|
-                              shape:M,N,K[,sym|asym][,bf16|fp16]]
+                              shape:M,N,K[,sym|asym][,bf16|fp16][,w4a4]]
 
 Other workloads (--workload) are for kernel studies and print the same line
 format for their own configuration.  --impl reference times the CPU oracle
@@ -67,6 +67,10 @@ def workload_points(name):
         asym = "asym" in f[3:]
         adt = "fp16" if "fp16" in f[3:] else "bf16"
         sdt = "fp16" if "f16s" in f[3:] else adt     # f16s: fp16 scales (bf16 activations)
+        if "w4a4" in f[3:]:   # NVFP4 weights and activations
+            return [dict(kind="w4a4", m=m, n=n, k=k, g=16, asym=False, adt="bf16")], dict(
+                workload=f"w4a4_nvfp4_{m}x{n}x{k}", m=m, n=n, k=k, weights="nvfp4",
+                act="bf16 -> nvfp4 per token")
         return [dict(m=m, n=n, k=k, g=128, asym=asym, adt=adt, sdt=sdt)], dict(
             workload=f"w4a16_{'asym' if asym else 'sym'}_{m}x{n}x{k}"
                      + ("_f16scales" if sdt != adt else ""), m=m, n=n, k=k, group=128,
@@ -1043,7 +1047,7 @@ def main():
     ap.add_argument("--workload", default="sweep",
                     help="sweep | f16s | w8a16 | nvfp4 | w4a4 | w4a4_large | w4a16_m16 | large | "
                          "w4a8 | moe16 | moe256 | moe4096 | "
-                         "shape:M,N,K[,sym|asym][,bf16|fp16][,f16s]")
+                         "shape:M,N,K[,sym|asym][,bf16|fp16][,f16s][,w4a4]")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-extra", action="store_true",
                     help="sweep only: skip timing the other configurations")
