@@ -140,3 +140,34 @@ def test_noalloc_w4a8_on_bf16_activations(Q, m):
         assert Q.qgemm_noalloc_check_status() == Q.QGEMM_OK
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("m,n,k", [(16, 512, 4096), (300, 384, 1024)])
+def test_noalloc_w4a4(Q, m, n, k):
+    """W4A4 layers through the allocation-free entry point: the NVFP4 codes and
+    block scales of the activations, and (at m = 16, a K split) the slices'
+    partial tiles live in the library's scratch; the K split's counters are
+    cleared by the call's own quantization kernel, so the bits equal the
+    workspace entry point's on two calls in a row."""
+    import synth
+    from oracle import codecs, quant
+    from quantized_weight_gemm_run_b300.api import W4A4Linear
+    g = synth.rng(60 + m)
+    wc, wsb, w_ts = quant.quantize_nvfp4(synth.weights_fp32(g, k, n))
+    cnk, snk = quant.pack_nvfp4(wc, wsb)
+    x32 = codecs.bf16(synth.activations_fp32(g, m, k))
+    a_ts = torch.tensor([float(np.float32(np.max(np.abs(x32)) / (6 * 448)))],
+                        dtype=torch.float32, device=DEV)
+    lin = W4A4Linear(torch.from_numpy(cnk).to(DEV), torch.from_numpy(snk).to(DEV),
+                     torch.tensor([w_ts], dtype=torch.float32, device=DEV), a_ts, n, k)
+    x = torch.from_numpy(x32.astype(np.float32)).to(torch.bfloat16).to(DEV)
+    ref = lin(x)
+    assert lin.status() == Q.QGEMM_OK
+    for _ in range(2):
+        out = torch.full_like(ref, float("nan"))
+        st = Q.qgemm_run_noalloc(lin.layer, lin.dense, None, m, x, lin.act_scale, lin.packed,
+                                 None, out)
+        assert st == Q.QGEMM_OK, Q.last_error()
+        assert Q.qgemm_noalloc_check_status() == Q.QGEMM_OK
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
