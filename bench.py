@@ -182,9 +182,58 @@ def point_flops(p):
 
 # ------------------------------------------------------------------ clocks
 
+def _nvml_sampler(index):
+    """(max SM MHz, sample) where sample() returns (SM MHz, clock-event reason
+    bits) through NVML's C library (read-only queries, ctypes; the Python
+    binding is not needed)."""
+    import ctypes
+    nv = ctypes.CDLL("libnvidia-ml.so.1")
+    if nv.nvmlInit_v2() != 0:
+        raise RuntimeError("nvmlInit failed")
+    h = ctypes.c_void_p()
+    if nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) != 0:
+        raise RuntimeError("no NVML handle for device %d" % index)
+    clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+    nvml_clock_sm = 1
+    nv.nvmlDeviceGetMaxClockInfo(h, nvml_clock_sm, ctypes.byref(mx))
+
+    def sample():
+        if nv.nvmlDeviceGetClockInfo(h, nvml_clock_sm, ctypes.byref(clk)) != 0:
+            raise RuntimeError("nvmlDeviceGetClockInfo failed")
+        if nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) != 0:
+            raise RuntimeError("nvmlDeviceGetCurrentClocksEventReasons failed")
+        return clk.value, rs.value
+    return mx.value, sample
+
+
+def _clock_sampler_proc(index, period, stop, conn):
+    """Child process of ClockSampler: NVML SM clock and clock-event reasons
+    (read-only queries) every `period` seconds until `stop` is set.  A process
+    of its own, so that the sampling does not wait on the interpreter lock of
+    the process that launches the work."""
+    import time
+    try:
+        mx, sample = _nvml_sampler(index)
+        conn.send(("ready", mx))
+    except Exception as e:   # no NVML here: the parent samples by itself
+        conn.send(("error", str(e)))
+        return
+    out = []
+    while not stop.is_set():
+        t = time.monotonic()
+        try:
+            out.append((t, *sample()))
+        except Exception:
+            pass
+        time.sleep(period)
+    conn.send(("done", out))
+
+
 class ClockSampler:
-    """SM clock and clock-event reasons sampled through NVML (read-only queries)
-    every `period` seconds on a background thread while the timed region runs."""
+    """SM clock and clock-event reasons sampled through NVML every `period`
+    seconds while the timed region runs: in a spawned child process (no CUDA in
+    it), else on a background thread, else by polling nvidia-smi.  mark_start /
+    mark_end bound the window whose samples stop() summarises."""
 
     REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
                "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
@@ -192,28 +241,62 @@ class ClockSampler:
     def __init__(self, index, period=0.005):
         self.index = index
         self.period = period
-        self.samples = []
+        self.samples = []          # (time.monotonic(), sm_mhz, reasons)
         self.max_mhz = None
         self._stop = None
         self._thread = None
+        self._proc = None
+        self._conn = None
+        self.window = None
         self.error = None
+        self.how = None
+
+    def mark_start(self):
+        self.window = [time.monotonic(), None]
+
+    def mark_end(self):
+        if self.window:
+            self.window[1] = time.monotonic()
+
+    def _start_process(self):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self._stop = ctx.Event()
+        self._conn, child = ctx.Pipe(duplex=False)
+        self._proc = ctx.Process(target=_clock_sampler_proc,
+                                 args=(self.index, self.period, self._stop, child), daemon=True)
+        self._proc.start()
+        child.close()
+        t_end = time.monotonic() + 60
+        while not self._conn.poll(0.1):
+            if not self._proc.is_alive() or time.monotonic() > t_end:
+                raise RuntimeError("clock sampler process did not start")
+        tag, val = self._conn.recv()
+        if tag != "ready":
+            self._proc.join(10)
+            raise RuntimeError(f"clock sampler process: {val}")
+        self.max_mhz = val
+        self.how = "nvml, own process"
 
     def start(self):
+        try:
+            self._start_process()
+            return
+        except Exception as e:            # no spawn or no NVML binding: sample in this process
+            self.error = str(e)
+            if self._proc is not None and self._proc.is_alive():
+                self._proc.kill()
+            self._proc = None
         import threading
         self._stop = threading.Event()
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
-
-            def sample():
-                return (pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM),
-                        pynvml.nvmlDeviceGetCurrentClocksEventReasons(h))
-        except Exception:            # no NVML binding: poll nvidia-smi instead
+            self.max_mhz, sample = _nvml_sampler(self.index)
+            self.how = "nvml, thread"
+        except Exception:            # no NVML library: poll nvidia-smi instead
             import subprocess
             q = ["nvidia-smi", "-i", str(self.index), "--format=csv,noheader,nounits",
                  "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active"]
+            self.how = "nvidia-smi, thread"
 
             def sample():
                 out = subprocess.run(q, capture_output=True, text=True, timeout=5).stdout
@@ -224,7 +307,8 @@ class ClockSampler:
         def run():
             while not self._stop.is_set():
                 try:
-                    self.samples.append(sample())
+                    t = time.monotonic()
+                    self.samples.append((t, *sample()))
                 except Exception as e:
                     self.error = str(e)
                 self._stop.wait(self.period)
@@ -233,19 +317,35 @@ class ClockSampler:
         self._thread.start()
 
     def stop(self):
-        if self._thread is not None:
+        if self._proc is not None:
+            self._stop.set()
+            if self._conn.poll(60):
+                tag, out = self._conn.recv()
+                self.samples = out
+            else:
+                self.error = "clock sampler process sent no samples"
+            self._proc.join(10)
+            if self._proc.is_alive():
+                self._proc.kill()
+        elif self._thread is not None:
             self._stop.set()
             self._thread.join()
-        if not self.samples:
+        return self.summary()
+
+    def summary(self):
+        s = self.samples
+        if self.window and self.window[1] is not None:
+            t0, t1 = self.window
+            inside = [x for x in s if t0 <= x[0] <= t1]
+            # a window shorter than the sampling period: the samples next to it
+            s = inside or [x for x in s if t0 - 0.05 <= x[0] <= t1 + 0.05]
+        if not s:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "samples": 0,
-                    "reasons": [self.error or "no samples"]}
-        reasons = sorted({nm for _, rs in self.samples for nm, bit in self.REASONS.items()
-                          if rs & bit})
-        return {"sm_mhz": statistics.median(m for m, _ in self.samples),
-                "sm_max_mhz": self.max_mhz, "samples": len(self.samples), "reasons": reasons}
+                    "reasons": [self.error or "no samples"], "how": self.how}
+        reasons = sorted({nm for _, _, rs in s for nm, bit in self.REASONS.items() if rs & bit})
+        return {"sm_mhz": statistics.median(m for _, m, _ in s), "sm_max_mhz": self.max_mhz,
+                "samples": len(s), "reasons": reasons, "how": self.how}
 
-
-# ------------------------------------------------------------------ our arm
 
 class GemmPoint:
     """Buffers of one GEMM of the workload (own weights, activations, output).
@@ -489,7 +589,9 @@ def kernel_name(p):
             bt = next((b for b in (32, 64) if b < bt and -(-m // b) * (p["n"] // 128) <= 148), bt)
         return f"act_quant_nvfp4_kernel + w4a4_kernel<{bt}>"
     nv_small = kind == "nvfp4" and (p["n"] * p["k"] <= 1 << 24 or (m <= 8 and p["k"] <= 4096))
-    if (kind in ("w4a16", "w4a8") or nv_small) and m <= 16:
+    # the planner's long-K rule: 9-16 rows with K >= 2 N go to the tcgen05 kernel
+    long_k = kind == "w4a16" and not f16_scales(p) and m > 8 and p["k"] >= 2 * p["n"]
+    if (kind in ("w4a16", "w4a8") or nv_small) and m <= 16 and not long_k:
         # the planner's default for dense INT4/UINT4 and W4A8 GEMMs of at most
         # 16 rows, and for NVFP4 ones up to 2^24 weights or 8 rows with K <= 4096
         dt = ("w4a8_fused_act_quant" if kind == "w4a8" else "nvfp4_" + p["adt"] if nv_small
@@ -698,19 +800,22 @@ def run_ours(args, rank, world, device):
             import torch.distributed as dist
             dist.barrier()
 
-    # the timed region can be a few ms: sample every millisecond
-    clocks = ClockSampler(torch.cuda.current_device(), period=0.001)
+    # the timed region can be a few ms: sample every half millisecond, from a
+    # process of its own, and keep the samples taken inside the region
+    clocks = ClockSampler(torch.cuda.current_device(), period=0.0005)
     clocks.start()
     barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
     with torch.cuda.stream(stream), nvtx("timed steps"):
         e0.record(stream)
         for _ in range(args.steps):
             graph.replay()
         e1.record(stream)
     torch.cuda.synchronize()
+    clocks.mark_end()
     barrier()
     clk = clocks.stop()
     # a kernel that gave up a bounded wait makes the step time invalid

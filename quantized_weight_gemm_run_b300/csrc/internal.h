@@ -212,6 +212,8 @@ struct W4A4Params {
   int splits;
   float* part;
   int* cnt;
+  long long part_rows;       // rows of 128 fp32 the partials region holds (checked build)
+  int cnt_words;             // counters the region holds (checked build)
 };
 constexpr int kW4A4TileK = 256;
 int w4a4_smem_bytes(int block_tok);

@@ -425,7 +425,12 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   // up to 2^24 weights, or at M <= 8 with K <= 4096.
   const bool nv_small = !is_nv(L) || L->n * L->k <= (int64_t(1) << 24) ||
                         (rows <= 8 && L->k <= 4096);
-  const bool use_mma = want == 2 || (want == 0 && mma_ok && !k1_tuned && nv_small);
+  // 9-16 rows on a long K (at least twice as many k-tiles as n-tiles) go to
+  // the tcgen05 kernel.  Measured on B300, UINT4 bf16 16 x 4096 x 11008: 12.3
+  // us against 12.9-13.4 on the small-M kernel; at 8 rows, and at 16 rows on
+  // 4096^2 and 11008 x 4096, the small-M kernel is faster.
+  const bool long_k = rows > 8 && ktl >= 2 * ntl && !is_mx(L) && !is_nv(L) && !is_f16s(L);
+  const bool use_mma = want == 2 || (want == 0 && mma_ok && !k1_tuned && nv_small && !long_k);
   if (use_mma) {
     if (ntl * S >= (int64_t(1) << 31)) return fail(QGEMM_ERR_UNSUPPORTED, "grid too large");
     P->kernel = 2;
@@ -759,6 +764,8 @@ static qgemm_status run_w4a4(const qgemm_layer_config* L, const qgemm_tuning_con
   p.splits = P.splits;
   p.cnt = reinterpret_cast<int*>(wsb + P.cnt_off);
   p.part = reinterpret_cast<float*>(wsb + P.part_off);
+  p.part_rows = P.splits > 1 ? (long long)P.grid * P.bt : 0;   // tiles x slices x BT
+  p.cnt_words = P.splits > 1 ? (int)(P.grid / P.splits * 4) : 0;
   // the quantization kernel also clears the K split's counters
   const int64_t n_cnt = P.splits > 1 ? P.grid / P.splits * 4 : 0;
   cudaError_t e = launch_act_quant_nvfp4(static_cast<const uint16_t*>(a), rows, (int64_t)k,

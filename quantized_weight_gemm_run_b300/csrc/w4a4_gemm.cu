@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (S == 1) {
               const float o = fmaf(__uint_as_float(v[j]), sc, bias);
               p.c[(long long)(m0 + tl) * p.n + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-            } else {
+            } else if (qg_check((long long)it * BT + tl < p.part_rows, p.status)) {
               __stcg(slot + tl * 128, __uint_as_float(v[j]));
             }
           }
@@ -313,7 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         __syncwarp();
         int before = 0;
-        if (lane == 0) before = atomic_add_acq_rel(p.cnt + t * 4 + q, 1);
+        if (lane == 0 && qg_check(t * 4 + q < p.cnt_words, p.status))
+          before = atomic_add_acq_rel(p.cnt + t * 4 + q, 1);
         __syncwarp();
         before = __shfl_sync(0xFFFFFFFFu, before, 0);
         if (before == S - 1) {
@@ -322,6 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // loads (32 per lane) are in flight at once
           const float* base = p.part + (size_t)t * S * (BT * 128) + col;
           constexpr size_t kSl = (size_t)BT * 128;   // floats between slices
+          // checked build: the tile's last partial row lies inside the region
+          if (!qg_check(((long long)t * S + S) * BT <= p.part_rows, p.status)) continue;
 #pragma unroll 1
           for (int c0 = 0; c0 < live; c0 += 16) {
             const float* b0 = base + (size_t)c0 * 128;

@@ -45,6 +45,10 @@ def test_kernel_names_follow_the_planner():
     # dense INT4/UINT4 with scales in the activation dtype: small-M kernel up to 16 rows
     assert bench.kernel_name(dict(_pt("sweep"), m=16)).startswith("w4a16_mma_kernel")
     assert bench.kernel_name(dict(_pt("sweep"), m=17)) == "w4a16_kernel<32,bf16,dense>"
+    # ... except 9-16 rows on a long K (K >= 2 N): the tcgen05 kernel
+    long_k = dict(_pt("sweep"), n=4096, k=11008)
+    assert bench.kernel_name(dict(long_k, m=16)) == "w4a16_kernel<16,bf16,dense>"
+    assert bench.kernel_name(dict(long_k, m=8)) == "w4a16_mma_kernel<bf16,1>"
     # fp16 scales with bf16 activations: small-M kernel up to 16 rows, as for the sweep
     assert bench.kernel_name(dict(_pt("f16s"), m=1)) == "w4a16_mma_kernel<bf16_f16scales,1>"
     assert bench.kernel_name(dict(_pt("f16s"), m=64)) == "w4a16_kernel<64,bf16_f16scales,dense>"

@@ -142,3 +142,21 @@ def test_small_m_kernel_rejections(Q):
     # unknown kernel id (3 is the tcgen05 kernel's cluster split)
     st, _ = Q.qgemm_workspace_size(lin.layer, lin.dense, Q.tuning_config(kernel=4), 8)
     assert st == Q.QGEMM_ERR_INVALID_ARG
+
+
+def test_plan_sends_9_to_16_rows_on_a_long_k_to_the_tcgen05_kernel(Q):
+    """At 9-16 rows with at least twice as many k-tiles as n-tiles the planner
+    takes the tcgen05 kernel (measured faster there); at 8 rows, or on a
+    square layer, the small-M kernel.  Both match the oracle."""
+    c = Case(16, 256, 1024, 128, "bf16", False, seed=21)
+    lin = linear(c)
+    for m, kern in ((8, "w4a16_mma_sync_smallm"), (9, "w4a16_tcgen05_swapab"),
+                    (16, "w4a16_tcgen05_swapab")):
+        st, rec = Q.qgemm_describe_plan(lin.layer, lin.dense, m)
+        assert st == Q.QGEMM_OK and f"kernel={kern}" in rec, rec
+    sq = linear(Case(16, 512, 512, 128, "bf16", False, seed=22))
+    st, rec = Q.qgemm_describe_plan(sq.layer, sq.dense, 16)
+    assert st == Q.QGEMM_OK and "kernel=w4a16_mma_sync_smallm" in rec, rec
+    out = lin(c.dev_act())
+    assert lin.status() == Q.QGEMM_OK
+    assert_close(to_np(out), c.reference(), what="long-K 16 rows on the tcgen05 kernel")
