@@ -84,3 +84,19 @@ def test_committed_traffic_lines_parse():
         assert re.fullmatch(r"\d+x\d+x\d+,(sym|asym),(bf16|fp16)(,f16s)?", key), key
         assert nbytes > 0 and re.fullmatch(r"[0-9a-f]{16}", src)
     assert bench.source_without_comments("int a; // x\n/* y */ int b;\n") == "int a;\n int b;"
+
+
+def test_clock_sampler_keeps_the_timed_window():
+    """The summary keeps the samples taken inside [mark_start, mark_end]: the
+    median SM clock and the union of the named clock-event reasons there."""
+    c = bench.ClockSampler(0)
+    c.window = [10.0, 10.01]
+    c.samples = [(9.0, 1200, 0x4), (10.002, 2032, 0x0), (10.006, 2000, 0x4), (11.0, 900, 0x40)]
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 2016.0 and s["reasons"] == ["sw_power_cap"]
+    # a window with no sample inside takes the samples within 50 ms of it
+    c.window = [10.003, 10.004]
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 2016.0
+    c.samples = []
+    assert c.summary()["samples"] == 0
