@@ -423,9 +423,13 @@ template <int BT>
 cudaError_t launch_bt(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const CUtensorMap& tm_ws,
                       const CUtensorMap& tm_as, const W4A4Params& p, cudaStream_t stream) {
   using L = Lay<BT>;
-  cudaError_t e = cudaFuncSetAttribute(w4a4_kernel<BT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
-  if (e != cudaSuccess) return e;
+  static bool attr_set = false;   // the shared-memory opt-in, once per process
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(w4a4_kernel<BT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   const int items = p.mt * p.nt * p.splits;
   const int sms = device_sm_count();
   const int grid = sms > 0 && items > sms ? sms : items;   // one persistent CTA per SM
