@@ -62,6 +62,11 @@ def test_kernel_names_follow_the_planner():
     assert bench.kernel_name(dict(nv, m=9, n=11008, k=4096)) == "w4a16_kernel<16,nvfp4_bf16,dense>"
     assert bench.kernel_name(dict(nv, m=1, n=4096, k=11008)) == "w4a16_kernel<16,nvfp4_bf16,dense>"
     assert bench.kernel_name(dict(nv, m=256)) == "w4a16_kernel<128,nvfp4_bf16,dense>"
+    # W4A4: 16-token tiles up to 16 rows, then the smallest tile whose tiles fit one wave
+    w4 = _pt("w4a4")
+    for m, n, bt in ((16, 4096, 16), (64, 4096, 32), (64, 11008, 64), (256, 4096, 64),
+                     (256, 11008, 128), (1024, 4096, 128)):
+        assert bench.kernel_name(dict(w4, m=m, n=n)) == f"act_quant_nvfp4_kernel + w4a4_kernel<{bt}>"
 
 
 def test_traffic_keys_separate_formats():
