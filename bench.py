@@ -142,11 +142,11 @@ def point_bytes(p):
     kind = p.get("kind", "w4a16")
     if kind == "w4a8":
         # GEMM: bf16 activations read once, codes, e8m0 scales, bf16 out; above
-        # 16 rows the per-token quantization is its own kernel (bf16 in, e4m3
-        # and scales out, read back by the GEMM), at most 16 rows it runs
+        # 8 rows the per-token quantization is its own kernel (bf16 in, e4m3
+        # and scales out, read back by the GEMM), at most 8 rows it runs
         # inside the small-M kernel
         gemm = 2 * m * k + n * k // 2 + n * k // 32 + 2 * m * n
-        return gemm + (m * k + 4 * m) * 2 if m > 16 else gemm
+        return gemm + (m * k + 4 * m) * 2 if m > 8 else gemm
     if kind == "w8a16":
         # 8-bit codes, scales, 8-bit zero points, activations, output
         return n * k + (k // g) * n * 2 + (k // g) * n + m * k * 2 + m * n * 2
@@ -353,7 +353,7 @@ class GemmPoint:
     ``clone()`` duplicates every device buffer, so that a rotation of clones
     reads its operands cold from HBM.  A W4A8 point's launch is one library
     call on its bf16 activations: the per-token FP8 quantization runs inside
-    the small-M kernel at M <= 16, else as its own kernel ahead of the GEMM."""
+    the small-M kernel at M <= 8, else as its own kernel ahead of the GEMM."""
 
     def __init__(self, p, seed, device, host=False, src=None):
         import torch
@@ -417,7 +417,7 @@ class GemmPoint:
         if host:
             self.a_host = self.a.cpu().pin_memory()
             self.c_host = torch.empty(m, n, dtype=dt).pin_memory()
-        self.launches = 2 if (self.mx and m > 16) or p.get("kind") == "w4a4" else 1
+        self.launches = 2 if (self.mx and m > 8) or p.get("kind") == "w4a4" else 1
 
     def clone(self):
         return GemmPoint(self.p, 0, self.c.device, src=self)
@@ -591,7 +591,8 @@ def kernel_name(p):
     nv_small = kind == "nvfp4" and (p["n"] * p["k"] <= 1 << 24 or (m <= 8 and p["k"] <= 4096))
     # the planner's long-K rule: 9-16 rows with K >= 2 N go to the tcgen05 kernel
     long_k = kind == "w4a16" and not f16_scales(p) and m > 8 and p["k"] >= 2 * p["n"]
-    if (kind in ("w4a16", "w4a8") or nv_small) and m <= 16 and not long_k:
+    mx_rows = kind == "w4a8" and m > 8   # W4A8 above 8 rows: the tcgen05 kernel
+    if (kind in ("w4a16", "w4a8") or nv_small) and m <= 16 and not long_k and not mx_rows:
         # the planner's default for dense INT4/UINT4 and W4A8 GEMMs of at most
         # 16 rows, and for NVFP4 ones up to 2^24 weights or 8 rows with K <= 4096
         dt = ("w4a8_fused_act_quant" if kind == "w4a8" else "nvfp4_" + p["adt"] if nv_small

@@ -105,7 +105,7 @@ enum { QGEMM_ACT_NONE = 0, QGEMM_ACT_SILU_GLU = 1 };
  *                 per-row fp32 scales from qgemm_quantize_act_fp8) or
  *                 QGEMM_BF16 with MXFP4 weights (W4A8 whose bf16 activations
  *                 the library quantizes with the qgemm_quantize_act_fp8 rule:
- *                 at m <= 16 inside the small-M kernel, above in a separate
+ *                 at m <= 8 inside the small-M kernel, above in a separate
  *                 kernel into the workspace; results are bitwise those of the
  *                 two-call form; such a layer's workspace then holds its
  *                 quantized rows, so it must not be shared with other layers)

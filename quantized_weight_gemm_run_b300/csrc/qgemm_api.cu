@@ -428,9 +428,14 @@ static qgemm_status make_plan(const qgemm_layer_config* L, const qgemm_tuning_co
   // 9-16 rows on a long K (at least twice as many k-tiles as n-tiles) go to
   // the tcgen05 kernel.  Measured on B300, UINT4 bf16 16 x 4096 x 11008: 12.3
   // us against 12.9-13.4 on the small-M kernel; at 8 rows, and at 16 rows on
-  // 4096^2 and 11008 x 4096, the small-M kernel is faster.
+  // 4096^2 and 11008 x 4096, the small-M kernel is faster.  W4A8 layers take
+  // it above 8 rows at any shape (7168 x 2048, M = 16: 9.1 us with the
+  // separate quantizer against 10.3 fused into the small-M kernel's two n8
+  // token blocks; M = 8: 9.1 against 9.2).
   const bool long_k = rows > 8 && ktl >= 2 * ntl && !is_mx(L) && !is_nv(L) && !is_f16s(L);
-  const bool use_mma = want == 2 || (want == 0 && mma_ok && !k1_tuned && nv_small && !long_k);
+  const bool mx_rows = rows > 8 && is_mx(L);
+  const bool use_mma =
+      want == 2 || (want == 0 && mma_ok && !k1_tuned && nv_small && !long_k && !mx_rows);
   if (use_mma) {
     if (ntl * S >= (int64_t(1) << 31)) return fail(QGEMM_ERR_UNSUPPORTED, "grid too large");
     P->kernel = 2;

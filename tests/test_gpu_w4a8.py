@@ -183,7 +183,7 @@ def _lin(Q, c, **tuning):
 @pytest.mark.parametrize("m", [1, 3, 8, 9, 16, 17, 70])
 def test_w4a8_one_call_bitwise_equals_two_calls(Q, m):
     """The one-call form on bf16 activations (quantized inside the small-M
-    kernel at m <= 16, by the quantizer kernel into the workspace above) gives
+    kernel at m <= 8, by the quantizer kernel into the workspace above) gives
     the same bits as qgemm_quantize_act_fp8 followed by qgemm_run: the
     quantization is the same arithmetic, the maximum over the K slices is
     exact, and the GEMM then reads the same codes and scales."""
@@ -199,7 +199,7 @@ def test_w4a8_one_call_bitwise_equals_two_calls(Q, m):
     assert_close(to_np(one), c.reference(), frob=2e-2, what=f"w4a8 one call m={m}")
     st, plan = Q.qgemm_describe_plan(lin.layer_bf16, lin.dense, m)
     assert st == Q.QGEMM_OK
-    assert ("act_quant=fused" if m <= 16 else "act_quant=separate_kernel") in plan, plan
+    assert ("act_quant=fused" if m <= 8 else "act_quant=separate_kernel") in plan, plan
 
 
 @pytest.mark.parametrize("split_k", [1, 2, 4, 8, 16])

@@ -117,7 +117,7 @@ def test_noalloc_refuses_grouped(Q):
 @pytest.mark.parametrize("m", [5, 70])
 def test_noalloc_w4a8_on_bf16_activations(Q, m):
     """W4A8 layers on bf16 activations through the allocation-free entry point:
-    at m <= 16 the quantization runs inside the small-M kernel, above it the
+    at m <= 8 the quantization runs inside the small-M kernel, above it the
     quantized rows and scales live in the library's scratch (after the part
     that is cleared) before the tcgen05 kernel reads them."""
     import synth
